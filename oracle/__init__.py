@@ -1,0 +1,331 @@
+"""Plain CPU oracle for the MoE layer's local data path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package.  The product library
+(``routing_grouped_gemm_gb300``) never imports, links or calls it, and this
+package imports nothing from the product.  The two share no code.
+
+The arithmetic lives in ``moe_oracle.c`` (plain loops, fp64 accumulation);
+this module only compiles it with gcc on first use and marshals numpy arrays.
+
+Array conventions
+-----------------
+* ``np.float32`` / ``np.float64`` arrays are read as those types.
+* ``np.uint16`` arrays are bf16 bit patterns (the upper half of a binary32).
+* Integer outputs are ``np.int32``; float outputs are ``np.float64``.
+
+What each function follows (page title, section):
+* ``router_logits``       "Expert Parallelism (EP)" section 1, gating logits
+* ``topk``/``topk_weights`` same section, "top-k + score_func"
+* ``layout``/``permute_rows`` same section (tokens_per_expert, permute) and
+                          section 2 (expert-contiguous, M-tile aligned layout)
+* ``expert_ffn``/``moe_tokens``/``grouped_*`` same section, grouped
+                          fc1 -> act -> fc2, with the SwiGLU expert of the
+                          "Expert Tensor Parallel design" page, section 4.3
+* ``unpermute_combine``   "Expert Parallelism (EP)" section 1, combine
+                          post-process (top-k weighted reduce back to order)
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, brute force and the worked example of the
+"NCCL course 32" page, section "Expert Parallel / MoE data flow").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "liboracle.so")
+
+F32, BF16, F64 = 0, 1, 2
+SOFTMAX, SIGMOID = 0, 1
+CONTIGUOUS, MASKED = 0, 1
+OK, BAD_ARG, CAPACITY, BAD_ROUTING = 0, 1, 3, 6
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``moe_oracle.c`` into ``_lib/liboracle.so`` (gcc, -O2)."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB)
+             or os.path.getmtime(_LIB) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_long
+            lib.oracle_round_bf16.restype = ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_round_bf16_array.argtypes = [L, P, P]
+            lib.oracle_silu.restype = ctypes.c_double
+            lib.oracle_silu.argtypes = [ctypes.c_double]
+            lib.oracle_router_logits.argtypes = [I, I, I, P, I, P, I, P, P, I]
+            lib.oracle_topk.restype = I
+            lib.oracle_topk.argtypes = [I, I, I, P, P]
+            lib.oracle_topk_weights.argtypes = [I, I, I, P, P, I, I, P]
+            lib.oracle_rows_alloc.restype = L
+            lib.oracle_rows_alloc.argtypes = [I, I, I, I, I, I]
+            lib.oracle_layout.restype = I
+            lib.oracle_layout.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, L]
+            lib.oracle_permute_rows.argtypes = [L, I, I, P, P, P]
+            lib.oracle_expert_ffn.argtypes = [I, I, P, P, P, I, P, I, P]
+            lib.oracle_moe_tokens.restype = I
+            lib.oracle_moe_tokens.argtypes = [I, P, I, I, I, I, I, P, I, P, P, P, I,
+                                              P, P, I, P, I]
+            lib.oracle_grouped_gemm1_swiglu.argtypes = [I, I, I, P, P, P, I, P, P, I, I, P, I]
+            lib.oracle_grouped_gemm2.argtypes = [I, I, I, P, P, P, I, P, I, I, P, I]
+            lib.oracle_unpermute_combine.argtypes = [I, I, I, P, I, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _dt(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle: unsupported element type {a.dtype}")
+
+
+def _c(a: np.ndarray, dtype=None) -> np.ndarray:
+    return np.ascontiguousarray(a if dtype is None else a.astype(dtype, copy=False))
+
+
+def _p(a) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if a is None else a.ctypes.data)
+
+
+# --------------------------------------------------------------------------
+# scalar helpers
+# --------------------------------------------------------------------------
+
+def round_bf16(a) -> np.ndarray:
+    """Nearest bf16 value (ties to even) of each element, as float64."""
+    a = np.asarray(a, dtype=np.float64)
+    src = _c(a)
+    out = np.empty_like(src)
+    _load().oracle_round_bf16_array(src.size, _p(src), _p(out))
+    return out.reshape(a.shape)
+
+
+def silu(z: float) -> float:
+    return _load().oracle_silu(float(z))
+
+
+# --------------------------------------------------------------------------
+# router
+# --------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, wg: np.ndarray, bias=None, nthreads=None) -> np.ndarray:
+    """fp64 logits[t, e] = sum_d x[t,d] wg[e,d] (+ bias[e])."""
+    x = _c(x)
+    wg = _c(wg)
+    T, D = x.shape
+    E = wg.shape[0]
+    assert wg.shape[1] == D
+    b = None if bias is None else _c(bias, np.float64)
+    out = np.empty((T, E), np.float64)
+    _load().oracle_router_logits(T, D, E, _p(x), _dt(x), _p(wg), _dt(wg), _p(b),
+                                 _p(out), nthreads or default_threads())
+    return out
+
+
+def topk(logits_f32: np.ndarray, k: int):
+    """(topk_idx int32 [T,k], status) from fp32 keys; ties -> lower index."""
+    l = _c(logits_f32, np.float32)
+    T, E = l.shape
+    idx = np.empty((T, k), np.int32)
+    st = _load().oracle_topk(T, E, k, _p(l), _p(idx))
+    return idx, st
+
+
+def topk_weights(logits_f32: np.ndarray, idx: np.ndarray, score: int, renorm: bool) -> np.ndarray:
+    l = _c(logits_f32, np.float32)
+    idx = _c(idx, np.int32)
+    T, E = l.shape
+    k = idx.shape[1]
+    w = np.empty((T, k), np.float64)
+    _load().oracle_topk_weights(T, E, k, _p(l), _p(idx), int(score), int(bool(renorm)), _p(w))
+    return w
+
+
+def route(x, wg, bias, k: int, score: int, renorm: bool, nthreads=None):
+    """Whole router on the oracle's own logits.
+
+    Returns (logits_f64, keys_f32, topk_idx, topk_w, status); the selection
+    key is the fp32 rounding of the fp64 logit.
+    """
+    l64 = router_logits(x, wg, bias, nthreads)
+    keys = l64.astype(np.float32)
+    idx, st = topk(keys, k)
+    w = topk_weights(keys, idx, score, renorm)
+    return l64, keys, idx, w, st
+
+
+# --------------------------------------------------------------------------
+# layout
+# --------------------------------------------------------------------------
+
+def rows_alloc(T, k, E_local, layout=CONTIGUOUS, align_m=128, capacity=0) -> int:
+    return int(_load().oracle_rows_alloc(T, k, E_local, layout, align_m, capacity))
+
+
+def layout(idx: np.ndarray, E: int, e_first: int = 0, E_local=None,
+           layout_kind: int = CONTIGUOUS, align_m: int = 128, capacity: int = 0):
+    """tokens_per_expert, segment offsets and the permutation (dict)."""
+    idx = _c(idx, np.int32)
+    T, k = idx.shape
+    if E_local is None:
+        E_local = E - e_first
+    ra = rows_alloc(T, k, E_local, layout_kind, align_m, capacity)
+    cnt = np.zeros(E, np.int32)
+    seg = np.zeros(E_local + 1, np.int32)
+    row_of = np.empty((T, k), np.int32)
+    tor = np.empty(max(ra, 1), np.int32)
+    st = _load().oracle_layout(T, k, E, e_first, E_local, layout_kind, align_m, capacity,
+                               _p(idx), _p(cnt), _p(seg), _p(row_of), _p(tor), ra)
+    return dict(status=st, tokens_per_expert=cnt, seg_offsets=seg, row_of=row_of,
+                token_of_row=tor[:ra], rows_alloc=ra)
+
+
+def permute_rows(x: np.ndarray, token_of_row: np.ndarray, fill=0) -> np.ndarray:
+    """x_perm[r] = x[token_of_row[r]] (exact copy); unfilled rows = ``fill``."""
+    x = _c(x)
+    tor = _c(token_of_row, np.int32)
+    out = np.full((tor.shape[0], x.shape[1]), fill, dtype=x.dtype)
+    _load().oracle_permute_rows(tor.shape[0], x.shape[1], x.itemsize, _p(x), _p(tor), _p(out))
+    return out
+
+
+# --------------------------------------------------------------------------
+# experts
+# --------------------------------------------------------------------------
+
+def expert_ffn(v: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray,
+               round_bf16_: bool = False) -> np.ndarray:
+    """FFN(v) = w2 . (SiLU(w1 . v) * (w3 . v)) for one expert (fp64 result)."""
+    v = _c(v, np.float64)
+    w1, w3, w2 = _c(w1), _c(w3), _c(w2)
+    Hl, D = w1.shape
+    assert w3.shape == (Hl, D) and w2.shape == (D, Hl) and v.shape == (D,)
+    assert w1.dtype == w3.dtype == w2.dtype
+    y = np.empty(D, np.float64)
+    _load().oracle_expert_ffn(D, Hl, _p(w1), _p(w3), _p(w2), _dt(w1), _p(v),
+                              int(round_bf16_), _p(y))
+    return y
+
+
+def _ptr_table(ws, n):
+    arr = (ctypes.c_void_p * n)()
+    keep = []
+    for i in range(n):
+        w = ws[i] if i < len(ws) else None
+        if w is None:
+            arr[i] = None
+        else:
+            w = _c(w)
+            keep.append(w)
+            arr[i] = w.ctypes.data
+    return arr, keep
+
+
+def moe_tokens(tokens, x, w1s, w3s, w2s, topk_idx, topk_w, e_first: int = 0,
+               round_bf16_: bool = False, nthreads=None) -> np.ndarray:
+    """Brute-force per-token layer output (no permutation) for listed tokens.
+
+    ``w1s[i]``, ``w3s[i]`` ([Hl, D]) and ``w2s[i]`` ([D, Hl]) are the weights
+    of local expert ``e_first + i``; entries may be ``None`` for experts no
+    listed token uses.  Returns fp64 [len(tokens), D].
+    """
+    tokens = _c(np.asarray(tokens), np.int32)
+    x = _c(x)
+    idx = _c(topk_idx, np.int32)
+    w = _c(topk_w, np.float64)
+    E_local = len(w1s)
+    first = next(a for a in w1s if a is not None)
+    Hl, D = first.shape
+    wdt = _dt(first)
+    t1, k1 = _ptr_table(w1s, E_local)
+    t3, k3 = _ptr_table(w3s, E_local)
+    t2, k2 = _ptr_table(w2s, E_local)
+    out = np.empty((tokens.shape[0], D), np.float64)
+    st = _load().oracle_moe_tokens(tokens.shape[0], _p(tokens), D, Hl, idx.shape[1], e_first,
+                                   E_local, _p(x), _dt(x), t1, t3, t2, wdt, _p(idx), _p(w),
+                                   int(round_bf16_), _p(out), nthreads or default_threads())
+    if st != OK:
+        raise ValueError("oracle.moe_tokens: a listed token uses an expert whose weights are missing")
+    del k1, k3, k2
+    return out
+
+
+def grouped_gemm1_swiglu(x_perm, seg_offsets, cnt_local, w1s, w3s, round_bf16_=False,
+                         nthreads=None) -> np.ndarray:
+    """h over the permuted layout (fp64 [rows, Hl]; unfilled rows are NaN)."""
+    x_perm = _c(x_perm)
+    seg = _c(seg_offsets, np.int32)
+    cnt = _c(cnt_local, np.int32)
+    E_local = len(w1s)
+    first = next(a for a in w1s if a is not None)
+    Hl, D = first.shape
+    t1, k1 = _ptr_table(w1s, E_local)
+    t3, k3 = _ptr_table(w3s, E_local)
+    h = np.full((x_perm.shape[0], Hl), np.nan)
+    _load().oracle_grouped_gemm1_swiglu(D, Hl, E_local, _p(seg), _p(cnt), _p(x_perm), _dt(x_perm),
+                                        t1, t3, _dt(first), int(round_bf16_), _p(h),
+                                        nthreads or default_threads())
+    del k1, k3
+    return h
+
+
+def grouped_gemm2(h, seg_offsets, cnt_local, w2s, round_bf16_=False, nthreads=None) -> np.ndarray:
+    """y_perm over the permuted layout (fp64 [rows, D]; unfilled rows NaN)."""
+    h = _c(h)
+    seg = _c(seg_offsets, np.int32)
+    cnt = _c(cnt_local, np.int32)
+    E_local = len(w2s)
+    first = next(a for a in w2s if a is not None)
+    D, Hl = first.shape
+    t2, k2 = _ptr_table(w2s, E_local)
+    y = np.full((h.shape[0], D), np.nan)
+    _load().oracle_grouped_gemm2(D, Hl, E_local, _p(seg), _p(cnt), _p(h), _dt(h), t2, _dt(first),
+                                 int(round_bf16_), _p(y), nthreads or default_threads())
+    del k2
+    return y
+
+
+def unpermute_combine(y_perm, row_of, topk_w) -> np.ndarray:
+    """out[t] = sum_j w[t,j] y_perm[row_of[t,j]] (fp64 [T, D])."""
+    y = _c(y_perm)
+    ro = _c(row_of, np.int32)
+    w = _c(topk_w, np.float64)
+    T, k = ro.shape
+    D = y.shape[1]
+    out = np.empty((T, D), np.float64)
+    _load().oracle_unpermute_combine(T, k, D, _p(y), _dt(y), _p(ro), _p(w), _p(out))
+    return out

@@ -1,0 +1,528 @@
+/*
+ * Plain CPU oracle for the MoE layer's local data path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * Everything here is the slow, literal definition:
+ *   - floating point accumulates in fp64 (inputs may be fp32, bf16 or fp64);
+ *   - loops follow the order in which the method is stated, with no blocking,
+ *     fusion or reordering;
+ *   - bf16 rounding points (where the bf16 pipeline stores an intermediate
+ *     tensor) are applied only when the caller asks for them.
+ *
+ * Sources (page title, section):
+ *   [EP]    "Expert Parallelism (EP)", llm-infra-atlas, section 1 (MoE layer
+ *           forward path: gating logits x.W_g^T, top-k + score function,
+ *           tokens_per_expert, permute, grouped fc1 -> act -> fc2,
+ *           unpermute with top-k weighted reduce), section 2 (layout
+ *           contract: expert-contiguous segments aligned to the GEMM M tile),
+ *           section 5 (permute / unpermute symmetry).
+ *   [ETP]   "Expert Tensor Parallel design" (HyperParallel issue 104),
+ *           section 4.3 (GroupedExperts w1/w3 [E,H,D], w2 [E,D,H]; shards on
+ *           dim 1 and dim 2).
+ *   [NCCL32] "NCCL course 32: TP, PP, EP/MoE and multi-dim process groups",
+ *           section "Tensor Parallel matrix split" (F.linear computes X.W^T,
+ *           row-parallel partial outputs sum to the full output).
+ *   SwiGLU expert FFN_e(v) = w2_e . (SiLU(w1_e . v) (*) (w3_e . v)) is the
+ *   expert function named for this layer; SiLU(z) = z / (1 + exp(-z)).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* element type codes for inputs */
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+/* score functions */
+enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
+/* layouts */
+enum { ORC_CONTIGUOUS = 0, ORC_MASKED = 1 };
+/* return codes */
+enum { ORC_OK = 0, ORC_BAD_ARG = 1, ORC_CAPACITY = 3, ORC_BAD_ROUTING = 6 };
+
+/* ------------------------------------------------------------------ */
+/* element access and rounding                                          */
+/* ------------------------------------------------------------------ */
+
+/* bf16 is the upper 16 bits of an IEEE binary32 value. */
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *p, int dtype, size_t i)
+{
+    switch (dtype) {
+    case ORC_F32: return (double)((const float *)p)[i];
+    case ORC_BF16: return bf16_bits_to_double(((const uint16_t *)p)[i]);
+    default: return ((const double *)p)[i];
+    }
+}
+
+/*
+ * Round a double to the nearest bf16 value, ties to even.  bf16 keeps 8
+ * significant bits (1 implicit + 7 stored) and the binary32 exponent range.
+ * Below the smallest normal (2^-126) the spacing is fixed at 2^-133.
+ */
+double oracle_round_bf16(double v)
+{
+    if (!isfinite(v) || v == 0.0) return v;
+    const double min_normal = ldexp(1.0, -126);
+    const double max_finite = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+    double out;
+    if (fabs(v) < min_normal) {
+        out = ldexp(nearbyint(ldexp(v, 133)), -133);
+    } else {
+        int e;
+        double m = frexp(v, &e); /* v = m * 2^e, 0.5 <= |m| < 1 */
+        out = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+    }
+    if (fabs(out) > max_finite) return copysign(INFINITY, v);
+    return out;
+}
+
+void oracle_round_bf16_array(long n, const double *in, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = oracle_round_bf16(in[i]);
+}
+
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* ------------------------------------------------------------------ */
+/* a tiny thread pool: split [0, n) into contiguous chunks              */
+/* ------------------------------------------------------------------ */
+
+typedef void (*range_fn)(void *ctx, long lo, long hi);
+typedef struct { range_fn fn; void *ctx; long lo, hi; } range_job;
+
+static void *range_trampoline(void *arg)
+{
+    range_job *j = (range_job *)arg;
+    j->fn(j->ctx, j->lo, j->hi);
+    return NULL;
+}
+
+static void parallel_for(long n, int nthreads, range_fn fn, void *ctx)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((long)nthreads > n) nthreads = (int)(n > 0 ? n : 1);
+    if (nthreads == 1) { fn(ctx, 0, n); return; }
+    pthread_t th[256];
+    range_job jobs[256];
+    long chunk = (n + nthreads - 1) / nthreads;
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        long lo = (long)i * chunk, hi = lo + chunk < n ? lo + chunk : n;
+        if (lo >= hi) break;
+        jobs[i].fn = fn; jobs[i].ctx = ctx; jobs[i].lo = lo; jobs[i].hi = hi;
+        if (pthread_create(&th[i], NULL, range_trampoline, &jobs[i]) != 0) {
+            fn(ctx, lo, hi); /* run inline if a thread cannot start */
+            jobs[i].fn = NULL;
+        }
+        started = i + 1;
+    }
+    for (int i = 0; i < started; ++i)
+        if (jobs[i].fn) pthread_join(th[i], NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* router: gating logits  ([EP] section 1: logits = x . W_g^T, [T,E])   */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int T, D, E, xdt, wdt;
+    const void *x, *wg;
+    const double *bias;
+    double *logits;
+} logits_ctx;
+
+static void logits_range(void *c, long lo, long hi)
+{
+    logits_ctx *p = (logits_ctx *)c;
+    for (long t = lo; t < hi; ++t)
+        for (int e = 0; e < p->E; ++e) {
+            double acc = 0.0;
+            for (int d = 0; d < p->D; ++d)
+                acc += load_elem(p->x, p->xdt, (size_t)t * p->D + d) *
+                       load_elem(p->wg, p->wdt, (size_t)e * p->D + d);
+            if (p->bias) acc += p->bias[e];
+            p->logits[(size_t)t * p->E + e] = acc;
+        }
+}
+
+/* logits[t,e] = sum_d x[t,d] * wg[e,d] (+ bias[e]), accumulated in fp64. */
+void oracle_router_logits(int T, int D, int E, const void *x, int xdt,
+                          const void *wg, int wdt, const double *bias,
+                          double *logits, int nthreads)
+{
+    logits_ctx c = {T, D, E, xdt, wdt, x, wg, bias, logits};
+    parallel_for(T, nthreads, logits_range, &c);
+}
+
+/* ------------------------------------------------------------------ */
+/* top-k selection                                                       */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Selection order on the fp32 key l: a comes before b when l_a > l_b, or
+ * when they are equal and a < b (ties go to the lower expert index).  NaN
+ * sorts after every number, -inf included; two NaNs tie by index.  -0 and +0
+ * compare equal, so they tie by index as well.
+ */
+static int key_before(float la, int a, float lb, int b)
+{
+    int na = isnan(la), nb = isnan(lb);
+    if (na || nb) {
+        if (na && nb) return a < b;
+        return nb; /* the non-NaN one comes first */
+    }
+    if (la > lb) return 1;
+    if (la < lb) return 0;
+    return a < b;
+}
+
+/*
+ * topk_idx[t, j] = the j-th expert in selection order, j < k.  Plain
+ * selection: k passes over all E experts, each taking the best remaining.
+ * Returns ORC_BAD_ROUTING if any logit is NaN (the selection is still made).
+ */
+int oracle_topk(int T, int E, int k, const float *logits, int32_t *topk_idx)
+{
+    if (k < 1 || k > E) return ORC_BAD_ARG;
+    int status = ORC_OK;
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    if (!taken) return ORC_BAD_ARG;
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int e = 0; e < E; ++e)
+            if (isnan(l[e])) status = ORC_BAD_ROUTING;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || key_before(l[e], e, l[best], best)) best = e;
+            }
+            taken[best] = 1;
+            topk_idx[(size_t)t * k + j] = best;
+        }
+    }
+    free(taken);
+    return status;
+}
+
+/*
+ * Routing weights for the selected experts ([EP] section 1: "top-k +
+ * score_func -> probs").  Scores from the fp32 key l:
+ *   softmax: p_e = exp(l_e - max_e' l_e') / sum_e' exp(l_e' - max)
+ *            (over all E experts)
+ *   sigmoid: p_e = 1 / (1 + exp(-l_e))
+ * Weight of slot j: w_j = p[idx_j], or p[idx_j] / sum_i p[idx_i] when
+ * renormalising over the selected k.
+ */
+void oracle_topk_weights(int T, int E, int k, const float *logits,
+                         const int32_t *topk_idx, int score, int renorm,
+                         double *topk_w)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    if (!p) return;
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        if (score == ORC_SOFTMAX) {
+            double m = -INFINITY;
+            for (int e = 0; e < E; ++e)
+                if ((double)l[e] > m) m = (double)l[e];
+            double z = 0.0;
+            for (int e = 0; e < E; ++e) z += exp((double)l[e] - m);
+            for (int e = 0; e < E; ++e) p[e] = exp((double)l[e] - m) / z;
+        } else {
+            for (int e = 0; e < E; ++e) p[e] = 1.0 / (1.0 + exp(-(double)l[e]));
+        }
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) s += p[topk_idx[(size_t)t * k + j]];
+        for (int j = 0; j < k; ++j) {
+            double w = p[topk_idx[(size_t)t * k + j]];
+            topk_w[(size_t)t * k + j] = renorm ? w / s : w;
+        }
+    }
+    free(p);
+}
+
+/* ------------------------------------------------------------------ */
+/* layout: tokens_per_expert, segment offsets, permutation               */
+/* ------------------------------------------------------------------ */
+
+/* rows needed by the layout (same formula the library documents). */
+long oracle_rows_alloc(int T, int k, int E_local, int layout, int align_m,
+                       int capacity)
+{
+    if (layout == ORC_MASKED) return (long)E_local * capacity;
+    long kl = k < E_local ? k : E_local;
+    return (long)T * kl + (long)E_local * (align_m - 1);
+}
+
+/*
+ * tokens_per_expert over all E experts ([EP] section 1, "preprocess").
+ * Segment offsets over the local range [e_first, e_first + E_local):
+ *   contiguous: each segment padded up to a multiple of align_m
+ *               ([EP] section 2: segments aligned to the GEMM M tile);
+ *   masked:     segment i starts at i * capacity; cnt > capacity is an error.
+ * Inside a segment, rows hold the routed tokens in ascending token order.
+ * row_of[t, j] is that row (or -1 when expert idx[t,j] is not local);
+ * token_of_row[r] is the token in row r, or -1 for padding rows.
+ */
+int oracle_layout(int T, int k, int E, int e_first, int E_local, int layout,
+                  int align_m, int capacity, const int32_t *topk_idx,
+                  int32_t *cnt, int32_t *seg_off, int32_t *row_of,
+                  int32_t *token_of_row, long rows_alloc)
+{
+    if (E_local < 0 || e_first < 0 || e_first + E_local > E || align_m < 1)
+        return ORC_BAD_ARG;
+    for (int e = 0; e < E; ++e) cnt[e] = 0;
+    for (long i = 0; i < (long)T * k; ++i) {
+        int e = topk_idx[i];
+        if (e < 0 || e >= E) return ORC_BAD_ROUTING;
+        cnt[e] += 1;
+    }
+    seg_off[0] = 0;
+    for (int i = 0; i < E_local; ++i) {
+        int c = cnt[e_first + i];
+        if (layout == ORC_MASKED) {
+            if (c > capacity) return ORC_CAPACITY;
+            seg_off[i + 1] = (i + 1) * capacity;
+        } else {
+            int padded = (c + align_m - 1) / align_m * align_m;
+            seg_off[i + 1] = seg_off[i] + padded;
+        }
+    }
+    if ((long)seg_off[E_local] > rows_alloc) return ORC_BAD_ARG;
+    for (long r = 0; r < rows_alloc; ++r) token_of_row[r] = -1;
+    for (long i = 0; i < (long)T * k; ++i) row_of[i] = -1;
+    for (int i = 0; i < E_local; ++i) {
+        int e = e_first + i, n = 0;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j)
+                if (topk_idx[(size_t)t * k + j] == e) {
+                    int r = seg_off[i] + n;
+                    row_of[(size_t)t * k + j] = r;
+                    token_of_row[r] = t;
+                    n += 1;
+                }
+    }
+    return ORC_OK;
+}
+
+/* dispatch permute: x_perm[r] = x[token_of_row[r]] for every filled row. */
+void oracle_permute_rows(long rows, int D, int elem_bytes, const void *x,
+                         const int32_t *token_of_row, void *x_perm)
+{
+    size_t rb = (size_t)D * elem_bytes;
+    for (long r = 0; r < rows; ++r) {
+        int t = token_of_row[r];
+        if (t >= 0)
+            memcpy((char *)x_perm + (size_t)r * rb, (const char *)x + (size_t)t * rb, rb);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* expert FFN                                                            */
+/* ------------------------------------------------------------------ */
+
+/*
+ * One expert on one input vector v[D] (weights in the F.linear [out, in]
+ * convention, [NCCL32] "Tensor Parallel matrix split"; shapes from [ETP]
+ * section 4.3, here for one expert and one H shard of width Hl):
+ *   a[h] = SiLU(sum_d w1[h,d] v[d]) * (sum_d w3[h,d] v[d])     h < Hl
+ *   y[d] = sum_h w2[d,h] a[h]                                   d < D
+ * With round_bf16 set, a and y are rounded to bf16 where the bf16 pipeline
+ * stores them (the h and y_perm tensors).
+ */
+static void expert_ffn(int D, int Hl, const void *w1, const void *w3,
+                       const void *w2, int wdt, const double *v,
+                       int round_bf16, double *a, double *y)
+{
+    for (int h = 0; h < Hl; ++h) {
+        double g = 0.0, u = 0.0;
+        for (int d = 0; d < D; ++d) {
+            g += load_elem(w1, wdt, (size_t)h * D + d) * v[d];
+            u += load_elem(w3, wdt, (size_t)h * D + d) * v[d];
+        }
+        double act = oracle_silu(g) * u;
+        a[h] = round_bf16 ? oracle_round_bf16(act) : act;
+    }
+    for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int h = 0; h < Hl; ++h)
+            acc += load_elem(w2, wdt, (size_t)d * Hl + h) * a[h];
+        y[d] = round_bf16 ? oracle_round_bf16(acc) : acc;
+    }
+}
+
+void oracle_expert_ffn(int D, int Hl, const void *w1, const void *w3,
+                       const void *w2, int wdt, const double *v,
+                       int round_bf16, double *y)
+{
+    double *a = (double *)malloc(sizeof(double) * (size_t)(Hl > 0 ? Hl : 1));
+    if (!a) return;
+    expert_ffn(D, Hl, w1, w3, w2, wdt, v, round_bf16, a, y);
+    free(a);
+}
+
+/*
+ * Per-token brute force, no permutation at all ([EP] section 1, the whole
+ * layer for one token):  out[t] = sum_j w[t,j] * FFN_{idx[t,j]}(x[t]),
+ * summed in slot order j = 0..k-1, skipping experts outside the local
+ * range [e_first, e_first + E_local) (their contribution belongs to another
+ * shard).  Weights of local expert i are w1s[i], w3s[i], w2s[i]; a NULL
+ * entry is allowed for experts no listed token uses.
+ */
+typedef struct {
+    int D, Hl, k, e_first, E_local, xdt, wdt, round_bf16;
+    const void *x;
+    const void *const *w1s, *const *w3s, *const *w2s;
+    const int32_t *tokens, *topk_idx;
+    const double *topk_w;
+    double *out;
+    int *missing;
+} tokens_ctx;
+
+static void tokens_range(void *c, long lo, long hi)
+{
+    tokens_ctx *p = (tokens_ctx *)c;
+    double *v = (double *)malloc(sizeof(double) * (size_t)p->D);
+    double *y = (double *)malloc(sizeof(double) * (size_t)p->D);
+    double *a = (double *)malloc(sizeof(double) * (size_t)(p->Hl > 0 ? p->Hl : 1));
+    if (!v || !y || !a) { free(v); free(y); free(a); *p->missing = 1; return; }
+    for (long i = lo; i < hi; ++i) {
+        int t = p->tokens[i];
+        double *o = p->out + (size_t)i * p->D;
+        for (int d = 0; d < p->D; ++d) {
+            o[d] = 0.0;
+            v[d] = load_elem(p->x, p->xdt, (size_t)t * p->D + d);
+        }
+        for (int j = 0; j < p->k; ++j) {
+            int e = p->topk_idx[(size_t)t * p->k + j] - p->e_first;
+            if (e < 0 || e >= p->E_local) continue;
+            if (!p->w1s[e] || !p->w3s[e] || !p->w2s[e]) { *p->missing = 1; continue; }
+            expert_ffn(p->D, p->Hl, p->w1s[e], p->w3s[e], p->w2s[e], p->wdt, v,
+                       p->round_bf16, a, y);
+            double w = p->topk_w[(size_t)t * p->k + j];
+            for (int d = 0; d < p->D; ++d) o[d] += w * y[d];
+        }
+    }
+    free(v); free(y); free(a);
+}
+
+int oracle_moe_tokens(int ntok, const int32_t *tokens, int D, int Hl, int k,
+                      int e_first, int E_local, const void *x, int xdt,
+                      const void *const *w1s, const void *const *w3s,
+                      const void *const *w2s, int wdt, const int32_t *topk_idx,
+                      const double *topk_w, int round_bf16, double *out,
+                      int nthreads)
+{
+    int missing = 0;
+    tokens_ctx c = {D, Hl, k, e_first, E_local, xdt, wdt, round_bf16, x,
+                    w1s, w3s, w2s, tokens, topk_idx, topk_w, out, &missing};
+    parallel_for(ntok, nthreads, tokens_range, &c);
+    return missing ? ORC_BAD_ARG : ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* grouped form over the permuted layout                                  */
+/* ------------------------------------------------------------------ */
+
+/*
+ * First grouped GEMM with the SwiGLU gate, row by row over each local
+ * expert's filled rows [seg_off[i], seg_off[i] + cnt_local[i]):
+ *   h[r, c] = SiLU(sum_d x_perm[r,d] w1_i[c,d]) * (sum_d x_perm[r,d] w3_i[c,d])
+ * Rows outside the filled ranges are left untouched.
+ */
+typedef struct {
+    int D, Hl, E_local, xdt, wdt, round_bf16, which;
+    const int32_t *seg_off, *cnt_local;
+    const void *in;
+    const void *const *wa, *const *wb;
+    double *out;
+} grouped_ctx;
+
+static void grouped_range(void *c, long lo, long hi)
+{
+    grouped_ctx *p = (grouped_ctx *)c;
+    for (long i = lo; i < hi; ++i) {
+        if (!p->wa[i] || (p->which == 1 && !p->wb[i])) continue;
+        for (int n = 0; n < p->cnt_local[i]; ++n) {
+            long r = (long)p->seg_off[i] + n;
+            if (p->which == 1) {
+                for (int c2 = 0; c2 < p->Hl; ++c2) {
+                    double g = 0.0, u = 0.0;
+                    for (int d = 0; d < p->D; ++d) {
+                        double xv = load_elem(p->in, p->xdt, (size_t)r * p->D + d);
+                        g += xv * load_elem(p->wa[i], p->wdt, (size_t)c2 * p->D + d);
+                        u += xv * load_elem(p->wb[i], p->wdt, (size_t)c2 * p->D + d);
+                    }
+                    double act = oracle_silu(g) * u;
+                    p->out[(size_t)r * p->Hl + c2] = p->round_bf16 ? oracle_round_bf16(act) : act;
+                }
+            } else {
+                for (int d = 0; d < p->D; ++d) {
+                    double acc = 0.0;
+                    for (int c2 = 0; c2 < p->Hl; ++c2)
+                        acc += load_elem(p->in, p->xdt, (size_t)r * p->Hl + c2) *
+                               load_elem(p->wa[i], p->wdt, (size_t)d * p->Hl + c2);
+                    p->out[(size_t)r * p->D + d] = p->round_bf16 ? oracle_round_bf16(acc) : acc;
+                }
+            }
+        }
+    }
+}
+
+void oracle_grouped_gemm1_swiglu(int D, int Hl, int E_local,
+                                 const int32_t *seg_off, const int32_t *cnt_local,
+                                 const void *x_perm, int xdt,
+                                 const void *const *w1s, const void *const *w3s,
+                                 int wdt, int round_bf16, double *h, int nthreads)
+{
+    grouped_ctx c = {D, Hl, E_local, xdt, wdt, round_bf16, 1, seg_off, cnt_local,
+                     x_perm, w1s, w3s, h};
+    parallel_for(E_local, nthreads, grouped_range, &c);
+}
+
+/* Second grouped GEMM: y[r, d] = sum_c h[r, c] w2_i[d, c] over filled rows. */
+void oracle_grouped_gemm2(int D, int Hl, int E_local, const int32_t *seg_off,
+                          const int32_t *cnt_local, const void *h, int hdt,
+                          const void *const *w2s, int wdt, int round_bf16,
+                          double *y, int nthreads)
+{
+    grouped_ctx c = {D, Hl, E_local, hdt, wdt, round_bf16, 2, seg_off, cnt_local,
+                     h, w2s, NULL, y};
+    parallel_for(E_local, nthreads, grouped_range, &c);
+}
+
+/*
+ * Unpermute with the top-k weighted reduce ([EP] section 1, combine
+ * post-process):  out[t] = sum_j w[t,j] * y_perm[row_of[t,j]], j in slot
+ * order, skipping row_of = -1 (expert not local).
+ */
+void oracle_unpermute_combine(int T, int k, int D, const void *y_perm, int ydt,
+                              const int32_t *row_of, const double *topk_w,
+                              double *out)
+{
+    for (int t = 0; t < T; ++t) {
+        double *o = out + (size_t)t * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int r = row_of[(size_t)t * k + j];
+            if (r < 0) continue;
+            double w = topk_w[(size_t)t * k + j];
+            for (int d = 0; d < D; ++d)
+                o[d] += w * load_elem(y_perm, ydt, (size_t)r * D + d);
+        }
+    }
+}
