@@ -47,6 +47,7 @@ F32, BF16, F64 = 0, 1, 2
 SOFTMAX, SIGMOID = 0, 1
 CONTIGUOUS, MASKED = 0, 1
 OK, BAD_ARG, CAPACITY, BAD_ROUTING = 0, 1, 3, 6
+ROUND_H, ROUND_Y = 1, 2   # rounding points: h (bf16 tensor) and y
 
 _lock = threading.Lock()
 _lib = None
@@ -227,9 +228,17 @@ def permute_rows(x: np.ndarray, token_of_row: np.ndarray, fill=0) -> np.ndarray:
 # experts
 # --------------------------------------------------------------------------
 
+def _rounding(round_h: bool, round_y: bool) -> int:
+    return (ROUND_H if round_h else 0) | (ROUND_Y if round_y else 0)
+
+
 def expert_ffn(v: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray,
-               round_bf16_: bool = False) -> np.ndarray:
-    """FFN(v) = w2 . (SiLU(w1 . v) * (w3 . v)) for one expert (fp64 result)."""
+               round_h: bool = False, round_y: bool = False) -> np.ndarray:
+    """FFN(v) = w2 . (SiLU(w1 . v) * (w3 . v)) for one expert (fp64 result).
+
+    ``round_h`` / ``round_y`` round the hidden activation / the expert output
+    to bf16 (nearest, ties to even) where a bf16 pipeline stores them.
+    """
     v = _c(v, np.float64)
     w1, w3, w2 = _c(w1), _c(w3), _c(w2)
     Hl, D = w1.shape
@@ -237,7 +246,7 @@ def expert_ffn(v: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray,
     assert w1.dtype == w3.dtype == w2.dtype
     y = np.empty(D, np.float64)
     _load().oracle_expert_ffn(D, Hl, _p(w1), _p(w3), _p(w2), _dt(w1), _p(v),
-                              int(round_bf16_), _p(y))
+                              _rounding(round_h, round_y), _p(y))
     return y
 
 
@@ -256,7 +265,7 @@ def _ptr_table(ws, n):
 
 
 def moe_tokens(tokens, x, w1s, w3s, w2s, topk_idx, topk_w, e_first: int = 0,
-               round_bf16_: bool = False, nthreads=None) -> np.ndarray:
+               round_h: bool = False, round_y: bool = False, nthreads=None) -> np.ndarray:
     """Brute-force per-token layer output (no permutation) for listed tokens.
 
     ``w1s[i]``, ``w3s[i]`` ([Hl, D]) and ``w2s[i]`` ([D, Hl]) are the weights
@@ -277,14 +286,15 @@ def moe_tokens(tokens, x, w1s, w3s, w2s, topk_idx, topk_w, e_first: int = 0,
     out = np.empty((tokens.shape[0], D), np.float64)
     st = _load().oracle_moe_tokens(tokens.shape[0], _p(tokens), D, Hl, idx.shape[1], e_first,
                                    E_local, _p(x), _dt(x), t1, t3, t2, wdt, _p(idx), _p(w),
-                                   int(round_bf16_), _p(out), nthreads or default_threads())
+                                   _rounding(round_h, round_y), _p(out),
+                                   nthreads or default_threads())
     if st != OK:
         raise ValueError("oracle.moe_tokens: a listed token uses an expert whose weights are missing")
     del k1, k3, k2
     return out
 
 
-def grouped_gemm1_swiglu(x_perm, seg_offsets, cnt_local, w1s, w3s, round_bf16_=False,
+def grouped_gemm1_swiglu(x_perm, seg_offsets, cnt_local, w1s, w3s, round_h=False,
                          nthreads=None) -> np.ndarray:
     """h over the permuted layout (fp64 [rows, Hl]; unfilled rows are NaN)."""
     x_perm = _c(x_perm)
@@ -297,13 +307,13 @@ def grouped_gemm1_swiglu(x_perm, seg_offsets, cnt_local, w1s, w3s, round_bf16_=F
     t3, k3 = _ptr_table(w3s, E_local)
     h = np.full((x_perm.shape[0], Hl), np.nan)
     _load().oracle_grouped_gemm1_swiglu(D, Hl, E_local, _p(seg), _p(cnt), _p(x_perm), _dt(x_perm),
-                                        t1, t3, _dt(first), int(round_bf16_), _p(h),
+                                        t1, t3, _dt(first), _rounding(round_h, False), _p(h),
                                         nthreads or default_threads())
     del k1, k3
     return h
 
 
-def grouped_gemm2(h, seg_offsets, cnt_local, w2s, round_bf16_=False, nthreads=None) -> np.ndarray:
+def grouped_gemm2(h, seg_offsets, cnt_local, w2s, round_y=False, nthreads=None) -> np.ndarray:
     """y_perm over the permuted layout (fp64 [rows, D]; unfilled rows NaN)."""
     h = _c(h)
     seg = _c(seg_offsets, np.int32)
@@ -314,7 +324,7 @@ def grouped_gemm2(h, seg_offsets, cnt_local, w2s, round_bf16_=False, nthreads=No
     t2, k2 = _ptr_table(w2s, E_local)
     y = np.full((h.shape[0], D), np.nan)
     _load().oracle_grouped_gemm2(D, Hl, E_local, _p(seg), _p(cnt), _p(h), _dt(h), t2, _dt(first),
-                                 int(round_bf16_), _p(y), nthreads or default_threads())
+                                 _rounding(False, round_y), _p(y), nthreads or default_threads())
     del k2
     return y
 

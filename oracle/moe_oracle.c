@@ -40,6 +40,8 @@ enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
 enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1 };
 /* layouts */
 enum { ORC_CONTIGUOUS = 0, ORC_MASKED = 1 };
+/* rounding points (bit flags): where the bf16 pipeline stores a bf16 tensor */
+enum { ORC_ROUND_H = 1, ORC_ROUND_Y = 2 };
 /* return codes */
 enum { ORC_OK = 0, ORC_BAD_ARG = 1, ORC_CAPACITY = 3, ORC_BAD_ROUTING = 6 };
 
@@ -341,12 +343,12 @@ void oracle_permute_rows(long rows, int D, int elem_bytes, const void *x,
  * section 4.3, here for one expert and one H shard of width Hl):
  *   a[h] = SiLU(sum_d w1[h,d] v[d]) * (sum_d w3[h,d] v[d])     h < Hl
  *   y[d] = sum_h w2[d,h] a[h]                                   d < D
- * With round_bf16 set, a and y are rounded to bf16 where the bf16 pipeline
- * stores them (the h and y_perm tensors).
+ * `rounding` selects where values are rounded to bf16: ORC_ROUND_H rounds a
+ * (stored as the bf16 h tensor), ORC_ROUND_Y rounds y.
  */
 static void expert_ffn(int D, int Hl, const void *w1, const void *w3,
                        const void *w2, int wdt, const double *v,
-                       int round_bf16, double *a, double *y)
+                       int rounding, double *a, double *y)
 {
     for (int h = 0; h < Hl; ++h) {
         double g = 0.0, u = 0.0;
@@ -355,23 +357,23 @@ static void expert_ffn(int D, int Hl, const void *w1, const void *w3,
             u += load_elem(w3, wdt, (size_t)h * D + d) * v[d];
         }
         double act = oracle_silu(g) * u;
-        a[h] = round_bf16 ? oracle_round_bf16(act) : act;
+        a[h] = (rounding & ORC_ROUND_H) ? oracle_round_bf16(act) : act;
     }
     for (int d = 0; d < D; ++d) {
         double acc = 0.0;
         for (int h = 0; h < Hl; ++h)
             acc += load_elem(w2, wdt, (size_t)d * Hl + h) * a[h];
-        y[d] = round_bf16 ? oracle_round_bf16(acc) : acc;
+        y[d] = (rounding & ORC_ROUND_Y) ? oracle_round_bf16(acc) : acc;
     }
 }
 
 void oracle_expert_ffn(int D, int Hl, const void *w1, const void *w3,
                        const void *w2, int wdt, const double *v,
-                       int round_bf16, double *y)
+                       int rounding, double *y)
 {
     double *a = (double *)malloc(sizeof(double) * (size_t)(Hl > 0 ? Hl : 1));
     if (!a) return;
-    expert_ffn(D, Hl, w1, w3, w2, wdt, v, round_bf16, a, y);
+    expert_ffn(D, Hl, w1, w3, w2, wdt, v, rounding, a, y);
     free(a);
 }
 
@@ -384,7 +386,7 @@ void oracle_expert_ffn(int D, int Hl, const void *w1, const void *w3,
  * entry is allowed for experts no listed token uses.
  */
 typedef struct {
-    int D, Hl, k, e_first, E_local, xdt, wdt, round_bf16;
+    int D, Hl, k, e_first, E_local, xdt, wdt, rounding;
     const void *x;
     const void *const *w1s, *const *w3s, *const *w2s;
     const int32_t *tokens, *topk_idx;
@@ -412,7 +414,7 @@ static void tokens_range(void *c, long lo, long hi)
             if (e < 0 || e >= p->E_local) continue;
             if (!p->w1s[e] || !p->w3s[e] || !p->w2s[e]) { *p->missing = 1; continue; }
             expert_ffn(p->D, p->Hl, p->w1s[e], p->w3s[e], p->w2s[e], p->wdt, v,
-                       p->round_bf16, a, y);
+                       p->rounding, a, y);
             double w = p->topk_w[(size_t)t * p->k + j];
             for (int d = 0; d < p->D; ++d) o[d] += w * y[d];
         }
@@ -424,11 +426,11 @@ int oracle_moe_tokens(int ntok, const int32_t *tokens, int D, int Hl, int k,
                       int e_first, int E_local, const void *x, int xdt,
                       const void *const *w1s, const void *const *w3s,
                       const void *const *w2s, int wdt, const int32_t *topk_idx,
-                      const double *topk_w, int round_bf16, double *out,
+                      const double *topk_w, int rounding, double *out,
                       int nthreads)
 {
     int missing = 0;
-    tokens_ctx c = {D, Hl, k, e_first, E_local, xdt, wdt, round_bf16, x,
+    tokens_ctx c = {D, Hl, k, e_first, E_local, xdt, wdt, rounding, x,
                     w1s, w3s, w2s, tokens, topk_idx, topk_w, out, &missing};
     parallel_for(ntok, nthreads, tokens_range, &c);
     return missing ? ORC_BAD_ARG : ORC_OK;
@@ -445,7 +447,7 @@ int oracle_moe_tokens(int ntok, const int32_t *tokens, int D, int Hl, int k,
  * Rows outside the filled ranges are left untouched.
  */
 typedef struct {
-    int D, Hl, E_local, xdt, wdt, round_bf16, which;
+    int D, Hl, E_local, xdt, wdt, rounding, which;
     const int32_t *seg_off, *cnt_local;
     const void *in;
     const void *const *wa, *const *wb;
@@ -468,7 +470,8 @@ static void grouped_range(void *c, long lo, long hi)
                         u += xv * load_elem(p->wb[i], p->wdt, (size_t)c2 * p->D + d);
                     }
                     double act = oracle_silu(g) * u;
-                    p->out[(size_t)r * p->Hl + c2] = p->round_bf16 ? oracle_round_bf16(act) : act;
+                    p->out[(size_t)r * p->Hl + c2] =
+                        (p->rounding & ORC_ROUND_H) ? oracle_round_bf16(act) : act;
                 }
             } else {
                 for (int d = 0; d < p->D; ++d) {
@@ -476,7 +479,8 @@ static void grouped_range(void *c, long lo, long hi)
                     for (int c2 = 0; c2 < p->Hl; ++c2)
                         acc += load_elem(p->in, p->xdt, (size_t)r * p->Hl + c2) *
                                load_elem(p->wa[i], p->wdt, (size_t)d * p->Hl + c2);
-                    p->out[(size_t)r * p->D + d] = p->round_bf16 ? oracle_round_bf16(acc) : acc;
+                    p->out[(size_t)r * p->D + d] =
+                        (p->rounding & ORC_ROUND_Y) ? oracle_round_bf16(acc) : acc;
                 }
             }
         }
@@ -487,9 +491,9 @@ void oracle_grouped_gemm1_swiglu(int D, int Hl, int E_local,
                                  const int32_t *seg_off, const int32_t *cnt_local,
                                  const void *x_perm, int xdt,
                                  const void *const *w1s, const void *const *w3s,
-                                 int wdt, int round_bf16, double *h, int nthreads)
+                                 int wdt, int rounding, double *h, int nthreads)
 {
-    grouped_ctx c = {D, Hl, E_local, xdt, wdt, round_bf16, 1, seg_off, cnt_local,
+    grouped_ctx c = {D, Hl, E_local, xdt, wdt, rounding, 1, seg_off, cnt_local,
                      x_perm, w1s, w3s, h};
     parallel_for(E_local, nthreads, grouped_range, &c);
 }
@@ -497,10 +501,10 @@ void oracle_grouped_gemm1_swiglu(int D, int Hl, int E_local,
 /* Second grouped GEMM: y[r, d] = sum_c h[r, c] w2_i[d, c] over filled rows. */
 void oracle_grouped_gemm2(int D, int Hl, int E_local, const int32_t *seg_off,
                           const int32_t *cnt_local, const void *h, int hdt,
-                          const void *const *w2s, int wdt, int round_bf16,
+                          const void *const *w2s, int wdt, int rounding,
                           double *y, int nthreads)
 {
-    grouped_ctx c = {D, Hl, E_local, hdt, wdt, round_bf16, 2, seg_off, cnt_local,
+    grouped_ctx c = {D, Hl, E_local, hdt, wdt, rounding, 2, seg_off, cnt_local,
                      h, w2s, NULL, y};
     parallel_for(E_local, nthreads, grouped_range, &c);
 }

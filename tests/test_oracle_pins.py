@@ -275,7 +275,7 @@ def test_expert_ffn_one_hot_closed_form():
     assert not oracle.expert_ffn(v, w1, w3b, w2).any()
 
 
-def _numpy_moe(x, w1, w3, w2, idx, w, e_first=0, E_local=None, round_fn=None):
+def _numpy_moe(x, w1, w3, w2, idx, w, e_first=0, E_local=None, round_fn=None, round_y=True):
     """Layer output written with numpy matmuls (F.linear: X @ W^T)."""
     T, D = x.shape
     E_local = w1.shape[0] if E_local is None else E_local
@@ -292,7 +292,7 @@ def _numpy_moe(x, w1, w3, w2, idx, w, e_first=0, E_local=None, round_fn=None):
         if round_fn:
             hh = round_fn(hh)
         y = hh @ w2[i].T
-        if round_fn:
+        if round_fn and round_y:
             y = round_fn(y)
         np.add.at(out, tok, w[tok, slot][:, None] * y)
     return out
@@ -331,7 +331,8 @@ def test_bf16_rounding_points_match_torch():
 
     def tround(a):
         return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
-    got = oracle.moe_tokens(np.arange(T), x, list(w1), list(w3), list(w2), idx, w, round_bf16_=True)
+    got = oracle.moe_tokens(np.arange(T), x, list(w1), list(w3), list(w2), idx, w, round_h=True,
+                            round_y=True)
     # numpy evaluation rounding h and y through torch's bf16 cast; an fp64 ->
     # fp32 -> bf16 double rounding may differ by one bf16 step in rare cases
     ref = _numpy_moe(x, w1, w3, w2, idx, w, round_fn=tround)
@@ -339,6 +340,11 @@ def test_bf16_rounding_points_match_torch():
     assert err < 1e-2
     unrounded = oracle.moe_tokens(np.arange(T), x, list(w1), list(w3), list(w2), idx, w)
     assert np.abs(got - unrounded).max() > 0     # the rounding points are real
+    # h alone: numpy evaluation rounding only h
+    got_h = oracle.moe_tokens(np.arange(T), x, list(w1), list(w3), list(w2), idx, w, round_h=True)
+    ref_h = _numpy_moe(x, w1, w3, w2, idx, w, round_fn=tround, round_y=False)
+    assert np.abs(got_h - ref_h).max() / np.sqrt((ref_h ** 2).mean()) < 1e-2
+    assert np.abs(got_h - got).max() > 0 and np.abs(got_h - unrounded).max() > 0
 
 
 def test_h_shards_sum_to_full_output():
