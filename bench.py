@@ -1,0 +1,409 @@
+"""Benchmark of the MoE layer local data path on one GB300 (or N replicas).
+
+Workload: fine-grained-bf16 (T=4096 tokens, D=2048, H=1408, E=64 experts,
+top-6, softmax renormalised; bf16 activations and weights, fp32
+accumulation), seeded synthetic inputs from moe_inputs.py, resident in HBM.
+
+One step = router top-k -> permute -> grouped SwiGLU (GEMM1 + gate, GEMM2)
+-> weighted combine, issued as the four step calls of the C ABI on one
+stream.  The line reports routed tokens/s (value), the grouped GEMM's
+TFLOP/s against the measured bf16 peak (roofline), permute and combine GB/s
+(breakdown), an end-to-end figure through moe_layer_forward with host
+buffers (e2e), and the CPU oracle timed on a bounded sample (cpu_baseline).
+
+Multi-GPU: the path does not exchange data; each rank runs an independent
+replica on its own GPU ("scaling": "weak") and value = all ranks' tokens / the
+slowest rank's time.
+
+--impl reference times the CPU oracle (the reference arm of this build) on
+the same workload and prints the same kind of line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "fine-grained-bf16"
+METRIC = "MoE layer routed tokens/s"
+UNIT = "tokens/s"
+L2_NOTE = "inputs larger than L2: 1.1 GB of expert weights per step, no flush"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algorithmic(w):
+    R = w.T * w.k
+    b = 2 if w.dtype == "bf16" else 4
+    return dict(
+        ffn_flops=6.0 * R * w.D * w.H,
+        permute_bytes=float(w.T * w.D * b + R * w.D * b),
+        combine_bytes=float(R * w.D * b + w.T * w.D * b + R * 8),
+    )
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("grouped_tc.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "routing_grouped_gemm_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the grouped GEMM from a committed ncu summary,
+    only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "grouped_swiglu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_hash") != kernel_source_hash() or d.get("workload") != WORKLOAD:
+        return None
+    return d.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_tokens_per_s(inp_host, w, n_tokens, seed=0, nthreads=None):
+    """Time the oracle's whole layer (router + per-token experts) on a sample."""
+    import numpy as np
+    import oracle
+    x, wg, w1, w3, w2 = inp_host
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(w.T, size=n_tokens, replace=False)).astype(np.int32)
+    nth = nthreads or oracle.default_threads()
+    t0 = time.perf_counter()
+    xs = x[toks]
+    _, _, idx, wts, _ = oracle.route(xs, wg, None, w.k,
+                                     oracle.SOFTMAX if w.score == "softmax" else oracle.SIGMOID,
+                                     w.renorm, nthreads=nth)
+    oracle.moe_tokens(np.arange(n_tokens), xs, list(w1), list(w3), list(w2), idx, wts,
+                      round_h=(w.dtype == "bf16"), nthreads=nth)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, nth
+
+
+def host_inputs(inp):
+    import moe_inputs
+    H = moe_inputs.host_array
+    return H(inp.x), H(inp.wg), H(inp.w1), H(inp.w3), H(inp.w2)
+
+
+def cpu_model():
+    try:
+        for l in open("/proc/cpuinfo"):
+            if l.lower().startswith(("model name", "cpu part")):
+                return l.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands, on the host cores."""
+    import torch
+    import moe_inputs
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = moe_inputs.WORKLOADS[WORKLOAD]
+    inp = moe_inputs.make_inputs(w, device="cpu", seed=0)
+    hin = host_inputs(inp)
+    # calibrate so the whole run stays within about two minutes
+    tps, _, nth = oracle_tokens_per_s(hin, w, 16, seed=99)
+    budget_s = 120.0
+    per_step = max(1, min(w.T, int(tps * budget_s / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        oracle_tokens_per_s(hin, w, per_step, seed=i)
+    times = []
+    for i in range(args.steps):
+        _, dt, _ = oracle_tokens_per_s(hin, w, per_step, seed=1000 + i)
+        times.append(dt)
+    total = sum(times)
+    value = per_step * args.steps / total
+    sample = f"{per_step} sampled tokens per step of the {WORKLOAD} batch (router + per-token experts)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps * (w.T / per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
+                   "parallelism": "replicas" if world > 1 else "single", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import moe_inputs
+    import routing_grouped_gemm_gb300 as moe
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    w = moe_inputs.WORKLOADS[WORKLOAD]
+    inp = moe_inputs.make_inputs(w, device=dev, seed=rank)
+    cfg = moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k, dtype=moe.MOE_BF16,
+                     score=moe.MOE_SCORE_SOFTMAX, renorm=1, align_m=128)
+    ra = moe.rows_alloc(cfg)
+    ws = moe.alloc_workspace(cfg, device=dev)
+    logits = None
+    topk_idx = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    topk_w = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    tpe = torch.empty(w.E, dtype=torch.int32, device=dev)
+    seg = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    tor = torch.empty(ra, dtype=torch.int32, device=dev)
+    x_perm = torch.empty((ra, w.D), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((ra, w.H), dtype=torch.bfloat16, device=dev)
+    y_perm = torch.empty((ra, w.D), dtype=torch.float32, device=dev)
+    out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    LAUNCHES_PER_STEP = 8  # router, count, scan, index, copy, GEMM1, GEMM2, combine
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_route_topk(cfg, inp.x, inp.wg, inp.bias, logits, topk_idx, topk_w, ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_permute(cfg, inp.x, topk_idx, tpe, seg, row_of, tor, x_perm, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_grouped_swiglu(cfg, x_perm, seg, tpe, inp.w1, inp.w3, inp.w2, h, y_perm, ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_unpermute_combine(cfg, y_perm, row_of, topk_w, out, ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = moe.moe_get_device_status(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    st = moe.moe_get_device_status(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
+
+    parts = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
+    mean_parts = parts.mean(0)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * w.T / (ms_per_step * 1e-3)
+
+    # end to end: moe_layer_forward with pinned host input / output each step
+    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
+    x_host = inp.x.cpu().pin_memory()
+    out_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(cfg, x_dev, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, lws, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(10, args.steps // 4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st = moe.moe_get_device_status(lws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after e2e: {moe.status_string(st)}")
+
+    alg = algorithmic(w)
+    peaks = load_peaks()
+    gemm_ms = float(mean_parts[2])
+    achieved = alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12
+    tpe_h = tpe.cpu().numpy()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": WORKLOAD, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
+                   "router": "softmax, renormalised over top-k", "layout": "contiguous, align_m=128",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single", "l2": L2_NOTE},
+        "roofline": {"kernel": "grouped SwiGLU (GEMM1 + gate, GEMM2): 2 launches per call",
+                     "bound": "tensor", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": f"{peaks['source']} bf16 burst",
+                     "traffic": recorded_traffic(),
+                     "algorithmic_flops_per_call": alg["ffn_flops"]},
+        "breakdown_ms": {"route": float(mean_parts[0]), "permute": float(mean_parts[1]),
+                         "grouped_swiglu": gemm_ms, "combine": float(mean_parts[3])},
+        "bandwidth": {
+            "permute_gbs": alg["permute_bytes"] / (mean_parts[1] * 1e-3) / 1e9,
+            "combine_gbs": alg["combine_bytes"] / (mean_parts[3] * 1e-3) / 1e9,
+            "hbm_peak_gbs": peaks["hbm_gbs"]},
+        "gemm_tflops": achieved,
+        "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
+                              "zeros": int((tpe_h == 0).sum())},
+        "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(out_host.numel() * 2),
+                "api": "moe_layer_forward, pinned host x in / out each step"},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if rank == 0 and not args.no_cpu_baseline:
+        hin = host_inputs(inp)
+        tps, _, nth = oracle_tokens_per_s(hin, w, 16, seed=99)
+        n = int(max(16, min(w.T, tps * args.cpu_seconds)))
+        tps, dt, nth = oracle_tokens_per_s(hin, w, n, seed=7)
+        line["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": nth, "kind": "oracle",
+                                "sample": f"{n} sampled tokens of the {WORKLOAD} batch, router + "
+                                          f"per-token experts in fp64 ({dt:.1f} s)",
+                                "cpu": cpu_model()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

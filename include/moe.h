@@ -1,0 +1,222 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE layer local data path.
+ *
+ * The layer, per token t of x[T, D] (page "Expert Parallelism (EP)",
+ * llm-infra-atlas, section 1 "MoE layer forward path"):
+ *   1. gating logits  l = x . W_g^T (+ b)                     [T, E]
+ *   2. top-k experts and their routing weights (softmax or sigmoid scores,
+ *      optionally renormalised over the chosen k)
+ *   3. tokens_per_expert and the dispatch permute into an expert-contiguous
+ *      layout whose segments are padded to the GEMM M tile (same page,
+ *      section 2, the layout contract between dispatch and grouped GEMM)
+ *   4. m-grouped expert FFN, SwiGLU form: h = SiLU(X_e w1_e^T) * (X_e w3_e^T),
+ *      y = h w2_e^T, with GroupedExperts weights w1/w3 [E, H, D] and
+ *      w2 [E, D, H] (page "Expert Tensor Parallel design", HyperParallel
+ *      issue 104, section 4.3)
+ *   5. unpermute with the top-k weighted reduce back to token order
+ *      (page "Expert Parallelism (EP)", section 1, combine post-process).
+ *
+ * Shards.  A call may cover an expert range [e_first, e_first + E_local) and
+ * one H shard of width H_local (w1/w3 split on dim 1, w2 on dim 2: "Expert
+ * Tensor Parallel design", section 4.3).  Its output is then a partial sum;
+ * the partials of all shards add up to the layer output (row-parallel
+ * identity Y = sum_t Y_partial^(t), page "NCCL course 32", section "Tensor
+ * Parallel matrix split").  The library itself never communicates.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, dense,
+ *     row-major, and 16-byte aligned.  The library allocates nothing.
+ *   - Element type of x, W_g, weights, x_perm, h and out is cfg->dtype
+ *     (MOE_F32 or MOE_BF16).  y_perm (the second GEMM's accumulator), router
+ *     bias, logits and topk_w are always fp32; indices are int32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream) and performs no host synchronisation.
+ *   - Host-side argument errors are returned before anything is launched.
+ *     A failed launch returns MOE_ERR_CUDA.  Problems only the device can
+ *     see (an expert id out of range, a NaN logit, masked capacity exceeded,
+ *     a bounded wait that ran out) set bits in a status word inside the
+ *     workspace; the kernels then skip the offending row instead of
+ *     touching memory out of bounds.  moe_get_device_status() reads it.
+ *   - The workspace `ws` (ws_bytes >= the size query of the call) must be
+ *     zero-filled once before first use; calls keep it consistent after.
+ *     Two calls that share a workspace must not run concurrently.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or enum value */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dtype mix) */
+    MOE_ERR_CAPACITY = 3,     /* masked layout: an expert got > capacity rows */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime / launch error */
+    MOE_ERR_TIMEOUT = 5,      /* a bounded device wait ran out */
+    MOE_ERR_BAD_ROUTING = 6,  /* expert id out of range, NaN logit, bad offsets */
+    MOE_ERR_WORKSPACE = 7     /* workspace missing, misaligned or too small */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score;
+typedef enum { MOE_LAYOUT_CONTIGUOUS = 0, MOE_LAYOUT_MASKED = 1 } moe_layout;
+
+/*
+ * Problem description shared by every call.
+ *   T        tokens (rows of x), >= 0
+ *   D        model dim, multiple of 8 (bf16: 16-byte rows for TMA)
+ *   H_local  expert hidden width held by this call (H, or H/tp for an H
+ *            shard), multiple of 8
+ *   E        total number of experts (router width), 1..1024
+ *   k        experts per token, 1..min(E, 32)
+ *   e_first, E_local  local expert range, 0 <= e_first, e_first+E_local <= E
+ *   dtype    moe_dtype; score moe_score; renorm 0/1 (renormalise the k
+ *            chosen scores to sum to one)
+ *   layout   moe_layout
+ *   align_m  contiguous layout: each expert segment is padded up to a
+ *            multiple of align_m rows (the GEMM M tile is 128; the bf16
+ *            grouped GEMM is fastest when align_m is a multiple of 128)
+ *   capacity masked layout: rows reserved per local expert (segment i
+ *            starts at i*capacity); ignored for the contiguous layout
+ */
+typedef struct {
+    int32_t T, D, H_local, E, k;
+    int32_t e_first, E_local;
+    int32_t dtype, score, renorm, layout;
+    int32_t align_m, capacity;
+} moe_config;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *moe_status_string(int32_t status);
+
+/* Text of the last host-side error of the calling thread ("" if none). */
+const char *moe_last_error_string(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int32_t moe_abi_version(void);
+
+/* MOE_OK if cfg describes a problem every call below accepts. */
+moe_status moe_validate_config(const moe_config *cfg);
+
+/*
+ * Rows of the permuted buffers x_perm / h / y_perm:
+ *   contiguous: T * min(k, E_local) + E_local * (align_m - 1)
+ *   masked:     E_local * capacity
+ * Returns -1 if cfg is invalid.
+ */
+int64_t moe_rows_alloc(const moe_config *cfg);
+
+/* Workspace bytes for the step calls (route, permute, grouped, combine). */
+int64_t moe_workspace_size(const moe_config *cfg);
+
+/* Workspace bytes for moe_layer_forward (includes every intermediate). */
+int64_t moe_layer_workspace_size(const moe_config *cfg);
+
+/*
+ * Step 1+2: router logits, top-k and routing weights
+ * ("Expert Parallelism (EP)", section 1: router.gating, routing).
+ *   x [T, D] (dtype), wg [E, D] (dtype), bias [E] fp32 or NULL.
+ *   logits_out [T, E] fp32 or NULL: the selection key l = x.wg^T + b
+ *     accumulated in fp32.
+ *   topk_idx [T, k] int32: chosen experts in selection order -- larger key
+ *     first, equal keys by lower expert index, NaN after every number.
+ *   topk_w [T, k] fp32: softmax over all E (or sigmoid) of the key at the
+ *     chosen experts, divided by their sum when cfg->renorm.
+ * A NaN key sets MOE_ERR_BAD_ROUTING in the status word.
+ */
+moe_status moe_route_topk(const moe_config *cfg, const void *x, const void *wg,
+                          const float *bias, float *logits_out, int32_t *topk_idx,
+                          float *topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Step 3: tokens_per_expert, segment offsets and dispatch permute
+ * ("Expert Parallelism (EP)", section 1 preprocess + permute; section 2
+ * layout contract).
+ *   topk_idx [T, k] int32 (any source; ids outside [0, E) are skipped and
+ *     flag MOE_ERR_BAD_ROUTING).
+ *   tokens_per_expert [E] int32: count of (t, j) with topk_idx = e, over all
+ *     E experts (so it sums to T*k).
+ *   seg_offsets [E_local + 1] int32: first row of each local expert's
+ *     segment; contiguous: exclusive scan of counts padded to align_m;
+ *     masked: i * capacity.
+ *   row_of [T, k] int32: row of x_perm holding (t, j), or -1 when expert
+ *     topk_idx[t, j] is not local.  Inside a segment rows are in ascending
+ *     token order.
+ *   token_of_row [rows_alloc] int32: the token of each row, -1 for padding.
+ *   x_perm [rows_alloc, D] (dtype): x_perm[row_of[t, j]] = x[t] bit for
+ *     bit.  Padding rows are not written (their contents are unspecified).
+ * Masked layout: an expert with more than `capacity` tokens keeps its first
+ * `capacity` (in token order), the rest get row_of = -1, and the status word
+ * gets MOE_ERR_CAPACITY.
+ */
+moe_status moe_permute(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                       int32_t *tokens_per_expert, int32_t *seg_offsets, int32_t *row_of,
+                       int32_t *token_of_row, void *x_perm, void *ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/*
+ * Step 4: m-grouped SwiGLU expert FFN over the permuted layout
+ * ("Expert Parallelism (EP)", section 1 routed_experts_compute and section
+ * 2 m-grouped GEMM; weight shapes "Expert Tensor Parallel design" 4.3).
+ *   x_perm [rows_alloc, D], seg_offsets [E_local + 1],
+ *   tokens_per_expert [E] (the global counts; local expert i reads entry
+ *     e_first + i; valid rows of segment i are the first
+ *     min(count, seg_offsets[i+1] - seg_offsets[i])).
+ *   w1, w3 [E_local, H_local, D]; w2 [E_local, D, H_local] (dtype).
+ *   h [rows_alloc, H_local] (dtype, written for valid rows):
+ *     h = SiLU(x_perm w1^T) * (x_perm w3^T), fp32 accumulation, one rounding.
+ *   y_perm [rows_alloc, D] fp32 (written for valid rows): y = h w2^T, the
+ *     fp32 accumulator itself -- it is rounded to dtype only after the
+ *     weighted combine.
+ * Segments may have any length; offsets outside [0, rows_alloc] flag
+ * MOE_ERR_BAD_ROUTING and the segment is skipped.
+ */
+moe_status moe_grouped_swiglu(const moe_config *cfg, const void *x_perm,
+                              const int32_t *seg_offsets, const int32_t *tokens_per_expert,
+                              const void *w1, const void *w3, const void *w2, void *h,
+                              void *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Step 5: unpermute with the top-k weighted reduce ("Expert Parallelism
+ * (EP)", section 1 combine post-process; section 5: the transpose of the
+ * dispatch permute).
+ *   out[t, :] = sum_{j < k, row_of[t,j] >= 0} topk_w[t, j] * y_perm[row_of[t, j], :]
+ * y_perm [rows_alloc, D] fp32; summed in fp32 in slot order j, rounded once
+ * to dtype into out [T, D].  Tokens with no
+ * local expert get zeros.  Rows >= rows_alloc flag MOE_ERR_BAD_ROUTING and
+ * are skipped.
+ */
+moe_status moe_unpermute_combine(const moe_config *cfg, const void *y_perm,
+                                 const int32_t *row_of, const float *topk_w, void *out,
+                                 void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Steps 1-5 in order on one stream, every intermediate carved from ws
+ * (ws_bytes >= moe_layer_workspace_size(cfg)).  out [T, D] (dtype) is this
+ * call's partial output (the full layer output when the call holds every
+ * expert and the whole H).
+ */
+moe_status moe_layer_forward(const moe_config *cfg, const void *x, const void *wg,
+                             const float *bias, const void *w1, const void *w3,
+                             const void *w2, void *out, void *ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the workspace status word, clears it and
+ * returns the most serious flagged condition (MOE_OK if none).  Order:
+ * TIMEOUT, CAPACITY, BAD_ROUTING.
+ */
+moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

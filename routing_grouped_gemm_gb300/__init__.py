@@ -1,0 +1,309 @@
+"""Python binding of the GB300 MoE local data path (``include/moe.h``).
+
+Argument marshalling only: every function below checks shapes and dtypes,
+passes raw device pointers and the current CUDA stream to the C ABI of
+``_lib/libmoe.so`` and turns a non-OK status into ``MoeError``.  All compute
+runs in the library's sm_103a kernels; there is no fallback of any kind --
+importing this package fails if the library has not been built.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CAPACITY = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BAD_ROUTING, MOE_ERR_WORKSPACE = 4, 5, 6, 7
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
+MOE_LAYOUT_CONTIGUOUS, MOE_LAYOUT_MASKED = 0, 1
+
+# every symbol include/moe.h declares
+ABI_SYMBOLS = (
+    "moe_status_string", "moe_last_error_string", "moe_abi_version", "moe_validate_config",
+    "moe_rows_alloc", "moe_workspace_size", "moe_layer_workspace_size", "moe_route_topk",
+    "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine", "moe_layer_forward",
+    "moe_get_device_status",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({last_error_string()})")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "T", "D", "H_local", "E", "k", "e_first", "E_local", "dtype", "score", "renorm",
+        "layout", "align_m", "capacity")]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with routing_grouped_gemm_gb300.build.build() "
+            "(nvcc, sm_103a). There is no CPU or eager fallback.")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    C = ctypes.POINTER(moe_config)
+    sig = {
+        "moe_status_string": (ctypes.c_char_p, [I32]),
+        "moe_last_error_string": (ctypes.c_char_p, []),
+        "moe_abi_version": (I32, []),
+        "moe_validate_config": (I32, [C]),
+        "moe_rows_alloc": (I64, [C]),
+        "moe_workspace_size": (I64, [C]),
+        "moe_layer_workspace_size": (I64, [C]),
+        "moe_route_topk": (I32, [C, P, P, P, P, P, P, P, SZ, P]),
+        "moe_permute": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_grouped_swiglu": (I32, [C, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_unpermute_combine": (I32, [C, P, P, P, P, P, SZ, P]),
+        "moe_layer_forward": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_get_device_status": (I32, [P, SZ, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+# --------------------------------------------------------------------------
+# configuration
+# --------------------------------------------------------------------------
+
+@dataclass
+class Config:
+    T: int
+    D: int
+    H_local: int
+    E: int
+    k: int
+    e_first: int = 0
+    E_local: int = -1          # -1: every expert from e_first on
+    dtype: int = MOE_BF16
+    score: int = MOE_SCORE_SOFTMAX
+    renorm: int = 0
+    layout: int = MOE_LAYOUT_CONTIGUOUS
+    align_m: int = 128
+    capacity: int = 0
+
+    def c(self) -> moe_config:
+        el = self.E - self.e_first if self.E_local < 0 else self.E_local
+        return moe_config(self.T, self.D, self.H_local, self.E, self.k, self.e_first, el,
+                          self.dtype, self.score, int(bool(self.renorm)), self.layout,
+                          self.align_m, self.capacity)
+
+    @property
+    def e_local(self) -> int:
+        return self.E - self.e_first if self.E_local < 0 else self.E_local
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == MOE_BF16 else torch.float32
+
+
+def status_string(st: int) -> str:
+    return _lib.moe_status_string(int(st)).decode()
+
+
+def last_error_string() -> str:
+    return _lib.moe_last_error_string().decode()
+
+
+def abi_version() -> int:
+    return int(_lib.moe_abi_version())
+
+
+def validate_config(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_validate_config(ctypes.byref(c)))
+
+
+def rows_alloc(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_rows_alloc(ctypes.byref(c)))
+
+
+def workspace_size(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_workspace_size(ctypes.byref(c)))
+
+
+def layer_workspace_size(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_layer_workspace_size(ctypes.byref(c)))
+
+
+def alloc_workspace(cfg: Config, layer: bool = False, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace of the size the library asks for (torch-owned)."""
+    n = layer_workspace_size(cfg) if layer else workspace_size(cfg)
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "workspace size")
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(st: int, what: str):
+    if st != MOE_OK:
+        raise MoeError(st, what)
+
+
+def _expect(t, shape, dtype, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+# --------------------------------------------------------------------------
+# the ABI calls (same names as include/moe.h)
+# --------------------------------------------------------------------------
+
+def moe_route_topk(cfg: Config, x, wg, bias, logits_out, topk_idx, topk_w, ws, stream=None):
+    dt = cfg.torch_dtype
+    _expect(x, (cfg.T, cfg.D), dt, "x")
+    _expect(wg, (cfg.E, cfg.D), dt, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    if logits_out is not None:
+        _expect(logits_out, (cfg.T, cfg.E), torch.float32, "logits_out")
+    _expect(topk_idx, (cfg.T, cfg.k), torch.int32, "topk_idx")
+    _expect(topk_w, (cfg.T, cfg.k), torch.float32, "topk_w")
+    c = cfg.c()
+    _check(_lib.moe_route_topk(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(logits_out),
+                               _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_route_topk")
+
+
+def moe_permute(cfg: Config, x, topk_idx, tokens_per_expert, seg_offsets, row_of, token_of_row,
+                x_perm, ws, stream=None):
+    ra = rows_alloc(cfg)
+    _expect(x, (cfg.T, cfg.D), cfg.torch_dtype, "x")
+    _expect(topk_idx, (cfg.T, cfg.k), torch.int32, "topk_idx")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(seg_offsets, (cfg.e_local + 1,), torch.int32, "seg_offsets")
+    _expect(row_of, (cfg.T, cfg.k), torch.int32, "row_of")
+    _expect(token_of_row, (ra,), torch.int32, "token_of_row")
+    _expect(x_perm, (ra, cfg.D), cfg.torch_dtype, "x_perm")
+    c = cfg.c()
+    _check(_lib.moe_permute(ctypes.byref(c), _ptr(x), _ptr(topk_idx), _ptr(tokens_per_expert),
+                            _ptr(seg_offsets), _ptr(row_of), _ptr(token_of_row), _ptr(x_perm),
+                            _ptr(ws), ws.numel(), _stream(stream)), "moe_permute")
+
+
+def moe_grouped_swiglu(cfg: Config, x_perm, seg_offsets, tokens_per_expert, w1, w3, w2, h, y_perm,
+                       ws, stream=None):
+    ra = rows_alloc(cfg)
+    dt = cfg.torch_dtype
+    el = cfg.e_local
+    _expect(x_perm, (ra, cfg.D), dt, "x_perm")
+    _expect(seg_offsets, (el + 1,), torch.int32, "seg_offsets")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    _expect(h, (ra, cfg.H_local), dt, "h")
+    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    c = cfg.c()
+    _check(_lib.moe_grouped_swiglu(ctypes.byref(c), _ptr(x_perm), _ptr(seg_offsets),
+                                   _ptr(tokens_per_expert), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(h),
+                                   _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_swiglu")
+
+
+def moe_unpermute_combine(cfg: Config, y_perm, row_of, topk_w, out, ws, stream=None):
+    ra = rows_alloc(cfg)
+    dt = cfg.torch_dtype
+    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    _expect(row_of, (cfg.T, cfg.k), torch.int32, "row_of")
+    _expect(topk_w, (cfg.T, cfg.k), torch.float32, "topk_w")
+    _expect(out, (cfg.T, cfg.D), dt, "out")
+    c = cfg.c()
+    _check(_lib.moe_unpermute_combine(ctypes.byref(c), _ptr(y_perm), _ptr(row_of), _ptr(topk_w),
+                                      _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_unpermute_combine")
+
+
+def moe_layer_forward(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None):
+    dt = cfg.torch_dtype
+    el = cfg.e_local
+    _expect(x, (cfg.T, cfg.D), dt, "x")
+    _expect(wg, (cfg.E, cfg.D), dt, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    _expect(out, (cfg.T, cfg.D), dt, "out")
+    c = cfg.c()
+    _check(_lib.moe_layer_forward(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w1),
+                                  _ptr(w3), _ptr(w2), _ptr(out), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "moe_layer_forward")
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    """Synchronise, read and clear the workspace status word (returns a code)."""
+    return int(_lib.moe_get_device_status(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def layer_views(cfg: Config, ws: torch.Tensor) -> dict:
+    """Views of the intermediates moe_layer_forward keeps in its workspace.
+
+    Mirrors the carving order of the library (256-byte aligned regions after
+    the step workspace): topk_idx, topk_w, tokens_per_expert, seg_offsets,
+    row_of, token_of_row, x_perm, h, y_perm.
+    """
+    def up(n):
+        return (n + 255) // 256 * 256
+    off = workspace_size(cfg)
+    R = cfg.T * cfg.k
+    ra = rows_alloc(cfg)
+    el = cfg.e_local
+    dt = cfg.torch_dtype
+    eb = 2 if cfg.dtype == MOE_BF16 else 4
+    out = {}
+    for name, n, tdt, shape in (
+            ("topk_idx", R, torch.int32, (cfg.T, cfg.k)),
+            ("topk_w", R, torch.float32, (cfg.T, cfg.k)),
+            ("tokens_per_expert", cfg.E, torch.int32, (cfg.E,)),
+            ("seg_offsets", el + 1, torch.int32, (el + 1,)),
+            ("row_of", R, torch.int32, (cfg.T, cfg.k)),
+            ("token_of_row", ra, torch.int32, (ra,)),
+            ("x_perm", ra * cfg.D, dt, (ra, cfg.D)),
+            ("h", ra * cfg.H_local, dt, (ra, cfg.H_local)),
+            ("y_perm", ra * cfg.D, torch.float32, (ra, cfg.D))):
+        nbytes = n * (4 if tdt in (torch.int32, torch.float32) else eb)
+        out[name] = ws[off:off + nbytes].view(tdt).view(shape)
+        off += up(nbytes)
+    return out

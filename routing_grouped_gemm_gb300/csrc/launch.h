@@ -1,0 +1,43 @@
+// Internal launchers of the MoE data-path kernels (host side).  Each
+// returns the launch's cudaError_t; argument validation is done by the
+// C ABI layer before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
+                               int *topk_idx, float *topk_w, int T, int D, int E, int k,
+                               int score, int renorm, int is_bf16, int *status,
+                               cudaStream_t stream);
+
+// Scratch ints needed by launch_permute: blocks of 256 tokens x E, twice.
+int64_t permute_scratch_ints(int T, int E);
+
+cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_expert,
+                           int *seg_offsets, int *row_of, int *token_of_row, void *x_perm,
+                           int T, int D, int E, int k, int e_first, int E_local, int layout,
+                           int align_m, int capacity, int64_t rows_alloc, int elem_bytes,
+                           int *scratch, int *status, cudaStream_t stream);
+
+cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *topk_w, void *out,
+                           int T, int D, int k, int64_t rows_alloc, int is_bf16, int *status,
+                           cudaStream_t stream);
+
+// fp32 SIMT grouped SwiGLU (both GEMMs).
+cudaError_t launch_grouped_swiglu_f32(const float *x_perm, const int *seg_offsets,
+                                      const int *tokens_per_expert, const float *w1,
+                                      const float *w3, const float *w2, float *h, float *y_perm,
+                                      int D, int H_local, int e_first, int E_local,
+                                      int64_t rows_alloc, int *status, cudaStream_t stream);
+
+// bf16 tcgen05 grouped SwiGLU (both GEMMs).
+cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offsets,
+                                       const int *tokens_per_expert, const void *w1,
+                                       const void *w3, const void *w2, void *h, void *y_perm,
+                                       int D, int H_local, int e_first, int E_local,
+                                       int64_t rows_alloc, int *status, cudaStream_t stream);
+
+}  // namespace moe

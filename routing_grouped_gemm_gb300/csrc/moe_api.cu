@@ -1,0 +1,328 @@
+// C ABI of the MoE layer local data path: argument validation, workspace
+// carving and the launch sequence.  Declarations and contracts: moe.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "launch.h"
+
+#define MOE_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr int32_t kAbiVersion = 10000;  // 1.0.0
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int64_t kAlign = 256;
+
+thread_local char g_last_error[256] = "";
+
+int64_t align_up(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+moe_status cuda_fail(cudaError_t e, const char *where) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
+
+moe_status arg_fail(const char *why, moe_status st = MOE_ERR_INVALID_ARG) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", why);
+    return st;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_bytes(const moe_config *c) { return c->dtype == MOE_BF16 ? 2 : 4; }
+
+int64_t rows_alloc_of(const moe_config *c) {
+    if (c->layout == MOE_LAYOUT_MASKED) return (int64_t)c->E_local * c->capacity;
+    const int64_t kl = c->k < c->E_local ? c->k : c->E_local;
+    return (int64_t)c->T * kl + (int64_t)c->E_local * (c->align_m - 1);
+}
+
+moe_status validate(const moe_config *c) {
+    if (!c) return arg_fail("config is NULL");
+    if (c->T < 0) return arg_fail("T < 0");
+    if (c->D < 8 || c->D % 8) return arg_fail("D must be a positive multiple of 8");
+    if (c->H_local < 8 || c->H_local % 8) return arg_fail("H_local must be a positive multiple of 8");
+    if (c->E < 1 || c->E > kMaxExperts) return arg_fail("E must be in 1..1024");
+    if (c->k < 1 || c->k > c->E || c->k > kMaxTopK) return arg_fail("k must be in 1..min(E, 32)");
+    if (c->e_first < 0 || c->E_local < 0 || c->e_first + c->E_local > c->E)
+        return arg_fail("expert range outside [0, E)");
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return arg_fail("unknown dtype");
+    if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID)
+        return arg_fail("unknown score function");
+    if (c->renorm != 0 && c->renorm != 1) return arg_fail("renorm must be 0 or 1");
+    if (c->layout != MOE_LAYOUT_CONTIGUOUS && c->layout != MOE_LAYOUT_MASKED)
+        return arg_fail("unknown layout");
+    if (c->layout == MOE_LAYOUT_CONTIGUOUS && (c->align_m < 1 || c->align_m > (1 << 16)))
+        return arg_fail("align_m must be in 1..65536");
+    if (c->layout == MOE_LAYOUT_MASKED && c->capacity < 0) return arg_fail("capacity < 0");
+    if ((int64_t)c->T * c->k >= (int64_t)1 << 31) return arg_fail("T*k too large");
+    if (rows_alloc_of(c) >= (int64_t)1 << 31) return arg_fail("permuted rows exceed 2^31");
+    return MOE_OK;
+}
+
+struct StepWs {
+    moe::StatusBlock *status;
+    int *scratch;
+};
+
+int64_t step_ws_bytes(const moe_config *c) {
+    return (int64_t)sizeof(moe::StatusBlock) + align_up(4 * moe::permute_scratch_ints(c->T, c->E));
+}
+
+moe_status carve_step(const moe_config *c, void *ws, size_t ws_bytes, StepWs *out) {
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < step_ws_bytes(c)) return arg_fail("workspace too small", MOE_ERR_WORKSPACE);
+    out->status = static_cast<moe::StatusBlock *>(ws);
+    out->scratch = reinterpret_cast<int *>(static_cast<char *>(ws) + sizeof(moe::StatusBlock));
+    return MOE_OK;
+}
+
+struct LayerWs {
+    StepWs step;
+    int *topk_idx, *tpe, *seg_off, *row_of, *token_of_row;
+    float *topk_w;
+    void *x_perm, *h, *y_perm;
+};
+
+int64_t layer_ws_layout(const moe_config *c, char *base, LayerWs *L) {
+    int64_t off = step_ws_bytes(c);
+    const int64_t R = (int64_t)c->T * c->k;
+    const int64_t rows = rows_alloc_of(c);
+    const int eb = elem_bytes(c);
+    auto take = [&](int64_t bytes) -> char * {
+        char *p = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return p;
+    };
+    char *p_idx = take(4 * R);
+    char *p_w = take(4 * R);
+    char *p_tpe = take(4 * (int64_t)c->E);
+    char *p_seg = take(4 * ((int64_t)c->E_local + 1));
+    char *p_row = take(4 * R);
+    char *p_tor = take(4 * rows);
+    char *p_xp = take(rows * c->D * eb);
+    char *p_h = take(rows * c->H_local * eb);
+    char *p_yp = take(rows * c->D * 4);  // y_perm is fp32 for every dtype
+    if (L) {
+        L->topk_idx = reinterpret_cast<int *>(p_idx);
+        L->topk_w = reinterpret_cast<float *>(p_w);
+        L->tpe = reinterpret_cast<int *>(p_tpe);
+        L->seg_off = reinterpret_cast<int *>(p_seg);
+        L->row_of = reinterpret_cast<int *>(p_row);
+        L->token_of_row = reinterpret_cast<int *>(p_tor);
+        L->x_perm = p_xp;
+        L->h = p_h;
+        L->y_perm = p_yp;
+    }
+    return off;
+}
+
+bool need16(const void *p) { return p && aligned(p, 16); }
+
+// ---------------------------------------------------------------------
+// step implementations (arguments already validated)
+// ---------------------------------------------------------------------
+moe_status do_route(const moe_config *c, const void *x, const void *wg, const float *bias,
+                    float *logits_out, int32_t *topk_idx, float *topk_w, const StepWs &w,
+                    cudaStream_t s) {
+    cudaError_t e = moe::launch_router_topk(x, wg, bias, logits_out, topk_idx, topk_w, c->T, c->D,
+                                            c->E, c->k, c->score, c->renorm, c->dtype == MOE_BF16,
+                                            &w.status->flags, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_topk");
+}
+
+moe_status do_permute(const moe_config *c, const void *x, const int32_t *topk_idx, int32_t *tpe,
+                      int32_t *seg, int32_t *row_of, int32_t *tor, void *x_perm, const StepWs &w,
+                      cudaStream_t s) {
+    cudaError_t e = moe::launch_permute(x, topk_idx, tpe, seg, row_of, tor, x_perm, c->T, c->D, c->E,
+                                        c->k, c->e_first, c->E_local, c->layout, c->align_m,
+                                        c->capacity, rows_alloc_of(c), elem_bytes(c), w.scratch,
+                                        &w.status->flags, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_permute");
+}
+
+moe_status do_grouped(const moe_config *c, const void *x_perm, const int32_t *seg,
+                      const int32_t *tpe, const void *w1, const void *w3, const void *w2, void *h,
+                      void *y_perm, const StepWs &w, cudaStream_t s) {
+    cudaError_t e;
+    if (c->dtype == MOE_BF16)
+        e = moe::launch_grouped_swiglu_bf16(x_perm, seg, tpe, w1, w3, w2, h, y_perm, c->D,
+                                            c->H_local, c->e_first, c->E_local, rows_alloc_of(c),
+                                            &w.status->flags, s);
+    else
+        e = moe::launch_grouped_swiglu_f32((const float *)x_perm, seg, tpe, (const float *)w1,
+                                           (const float *)w3, (const float *)w2, (float *)h,
+                                           (float *)y_perm, c->D, c->H_local, c->e_first,
+                                           c->E_local, rows_alloc_of(c), &w.status->flags, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_grouped_swiglu");
+}
+
+moe_status do_combine(const moe_config *c, const void *y_perm, const int32_t *row_of,
+                      const float *topk_w, void *out, const StepWs &w, cudaStream_t s) {
+    cudaError_t e = moe::launch_combine(y_perm, row_of, topk_w, out, c->T, c->D, c->k,
+                                        rows_alloc_of(c), c->dtype == MOE_BF16, &w.status->flags, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_unpermute_combine");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------
+// exported ABI
+// ---------------------------------------------------------------------
+MOE_EXPORT const char *moe_status_string(int32_t status) {
+    switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_BAD_ROUTING: return "MOE_ERR_BAD_ROUTING";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+MOE_EXPORT const char *moe_last_error_string(void) { return g_last_error; }
+
+MOE_EXPORT int32_t moe_abi_version(void) { return kAbiVersion; }
+
+MOE_EXPORT moe_status moe_validate_config(const moe_config *cfg) { return validate(cfg); }
+
+MOE_EXPORT int64_t moe_rows_alloc(const moe_config *cfg) {
+    return validate(cfg) == MOE_OK ? rows_alloc_of(cfg) : -1;
+}
+
+MOE_EXPORT int64_t moe_workspace_size(const moe_config *cfg) {
+    return validate(cfg) == MOE_OK ? step_ws_bytes(cfg) : -1;
+}
+
+MOE_EXPORT int64_t moe_layer_workspace_size(const moe_config *cfg) {
+    return validate(cfg) == MOE_OK ? layer_ws_layout(cfg, nullptr, nullptr) : -1;
+}
+
+MOE_EXPORT moe_status moe_route_topk(const moe_config *cfg, const void *x, const void *wg,
+                                     const float *bias, float *logits_out, int32_t *topk_idx,
+                                     float *topk_w, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    if (!x || !wg || !topk_idx || !topk_w) return arg_fail("moe_route_topk: NULL tensor");
+    const uintptr_t a = (uintptr_t)elem_bytes(cfg);
+    if (!aligned(x, a) || !aligned(wg, a) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+        (bias && !aligned(bias, 4)) || (logits_out && !aligned(logits_out, 4)))
+        return arg_fail("moe_route_topk: misaligned tensor");
+    return do_route(cfg, x, wg, bias, logits_out, topk_idx, topk_w, w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_permute(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                                  int32_t *tokens_per_expert, int32_t *seg_offsets,
+                                  int32_t *row_of, int32_t *token_of_row, void *x_perm, void *ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (!tokens_per_expert || !seg_offsets) return arg_fail("moe_permute: NULL tensor");
+    if (cfg->T > 0 && (!topk_idx || !row_of || !need16(x)))
+        return arg_fail("moe_permute: NULL or misaligned tensor");
+    if (rows_alloc_of(cfg) > 0 && (!token_of_row || !need16(x_perm)))
+        return arg_fail("moe_permute: NULL or misaligned tensor");
+    return do_permute(cfg, x, topk_idx, tokens_per_expert, seg_offsets, row_of, token_of_row,
+                      x_perm, w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_grouped_swiglu(const moe_config *cfg, const void *x_perm,
+                                         const int32_t *seg_offsets,
+                                         const int32_t *tokens_per_expert, const void *w1,
+                                         const void *w3, const void *w2, void *h, void *y_perm,
+                                         void *ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (cfg->E_local == 0 || rows_alloc_of(cfg) == 0) return MOE_OK;
+    if (!seg_offsets || !tokens_per_expert) return arg_fail("moe_grouped_swiglu: NULL offsets");
+    if (!need16(x_perm) || !need16(w1) || !need16(w3) || !need16(w2) || !need16(h) ||
+        !need16(y_perm))
+        return arg_fail("moe_grouped_swiglu: NULL or misaligned tensor");
+    return do_grouped(cfg, x_perm, seg_offsets, tokens_per_expert, w1, w3, w2, h, y_perm, w,
+                      (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_unpermute_combine(const moe_config *cfg, const void *y_perm,
+                                            const int32_t *row_of, const float *topk_w,
+                                            void *out, void *ws, size_t ws_bytes,
+                                            moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    if (!row_of || !topk_w || !need16(out)) return arg_fail("moe_unpermute_combine: NULL tensor");
+    if (rows_alloc_of(cfg) > 0 && !need16(y_perm))
+        return arg_fail("moe_unpermute_combine: NULL or misaligned y_perm");
+    return do_combine(cfg, y_perm, row_of, topk_w, out, w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_layer_forward(const moe_config *cfg, const void *x, const void *wg,
+                                        const float *bias, const void *w1, const void *w3,
+                                        const void *w2, void *out, void *ws, size_t ws_bytes,
+                                        moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < layer_ws_layout(cfg, nullptr, nullptr))
+        return arg_fail("workspace too small for moe_layer_forward", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!need16(x) || !need16(wg) || !need16(out) || (bias && !aligned(bias, 4)))
+        return arg_fail("moe_layer_forward: NULL or misaligned tensor");
+    if (cfg->E_local > 0 && (!need16(w1) || !need16(w3) || !need16(w2)))
+        return arg_fail("moe_layer_forward: NULL or misaligned expert weights");
+    LayerWs L;
+    carve_step(cfg, ws, ws_bytes, &L.step);
+    layer_ws_layout(cfg, static_cast<char *>(ws), &L);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = do_route(cfg, x, wg, bias, nullptr, L.topk_idx, L.topk_w, L.step, s)) != MOE_OK)
+        return st;
+    if ((st = do_permute(cfg, x, L.topk_idx, L.tpe, L.seg_off, L.row_of, L.token_of_row, L.x_perm,
+                         L.step, s)) != MOE_OK)
+        return st;
+    if (cfg->E_local > 0 && rows_alloc_of(cfg) > 0 &&
+        (st = do_grouped(cfg, L.x_perm, L.seg_off, L.tpe, w1, w3, w2, L.h, L.y_perm, L.step, s)) !=
+            MOE_OK)
+        return st;
+    return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
+}
+
+MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!ws || ws_bytes < sizeof(moe::StatusBlock) || !aligned(ws, kAlign))
+        return arg_fail("moe_get_device_status: bad workspace", MOE_ERR_WORKSPACE);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status: sync");
+    int host[2] = {0, 0};
+    e = cudaMemcpy(host, ws, sizeof host, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status: read");
+    if (host[0] != 0) {
+        e = cudaMemset(const_cast<void *>(ws), 0, sizeof host);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status: clear");
+    }
+    if (host[0] & moe::FLAG_TIMEOUT) {
+        snprintf(g_last_error, sizeof g_last_error, "bounded device wait ran out (CTA %d)", host[1] - 1);
+        return MOE_ERR_TIMEOUT;
+    }
+    if (host[0] & moe::FLAG_CAPACITY) return MOE_ERR_CAPACITY;
+    if (host[0] & moe::FLAG_BAD_ROUTING) return MOE_ERR_BAD_ROUTING;
+    return MOE_OK;
+}

@@ -1,0 +1,335 @@
+// Dispatch permute and weighted combine.
+//
+// Page "Expert Parallelism (EP)" (llm-infra-atlas):
+//   section 1 -- preprocess computes tokens_per_expert; permute-1 sorts the
+//     tokens by expert; combine post-process is the unpermute that reduces
+//     the top-k weighted expert outputs back into the original order;
+//   section 2 -- the layout contract: each expert's rows are contiguous and
+//     every segment is aligned to the grouped GEMM's M tile;
+//   section 5 -- permute (gather) and unpermute (scatter-add) are each
+//     other's transpose.
+//
+// The permutation is a stable counting sort (rows of an expert are in
+// ascending token order), built without order-dependent atomics so that it
+// is bit-identical run to run:
+//   count : per block of 256 tokens, per warp of 32 tokens, a bitmask per
+//           expert of which lanes route to it; block counts per expert
+//   scan  : one CTA; per-expert exclusive scan over blocks, tokens_per_expert,
+//           padded segment offsets, padding rows of token_of_row
+//   index : recomputes the masks; rank of (t, e) = rows of e in earlier
+//           blocks + earlier warps + popc(mask & lanes below)
+//   copy  : one warp per token reads x[t] once and writes its k copies
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int PB_TOKENS = 256;  // tokens per count/index block (8 warps x 32)
+constexpr int PB_WARPS = PB_TOKENS / 32;
+
+// Slot (t, j) takes part in the layout when its expert id is in [0, E) and
+// no earlier slot of the same token names the same expert.
+__device__ __forceinline__ bool slot_active(const int *__restrict__ row, int j, int E) {
+    const int e = row[j];
+    if (e < 0 || e >= E) return false;
+    for (int q = 0; q < j; ++q)
+        if (row[q] == e) return false;
+    return true;
+}
+
+__device__ __forceinline__ void build_masks(const int *__restrict__ topk_idx, int T, int k, int E,
+                                            uint32_t *s_mask, int *status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t *m = s_mask + warp * E;
+    for (int e = lane; e < E; e += 32) m[e] = 0u;
+    __syncwarp();
+    const int t = blockIdx.x * PB_TOKENS + warp * 32 + lane;
+    if (t < T) {
+        const int *row = topk_idx + (size_t)t * k;
+        bool bad = false;
+        for (int j = 0; j < k; ++j) {
+            if (slot_active(row, j, E)) atomicOr(&m[row[j]], 1u << lane);
+            else bad = true;
+        }
+        if (bad) raise_flag(status, FLAG_BAD_ROUTING);
+    }
+}
+
+__global__ void __launch_bounds__(PB_TOKENS)
+permute_count_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int *__restrict__ blk_cnt,
+                     int *status) {
+    extern __shared__ uint32_t s_mask[];  // [PB_WARPS][E]
+    build_masks(topk_idx, T, k, E, s_mask, status);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += PB_TOKENS) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < PB_WARPS; ++w) c += __popc(s_mask[w * E + e]);
+        blk_cnt[(size_t)blockIdx.x * E + e] = c;
+    }
+}
+
+constexpr int SCAN_THREADS = 1024;
+
+__global__ void __launch_bounds__(SCAN_THREADS)
+permute_scan_kernel(const int *__restrict__ blk_cnt, int nblk, int E, int e_first, int E_local,
+                    int layout, int align_m, int capacity, long long rows_alloc,
+                    int *__restrict__ tokens_per_expert, int *__restrict__ seg_offsets,
+                    int *__restrict__ blk_base, int *__restrict__ token_of_row, int *status) {
+    extern __shared__ int s_int[];
+    int *s_cnt = s_int;              // [E]
+    int *s_off = s_cnt + E;          // [E_local + 1]  (inclusive scan, shifted)
+    const int tid = threadIdx.x;
+
+    for (int e = tid; e < E; e += SCAN_THREADS) {
+        int run = 0;
+        for (int b = 0; b < nblk; ++b) {
+            const int c = blk_cnt[(size_t)b * E + e];
+            blk_base[(size_t)b * E + e] = run;
+            run += c;
+        }
+        tokens_per_expert[e] = run;
+        s_cnt[e] = run;
+    }
+    __syncthreads();
+
+    // padded segment sizes -> inclusive scan (E_local <= 1024, one per thread)
+    int size = 0;
+    if (tid < E_local) {
+        const int c = s_cnt[e_first + tid];
+        if (layout == 1) {
+            size = capacity;
+            if (c > capacity) raise_flag(status, FLAG_CAPACITY);
+        } else {
+            size = (c + align_m - 1) / align_m * align_m;
+        }
+        s_off[tid + 1] = size;
+    }
+    if (tid == 0) s_off[0] = 0;
+    __syncthreads();
+    for (int o = 1; o < E_local; o <<= 1) {
+        int v = 0;
+        if (tid < E_local && tid + 1 > o) v = s_off[tid + 1 - o];
+        __syncthreads();
+        if (tid < E_local && tid + 1 > o) s_off[tid + 1] += v;
+        __syncthreads();
+    }
+    for (int i = tid; i <= E_local; i += SCAN_THREADS) seg_offsets[i] = s_off[i];
+
+    // local experts: block bases become absolute rows; padding rows -> -1
+    for (int i = tid; i < E_local; i += SCAN_THREADS) {
+        const int e = e_first + i;
+        const int base = s_off[i];
+        for (int b = 0; b < nblk; ++b) blk_base[(size_t)b * E + e] += base;
+        const int used = min(s_cnt[e], s_off[i + 1] - base);
+        for (int r = base + used; r < s_off[i + 1]; ++r) token_of_row[r] = -1;
+    }
+    for (long long r = (long long)s_off[E_local] + tid; r < rows_alloc; r += SCAN_THREADS)
+        token_of_row[r] = -1;
+}
+
+__global__ void __launch_bounds__(PB_TOKENS)
+permute_index_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int e_first,
+                     int E_local, const int *__restrict__ blk_base,
+                     const int *__restrict__ seg_offsets, int *__restrict__ row_of,
+                     int *__restrict__ token_of_row, int *status) {
+    extern __shared__ uint32_t s_mask[];  // [PB_WARPS][E]
+    build_masks(topk_idx, T, k, E, s_mask, nullptr);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * PB_TOKENS + warp * 32 + lane;
+    if (t >= T) return;
+    const int *row = topk_idx + (size_t)t * k;
+    const uint32_t below = lanemask_lt();
+    for (int j = 0; j < k; ++j) {
+        int r = -1;
+        if (slot_active(row, j, E)) {
+            const int e = row[j];
+            const int i = e - e_first;
+            if (i >= 0 && i < E_local) {
+                int prior = __popc(s_mask[warp * E + e] & below);
+                for (int w = 0; w < warp; ++w) prior += __popc(s_mask[w * E + e]);
+                const int cand = blk_base[(size_t)blockIdx.x * E + e] + prior;
+                if (cand < seg_offsets[i + 1]) {
+                    r = cand;
+                    token_of_row[cand] = t;
+                } else {
+                    raise_flag(status, FLAG_CAPACITY);
+                }
+            }
+        }
+        row_of[(size_t)t * k + j] = r;
+    }
+}
+
+// One warp per token: read x[t] once in 16-byte vectors, write k copies.
+constexpr int CP_UNROLL = 4;
+
+__global__ void __launch_bounds__(256)
+permute_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_of,
+                    uint4 *__restrict__ x_perm, int T, int k, int vpr) {
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int my_row = lane < k ? row_of[(size_t)t * k + lane] : -1;
+    const uint4 *src = x + (size_t)t * vpr;
+    for (int v0 = 0; v0 < vpr; v0 += 32 * CP_UNROLL) {
+        uint4 buf[CP_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CP_UNROLL; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < vpr) buf[u] = __ldg(src + v);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int r = __shfl_sync(0xffffffffu, my_row, j);
+            if (r < 0) continue;
+            uint4 *dst = x_perm + (size_t)r * vpr;
+#pragma unroll
+            for (int u = 0; u < CP_UNROLL; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < vpr) dst[v] = buf[u];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------
+// combine: out[t] = sum_j w[t,j] * y_perm[row_of[t,j]]  (fp32, slot order)
+// ---------------------------------------------------------------------
+constexpr int CB_SLOTS = 8;  // slots whose loads are issued together
+
+// y_perm is fp32 for every dtype; out is bf16 or fp32.  The loop over
+// 16-byte output vectors is uniform across the warp (the shuffles inside
+// need every lane), with per-lane predicates for the row tail.
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
+               const float *__restrict__ topk_w, void *__restrict__ out, int T, int k, int D,
+               long long rows_alloc, int *status) {
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    int my_row = -1;
+    float my_w = 0.f;
+    if (lane < k) {
+        my_row = row_of[(size_t)t * k + lane];
+        my_w = topk_w[(size_t)t * k + lane];
+        if (my_row < -1 || (long long)my_row >= rows_alloc) {
+            raise_flag(status, FLAG_BAD_ROUTING);
+            my_row = -1;
+        }
+    }
+    constexpr int EPV = BF16 ? 8 : 4;      // output elements per 16-byte vector
+    const int vpr_out = D / EPV;           // output vectors per row
+    const int f4_per_out = EPV / 4;        // fp32 float4 loads per output vector
+    const int yvpr = D / 4;                // float4 per y row
+    for (int v0 = 0; v0 < vpr_out; v0 += 32) {
+        const int v = v0 + lane;
+        const bool act = v < vpr_out;
+        float acc[EPV];
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) acc[i] = 0.f;
+        for (int j0 = 0; j0 < k; j0 += CB_SLOTS) {
+            float4 val[CB_SLOTS][EPV / 4];
+            float wj[CB_SLOTS];
+            bool ok[CB_SLOTS];
+#pragma unroll
+            for (int u = 0; u < CB_SLOTS; ++u) {
+                const int j = j0 + u;
+                const int r = __shfl_sync(0xffffffffu, my_row, j & 31);
+                wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
+                ok[u] = act && (j < k) && (r >= 0);
+                if (ok[u]) {
+#pragma unroll
+                    for (int q = 0; q < EPV / 4; ++q)
+                        val[u][q] = __ldg(y + (size_t)r * yvpr + (size_t)v * f4_per_out + q);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < CB_SLOTS; ++u) {
+                if (!ok[u]) continue;
+#pragma unroll
+                for (int q = 0; q < EPV / 4; ++q) {
+                    acc[4 * q + 0] = fmaf(wj[u], val[u][q].x, acc[4 * q + 0]);
+                    acc[4 * q + 1] = fmaf(wj[u], val[u][q].y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(wj[u], val[u][q].z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(wj[u], val[u][q].w, acc[4 * q + 3]);
+                }
+            }
+        }
+        if (!act) continue;
+        uint4 o;
+        if (BF16) {
+            __nv_bfloat162 *hh = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        } else {
+            o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                           __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+        }
+        reinterpret_cast<uint4 *>(out)[(size_t)t * vpr_out + v] = o;
+    }
+}
+
+}  // namespace
+
+int64_t permute_scratch_ints(int T, int E) {
+    const int64_t nblk = (T + PB_TOKENS - 1) / PB_TOKENS;
+    return 2 * nblk * (int64_t)E;
+}
+
+cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_expert,
+                           int *seg_offsets, int *row_of, int *token_of_row, void *x_perm,
+                           int T, int D, int E, int k, int e_first, int E_local, int layout,
+                           int align_m, int capacity, int64_t rows_alloc, int elem_bytes,
+                           int *scratch, int *status, cudaStream_t stream) {
+    const int nblk = (T + PB_TOKENS - 1) / PB_TOKENS;
+    int *blk_cnt = scratch;
+    int *blk_base = scratch + (size_t)nblk * E;
+    const size_t mask_smem = sizeof(uint32_t) * PB_WARPS * (size_t)E;
+    cudaError_t err;
+    if (nblk > 0) {
+        err = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)mask_smem);
+        if (err != cudaSuccess) return err;
+        permute_count_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(topk_idx, T, k, E, blk_cnt,
+                                                                     status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    const size_t scan_smem = sizeof(int) * ((size_t)E + E_local + 1);
+    permute_scan_kernel<<<1, SCAN_THREADS, scan_smem, stream>>>(
+        blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
+        tokens_per_expert, seg_offsets, blk_base, token_of_row, status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (nblk == 0) return cudaSuccess;
+    err = cudaFuncSetAttribute(permute_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)mask_smem);
+    if (err != cudaSuccess) return err;
+    permute_index_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(
+        topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int vpr = D * elem_bytes / 16;
+    const int warps_per_block = 8;
+    const int blocks = (T + warps_per_block - 1) / warps_per_block;
+    permute_copy_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(
+        (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *topk_w, void *out,
+                           int T, int D, int k, int64_t rows_alloc, int is_bf16, int *status,
+                           cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    const int blocks = (T + warps_per_block - 1) / warps_per_block;
+    if (is_bf16)
+        combine_kernel<true><<<blocks, 32 * warps_per_block, 0, stream>>>(
+            (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
+    else
+        combine_kernel<false><<<blocks, 32 * warps_per_block, 0, stream>>>(
+            (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI library (no GPU needed, no compute calls).
+
+The library must build for sm_103a, load, export every function that
+include/moe.h declares, and reject bad arguments on the host before anything
+is launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import routing_grouped_gemm_gb300 as m
+    return m
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(moe):
+    declared = header_functions()
+    assert declared, "no declarations found in include/moe.h"
+    assert sorted(moe.ABI_SYMBOLS) == declared
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm103a():
+    import __graft_entry__
+    assert "arch=compute_103a,code=sm_103a" in __graft_entry__._build_module().ARCH
+
+
+def _cfg(moe, **kw):
+    base = dict(T=64, D=128, H_local=64, E=8, k=2, dtype=moe.MOE_BF16)
+    base.update(kw)
+    return moe.Config(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(D=12), dict(D=0), dict(H_local=4), dict(E=0), dict(E=2000), dict(k=0), dict(k=9),
+    dict(T=-1), dict(e_first=6, E_local=4), dict(dtype=7), dict(score=3), dict(align_m=0),
+    dict(layout=1, capacity=-1), dict(layout=5),
+])
+def test_invalid_configs_rejected(moe, bad):
+    assert moe.validate_config(_cfg(moe, **bad)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.rows_alloc(_cfg(moe, **bad)) == -1
+    assert moe.workspace_size(_cfg(moe, **bad)) == -1
+
+
+def test_rows_alloc_formula_matches_oracle(moe):
+    import oracle
+    for kw in (dict(), dict(align_m=1), dict(e_first=2, E_local=3), dict(E_local=1, k=2),
+               dict(layout=1, capacity=40), dict(T=0)):
+        cfg = _cfg(moe, **kw)
+        el = cfg.e_local
+        ref = oracle.rows_alloc(cfg.T, cfg.k, el, cfg.layout, cfg.align_m, cfg.capacity)
+        assert moe.rows_alloc(cfg) == ref
+
+
+def test_workspace_sizes_are_positive_and_ordered(moe):
+    cfg = _cfg(moe)
+    assert 256 <= moe.workspace_size(cfg) <= moe.layer_workspace_size(cfg)
+    assert moe.layer_workspace_size(cfg) % 256 == 0
+
+
+def test_host_errors_before_any_launch(moe):
+    lib = moe._lib
+    c = _cfg(moe).c()
+    # NULL workspace
+    st = lib.moe_route_topk(ctypes.byref(c), 16, 16, None, None, 16, 16, None, 0, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    # misaligned workspace
+    st = lib.moe_permute(ctypes.byref(c), 16, 16, 16, 16, 16, 16, 16, 1024 + 8, 1 << 20, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    # workspace too small
+    st = lib.moe_unpermute_combine(ctypes.byref(c), 16, 16, 16, 16, 256 * 64, 256, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    # NULL tensor with a large enough fake workspace
+    big = moe.layer_workspace_size(_cfg(moe))
+    st = lib.moe_grouped_swiglu(ctypes.byref(c), None, 16, 16, 16, 16, 16, 16, 16, 1 << 20, big,
+                                None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # misaligned expert weights
+    st = lib.moe_layer_forward(ctypes.byref(c), 256, 256, None, 8, 256, 256, 256, 1 << 20, big, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert "misaligned" in moe.last_error_string()
+    # invalid config wins over everything else
+    bad = _cfg(moe, k=99).c()
+    assert lib.moe_layer_forward(ctypes.byref(bad), 0, 0, None, 0, 0, 0, 0, 0, 0, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_get_device_status(None, 0, None) == moe.MOE_ERR_WORKSPACE
+
+
+def test_status_strings(moe):
+    assert moe.status_string(moe.MOE_OK) == "MOE_OK"
+    assert moe.status_string(moe.MOE_ERR_CAPACITY) == "MOE_ERR_CAPACITY"
+    assert moe.status_string(1234) == "MOE_ERR_UNKNOWN"
+    assert moe.abi_version() >= 10000
+
+
+def test_product_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "routing_grouped_gemm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, f
+                assert "moe_oracle" not in txt and "liboracle" not in txt, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            txt = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not re.search(r"^\s*(import|from)\s+(routing_grouped_gemm_gb300|moe_inputs)", txt,
+                                 flags=re.M), f
+            assert "libmoe" not in txt, f

@@ -1,0 +1,192 @@
+"""End-to-end GPU parity of moe_layer_forward against the CPU oracle.
+
+Reduced-T versions of every workload are checked token by token on a
+sample; the full-size workloads (the launch configuration the benchmark
+times) are checked on sampled tokens plus properties of the whole layout.
+Shards (expert ranges and H shards) are summed on the host and compared
+with the unsharded output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle
+from helpers import (cfg_for, check_layout_properties, oracle_out_tokens, oracle_route, rel_err,
+                     routing_agreement, to_f64, tol)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import routing_grouped_gemm_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def run_layer(moe, cfg, inp, w1=None, w3=None, w2=None):
+    ws = moe.alloc_workspace(cfg, layer=True)
+    out = torch.empty((cfg.T, cfg.D), dtype=cfg.torch_dtype, device="cuda")
+    moe.moe_layer_forward(cfg, inp.x, inp.wg, inp.bias, inp.w1 if w1 is None else w1,
+                          inp.w3 if w3 is None else w3, inp.w2 if w2 is None else w2, out, ws)
+    st = moe.moe_get_device_status(ws)
+    assert st == moe.MOE_OK, moe.status_string(st)
+    return out, moe.layer_views(cfg, ws), ws
+
+
+def check_against_oracle(moe, w, inp, out, views, n_sample, seed=0):
+    l64, keys, oidx, owts, st = oracle_route(inp, w, inp.bias)
+    gidx = views["topk_idx"].cpu().numpy()
+    gl_err = 1e-3  # generous key tolerance for near ties (logits are O(1))
+    same_set, _ = routing_agreement(gidx, oidx, keys, key_tol=gl_err)
+    assert same_set.mean() > 0.99
+    rng = np.random.default_rng(seed)
+    cand = np.nonzero(same_set)[0]
+    toks = np.sort(rng.choice(cand, size=min(n_sample, len(cand)), replace=False))
+    ref = oracle_out_tokens(inp, w, toks, oidx, owts)
+    got = to_f64(out)[toks]
+    err = rel_err(got, ref)
+    assert err < tol(w), f"{w.name}: max err / rms = {err:.3e}"
+    return err
+
+
+SMALL = [
+    ("tiny-fp32", dict(), 256),
+    ("fine-grained-bf16", dict(T=640), 96),
+    ("deepseek-v3-shaped", dict(T=300), 12),
+    ("zipf-skewed", dict(T=1500), 48),
+    ("decode-masked", dict(), 16),
+]
+
+
+@pytest.mark.parametrize("name,over,n_sample", SMALL)
+def test_layer_reduced_workloads(moe, name, over, n_sample):
+    w = moe_inputs.WORKLOADS[name].scaled(**over)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=1)
+    cfg = cfg_for(moe, w)
+    out, views, _ = run_layer(moe, cfg, inp)
+    check_against_oracle(moe, w, inp, out, views, n_sample)
+    # layout of the whole batch, by properties that fix it uniquely
+    idx = views["topk_idx"].cpu().numpy()
+    lay = (views["tokens_per_expert"].cpu().numpy(), views["seg_offsets"].cpu().numpy(),
+           views["row_of"].cpu().numpy(), views["token_of_row"].cpu().numpy())
+    if w.layout == "masked":
+        check_layout_properties(idx, lay, w.E, 0, w.E, masked_cap=cfg.capacity)
+    else:
+        check_layout_properties(idx, lay, w.E, 0, w.E, align_m=cfg.align_m)
+
+
+def test_tiny_fp32_whole_batch_and_tp2_shards(moe):
+    w = moe_inputs.WORKLOADS["tiny-fp32"]
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=0)
+    cfg = cfg_for(moe, w)
+    out, views, _ = run_layer(moe, cfg, inp)
+    l64, keys, oidx, owts, _ = oracle_route(inp, w)
+    assert np.array_equal(views["topk_idx"].cpu().numpy(), oidx)
+    ref = oracle_out_tokens(inp, w, np.arange(w.T), oidx, owts)
+    assert rel_err(to_f64(out), ref) < 1e-4
+    # H shards: w1/w3 split on dim 1, w2 on dim 2; partial outputs sum to the layer
+    Hl = w.H // w.tp
+    acc = np.zeros((w.T, w.D))
+    for r in range(w.tp):
+        sl = slice(r * Hl, (r + 1) * Hl)
+        c = cfg_for(moe, w, H_local=Hl)
+        part, _, _ = run_layer(moe, c, inp, inp.w1[:, sl].contiguous(), inp.w3[:, sl].contiguous(),
+                               inp.w2[:, :, sl].contiguous())
+        acc += to_f64(part)
+        pref = oracle_out_tokens(inp, w, np.arange(w.T), oidx, owts, h0=r * Hl, Hl=Hl)
+        assert rel_err(to_f64(part), pref) < 1e-4
+    assert rel_err(acc, ref) < 1e-4
+
+
+def test_decode_masked_expert_ranges_times_h_shards(moe):
+    """8 expert ranges x 4 H shards; the 32 partials sum to the whole layer."""
+    w = moe_inputs.WORKLOADS["decode-masked"]
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=2)
+    cfg = cfg_for(moe, w)
+    full, views, _ = run_layer(moe, cfg, inp)
+    El, Hl = w.E // w.ep, w.H // w.tp
+    acc = torch.zeros((w.T, w.D), dtype=torch.float64, device="cuda")
+    for er in range(w.ep):
+        es = slice(er * El, (er + 1) * El)
+        for r in range(w.tp):
+            hs = slice(r * Hl, (r + 1) * Hl)
+            c = cfg_for(moe, w, e_first=er * El, E_local=El, H_local=Hl)
+            part, pv, _ = run_layer(moe, c, inp, inp.w1[es, hs].contiguous(),
+                                    inp.w3[es, hs].contiguous(), inp.w2[es, :, hs].contiguous())
+            acc += part.double()
+            if er == 0 and r == 0:
+                # counts cover every expert; segments only the local range
+                assert int(pv["tokens_per_expert"].sum()) == w.T * w.k
+                assert pv["seg_offsets"].cpu().numpy().tolist() == [i * w.T for i in range(El + 1)]
+    accn = acc.cpu().numpy()
+    fulln = to_f64(full)
+    assert rel_err(accn, fulln) < 2e-2
+    l64, keys, oidx, owts, _ = oracle_route(inp, w)
+    toks = np.arange(0, w.T, 8)
+    assert np.array_equal(views["topk_idx"].cpu().numpy()[toks], oidx[toks])
+    ref = oracle_out_tokens(inp, w, toks, oidx, owts)
+    assert rel_err(accn[toks], ref) < 2e-2
+
+
+def test_layer_without_local_experts_gives_zeros(moe):
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=100, E=16, D=256, H=128)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=4)
+    cfg = cfg_for(moe, w, e_first=16, E_local=0)
+    e0 = inp.w1[:0]
+    out, views, _ = run_layer(moe, cfg, inp, e0, e0, inp.w2[:0])
+    assert (out.float() == 0).all()
+    assert int(views["tokens_per_expert"].sum()) == w.T * w.k
+
+
+def test_layer_single_token_and_k1(moe):
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=1, E=8, k=1, D=512, H=256)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=6)
+    out, views, _ = run_layer(moe, cfg_for(moe, w), inp)
+    check_against_oracle(moe, w, inp, out, views, 1)
+
+
+def test_layer_is_deterministic(moe):
+    w = moe_inputs.WORKLOADS["zipf-skewed"].scaled(T=3000)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=8)
+    cfg = cfg_for(moe, w)
+    a, _, _ = run_layer(moe, cfg, inp)
+    b, _, _ = run_layer(moe, cfg, inp)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ full sizes
+
+FULL = [
+    ("fine-grained-bf16", 48),
+    ("deepseek-v3-shaped", 4),
+    ("zipf-skewed", 24),
+    ("decode-masked", 16),
+]
+
+
+@pytest.mark.parametrize("name,n_sample", FULL)
+def test_layer_full_size_sampled(moe, name, n_sample):
+    w = moe_inputs.WORKLOADS[name]
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=0)
+    cfg = cfg_for(moe, w)
+    out, views, ws = run_layer(moe, cfg, inp)
+    check_against_oracle(moe, w, inp, out, views, n_sample, seed=1)
+    idx = views["topk_idx"].cpu().numpy()
+    cnt = views["tokens_per_expert"].cpu().numpy()
+    assert int(cnt.sum()) == w.T * w.k
+    lay = (cnt, views["seg_offsets"].cpu().numpy(), views["row_of"].cpu().numpy(),
+           views["token_of_row"].cpu().numpy())
+    if w.layout == "masked":
+        check_layout_properties(idx, lay, w.E, 0, w.E, masked_cap=cfg.capacity)
+    else:
+        check_layout_properties(idx, lay, w.E, 0, w.E, align_m=cfg.align_m)
+    # x_perm rows are the tokens' rows, bit for bit
+    row_of = views["row_of"]
+    sel = row_of[:, 0].long()
+    assert torch.equal(views["x_perm"][sel], inp.x)
+    if w.zipf_s:
+        assert (cnt == 0).sum() >= w.zipf_empty
+    del inp, out, views, ws
+    torch.cuda.empty_cache()

@@ -1,0 +1,336 @@
+"""GPU parity of each step of the path against the CPU oracle, via the C ABI.
+
+Integer work (routing indices, counts, offsets, permutation, x_perm bytes)
+is compared bit for bit; floats against the oracle with the tolerances of
+tests/helpers.py (max |gpu - oracle| / rms(oracle): 1e-4 fp32, 2e-2 bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle
+from helpers import check_layout_properties, rel_err, to_f64, within_bf16_rounding
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import routing_grouped_gemm_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+# ------------------------------------------------------------------ router
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("score,renorm", [("softmax", False), ("softmax", True), ("sigmoid", True),
+                                          ("sigmoid", False)])
+def test_route_exact_logits_bitexact(moe, dt, score, renorm):
+    """Integer-valued inputs make every logit exact in fp32, ties included."""
+    T, D, E, k = 300, 264, 72, 6
+    x, wg = moe_inputs.exact_router_inputs(T, D, E, seed=11)
+    bias = (np.arange(E) % 5 - 2).astype(np.float32) / 8.0
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k,
+                     dtype=moe.MOE_F32 if dt == "f32" else moe.MOE_BF16,
+                     score=moe.MOE_SCORE_SOFTMAX if score == "softmax" else moe.MOE_SCORE_SIGMOID,
+                     renorm=int(renorm))
+    ws = moe.alloc_workspace(cfg)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    gidx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(cfg, _dev(x, tdt), _dev(wg, tdt), _dev(bias), logits, gidx, gw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    ref = oracle.router_logits(x, wg, bias.astype(np.float64))
+    assert np.array_equal(logits.cpu().numpy(), ref.astype(np.float32))      # exact
+    keys = ref.astype(np.float32)
+    oidx, st = oracle.topk(keys, k)
+    assert st == oracle.OK
+    n_ties = sum(len(set(keys[t])) < E for t in range(T))
+    assert n_ties > T // 2                                   # the case exercises ties
+    assert np.array_equal(gidx.cpu().numpy(), oidx)
+    ow = oracle.topk_weights(keys, oidx, oracle.SOFTMAX if score == "softmax" else oracle.SIGMOID,
+                             renorm)
+    np.testing.assert_allclose(gw.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", moe_inputs.WORKLOAD_ORDER)
+def test_route_workload_shapes(moe, name):
+    """Config-shaped random inputs: logits within tolerance, selection valid."""
+    w = moe_inputs.WORKLOADS[name].scaled(T=min(moe_inputs.WORKLOADS[name].T, 1024))
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=5, weights=False)
+    from helpers import cfg_for, oracle_route, routing_agreement
+    cfg = cfg_for(moe, w)
+    ws = moe.alloc_workspace(cfg)
+    logits = torch.empty((w.T, w.E), dtype=torch.float32, device="cuda")
+    gidx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gw = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(cfg, inp.x, inp.wg, inp.bias, logits, gidx, gw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    l64, keys, oidx, ow, st = oracle_route(inp, w, inp.bias)
+    gl = logits.cpu().numpy()
+    lerr = np.abs(gl - l64).max()
+    assert lerr < 1e-4 * max(1.0, np.abs(l64).max())
+    g = gidx.cpu().numpy()
+    same_set, same_order = routing_agreement(g, oidx, keys, key_tol=4 * lerr + 1e-6)
+    assert same_order.mean() > 0.99
+    # the GPU's choice is exact for its own logits: sorted by (key desc, index asc)
+    for t in range(w.T):
+        order = sorted(range(w.E), key=lambda e: (-gl[t, e], e))[:w.k]
+        assert list(g[t]) == order
+    np.testing.assert_allclose(gw.cpu().numpy()[same_order], ow[same_order], rtol=1e-4, atol=1e-6)
+
+
+def test_route_nan_logit_sets_status(moe):
+    T, D, E, k = 64, 64, 16, 4
+    x = torch.randn(T, D, device="cuda")
+    x[7, 3] = float("nan")
+    wg = torch.randn(E, D, device="cuda")
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_F32)
+    ws = moe.alloc_workspace(cfg)
+    gidx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(cfg, x, wg, None, None, gidx, gw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK          # read clears
+    g = gidx.cpu().numpy()
+    assert ((g >= 0) & (g < E)).all()
+    assert all(len(set(r)) == k for r in g)
+
+
+# ------------------------------------------------------------------ permute
+
+def _run_permute(moe, cfg, x, idx):
+    ra = moe.rows_alloc(cfg)
+    el = cfg.e_local
+    ws = moe.alloc_workspace(cfg)
+    tpe = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    seg = torch.empty(el + 1, dtype=torch.int32, device="cuda")
+    row_of = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+    tor = torch.full((ra,), 7777, dtype=torch.int32, device="cuda")
+    xp = torch.zeros((ra, cfg.D), dtype=x.dtype, device="cuda")
+    moe.moe_permute(cfg, x, _dev(idx), tpe, seg, row_of, tor, xp, ws)
+    st = moe.moe_get_device_status(ws)
+    return st, tpe.cpu().numpy(), seg.cpu().numpy(), row_of.cpu().numpy(), tor.cpu().numpy(), xp
+
+
+@pytest.mark.parametrize("T,E,k,align,e_first,E_local,skew", [
+    (1000, 16, 4, 128, 0, 16, 1.3),      # ragged tail block, empty experts
+    (257, 64, 6, 128, 0, 64, 0.0),
+    (31, 8, 2, 1, 0, 8, 0.0),            # fewer tokens than a warp, no padding
+    (2000, 32, 8, 8, 8, 12, 0.8),        # expert range, small alignment
+    (513, 256, 8, 128, 0, 256, 0.3),
+    (700, 5, 1, 16, 2, 2, 0.0),          # k = 1
+])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_permute_bitexact(moe, T, E, k, align, e_first, E_local, skew, dt):
+    D = 136
+    idx = moe_inputs.random_topk_idx(T, E, k, seed=T + E, skew=skew)
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, e_first=e_first, E_local=E_local,
+                     dtype=moe.MOE_BF16 if dt == torch.bfloat16 else moe.MOE_F32, align_m=align)
+    x = torch.randn(T, D, device="cuda").to(dt)
+    st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
+    assert st == moe.MOE_OK
+    lay = oracle.layout(idx, E, e_first, E_local, oracle.CONTIGUOUS, align)
+    assert lay["status"] == oracle.OK
+    assert np.array_equal(tpe, lay["tokens_per_expert"])
+    assert np.array_equal(seg, lay["seg_offsets"])
+    assert np.array_equal(row_of, lay["row_of"])
+    assert np.array_equal(tor, lay["token_of_row"])
+    filled = lay["token_of_row"] >= 0
+    xh = moe_inputs.host_array(x)
+    ref = oracle.permute_rows(xh, lay["token_of_row"])
+    assert np.array_equal(moe_inputs.host_array(xp)[filled], ref[filled])   # bit for bit
+
+
+def test_permute_masked_and_capacity(moe):
+    T, E, k, D = 400, 12, 3, 64
+    idx = moe_inputs.random_topk_idx(T, E, k, seed=3, skew=1.0)
+    cnt = np.bincount(idx.ravel(), minlength=E)
+    cap = int(cnt.max())
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
+                     layout=moe.MOE_LAYOUT_MASKED, capacity=cap)
+    x = torch.randn(T, D, device="cuda").to(torch.bfloat16)
+    st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
+    assert st == moe.MOE_OK
+    lay = oracle.layout(idx, E, 0, E, oracle.MASKED, 1, cap)
+    for a, b in ((tpe, "tokens_per_expert"), (seg, "seg_offsets"), (row_of, "row_of"),
+                 (tor, "token_of_row")):
+        assert np.array_equal(a, lay[b])
+    check_layout_properties(idx, (tpe, seg, row_of, tor), E, 0, E, masked_cap=cap)
+    # capacity exceeded: first `cap2` tokens kept per expert, the rest dropped and flagged
+    cap2 = int(np.median(cnt))
+    cfg2 = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
+                      layout=moe.MOE_LAYOUT_MASKED, capacity=cap2)
+    st2, tpe2, seg2, row2, tor2, _ = _run_permute(moe, cfg2, x, idx)
+    assert st2 == moe.MOE_ERR_CAPACITY
+    assert np.array_equal(tpe2, cnt)
+    for e in range(E):
+        toks = np.nonzero((idx == e).any(1))[0]
+        kept = toks[:cap2]
+        assert np.array_equal(tor2[e * cap2:e * cap2 + len(kept)], kept)
+        for t in toks[cap2:]:
+            j = int(np.nonzero(idx[t] == e)[0][0])
+            assert row2[t, j] == -1
+
+
+def test_permute_bad_ids_flagged_and_skipped(moe):
+    T, E, k, D = 100, 8, 2, 32
+    idx = moe_inputs.random_topk_idx(T, E, k, seed=9)
+    idx[5, 1] = E          # out of range
+    idx[9, 0] = -3         # negative
+    idx[11, 1] = idx[11, 0]  # duplicate expert within a token
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_F32, align_m=4)
+    x = torch.randn(T, D, device="cuda")
+    st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
+    assert st == moe.MOE_ERR_BAD_ROUTING
+    assert row_of[5, 1] == -1 and row_of[9, 0] == -1 and row_of[11, 1] == -1
+    assert tpe.sum() == T * k - 3
+    good = row_of >= 0
+    tt = np.broadcast_to(np.arange(T)[:, None], idx.shape)
+    assert np.array_equal(tor[row_of[good]], tt[good])
+
+
+def test_permute_empty_batch(moe):
+    cfg = moe.Config(T=0, D=64, H_local=8, E=8, k=2, dtype=moe.MOE_BF16)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, np.zeros((0, 2), np.int32))
+    assert st == moe.MOE_OK
+    assert (tpe == 0).all() and (seg == 0).all()
+    assert (tor == -1).all()
+
+
+# ------------------------------------------------------------------ grouped GEMMs
+
+def _grouped_case(moe, dt, T, E_local, k, D, H, align, seed, skew=1.0):
+    idx = moe_inputs.random_topk_idx(T, E_local, k, seed=seed, skew=skew)
+    lay = oracle.layout(idx, E_local, 0, E_local, oracle.CONTIGUOUS, align)
+    ra = lay["rows_alloc"]
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    xp = torch.randn((ra, D), generator=g, device="cuda").to(tdt)
+    w1 = (torch.randn((E_local, H, D), generator=g, device="cuda") * 0.05).to(tdt)
+    w3 = (torch.randn((E_local, H, D), generator=g, device="cuda") * 0.05).to(tdt)
+    w2 = (torch.randn((E_local, D, H), generator=g, device="cuda") * 0.05).to(tdt)
+    cfg = moe.Config(T=T, D=D, H_local=H, E=E_local, k=k, align_m=align,
+                     dtype=moe.MOE_BF16 if dt == "bf16" else moe.MOE_F32)
+    assert moe.rows_alloc(cfg) == ra
+    ws = moe.alloc_workspace(cfg)
+    h = torch.full((ra, H), float("nan"), device="cuda").to(tdt)
+    y = torch.full((ra, D), float("nan"), device="cuda")          # fp32 accumulator
+    moe.moe_grouped_swiglu(cfg, xp, _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"]),
+                           w1, w3, w2, h, y, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    return lay, xp, w1, w3, w2, h, y
+
+
+@pytest.mark.parametrize("dt,T,E_local,k,D,H,align", [
+    ("bf16", 700, 6, 2, 640, 200, 128),   # N tails (640 = 2.5 x 256, 200 = 1.56 x 128), K tail
+    ("bf16", 1500, 9, 3, 512, 384, 128),  # several m-tiles per expert, empty experts
+    ("bf16", 333, 5, 2, 256, 128, 1),     # unpadded segments: tiles start mid-buffer
+    ("bf16", 900, 4, 1, 1024, 256, 64),   # k = 1, segments aligned to half a tile
+    ("f32", 600, 6, 2, 128, 256, 128),
+    ("f32", 301, 7, 3, 136, 72, 8),
+])
+def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align):
+    lay, xp, w1, w3, w2, h, y = _grouped_case(moe, dt, T, E_local, k, D, H, align, seed=T + H)
+    H_ = moe_inputs.host_array
+    seg, cnt = lay["seg_offsets"], lay["tokens_per_expert"]
+    rb = dt == "bf16"
+    oh = oracle.grouped_gemm1_swiglu(H_(xp), seg, cnt, list(H_(w1)), list(H_(w3)), round_h=rb)
+    filled = lay["token_of_row"] >= 0
+    gh = to_f64(h)
+    # second GEMM from the oracle's own h (no GPU value feeds the oracle)
+    ohb = oh.astype(np.float32)
+    oy = oracle.grouped_gemm2(ohb, seg, cnt, list(H_(w2)))
+    gy = to_f64(y)
+    if rb:
+        # h is a bf16 intermediate rounded once on each side: compared per element
+        assert within_bf16_rounding(gh[filled], oh[filled]) <= 1.0
+        # y (fp32) differs by what those h differences carry through w2, plus
+        # fp32 accumulation error: |dy| <= |dh| |w2|^T + 2^-20 |h| |w2|^T
+        w2h = to_f64(w2)
+        dh = np.abs(np.nan_to_num(gh) - np.nan_to_num(oh))
+        for i in range(E_local):
+            rows = np.arange(seg[i], seg[i] + cnt[i])
+            if len(rows) == 0:
+                continue
+            aw2 = np.abs(w2h[i])
+            bound = dh[rows] @ aw2.T + 2.0 ** -20 * (np.abs(oh[rows]) @ aw2.T) + 1e-30
+            assert (np.abs(gy[rows] - oy[rows]) <= bound).all()
+        assert rel_err(gy[filled], oy[filled]) < 1e-2
+    else:
+        assert rel_err(gh[filled], oh[filled]) < 1e-4
+        assert rel_err(gy[filled], oy[filled]) < 1e-4
+    # rows that hold no token were never written
+    if (~filled).any():
+        assert torch.isnan(h.float()[torch.from_numpy(~filled).cuda()]).all()
+
+
+def test_grouped_swiglu_bad_offsets_flagged(moe):
+    E_local, D, H = 3, 128, 128
+    cfg = moe.Config(T=64, D=D, H_local=H, E=E_local, k=1, dtype=moe.MOE_BF16)
+    ra = moe.rows_alloc(cfg)
+    ws = moe.alloc_workspace(cfg)
+    seg = _dev(np.array([0, 128, 64, ra + 500], np.int32))     # decreasing, then out of range
+    cnt = _dev(np.array([10, 10, 10], np.int32))
+    xp = torch.zeros((ra, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((E_local, H, D), dtype=torch.bfloat16, device="cuda")
+    w2 = torch.zeros((E_local, D, H), dtype=torch.bfloat16, device="cuda")
+    h = torch.zeros((ra, H), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((ra, D), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_swiglu(cfg, xp, seg, cnt, w, w, w2, h, y, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
+
+
+# ------------------------------------------------------------------ combine
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("T,E,k,D,e_first,E_local", [(513, 16, 4, 264, 0, 16), (200, 64, 8, 2048, 16, 32),
+                                                     (77, 4, 1, 8, 0, 4)])
+def test_combine_parity(moe, dt, T, E, k, D, e_first, E_local):
+    idx = moe_inputs.random_topk_idx(T, E, k, seed=T)
+    lay = oracle.layout(idx, E, e_first, E_local, oracle.CONTIGUOUS, 128)
+    ra = lay["rows_alloc"]
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    y = torch.randn((ra, D), device="cuda")                       # fp32 accumulator
+    w = moe_inputs.random_weights(T, k, seed=T)
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, e_first=e_first, E_local=E_local,
+                     dtype=moe.MOE_BF16 if dt == "bf16" else moe.MOE_F32)
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty((T, D), dtype=tdt, device="cuda")
+    moe.moe_unpermute_combine(cfg, y, _dev(lay["row_of"]), _dev(w), out, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    yh = moe_inputs.host_array(y)
+    ref = oracle.unpermute_combine(yh, lay["row_of"], w.astype(np.float64))
+    # bound: fp32 accumulation error (k terms) plus one final rounding (one ulp)
+    yabs = np.abs(to_f64(y))
+    mag = oracle.unpermute_combine(yabs, lay["row_of"], np.abs(w).astype(np.float64))
+    got = to_f64(out)
+    ulp = 2.0 ** -7 if dt == "bf16" else 2.0 ** -23
+    assert (np.abs(got - ref) <= ulp * np.abs(ref) + 2 * k * 2.0 ** -24 * mag).all()
+    none_local = (lay["row_of"] < 0).all(1)
+    assert (got[none_local] == 0).all()
+
+
+def test_permute_then_combine_is_identity(moe):
+    T, E, D = 999, 24, 520
+    idx = moe_inputs.random_topk_idx(T, E, 1, seed=1)
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=1, dtype=moe.MOE_BF16)
+    x = torch.randn(T, D, device="cuda").to(torch.bfloat16)
+    st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
+    assert st == moe.MOE_OK
+    out = torch.empty_like(x)
+    ws = moe.alloc_workspace(cfg)
+    moe.moe_unpermute_combine(cfg, xp.float(), _dev(row_of), torch.ones((T, 1), device="cuda"), out,
+                              ws)
+    assert torch.equal(out, x)
