@@ -52,7 +52,8 @@ def algorithmic(w):
     return dict(
         ffn_flops=6.0 * R * w.D * w.H,
         permute_bytes=float(w.T * w.D * b + R * w.D * b),
-        combine_bytes=float(R * w.D * b + w.T * w.D * b + R * 8),
+        # y_perm is the fp32 accumulator of the second GEMM
+        combine_bytes=float(R * w.D * 4 + w.T * w.D * b + R * 8),
     )
 
 
@@ -219,6 +220,48 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
+    """moe_layer_forward through host buffers: pinned x in, out back, every step."""
+    import torch
+    import torch.distributed as dist
+    w = inp.w
+    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
+    x_host = inp.x.cpu().pin_memory()
+    out_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(cfg, x_dev, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, lws, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(10, args.steps // 4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st = moe.moe_get_device_status(lws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after e2e: {moe.status_string(st)}")
+    return {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": int(x_host.numel() * 2),
+            "d2h_bytes_per_step": int(out_host.numel() * 2),
+            "api": "moe_layer_forward, pinned host x in / out each step"}
+
+
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -305,36 +348,9 @@ def run_gpu(args):
     value = world * w.T / (ms_per_step * 1e-3)
 
     # end to end: moe_layer_forward with pinned host input / output each step
-    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
-    x_host = inp.x.cpu().pin_memory()
-    out_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(inp.x)
-
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(cfg, x_dev, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, lws, stream)
-        out_host.copy_(out, non_blocking=True)
-
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e_steps = max(10, args.steps // 4)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    st = moe.moe_get_device_status(lws, stream)
-    if st != moe.MOE_OK:
-        raise RuntimeError(f"device status after e2e: {moe.status_string(st)}")
-
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(moe, cfg, inp, out, stream, dev, world, args)
     alg = algorithmic(w)
     peaks = load_peaks()
     gemm_ms = float(mean_parts[2])
@@ -365,10 +381,7 @@ def run_gpu(args):
         "gemm_tflops": achieved,
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
                               "zeros": int((tpe_h == 0).sum())},
-        "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": int(x_host.numel() * 2),
-                "d2h_bytes_per_step": int(out_host.numel() * 2),
-                "api": "moe_layer_forward, pinned host x in / out each step"},
+        "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
     }
@@ -396,6 +409,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
