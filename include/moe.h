@@ -209,6 +209,36 @@ moe_status moe_layer_forward(const moe_config *cfg, const void *x, const void *w
                              moe_stream_t stream);
 
 /*
+ * moe_permute without a workspace (this entry point has no counterpart in
+ * the pages; it exists for callers that cannot allocate device memory).
+ *
+ * Some callers cannot call cudaMalloc where they dispatch: code running in a
+ * memory pool it does not own, plugins handed only their input and output
+ * tensors, or latency-critical loops where an allocation's implicit device
+ * synchronisation is not acceptable.  This call does the same work as
+ * moe_permute (same arguments and outputs, same bit-exact results) but keeps
+ * its scratch in a fixed 1 MiB device array inside the library, which every
+ * GPU that loads the library holds until the process exits.  It allocates
+ * nothing.
+ *   Limit: 2 * ceil(T / 256) * E <= 262144 (e.g. T = 16384 with E <= 2048);
+ *     larger problems return MOE_ERR_UNSUPPORTED before any launch.
+ *   device_flags: device int32 that the kernels OR their MOE status flags
+ *     into (bad expert id: 1, capacity exceeded: 2), or NULL to drop them.
+ *     The caller zeroes it; moe_get_device_status does not see these flags.
+ *   The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   Every call shares the one array and leaves its contents behind; nothing
+ *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race on it: order them on one
+ *     stream.
+ */
+moe_status moe_permute_noalloc(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                               int32_t *tokens_per_expert, int32_t *seg_offsets,
+                               int32_t *row_of, int32_t *token_of_row, void *x_perm,
+                               int32_t *device_flags, moe_stream_t stream);
+
+/*
  * Synchronises `stream`, reads the workspace status word, clears it and
  * returns the most serious flagged condition (MOE_OK if none).  Order:
  * TIMEOUT, CAPACITY, BAD_ROUTING.

@@ -30,7 +30,7 @@ ABI_SYMBOLS = (
     "moe_status_string", "moe_last_error_string", "moe_abi_version", "moe_validate_config",
     "moe_rows_alloc", "moe_workspace_size", "moe_layer_workspace_size", "moe_route_topk",
     "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine", "moe_layer_forward",
-    "moe_get_device_status",
+    "moe_get_device_status", "moe_permute_noalloc",
 )
 
 
@@ -68,6 +68,7 @@ def _load() -> ctypes.CDLL:
         "moe_unpermute_combine": (I32, [C, P, P, P, P, P, SZ, P]),
         "moe_layer_forward": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_get_device_status": (I32, [P, SZ, P]),
+        "moe_permute_noalloc": (I32, [C, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -220,6 +221,32 @@ def moe_permute(cfg: Config, x, topk_idx, tokens_per_expert, seg_offsets, row_of
     _check(_lib.moe_permute(ctypes.byref(c), _ptr(x), _ptr(topk_idx), _ptr(tokens_per_expert),
                             _ptr(seg_offsets), _ptr(row_of), _ptr(token_of_row), _ptr(x_perm),
                             _ptr(ws), ws.numel(), _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg: Config, x, topk_idx, tokens_per_expert, seg_offsets, row_of,
+                        token_of_row, x_perm, device_flags=None, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace argument.
+
+    The library keeps the counting-sort scratch in a fixed device array of
+    its own (limit 2 * ceil(T/256) * E <= 262144 int32), shared by every
+    call -- calls must not overlap on the GPU.  ``device_flags`` is an
+    optional int32 CUDA tensor of one element that receives the status flags.
+    """
+    ra = rows_alloc(cfg)
+    _expect(x, (cfg.T, cfg.D), cfg.torch_dtype, "x")
+    _expect(topk_idx, (cfg.T, cfg.k), torch.int32, "topk_idx")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(seg_offsets, (cfg.e_local + 1,), torch.int32, "seg_offsets")
+    _expect(row_of, (cfg.T, cfg.k), torch.int32, "row_of")
+    _expect(token_of_row, (ra,), torch.int32, "token_of_row")
+    _expect(x_perm, (ra, cfg.D), cfg.torch_dtype, "x_perm")
+    if device_flags is not None:
+        _expect(device_flags, (1,), torch.int32, "device_flags")
+    c = cfg.c()
+    _check(_lib.moe_permute_noalloc(ctypes.byref(c), _ptr(x), _ptr(topk_idx),
+                                    _ptr(tokens_per_expert), _ptr(seg_offsets), _ptr(row_of),
+                                    _ptr(token_of_row), _ptr(x_perm), _ptr(device_flags),
+                                    _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_grouped_swiglu(cfg: Config, x_perm, seg_offsets, tokens_per_expert, w1, w3, w2, h, y_perm,

@@ -8,6 +8,9 @@
 
 namespace moe {
 
+// Sets the text returned by moe_last_error_string() for the calling thread.
+void set_last_error(const char *msg);
+
 cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
                                int *topk_idx, float *topk_w, int T, int D, int E, int k,
                                int score, int renorm, int is_bf16, int *status,

@@ -172,6 +172,10 @@ moe_status do_combine(const moe_config *c, const void *y_perm, const int32_t *ro
 
 }  // namespace
 
+namespace moe {
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace moe
+
 // ---------------------------------------------------------------------
 // exported ABI
 // ---------------------------------------------------------------------

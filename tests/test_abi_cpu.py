@@ -123,3 +123,16 @@ def test_product_does_not_import_oracle():
             assert not re.search(r"^\s*(import|from)\s+(routing_grouped_gemm_gb300|moe_inputs)", txt,
                                  flags=re.M), f
             assert "libmoe" not in txt, f
+
+
+def test_permute_noalloc_rejects_problems_beyond_its_scratch_on_the_host(moe):
+    """The size check of moe_permute_noalloc runs before any CUDA call."""
+    lib = moe._lib
+    # 2 * ceil(T/256) * E = 2 * 1024 * 256 = 524288 int32 > the 262144 of its fixed scratch
+    c = _cfg(moe, T=262144, E=256, k=8).c()
+    st = lib.moe_permute_noalloc(ctypes.byref(c), 256, 256, 256, 256, 256, 256, 256, None, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+    assert "fixed scratch" in moe.last_error_string()
+    bad = _cfg(moe, k=0).c()
+    assert lib.moe_permute_noalloc(ctypes.byref(bad), 0, 0, 0, 0, 0, 0, 0, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
