@@ -294,7 +294,8 @@ def run_gpu(args):
     y_perm = torch.empty((ra, w.D), dtype=torch.float32, device=dev)
     out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    LAUNCHES_PER_STEP = 8  # router, count, scan, index, copy, GEMM1, GEMM2, combine
+    # router logits (tensor cores) + reduce/top-k, count, scan, index, copy, GEMM1, GEMM2, combine
+    LAUNCHES_PER_STEP = 9
 
     def step(ev=None):
         if ev is not None:

@@ -3,6 +3,7 @@
 // C ABI layer before any of these is called.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -11,10 +12,23 @@ namespace moe {
 // Sets the text returned by moe_last_error_string() for the calling thread.
 void set_last_error(const char *msg);
 
+// TMA tensor maps over bf16 row-major data, 128-byte swizzle, boxes of 64
+// columns x box_rows rows (x 1 expert for the 3-D form [experts, rows, cols]).
+bool make_tmap_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows);
+bool make_tmap_3d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t experts,
+                  uint32_t box_rows);
+int sm_count();  // SMs of the current device (0 on error)
+
+// Router.  bf16 with E <= kRouterTcMaxE runs on the tensor cores and needs
+// router_scratch_floats(T, E, 1) floats of scratch for the split partials;
+// everything else (or a missing scratch) runs the fused SIMT kernel.
+constexpr int kRouterTcMaxE = 256;
+constexpr int kRouterMaxSplits = 8;
+int64_t router_scratch_floats(int T, int E, int is_bf16);
 cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
                                int *topk_idx, float *topk_w, int T, int D, int E, int k,
-                               int score, int renorm, int is_bf16, int *status,
-                               cudaStream_t stream);
+                               int score, int renorm, int is_bf16, float *scratch,
+                               int64_t scratch_floats, int *status, cudaStream_t stream);
 
 // Scratch ints needed by launch_permute: blocks of 256 tokens x E, twice.
 int64_t permute_scratch_ints(int T, int E);

@@ -67,19 +67,35 @@ moe_status validate(const moe_config *c) {
 
 struct StepWs {
     moe::StatusBlock *status;
-    int *scratch;
+    int *scratch;           // permute counting-sort scratch
+    float *router_part;     // router split partials (bf16 tensor-core path)
+    int64_t router_floats;
 };
 
+int64_t permute_ws_bytes(const moe_config *c) {
+    return align_up(4 * moe::permute_scratch_ints(c->T, c->E));
+}
+
+int64_t router_ws_bytes(const moe_config *c) {
+    return align_up(4 * moe::router_scratch_floats(c->T, c->E, c->dtype == MOE_BF16));
+}
+
 int64_t step_ws_bytes(const moe_config *c) {
-    return (int64_t)sizeof(moe::StatusBlock) + align_up(4 * moe::permute_scratch_ints(c->T, c->E));
+    return (int64_t)sizeof(moe::StatusBlock) + permute_ws_bytes(c) + router_ws_bytes(c);
 }
 
 moe_status carve_step(const moe_config *c, void *ws, size_t ws_bytes, StepWs *out) {
     if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
     if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
     if ((int64_t)ws_bytes < step_ws_bytes(c)) return arg_fail("workspace too small", MOE_ERR_WORKSPACE);
-    out->status = static_cast<moe::StatusBlock *>(ws);
-    out->scratch = reinterpret_cast<int *>(static_cast<char *>(ws) + sizeof(moe::StatusBlock));
+    char *base = static_cast<char *>(ws);
+    out->status = reinterpret_cast<moe::StatusBlock *>(base);
+    out->scratch = reinterpret_cast<int *>(base + sizeof(moe::StatusBlock));
+    out->router_floats = moe::router_scratch_floats(c->T, c->E, c->dtype == MOE_BF16);
+    out->router_part = out->router_floats
+                           ? reinterpret_cast<float *>(base + sizeof(moe::StatusBlock) +
+                                                       permute_ws_bytes(c))
+                           : nullptr;
     return MOE_OK;
 }
 
@@ -133,7 +149,7 @@ moe_status do_route(const moe_config *c, const void *x, const void *wg, const fl
                     cudaStream_t s) {
     cudaError_t e = moe::launch_router_topk(x, wg, bias, logits_out, topk_idx, topk_w, c->T, c->D,
                                             c->E, c->k, c->score, c->renorm, c->dtype == MOE_BF16,
-                                            &w.status->flags, s);
+                                            w.router_part, w.router_floats, &w.status->flags, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_topk");
 }
 
@@ -221,7 +237,7 @@ MOE_EXPORT moe_status moe_route_topk(const moe_config *cfg, const void *x, const
     if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
     if (cfg->T == 0) return MOE_OK;
     if (!x || !wg || !topk_idx || !topk_w) return arg_fail("moe_route_topk: NULL tensor");
-    const uintptr_t a = (uintptr_t)elem_bytes(cfg);
+    const uintptr_t a = cfg->dtype == MOE_BF16 ? 16 : (uintptr_t)elem_bytes(cfg);
     if (!aligned(x, a) || !aligned(wg, a) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
         (bias && !aligned(bias, 4)) || (logits_out && !aligned(logits_out, 4)))
         return arg_fail("moe_route_topk: misaligned tensor");

@@ -14,8 +14,8 @@
 // is bit-identical run to run:
 //   count : per block of 256 tokens, per warp of 32 tokens, a bitmask per
 //           expert of which lanes route to it; block counts per expert
-//   scan  : one CTA; per-expert exclusive scan over blocks, tokens_per_expert,
-//           padded segment offsets, padding rows of token_of_row
+//   scan  : one CTA; tokens_per_expert, padded segment offsets, each block's
+//           first row per local expert, padding rows of token_of_row
 //   index : recomputes the masks; rank of (t, e) = rows of e in earlier
 //           blocks + earlier warps + popc(mask & lanes below)
 //   copy  : one warp per token reads x[t] once and writes its k copies
@@ -72,6 +72,21 @@ permute_count_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int 
 
 constexpr int SCAN_THREADS = 1024;
 
+// Sum of one expert's counts over the blocks; loads are issued 8 at a time
+// so the chain of L2 round trips is nblk / 8 long, not nblk.
+__device__ __forceinline__ int sum_blocks(const int *__restrict__ blk_cnt, int nblk, int E, int e) {
+    int run = 0, b = 0;
+    for (; b + 8 <= nblk; b += 8) {
+        int c[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) c[u] = blk_cnt[(size_t)(b + u) * E + e];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) run += c[u];
+    }
+    for (; b < nblk; ++b) run += blk_cnt[(size_t)b * E + e];
+    return run;
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS)
 permute_scan_kernel(const int *__restrict__ blk_cnt, int nblk, int E, int e_first, int E_local,
                     int layout, int align_m, int capacity, long long rows_alloc,
@@ -83,21 +98,16 @@ permute_scan_kernel(const int *__restrict__ blk_cnt, int nblk, int E, int e_firs
     const int tid = threadIdx.x;
 
     for (int e = tid; e < E; e += SCAN_THREADS) {
-        int run = 0;
-        for (int b = 0; b < nblk; ++b) {
-            const int c = blk_cnt[(size_t)b * E + e];
-            blk_base[(size_t)b * E + e] = run;
-            run += c;
-        }
-        tokens_per_expert[e] = run;
-        s_cnt[e] = run;
+        const int total = sum_blocks(blk_cnt, nblk, E, e);
+        tokens_per_expert[e] = total;
+        s_cnt[e] = total;
     }
     __syncthreads();
 
     // padded segment sizes -> inclusive scan (E_local <= 1024, one per thread)
-    int size = 0;
     if (tid < E_local) {
         const int c = s_cnt[e_first + tid];
+        int size;
         if (layout == 1) {
             size = capacity;
             if (c > capacity) raise_flag(status, FLAG_CAPACITY);
@@ -117,11 +127,25 @@ permute_scan_kernel(const int *__restrict__ blk_cnt, int nblk, int E, int e_firs
     }
     for (int i = tid; i <= E_local; i += SCAN_THREADS) seg_offsets[i] = s_off[i];
 
-    // local experts: block bases become absolute rows; padding rows -> -1
+    // local experts: absolute first row of each block's run; padding rows -> -1
     for (int i = tid; i < E_local; i += SCAN_THREADS) {
         const int e = e_first + i;
         const int base = s_off[i];
-        for (int b = 0; b < nblk; ++b) blk_base[(size_t)b * E + e] += base;
+        int run = base, b = 0;
+        for (; b + 8 <= nblk; b += 8) {
+            int c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk_cnt[(size_t)(b + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                blk_base[(size_t)(b + u) * E + e] = run;
+                run += c[u];
+            }
+        }
+        for (; b < nblk; ++b) {
+            blk_base[(size_t)b * E + e] = run;
+            run += blk_cnt[(size_t)b * E + e];
+        }
         const int used = min(s_cnt[e], s_off[i + 1] - base);
         for (int r = base + used; r < s_off[i + 1]; ++r) token_of_row[r] = -1;
     }

@@ -1,11 +1,23 @@
-// Router: gating logits, top-k selection and routing weights, fused.
+// Router: gating logits, top-k selection and routing weights.
 //
 // Page "Expert Parallelism (EP)" (llm-infra-atlas), section 1: the router
 // computes logits = x . W_g^T ([T, E]) and then "top-k + score_func" gives
-// the routing probabilities and the routing map.  One CTA owns 32 tokens:
-// it accumulates their logits for all E experts in fp32 (SIMT FFMA over
-// shared-memory tiles), keeps them in shared memory, and one warp per token
-// then selects the top-k by warp-wide arg-max rounds and computes weights.
+// the routing probabilities and the routing map.
+//
+// Two implementations of the same contract:
+//   * bf16 with E <= 256: the logits are a dense contraction, so they run on
+//     the tensor cores (tcgen05, TMA-fed, fp32 accumulation in TMEM), split
+//     along D so that every SM takes part; a second kernel adds the fp32
+//     partials in a fixed split order (deterministic), adds the bias and
+//     selects the top-k with one warp per token;
+//   * otherwise (fp32, where TF32 would miss the 1e-4 accuracy, or E > 256):
+//     one fused SIMT kernel -- a CTA accumulates 32 tokens' logits for all E
+//     in fp32 FFMA, keeps them in shared memory, and one warp per token
+//     selects the top-k.
+#include <cuda.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -23,6 +35,63 @@ template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
     return __bfloat162float(v);
+}
+
+// Top-k of one token's E keys (in shared memory) by one warp: k rounds of a
+// warp-wide arg-max in the selection order of key_before (larger key first,
+// equal keys by lower expert index, NaN last), then the routing weights:
+// softmax over all E (or sigmoid) of the chosen keys, divided by their sum
+// when renormalising.  Lane i owns experts i, i+32, ... (E <= 1024).
+__device__ void warp_topk_weights(const float *l, int E, int k, int score, int renorm, int t,
+                                  int *__restrict__ topk_idx, float *__restrict__ topk_w,
+                                  int *status, int lane) {
+    bool any_nan = false;
+    for (int e = lane; e < E; e += 32) any_nan |= (l[e] != l[e]);
+    if (__any_sync(0xffffffffu, any_nan) && lane == 0) raise_flag(status, FLAG_BAD_ROUTING);
+
+    uint32_t taken = 0;  // bit q: expert lane + 32 q already chosen
+    int sel_e[32];
+    float sel_v[32];
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.f;
+        int be = -1;
+        for (int q = 0, e = lane; e < E; ++q, e += 32) {
+            if (taken & (1u << q)) continue;
+            if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (oe >= 0 && (be < 0 || key_before(ov, oe, bv, be))) { bv = ov; be = oe; }
+        }
+        if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
+        sel_e[j] = be;
+        sel_v[j] = bv;
+    }
+
+    const float m = sel_v[0];  // the largest key (unless NaN)
+    float denom = 1.f;
+    if (score == 0 && !renorm) {
+        float sum = 0.f;
+        for (int e = lane; e < E; e += 32) sum += expf(l[e] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        denom = sum;
+    }
+    if (lane == 0) {
+        float p[32];
+        float psum = 0.f;
+        for (int j = 0; j < k; ++j) {
+            p[j] = (score == 0) ? expf(sel_v[j] - m) : 1.f / (1.f + expf(-sel_v[j]));
+            psum += p[j];
+        }
+        const float div = renorm ? psum : (score == 0 ? denom : 1.f);
+        for (int j = 0; j < k; ++j) {
+            topk_idx[(size_t)t * k + j] = sel_e[j];
+            topk_w[(size_t)t * k + j] = p[j] / div;
+        }
+    }
 }
 
 template <typename T>
@@ -98,66 +167,227 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
     for (int tt = warp; tt < RT_TOKENS; tt += RT_THREADS / 32) {
         const int t = t0 + tt;
         if (t >= Tn) break;
-        const float *l = s_logit + tt * E;
-        bool any_nan = false;
-        for (int e = lane; e < E; e += 32) any_nan |= (l[e] != l[e]);
-        if (__any_sync(0xffffffffu, any_nan) && lane == 0) raise_flag(status, FLAG_BAD_ROUTING);
+        warp_topk_weights(s_logit + tt * E, E, k, score, renorm, t, topk_idx, topk_w, status, lane);
+    }
+}
 
-        // experts already chosen by this lane: bit q stands for expert lane + 32 q
-        uint32_t taken = 0;
-        int sel_e[32];
-        float sel_v[32];
-        for (int j = 0; j < k; ++j) {
-            float bv = 0.f;
-            int be = -1;
-            for (int q = 0, e = lane; e < E; ++q, e += 32) {
-                if (taken & (1u << q)) continue;
-                if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (oe >= 0 && (be < 0 || key_before(ov, oe, bv, be))) { bv = ov; be = oe; }
-            }
-            if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
-            sel_e[j] = be;
-            sel_v[j] = bv;
-        }
 
-        // scores of the chosen experts
-        float m = sel_v[0];  // the largest key (unless NaN)
-        float denom = 1.f;
-        if (score == 0 && !renorm) {
-            float s = 0.f;
-            for (int e = lane; e < E; e += 32) s += expf(l[e] - m);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            denom = s;
+// ---------------------------------------------------------------------
+// tensor-core logits: part[s][t][e] = sum over D-slice s of x[t,:] wg[e,:]
+// ---------------------------------------------------------------------
+constexpr int RC_BM = 128, RC_BK = 64, RC_STAGES = 4, RC_THREADS = 192;
+constexpr int RC_A_BYTES = RC_BM * RC_BK * 2;  // 16 KB
+
+struct RouterTcParams {
+    int T, E, n_pad, nk, kps;
+    float *part;  // [splits][T][E]
+    int *status;
+};
+
+__host__ __device__ inline int rc_stage_bytes(int n_pad) { return RC_A_BYTES + n_pad * RC_BK * 2; }
+
+inline size_t rc_smem_bytes(int n_pad) {
+    return 1024 + (size_t)RC_STAGES * rc_stage_bytes(n_pad) + 16 * sizeof(uint64_t) + 16;
+}
+
+__host__ __device__ inline uint32_t rc_tmem_cols(int n_pad) {
+    uint32_t c = 32;
+    while (c < (uint32_t)n_pad) c <<= 1;
+    return c;
+}
+
+__global__ void __launch_bounds__(RC_THREADS)
+router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                        const __grid_constant__ CUtensorMap tmW, const RouterTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const int stage_bytes = rc_stage_bytes(p.n_pad);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + RC_STAGES * stage_bytes);
+    uint64_t *full = bars;                 // [RC_STAGES]
+    uint64_t *empty = bars + RC_STAGES;    // [RC_STAGES]
+    uint64_t *done = bars + 2 * RC_STAGES; // accumulator complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * RC_BM;
+    const int split = blockIdx.y;
+    const int kb0 = split * p.kps;
+    const int kb1 = min(p.nk, kb0 + p.kps);
+    const uint32_t ncols = rc_tmem_cols(p.n_pad);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < RC_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    } else if (warp == 1) {
+        tmem_alloc(tmem_slot, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
         if (lane == 0) {
-            float p[32];
-            float psum = 0.f;
-            for (int j = 0; j < k; ++j) {
-                p[j] = (score == 0) ? expf(sel_v[j] - m) : 1.f / (1.f + expf(-sel_v[j]));
-                psum += p[j];
+            int s = 0;
+            uint32_t ph = 0;
+            int last_parity[RC_STAGES];
+            for (int q = 0; q < RC_STAGES; ++q) last_parity[q] = -1;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                uint8_t *sa = ring + s * stage_bytes;
+                tma_load_2d(sa, &tmX, &full[s], kb * RC_BK, m0);
+                tma_load_2d(sa + RC_A_BYTES, &tmW, &full[s], kb * RC_BK, 0);
+                last_parity[s] = (int)ph;
+                if (++s == RC_STAGES) { s = 0; ph ^= 1u; }
             }
-            const float div = renorm ? psum : (score == 0 ? denom : 1.f);
-            for (int j = 0; j < k; ++j) {
-                topk_idx[(size_t)t * k + j] = sel_e[j];
-                topk_w[(size_t)t * k + j] = p[j] / div;
+            if (!ok) {
+                volatile int local_abort = 0;
+                for (int q = 0; q < RC_STAGES; ++q)
+                    if (last_parity[q] >= 0)
+                        mbar_wait_bounded(&full[q], (uint32_t)last_parity[q], &local_abort);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(RC_BM, p.n_pad);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(&full[s], ph, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(ring + s * stage_bytes);
+                const uint32_t b_addr = a_addr + RC_A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < RC_BK / 16; ++kk)
+                    tc_mma_f16(tmem_base, sdesc_kmajor_sw128(a_addr + kk * 32),
+                               sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                               (kb > kb0 || kk > 0) ? 1u : 0u);
+                tc_commit(&empty[s]);
+                if (++s == RC_STAGES) { s = 0; ph ^= 1u; }
+            }
+            tc_commit(done);  // arrives once every MMA above has completed
+            // every MMA issued here completes before TMEM is freed, even if
+            // the epilogue gave up waiting
+            volatile int local_abort = 0;
+            mbar_wait_bounded(done, 0u, &local_abort);
+        }
+    } else {
+        const int q = warp & 3;
+        const bool got = mbar_wait_bounded(done, 0u, abort_flag);
+        if (__all_sync(0xffffffffu, got) && !*abort_flag) {
+            tc_fence_after();
+            const int r = q * 32 + lane;
+            const int t = m0 + r;
+            float *prow = p.part + ((size_t)split * p.T + (t < p.T ? t : 0)) * p.E;
+            for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+                tc_wait_ld();
+                if (t < p.T) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < p.E) prow[c0 + i] = __uint_as_float(v[i]);
+                }
             }
         }
     }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        raise_flag(p.status, FLAG_TIMEOUT);
+        atomicCAS(p.status + 1, 0, 1 + blockIdx.x);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, ncols);
+    }
+}
+
+// Sum of the split partials (fixed order), bias, then the warp top-k.
+constexpr int RR_THREADS = 256;
+
+__global__ void __launch_bounds__(RR_THREADS)
+router_reduce_topk_kernel(const float *__restrict__ part, int splits, const float *__restrict__ bias,
+                          float *__restrict__ logits_out, int *__restrict__ topk_idx,
+                          float *__restrict__ topk_w, int Tn, int E, int k, int score, int renorm,
+                          int *status) {
+    extern __shared__ float s_row[];  // [RR_THREADS / 32][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (RR_THREADS / 32) + warp;
+    if (t >= Tn) return;
+    float *l = s_row + warp * E;
+    for (int e = lane; e < E; e += 32) {
+        float v = 0.f;
+        for (int s = 0; s < splits; ++s) v += part[((size_t)s * Tn + t) * E + e];
+        if (bias) v += bias[e];
+        l[e] = v;
+        if (logits_out) logits_out[(size_t)t * E + e] = v;
+    }
+    __syncwarp();
+    warp_topk_weights(l, E, k, score, renorm, t, topk_idx, topk_w, status, lane);
+}
+
+}  // namespace
+
+int64_t router_scratch_floats(int T, int E, int is_bf16) {
+    if (!is_bf16 || E > kRouterTcMaxE) return 0;
+    return (int64_t)kRouterMaxSplits * T * E;
+}
+
+namespace {
+
+cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, float *logits_out,
+                             int *topk_idx, float *topk_w, int T, int D, int E, int k, int score,
+                             int renorm, float *part, int *status, cudaStream_t stream) {
+    const int n_pad = (E + 15) / 16 * 16;
+    CUtensorMap tm_x, tm_w;
+    if (!make_tmap_2d(&tm_x, x, D, T, RC_BM) || !make_tmap_2d(&tm_w, wg, D, E, n_pad))
+        return cudaErrorInvalidValue;
+    const int nsm = sm_count();
+    if (nsm <= 0) return cudaErrorNoDevice;
+    const int m_tiles = (T + RC_BM - 1) / RC_BM;
+    const int nk = (D + RC_BK - 1) / RC_BK;
+    int splits = std::max(1, std::min({kRouterMaxSplits, nk, (2 * nsm + m_tiles - 1) / m_tiles}));
+    const int kps = (nk + splits - 1) / splits;
+    splits = (nk + kps - 1) / kps;  // no empty split
+    RouterTcParams p{T, E, n_pad, nk, kps, part, status};
+    const size_t smem = rc_smem_bytes(n_pad);
+    cudaError_t err = cudaFuncSetAttribute(router_logits_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    router_logits_tc_kernel<<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int per_block = RR_THREADS / 32;
+    const size_t rsmem = sizeof(float) * per_block * (size_t)E;
+    router_reduce_topk_kernel<<<(T + per_block - 1) / per_block, RR_THREADS, rsmem, stream>>>(
+        part, splits, bias, logits_out, topk_idx, topk_w, T, E, k, score, renorm, status);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
                                int *topk_idx, float *topk_w, int T, int D, int E, int k,
-                               int score, int renorm, int is_bf16, int *status,
-                               cudaStream_t stream) {
+                               int score, int renorm, int is_bf16, float *scratch,
+                               int64_t scratch_floats, int *status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
+    if (is_bf16 && E <= kRouterTcMaxE && scratch &&
+        scratch_floats >= router_scratch_floats(T, E, is_bf16))
+        return launch_router_tc(x, wg, bias, logits_out, topk_idx, topk_w, T, D, E, k, score,
+                                renorm, scratch, status, stream);
     const size_t smem = sizeof(float) * ((size_t)RT_TOKENS * E + RT_BK * SX_LD + RT_BK * SW_LD);
     const dim3 grid((T + RT_TOKENS - 1) / RT_TOKENS);
     cudaError_t err;
