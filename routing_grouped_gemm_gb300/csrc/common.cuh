@@ -129,6 +129,53 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Bring a tile into L2 ahead of its shared-memory load (no completion
+// signal; coordinates outside the tensor are simply not fetched).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+// Shared -> global tile store (bulk async group).  Rows / columns outside
+// the tensor are clipped.  The smem source must be 128-byte aligned.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N committed bulk groups still read their smem source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until every committed bulk group has completed (writes visible).
+__device__ __forceinline__ void bulk_wait_group_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -226,13 +273,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // grouped-layout tile table (shared by the grouped GEMM kernels)
 // ---------------------------------------------------------------------
 // For local expert i: rows [base_i, base_i + valid_i) of the permuted
-// buffers, valid_i = min(count, segment length); mt_off is the exclusive
-// scan of ceil(valid_i / BM).  Built by one warp.  Offsets that fall outside
+// buffers, valid_i = min(count, segment length), segment end end_i (the
+// rows up to it are this expert's, valid or padding); mt_off is the
+// exclusive scan of ceil(valid_i / BM).  Built by one warp.  Offsets that fall outside
 // [0, rows_alloc] or decrease flag FLAG_BAD_ROUTING and empty the segment.
 __device__ __forceinline__ void build_tile_table(int lane, int E_local, int e_first, int rows_alloc,
                                                  int BM, const int *__restrict__ seg_off,
                                                  const int *__restrict__ tpe, int *s_base,
-                                                 int *s_valid, int *s_mtoff, int *status) {
+                                                 int *s_valid, int *s_mtoff, int *status,
+                                                 int *s_end = nullptr) {
     // each lane takes a contiguous run of experts
     const int per = (E_local + 31) / 32;
     const int lo = lane * per;
@@ -248,6 +297,7 @@ __device__ __forceinline__ void build_tile_table(int lane, int E_local, int e_fi
         const int v = min(c, e - b);
         s_base[i] = b;
         s_valid[i] = v < 0 ? 0 : v;
+        if (s_end) s_end[i] = e;
         run += (s_valid[i] + BM - 1) / BM;
     }
     int incl = run;

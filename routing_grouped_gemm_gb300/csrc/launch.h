@@ -17,7 +17,15 @@ void set_last_error(const char *msg);
 bool make_tmap_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows);
 bool make_tmap_3d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t experts,
                   uint32_t box_rows);
+// fp32 row-major [rows, cols], box = box_cols x box_rows, 128-byte swizzle.
+bool make_tmap_2d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                      uint32_t box_cols, uint32_t box_rows);
 int sm_count();  // SMs of the current device (0 on error)
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute is set once per (kernel, device) and
+// raised only when a larger size is asked for, so launches do not pay for it.
+cudaError_t ensure_smem(const void *kernel, size_t bytes);
 
 // Router.  bf16 with E <= kRouterTcMaxE runs on the tensor cores and needs
 // router_scratch_floats(T, E, 1) floats of scratch for the split partials;

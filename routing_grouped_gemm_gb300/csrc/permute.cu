@@ -314,8 +314,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     const size_t mask_smem = sizeof(uint32_t) * PB_WARPS * (size_t)E;
     cudaError_t err;
     if (nblk > 0) {
-        err = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)mask_smem);
+        err = ensure_smem((const void *)permute_count_kernel, mask_smem);
         if (err != cudaSuccess) return err;
         permute_count_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(topk_idx, T, k, E, blk_cnt,
                                                                      status);
@@ -327,8 +326,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         tokens_per_expert, seg_offsets, blk_base, token_of_row, status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nblk == 0) return cudaSuccess;
-    err = cudaFuncSetAttribute(permute_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)mask_smem);
+    err = ensure_smem((const void *)permute_index_kernel, mask_smem);
     if (err != cudaSuccess) return err;
     permute_index_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(
         topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);

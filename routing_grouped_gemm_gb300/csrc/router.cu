@@ -365,8 +365,7 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     splits = (nk + kps - 1) / kps;  // no empty split
     RouterTcParams p{T, E, n_pad, nk, kps, part, status};
     const size_t smem = rc_smem_bytes(n_pad);
-    cudaError_t err = cudaFuncSetAttribute(router_logits_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem((const void *)router_logits_tc_kernel, smem);
     if (err != cudaSuccess) return err;
     router_logits_tc_kernel<<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -393,14 +392,14 @@ cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias,
     cudaError_t err;
     if (is_bf16) {
         auto kern = router_topk_kernel<__nv_bfloat16>;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = ensure_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
         kern<<<grid, RT_THREADS, smem, stream>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)wg,
                                                  bias, logits_out, topk_idx, topk_w, T, D, E, k,
                                                  score, renorm, status);
     } else {
         auto kern = router_topk_kernel<float>;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = ensure_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
         kern<<<grid, RT_THREADS, smem, stream>>>((const float *)x, (const float *)wg, bias,
                                                  logits_out, topk_idx, topk_w, T, D, E, k, score,
