@@ -175,9 +175,8 @@ moe_status moe_permute(const moe_config *cfg, const void *x, const int32_t *topk
  *   y_perm [rows_alloc, D] fp32 (written for valid rows): y = h w2^T, the
  *     fp32 accumulator itself -- it is rounded to dtype only after the
  *     weighted combine.
- *   Rows of a segment's padding (between its valid rows and the next
- *   segment's start) may be written with unspecified values; rows of other
- *   segments are never touched.
+ *   Rows that hold no token (padding) and rows of other segments are never
+ *   written.
  * Segments may have any length; offsets outside [0, rows_alloc] flag
  * MOE_ERR_BAD_ROUTING and the segment is skipped.
  */

@@ -312,8 +312,7 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     const int nsm = sm_count();
     if (nsm <= 0) return cudaErrorNoDevice;
     const size_t smem = tc_smem_bytes(E_local);
-    cudaError_t err = cudaFuncSetAttribute(grouped_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = ensure_smem((const void *)grouped_tc_kernel, smem);
     if (err != cudaSuccess) return err;
     const long long mt_bound = (rows_alloc + TC_BM - 1) / TC_BM + E_local;
 
