@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/moe.h"
@@ -167,10 +168,34 @@ moe_status do_grouped(const moe_config *c, const void *x_perm, const int32_t *se
                       const int32_t *tpe, const void *w1, const void *w3, const void *w2, void *h,
                       void *y_perm, const StepWs &w, cudaStream_t s) {
     cudaError_t e;
-    if (c->dtype == MOE_BF16)
-        e = moe::launch_grouped_swiglu_bf16(x_perm, seg, tpe, w1, w3, w2, h, y_perm, c->D,
-                                            c->H_local, c->e_first, c->E_local, rows_alloc_of(c),
-                                            &w.status->flags, s);
+    if (c->dtype == MOE_BF16) {
+        // Two tcgen05 implementations: one CTA per 128x256 tile, or CTA pairs
+        // on 256x256 tiles (cta_group::2).  Pairs read fewer operand bytes per
+        // SM but pad each expert's rows to 256 instead of 128.  Measured on
+        // GB300 (grouped SwiGLU call): pairs win with large segments (2048
+        // rows per expert: 1537 vs 1513 TFLOP/s) and with large D, where the
+        // weights stream from HBM (D=7168, 256 rows: 5.47 vs 5.73 ms);
+        // single CTAs win at D=2048 with 384 rows (0.369 vs 0.383 ms) and in
+        // decode (a few rows per expert).  MOE_GROUPED_KERNEL=single|pair
+        // overrides the choice.
+        const int64_t avg_rows =
+            c->E_local ? (int64_t)c->T * (c->k < c->E_local ? c->k : c->E_local) / c->E_local : 0;
+        bool single = !(avg_rows >= 512 || (c->D >= 4096 && avg_rows >= 128));
+        const char *sel = getenv("MOE_GROUPED_KERNEL");
+        if (sel && strcmp(sel, "single") == 0) single = true;
+        if (sel && strcmp(sel, "pair") == 0) single = false;
+        bool launched = false;
+        e = cudaSuccess;
+        if (!single)
+            e = moe::launch_grouped_swiglu_bf16_pair(x_perm, seg, tpe, w1, w3, w2, h, y_perm, c->D,
+                                                     c->H_local, c->e_first, c->E_local,
+                                                     rows_alloc_of(c), &w.status->flags, s,
+                                                     &launched);
+        if (e == cudaSuccess && !launched)
+            e = moe::launch_grouped_swiglu_bf16(x_perm, seg, tpe, w1, w3, w2, h, y_perm, c->D,
+                                                c->H_local, c->e_first, c->E_local,
+                                                rows_alloc_of(c), &w.status->flags, s);
+    }
     else
         e = moe::launch_grouped_swiglu_f32((const float *)x_perm, seg, tpe, (const float *)w1,
                                            (const float *)w3, (const float *)w2, (float *)h,

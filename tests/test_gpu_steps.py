@@ -241,7 +241,12 @@ def _grouped_case(moe, dt, T, E_local, k, D, H, align, seed, skew=1.0):
     ("f32", 600, 6, 2, 128, 256, 128),
     ("f32", 301, 7, 3, 136, 72, 8),
 ])
-def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align):
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monkeypatch):
+    # bf16: the CTA-pair (cta_group::2) and the one-CTA-per-tile kernels
+    if dt == "f32" and kernel == "single":
+        pytest.skip("one fp32 implementation")
+    monkeypatch.setenv("MOE_GROUPED_KERNEL", kernel)
     lay, xp, w1, w3, w2, h, y = _grouped_case(moe, dt, T, E_local, k, D, H, align, seed=T + H)
     H_ = moe_inputs.host_array
     seg, cnt = lay["seg_offsets"], lay["tokens_per_expert"]
