@@ -31,7 +31,10 @@ cudaError_t ensure_smem(const void *kernel, size_t bytes);
 // router_scratch_floats(T, E, 1) floats of scratch for the split partials;
 // everything else (or a missing scratch) runs the fused SIMT kernel.
 constexpr int kRouterTcMaxE = 256;
-constexpr int kRouterMaxSplits = 8;
+#ifndef MOE_ROUTER_SPLITS
+#define MOE_ROUTER_SPLITS 8
+#endif
+constexpr int kRouterMaxSplits = MOE_ROUTER_SPLITS;
 int64_t router_scratch_floats(int T, int E, int is_bf16);
 cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
                                int *topk_idx, float *topk_w, int T, int D, int E, int k,

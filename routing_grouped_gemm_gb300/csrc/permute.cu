@@ -14,10 +14,12 @@
 // is bit-identical run to run:
 //   count : per block of 256 tokens, per warp of 32 tokens, a bitmask per
 //           expert of which lanes route to it; block counts per expert
-//   scan  : one CTA; tokens_per_expert, padded segment offsets, each block's
-//           first row per local expert, padding rows of token_of_row
 //   index : recomputes the masks; rank of (t, e) = rows of e in earlier
-//           blocks + earlier warps + popc(mask & lanes below)
+//           blocks + earlier warps + popc(mask & lanes below); for small
+//           count matrices each block also derives the totals and padded
+//           segment offsets itself (no separate scan launch), otherwise
+//   scan  : one CTA computes tokens_per_expert, the padded segment offsets,
+//           each block's first row per local expert and the padding rows
 //   copy  : one warp per token reads x[t] once and writes its k copies
 #include "common.cuh"
 #include "launch.h"
@@ -187,6 +189,125 @@ permute_index_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int 
     }
 }
 
+// Index kernel with the scan folded in, for small count matrices: every
+// block re-derives the per-expert totals, the padded segment offsets and its
+// own first row per expert from blk_cnt [nblk][E] (a few KB), so no
+// separate single-CTA scan launch sits between count and index.  Block b
+// also writes the padding entries of token_of_row for local experts
+// i = b, b + nblk, ... and its share of the rows after the last segment;
+// block 0 writes tokens_per_expert and seg_offsets.
+constexpr int FUSED_MAX_CELLS = 16384;  // nblk * E handled by the fused kernel
+
+__global__ void __launch_bounds__(PB_TOKENS)
+permute_index_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int e_first,
+                          int E_local, int layout, int align_m, int capacity, long long rows_alloc,
+                          const int *__restrict__ blk_cnt, int nblk,
+                          int *__restrict__ tokens_per_expert, int *__restrict__ seg_offsets,
+                          int *__restrict__ row_of, int *__restrict__ token_of_row, int *status) {
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t *s_mask = s_dyn;                                       // [PB_WARPS][E]
+    int *s_tot = reinterpret_cast<int *>(s_mask + PB_WARPS * E);    // [E]  totals
+    int *s_pre = s_tot + E;                                         // [E]  rows in earlier blocks
+    int *s_off = s_pre + E;                                         // [E_local + 1] padded offsets
+    __shared__ int s_warp_sum[PB_TOKENS / 32];
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+
+    build_masks(topk_idx, T, k, E, s_mask, nullptr);
+    // totals and this block's prefix, per expert
+    for (int e = tid; e < E; e += PB_TOKENS) {
+        int tot = 0, pre = 0, bb = 0;
+        for (; bb + 8 <= nblk; bb += 8) {  // 8 independent loads in flight
+            int c[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = blk_cnt[(size_t)(bb + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                tot += c[u];
+                pre += (bb + u) < b ? c[u] : 0;
+            }
+        }
+        for (; bb < nblk; ++bb) {
+            const int c = blk_cnt[(size_t)bb * E + e];
+            tot += c;
+            pre += bb < b ? c : 0;
+        }
+        s_tot[e] = tot;
+        s_pre[e] = pre;
+    }
+    __syncthreads();
+    // padded sizes of the local segments -> exclusive scan (thread chunks)
+    const int per = (E_local + PB_TOKENS - 1) / PB_TOKENS;
+    const int lo = tid * per, hi = min(E_local, lo + per);
+    int run = 0;
+    for (int i = lo; i < hi; ++i) {
+        const int c = s_tot[e_first + i];
+        const int size = layout == 1 ? capacity : (c + align_m - 1) / align_m * align_m;
+        s_off[i] = size;  // temporarily the size
+        run += size;
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp_sum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_warp_sum[w];
+    int acc = base + incl - run;
+    for (int i = lo; i < hi; ++i) {
+        const int size = s_off[i];
+        s_off[i] = acc;
+        acc += size;
+    }
+    if (tid == PB_TOKENS - 1) s_off[E_local] = acc;
+    __syncthreads();
+
+    if (b == 0) {
+        for (int e = tid; e < E; e += PB_TOKENS) tokens_per_expert[e] = s_tot[e];
+        for (int i = tid; i <= E_local; i += PB_TOKENS) seg_offsets[i] = s_off[i];
+        if (layout == 1)
+            for (int i = tid; i < E_local; i += PB_TOKENS)
+                if (s_tot[e_first + i] > capacity) raise_flag(status, FLAG_CAPACITY);
+    }
+    // padding rows of this block's share of the local experts
+    for (int i = b; i < E_local; i += nblk) {
+        const int used = min(s_tot[e_first + i], s_off[i + 1] - s_off[i]);
+        for (int r = s_off[i] + used + tid; r < s_off[i + 1]; r += PB_TOKENS) token_of_row[r] = -1;
+    }
+    // rows after the last segment, split over the blocks
+    for (long long r = (long long)s_off[E_local] + (long long)b * PB_TOKENS + tid; r < rows_alloc;
+         r += (long long)nblk * PB_TOKENS)
+        token_of_row[r] = -1;
+
+    const int t = b * PB_TOKENS + warp * 32 + lane;
+    if (t >= T) return;
+    const int *row = topk_idx + (size_t)t * k;
+    const uint32_t below = lanemask_lt();
+    for (int j = 0; j < k; ++j) {
+        int r = -1;
+        if (slot_active(row, j, E)) {
+            const int e = row[j];
+            const int i = e - e_first;
+            if (i >= 0 && i < E_local) {
+                int prior = __popc(s_mask[warp * E + e] & below);
+                for (int w = 0; w < warp; ++w) prior += __popc(s_mask[w * E + e]);
+                const int cand = s_off[i] + s_pre[e] + prior;
+                if (cand < s_off[i + 1]) {
+                    r = cand;
+                    token_of_row[cand] = t;
+                } else {
+                    raise_flag(status, FLAG_CAPACITY);
+                }
+            }
+        }
+        row_of[(size_t)t * k + j] = r;
+    }
+}
+
 // One warp per token: read x[t] once in 16-byte vectors, write k copies.
 constexpr int CP_UNROLL = 4;
 
@@ -320,6 +441,15 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                                                                      status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
+    if (nblk > 0 && (int64_t)nblk * E <= FUSED_MAX_CELLS) {
+        const size_t smem = mask_smem + sizeof(int) * (2 * (size_t)E + E_local + 1);
+        err = ensure_smem((const void *)permute_index_scan_kernel, smem);
+        if (err != cudaSuccess) return err;
+        permute_index_scan_kernel<<<nblk, PB_TOKENS, smem, stream>>>(
+            topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity, rows_alloc, blk_cnt,
+            nblk, tokens_per_expert, seg_offsets, row_of, token_of_row, status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    } else {
     const size_t scan_smem = sizeof(int) * ((size_t)E + E_local + 1);
     permute_scan_kernel<<<1, SCAN_THREADS, scan_smem, stream>>>(
         blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
@@ -331,6 +461,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     permute_index_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(
         topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     const int vpr = D * elem_bytes / 16;
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;

@@ -41,7 +41,8 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 // warp-wide arg-max in the selection order of key_before (larger key first,
 // equal keys by lower expert index, NaN last), then the routing weights:
 // softmax over all E (or sigmoid) of the chosen keys, divided by their sum
-// when renormalising.  Lane i owns experts i, i+32, ... (E <= 1024).
+// when renormalising.  Lane i owns experts i, i+32, ... (E <= 1024); the
+// winner of round j is kept by lane j, which computes and writes slot j.
 __device__ void warp_topk_weights(const float *l, int E, int k, int score, int renorm, int t,
                                   int *__restrict__ topk_idx, float *__restrict__ topk_w,
                                   int *status, int lane) {
@@ -50,8 +51,8 @@ __device__ void warp_topk_weights(const float *l, int E, int k, int score, int r
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) raise_flag(status, FLAG_BAD_ROUTING);
 
     uint32_t taken = 0;  // bit q: expert lane + 32 q already chosen
-    int sel_e[32];
-    float sel_v[32];
+    int my_e = -1;       // slot `lane`'s expert and key (lanes < k)
+    float my_v = 0.f, top = 0.f;
     for (int j = 0; j < k; ++j) {
         float bv = 0.f;
         int be = -1;
@@ -66,31 +67,28 @@ __device__ void warp_topk_weights(const float *l, int E, int k, int score, int r
             if (oe >= 0 && (be < 0 || key_before(ov, oe, bv, be))) { bv = ov; be = oe; }
         }
         if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
-        sel_e[j] = be;
-        sel_v[j] = bv;
+        if (lane == j) { my_e = be; my_v = bv; }
+        if (j == 0) top = bv;  // the largest key (unless NaN)
     }
 
-    const float m = sel_v[0];  // the largest key (unless NaN)
-    float denom = 1.f;
-    if (score == 0 && !renorm) {
-        float sum = 0.f;
-        for (int e = lane; e < E; e += 32) sum += expf(l[e] - m);
+    float p = 0.f;
+    if (lane < k) p = (score == 0) ? expf(my_v - top) : 1.f / (1.f + expf(-my_v));
+    float div = 1.f;
+    if (renorm) {
+        float sum = p;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        denom = sum;
+        div = sum;
+    } else if (score == 0) {
+        float sum = 0.f;
+        for (int e = lane; e < E; e += 32) sum += expf(l[e] - top);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        div = sum;
     }
-    if (lane == 0) {
-        float p[32];
-        float psum = 0.f;
-        for (int j = 0; j < k; ++j) {
-            p[j] = (score == 0) ? expf(sel_v[j] - m) : 1.f / (1.f + expf(-sel_v[j]));
-            psum += p[j];
-        }
-        const float div = renorm ? psum : (score == 0 ? denom : 1.f);
-        for (int j = 0; j < k; ++j) {
-            topk_idx[(size_t)t * k + j] = sel_e[j];
-            topk_w[(size_t)t * k + j] = p[j] / div;
-        }
+    if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = my_e;
+        topk_w[(size_t)t * k + lane] = p / div;
     }
 }
 
@@ -173,14 +171,14 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
 
 
 // ---------------------------------------------------------------------
-// tensor-core logits: part[s][t][e] = sum over D-slice s of x[t,:] wg[e,:]
+// tensor-core logits: part[s][e][t] = sum over D-slice s of x[t,:] wg[e,:]
 // ---------------------------------------------------------------------
 constexpr int RC_BM = 128, RC_BK = 64, RC_STAGES = 4, RC_THREADS = 192;
 constexpr int RC_A_BYTES = RC_BM * RC_BK * 2;  // 16 KB
 
 struct RouterTcParams {
     int T, E, n_pad, nk, kps;
-    float *part;  // [splits][T][E]
+    float *part;  // [splits][E][T]
     int *status;
 };
 
@@ -288,9 +286,11 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         const bool got = mbar_wait_bounded(done, 0u, abort_flag);
         if (__all_sync(0xffffffffu, got) && !*abort_flag) {
             tc_fence_after();
-            const int r = q * 32 + lane;
-            const int t = m0 + r;
-            float *prow = p.part + ((size_t)split * p.T + (t < p.T ? t : 0)) * p.E;
+            // partials are token-minor, part[split][e][t]: for each expert
+            // column the warp's 32 lanes (32 consecutive tokens) write one
+            // contiguous 128-byte line
+            const int t = m0 + q * 32 + lane;
+            float *pcol = p.part + (size_t)split * p.E * p.T + t;
             for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
@@ -298,7 +298,7 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                 if (t < p.T) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (c0 + i < p.E) prow[c0 + i] = __uint_as_float(v[i]);
+                        if (c0 + i < p.E) pcol[(size_t)(c0 + i) * p.T] = __uint_as_float(v[i]);
                 }
             }
         }
@@ -316,28 +316,40 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     }
 }
 
-// Sum of the split partials (fixed order), bias, then the warp top-k.
-constexpr int RR_THREADS = 256;
+// Sum of the split partials (fixed split order), bias, then the warp top-k.
+// A block owns 32 tokens: lanes read the token-minor partials coalesced and
+// build the 32 x E keys in shared memory, then each of the 32 warps selects
+// the top-k of one token.
+constexpr int RR_THREADS = 1024;
+constexpr int RR_TOKENS = 32;
 
 __global__ void __launch_bounds__(RR_THREADS)
 router_reduce_topk_kernel(const float *__restrict__ part, int splits, const float *__restrict__ bias,
                           float *__restrict__ logits_out, int *__restrict__ topk_idx,
                           float *__restrict__ topk_w, int Tn, int E, int k, int score, int renorm,
                           int *status) {
-    extern __shared__ float s_row[];  // [RR_THREADS / 32][E]
+    extern __shared__ float s_key[];  // [RR_TOKENS][E + 1]
+    const int ld = E + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (RR_THREADS / 32) + warp;
-    if (t >= Tn) return;
-    float *l = s_row + warp * E;
-    for (int e = lane; e < E; e += 32) {
+    const int t0 = blockIdx.x * RR_TOKENS;
+    const int t = t0 + lane;
+    for (int e = warp; e < E; e += RR_THREADS / 32) {
         float v = 0.f;
-        for (int s = 0; s < splits; ++s) v += part[((size_t)s * Tn + t) * E + e];
-        if (bias) v += bias[e];
-        l[e] = v;
-        if (logits_out) logits_out[(size_t)t * E + e] = v;
+        if (t < Tn) {
+            for (int s = 0; s < splits; ++s) v += part[((size_t)s * E + e) * Tn + t];
+            if (bias) v += bias[e];
+        }
+        s_key[lane * ld + e] = v;
     }
-    __syncwarp();
-    warp_topk_weights(l, E, k, score, renorm, t, topk_idx, topk_w, status, lane);
+    __syncthreads();
+    for (int tt = warp; tt < RR_TOKENS; tt += RR_THREADS / 32) {
+        const int tok = t0 + tt;
+        if (tok >= Tn) break;
+        const float *l = s_key + tt * ld;
+        if (logits_out)
+            for (int e = lane; e < E; e += 32) logits_out[(size_t)tok * E + e] = l[e];
+        warp_topk_weights(l, E, k, score, renorm, tok, topk_idx, topk_w, status, lane);
+    }
 }
 
 }  // namespace
@@ -360,7 +372,9 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     if (nsm <= 0) return cudaErrorNoDevice;
     const int m_tiles = (T + RC_BM - 1) / RC_BM;
     const int nk = (D + RC_BK - 1) / RC_BK;
-    int splits = std::max(1, std::min({kRouterMaxSplits, nk, (2 * nsm + m_tiles - 1) / m_tiles}));
+    // about one CTA per SM (measured on GB300: T=4096, E=64 best at 4 splits
+    // of 32 m-tiles; T=8192, E=256 at 2 splits of 64 m-tiles)
+    int splits = std::max(1, std::min({kRouterMaxSplits, nk, nsm / m_tiles}));
     const int kps = (nk + splits - 1) / splits;
     splits = (nk + kps - 1) / kps;  // no empty split
     RouterTcParams p{T, E, n_pad, nk, kps, part, status};
@@ -369,9 +383,8 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     if (err != cudaSuccess) return err;
     router_logits_tc_kernel<<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const int per_block = RR_THREADS / 32;
-    const size_t rsmem = sizeof(float) * per_block * (size_t)E;
-    router_reduce_topk_kernel<<<(T + per_block - 1) / per_block, RR_THREADS, rsmem, stream>>>(
+    const size_t rsmem = sizeof(float) * RR_TOKENS * (size_t)(E + 1);
+    router_reduce_topk_kernel<<<(T + RR_TOKENS - 1) / RR_TOKENS, RR_THREADS, rsmem, stream>>>(
         part, splits, bias, logits_out, topk_idx, topk_w, T, E, k, score, renorm, status);
     return cudaGetLastError();
 }

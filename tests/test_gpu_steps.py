@@ -130,6 +130,7 @@ def _run_permute(moe, cfg, x, idx):
     (2000, 32, 8, 8, 8, 12, 0.8),        # expert range, small alignment
     (513, 256, 8, 128, 0, 256, 0.3),
     (700, 5, 1, 16, 2, 2, 0.0),          # k = 1
+    (20000, 256, 8, 128, 0, 256, 0.3),   # count matrix above the fused-scan limit
 ])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 def test_permute_bitexact(moe, T, E, k, align, e_first, E_local, skew, dt):
