@@ -13,11 +13,16 @@
 //     are 32 KB per k-step instead of 48 KB for a 128x256 single-SM tile;
 //     measured with L2-resident weights, the MMA issuer waits for operands
 //     15% of the time here against 27% with single-SM tiles;
-//   * GEMM1: CTA 0 holds 128 rows of w1 and CTA 1 the same 128 rows of w3,
-//     so each CTA's accumulator holds gate (columns 0-127) and up (128-255)
-//     for its own rows and the epilogue writes h = SiLU(gate) * up directly;
-//     GEMM2: the two CTAs hold consecutive 128-row halves of a 256-row w2
-//     tile and store y in fp32;
+//   * GEMM1: CTA r holds rows n0+64r .. n0+64r+63 of w1 followed by the same
+//     rows of w3, so the pair's N=256 columns are [gate, up] of hidden units
+//     n0..n0+63 and then of n0+64..n0+127; the epilogue pairs column c with
+//     c+64 and writes h = SiLU(gate) * up directly.  GEMM2: the two CTAs hold
+//     consecutive 128-row halves of a 256-row w2 tile and store y in fp32;
+//   * an expert's last tile with at most 128 valid rows runs as an M=128
+//     pair MMA (64 rows per CTA) instead of M=256, so segments are padded to
+//     128 rows as with single-SM tiles.  With M=128 each CTA's 64 rows sit in
+//     TMEM lanes 0-63 for the first half of N and again in lanes 64-127 for
+//     the second half (128 TMEM columns; determined on GB300 with a probe);
 //   * the leader CTA (rank 0) issues the MMAs; both producers' TMA loads
 //     complete on the leader's "full" barrier; the leader's commits arrive
 //     on both CTAs' "empty" / "tmem full" barriers (multicast); both
@@ -50,6 +55,7 @@ constexpr int P_THREADS = 192;
 constexpr int P_ACC_COLS = 256;
 constexpr int P_TMEM_COLS = 512;
 constexpr uint32_t P_IDESC = idesc_bf16_f32(P_PAIR_M, P_BN);
+constexpr uint32_t P_IDESC_HALF = idesc_bf16_f32(P_PAIR_M / 2, P_BN);
 constexpr int P_NBARS = 24;
 
 
@@ -94,8 +100,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(P_THREADS, 1)
-grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const PairParams p) {
+grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
+                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                    const PairParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -133,6 +140,7 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             *abort_flag = 0;
             fence_mbarrier_init();
             prefetch_tmap(&tmA);
+            prefetch_tmap(&tmA64);
             prefetch_tmap(&tmB0);
             if (p.mode == 0) prefetch_tmap(&tmB1);
         }
@@ -157,18 +165,21 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph = 0;
             for (int tile = pair_id; tile < total_tiles; tile += n_pairs) {
                 const PairTile c = decode_pair(tile, p.n_tiles, s_mtoff, s_base, s_valid, p.E_local);
-                const int arow = c.row0 + (int)rank * P_BM;
+                const bool half = c.nvalid <= P_BM;  // M=128: 64 rows per CTA
+                const int arow = c.row0 + (int)rank * (half ? P_BM / 2 : P_BM);
+                const uint32_t tx = 2u * (half ? P_A_BYTES / 2 + P_B_BYTES : P_STAGE_BYTES);
                 bool ok = true;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    if (leader) mbar_arrive_expect_tx(&full[s], 2 * P_STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(&full[s], tx);
                     uint8_t *sa = ring + s * P_STAGE_BYTES;
                     uint8_t *sb = sa + P_A_BYTES;
                     const uint32_t fb = full_leader + (uint32_t)(s * sizeof(uint64_t));
-                    tma_load_2d_pair(sa, &tmA, fb, kb * P_BK, arow);
+                    tma_load_2d_pair(sa, half ? &tmA64 : &tmA, fb, kb * P_BK, arow);
                     if (p.mode == 0) {
-                        tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, fb, kb * P_BK, c.nt * 128,
-                                         c.expert);
+                        const int hrow = c.nt * 128 + (int)rank * 64;
+                        tma_load_3d_pair(sb, &tmB0, fb, kb * P_BK, hrow, c.expert);
+                        tma_load_3d_pair(sb + P_B_BYTES / 2, &tmB1, fb, kb * P_BK, hrow, c.expert);
                     } else {
                         tma_load_3d_pair(sb, &tmB0, fb, kb * P_BK, c.nt * P_BN + (int)rank * 128,
                                          c.expert);
@@ -188,6 +199,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int tile = pair_id; ok && tile < total_tiles; tile += n_pairs, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+                const PairTile c = decode_pair(tile, p.n_tiles, s_mtoff, s_base, s_valid, p.E_local);
+                const uint32_t idesc = c.nvalid <= P_BM ? P_IDESC_HALF : P_IDESC;
                 if (!mbar_wait_bounded(&tempty[acc], acc_ph ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * P_ACC_COLS);
@@ -199,7 +212,7 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                     for (int kk = 0; kk < P_BK / 16; ++kk) {
                         tc_mma_f16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
-                                        sdesc_kmajor_sw128(b_addr + kk * 32), P_IDESC,
+                                        sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
                                         (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair(&empty[s], 0x3);
@@ -229,22 +242,34 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const bool got = mbar_wait_bounded(&tfull[acc], acc_ph, abort_flag);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
-            const int crow0 = c.row0 + (int)rank * P_BM;                    // this CTA's rows
-            const int cvalid = max(0, min(P_BM, c.nvalid - (int)rank * P_BM));
-            const int r = q * 32 + lane;
+            // Rows and columns this lane drains.  Full tile: lane l holds row l
+            // and the pair's N columns 0..255.  Half tile: lane l holds row
+            // l % 64 and N columns 128*(l / 64) .. +127 in TMEM columns 0..127.
+            const bool half = c.nvalid <= P_BM;
+            const int rows_cta = half ? P_BM / 2 : P_BM;
+            const int crow0 = c.row0 + (int)rank * rows_cta;                // this CTA's rows
+            const int cvalid = max(0, min(rows_cta, c.nvalid - (int)rank * rows_cta));
+            const int l = q * 32 + lane;
+            const int r = half ? (l & 63) : l;
+            const int nhalf = half ? (l >> 6) : 0;                          // N half of this lane
             const bool row_ok = r < cvalid;
+            const bool warp_has_rows = (half ? (q & 1) * 32 : q * 32) < cvalid;
             const size_t orow = (size_t)(crow0 + (row_ok ? r : 0)) * p.N_out;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_ACC_COLS);
-            if (q * 32 < cvalid) {
+            if (warp_has_rows) {
                 if (p.mode == 0) {
+                    // h chunks of 32 hidden units: gate at TMEM column gc, up at gc + 64
                     __nv_bfloat16 *hrow = static_cast<__nv_bfloat16 *>(p.out) + orow;
+                    const int nch = half ? 2 : 4;
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
+                    for (int ch = 0; ch < nch; ++ch) {
+                        const int gc = half ? ch * 32 : (ch >> 1) * 128 + (ch & 1) * 32;
+                        const int hcol = half ? nhalf * 64 + ch * 32 : ch * 32;
                         uint32_t g[32], u[32];
-                        tmem_ld_32x32b_x32(tbase + ch * 32, g);
-                        tmem_ld_32x32b_x32(tbase + 128 + ch * 32, u);
+                        tmem_ld_32x32b_x32(tbase + gc, g);
+                        tmem_ld_32x32b_x32(tbase + gc + 64, u);
                         tc_wait_ld();
-                        const int col0 = c.nt * 128 + ch * 32;
+                        const int col0 = c.nt * 128 + hcol;
                         if (row_ok) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
@@ -269,12 +294,13 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 } else {
                     float *yrow = static_cast<float *>(p.out) + orow;
+                    const int nch = half ? 4 : P_BN / 32;
 #pragma unroll 1
-                    for (int ch = 0; ch < P_BN / 32; ++ch) {
+                    for (int ch = 0; ch < nch; ++ch) {
                         uint32_t d[32];
                         tmem_ld_32x32b_x32(tbase + ch * 32, d);
                         tc_wait_ld();
-                        const int col0 = c.nt * P_BN + ch * 32;
+                        const int col0 = c.nt * P_BN + nhalf * 128 + ch * 32;
                         if (row_ok) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
@@ -334,8 +360,9 @@ int max_pair_clusters(size_t smem) {
     return n;
 }
 
-cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                        const PairParams &p, int clusters, size_t smem, cudaStream_t stream) {
+cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &a64, const CUtensorMap &b0,
+                        const CUtensorMap &b1, const PairParams &p, int clusters, size_t smem,
+                        cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(P_THREADS);
@@ -348,7 +375,7 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUten
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_pair_kernel, a, b0, b1, p);
+    return cudaLaunchKernelEx(&cfg, grouped_pair_kernel, a, a64, b0, b1, p);
 }
 
 }  // namespace
@@ -371,11 +398,13 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     const int clusters_max = max_pair_clusters(smem);
     if (clusters_max <= 0) return cudaSuccess;  // not launched: caller falls back
 
-    CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
+    CUtensorMap tm_x, tm_x64, tm_w1, tm_w3, tm_h, tm_h64, tm_w2;
     if (!make_tmap_2d(&tm_x, x_perm, D, rows_alloc, P_BM) ||
-        !make_tmap_3d(&tm_w1, w1, D, H_local, E_local, 128) ||
-        !make_tmap_3d(&tm_w3, w3, D, H_local, E_local, 128) ||
+        !make_tmap_2d(&tm_x64, x_perm, D, rows_alloc, P_BM / 2) ||
+        !make_tmap_3d(&tm_w1, w1, D, H_local, E_local, 64) ||
+        !make_tmap_3d(&tm_w3, w3, D, H_local, E_local, 64) ||
         !make_tmap_2d(&tm_h, h, H_local, rows_alloc, P_BM) ||
+        !make_tmap_2d(&tm_h64, h, H_local, rows_alloc, P_BM / 2) ||
         !make_tmap_3d(&tm_w2, w2, H_local, D, E_local, 128))
         return cudaErrorInvalidValue;
     const long long pt_bound = (rows_alloc + P_PAIR_M - 1) / P_PAIR_M + E_local;
@@ -393,7 +422,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     p1.out = h;
     p1.status = status;
     const int c1 = (int)std::min<long long>(clusters_max, pt_bound * p1.n_tiles);
-    if ((err = launch_pair(tm_x, tm_w1, tm_w3, p1, c1, smem, stream)) != cudaSuccess) return err;
+    if ((err = launch_pair(tm_x, tm_x64, tm_w1, tm_w3, p1, c1, smem, stream)) != cudaSuccess) return err;
 
     PairParams p2 = p1;
     p2.mode = 1;
@@ -402,7 +431,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     p2.n_tiles = (D + P_BN - 1) / P_BN;
     p2.out = y_perm;
     const int c2 = (int)std::min<long long>(clusters_max, pt_bound * p2.n_tiles);
-    if ((err = launch_pair(tm_h, tm_w2, tm_w2, p2, c2, smem, stream)) != cudaSuccess) return err;
+    if ((err = launch_pair(tm_h, tm_h64, tm_w2, tm_w2, p2, c2, smem, stream)) != cudaSuccess) return err;
     *launched = true;
     return cudaSuccess;
 }

@@ -170,17 +170,15 @@ moe_status do_grouped(const moe_config *c, const void *x_perm, const int32_t *se
     cudaError_t e;
     if (c->dtype == MOE_BF16) {
         // Two tcgen05 implementations: one CTA per 128x256 tile, or CTA pairs
-        // on 256x256 tiles (cta_group::2).  Pairs read fewer operand bytes per
-        // SM but pad each expert's rows to 256 instead of 128.  Measured on
-        // GB300 (grouped SwiGLU call): pairs win with large segments (2048
-        // rows per expert: 1537 vs 1513 TFLOP/s) and with large D, where the
-        // weights stream from HBM (D=7168, 256 rows: 5.47 vs 5.73 ms);
-        // single CTAs win at D=2048 with 384 rows (0.369 vs 0.383 ms) and in
-        // decode (a few rows per expert).  MOE_GROUPED_KERNEL=single|pair
+        // on 256x256 tiles (cta_group::2, with an M=128 pair tile for an
+        // expert's last <= 128 rows).  Measured on GB300 (grouped SwiGLU call,
+        // single vs pair): fine-grained 0.364 vs 0.359 ms, DeepSeek-V3-shaped
+        // 5.24 vs 4.87 ms, Zipf-skewed 3.19 vs 3.11 ms; decode (about four
+        // rows per expert) 3.20 vs 3.28 ms.  MOE_GROUPED_KERNEL=single|pair
         // overrides the choice.
         const int64_t avg_rows =
             c->E_local ? (int64_t)c->T * (c->k < c->E_local ? c->k : c->E_local) / c->E_local : 0;
-        bool single = !(avg_rows >= 512 || (c->D >= 4096 && avg_rows >= 128));
+        bool single = avg_rows < 64;
         const char *sel = getenv("MOE_GROUPED_KERNEL");
         if (sel && strcmp(sel, "single") == 0) single = true;
         if (sel && strcmp(sel, "pair") == 0) single = false;
