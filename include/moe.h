@@ -102,6 +102,14 @@ const char *moe_last_error_string(void);
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int32_t moe_abi_version(void);
 
+/*
+ * Kernels this library has launched in the calling process so far (all
+ * threads, all devices; a launch counts when it was issued, whether or not
+ * the kernel has run yet).  Instrumentation only: read it before and after
+ * a region to count the region's launches.  Never fails.
+ */
+uint64_t moe_kernel_launches(void);
+
 /* MOE_OK if cfg describes a problem every call below accepts. */
 moe_status moe_validate_config(const moe_config *cfg);
 

@@ -30,7 +30,7 @@ ABI_SYMBOLS = (
     "moe_status_string", "moe_last_error_string", "moe_abi_version", "moe_validate_config",
     "moe_rows_alloc", "moe_workspace_size", "moe_layer_workspace_size", "moe_route_topk",
     "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine", "moe_layer_forward",
-    "moe_get_device_status", "moe_permute_noalloc",
+    "moe_get_device_status", "moe_permute_noalloc", "moe_kernel_launches",
 )
 
 
@@ -69,6 +69,7 @@ def _load() -> ctypes.CDLL:
         "moe_layer_forward": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_get_device_status": (I32, [P, SZ, P]),
         "moe_permute_noalloc": (I32, [C, P, P, P, P, P, P, P, P, P]),
+        "moe_kernel_launches": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -125,6 +126,11 @@ def last_error_string() -> str:
 
 def abi_version() -> int:
     return int(_lib.moe_abi_version())
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(_lib.moe_kernel_launches())
 
 
 def validate_config(cfg: Config) -> int:

@@ -114,11 +114,13 @@ cudaError_t launch_grouped_swiglu_f32(const float *x_perm, const int *seg_offset
     grouped_f32_kernel<1><<<(unsigned)(mt_bound * nt1), F_THREADS, 0, stream>>>(
         x_perm, D, w1, w3, H_local, h, seg_offsets, tokens_per_expert, e_first, E_local,
         rows_alloc, nt1, status);
+    count_launch();
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     grouped_f32_kernel<2><<<(unsigned)(mt_bound * nt2), F_THREADS, 0, stream>>>(
         h, H_local, w2, nullptr, D, y_perm, seg_offsets, tokens_per_expert, e_first, E_local,
         rows_alloc, nt2, nullptr);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -330,6 +330,7 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p1.status = status;
     const long long g1 = std::min<long long>(nsm, mt_bound * p1.n_tiles);
     grouped_tc_kernel<<<(unsigned)g1, TC_THREADS, smem, stream>>>(tm_x, tm_w1, tm_w3, p1);
+    count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     TcParams p2 = p1;
@@ -340,6 +341,7 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p2.out = y_perm;
     const long long g2 = std::min<long long>(nsm, mt_bound * p2.n_tiles);
     grouped_tc_kernel<<<(unsigned)g2, TC_THREADS, smem, stream>>>(tm_h, tm_w2, tm_w2, p2);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -375,6 +375,7 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &a64, const CUte
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    count_launch();
     return cudaLaunchKernelEx(&cfg, grouped_pair_kernel, a, a64, b0, b1, p);
 }
 

@@ -12,6 +12,10 @@ namespace moe {
 // Sets the text returned by moe_last_error_string() for the calling thread.
 void set_last_error(const char *msg);
 
+// Adds n to the count returned by moe_kernel_launches(); every launch site
+// calls it once per kernel it issues.
+void count_launch(int n = 1);
+
 // TMA tensor maps over bf16 row-major data, 128-byte swizzle, boxes of 64
 // columns x box_rows rows (x 1 expert for the 3-D form [experts, rows, cols]).
 bool make_tmap_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows);

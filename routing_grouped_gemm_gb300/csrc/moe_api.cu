@@ -1,6 +1,7 @@
 // C ABI of the MoE layer local data path: argument validation, workspace
 // carving and the launch sequence.  Declarations and contracts: moe.h.
 #include <cuda_runtime.h>
+#include <atomic>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -14,7 +15,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 10000;  // 1.0.0
+constexpr int32_t kAbiVersion = 10100;  // 1.1.0
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int64_t kAlign = 256;
@@ -213,6 +214,9 @@ moe_status do_combine(const moe_config *c, const void *y_perm, const int32_t *ro
 
 namespace moe {
 void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 }  // namespace moe
 
 // ---------------------------------------------------------------------
@@ -235,6 +239,8 @@ MOE_EXPORT const char *moe_status_string(int32_t status) {
 MOE_EXPORT const char *moe_last_error_string(void) { return g_last_error; }
 
 MOE_EXPORT int32_t moe_abi_version(void) { return kAbiVersion; }
+
+MOE_EXPORT uint64_t moe_kernel_launches(void) { return moe::g_launches.load(std::memory_order_relaxed); }
 
 MOE_EXPORT moe_status moe_validate_config(const moe_config *cfg) { return validate(cfg); }
 

@@ -439,6 +439,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         if (err != cudaSuccess) return err;
         permute_count_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(topk_idx, T, k, E, blk_cnt,
                                                                      status);
+        count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (nblk > 0 && (int64_t)nblk * E <= FUSED_MAX_CELLS) {
@@ -448,18 +449,21 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         permute_index_scan_kernel<<<nblk, PB_TOKENS, smem, stream>>>(
             topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity, rows_alloc, blk_cnt,
             nblk, tokens_per_expert, seg_offsets, row_of, token_of_row, status);
+        count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     } else {
     const size_t scan_smem = sizeof(int) * ((size_t)E + E_local + 1);
     permute_scan_kernel<<<1, SCAN_THREADS, scan_smem, stream>>>(
         blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
         tokens_per_expert, seg_offsets, blk_base, token_of_row, status);
+    count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nblk == 0) return cudaSuccess;
     err = ensure_smem((const void *)permute_index_kernel, mask_smem);
     if (err != cudaSuccess) return err;
     permute_index_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(
         topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);
+    count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const int vpr = D * elem_bytes / 16;
@@ -467,6 +471,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     const int blocks = (T + warps_per_block - 1) / warps_per_block;
     permute_copy_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(
         (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -482,6 +487,7 @@ cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *t
     else
         combine_kernel<false><<<blocks, 32 * warps_per_block, 0, stream>>>(
             (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -382,10 +382,12 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     cudaError_t err = ensure_smem((const void *)router_logits_tc_kernel, smem);
     if (err != cudaSuccess) return err;
     router_logits_tc_kernel<<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
+    count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t rsmem = sizeof(float) * RR_TOKENS * (size_t)(E + 1);
     router_reduce_topk_kernel<<<(T + RR_TOKENS - 1) / RR_TOKENS, RR_THREADS, rsmem, stream>>>(
         part, splits, bias, logits_out, topk_idx, topk_w, T, E, k, score, renorm, status);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -418,6 +420,7 @@ cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias,
                                                  logits_out, topk_idx, topk_w, T, D, E, k, score,
                                                  renorm, status);
     }
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -102,11 +102,22 @@ def test_host_errors_before_any_launch(moe):
     assert lib.moe_get_device_status(None, 0, None) == moe.MOE_ERR_WORKSPACE
 
 
+def test_host_rejections_launch_nothing(moe):
+    lib = moe._lib
+    before = moe.kernel_launches()
+    bad = moe.Config(T=10, D=12, H_local=8, E=4, k=5).c()
+    assert lib.moe_layer_forward(ctypes.byref(bad), 0, 0, None, 0, 0, 0, 0, 0, 0, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(ctypes.byref(bad), 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert moe.kernel_launches() == before
+
+
 def test_status_strings(moe):
     assert moe.status_string(moe.MOE_OK) == "MOE_OK"
     assert moe.status_string(moe.MOE_ERR_CAPACITY) == "MOE_ERR_CAPACITY"
     assert moe.status_string(1234) == "MOE_ERR_UNKNOWN"
-    assert moe.abi_version() >= 10000
+    assert moe.abi_version() >= 10100
 
 
 def test_product_does_not_import_oracle():
