@@ -313,6 +313,10 @@ def run_gpu(args):
 
     for _ in range(max(3, args.warmup)):
         step()
+    # launches of one grouped SwiGLU call (one cooperative launch or two)
+    n0 = moe.kernel_launches()
+    moe.moe_grouped_swiglu(cfg, x_perm, seg, tpe, inp.w1, inp.w3, inp.w2, h, y_perm, ws, stream)
+    gemm_launches = moe.kernel_launches() - n0
     torch.cuda.synchronize(dev)
     st = moe.moe_get_device_status(ws, stream)
     if st != moe.MOE_OK:
@@ -366,7 +370,8 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
                    "router": "softmax, renormalised over top-k", "layout": "contiguous, align_m=128",
                    "parallelism": f"replicas x{world}" if world > 1 else "single", "l2": L2_NOTE},
-        "roofline": {"kernel": "grouped SwiGLU on CTA pairs (GEMM1 + gate, GEMM2): 2 launches per call",
+        "roofline": {"kernel": "grouped SwiGLU on CTA pairs (GEMM1 + SwiGLU, GEMM2): "
+                               f"{gemm_launches} launch{'es' if gemm_launches != 1 else ''} per call",
                      "bound": "tensor", "achieved": achieved,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],

@@ -109,6 +109,40 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------
+// Counters in global memory shared by the CTAs of one launch
+// ---------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) accesses, in both directions.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *ctr >= target (acquire).  Gives up like mbar_wait_bounded.
+__device__ __forceinline__ bool wait_count_bounded(const int *ctr, int target, volatile int *abort) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(ctr) >= target) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (abort) *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), tile mode, completion on an mbarrier
 // ---------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int c0,

@@ -65,15 +65,21 @@ cudaError_t launch_grouped_swiglu_f32(const float *x_perm, const int *seg_offset
                                       int D, int H_local, int e_first, int E_local,
                                       int64_t rows_alloc, int *status, cudaStream_t stream);
 
-// bf16 tcgen05 grouped SwiGLU on CTA pairs (cta_group::2).  Sets *launched
-// to false (and returns cudaSuccess) when the device cannot run clusters of
-// two with this shared-memory size, so the caller can use the 1-CTA kernel.
+// Scratch ints of the pair kernel's one-launch schedule (block counters);
+// they must be zero before the first call and are left zero by each call.
+int64_t grouped_pair_scratch_ints(int64_t rows_alloc, int E_local);
+
+// bf16 tcgen05 grouped SwiGLU on CTA pairs (cta_group::2).  With `scratch`
+// both GEMMs run in one cooperative launch; without it, or where the device
+// refuses a cooperative cluster launch, in two.  Sets *launched to false (and
+// returns cudaSuccess) when the device cannot run clusters of two with this
+// shared-memory size, so the caller can use the 1-CTA kernel.
 cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_offsets,
                                             const int *tokens_per_expert, const void *w1,
                                             const void *w3, const void *w2, void *h, void *y_perm,
                                             int D, int H_local, int e_first, int E_local,
-                                            int64_t rows_alloc, int *status, cudaStream_t stream,
-                                            bool *launched);
+                                            int64_t rows_alloc, int *scratch, int *status,
+                                            cudaStream_t stream, bool *launched);
 
 // bf16 tcgen05 grouped SwiGLU (both GEMMs), one CTA per tile.
 cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offsets,

@@ -72,6 +72,7 @@ struct StepWs {
     int *scratch;           // permute counting-sort scratch
     float *router_part;     // router split partials (bf16 tensor-core path)
     int64_t router_floats;
+    int *grouped;           // grouped GEMM block counters (bf16), zero between calls
 };
 
 int64_t permute_ws_bytes(const moe_config *c) {
@@ -82,8 +83,15 @@ int64_t router_ws_bytes(const moe_config *c) {
     return align_up(4 * moe::router_scratch_floats(c->T, c->E, c->dtype == MOE_BF16));
 }
 
+int64_t grouped_ws_bytes(const moe_config *c) {
+    return c->dtype == MOE_BF16
+               ? align_up(4 * moe::grouped_pair_scratch_ints(rows_alloc_of(c), c->E_local))
+               : 0;
+}
+
 int64_t step_ws_bytes(const moe_config *c) {
-    return (int64_t)sizeof(moe::StatusBlock) + permute_ws_bytes(c) + router_ws_bytes(c);
+    return (int64_t)sizeof(moe::StatusBlock) + permute_ws_bytes(c) + router_ws_bytes(c) +
+           grouped_ws_bytes(c);
 }
 
 moe_status carve_step(const moe_config *c, void *ws, size_t ws_bytes, StepWs *out) {
@@ -98,6 +106,10 @@ moe_status carve_step(const moe_config *c, void *ws, size_t ws_bytes, StepWs *ou
                            ? reinterpret_cast<float *>(base + sizeof(moe::StatusBlock) +
                                                        permute_ws_bytes(c))
                            : nullptr;
+    out->grouped = grouped_ws_bytes(c)
+                       ? reinterpret_cast<int *>(base + sizeof(moe::StatusBlock) +
+                                                 permute_ws_bytes(c) + router_ws_bytes(c))
+                       : nullptr;
     return MOE_OK;
 }
 
@@ -175,7 +187,7 @@ moe_status do_grouped(const moe_config *c, const void *x_perm, const int32_t *se
         // expert's last <= 128 rows).  Measured on GB300 (grouped SwiGLU call,
         // single vs pair): fine-grained 0.364 vs 0.359 ms, DeepSeek-V3-shaped
         // 5.24 vs 4.87 ms, Zipf-skewed 3.19 vs 3.11 ms; decode (about four
-        // rows per expert) 3.20 vs 3.28 ms.  MOE_GROUPED_KERNEL=single|pair
+        // rows per expert) 3.20 vs 3.28 ms.  MOE_GROUPED_KERNEL=single|pair|pair2
         // overrides the choice.
         const int64_t avg_rows =
             c->E_local ? (int64_t)c->T * (c->k < c->E_local ? c->k : c->E_local) / c->E_local : 0;
@@ -183,13 +195,17 @@ moe_status do_grouped(const moe_config *c, const void *x_perm, const int32_t *se
         const char *sel = getenv("MOE_GROUPED_KERNEL");
         if (sel && strcmp(sel, "single") == 0) single = true;
         if (sel && strcmp(sel, "pair") == 0) single = false;
+        // "pair2": the pair kernel as two launches (GEMM1, then GEMM2)
+        const bool two_launches = sel && strcmp(sel, "pair2") == 0;
+        if (two_launches) single = false;
         bool launched = false;
         e = cudaSuccess;
         if (!single)
             e = moe::launch_grouped_swiglu_bf16_pair(x_perm, seg, tpe, w1, w3, w2, h, y_perm, c->D,
                                                      c->H_local, c->e_first, c->E_local,
-                                                     rows_alloc_of(c), &w.status->flags, s,
-                                                     &launched);
+                                                     rows_alloc_of(c),
+                                                     two_launches ? nullptr : w.grouped,
+                                                     &w.status->flags, s, &launched);
         if (e == cudaSuccess && !launched)
             e = moe::launch_grouped_swiglu_bf16(x_perm, seg, tpe, w1, w3, w2, h, y_perm, c->D,
                                                 c->H_local, c->e_first, c->E_local,

@@ -242,10 +242,11 @@ def _grouped_case(moe, dt, T, E_local, k, D, H, align, seed, skew=1.0):
     ("f32", 600, 6, 2, 128, 256, 128),
     ("f32", 301, 7, 3, 136, 72, 8),
 ])
-@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("kernel", ["pair", "pair2", "single"])
 def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monkeypatch):
-    # bf16: the CTA-pair (cta_group::2) and the one-CTA-per-tile kernels
-    if dt == "f32" and kernel == "single":
+    # bf16: the CTA-pair (cta_group::2) kernel in one launch (GEMM1 and GEMM2
+    # tiles interleaved) and in two, and the one-CTA-per-tile kernel
+    if dt == "f32" and kernel != "pair":
         pytest.skip("one fp32 implementation")
     monkeypatch.setenv("MOE_GROUPED_KERNEL", kernel)
     lay, xp, w1, w3, w2, h, y = _grouped_case(moe, dt, T, E_local, k, D, H, align, seed=T + H)
@@ -282,6 +283,69 @@ def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monk
     if tail.any():
         tt = torch.from_numpy(tail).cuda()
         assert torch.isnan(h.float()[tt]).all() and torch.isnan(y[tt]).all()
+
+
+def _grouped_run(moe, cfg, lay, xp, w1, w3, w2, ws):
+    ra, H, D = lay["rows_alloc"], cfg.H_local, cfg.D
+    h = torch.full((ra, H), float("nan"), device="cuda").to(torch.bfloat16)
+    y = torch.full((ra, D), float("nan"), device="cuda")
+    before = moe.kernel_launches()
+    moe.moe_grouped_swiglu(cfg, xp, _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"]),
+                           w1, w3, w2, h, y, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    return h, y, moe.kernel_launches() - before
+
+
+@pytest.mark.parametrize("T,E_local,k,D,H,skew", [
+    (1500, 9, 3, 512, 384, 1.0),
+    (4096, 64, 6, 2048, 1408, 1.0),    # the fine-grained layer's shapes
+    (3000, 16, 4, 768, 640, 1.5),      # skewed: a few long segments, several empty
+])
+def test_grouped_one_launch_equals_two(moe, T, E_local, k, D, H, skew, monkeypatch):
+    """The one-launch schedule (GEMM2 tiles wait on per-block GEMM1 counters)
+    gives bit-identical h and y to GEMM1 and GEMM2 run as two launches, also
+    when the workspace (and its counters) was used by a different problem
+    just before."""
+    cfg = moe.Config(T=T, D=D, H_local=H, E=E_local, k=k, align_m=128, dtype=moe.MOE_BF16)
+    ws = moe.alloc_workspace(cfg)
+    cases = []
+    for seed in (5, 6):
+        idx = moe_inputs.random_topk_idx(T, E_local, k, seed=seed, skew=skew)
+        lay = oracle.layout(idx, E_local, 0, E_local, oracle.CONTIGUOUS, 128)
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        xp = torch.randn((lay["rows_alloc"], D), generator=g, device="cuda").to(torch.bfloat16)
+        ws_ = [(torch.randn(s, generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+               for s in ((E_local, H, D), (E_local, H, D), (E_local, D, H))]
+        cases.append((lay, xp, ws_))
+    monkeypatch.setenv("MOE_GROUPED_KERNEL", "pair")
+    for lay, xp, (w1, w3, w2) in cases:
+        h1, y1, n1 = _grouped_run(moe, cfg, lay, xp, w1, w3, w2, ws)
+    assert n1 == 1
+    monkeypatch.setenv("MOE_GROUPED_KERNEL", "pair2")
+    h2, y2, n2 = _grouped_run(moe, cfg, lay, xp, w1, w3, w2, ws)
+    assert n2 == 2
+    filled = torch.from_numpy(lay["token_of_row"] >= 0).cuda()
+    assert torch.equal(h1[filled], h2[filled])
+    assert torch.equal(y1[filled], y2[filled])
+    assert torch.isnan(y1[~filled]).all()
+
+
+def test_grouped_overlapping_segments_flagged(moe):
+    """Segments that overlap cover more 256-row blocks than the buffer has;
+    the one-launch schedule then computes nothing and flags the routing."""
+    E_local, D, H, T = 3, 128, 128, 1024
+    cfg = moe.Config(T=T, D=D, H_local=H, E=E_local, k=1, dtype=moe.MOE_BF16)
+    ra = moe.rows_alloc(cfg)
+    ws = moe.alloc_workspace(cfg)
+    seg = _dev(np.array([0, ra, 0, ra], np.int32))   # experts 0 and 2 both claim every row
+    cnt = _dev(np.array([ra, 0, ra], np.int32))
+    xp = torch.zeros((ra, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((E_local, H, D), dtype=torch.bfloat16, device="cuda")
+    w2 = torch.zeros((E_local, D, H), dtype=torch.bfloat16, device="cuda")
+    h = torch.zeros((ra, H), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((ra, D), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_swiglu(cfg, xp, seg, cnt, w, w, w2, h, y, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
 
 
 def test_grouped_swiglu_bad_offsets_flagged(moe):
