@@ -72,6 +72,21 @@ constexpr int P_TMEM_COLS = 512;
 constexpr uint32_t P_IDESC = idesc_bf16_f32(P_PAIR_M, P_BN);
 constexpr uint32_t P_IDESC_HALF = idesc_bf16_f32(P_PAIR_M / 2, P_BN);
 constexpr int P_NBARS = 24;
+// An expert's last tile with at most P_SWAP_MAX valid rows runs transposed:
+// the weights are the M=256 operand and the tile's tokens the N operand
+// (N = valid rows rounded up to 32), so the MMA time follows the valid rows.
+// (An M=128 pair MMA takes as long as an M=256 one on GB300.)  Measured on
+// GB300: with at most 32 rows, DeepSeek-V3-shaped (tails of a few rows)
+// 4.97 vs 5.01 ms; raising the limit to 128 makes the fine-grained call
+// slower (0.40 vs 0.356 ms), because a transposed tile still streams a full
+// 128-row weight slice per k-step and its epilogue writes one row per
+// 32-lane store.
+#ifndef MOE_PAIR_SWAP_MAX
+#define MOE_PAIR_SWAP_MAX 32
+#endif
+constexpr int P_SWAP_MAX = MOE_PAIR_SWAP_MAX;
+static_assert(P_SWAP_MAX <= P_PAIR_M, "a transposed tile holds at most 256 tokens");
+constexpr int P_XBUF_BYTES = 2 * 32 * 32 * 4;  // GEMM1 transposed tiles: up -> gate handoff
 
 
 // Tile schedules.
@@ -99,7 +114,7 @@ struct PairParams {
 };
 
 size_t pair_smem_bytes(int E_local) {
-    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_NBARS * sizeof(uint64_t) + 16 +
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES + P_NBARS * sizeof(uint64_t) + 16 +
            sizeof(int) * (4 * (size_t)E_local + 1);
 }
 
@@ -130,6 +145,20 @@ __device__ __forceinline__ PairTile decode_pair(int v, const PairParams &p, int 
     return c;
 }
 
+// L2 prefetch of this CTA's weight slice of tile c at k-step kb (the rows
+// its TMA loads will read: w1 and w3 rows for GEMM1, w2 rows for GEMM2).
+__device__ __forceinline__ void prefetch_weights(const PairTile &c, int kb, uint32_t rank,
+                                                 const CUtensorMap *w1, const CUtensorMap *w3,
+                                                 const CUtensorMap *w2) {
+    if (c.mode == 0) {
+        const int hrow = c.nt * 128 + (int)rank * 64;
+        tma_prefetch_l2_3d(w1, kb * P_BK, hrow, c.expert);
+        tma_prefetch_l2_3d(w3, kb * P_BK, hrow, c.expert);
+    } else {
+        tma_prefetch_l2_3d(w2, kb * P_BK, c.nt * P_BN + (int)rank * 128, c.expert);
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -137,18 +166,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
 
 __global__ void __launch_bounds__(P_THREADS, 1)
 grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmX64,
+                    const __grid_constant__ CUtensorMap tmX16,
                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
                     const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmH64,
+                    const __grid_constant__ CUtensorMap tmH16,
                     const __grid_constant__ CUtensorMap tmW2, const PairParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + P_STAGES * P_STAGE_BYTES);
+    float *xbuf = reinterpret_cast<float *>(ring + P_STAGES * P_STAGE_BYTES);  // [2][32 cols][32 lanes]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES);
     uint64_t *full = bars;                   // [P_STAGES]  leader: both CTAs' TMA -> MMA
     uint64_t *empty = bars + P_STAGES;       // [P_STAGES]  MMA -> each CTA's TMA
     uint64_t *tfull = bars + 2 * P_STAGES;   // [2]         MMA -> each CTA's epilogue
     uint64_t *tempty = tfull + 2;            // [2]         leader: both epilogues -> MMA
     uint64_t *drain = tempty + 2;            // [1]         leader: MMA completion at exit
+    uint64_t *xfull = drain + 1;             // [2]         up warp -> gate warp (transposed GEMM1)
+    uint64_t *xempty = xfull + 2;            // [2]         gate warp -> up warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + P_NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_cta = reinterpret_cast<int *>(tmem_slot + 2);
@@ -175,17 +209,23 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 mbar_init(&tempty[a], P_SIGNALS_PER_TILE);  // epilogue warps of both CTAs
             }
             mbar_init(drain, 1);
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(&xfull[a], 1);
+                mbar_init(&xempty[a], 1);
+            }
             *abort_flag = 0;
             fence_mbarrier_init();
             if (p.sched != SCHED_GEMM2) {
                 prefetch_tmap(&tmX);
                 prefetch_tmap(&tmX64);
+                prefetch_tmap(&tmX16);
                 prefetch_tmap(&tmW1);
                 prefetch_tmap(&tmW3);
             }
             if (p.sched != SCHED_GEMM1) {
                 prefetch_tmap(&tmH);
                 prefetch_tmap(&tmH64);
+                prefetch_tmap(&tmH16);
                 prefetch_tmap(&tmW2);
             }
         }
@@ -214,12 +254,32 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0);
             int s = 0;
             uint32_t ph = 0;
+#ifndef MOE_PAIR_PF
+#define MOE_PAIR_PF 0
+#endif
+            constexpr int PF = MOE_PAIR_PF;  // weight prefetch distance in k-steps (0: off)
+            if (PF > 0 && pair_id < total_tiles) {
+                const PairTile c0 = decode_pair(pair_id, p, n_blocks, s_mtoff, s_base, s_valid);
+                const int nk0 = c0.mode ? p.nk1 : p.nk0;
+                for (int kb = 0; kb < PF && kb < nk0; ++kb) prefetch_weights(c0, kb, rank, &tmW1, &tmW3, &tmW2);
+            }
             for (int tile = pair_id; tile < total_tiles; tile += n_pairs) {
                 const PairTile c = decode_pair(tile, p, n_blocks, s_mtoff, s_base, s_valid);
-                const bool half = c.nvalid <= P_BM;  // M=128: 64 rows per CTA
-                const int arow = c.row0 + (int)rank * (half ? P_BM / 2 : P_BM);
-                const uint32_t tx = 2u * (half ? P_A_BYTES / 2 + P_B_BYTES : P_STAGE_BYTES);
+                PairTile cn{};
+                int nkn = 0;
+                if (PF > 0 && tile + n_pairs < total_tiles) {
+                    cn = decode_pair(tile + n_pairs, p, n_blocks, s_mtoff, s_base, s_valid);
+                    nkn = cn.mode ? p.nk1 : p.nk0;
+                }
+                const bool swap = c.nvalid <= P_SWAP_MAX;         // transposed tail tile
+                const bool half = !swap && c.nvalid <= P_BM;      // M=128: 64 rows per CTA
+                const int srows = ((c.nvalid + 31) & ~31) / 2;    // transposed: token rows per CTA
+                const int arow = c.row0 + (int)rank * (swap ? srows : half ? P_BM / 2 : P_BM);
+                const uint32_t tx =
+                    2u * (swap ? P_A_BYTES + srows * P_BK * 2
+                               : half ? P_A_BYTES / 2 + P_B_BYTES : P_STAGE_BYTES);
                 const CUtensorMap *ta = c.mode ? (half ? &tmH64 : &tmH) : (half ? &tmX64 : &tmX);
+                const CUtensorMap *t16 = c.mode ? &tmH16 : &tmX16;
                 const int nk = c.mode ? p.nk1 : p.nk0;
                 bool ok = true;
                 if (c.mode == 1 && p.sched == SCHED_BOTH) {
@@ -229,11 +289,32 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     fence_proxy_async_global();
                 }
                 for (int kb = 0; kb < nk; ++kb) {
+                    if (PF > 0) {
+                        const int pk = kb + PF;
+                        if (pk < nk) prefetch_weights(c, pk, rank, &tmW1, &tmW3, &tmW2);
+                        else if (pk - nk < nkn) prefetch_weights(cn, pk - nk, rank, &tmW1, &tmW3, &tmW2);
+                    }
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&full[s], tx);
                     uint8_t *sa = ring + s * P_STAGE_BYTES;
                     uint8_t *sb = sa + P_A_BYTES;
                     const uint32_t fb = full_leader + (uint32_t)(s * sizeof(uint64_t));
+                    if (swap) {
+                        // weights into the A slot (this CTA's 128 of the 256 M rows),
+                        // token rows into the B slot (this CTA's half of N), 16 rows a load
+                        if (c.mode == 0) {
+                            const int hrow = c.nt * 128 + (int)rank * 64;
+                            tma_load_3d_pair(sa, &tmW1, fb, kb * P_BK, hrow, c.expert);
+                            tma_load_3d_pair(sa + P_A_BYTES / 2, &tmW3, fb, kb * P_BK, hrow, c.expert);
+                        } else {
+                            tma_load_3d_pair(sa, &tmW2, fb, kb * P_BK, c.nt * P_BN + (int)rank * 128,
+                                             c.expert);
+                        }
+                        for (int i = 0; i < srows / 16; ++i)
+                            tma_load_2d_pair(sb + i * 16 * P_BK * 2, t16, fb, kb * P_BK, arow + 16 * i);
+                        if (++s == P_STAGES) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
                     tma_load_2d_pair(sa, ta, fb, kb * P_BK, arow);
                     if (c.mode == 0) {
                         const int hrow = c.nt * 128 + (int)rank * 64;
@@ -259,7 +340,10 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const int acc = it & 1;
                 const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
                 const PairTile c = decode_pair(tile, p, n_blocks, s_mtoff, s_base, s_valid);
-                const uint32_t idesc = c.nvalid <= P_BM ? P_IDESC_HALF : P_IDESC;
+                const uint32_t idesc =
+                    c.nvalid <= P_SWAP_MAX ? idesc_bf16_f32(P_PAIR_M, (c.nvalid + 31) & ~31)
+                    : c.nvalid <= P_BM     ? P_IDESC_HALF
+                                           : P_IDESC;
                 const int nk = c.mode ? p.nk1 : p.nk0;
                 if (!mbar_wait_bounded(&tempty[acc], acc_ph ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -295,13 +379,80 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
         int it = 0;
-        for (int tile = pair_id; tile < total_tiles; tile += n_pairs, ++it) {
+        uint32_t xi = 0;  // handoffs done through xbuf (transposed GEMM1 tiles)
+        bool xok = true;
+        for (int tile = pair_id; xok && tile < total_tiles; tile += n_pairs, ++it) {
             const PairTile c = decode_pair(tile, p, n_blocks, s_mtoff, s_base, s_valid);
             const int acc = it & 1;
             const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
             const bool got = mbar_wait_bounded(&tfull[acc], acc_ph, abort_flag);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
+            if (c.nvalid <= P_SWAP_MAX) {
+                // Transposed tile: TMEM lane l holds weight row l of this CTA's
+                // 128 and columns 0..nsw-1 hold the tile's tokens.
+                const int nsw = (c.nvalid + 31) & ~31;
+                const int l = q * 32 + lane;
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_ACC_COLS);
+                if (c.mode == 1) {
+                    // y column of this lane; each store is 32 consecutive fp32 of one row
+                    const int dcol = c.nt * P_BN + (int)rank * 128 + l;
+                    float *ycol = static_cast<float *>(p.out1) + (size_t)c.row0 * p.n_out1 + dcol;
+#pragma unroll 1
+                    for (int ch = 0; ch < nsw / 32; ++ch) {
+                        uint32_t d[32];
+                        tmem_ld_32x32b_x32(tb + ch * 32, d);
+                        tc_wait_ld();
+                        if (dcol < p.n_out1) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (ch * 32 + j < c.nvalid)
+                                    ycol[(size_t)(ch * 32 + j) * p.n_out1] = __uint_as_float(d[j]);
+                        }
+                    }
+                } else {
+                    // lanes 0-63: gate of hidden unit u, lanes 64-127: up of the same
+                    // units.  The up warps (quarters 2, 3) hand their values to the
+                    // gate warps (quarters 0, 1) through xbuf, one 32-token chunk at a
+                    // time; the gate warps write h.
+                    const int slot = q & 1;
+                    float *xb = xbuf + slot * 1024;  // [32 tokens][32 lanes]
+                    const int u = c.nt * 128 + (int)rank * 64 + (l & 63);
+                    __nv_bfloat16 *hcol = static_cast<__nv_bfloat16 *>(p.out0) + (size_t)c.row0 * p.n_out0 + u;
+#pragma unroll 1
+                    for (int ch = 0; ch < nsw / 32; ++ch, ++xi) {
+                        uint32_t d[32];
+                        tmem_ld_32x32b_x32(tb + ch * 32, d);
+                        tc_wait_ld();
+                        const uint32_t xph = xi & 1u;
+                        if (q >= 2) {
+                            const bool ok = mbar_wait_bounded(&xempty[slot], xph ^ 1u, abort_flag);
+                            if (!__all_sync(0xffffffffu, ok)) { xok = false; break; }
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) xb[j * 32 + lane] = __uint_as_float(d[j]);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xfull[slot]);
+                        } else {
+                            const bool ok = mbar_wait_bounded(&xfull[slot], xph, abort_flag);
+                            if (!__all_sync(0xffffffffu, ok)) { xok = false; break; }
+                            if (u < p.n_out0) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    if (ch * 32 + j < c.nvalid) {
+                                        const float gv = __uint_as_float(d[j]);
+                                        const float uv = xb[j * 32 + lane];
+                                        hcol[(size_t)(ch * 32 + j) * p.n_out0] =
+                                            __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
+                                    }
+                                }
+                            }
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xempty[slot]);
+                        }
+                    }
+                    if (!xok) break;
+                }
+            } else {
             // Rows and columns this lane drains.  Full tile: lane l holds row l
             // and the pair's N columns 0..255.  Half tile: lane l holds row
             // l % 64 and N columns 128*(l / 64) .. +127 in TMEM columns 0..127.
@@ -372,6 +523,7 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         }
                     }
                 }
+            }
             }
             tc_fence_before();
             if (c.mode == 0 && p.sched == SCHED_BOTH) {
@@ -447,7 +599,7 @@ int max_pair_clusters(size_t smem) {
 }
 
 struct PairMaps {
-    CUtensorMap x, x64, w1, w3, h, h64, w2;
+    CUtensorMap x, x64, x16, w1, w3, h, h64, h16, w2;
 };
 
 cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, size_t smem,
@@ -466,8 +618,8 @@ cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, si
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = cooperative ? 2 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_pair_kernel, m.x, m.x64, m.w1, m.w3,
-                                             m.h, m.h64, m.w2, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_pair_kernel, m.x, m.x64, m.x16, m.w1,
+                                             m.w3, m.h, m.h64, m.h16, m.w2, p);
     if (e == cudaSuccess) count_launch();
     return e;
 }
@@ -502,10 +654,12 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     PairMaps m;
     if (!make_tmap_2d(&m.x, x_perm, D, rows_alloc, P_BM) ||
         !make_tmap_2d(&m.x64, x_perm, D, rows_alloc, P_BM / 2) ||
+        !make_tmap_2d(&m.x16, x_perm, D, rows_alloc, 16) ||
         !make_tmap_3d(&m.w1, w1, D, H_local, E_local, 64) ||
         !make_tmap_3d(&m.w3, w3, D, H_local, E_local, 64) ||
         !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
         !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
+        !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
         !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128))
         return cudaErrorInvalidValue;
     const long long pt_bound = (rows_alloc + P_PAIR_M - 1) / P_PAIR_M + E_local;

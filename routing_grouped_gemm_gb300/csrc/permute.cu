@@ -21,6 +21,8 @@
 //   scan  : one CTA computes tokens_per_expert, the padded segment offsets,
 //           each block's first row per local expert and the padding rows
 //   copy  : one warp per token reads x[t] once and writes its k copies
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -343,6 +345,11 @@ permute_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_of,
 // combine: out[t] = sum_j w[t,j] * y_perm[row_of[t,j]]  (fp32, slot order)
 // ---------------------------------------------------------------------
 constexpr int CB_SLOTS = 8;  // slots whose loads are issued together
+#ifndef MOE_COMBINE_PARTS
+#define MOE_COMBINE_PARTS 1
+#endif
+constexpr int CB_PARTS = MOE_COMBINE_PARTS;  // warps per token (1: 45 us, 2: 52 us, 4: 51 us
+                                              // on the fine-grained step)
 
 // y_perm is fp32 for every dtype; out is bf16 or fp32.  The loop over
 // 16-byte output vectors is uniform across the warp (the shuffles inside
@@ -352,8 +359,17 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
                const float *__restrict__ topk_w, void *__restrict__ out, int T, int k, int D,
                long long rows_alloc, int *status) {
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // One warp per (token, part): a token's row is split into CB_PARTS parts
+    // of whole 32-vector chunks, so the grid has CB_PARTS x T warps.
+    constexpr int EPV = BF16 ? 8 : 4;      // output elements per 16-byte vector
+    const int vpr_out = D / EPV;           // output vectors per row
+    const int f4_per_out = EPV / 4;        // fp32 float4 loads per output vector
+    const int yvpr = D / 4;                // float4 per y row
+    const int nchunk = (vpr_out + 31) / 32;
     const int lane = threadIdx.x & 31;
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int t = (int)(wid / CB_PARTS);
+    const int part = (int)(wid - (long long)t * CB_PARTS);
     if (t >= T) return;
     int my_row = -1;
     float my_w = 0.f;
@@ -361,16 +377,13 @@ combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
         my_row = row_of[(size_t)t * k + lane];
         my_w = topk_w[(size_t)t * k + lane];
         if (my_row < -1 || (long long)my_row >= rows_alloc) {
-            raise_flag(status, FLAG_BAD_ROUTING);
+            if (part == 0) raise_flag(status, FLAG_BAD_ROUTING);
             my_row = -1;
         }
     }
-    constexpr int EPV = BF16 ? 8 : 4;      // output elements per 16-byte vector
-    const int vpr_out = D / EPV;           // output vectors per row
-    const int f4_per_out = EPV / 4;        // fp32 float4 loads per output vector
-    const int yvpr = D / 4;                // float4 per y row
-    for (int v0 = 0; v0 < vpr_out; v0 += 32) {
-        const int v = v0 + lane;
+    const int c_lo = part * nchunk / CB_PARTS, c_hi = (part + 1) * nchunk / CB_PARTS;
+    for (int c = c_lo; c < c_hi; ++c) {
+        const int v = c * 32 + lane;
         const bool act = v < vpr_out;
         float acc[EPV];
 #pragma unroll
@@ -416,6 +429,7 @@ combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
         reinterpret_cast<uint4 *>(out)[(size_t)t * vpr_out + v] = o;
     }
 }
+
 
 }  // namespace
 
@@ -480,7 +494,8 @@ cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *t
                            cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const int warps_per_block = 8;
-    const int blocks = (T + warps_per_block - 1) / warps_per_block;
+    const long long warps = (long long)T * CB_PARTS;
+    const int blocks = (int)((warps + warps_per_block - 1) / warps_per_block);
     if (is_bf16)
         combine_kernel<true><<<blocks, 32 * warps_per_block, 0, stream>>>(
             (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);

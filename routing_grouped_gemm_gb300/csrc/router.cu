@@ -16,6 +16,9 @@
 //     selects the top-k.
 #include <cuda.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -174,12 +177,24 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
 // tensor-core logits: part[s][e][t] = sum over D-slice s of x[t,:] wg[e,:]
 // ---------------------------------------------------------------------
 constexpr int RC_BM = 128, RC_BK = 64, RC_STAGES = 4, RC_THREADS = 192;
+// The cluster form runs extra warps that only join the reduction and top-k.
+#ifndef MOE_ROUTER_CL_WARPS
+#define MOE_ROUTER_CL_WARPS 16
+#endif
+constexpr int RC_CL_THREADS = 32 * MOE_ROUTER_CL_WARPS;
+static_assert(MOE_ROUTER_CL_WARPS >= 6, "warps 0-5 hold the pipeline roles");
 constexpr int RC_A_BYTES = RC_BM * RC_BK * 2;  // 16 KB
 
 struct RouterTcParams {
     int T, E, n_pad, nk, kps;
-    float *part;  // [splits][E][T]
+    float *part;  // [splits][E][T] (two-kernel form)
     int *status;
+    // one-kernel (cluster) form: the top-k arguments
+    const float *bias;
+    float *logits_out;
+    int *topk_idx;
+    float *topk_w;
+    int k, score, renorm, splits;
 };
 
 __host__ __device__ inline int rc_stage_bytes(int n_pad) { return RC_A_BYTES + n_pad * RC_BK * 2; }
@@ -194,7 +209,14 @@ __host__ __device__ inline uint32_t rc_tmem_cols(int n_pad) {
     return c;
 }
 
-__global__ void __launch_bounds__(RC_THREADS)
+// kCluster = false: the CTA writes its fp32 partial to part[split][e][t] and a
+// second kernel reduces.  kCluster = true: the `splits` CTAs of one m-tile
+// form a cluster; each stages its partial in its own shared memory (the
+// operand ring, free once the MMAs are done), and after a cluster barrier
+// CTA r sums the partials of its share of the 128 tokens from all CTAs
+// through distributed shared memory, in split order, then selects the top-k.
+template <bool kCluster>
+__global__ void __launch_bounds__(kCluster ? RC_CL_THREADS : RC_THREADS)
 router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, const RouterTcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -210,7 +232,7 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * RC_BM;
-    const int split = blockIdx.y;
+    const int split = kCluster ? (int)cluster_ctarank() : (int)blockIdx.y;
     const int kb0 = split * p.kps;
     const int kb1 = min(p.nk, kb0 + p.kps);
     const uint32_t ncols = rc_tmem_cols(p.n_pad);
@@ -281,11 +303,27 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
             volatile int local_abort = 0;
             mbar_wait_bounded(done, 0u, &local_abort);
         }
-    } else {
+    } else if (warp < 6) {
         const int q = warp & 3;
         const bool got = mbar_wait_bounded(done, 0u, abort_flag);
         if (__all_sync(0xffffffffu, got) && !*abort_flag) {
             tc_fence_after();
+            if (kCluster) {
+                // this CTA's partial into its own shared memory, [token][e]
+                // with an odd row stride (conflict-free for these writes and
+                // for the peers' row reads)
+                float *sp = reinterpret_cast<float *>(ring);
+                const int ld = p.n_pad + 1;
+                const int tl = q * 32 + lane;
+                for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < p.n_pad) sp[tl * ld + c0 + i] = __uint_as_float(v[i]);
+                }
+            } else {
             // partials are token-minor, part[split][e][t]: for each expert
             // column the warp's 32 lanes (32 consecutive tokens) write one
             // contiguous 128-byte line
@@ -301,6 +339,7 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                         if (c0 + i < p.E) pcol[(size_t)(c0 + i) * p.T] = __uint_as_float(v[i]);
                 }
             }
+            }
         }
     }
 
@@ -313,6 +352,41 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, ncols);
+    }
+    if (kCluster) {
+        cluster_sync();  // every CTA's partial is in its shared memory
+        const int S = p.splits;
+        const int per = (RC_BM + S - 1) / S;
+        const int tl0 = split * per, tl1 = min(RC_BM, tl0 + per);
+        const int ld = p.n_pad + 1;
+        const uint32_t sp_local = smem_u32(ring);
+        // per-warp key row after the partial buffer
+        float *key = reinterpret_cast<float *>(ring) + (size_t)RC_BM * ld + warp * p.E;
+        const int nwarps = (int)(blockDim.x >> 5);
+        for (int tl = tl0 + warp; tl < tl1; tl += nwarps) {
+            const int t = m0 + tl;
+            if (t >= p.T) break;
+            for (int e = lane; e < p.E; e += 32) {
+                const uint32_t off = (uint32_t)((tl * ld + e) * sizeof(float));
+                // all splits' loads in flight together, then the sum in split order
+                float part[kRouterMaxSplits];
+#pragma unroll
+                for (int sidx = 0; sidx < kRouterMaxSplits; ++sidx)
+                    if (sidx < S) part[sidx] = ld_shared_cluster_f32(mapa_shared(sp_local + off, (uint32_t)sidx));
+                float v = 0.f;
+#pragma unroll
+                for (int sidx = 0; sidx < kRouterMaxSplits; ++sidx)
+                    if (sidx < S) v += part[sidx];
+                if (p.bias) v += p.bias[e];
+                key[e] = v;
+                if (p.logits_out) p.logits_out[(size_t)t * p.E + e] = v;
+            }
+            __syncwarp();
+            warp_topk_weights(key, p.E, p.k, p.score, p.renorm, t, p.topk_idx, p.topk_w, p.status,
+                              lane);
+            __syncwarp();
+        }
+        cluster_sync();  // the peers are done reading this CTA's partial
     }
 }
 
@@ -379,9 +453,47 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     splits = (nk + kps - 1) / kps;  // no empty split
     RouterTcParams p{T, E, n_pad, nk, kps, part, status};
     const size_t smem = rc_smem_bytes(n_pad);
-    cudaError_t err = ensure_smem((const void *)router_logits_tc_kernel, smem);
+    cudaError_t err;
+    {
+        // one launch: clusters of `splits` CTAs reduce through shared memory.
+        // The partials and the key rows reuse the operand ring.
+        const size_t need = sizeof(float) * ((size_t)RC_BM * (n_pad + 1) + (RC_CL_THREADS / 32) * (size_t)E);
+        const char *sel = getenv("MOE_ROUTER_KERNEL");
+        const bool two = sel && strcmp(sel, "split") == 0;
+        if (!two && need <= (size_t)RC_STAGES * rc_stage_bytes(n_pad)) {
+            p.bias = bias;
+            p.logits_out = logits_out;
+            p.topk_idx = topk_idx;
+            p.topk_w = topk_w;
+            p.k = k;
+            p.score = score;
+            p.renorm = renorm;
+            p.splits = splits;
+            err = ensure_smem((const void *)router_logits_tc_kernel<true>, smem);
+            if (err != cudaSuccess) return err;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(m_tiles, splits);
+            cfg.blockDim = dim3(RC_CL_THREADS);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = splits;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&cfg, router_logits_tc_kernel<true>, tm_x, tm_w, p);
+            if (err == cudaSuccess) {
+                count_launch();
+                return cudaSuccess;
+            }
+            cudaGetLastError();  // cluster refused: the two-kernel form below
+        }
+    }
+    err = ensure_smem((const void *)router_logits_tc_kernel<false>, smem);
     if (err != cudaSuccess) return err;
-    router_logits_tc_kernel<<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
+    router_logits_tc_kernel<false><<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t rsmem = sizeof(float) * RR_TOKENS * (size_t)(E + 1);

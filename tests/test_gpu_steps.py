@@ -90,6 +90,36 @@ def test_route_workload_shapes(moe, name):
     np.testing.assert_allclose(gw.cpu().numpy()[same_order], ow[same_order], rtol=1e-4, atol=1e-6)
 
 
+@pytest.mark.parametrize("T,D,E,k,score", [(1000, 2048, 64, 6, "softmax"), (300, 7168, 256, 8, "sigmoid"),
+                                           (77, 512, 8, 2, "softmax"), (4096, 2048, 64, 6, "softmax")])
+def test_route_one_kernel_equals_two(moe, T, D, E, k, score, monkeypatch):
+    """bf16 router: one cluster launch (split-D partials summed through
+    distributed shared memory) and the two-kernel form (partials through the
+    workspace) add the same partials in the same order: bitwise equal."""
+    g = torch.Generator(device="cuda").manual_seed(T + E)
+    x = torch.randn((T, D), generator=g, device="cuda").to(torch.bfloat16)
+    wg = (torch.randn((E, D), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    bias = torch.randn((E,), generator=g, device="cuda") * 0.1
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
+                     score=moe.MOE_SCORE_SOFTMAX if score == "softmax" else moe.MOE_SCORE_SIGMOID)
+    ws = moe.alloc_workspace(cfg)
+    outs = {}
+    for mode in ("cluster", "split"):
+        if mode == "split":
+            monkeypatch.setenv("MOE_ROUTER_KERNEL", "split")
+        logits = torch.full((T, E), float("nan"), device="cuda")
+        gidx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+        gw = torch.full((T, k), float("nan"), device="cuda")
+        n0 = moe.kernel_launches()
+        moe.moe_route_topk(cfg, x, wg, bias, logits, gidx, gw, ws)
+        n = moe.kernel_launches() - n0
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        outs[mode] = (logits, gidx, gw, n)
+    assert outs["cluster"][3] == 1 and outs["split"][3] == 2
+    for a, b in zip(outs["cluster"][:3], outs["split"][:3]):
+        assert torch.equal(a, b)
+
+
 def test_route_nan_logit_sets_status(moe):
     T, D, E, k = 64, 64, 16, 4
     x = torch.randn(T, D, device="cuda")
@@ -250,9 +280,13 @@ def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monk
         pytest.skip("one fp32 implementation")
     monkeypatch.setenv("MOE_GROUPED_KERNEL", kernel)
     lay, xp, w1, w3, w2, h, y = _grouped_case(moe, dt, T, E_local, k, D, H, align, seed=T + H)
+    _assert_grouped_parity(lay, xp, w1, w3, w2, h, y, dt == "bf16")
+
+
+def _assert_grouped_parity(lay, xp, w1, w3, w2, h, y, rb):
     H_ = moe_inputs.host_array
     seg, cnt = lay["seg_offsets"], lay["tokens_per_expert"]
-    rb = dt == "bf16"
+    E_local = len(cnt)
     oh = oracle.grouped_gemm1_swiglu(H_(xp), seg, cnt, list(H_(w1)), list(H_(w3)), round_h=rb)
     filled = lay["token_of_row"] >= 0
     gh = to_f64(h)
@@ -273,7 +307,7 @@ def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monk
                 continue
             aw2 = np.abs(w2h[i])
             bound = dh[rows] @ aw2.T + 2.0 ** -20 * (np.abs(oh[rows]) @ aw2.T) + 1e-30
-            assert (np.abs(gy[rows] - oy[rows]) <= bound).all()
+            assert (np.abs(gy[rows] - oy[rows]) <= bound).all(), f"expert {i}"
         assert rel_err(gy[filled], oy[filled]) < 1e-2
     else:
         assert rel_err(gh[filled], oh[filled]) < 1e-4
@@ -283,6 +317,37 @@ def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monk
     if tail.any():
         tt = torch.from_numpy(tail).cuda()
         assert torch.isnan(h.float()[tt]).all() and torch.isnan(y[tt]).all()
+
+
+@pytest.mark.parametrize("kernel", ["pair", "pair2", "single"])
+def test_grouped_tile_shapes(moe, kernel, monkeypatch):
+    """Every tile shape the grouped kernels choose from, by exact expert
+    counts: transposed tail tiles (1..128 valid rows, N = 32..128), full
+    tiles with partial rows (129..255), several tiles per expert, empty
+    experts; H and D with N tails."""
+    counts = [1, 31, 32, 33, 0, 64, 96, 127, 128, 129, 200, 255, 256, 257, 384, 0, 500, 17]
+    E_local, D, H = len(counts), 320, 192
+    idx = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])[:, None]
+    idx = idx[np.random.default_rng(3).permutation(len(idx))]
+    T = len(idx)
+    lay = oracle.layout(idx, E_local, 0, E_local, oracle.CONTIGUOUS, 128)
+    assert lay["tokens_per_expert"].tolist() == counts
+    monkeypatch.setenv("MOE_GROUPED_KERNEL", kernel)
+    ra = lay["rows_alloc"]
+    g = torch.Generator(device="cuda").manual_seed(11)
+    xp = torch.randn((ra, D), generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn((E_local, H, D), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    w3 = (torch.randn((E_local, H, D), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn((E_local, D, H), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    cfg = moe.Config(T=T, D=D, H_local=H, E=E_local, k=1, align_m=128, dtype=moe.MOE_BF16)
+    assert moe.rows_alloc(cfg) == ra
+    ws = moe.alloc_workspace(cfg)
+    h = torch.full((ra, H), float("nan"), device="cuda").to(torch.bfloat16)
+    y = torch.full((ra, D), float("nan"), device="cuda")
+    moe.moe_grouped_swiglu(cfg, xp, _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"]),
+                           w1, w3, w2, h, y, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    _assert_grouped_parity(lay, xp, w1, w3, w2, h, y, True)
 
 
 def _grouped_run(moe, cfg, lay, xp, w1, w3, w2, ws):
