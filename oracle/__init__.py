@@ -83,6 +83,8 @@ def _load():
             lib.oracle_router_logits.argtypes = [I, I, I, P, I, P, I, P, P, I]
             lib.oracle_topk.restype = I
             lib.oracle_topk.argtypes = [I, I, I, P, P]
+            lib.oracle_topk_grouped.restype = I
+            lib.oracle_topk_grouped.argtypes = [I, I, I, I, I, P, P]
             lib.oracle_topk_weights.argtypes = [I, I, I, P, P, I, I, P]
             lib.oracle_rows_alloc.restype = L
             lib.oracle_rows_alloc.argtypes = [I, I, I, I, I, I]
@@ -157,12 +159,20 @@ def router_logits(x: np.ndarray, wg: np.ndarray, bias=None, nthreads=None) -> np
     return out
 
 
-def topk(logits_f32: np.ndarray, k: int):
-    """(topk_idx int32 [T,k], status) from fp32 keys; ties -> lower index."""
+def topk(logits_f32: np.ndarray, k: int, n_group: int = 0, topk_group: int = 0):
+    """(topk_idx int32 [T,k], status) from fp32 keys; ties -> lower index.
+
+    With n_group > 1: group-limited selection (only experts of the
+    topk_group best groups; a group scores the fp32 sum of its k/topk_group
+    best keys).
+    """
     l = _c(logits_f32, np.float32)
     T, E = l.shape
     idx = np.empty((T, k), np.int32)
-    st = _load().oracle_topk(T, E, k, _p(l), _p(idx))
+    if n_group and n_group > 1:
+        st = _load().oracle_topk_grouped(T, E, k, n_group, topk_group, _p(l), _p(idx))
+    else:
+        st = _load().oracle_topk(T, E, k, _p(l), _p(idx))
     return idx, st
 
 
@@ -176,7 +186,8 @@ def topk_weights(logits_f32: np.ndarray, idx: np.ndarray, score: int, renorm: bo
     return w
 
 
-def route(x, wg, bias, k: int, score: int, renorm: bool, nthreads=None):
+def route(x, wg, bias, k: int, score: int, renorm: bool, nthreads=None, n_group: int = 0,
+          topk_group: int = 0):
     """Whole router on the oracle's own logits.
 
     Returns (logits_f64, keys_f32, topk_idx, topk_w, status); the selection
@@ -184,7 +195,7 @@ def route(x, wg, bias, k: int, score: int, renorm: bool, nthreads=None):
     """
     l64 = router_logits(x, wg, bias, nthreads)
     keys = l64.astype(np.float32)
-    idx, st = topk(keys, k)
+    idx, st = topk(keys, k, n_group, topk_group)
     w = topk_weights(keys, idx, score, renorm)
     return l64, keys, idx, w, st
 

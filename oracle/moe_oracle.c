@@ -18,7 +18,9 @@
  *           tokens_per_expert, permute, grouped fc1 -> act -> fc2,
  *           unpermute with top-k weighted reduce), section 2 (layout
  *           contract: expert-contiguous segments aligned to the GEMM M tile),
- *           section 5 (permute / unpermute symmetry).
+ *           section 3 (DeepSeek-V3-style group-limited routing: a token may
+ *           only reach topk_group expert groups), section 5 (permute /
+ *           unpermute symmetry).
  *   [ETP]   "Expert Tensor Parallel design" (HyperParallel issue 104),
  *           section 4.3 (GroupedExperts w1/w3 [E,H,D], w2 [E,D,H]; shards on
  *           dim 1 and dim 2).
@@ -219,6 +221,91 @@ int oracle_topk(int T, int E, int k, const float *logits, int32_t *topk_idx)
     free(taken);
     return status;
 }
+
+/*
+ * Group-limited top-k ([EP] section 3: DeepSeek-V3-style group-limited
+ * routing splits the experts into groups and lets each token reach only
+ * topk_group of them, which bounds the all-to-all fan-out).
+ *
+ * The pages do not say how a group is scored.  Reading taken here: the E
+ * experts form n_group equal groups of consecutive indices; a group's score
+ * is the sum of its m = k / topk_group best keys, taken in selection order
+ * and added in fp32 (the precision in which the kernel takes the same
+ * decision); groups are ranked by that score, ties to the lower group index
+ * and NaN last, as for keys; the top-k is then the plain selection over the
+ * experts of the topk_group best groups.  n_group <= 1 is plain top-k.
+ * Returns ORC_BAD_ARG for an unusable grouping, ORC_BAD_ROUTING on a NaN key.
+ */
+static int score_before(float sa, int a, float sb, int b)
+{
+    return key_before(sa, a, sb, b);
+}
+
+int oracle_topk_grouped(int T, int E, int k, int n_group, int topk_group, const float *logits,
+                        int32_t *topk_idx)
+{
+    if (n_group <= 1) return oracle_topk(T, E, k, logits, topk_idx);
+    if (E % n_group != 0 || topk_group < 1 || topk_group > n_group || k < topk_group ||
+        k > topk_group * (E / n_group) || k > E)
+        return ORC_BAD_ARG;
+    const int gs = E / n_group, m = k / topk_group;
+    int status = ORC_OK;
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    unsigned char *gsel = (unsigned char *)malloc((size_t)n_group);
+    float *gscore = (float *)malloc(sizeof(float) * (size_t)n_group);
+    if (!taken || !gsel || !gscore) {
+        free(taken);
+        free(gsel);
+        free(gscore);
+        return ORC_BAD_ARG;
+    }
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        for (int e = 0; e < E; ++e)
+            if (isnan(l[e])) status = ORC_BAD_ROUTING;
+        /* group scores */
+        memset(taken, 0, (size_t)E);
+        for (int g = 0; g < n_group; ++g) {
+            float sum = 0.f;
+            for (int i = 0; i < m; ++i) {
+                int best = -1;
+                for (int e = g * gs; e < (g + 1) * gs; ++e) {
+                    if (taken[e]) continue;
+                    if (best < 0 || key_before(l[e], e, l[best], best)) best = e;
+                }
+                taken[best] = 1;
+                sum += l[best];
+            }
+            gscore[g] = sum;
+        }
+        /* the topk_group best groups */
+        memset(gsel, 0, (size_t)n_group);
+        for (int r = 0; r < topk_group; ++r) {
+            int best = -1;
+            for (int g = 0; g < n_group; ++g) {
+                if (gsel[g]) continue;
+                if (best < 0 || score_before(gscore[g], g, gscore[best], best)) best = g;
+            }
+            gsel[best] = 1;
+        }
+        /* plain selection restricted to the chosen groups */
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e] || !gsel[e / gs]) continue;
+                if (best < 0 || key_before(l[e], e, l[best], best)) best = e;
+            }
+            taken[best] = 1;
+            topk_idx[(size_t)t * k + j] = best;
+        }
+    }
+    free(taken);
+    free(gsel);
+    free(gscore);
+    return status;
+}
+
 
 /*
  * Routing weights for the selected experts ([EP] section 1: "top-k +

@@ -115,6 +115,78 @@ def test_topk_nan_and_signed_zero():
     assert list(idx[0]) == [4, 0, 3, 2, 1]       # +0 and -0 tie -> lower index first
 
 
+# ---------------------------------------------------------------- group-limited top-k
+# Reading of the "Expert Parallelism (EP)" page, section 3 (DeepSeek-V3 style
+# group-limited routing): n_group equal groups of consecutive experts; a group
+# scores the fp32 sum of its m = k / topk_group best keys; the topk_group best
+# groups (ties to the lower group) are the only ones a token may use.
+
+def test_group_limited_topk_hand_example():
+    # keys of 8 experts, groups {0,1} {2,3} {4,5} {6,7}, k = 4, topk_group = 2,
+    # so m = 2: group scores 9+0=9, 5+5=10, 8+1=9, 7+7=14 -> groups 3 and 1;
+    # the top-4 of experts {2,3,6,7} by (key desc, index asc) is 6, 7, 2, 3.
+    # Plain top-4 would be 0, 4, 6, 7.
+    keys = np.array([[9, 0, 5, 5, 8, 1, 7, 7]], np.float32)
+    idx, st = oracle.topk(keys, 4, n_group=4, topk_group=2)
+    assert st == oracle.OK and idx.tolist() == [[6, 7, 2, 3]]
+    assert oracle.topk(keys, 4)[0].tolist() == [[0, 4, 6, 7]]
+    # tied group scores go to the lower group: m = 1 gives 9, 5, 9, 7; with
+    # topk_group = 1 group 0 wins the tie with group 2
+    idx, _ = oracle.topk(keys, 1, n_group=4, topk_group=1)
+    assert idx.tolist() == [[0]]
+    keys2 = np.array([[0, 9, 5, 5, 9, 1, 7, 7]], np.float32)
+    idx, _ = oracle.topk(keys2, 2, n_group=4, topk_group=2)   # m = 1: 9, 5, 9, 7 -> groups 0, 2
+    assert idx.tolist() == [[1, 4]]
+
+
+def _grouped_topk_by_sorting(keys, k, G, tg):
+    """Independent statement of the reading with Python sorts."""
+    T, E = keys.shape
+    gs, m = E // G, k // tg
+    out = np.empty((T, k), np.int32)
+    for t in range(T):
+        sc = []
+        for g in range(G):
+            best = sorted(range(g * gs, (g + 1) * gs), key=lambda e: (-keys[t, e], e))[:m]
+            s32 = np.float32(0)
+            for e in best:
+                s32 = np.float32(s32 + keys[t, e])
+            sc.append((-float(s32), g))
+        chosen = {g for _, g in sorted(sc)[:tg]}
+        allowed = [e for e in range(E) if e // gs in chosen]
+        out[t] = sorted(allowed, key=lambda e: (-keys[t, e], e))[:k]
+    return out
+
+
+@pytest.mark.parametrize("E,G,tg,k", [(8, 4, 2, 4), (16, 4, 2, 2), (32, 8, 4, 8), (24, 3, 1, 5),
+                                      (64, 8, 3, 7)])
+def test_group_limited_topk_matches_sorting(E, G, tg, k):
+    rng = np.random.default_rng(E * 100 + k)
+    keys = rng.integers(-4, 5, size=(300, E)).astype(np.float32)   # many ties
+    keys[:100] = rng.standard_normal((100, E)).astype(np.float32)
+    idx, st = oracle.topk(keys, k, n_group=G, topk_group=tg)
+    assert st == oracle.OK
+    assert np.array_equal(idx, _grouped_topk_by_sorting(keys, k, G, tg))
+
+
+def test_group_limited_topk_reduces_to_plain():
+    rng = np.random.default_rng(7)
+    keys = rng.integers(-3, 4, size=(200, 32)).astype(np.float32)
+    plain, _ = oracle.topk(keys, 6)
+    assert np.array_equal(oracle.topk(keys, 6, n_group=1, topk_group=1)[0], plain)
+    assert np.array_equal(oracle.topk(keys, 6, n_group=4, topk_group=4)[0], plain)   # every group allowed
+
+
+def test_group_limited_topk_rejects_bad_groupings():
+    keys = np.zeros((2, 12), np.float32)
+    assert oracle.topk(keys, 2, n_group=5, topk_group=2)[1] == oracle.BAD_ARG    # 12 % 5
+    assert oracle.topk(keys, 1, n_group=4, topk_group=2)[1] == oracle.BAD_ARG    # k < topk_group
+    assert oracle.topk(keys, 7, n_group=4, topk_group=2)[1] == oracle.BAD_ARG    # 7 > 2 groups x 3
+    nan = keys.copy()
+    nan[1, 3] = np.nan
+    assert oracle.topk(nan, 2, n_group=4, topk_group=2)[1] == oracle.BAD_ROUTING
+
+
 def test_scores_closed_forms():
     l = np.array([[0.0, math.log(3.0)]], np.float32)
     idx, _ = oracle.topk(l, 2)
