@@ -85,12 +85,22 @@ typedef enum { MOE_LAYOUT_CONTIGUOUS = 0, MOE_LAYOUT_MASKED = 1 } moe_layout;
  *            grouped GEMM is fastest when align_m is a multiple of 128)
  *   capacity masked layout: rows reserved per local expert (segment i
  *            starts at i*capacity); ignored for the contiguous layout
+ *   n_group, topk_group  group-limited routing ("Expert Parallelism (EP)",
+ *            section 3, DeepSeek-V3 style): with n_group > 1 the E experts
+ *            form n_group equal groups of consecutive indices and a token
+ *            may only choose experts of its topk_group best groups; a group
+ *            scores the fp32 sum of its k/topk_group largest keys (added in
+ *            selection order), ties to the lower group.  Requires
+ *            E % n_group == 0, n_group <= 32, 1 <= topk_group <= n_group and
+ *            topk_group <= k <= topk_group * E / n_group.  n_group 0 or 1:
+ *            plain top-k (topk_group ignored).
  */
 typedef struct {
     int32_t T, D, H_local, E, k;
     int32_t e_first, E_local;
     int32_t dtype, score, renorm, layout;
     int32_t align_m, capacity;
+    int32_t n_group, topk_group;
 } moe_config;
 
 /* Human-readable name of a status code (static storage, never NULL). */

@@ -62,6 +62,8 @@ class Workload:
     zipf_empty: int = 4          # lowest-ranked experts pushed to zero load
     tp: int = 1                  # H-shards used by the shard-equivalence check
     ep: int = 1                  # expert ranges used by the shard check
+    n_group: int = 0             # > 1: group-limited routing over n_group groups
+    topk_group: int = 0          # groups a token may use
 
     def scaled(self, **kw) -> "Workload":
         return replace(self, **kw)

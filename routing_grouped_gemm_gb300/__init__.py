@@ -43,7 +43,7 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "T", "D", "H_local", "E", "k", "e_first", "E_local", "dtype", "score", "renorm",
-        "layout", "align_m", "capacity")]
+        "layout", "align_m", "capacity", "n_group", "topk_group")]
 
 
 def _load() -> ctypes.CDLL:
@@ -100,12 +100,14 @@ class Config:
     layout: int = MOE_LAYOUT_CONTIGUOUS
     align_m: int = 128
     capacity: int = 0
+    n_group: int = 0           # > 1: group-limited routing over n_group expert groups
+    topk_group: int = 0
 
     def c(self) -> moe_config:
         el = self.E - self.e_first if self.E_local < 0 else self.E_local
         return moe_config(self.T, self.D, self.H_local, self.E, self.k, self.e_first, el,
                           self.dtype, self.score, int(bool(self.renorm)), self.layout,
-                          self.align_m, self.capacity)
+                          self.align_m, self.capacity, self.n_group, self.topk_group)
 
     @property
     def e_local(self) -> int:

@@ -40,10 +40,12 @@ constexpr int kRouterTcMaxE = 256;
 #endif
 constexpr int kRouterMaxSplits = MOE_ROUTER_SPLITS;
 int64_t router_scratch_floats(int T, int E, int is_bf16);
+// n_group > 1: group-limited selection (validated by the caller).
 cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
                                int *topk_idx, float *topk_w, int T, int D, int E, int k,
-                               int score, int renorm, int is_bf16, float *scratch,
-                               int64_t scratch_floats, int *status, cudaStream_t stream);
+                               int score, int renorm, int n_group, int topk_group, int is_bf16,
+                               float *scratch, int64_t scratch_floats, int *status,
+                               cudaStream_t stream);
 
 // Scratch ints needed by launch_permute: blocks of 256 tokens x E, twice.
 int64_t permute_scratch_ints(int T, int E);

@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 10100;  // 1.1.0
+constexpr int32_t kAbiVersion = 10200;  // 1.2.0
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int64_t kAlign = 256;
@@ -62,6 +62,15 @@ moe_status validate(const moe_config *c) {
     if (c->layout == MOE_LAYOUT_CONTIGUOUS && (c->align_m < 1 || c->align_m > (1 << 16)))
         return arg_fail("align_m must be in 1..65536");
     if (c->layout == MOE_LAYOUT_MASKED && c->capacity < 0) return arg_fail("capacity < 0");
+    if (c->n_group < 0) return arg_fail("n_group < 0");
+    if (c->n_group > 1) {
+        if (c->n_group > 32 || c->E % c->n_group != 0)
+            return arg_fail("n_group must divide E and be at most 32");
+        if (c->topk_group < 1 || c->topk_group > c->n_group || c->k < c->topk_group ||
+            c->k > c->topk_group * (c->E / c->n_group))
+            return arg_fail("topk_group must satisfy 1 <= topk_group <= n_group and "
+                            "topk_group <= k <= topk_group * E / n_group");
+    }
     if ((int64_t)c->T * c->k >= (int64_t)1 << 31) return arg_fail("T*k too large");
     if (rows_alloc_of(c) >= (int64_t)1 << 31) return arg_fail("permuted rows exceed 2^31");
     return MOE_OK;
@@ -162,7 +171,9 @@ moe_status do_route(const moe_config *c, const void *x, const void *wg, const fl
                     float *logits_out, int32_t *topk_idx, float *topk_w, const StepWs &w,
                     cudaStream_t s) {
     cudaError_t e = moe::launch_router_topk(x, wg, bias, logits_out, topk_idx, topk_w, c->T, c->D,
-                                            c->E, c->k, c->score, c->renorm, c->dtype == MOE_BF16,
+                                            c->E, c->k, c->score, c->renorm,
+                                            c->n_group > 1 ? c->n_group : 0, c->topk_group,
+                                            c->dtype == MOE_BF16,
                                             w.router_part, w.router_floats, &w.status->flags, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_topk");
 }

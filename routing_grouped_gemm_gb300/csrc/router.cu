@@ -46,12 +46,63 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 // softmax over all E (or sigmoid) of the chosen keys, divided by their sum
 // when renormalising.  Lane i owns experts i, i+32, ... (E <= 1024); the
 // winner of round j is kept by lane j, which computes and writes slot j.
-__device__ void warp_topk_weights(const float *l, int E, int k, int score, int renorm, int t,
+//
+// Group-limited routing (n_group > 1; page "Expert Parallelism (EP)",
+// section 3): first each of the n_group groups of E/n_group consecutive
+// experts is scored by the fp32 sum of its m = k/topk_group largest keys
+// (added in selection order), the topk_group best groups are kept (ties to
+// the lower group, NaN last), and the k rounds only consider their experts.
+
+// Warp-wide arg-max in selection order; every lane ends with the winner.
+__device__ __forceinline__ void warp_argmax(float &bv, int &be) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (oe >= 0 && (be < 0 || key_before(ov, oe, bv, be))) { bv = ov; be = oe; }
+    }
+}
+
+__device__ void warp_topk_weights(const float *l, int E, int k, int score, int renorm,
+                                  int n_group, int topk_group, int t,
                                   int *__restrict__ topk_idx, float *__restrict__ topk_w,
                                   int *status, int lane) {
     bool any_nan = false;
     for (int e = lane; e < E; e += 32) any_nan |= (l[e] != l[e]);
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) raise_flag(status, FLAG_BAD_ROUTING);
+
+    const bool grouped = n_group > 1;
+    const int gsz = grouped ? E / n_group : E;
+    uint32_t allowed = 0xffffffffu;  // bit g: group g may be chosen
+    if (grouped) {
+        const int m = k / topk_group;
+        float my_score = 0.f;  // lane g: score of group g
+        for (int g = 0; g < n_group; ++g) {
+            const int e0 = g * gsz;
+            uint32_t gt = 0;  // bit q: expert e0 + lane + 32 q already counted
+            float sum = 0.f;
+            for (int i = 0; i < m; ++i) {
+                float bv = 0.f;
+                int be = -1;
+                for (int q = 0, e = e0 + lane; e < e0 + gsz; ++q, e += 32) {
+                    if (gt & (1u << q)) continue;
+                    if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
+                }
+                warp_argmax(bv, be);
+                if (be >= 0 && ((be - e0) & 31) == lane) gt |= 1u << ((be - e0) >> 5);
+                sum += bv;
+            }
+            if (lane == g) my_score = sum;
+        }
+        allowed = 0;
+        for (int r = 0; r < topk_group; ++r) {
+            float bv = 0.f;
+            int be = -1;
+            if (lane < n_group && !(allowed & (1u << lane))) { bv = my_score; be = lane; }
+            warp_argmax(bv, be);
+            if (be >= 0) allowed |= 1u << be;
+        }
+    }
 
     uint32_t taken = 0;  // bit q: expert lane + 32 q already chosen
     int my_e = -1;       // slot `lane`'s expert and key (lanes < k)
@@ -61,17 +112,23 @@ __device__ void warp_topk_weights(const float *l, int E, int k, int score, int r
         int be = -1;
         for (int q = 0, e = lane; e < E; ++q, e += 32) {
             if (taken & (1u << q)) continue;
+            if (grouped && !((allowed >> (e / gsz)) & 1u)) continue;
             if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (oe >= 0 && (be < 0 || key_before(ov, oe, bv, be))) { bv = ov; be = oe; }
-        }
+        warp_argmax(bv, be);
         if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
         if (lane == j) { my_e = be; my_v = bv; }
-        if (j == 0) top = bv;  // the largest key (unless NaN)
+        if (j == 0) top = bv;  // the largest chosen key (unless NaN)
+    }
+    if (grouped && score == 0 && !renorm) {
+        // softmax over all E: shift by the largest key of all, which may lie
+        // in a group that was not chosen
+        float bv = 0.f;
+        int be = -1;
+        for (int e = lane; e < E; e += 32)
+            if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
+        warp_argmax(bv, be);
+        top = bv;
     }
 
     float p = 0.f;
@@ -100,7 +157,7 @@ __global__ void __launch_bounds__(RT_THREADS)
 router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const float *__restrict__ bias,
                    float *__restrict__ logits_out, int *__restrict__ topk_idx,
                    float *__restrict__ topk_w, int Tn, int D, int E, int k, int score, int renorm,
-                   int *status) {
+                   int n_group, int topk_group, int *status) {
     extern __shared__ float smem[];
     float *s_logit = smem;                              // [RT_TOKENS][E]
     float *s_x = s_logit + RT_TOKENS * E;               // [RT_BK][SX_LD]
@@ -168,7 +225,8 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
     for (int tt = warp; tt < RT_TOKENS; tt += RT_THREADS / 32) {
         const int t = t0 + tt;
         if (t >= Tn) break;
-        warp_topk_weights(s_logit + tt * E, E, k, score, renorm, t, topk_idx, topk_w, status, lane);
+        warp_topk_weights(s_logit + tt * E, E, k, score, renorm, n_group, topk_group, t, topk_idx,
+                          topk_w, status, lane);
     }
 }
 
@@ -195,6 +253,7 @@ struct RouterTcParams {
     int *topk_idx;
     float *topk_w;
     int k, score, renorm, splits;
+    int n_group, topk_group;
 };
 
 __host__ __device__ inline int rc_stage_bytes(int n_pad) { return RC_A_BYTES + n_pad * RC_BK * 2; }
@@ -382,8 +441,8 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                 if (p.logits_out) p.logits_out[(size_t)t * p.E + e] = v;
             }
             __syncwarp();
-            warp_topk_weights(key, p.E, p.k, p.score, p.renorm, t, p.topk_idx, p.topk_w, p.status,
-                              lane);
+            warp_topk_weights(key, p.E, p.k, p.score, p.renorm, p.n_group, p.topk_group, t,
+                              p.topk_idx, p.topk_w, p.status, lane);
             __syncwarp();
         }
         cluster_sync();  // the peers are done reading this CTA's partial
@@ -401,7 +460,7 @@ __global__ void __launch_bounds__(RR_THREADS)
 router_reduce_topk_kernel(const float *__restrict__ part, int splits, const float *__restrict__ bias,
                           float *__restrict__ logits_out, int *__restrict__ topk_idx,
                           float *__restrict__ topk_w, int Tn, int E, int k, int score, int renorm,
-                          int *status) {
+                          int n_group, int topk_group, int *status) {
     extern __shared__ float s_key[];  // [RR_TOKENS][E + 1]
     const int ld = E + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -422,7 +481,8 @@ router_reduce_topk_kernel(const float *__restrict__ part, int splits, const floa
         const float *l = s_key + tt * ld;
         if (logits_out)
             for (int e = lane; e < E; e += 32) logits_out[(size_t)tok * E + e] = l[e];
-        warp_topk_weights(l, E, k, score, renorm, tok, topk_idx, topk_w, status, lane);
+        warp_topk_weights(l, E, k, score, renorm, n_group, topk_group, tok, topk_idx, topk_w, status,
+                          lane);
     }
 }
 
@@ -437,7 +497,8 @@ namespace {
 
 cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, float *logits_out,
                              int *topk_idx, float *topk_w, int T, int D, int E, int k, int score,
-                             int renorm, float *part, int *status, cudaStream_t stream) {
+                             int renorm, int n_group, int topk_group, float *part, int *status,
+                             cudaStream_t stream) {
     const int n_pad = (E + 15) / 16 * 16;
     CUtensorMap tm_x, tm_w;
     if (!make_tmap_2d(&tm_x, x, D, T, RC_BM) || !make_tmap_2d(&tm_w, wg, D, E, n_pad))
@@ -469,6 +530,8 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
             p.score = score;
             p.renorm = renorm;
             p.splits = splits;
+            p.n_group = n_group;
+            p.topk_group = topk_group;
             err = ensure_smem((const void *)router_logits_tc_kernel<true>, smem);
             if (err != cudaSuccess) return err;
             cudaLaunchConfig_t cfg = {};
@@ -498,7 +561,8 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t rsmem = sizeof(float) * RR_TOKENS * (size_t)(E + 1);
     router_reduce_topk_kernel<<<(T + RR_TOKENS - 1) / RR_TOKENS, RR_THREADS, rsmem, stream>>>(
-        part, splits, bias, logits_out, topk_idx, topk_w, T, E, k, score, renorm, status);
+        part, splits, bias, logits_out, topk_idx, topk_w, T, E, k, score, renorm, n_group, topk_group,
+        status);
     count_launch();
     return cudaGetLastError();
 }
@@ -507,13 +571,14 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
 
 cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias, float *logits_out,
                                int *topk_idx, float *topk_w, int T, int D, int E, int k,
-                               int score, int renorm, int is_bf16, float *scratch,
-                               int64_t scratch_floats, int *status, cudaStream_t stream) {
+                               int score, int renorm, int n_group, int topk_group, int is_bf16,
+                               float *scratch, int64_t scratch_floats, int *status,
+                               cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     if (is_bf16 && E <= kRouterTcMaxE && scratch &&
         scratch_floats >= router_scratch_floats(T, E, is_bf16))
         return launch_router_tc(x, wg, bias, logits_out, topk_idx, topk_w, T, D, E, k, score,
-                                renorm, scratch, status, stream);
+                                renorm, n_group, topk_group, scratch, status, stream);
     const size_t smem = sizeof(float) * ((size_t)RT_TOKENS * E + RT_BK * SX_LD + RT_BK * SW_LD);
     const dim3 grid((T + RT_TOKENS - 1) / RT_TOKENS);
     cudaError_t err;
@@ -523,14 +588,14 @@ cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias,
         if (err != cudaSuccess) return err;
         kern<<<grid, RT_THREADS, smem, stream>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)wg,
                                                  bias, logits_out, topk_idx, topk_w, T, D, E, k,
-                                                 score, renorm, status);
+                                                 score, renorm, n_group, topk_group, status);
     } else {
         auto kern = router_topk_kernel<float>;
         err = ensure_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
         kern<<<grid, RT_THREADS, smem, stream>>>((const float *)x, (const float *)wg, bias,
                                                  logits_out, topk_idx, topk_w, T, D, E, k, score,
-                                                 renorm, status);
+                                                 renorm, n_group, topk_group, status);
     }
     count_launch();
     return cudaGetLastError();

@@ -19,7 +19,8 @@ def cfg_for(moe, w, **over):
               score=moe.MOE_SCORE_SOFTMAX if w.score == "softmax" else moe.MOE_SCORE_SIGMOID,
               renorm=int(w.renorm),
               layout=moe.MOE_LAYOUT_MASKED if w.layout == "masked" else moe.MOE_LAYOUT_CONTIGUOUS,
-              align_m=128, capacity=w.T if w.layout == "masked" else 0)
+              align_m=128, capacity=w.T if w.layout == "masked" else 0,
+              n_group=w.n_group, topk_group=w.topk_group)
     kw.update(over)
     return moe.Config(**kw)
 
@@ -58,7 +59,8 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 def oracle_route(inp, w, bias=None):
     H = moe_inputs.host_array
     b = None if bias is None else bias.detach().cpu().numpy().astype(np.float64)
-    return oracle.route(H(inp.x), H(inp.wg), b, w.k, oscore(w), w.renorm)
+    return oracle.route(H(inp.x), H(inp.wg), b, w.k, oscore(w), w.renorm, n_group=w.n_group,
+                        topk_group=w.topk_group)
 
 
 def routing_agreement(gidx: np.ndarray, oidx: np.ndarray, keys: np.ndarray, key_tol: float):

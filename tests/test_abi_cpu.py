@@ -102,6 +102,20 @@ def test_host_errors_before_any_launch(moe):
     assert lib.moe_get_device_status(None, 0, None) == moe.MOE_ERR_WORKSPACE
 
 
+@pytest.mark.parametrize("n_group,topk_group,k,ok", [
+    (0, 0, 6, True), (1, 0, 6, True), (8, 4, 8, True), (8, 8, 8, True), (32, 4, 8, True),
+    (7, 2, 6, False),    # 7 does not divide 64
+    (64, 2, 6, False),   # more than 32 groups
+    (8, 0, 6, False), (8, 9, 9, False),   # topk_group out of 1..n_group
+    (8, 4, 3, False),    # k < topk_group
+    (16, 1, 5, False),   # k > topk_group * E / n_group = 4
+])
+def test_group_limited_config_validation(moe, n_group, topk_group, k, ok):
+    cfg = moe.Config(T=16, D=64, H_local=64, E=64, k=k, n_group=n_group, topk_group=topk_group)
+    st = moe.validate_config(cfg)
+    assert (st == moe.MOE_OK) == ok, moe.last_error_string()
+
+
 def test_host_rejections_launch_nothing(moe):
     lib = moe._lib
     before = moe.kernel_launches()
@@ -117,7 +131,7 @@ def test_status_strings(moe):
     assert moe.status_string(moe.MOE_OK) == "MOE_OK"
     assert moe.status_string(moe.MOE_ERR_CAPACITY) == "MOE_ERR_CAPACITY"
     assert moe.status_string(1234) == "MOE_ERR_UNKNOWN"
-    assert moe.abi_version() >= 10100
+    assert moe.abi_version() >= 10200
 
 
 def test_product_does_not_import_oracle():

@@ -156,6 +156,15 @@ def test_layer_is_deterministic(moe):
     assert torch.equal(a, b)
 
 
+def test_layer_group_limited_routing(moe):
+    w = moe_inputs.WORKLOADS["deepseek-v3-shaped"].scaled(T=300, n_group=8, topk_group=4)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=12)
+    out, views, _ = run_layer(moe, cfg_for(moe, w), inp)
+    check_against_oracle(moe, w, inp, out, views, 12)
+    idx = views["topk_idx"].cpu().numpy()
+    assert max(len(set(row // (w.E // w.n_group))) for row in idx) <= w.topk_group
+
+
 def test_layer_launch_count(moe):
     # bf16, E <= 256: router logits on the tensor cores with the top-k in the
     # same cluster launch (1), count + fused scan/index (2; 4 blocks x 64

@@ -34,8 +34,10 @@ def _dev(a, dtype=None):
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("score,renorm", [("softmax", False), ("softmax", True), ("sigmoid", True),
                                           ("sigmoid", False)])
-def test_route_exact_logits_bitexact(moe, dt, score, renorm):
-    """Integer-valued inputs make every logit exact in fp32, ties included."""
+@pytest.mark.parametrize("n_group,topk_group", [(0, 0), (8, 3), (4, 1)])
+def test_route_exact_logits_bitexact(moe, dt, score, renorm, n_group, topk_group):
+    """Integer-valued inputs make every logit exact in fp32, ties included;
+    also with group-limited routing (groups of 9 or 18 experts)."""
     T, D, E, k = 300, 264, 72, 6
     x, wg = moe_inputs.exact_router_inputs(T, D, E, seed=11)
     bias = (np.arange(E) % 5 - 2).astype(np.float32) / 8.0
@@ -43,7 +45,7 @@ def test_route_exact_logits_bitexact(moe, dt, score, renorm):
     cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k,
                      dtype=moe.MOE_F32 if dt == "f32" else moe.MOE_BF16,
                      score=moe.MOE_SCORE_SOFTMAX if score == "softmax" else moe.MOE_SCORE_SIGMOID,
-                     renorm=int(renorm))
+                     renorm=int(renorm), n_group=n_group, topk_group=topk_group)
     ws = moe.alloc_workspace(cfg)
     logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
     gidx = torch.empty((T, k), dtype=torch.int32, device="cuda")
@@ -53,10 +55,12 @@ def test_route_exact_logits_bitexact(moe, dt, score, renorm):
     ref = oracle.router_logits(x, wg, bias.astype(np.float64))
     assert np.array_equal(logits.cpu().numpy(), ref.astype(np.float32))      # exact
     keys = ref.astype(np.float32)
-    oidx, st = oracle.topk(keys, k)
+    oidx, st = oracle.topk(keys, k, n_group, topk_group)
     assert st == oracle.OK
     n_ties = sum(len(set(keys[t])) < E for t in range(T))
     assert n_ties > T // 2                                   # the case exercises ties
+    if n_group:
+        assert (oidx != oracle.topk(keys, k)[0]).any()       # the grouping changes choices
     assert np.array_equal(gidx.cpu().numpy(), oidx)
     ow = oracle.topk_weights(keys, oidx, oracle.SOFTMAX if score == "softmax" else oracle.SIGMOID,
                              renorm)
@@ -88,6 +92,33 @@ def test_route_workload_shapes(moe, name):
         order = sorted(range(w.E), key=lambda e: (-gl[t, e], e))[:w.k]
         assert list(g[t]) == order
     np.testing.assert_allclose(gw.cpu().numpy()[same_order], ow[same_order], rtol=1e-4, atol=1e-6)
+
+
+def test_route_group_limited_workload(moe):
+    """DeepSeek-V3-shaped router with 8 groups, top-4 groups: the GPU's
+    choice is exactly the grouped selection on its own fp32 logits, agrees
+    with the oracle's routing on > 99% of tokens and uses at most 4 groups."""
+    w = moe_inputs.WORKLOADS["deepseek-v3-shaped"].scaled(T=1024, n_group=8, topk_group=4)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=5, weights=False)
+    from helpers import cfg_for, oracle_route, routing_agreement
+    cfg = cfg_for(moe, w)
+    ws = moe.alloc_workspace(cfg)
+    logits = torch.empty((w.T, w.E), dtype=torch.float32, device="cuda")
+    gidx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gw = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(cfg, inp.x, inp.wg, inp.bias, logits, gidx, gw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    gl = logits.cpu().numpy()
+    g = gidx.cpu().numpy()
+    own, _ = oracle.topk(gl, w.k, w.n_group, w.topk_group)
+    assert np.array_equal(g, own)
+    assert max(len(set(row // (w.E // w.n_group))) for row in g) <= w.topk_group
+    l64, keys, oidx, ow, st = oracle_route(inp, w, inp.bias)
+    lerr = np.abs(gl - l64).max()
+    same_set = np.array([set(a) == set(b) for a, b in zip(g, oidx)])
+    assert same_set.mean() > 0.99, f"{same_set.mean():.4f} (logit error {lerr:.2e})"
+    assert (oidx != oracle.topk(keys, w.k)[0]).any()
+    np.testing.assert_allclose(gw.cpu().numpy()[same_set], ow[same_set], rtol=1e-4, atol=1e-6)
 
 
 @pytest.mark.parametrize("T,D,E,k,score", [(1000, 2048, 64, 6, "softmax"), (300, 7168, 256, 8, "sigmoid"),
