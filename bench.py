@@ -225,15 +225,13 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
     import torch
     import torch.distributed as dist
     w = inp.w
-    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
+    lws = moe.alloc_workspace(cfg, host=True, device=dev)
     x_host = inp.x.cpu().pin_memory()
     out_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(inp.x)
 
     def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(cfg, x_dev, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, lws, stream)
-        out_host.copy_(out, non_blocking=True)
+        moe.moe_layer_forward_host(cfg, x_host, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out_host,
+                                   lws, stream)
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
@@ -257,7 +255,7 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
     return {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
             "h2d_bytes_per_step": int(x_host.numel() * 2),
             "d2h_bytes_per_step": int(out_host.numel() * 2),
-            "api": "moe_layer_forward, pinned host x in / out each step"}
+            "api": "moe_layer_forward_host (C ABI): pinned host x copied in, out copied back, every step"}
 
 
 

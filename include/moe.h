@@ -228,6 +228,25 @@ moe_status moe_layer_forward(const moe_config *cfg, const void *x, const void *w
                              const void *w2, void *out, void *ws, size_t ws_bytes,
                              moe_stream_t stream);
 
+/* Workspace bytes for moe_layer_forward_host: the layer workspace plus
+ * device staging for x and out. */
+int64_t moe_layer_host_workspace_size(const moe_config *cfg);
+
+/*
+ * moe_layer_forward with the activations in HOST memory: x_host [T, D] and
+ * out_host [T, D] (dtype, row-major) are host pointers; the router and
+ * expert weights stay device pointers.  On `stream`, the call copies x_host
+ * into device staging carved from ws, runs steps 1-5, and copies the
+ * output back to out_host (one cudaMemcpyAsync each way).  out_host holds
+ * the result once `stream` has completed.  Page-locked host buffers let the
+ * copies run asynchronously; pageable ones work but the copies then
+ * synchronise with the host.  ws_bytes >= moe_layer_host_workspace_size(cfg).
+ */
+moe_status moe_layer_forward_host(const moe_config *cfg, const void *x_host, const void *wg,
+                                  const float *bias, const void *w1, const void *w3,
+                                  const void *w2, void *out_host, void *ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
 /*
  * moe_permute without a workspace (this entry point has no counterpart in
  * the pages; it exists for callers that cannot allocate device memory).

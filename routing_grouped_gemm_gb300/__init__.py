@@ -31,6 +31,7 @@ ABI_SYMBOLS = (
     "moe_rows_alloc", "moe_workspace_size", "moe_layer_workspace_size", "moe_route_topk",
     "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine", "moe_layer_forward",
     "moe_get_device_status", "moe_permute_noalloc", "moe_kernel_launches",
+    "moe_layer_host_workspace_size", "moe_layer_forward_host",
 )
 
 
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
         "moe_get_device_status": (I32, [P, SZ, P]),
         "moe_permute_noalloc": (I32, [C, P, P, P, P, P, P, P, P, P]),
         "moe_kernel_launches": (ctypes.c_uint64, []),
+        "moe_layer_host_workspace_size": (I64, [C]),
+        "moe_layer_forward_host": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -155,9 +158,17 @@ def layer_workspace_size(cfg: Config) -> int:
     return int(_lib.moe_layer_workspace_size(ctypes.byref(c)))
 
 
-def alloc_workspace(cfg: Config, layer: bool = False, device="cuda") -> torch.Tensor:
-    """Zero-filled workspace of the size the library asks for (torch-owned)."""
-    n = layer_workspace_size(cfg) if layer else workspace_size(cfg)
+def layer_host_workspace_size(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_layer_host_workspace_size(ctypes.byref(c)))
+
+
+def alloc_workspace(cfg: Config, layer: bool = False, device="cuda", host: bool = False) -> torch.Tensor:
+    """Zero-filled workspace of the size the library asks for (torch-owned).
+
+    layer: for moe_layer_forward; host: for moe_layer_forward_host."""
+    n = (layer_host_workspace_size(cfg) if host else
+         layer_workspace_size(cfg) if layer else workspace_size(cfg))
     if n < 0:
         raise MoeError(MOE_ERR_INVALID_ARG, "workspace size")
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
@@ -305,6 +316,26 @@ def moe_layer_forward(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None
     _check(_lib.moe_layer_forward(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w1),
                                   _ptr(w3), _ptr(w2), _ptr(out), _ptr(ws), ws.numel(),
                                   _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_host(cfg: Config, x_host, wg, bias, w1, w3, w2, out_host, ws, stream=None):
+    """moe_layer_forward with x and out in host memory (page-locked for
+    asynchronous copies); the weights are CUDA tensors."""
+    dt = cfg.torch_dtype
+    el = cfg.e_local
+    for t, shape, name in ((x_host, (cfg.T, cfg.D), "x_host"), (out_host, (cfg.T, cfg.D), "out_host")):
+        if tuple(t.shape) != shape or t.dtype != dt or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous host tensor {shape} {dt}")
+    _expect(wg, (cfg.E, cfg.D), dt, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    c = cfg.c()
+    _check(_lib.moe_layer_forward_host(ctypes.byref(c), x_host.data_ptr(), _ptr(wg), _ptr(bias),
+                                       _ptr(w1), _ptr(w3), _ptr(w2), out_host.data_ptr(), _ptr(ws),
+                                       ws.numel(), _stream(stream)), "moe_layer_forward_host")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

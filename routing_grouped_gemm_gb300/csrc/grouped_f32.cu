@@ -27,6 +27,8 @@ grouped_f32_kernel(const float *__restrict__ A, int K, const float *__restrict__
                    const float *__restrict__ Bu, int N, float *__restrict__ out,
                    const int *__restrict__ seg_off, const int *__restrict__ tpe, int e_first,
                    int E_local, long long rows_alloc, int n_tiles, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     __shared__ int s_base[F_MAX_EXPERTS], s_valid[F_MAX_EXPERTS], s_mtoff[F_MAX_EXPERTS + 1];
     __shared__ float As[F_BK][F_LD], Bgs[F_BK][F_LD], Bus[F_BK][F_LD];
 
@@ -111,15 +113,21 @@ cudaError_t launch_grouped_swiglu_f32(const float *x_perm, const int *seg_offset
     const long long mt_bound = (rows_alloc + F_BM - 1) / F_BM + E_local;
     const int nt1 = (H_local + F_BN - 1) / F_BN;
     const int nt2 = (D + F_BN - 1) / F_BN;
-    grouped_f32_kernel<1><<<(unsigned)(mt_bound * nt1), F_THREADS, 0, stream>>>(
-        x_perm, D, w1, w3, H_local, h, seg_offsets, tokens_per_expert, e_first, E_local,
+    {
+        const cudaError_t e_ = launch_pdl(grouped_f32_kernel<1>, dim3((unsigned)(mt_bound * nt1)), dim3(F_THREADS), 0, stream,
+            x_perm, D, w1, w3, H_local, h, seg_offsets, tokens_per_expert, e_first, E_local,
         rows_alloc, nt1, status);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    grouped_f32_kernel<2><<<(unsigned)(mt_bound * nt2), F_THREADS, 0, stream>>>(
-        h, H_local, w2, nullptr, D, y_perm, seg_offsets, tokens_per_expert, e_first, E_local,
+    {
+        const cudaError_t e_ = launch_pdl(grouped_f32_kernel<2>, dim3((unsigned)(mt_bound * nt2)), dim3(F_THREADS), 0, stream,
+            h, H_local, w2, nullptr, D, y_perm, seg_offsets, tokens_per_expert, e_first, E_local,
         rows_alloc, nt2, nullptr);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     return cudaGetLastError();
 }

@@ -90,6 +90,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(TC_THREADS, 1)
 grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                   const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -329,7 +331,11 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p1.out = h;
     p1.status = status;
     const long long g1 = std::min<long long>(nsm, mt_bound * p1.n_tiles);
-    grouped_tc_kernel<<<(unsigned)g1, TC_THREADS, smem, stream>>>(tm_x, tm_w1, tm_w3, p1);
+    {
+        const cudaError_t e_ = launch_pdl(grouped_tc_kernel, dim3((unsigned)g1), dim3(TC_THREADS), smem, stream,
+            tm_x, tm_w1, tm_w3, p1);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
@@ -340,7 +346,11 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p2.n_tiles = (D + TC_BN - 1) / TC_BN;
     p2.out = y_perm;
     const long long g2 = std::min<long long>(nsm, mt_bound * p2.n_tiles);
-    grouped_tc_kernel<<<(unsigned)g2, TC_THREADS, smem, stream>>>(tm_h, tm_w2, tm_w2, p2);
+    {
+        const cudaError_t e_ = launch_pdl(grouped_tc_kernel, dim3((unsigned)g2), dim3(TC_THREADS), smem, stream,
+            tm_h, tm_w2, tm_w2, p2);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     return cudaGetLastError();
 }

@@ -171,6 +171,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmH64,
                     const __grid_constant__ CUtensorMap tmH16,
                     const __grid_constant__ CUtensorMap tmW2, const PairParams p) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -609,15 +611,22 @@ cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, si
     cfg.blockDim = dim3(P_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    // the cooperative one-launch form keeps plain stream order; the
+    // two-launch form may start while the previous kernel drains
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
+    if (cooperative) {
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+    } else {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = cooperative ? 2 : 1;
+    cfg.numAttrs = (cooperative || MOE_PDL) ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_pair_kernel, m.x, m.x64, m.x16, m.w1,
                                              m.w3, m.h, m.h64, m.h16, m.w2, p);
     if (e == cudaSuccess) count_launch();

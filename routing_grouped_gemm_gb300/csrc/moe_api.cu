@@ -283,6 +283,16 @@ MOE_EXPORT int64_t moe_layer_workspace_size(const moe_config *cfg) {
     return validate(cfg) == MOE_OK ? layer_ws_layout(cfg, nullptr, nullptr) : -1;
 }
 
+// The host-buffer form: the layer workspace, then x staging, then out staging.
+static int64_t act_bytes(const moe_config *c) {
+    return (int64_t)c->T * c->D * elem_bytes(c);
+}
+
+MOE_EXPORT int64_t moe_layer_host_workspace_size(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK) return -1;
+    return layer_ws_layout(cfg, nullptr, nullptr) + 2 * align_up(act_bytes(cfg));
+}
+
 MOE_EXPORT moe_status moe_route_topk(const moe_config *cfg, const void *x, const void *wg,
                                      const float *bias, float *logits_out, int32_t *topk_idx,
                                      float *topk_w, void *ws, size_t ws_bytes,
@@ -379,6 +389,32 @@ MOE_EXPORT moe_status moe_layer_forward(const moe_config *cfg, const void *x, co
             MOE_OK)
         return st;
     return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
+}
+
+MOE_EXPORT moe_status moe_layer_forward_host(const moe_config *cfg, const void *x_host,
+                                             const void *wg, const float *bias, const void *w1,
+                                             const void *w3, const void *w2, void *out_host,
+                                             void *ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    const int64_t lws = layer_ws_layout(cfg, nullptr, nullptr);
+    if ((int64_t)ws_bytes < lws + 2 * align_up(act_bytes(cfg)))
+        return arg_fail("workspace too small for moe_layer_forward_host", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!x_host || !out_host) return arg_fail("moe_layer_forward_host: NULL host buffer");
+    char *base = static_cast<char *>(ws);
+    void *x_dev = base + lws;
+    void *out_dev = base + lws + align_up(act_bytes(cfg));
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, (size_t)act_bytes(cfg), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_layer_forward_host: copy in");
+    if ((st = moe_layer_forward(cfg, x_dev, wg, bias, w1, w3, w2, out_dev, ws, (size_t)lws, stream)) !=
+        MOE_OK)
+        return st;
+    e = cudaMemcpyAsync(out_host, out_dev, (size_t)act_bytes(cfg), cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_host: copy out");
 }
 
 MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream) {

@@ -63,6 +63,8 @@ __device__ __forceinline__ void build_masks(const int *__restrict__ topk_idx, in
 __global__ void __launch_bounds__(PB_TOKENS)
 permute_count_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int *__restrict__ blk_cnt,
                      int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint32_t s_mask[];  // [PB_WARPS][E]
     build_masks(topk_idx, T, k, E, s_mask, status);
     __syncthreads();
@@ -96,6 +98,8 @@ permute_scan_kernel(const int *__restrict__ blk_cnt, int nblk, int E, int e_firs
                     int layout, int align_m, int capacity, long long rows_alloc,
                     int *__restrict__ tokens_per_expert, int *__restrict__ seg_offsets,
                     int *__restrict__ blk_base, int *__restrict__ token_of_row, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ int s_int[];
     int *s_cnt = s_int;              // [E]
     int *s_off = s_cnt + E;          // [E_local + 1]  (inclusive scan, shifted)
@@ -162,6 +166,8 @@ permute_index_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int 
                      int E_local, const int *__restrict__ blk_base,
                      const int *__restrict__ seg_offsets, int *__restrict__ row_of,
                      int *__restrict__ token_of_row, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint32_t s_mask[];  // [PB_WARPS][E]
     build_masks(topk_idx, T, k, E, s_mask, nullptr);
     __syncthreads();
@@ -206,6 +212,8 @@ permute_index_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
                           const int *__restrict__ blk_cnt, int nblk,
                           int *__restrict__ tokens_per_expert, int *__restrict__ seg_offsets,
                           int *__restrict__ row_of, int *__restrict__ token_of_row, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint32_t s_dyn[];
     uint32_t *s_mask = s_dyn;                                       // [PB_WARPS][E]
     int *s_tot = reinterpret_cast<int *>(s_mask + PB_WARPS * E);    // [E]  totals
@@ -316,6 +324,8 @@ constexpr int CP_UNROLL = 4;
 __global__ void __launch_bounds__(256)
 permute_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_of,
                     uint4 *__restrict__ x_perm, int T, int k, int vpr) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -359,6 +369,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
                const float *__restrict__ topk_w, void *__restrict__ out, int T, int k, int D,
                long long rows_alloc, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     // One warp per (token, part): a token's row is split into CB_PARTS parts
     // of whole 32-vector chunks, so the grid has CB_PARTS x T warps.
     constexpr int EPV = BF16 ? 8 : 4;      // output elements per 16-byte vector
@@ -451,8 +463,12 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     if (nblk > 0) {
         err = ensure_smem((const void *)permute_count_kernel, mask_smem);
         if (err != cudaSuccess) return err;
-        permute_count_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(topk_idx, T, k, E, blk_cnt,
+        {
+        const cudaError_t e_ = launch_pdl(permute_count_kernel, dim3(nblk), dim3(PB_TOKENS), mask_smem, stream,
+            topk_idx, T, k, E, blk_cnt,
                                                                      status);
+        if (e_ != cudaSuccess) return e_;
+    }
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
@@ -460,31 +476,43 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         const size_t smem = mask_smem + sizeof(int) * (2 * (size_t)E + E_local + 1);
         err = ensure_smem((const void *)permute_index_scan_kernel, smem);
         if (err != cudaSuccess) return err;
-        permute_index_scan_kernel<<<nblk, PB_TOKENS, smem, stream>>>(
+        {
+        const cudaError_t e_ = launch_pdl(permute_index_scan_kernel, dim3(nblk), dim3(PB_TOKENS), smem, stream,
             topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity, rows_alloc, blk_cnt,
             nblk, tokens_per_expert, seg_offsets, row_of, token_of_row, status);
+        if (e_ != cudaSuccess) return e_;
+    }
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     } else {
     const size_t scan_smem = sizeof(int) * ((size_t)E + E_local + 1);
-    permute_scan_kernel<<<1, SCAN_THREADS, scan_smem, stream>>>(
-        blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
+    {
+        const cudaError_t e_ = launch_pdl(permute_scan_kernel, dim3(1), dim3(SCAN_THREADS), scan_smem, stream,
+            blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
         tokens_per_expert, seg_offsets, blk_base, token_of_row, status);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nblk == 0) return cudaSuccess;
     err = ensure_smem((const void *)permute_index_kernel, mask_smem);
     if (err != cudaSuccess) return err;
-    permute_index_kernel<<<nblk, PB_TOKENS, mask_smem, stream>>>(
-        topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);
+    {
+        const cudaError_t e_ = launch_pdl(permute_index_kernel, dim3(nblk), dim3(PB_TOKENS), mask_smem, stream,
+            topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const int vpr = D * elem_bytes / 16;
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;
-    permute_copy_kernel<<<blocks, 32 * warps_per_block, 0, stream>>>(
-        (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr);
+    {
+        const cudaError_t e_ = launch_pdl(permute_copy_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+            (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     return cudaGetLastError();
 }
@@ -497,11 +525,17 @@ cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *t
     const long long warps = (long long)T * CB_PARTS;
     const int blocks = (int)((warps + warps_per_block - 1) / warps_per_block);
     if (is_bf16)
-        combine_kernel<true><<<blocks, 32 * warps_per_block, 0, stream>>>(
+        {
+        const cudaError_t e_ = launch_pdl(combine_kernel<true>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
             (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
+        if (e_ != cudaSuccess) return e_;
+    }
     else
-        combine_kernel<false><<<blocks, 32 * warps_per_block, 0, stream>>>(
+        {
+        const cudaError_t e_ = launch_pdl(combine_kernel<false>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
             (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
+        if (e_ != cudaSuccess) return e_;
+    }
     count_launch();
     return cudaGetLastError();
 }

@@ -158,6 +158,8 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
                    float *__restrict__ logits_out, int *__restrict__ topk_idx,
                    float *__restrict__ topk_w, int Tn, int D, int E, int k, int score, int renorm,
                    int n_group, int topk_group, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ float smem[];
     float *s_logit = smem;                              // [RT_TOKENS][E]
     float *s_x = s_logit + RT_TOKENS * E;               // [RT_BK][SX_LD]
@@ -278,6 +280,8 @@ template <bool kCluster>
 __global__ void __launch_bounds__(kCluster ? RC_CL_THREADS : RC_THREADS)
 router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, const RouterTcParams p) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -461,6 +465,8 @@ router_reduce_topk_kernel(const float *__restrict__ part, int splits, const floa
                           float *__restrict__ logits_out, int *__restrict__ topk_idx,
                           float *__restrict__ topk_w, int Tn, int E, int k, int score, int renorm,
                           int n_group, int topk_group, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
     extern __shared__ float s_key[];  // [RR_TOKENS][E + 1]
     const int ld = E + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -539,13 +545,15 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
             cfg.blockDim = dim3(RC_CL_THREADS);
             cfg.dynamicSmemBytes = smem;
             cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
+            cudaLaunchAttribute attr[2];
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = 1;
             attr[0].val.clusterDim.y = splits;
             attr[0].val.clusterDim.z = 1;
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
-            cfg.numAttrs = 1;
+            cfg.numAttrs = MOE_PDL ? 2 : 1;
             err = cudaLaunchKernelEx(&cfg, router_logits_tc_kernel<true>, tm_x, tm_w, p);
             if (err == cudaSuccess) {
                 count_launch();
@@ -556,13 +564,16 @@ cudaError_t launch_router_tc(const void *x, const void *wg, const float *bias, f
     }
     err = ensure_smem((const void *)router_logits_tc_kernel<false>, smem);
     if (err != cudaSuccess) return err;
-    router_logits_tc_kernel<false><<<dim3(m_tiles, splits), RC_THREADS, smem, stream>>>(tm_x, tm_w, p);
+    if ((err = launch_pdl(router_logits_tc_kernel<false>, dim3(m_tiles, splits), dim3(RC_THREADS), smem,
+                          stream, tm_x, tm_w, p)) != cudaSuccess)
+        return err;
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t rsmem = sizeof(float) * RR_TOKENS * (size_t)(E + 1);
-    router_reduce_topk_kernel<<<(T + RR_TOKENS - 1) / RR_TOKENS, RR_THREADS, rsmem, stream>>>(
-        part, splits, bias, logits_out, topk_idx, topk_w, T, E, k, score, renorm, n_group, topk_group,
-        status);
+    if ((err = launch_pdl(router_reduce_topk_kernel, dim3((T + RR_TOKENS - 1) / RR_TOKENS),
+                          dim3(RR_THREADS), rsmem, stream, part, splits, bias, logits_out, topk_idx,
+                          topk_w, T, E, k, score, renorm, n_group, topk_group, status)) != cudaSuccess)
+        return err;
     count_launch();
     return cudaGetLastError();
 }
@@ -586,16 +597,18 @@ cudaError_t launch_router_topk(const void *x, const void *wg, const float *bias,
         auto kern = router_topk_kernel<__nv_bfloat16>;
         err = ensure_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
-        kern<<<grid, RT_THREADS, smem, stream>>>((const __nv_bfloat16 *)x, (const __nv_bfloat16 *)wg,
-                                                 bias, logits_out, topk_idx, topk_w, T, D, E, k,
-                                                 score, renorm, n_group, topk_group, status);
+        if ((err = launch_pdl(kern, grid, dim3(RT_THREADS), smem, stream, (const __nv_bfloat16 *)x,
+                              (const __nv_bfloat16 *)wg, bias, logits_out, topk_idx, topk_w, T, D, E,
+                              k, score, renorm, n_group, topk_group, status)) != cudaSuccess)
+            return err;
     } else {
         auto kern = router_topk_kernel<float>;
         err = ensure_smem((const void *)kern, smem);
         if (err != cudaSuccess) return err;
-        kern<<<grid, RT_THREADS, smem, stream>>>((const float *)x, (const float *)wg, bias,
-                                                 logits_out, topk_idx, topk_w, T, D, E, k, score,
-                                                 renorm, n_group, topk_group, status);
+        if ((err = launch_pdl(kern, grid, dim3(RT_THREADS), smem, stream, (const float *)x,
+                              (const float *)wg, bias, logits_out, topk_idx, topk_w, T, D, E, k, score,
+                              renorm, n_group, topk_group, status)) != cudaSuccess)
+            return err;
     }
     count_launch();
     return cudaGetLastError();

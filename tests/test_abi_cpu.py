@@ -116,6 +116,12 @@ def test_group_limited_config_validation(moe, n_group, topk_group, k, ok):
     assert (st == moe.MOE_OK) == ok, moe.last_error_string()
 
 
+def test_layer_host_workspace_size(moe):
+    cfg = moe.Config(T=1000, D=264, H_local=64, E=16, k=4)
+    extra = 2 * ((1000 * 264 * 2 + 255) // 256 * 256)
+    assert moe.layer_host_workspace_size(cfg) == moe.layer_workspace_size(cfg) + extra
+
+
 def test_host_rejections_launch_nothing(moe):
     lib = moe._lib
     before = moe.kernel_launches()

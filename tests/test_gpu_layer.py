@@ -165,6 +165,25 @@ def test_layer_group_limited_routing(moe):
     assert max(len(set(row // (w.E // w.n_group))) for row in idx) <= w.topk_group
 
 
+def test_layer_forward_host_buffers(moe):
+    """The host-buffer entry point copies x in and out around the same layer:
+    bit-identical to moe_layer_forward, also on a second call that reuses
+    the workspace with another input."""
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=700, D=512, H=384)
+    cfg = cfg_for(moe, w)
+    hws = moe.alloc_workspace(cfg, host=True)
+    for seed in (13, 14):
+        inp = moe_inputs.make_inputs(w, device="cuda", seed=seed)
+        ref, _, _ = run_layer(moe, cfg, inp)
+        x_host = inp.x.cpu().pin_memory()
+        out_host = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16).pin_memory()
+        moe.moe_layer_forward_host(cfg, x_host, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out_host,
+                                   hws)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(hws) == moe.MOE_OK
+        assert torch.equal(out_host, ref.cpu())
+
+
 def test_layer_launch_count(moe):
     # bf16, E <= 256: router logits on the tensor cores with the top-k in the
     # same cluster launch (1), count + fused scan/index (2; 4 blocks x 64
