@@ -113,23 +113,18 @@ cudaError_t launch_grouped_swiglu_f32(const float *x_perm, const int *seg_offset
     const long long mt_bound = (rows_alloc + F_BM - 1) / F_BM + E_local;
     const int nt1 = (H_local + F_BN - 1) / F_BN;
     const int nt2 = (D + F_BN - 1) / F_BN;
-    {
-        const cudaError_t e_ = launch_pdl(grouped_f32_kernel<1>, dim3((unsigned)(mt_bound * nt1)), dim3(F_THREADS), 0, stream,
-            x_perm, D, w1, w3, H_local, h, seg_offsets, tokens_per_expert, e_first, E_local,
-        rows_alloc, nt1, status);
-        if (e_ != cudaSuccess) return e_;
-    }
-    count_launch();
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(grouped_f32_kernel<1>, dim3((unsigned)(mt_bound * nt1)),
+                                 dim3(F_THREADS), 0, stream, x_perm, D, w1, w3, H_local, h,
+                                 seg_offsets, tokens_per_expert, e_first, E_local, rows_alloc,
+                                 nt1, status);
     if (err != cudaSuccess) return err;
-    {
-        const cudaError_t e_ = launch_pdl(grouped_f32_kernel<2>, dim3((unsigned)(mt_bound * nt2)), dim3(F_THREADS), 0, stream,
-            h, H_local, w2, nullptr, D, y_perm, seg_offsets, tokens_per_expert, e_first, E_local,
-        rows_alloc, nt2, nullptr);
-        if (e_ != cudaSuccess) return e_;
-    }
     count_launch();
-    return cudaGetLastError();
+    err = launch_pdl(grouped_f32_kernel<2>, dim3((unsigned)(mt_bound * nt2)), dim3(F_THREADS), 0,
+                     stream, h, H_local, w2, nullptr, D, y_perm, seg_offsets, tokens_per_expert,
+                     e_first, E_local, rows_alloc, nt2, nullptr);
+    if (err != cudaSuccess) return err;
+    count_launch();
+    return cudaSuccess;
 }
 
 }  // namespace moe

@@ -331,11 +331,9 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p1.out = h;
     p1.status = status;
     const long long g1 = std::min<long long>(nsm, mt_bound * p1.n_tiles);
-    {
-        const cudaError_t e_ = launch_pdl(grouped_tc_kernel, dim3((unsigned)g1), dim3(TC_THREADS), smem, stream,
-            tm_x, tm_w1, tm_w3, p1);
-        if (e_ != cudaSuccess) return e_;
-    }
+    if ((err = launch_pdl(grouped_tc_kernel, dim3((unsigned)g1), dim3(TC_THREADS), smem, stream,
+                          tm_x, tm_w1, tm_w3, p1)) != cudaSuccess)
+        return err;
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
@@ -346,11 +344,9 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p2.n_tiles = (D + TC_BN - 1) / TC_BN;
     p2.out = y_perm;
     const long long g2 = std::min<long long>(nsm, mt_bound * p2.n_tiles);
-    {
-        const cudaError_t e_ = launch_pdl(grouped_tc_kernel, dim3((unsigned)g2), dim3(TC_THREADS), smem, stream,
-            tm_h, tm_w2, tm_w2, p2);
-        if (e_ != cudaSuccess) return e_;
-    }
+    if ((err = launch_pdl(grouped_tc_kernel, dim3((unsigned)g2), dim3(TC_THREADS), smem, stream,
+                          tm_h, tm_w2, tm_w2, p2)) != cudaSuccess)
+        return err;
     count_launch();
     return cudaGetLastError();
 }

@@ -145,20 +145,6 @@ __device__ __forceinline__ PairTile decode_pair(int v, const PairParams &p, int 
     return c;
 }
 
-// L2 prefetch of this CTA's weight slice of tile c at k-step kb (the rows
-// its TMA loads will read: w1 and w3 rows for GEMM1, w2 rows for GEMM2).
-__device__ __forceinline__ void prefetch_weights(const PairTile &c, int kb, uint32_t rank,
-                                                 const CUtensorMap *w1, const CUtensorMap *w3,
-                                                 const CUtensorMap *w2) {
-    if (c.mode == 0) {
-        const int hrow = c.nt * 128 + (int)rank * 64;
-        tma_prefetch_l2_3d(w1, kb * P_BK, hrow, c.expert);
-        tma_prefetch_l2_3d(w3, kb * P_BK, hrow, c.expert);
-    } else {
-        tma_prefetch_l2_3d(w2, kb * P_BK, c.nt * P_BN + (int)rank * 128, c.expert);
-    }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -176,7 +162,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    float *xbuf = reinterpret_cast<float *>(ring + P_STAGES * P_STAGE_BYTES);  // [2][32 cols][32 lanes]
+    // transposed GEMM1 tiles hand the up values over through xbuf [2][32 tokens][32 lanes]
+    float *xbuf = reinterpret_cast<float *>(ring + P_STAGES * P_STAGE_BYTES);
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES);
     uint64_t *full = bars;                   // [P_STAGES]  leader: both CTAs' TMA -> MMA
     uint64_t *empty = bars + P_STAGES;       // [P_STAGES]  MMA -> each CTA's TMA
@@ -256,23 +243,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0);
             int s = 0;
             uint32_t ph = 0;
-#ifndef MOE_PAIR_PF
-#define MOE_PAIR_PF 0
-#endif
-            constexpr int PF = MOE_PAIR_PF;  // weight prefetch distance in k-steps (0: off)
-            if (PF > 0 && pair_id < total_tiles) {
-                const PairTile c0 = decode_pair(pair_id, p, n_blocks, s_mtoff, s_base, s_valid);
-                const int nk0 = c0.mode ? p.nk1 : p.nk0;
-                for (int kb = 0; kb < PF && kb < nk0; ++kb) prefetch_weights(c0, kb, rank, &tmW1, &tmW3, &tmW2);
-            }
             for (int tile = pair_id; tile < total_tiles; tile += n_pairs) {
                 const PairTile c = decode_pair(tile, p, n_blocks, s_mtoff, s_base, s_valid);
-                PairTile cn{};
-                int nkn = 0;
-                if (PF > 0 && tile + n_pairs < total_tiles) {
-                    cn = decode_pair(tile + n_pairs, p, n_blocks, s_mtoff, s_base, s_valid);
-                    nkn = cn.mode ? p.nk1 : p.nk0;
-                }
                 const bool swap = c.nvalid <= P_SWAP_MAX;         // transposed tail tile
                 const bool half = !swap && c.nvalid <= P_BM;      // M=128: 64 rows per CTA
                 const int srows = ((c.nvalid + 31) & ~31) / 2;    // transposed: token rows per CTA
@@ -291,11 +263,6 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     fence_proxy_async_global();
                 }
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (PF > 0) {
-                        const int pk = kb + PF;
-                        if (pk < nk) prefetch_weights(c, pk, rank, &tmW1, &tmW3, &tmW2);
-                        else if (pk - nk < nkn) prefetch_weights(cn, pk - nk, rank, &tmW1, &tmW3, &tmW2);
-                    }
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
                     if (leader) mbar_arrive_expect_tx(&full[s], tx);
                     uint8_t *sa = ring + s * P_STAGE_BYTES;

@@ -463,12 +463,9 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     if (nblk > 0) {
         err = ensure_smem((const void *)permute_count_kernel, mask_smem);
         if (err != cudaSuccess) return err;
-        {
-        const cudaError_t e_ = launch_pdl(permute_count_kernel, dim3(nblk), dim3(PB_TOKENS), mask_smem, stream,
-            topk_idx, T, k, E, blk_cnt,
-                                                                     status);
-        if (e_ != cudaSuccess) return e_;
-    }
+        if ((err = launch_pdl(permute_count_kernel, dim3(nblk), dim3(PB_TOKENS), mask_smem, stream,
+                              topk_idx, T, k, E, blk_cnt, status)) != cudaSuccess)
+            return err;
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
@@ -476,43 +473,38 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         const size_t smem = mask_smem + sizeof(int) * (2 * (size_t)E + E_local + 1);
         err = ensure_smem((const void *)permute_index_scan_kernel, smem);
         if (err != cudaSuccess) return err;
-        {
-        const cudaError_t e_ = launch_pdl(permute_index_scan_kernel, dim3(nblk), dim3(PB_TOKENS), smem, stream,
-            topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity, rows_alloc, blk_cnt,
-            nblk, tokens_per_expert, seg_offsets, row_of, token_of_row, status);
-        if (e_ != cudaSuccess) return e_;
-    }
+        if ((err = launch_pdl(permute_index_scan_kernel, dim3(nblk), dim3(PB_TOKENS), smem, stream,
+                              topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity,
+                              rows_alloc, blk_cnt, nblk, tokens_per_expert, seg_offsets, row_of,
+                              token_of_row, status)) != cudaSuccess)
+            return err;
         count_launch();
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     } else {
     const size_t scan_smem = sizeof(int) * ((size_t)E + E_local + 1);
-    {
-        const cudaError_t e_ = launch_pdl(permute_scan_kernel, dim3(1), dim3(SCAN_THREADS), scan_smem, stream,
-            blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
-        tokens_per_expert, seg_offsets, blk_base, token_of_row, status);
-        if (e_ != cudaSuccess) return e_;
-    }
+    if ((err = launch_pdl(permute_scan_kernel, dim3(1), dim3(SCAN_THREADS), scan_smem, stream,
+                          blk_cnt, nblk, E, e_first, E_local, layout, align_m, capacity, rows_alloc,
+                          tokens_per_expert, seg_offsets, blk_base, token_of_row, status)) !=
+        cudaSuccess)
+        return err;
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nblk == 0) return cudaSuccess;
     err = ensure_smem((const void *)permute_index_kernel, mask_smem);
     if (err != cudaSuccess) return err;
-    {
-        const cudaError_t e_ = launch_pdl(permute_index_kernel, dim3(nblk), dim3(PB_TOKENS), mask_smem, stream,
-            topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of, token_of_row, status);
-        if (e_ != cudaSuccess) return e_;
-    }
+    if ((err = launch_pdl(permute_index_kernel, dim3(nblk), dim3(PB_TOKENS), mask_smem, stream,
+                          topk_idx, T, k, E, e_first, E_local, blk_base, seg_offsets, row_of,
+                          token_of_row, status)) != cudaSuccess)
+        return err;
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const int vpr = D * elem_bytes / 16;
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;
-    {
-        const cudaError_t e_ = launch_pdl(permute_copy_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
-            (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr);
-        if (e_ != cudaSuccess) return e_;
-    }
+    if ((err = launch_pdl(permute_copy_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+                          (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr)) != cudaSuccess)
+        return err;
     count_launch();
     return cudaGetLastError();
 }
@@ -524,20 +516,16 @@ cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *t
     const int warps_per_block = 8;
     const long long warps = (long long)T * CB_PARTS;
     const int blocks = (int)((warps + warps_per_block - 1) / warps_per_block);
-    if (is_bf16)
-        {
-        const cudaError_t e_ = launch_pdl(combine_kernel<true>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
-            (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
-        if (e_ != cudaSuccess) return e_;
-    }
-    else
-        {
-        const cudaError_t e_ = launch_pdl(combine_kernel<false>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
-            (const float4 *)y_perm, row_of, topk_w, out, T, k, D, rows_alloc, status);
-        if (e_ != cudaSuccess) return e_;
-    }
+    const cudaError_t err =
+        is_bf16 ? launch_pdl(combine_kernel<true>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+                             (const float4 *)y_perm, row_of, topk_w, out, T, k, D,
+                             (long long)rows_alloc, status)
+                : launch_pdl(combine_kernel<false>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+                             (const float4 *)y_perm, row_of, topk_w, out, T, k, D,
+                             (long long)rows_alloc, status);
+    if (err != cudaSuccess) return err;
     count_launch();
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace moe

@@ -464,7 +464,8 @@ def test_grouped_swiglu_bad_offsets_flagged(moe):
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("T,E,k,D,e_first,E_local", [(513, 16, 4, 264, 0, 16), (200, 64, 8, 2048, 16, 32),
-                                                     (77, 4, 1, 8, 0, 4)])
+                                                     (77, 4, 1, 8, 0, 4), (300, 32, 12, 136, 0, 32),
+                                                     (41, 8, 3, 3080, 0, 8)])
 def test_combine_parity(moe, dt, T, E, k, D, e_first, E_local):
     idx = moe_inputs.random_topk_idx(T, E, k, seed=T)
     lay = oracle.layout(idx, E, e_first, E_local, oracle.CONTIGUOUS, 128)
