@@ -336,7 +336,7 @@ permute_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_of,
 #pragma unroll
         for (int u = 0; u < CP_UNROLL; ++u) {
             const int v = v0 + u * 32 + lane;
-            if (v < vpr) buf[u] = __ldg(src + v);
+            if (v < vpr) buf[u] = __ldcs(src + v);  // x[t] is read once here
         }
         for (int j = 0; j < k; ++j) {
             const int r = __shfl_sync(0xffffffffu, my_row, j);
