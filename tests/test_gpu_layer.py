@@ -184,6 +184,14 @@ def test_layer_forward_host_buffers(moe):
         assert torch.equal(out_host, ref.cpu())
 
 
+def test_layer_k32_many_experts(moe):
+    """k = 32 of E = 256 (the largest k the ABI accepts), bf16."""
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=96, E=256, k=32, D=256, H=128)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=15)
+    out, views, _ = run_layer(moe, cfg_for(moe, w), inp)
+    check_against_oracle(moe, w, inp, out, views, 24)
+
+
 def test_layer_launch_count(moe):
     # bf16, E <= 256: router logits on the tensor cores with the top-k in the
     # same cluster launch (1), count + fused scan/index (2; 4 blocks x 64

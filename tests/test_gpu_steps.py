@@ -151,6 +151,34 @@ def test_route_one_kernel_equals_two(moe, T, D, E, k, score, monkeypatch):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_route_largest_E_and_k_bitexact(moe, dt):
+    """E = 1024 and k = 32, the largest the ABI accepts (the bf16 router runs
+    the SIMT form above 256 experts); with and without 32 groups."""
+    T, D, E, k = 160, 96, 1024, 32
+    x, wg = moe_inputs.exact_router_inputs(T, D, E, seed=3)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    ref = oracle.router_logits(x, wg, None)
+    keys = ref.astype(np.float32)
+    for n_group, topk_group in ((0, 0), (32, 8)):
+        cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k,
+                         dtype=moe.MOE_F32 if dt == "f32" else moe.MOE_BF16,
+                         score=moe.MOE_SCORE_SIGMOID, renorm=1, n_group=n_group,
+                         topk_group=topk_group)
+        ws = moe.alloc_workspace(cfg)
+        logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        gidx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        gw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        moe.moe_route_topk(cfg, _dev(x, tdt), _dev(wg, tdt), None, logits, gidx, gw, ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        assert np.array_equal(logits.cpu().numpy(), keys)
+        oidx, st = oracle.topk(keys, k, n_group, topk_group)
+        assert st == oracle.OK
+        assert np.array_equal(gidx.cpu().numpy(), oidx)
+        ow = oracle.topk_weights(keys, oidx, oracle.SIGMOID, True)
+        np.testing.assert_allclose(gw.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+
+
 def test_route_nan_logit_sets_status(moe):
     T, D, E, k = 64, 64, 16, 4
     x = torch.randn(T, D, device="cuda")
@@ -192,6 +220,8 @@ def _run_permute(moe, cfg, x, idx):
     (513, 256, 8, 128, 0, 256, 0.3),
     (700, 5, 1, 16, 2, 2, 0.0),          # k = 1
     (20000, 256, 8, 128, 0, 256, 0.3),   # count matrix above the fused-scan limit
+    (3000, 1024, 32, 128, 0, 1024, 0.5),  # the largest E and k the ABI accepts
+    (70000, 64, 8, 128, 0, 64, 1.0),     # T above 2^16, R = 560000 rows
 ])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 def test_permute_bitexact(moe, T, E, k, align, e_first, E_local, skew, dt):
