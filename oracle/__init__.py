@@ -85,6 +85,11 @@ def _load():
             lib.oracle_topk.argtypes = [I, I, I, P, P]
             lib.oracle_topk_grouped.restype = I
             lib.oracle_topk_grouped.argtypes = [I, I, I, I, I, P, P]
+            lib.oracle_moe_forward64.restype = I
+            lib.oracle_moe_forward64.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, I, I, I, P, P]
+            lib.oracle_moe_backward.restype = I
+            lib.oracle_moe_backward.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, I, I, I, P,
+                                                P, P, P, P, P, P, P]
             lib.oracle_topk_weights.argtypes = [I, I, I, P, P, I, I, P]
             lib.oracle_rows_alloc.restype = L
             lib.oracle_rows_alloc.argtypes = [I, I, I, I, I, I]
@@ -350,3 +355,49 @@ def unpermute_combine(y_perm, row_of, topk_w) -> np.ndarray:
     out = np.empty((T, D), np.float64)
     _load().oracle_unpermute_combine(T, k, D, _p(y), _dt(y), _p(ro), _p(w), _p(out))
     return out
+
+
+# --------------------------------------------------------------------------
+# backward (fp64 throughout)
+# --------------------------------------------------------------------------
+
+def _f64(a):
+    return None if a is None else _c(np.asarray(a, dtype=np.float64), np.float64)
+
+
+def moe_forward64(x, wg, bias, w1, w3, w2, k: int, score: int, renorm: bool, n_group: int = 0,
+                  topk_group: int = 0):
+    """The whole layer in fp64 (selection on the fp64 logits), the function
+    moe_backward differentiates.  x [T,D], wg [E,D], bias [E] or None,
+    w1/w3 [E,H,D], w2 [E,D,H].  Returns (out [T,D], topk_idx [T,k])."""
+    x, wg, b, w1, w3, w2 = (_f64(a) for a in (x, wg, bias, w1, w3, w2))
+    T, D = x.shape
+    E, H = w1.shape[0], w1.shape[1]
+    out = np.empty((T, D), np.float64)
+    idx = np.empty((T, k), np.int32)
+    st = _load().oracle_moe_forward64(T, D, H, E, k, _p(x), _p(wg), _p(b) if b is not None else None,
+                                      _p(w1), _p(w3), _p(w2), int(score), int(bool(renorm)),
+                                      int(n_group), int(topk_group), _p(out), _p(idx))
+    if st != OK:
+        raise ValueError("oracle.moe_forward64: bad arguments")
+    return out, idx
+
+
+def moe_backward(x, wg, bias, w1, w3, w2, dout, k: int, score: int, renorm: bool,
+                 n_group: int = 0, topk_group: int = 0) -> dict:
+    """Gradients of sum(dout * out) for the fp64 layer of moe_forward64:
+    keys dx, dwg, dbias, dw1, dw3, dw2 (and topk_idx, the selection used)."""
+    x, wg, b, w1, w3, w2, go = (_f64(a) for a in (x, wg, bias, w1, w3, w2, dout))
+    T, D = x.shape
+    E, H = w1.shape[0], w1.shape[1]
+    r = dict(dx=np.empty((T, D)), dwg=np.empty((E, D)), dbias=np.empty(E),
+             dw1=np.empty((E, H, D)), dw3=np.empty((E, H, D)), dw2=np.empty((E, D, H)),
+             topk_idx=np.empty((T, k), np.int32))
+    st = _load().oracle_moe_backward(T, D, H, E, k, _p(x), _p(wg), _p(b) if b is not None else None,
+                                     _p(w1), _p(w3), _p(w2), int(score), int(bool(renorm)),
+                                     int(n_group), int(topk_group), _p(go), _p(r["dx"]),
+                                     _p(r["dwg"]), _p(r["dbias"]), _p(r["dw1"]), _p(r["dw3"]),
+                                     _p(r["dw2"]), _p(r["topk_idx"]))
+    if st != OK:
+        raise ValueError("oracle.moe_backward: bad arguments")
+    return r

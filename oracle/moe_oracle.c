@@ -617,3 +617,260 @@ void oracle_unpermute_combine(int T, int k, int D, const void *y_perm, int ydt,
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* backward of the layer (fp64 throughout)                               */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The layer written once more entirely in fp64, as the function that the
+ * backward below differentiates ([EP] section 1 forward path; [EP] section 5:
+ * the backward mirrors it -- combine-bwd is a dispatch, dispatch-bwd a
+ * combine -- and the expert weights get m-grouped dgrad / k-grouped wgrad):
+ *   l = x.wg^T + b                         (fp64, no fp32 key here)
+ *   S = top-k of l (same order and grouping rules as the fp32 selection)
+ *   w_j = score weights of l over S (softmax over all E or sigmoid, renorm)
+ *   out[t] = sum_j w_j FFN_{S_j}(x[t])
+ * The selection is piecewise constant: it carries no gradient.
+ */
+static int before64(double a, int ia, double b, int ib)
+{
+    int na = isnan(a), nb = isnan(b);
+    if (na || nb) {
+        if (na && nb) return ia < ib;
+        return nb;
+    }
+    if (a > b) return 1;
+    if (a < b) return 0;
+    return ia < ib;
+}
+
+static void select64(int E, int k, int n_group, int topk_group, const double *l, int32_t *idx)
+{
+    unsigned char taken[1024], gsel[1024];
+    double gscore[1024];
+    const int grouped = n_group > 1;
+    const int gs = grouped ? E / n_group : E;
+    if (grouped) {
+        const int m = k / topk_group;
+        memset(taken, 0, (size_t)E);
+        for (int g = 0; g < n_group; ++g) {
+            double sum = 0.0;
+            for (int i = 0; i < m; ++i) {
+                int best = -1;
+                for (int e = g * gs; e < (g + 1) * gs; ++e)
+                    if (!taken[e] && (best < 0 || before64(l[e], e, l[best], best))) best = e;
+                taken[best] = 1;
+                sum += l[best];
+            }
+            gscore[g] = sum;
+        }
+        memset(gsel, 0, (size_t)n_group);
+        for (int r = 0; r < topk_group; ++r) {
+            int best = -1;
+            for (int g = 0; g < n_group; ++g)
+                if (!gsel[g] && (best < 0 || before64(gscore[g], g, gscore[best], best))) best = g;
+            gsel[best] = 1;
+        }
+    }
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        for (int e = 0; e < E; ++e) {
+            if (taken[e] || (grouped && !gsel[e / gs])) continue;
+            if (best < 0 || before64(l[e], e, l[best], best)) best = e;
+        }
+        taken[best] = 1;
+        idx[j] = best;
+    }
+}
+
+/* softmax over all E (p_all) or sigmoid scores, then the k weights */
+static void weights64(int E, int k, const double *l, const int32_t *idx, int score, int renorm,
+                      double *p_all, double *w)
+{
+    if (score == ORC_SOFTMAX) {
+        double m = -INFINITY, z = 0.0;
+        for (int e = 0; e < E; ++e) if (l[e] > m) m = l[e];
+        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        for (int e = 0; e < E; ++e) p_all[e] = exp(l[e] - m) / z;
+    } else {
+        for (int e = 0; e < E; ++e) p_all[e] = 1.0 / (1.0 + exp(-l[e]));
+    }
+    double s = 0.0;
+    for (int j = 0; j < k; ++j) s += p_all[idx[j]];
+    for (int j = 0; j < k; ++j) w[j] = renorm ? p_all[idx[j]] / s : p_all[idx[j]];
+}
+
+static int backward_args_ok(int D, int H, int E, int k, int n_group, int topk_group)
+{
+    if (D < 1 || H < 1 || E < 1 || E > 1024 || k < 1 || k > E) return 0;
+    if (n_group > 1 && (E % n_group || topk_group < 1 || topk_group > n_group ||
+                        k < topk_group || k > topk_group * (E / n_group)))
+        return 0;
+    return 1;
+}
+
+int oracle_moe_forward64(int T, int D, int H, int E, int k, const double *x, const double *wg,
+                         const double *bias, const double *w1, const double *w3,
+                         const double *w2, int score, int renorm, int n_group, int topk_group,
+                         double *out, int32_t *topk_idx)
+{
+    if (!backward_args_ok(D, H, E, k, n_group, topk_group)) return ORC_BAD_ARG;
+    double *l = malloc(sizeof(double) * E), *p = malloc(sizeof(double) * E);
+    double *w = malloc(sizeof(double) * k), *a = malloc(sizeof(double) * H);
+    double *y = malloc(sizeof(double) * D);
+    if (!l || !p || !w || !a || !y) { free(l); free(p); free(w); free(a); free(y); return ORC_BAD_ARG; }
+    for (int t = 0; t < T; ++t) {
+        const double *xt = x + (size_t)t * D;
+        for (int e = 0; e < E; ++e) {
+            double s = bias ? bias[e] : 0.0;
+            for (int d = 0; d < D; ++d) s += xt[d] * wg[(size_t)e * D + d];
+            l[e] = s;
+        }
+        int32_t *idx = topk_idx + (size_t)t * k;
+        select64(E, k, n_group, topk_group, l, idx);
+        weights64(E, k, l, idx, score, renorm, p, w);
+        double *o = out + (size_t)t * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[j];
+            expert_ffn(D, H, w1 + (size_t)e * H * D, w3 + (size_t)e * H * D,
+                       w2 + (size_t)e * D * H, ORC_F64, xt, 0, a, y);
+            for (int d = 0; d < D; ++d) o[d] += w[j] * y[d];
+        }
+    }
+    free(l); free(p); free(w); free(a); free(y);
+    return ORC_OK;
+}
+
+/*
+ * Gradients of L = sum_t <dout[t], out[t]> for the layer above.  Per token,
+ * with g = w1_e x, u = w3_e x, a = SiLU(g), h = a * u, y_j = w2_e h:
+ *   dw_j  = <dout, y_j>                 (the combine's backward: a dot per slot)
+ *   dy    = w_j dout                    (combine-bwd = dispatch, [EP] section 5)
+ *   dh    = w2_e^T dy;  du = dh * a;  dg = dh * u * SiLU'(g),
+ *           SiLU'(g) = s (1 + g (1 - s)),  s = 1 / (1 + exp(-g))
+ *   dx   += w1_e^T dg + w3_e^T du       (dispatch-bwd = combine over the slots)
+ *   dw2_e += dy h^T,  dw1_e += dg x^T,  dw3_e += du x^T
+ * Router, with dl = dL/dl over all E:
+ *   softmax:           dl_e = p_e (G_e - sum_j dw_j p_{S_j}),  G_e = dw_j if e = S_j
+ *   softmax, renorm:   dl_{S_j} = w_j (dw_j - sum_i dw_i w_i), 0 elsewhere
+ *   sigmoid:           dl_{S_j} = dw_j s_j (1 - s_j)
+ *   sigmoid, renorm:   dl_{S_j} = (dw_j - sum_i dw_i w_i) / sum_i s_i * s_j (1 - s_j)
+ *   dbias += dl,  dwg += dl x^T,  dx += wg^T dl.
+ * Outputs are overwritten (dx [T,D], dwg [E,D], dbias [E], dw1/dw3 [E,H,D],
+ * dw2 [E,D,H]); topk_idx receives the selection used.
+ */
+int oracle_moe_backward(int T, int D, int H, int E, int k, const double *x, const double *wg,
+                        const double *bias, const double *w1, const double *w3,
+                        const double *w2, int score, int renorm, int n_group, int topk_group,
+                        const double *dout, double *dx, double *dwg, double *dbias, double *dw1,
+                        double *dw3, double *dw2, int32_t *topk_idx)
+{
+    if (!backward_args_ok(D, H, E, k, n_group, topk_group)) return ORC_BAD_ARG;
+    memset(dx, 0, sizeof(double) * (size_t)T * D);
+    memset(dwg, 0, sizeof(double) * (size_t)E * D);
+    memset(dbias, 0, sizeof(double) * (size_t)E);
+    memset(dw1, 0, sizeof(double) * (size_t)E * H * D);
+    memset(dw3, 0, sizeof(double) * (size_t)E * H * D);
+    memset(dw2, 0, sizeof(double) * (size_t)E * D * H);
+    double *l = malloc(sizeof(double) * E), *p = malloc(sizeof(double) * E);
+    double *dl = malloc(sizeof(double) * E), *w = malloc(sizeof(double) * k);
+    double *dw = malloc(sizeof(double) * k), *g = malloc(sizeof(double) * H);
+    double *u = malloc(sizeof(double) * H), *hh = malloc(sizeof(double) * H);
+    double *dh = malloc(sizeof(double) * H), *y = malloc(sizeof(double) * D);
+    double *dy = malloc(sizeof(double) * D);
+    if (!l || !p || !dl || !w || !dw || !g || !u || !hh || !dh || !y || !dy) {
+        free(l); free(p); free(dl); free(w); free(dw); free(g); free(u); free(hh); free(dh);
+        free(y); free(dy);
+        return ORC_BAD_ARG;
+    }
+    for (int t = 0; t < T; ++t) {
+        const double *xt = x + (size_t)t * D;
+        const double *go = dout + (size_t)t * D;
+        double *gx = dx + (size_t)t * D;
+        for (int e = 0; e < E; ++e) {
+            double s = bias ? bias[e] : 0.0;
+            for (int d = 0; d < D; ++d) s += xt[d] * wg[(size_t)e * D + d];
+            l[e] = s;
+        }
+        int32_t *idx = topk_idx + (size_t)t * k;
+        select64(E, k, n_group, topk_group, l, idx);
+        weights64(E, k, l, idx, score, renorm, p, w);
+        /* experts */
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[j];
+            const double *W1 = w1 + (size_t)e * H * D, *W3 = w3 + (size_t)e * H * D;
+            const double *W2 = w2 + (size_t)e * D * H;
+            for (int c = 0; c < H; ++c) {
+                double gs = 0.0, us = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    gs += W1[(size_t)c * D + d] * xt[d];
+                    us += W3[(size_t)c * D + d] * xt[d];
+                }
+                g[c] = gs;
+                u[c] = us;
+                hh[c] = oracle_silu(gs) * us;
+            }
+            double dwj = 0.0;
+            for (int d = 0; d < D; ++d) {
+                double acc = 0.0;
+                for (int c = 0; c < H; ++c) acc += W2[(size_t)d * H + c] * hh[c];
+                y[d] = acc;
+                dwj += go[d] * acc;
+                dy[d] = w[j] * go[d];
+            }
+            dw[j] = dwj;
+            for (int c = 0; c < H; ++c) {
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d) acc += W2[(size_t)d * H + c] * dy[d];
+                dh[c] = acc;
+            }
+            double *G1 = dw1 + (size_t)e * H * D, *G3 = dw3 + (size_t)e * H * D;
+            double *G2 = dw2 + (size_t)e * D * H;
+            for (int d = 0; d < D; ++d)
+                for (int c = 0; c < H; ++c) G2[(size_t)d * H + c] += dy[d] * hh[c];
+            for (int c = 0; c < H; ++c) {
+                const double s = 1.0 / (1.0 + exp(-g[c]));
+                const double dgc = dh[c] * u[c] * s * (1.0 + g[c] * (1.0 - s));
+                const double duc = dh[c] * oracle_silu(g[c]);
+                for (int d = 0; d < D; ++d) {
+                    gx[d] += W1[(size_t)c * D + d] * dgc + W3[(size_t)c * D + d] * duc;
+                    G1[(size_t)c * D + d] += dgc * xt[d];
+                    G3[(size_t)c * D + d] += duc * xt[d];
+                }
+            }
+        }
+        /* router */
+        for (int e = 0; e < E; ++e) dl[e] = 0.0;
+        double dot = 0.0;
+        for (int j = 0; j < k; ++j) dot += dw[j] * w[j];
+        if (score == ORC_SOFTMAX && !renorm) {
+            double sp = 0.0;
+            for (int j = 0; j < k; ++j) sp += dw[j] * p[idx[j]];
+            for (int e = 0; e < E; ++e) dl[e] = -p[e] * sp;
+            for (int j = 0; j < k; ++j) dl[idx[j]] += p[idx[j]] * dw[j];
+        } else if (score == ORC_SOFTMAX) {
+            for (int j = 0; j < k; ++j) dl[idx[j]] = w[j] * (dw[j] - dot);
+        } else if (!renorm) {
+            for (int j = 0; j < k; ++j) dl[idx[j]] = dw[j] * p[idx[j]] * (1.0 - p[idx[j]]);
+        } else {
+            double ssum = 0.0;
+            for (int j = 0; j < k; ++j) ssum += p[idx[j]];
+            for (int j = 0; j < k; ++j)
+                dl[idx[j]] = (dw[j] - dot) / ssum * p[idx[j]] * (1.0 - p[idx[j]]);
+        }
+        for (int e = 0; e < E; ++e) {
+            if (dl[e] == 0.0) continue;
+            dbias[e] += dl[e];
+            for (int d = 0; d < D; ++d) {
+                dwg[(size_t)e * D + d] += dl[e] * xt[d];
+                gx[d] += wg[(size_t)e * D + d] * dl[e];
+            }
+        }
+    }
+    free(l); free(p); free(dl); free(w); free(dw); free(g); free(u); free(hh); free(dh);
+    free(y); free(dy);
+    return ORC_OK;
+}
