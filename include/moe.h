@@ -248,6 +248,54 @@ moe_status moe_layer_forward_host(const moe_config *cfg, const void *x_host, con
                                   moe_stream_t stream);
 
 /*
+ * Training: the forward that keeps what the backward needs, and the backward
+ * of the whole layer ("Expert Parallelism (EP)", section 5: the backward runs
+ * the forward in mirror -- the combine's backward is a dispatch of the output
+ * gradient times the slot weights, the dispatch's backward a combine -- with
+ * m-grouped dgrad and k-grouped wgrad GEMMs for the experts and the router
+ * differentiated through its score function; the top-k selection itself has
+ * no gradient).
+ *
+ * Supported: bf16, every expert and the whole H on this call (e_first = 0,
+ * E_local = E, H_local = H), D and H_local multiples of 64, align_m (masked:
+ * capacity) a multiple of 64; otherwise MOE_ERR_UNSUPPORTED.  The workspace
+ * (ws_bytes >= moe_layer_train_workspace_size(cfg), -1 when unsupported)
+ * holds the forward's intermediates plus the gate/up pre-activations [rows,
+ * 2H] and the router logits, and the backward's own buffers.
+ */
+int64_t moe_layer_train_workspace_size(const moe_config *cfg);
+
+/*
+ * moe_layer_forward that also keeps, in ws, the gate and up pre-activations
+ * (bf16) and the router logits.  Same output as moe_layer_forward.
+ */
+moe_status moe_layer_forward_train(const moe_config *cfg, const void *x, const void *wg,
+                                   const float *bias, const void *w1, const void *w3,
+                                   const void *w2, void *out, void *ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
+/*
+ * Gradients of L = sum(dout * out) for the forward last run with
+ * moe_layer_forward_train on the same ws and the same x, wg, w1, w3, w2.
+ *   dout [T, D] bf16: output gradient; dx [T, D] bf16: input gradient.
+ *   dwg [E, D], dbias [E] (or NULL), dw1 / dw3 [E, H, D], dw2 [E, D, H]: fp32,
+ *   overwritten.
+ * Per token t and slot j (row r, expert e, weight w_j):
+ *   gy[r] = w_j dout[t],  dw_j = <dout[t], y_perm[r]>;
+ *   dh = gy w2_e,  dg = dh * u * SiLU'(g),  du = dh * SiLU(g),
+ *   dx[t] = sum_j (dg w1_e + du w3_e)[r] + (dl[t] wg);
+ *   dw2_e = sum_r gy^T h,  dw1_e = sum_r dg^T x,  dw3_e = sum_r du^T x;
+ *   dl = the score function's backward of dw (softmax over E or sigmoid,
+ *   with renorm), dbias = sum_t dl,  dwg = dl^T x.
+ * The backward overwrites the padding rows of the saved x_perm and h with
+ * zeros.  Reduction orders are fixed: results are bit-identical run to run.
+ */
+moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *wg,
+                              const void *w1, const void *w3, const void *w2, const void *dout,
+                              void *dx, float *dwg, float *dbias, float *dw1, float *dw3,
+                              float *dw2, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_permute without a workspace (this entry point has no counterpart in
  * the pages; it exists for callers that cannot allocate device memory).
  *

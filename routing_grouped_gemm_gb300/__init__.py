@@ -32,6 +32,7 @@ ABI_SYMBOLS = (
     "moe_permute", "moe_grouped_swiglu", "moe_unpermute_combine", "moe_layer_forward",
     "moe_get_device_status", "moe_permute_noalloc", "moe_kernel_launches",
     "moe_layer_host_workspace_size", "moe_layer_forward_host",
+    "moe_layer_train_workspace_size", "moe_layer_forward_train", "moe_layer_backward",
 )
 
 
@@ -73,6 +74,9 @@ def _load() -> ctypes.CDLL:
         "moe_kernel_launches": (ctypes.c_uint64, []),
         "moe_layer_host_workspace_size": (I64, [C]),
         "moe_layer_forward_host": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_layer_train_workspace_size": (I64, [C]),
+        "moe_layer_forward_train": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_layer_backward": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -163,11 +167,19 @@ def layer_host_workspace_size(cfg: Config) -> int:
     return int(_lib.moe_layer_host_workspace_size(ctypes.byref(c)))
 
 
-def alloc_workspace(cfg: Config, layer: bool = False, device="cuda", host: bool = False) -> torch.Tensor:
+def layer_train_workspace_size(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_layer_train_workspace_size(ctypes.byref(c)))
+
+
+def alloc_workspace(cfg: Config, layer: bool = False, device="cuda", host: bool = False,
+                    train: bool = False) -> torch.Tensor:
     """Zero-filled workspace of the size the library asks for (torch-owned).
 
-    layer: for moe_layer_forward; host: for moe_layer_forward_host."""
-    n = (layer_host_workspace_size(cfg) if host else
+    layer: for moe_layer_forward; host: for moe_layer_forward_host; train: for
+    moe_layer_forward_train / moe_layer_backward."""
+    n = (layer_train_workspace_size(cfg) if train else
+         layer_host_workspace_size(cfg) if host else
          layer_workspace_size(cfg) if layer else workspace_size(cfg))
     if n < 0:
         raise MoeError(MOE_ERR_INVALID_ARG, "workspace size")
@@ -336,6 +348,44 @@ def moe_layer_forward_host(cfg: Config, x_host, wg, bias, w1, w3, w2, out_host, 
     _check(_lib.moe_layer_forward_host(ctypes.byref(c), x_host.data_ptr(), _ptr(wg), _ptr(bias),
                                        _ptr(w1), _ptr(w3), _ptr(w2), out_host.data_ptr(), _ptr(ws),
                                        ws.numel(), _stream(stream)), "moe_layer_forward_host")
+
+
+def moe_layer_forward_train(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None):
+    dt = cfg.torch_dtype
+    el = cfg.e_local
+    _expect(x, (cfg.T, cfg.D), dt, "x")
+    _expect(wg, (cfg.E, cfg.D), dt, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    _expect(out, (cfg.T, cfg.D), dt, "out")
+    c = cfg.c()
+    _check(_lib.moe_layer_forward_train(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w1),
+                                        _ptr(w3), _ptr(w2), _ptr(out), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "moe_layer_forward_train")
+
+
+def moe_layer_backward(cfg: Config, x, wg, w1, w3, w2, dout, dx, dwg, dbias, dw1, dw3, dw2, ws,
+                       stream=None):
+    """Gradients for the forward last run by moe_layer_forward_train on ws."""
+    dt = cfg.torch_dtype
+    el = cfg.e_local
+    f32 = torch.float32
+    _expect(dout, (cfg.T, cfg.D), dt, "dout")
+    _expect(dx, (cfg.T, cfg.D), dt, "dx")
+    _expect(dwg, (cfg.E, cfg.D), f32, "dwg")
+    if dbias is not None:
+        _expect(dbias, (cfg.E,), f32, "dbias")
+    _expect(dw1, (el, cfg.H_local, cfg.D), f32, "dw1")
+    _expect(dw3, (el, cfg.H_local, cfg.D), f32, "dw3")
+    _expect(dw2, (el, cfg.D, cfg.H_local), f32, "dw2")
+    c = cfg.c()
+    _check(_lib.moe_layer_backward(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(w1), _ptr(w3), _ptr(w2),
+                                   _ptr(dout), _ptr(dx), _ptr(dwg), _ptr(dbias), _ptr(dw1),
+                                   _ptr(dw3), _ptr(dw2), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_layer_backward")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

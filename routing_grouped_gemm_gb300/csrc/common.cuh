@@ -397,6 +397,22 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle, as
+// TMA writes boxes of 64 M (or N) elements x K rows: within a box the K rows
+// are 128 bytes apart (8-row groups 1024 bytes apart: SBO), and the next 64
+// M/N elements start in the next box, `chunk_bytes` further (LBO).  The
+// K-advance for one MMA (K = 16) is 16 rows = 2048 bytes.  (Checked on GB300
+// against a host product, with both operands MN-major as well.)
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t chunk_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)(chunk_bytes >> 4) << 16;       // leading byte offset: next 64 M/N elements
+    d |= (uint64_t)(1024u >> 4) << 32;              // stride byte offset: 8 K rows x 128 B
+    d |= (uint64_t)1 << 46;                         // descriptor version (tcgen05)
+    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4)                       // D format: f32
@@ -404,6 +420,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | (1u << 10)                    // B format: bf16
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// The same with A and/or B MN-major (transpose bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, int a_mn, int b_mn) {
+    return idesc_bf16_f32(M, N) | ((uint32_t)(a_mn != 0) << 15) | ((uint32_t)(b_mn != 0) << 16);
 }
 
 // ---------------------------------------------------------------------

@@ -1,0 +1,574 @@
+// Backward of the grouped SwiGLU experts on CTA pairs (tcgen05 cta_group::2).
+//
+// Page "Expert Parallelism (EP)" (llm-infra-atlas), section 5: the backward
+// mirrors the forward -- the expert weights get m-grouped dgrad GEMMs over
+// the same expert-contiguous layout and k-grouped wgrad GEMMs whose reduction
+// runs over each expert's rows.  With gy = dL/dy_perm (bf16), g and u the
+// forward's gate / up pre-activations (saved as gu [rows, 2H]), per expert e:
+//   dh   = gy_e . w2_e                  m-grouped, K = D   (w2_e [D, H]: B MN-major)
+//   dg   = dh * u * SiLU'(g),  du = dh * SiLU(g)       fused into dh's epilogue
+//   dxp  = [dg | du] . [w1_e ; w3_e]    m-grouped, K = 2H  (w1_e, w3_e [H, D]: B MN-major)
+//   dw2_e = gy_e^T . h_e                k-grouped, K = rows of e (both operands MN-major)
+//   [dw1_e ; dw3_e] = [dg | du]_e^T . x_e            k-grouped, K = rows of e
+// The operands are read in the layouts the forward already has: tcgen05
+// reads an MN-major operand straight from shared memory (transpose bits of
+// the instruction descriptor), so nothing is transposed in memory.
+//
+// Structure as the forward pair kernel: a cluster of two CTAs computes a
+// 256 x 256 tile with M=256 MMAs, each CTA holding 128 M rows of A and 128
+// N columns of B; warp 0 issues TMA into a 6-stage ring of 32 KB, warp 1 of
+// the leader issues the MMAs into one of two TMEM accumulators, warps 2-5 of
+// both CTAs drain them.  Every wait is bounded (FLAG_TIMEOUT).
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int B_BM = 128;                         // M rows per CTA
+constexpr int B_PAIR_M = 2 * B_BM;
+constexpr int B_BN = 256;                         // N of the pair MMA
+constexpr int B_BK = 64;
+constexpr int B_STAGES = 6;
+constexpr int B_A_BYTES = B_BM * B_BK * 2;        // 16 KB
+constexpr int B_B_BYTES = (B_BN / 2) * B_BK * 2;  // 16 KB: this CTA's half of B
+constexpr int B_STAGE_BYTES = B_A_BYTES + B_B_BYTES;
+constexpr int B_CHUNK = 64 * B_BK * 2;            // one MN-major box: 64 M/N elements x 64 K rows
+constexpr int B_EPI_WARPS = 4;
+constexpr int B_THREADS = 64 + 32 * B_EPI_WARPS;
+constexpr int B_ACC_COLS = 256;
+constexpr int B_TMEM_COLS = 512;
+constexpr int B_NBARS = 24;
+constexpr int B_SIGNALS = 2 * B_EPI_WARPS;
+
+enum : int {
+    BS_MGROUPED = 0,  // tiles over each expert's rows; K fixed
+    BS_KGROUPED = 1,  // tiles over a per-expert [M, N] output; K = the expert's rows
+};
+enum : int {
+    BE_STORE = 0,        // fp32 store
+    BE_SWIGLU_BWD = 1,   // dh -> dg, du (bf16) with the saved g, u
+};
+
+struct BwdParams {
+    int sched, epi;
+    int a_mn, b_mn;        // operand major-ness (1: MN-major)
+    int E_local, e_first, rows_alloc;
+    int M, N, nk;          // k-grouped: per-expert M x N; m-grouped: N and K / 64
+    int mt, nt;            // tiles along M (k-grouped) and N
+    int k_split;           // m-grouped: k-blocks >= k_split read B from tmB1 (at k - k_split)
+    const int *seg_off, *tpe;
+    float *out;            // BE_STORE: m-grouped [rows, N] (ld N); k-grouped [E_local, M, N]
+    float *out_hi;         // k-grouped: output rows m >= m_split go here ([E_local, M - m_split, N])
+    int m_split;           //   (M when unused)
+    const __nv_bfloat16 *gu;  // BE_SWIGLU_BWD: [rows, 2H] saved g | u
+    __nv_bfloat16 *dgu;       //                [rows, 2H] dg | du out
+    int H;
+    int *status;
+};
+
+size_t bwd_smem_bytes(int E_local) {
+    return 1024 + (size_t)B_STAGES * B_STAGE_BYTES + B_NBARS * sizeof(uint64_t) + 16 +
+           sizeof(int) * (4 * (size_t)E_local + 1);
+}
+
+struct BwdTile {
+    int expert;
+    int row0, nvalid, seg_rows;  // m-grouped: first row, valid rows (<= 256), rows to the segment end
+    int m0, n0;                  // k-grouped: output origin; m-grouped: n0
+    int kbase, nk;               // first K row (k-grouped) and k-blocks
+};
+
+__device__ __forceinline__ BwdTile decode_bwd(int v, const BwdParams &p, const int *s_mtoff,
+                                              const int *s_base, const int *s_valid,
+                                              const int *s_end) {
+    BwdTile c;
+    if (p.sched == BS_MGROUPED) {
+        const int blk = v / p.nt;
+        const int ni = v - blk * p.nt;
+        c.expert = tile_expert(s_mtoff, p.E_local, blk);
+        const int lm = blk - s_mtoff[c.expert];
+        c.row0 = s_base[c.expert] + lm * B_PAIR_M;
+        c.nvalid = min(B_PAIR_M, s_valid[c.expert] - lm * B_PAIR_M);
+        c.seg_rows = min(B_PAIR_M, s_end[c.expert] - c.row0);
+        c.m0 = 0;
+        c.n0 = ni * B_BN;
+        c.kbase = 0;
+        c.nk = p.nk;
+    } else {
+        const int per = p.mt * p.nt;
+        c.expert = v / per;
+        const int rem = v - c.expert * per;
+        const int mi = rem / p.nt;
+        c.m0 = mi * B_PAIR_M;
+        c.n0 = (rem - mi * p.nt) * B_BN;
+        c.row0 = 0;
+        c.nvalid = 0;
+        c.seg_rows = 0;
+        c.kbase = s_base[c.expert];
+        c.nk = (s_valid[c.expert] + B_BK - 1) / B_BK;
+    }
+    return c;
+}
+
+__global__ void __launch_bounds__(B_THREADS, 1)
+bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const BwdParams p) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + B_STAGES * B_STAGE_BYTES);
+    uint64_t *full = bars;                   // [B_STAGES]  leader: both CTAs' TMA -> MMA
+    uint64_t *empty = bars + B_STAGES;       // [B_STAGES]  MMA -> each CTA's TMA
+    uint64_t *tfull = bars + 2 * B_STAGES;   // [2]         MMA -> each CTA's epilogue
+    uint64_t *tempty = tfull + 2;            // [2]         leader: both epilogues -> MMA
+    uint64_t *drain = tempty + 2;            // [1]         leader: MMA completion at exit
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B_NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *s_base = reinterpret_cast<int *>(tmem_slot + 4);
+    int *s_valid = s_base + p.E_local;
+    int *s_end = s_valid + p.E_local;
+    int *s_mtoff = s_end + p.E_local;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        build_tile_table(lane, p.E_local, p.e_first, p.rows_alloc, B_PAIR_M, p.seg_off, p.tpe,
+                         s_base, s_valid, s_mtoff, blockIdx.x == 0 ? p.status : nullptr, s_end);
+        if (lane == 0) {
+            for (int s = 0; s < B_STAGES; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
+            }
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(&tfull[a], 1);
+                mbar_init(&tempty[a], B_SIGNALS);
+            }
+            mbar_init(drain, 1);
+            *abort_flag = 0;
+            fence_mbarrier_init();
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB0);
+            prefetch_tmap(&tmB1);
+        }
+    } else if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, B_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist before anything arrives on them
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_tiles =
+        p.sched == BS_MGROUPED ? s_mtoff[p.E_local] * p.nt : p.E_local * p.mt * p.nt;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = pair_id; ok && tile < total_tiles; tile += n_pairs) {
+                const BwdTile c = decode_bwd(tile, p, s_mtoff, s_base, s_valid, s_end);
+                for (int kb = 0; kb < c.nk; ++kb) {
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                    if (leader) mbar_arrive_expect_tx(&full[s], 2u * B_STAGE_BYTES);
+                    uint8_t *sa = ring + s * B_STAGE_BYTES;
+                    uint8_t *sb = sa + B_A_BYTES;
+                    const uint32_t fb = full_leader + (uint32_t)(s * sizeof(uint64_t));
+                    const int k0 = c.kbase + kb * B_BK;
+                    // A: this CTA's 128 M rows
+                    if (p.a_mn) {
+                        const int m = c.m0 + (int)rank * B_BM;
+                        tma_load_2d_pair(sa, &tmA, fb, m, k0);
+                        tma_load_2d_pair(sa + B_CHUNK, &tmA, fb, m + 64, k0);
+                    } else {
+                        tma_load_2d_pair(sa, &tmA, fb, k0, c.row0 + (int)rank * B_BM);
+                    }
+                    // B: this CTA's 128 N columns, MN-major
+                    const int n = c.n0 + (int)rank * (B_BN / 2);
+                    if (p.sched == BS_MGROUPED) {
+                        const bool hi = kb >= p.k_split;
+                        const CUtensorMap *tb = hi ? &tmB1 : &tmB0;
+                        const int kk = hi ? (kb - p.k_split) * B_BK : k0;
+                        tma_load_3d_pair(sb, tb, fb, n, kk, c.expert);
+                        tma_load_3d_pair(sb + B_CHUNK, tb, fb, n + 64, kk, c.expert);
+                    } else {
+                        tma_load_2d_pair(sb, &tmB0, fb, n, k0);
+                        tma_load_2d_pair(sb + B_CHUNK, &tmB0, fb, n + 64, k0);
+                    }
+                    if (++s == B_STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader CTA) ----------------
+            const uint32_t idesc = idesc_bf16_f32_major(B_PAIR_M, B_BN, p.a_mn, p.b_mn);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            int it = 0;
+            for (int tile = pair_id; ok && tile < total_tiles; tile += n_pairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+                const BwdTile c = decode_bwd(tile, p, s_mtoff, s_base, s_valid, s_end);
+                if (!mbar_wait_bounded(&tempty[acc], acc_ph ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * B_ACC_COLS);
+                for (int kb = 0; kb < c.nk; ++kb) {
+                    if (!mbar_wait_bounded(&full[s], ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(ring + s * B_STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + B_A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < B_BK / 16; ++kk) {
+                        const uint64_t da = p.a_mn ? sdesc_mnmajor_sw128(a_addr + kk * 2048, B_CHUNK)
+                                                   : sdesc_kmajor_sw128(a_addr + kk * 32);
+                        const uint64_t db = sdesc_mnmajor_sw128(b_addr + kk * 2048, B_CHUNK);
+                        tc_mma_f16_pair(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair(&empty[s], 0x3);
+                    if (++s == B_STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                // an expert without rows issues no MMA: its epilogue writes zeros
+                tc_commit_pair(&tfull[acc], 0x3);
+            }
+            tc_commit_pair(drain, 0x1);
+            volatile int local_abort = 0;
+            mbar_wait_bounded(drain, 0u, &local_abort);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
+        const int l = q * 32 + lane;  // this lane's accumulator row within the CTA
+        int it = 0;
+        for (int tile = pair_id; tile < total_tiles; tile += n_pairs, ++it) {
+            const BwdTile c = decode_bwd(tile, p, s_mtoff, s_base, s_valid, s_end);
+            const int acc = it & 1;
+            const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+            const bool got = mbar_wait_bounded(&tfull[acc], acc_ph, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * B_ACC_COLS);
+            if (p.sched == BS_MGROUPED) {
+                const int rl = (int)rank * B_BM + l;  // row within the pair tile
+                const int r = c.row0 + rl;
+                const bool valid = rl < c.nvalid;
+                const bool pad = !valid && rl < c.seg_rows;  // padding row of this segment
+#pragma unroll 1
+                for (int ch = 0; ch < B_BN / 32; ++ch) {
+                    uint32_t d[32];
+                    tmem_ld_32x32b_x32(tbase + ch * 32, d);
+                    tc_wait_ld();
+                    const int col0 = c.n0 + ch * 32;
+                    if (p.epi == BE_STORE) {
+                        if (valid) {
+                            float *o = p.out + (size_t)r * p.N;
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                if (col0 + v * 4 < p.N)
+                                    *reinterpret_cast<uint4 *>(o + col0 + v * 4) =
+                                        make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2], d[v * 4 + 3]);
+                        }
+                    } else if (valid || pad) {
+                        // dh -> dg, du; padding rows of the segment get zeros (the
+                        // k-grouped wgrad reads whole 64-row blocks)
+                        const size_t ld2 = 2 * (size_t)p.H;
+                        const __nv_bfloat16 *gr = p.gu + (size_t)r * ld2;
+                        __nv_bfloat16 *dr = p.dgu + (size_t)r * ld2;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int c8 = col0 + v * 8;
+                            if (c8 >= p.H) break;
+                            uint4 gq = make_uint4(0, 0, 0, 0), uq = make_uint4(0, 0, 0, 0);
+                            if (valid) {
+                                gq = *reinterpret_cast<const uint4 *>(gr + c8);
+                                uq = *reinterpret_cast<const uint4 *>(gr + p.H + c8);
+                            }
+                            const __nv_bfloat16 *gv = reinterpret_cast<const __nv_bfloat16 *>(&gq);
+                            const __nv_bfloat16 *uv = reinterpret_cast<const __nv_bfloat16 *>(&uq);
+                            uint32_t og[4], ou[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                float dg[2], du[2];
+#pragma unroll
+                                for (int z = 0; z < 2; ++z) {
+                                    const int i = v * 8 + e2 * 2 + z;
+                                    const float dh = valid ? __uint_as_float(d[i]) : 0.f;
+                                    const float g = __bfloat162float(gv[e2 * 2 + z]);
+                                    const float u = __bfloat162float(uv[e2 * 2 + z]);
+                                    const float sg = 1.f / (1.f + __expf(-g));
+                                    dg[z] = dh * u * sg * (1.f + g * (1.f - sg));
+                                    du[z] = dh * g * sg;
+                                }
+                                __nv_bfloat162 pg = __floats2bfloat162_rn(dg[0], dg[1]);
+                                __nv_bfloat162 pu = __floats2bfloat162_rn(du[0], du[1]);
+                                og[e2] = *reinterpret_cast<uint32_t *>(&pg);
+                                ou[e2] = *reinterpret_cast<uint32_t *>(&pu);
+                            }
+                            *reinterpret_cast<uint4 *>(dr + c8) = make_uint4(og[0], og[1], og[2], og[3]);
+                            *reinterpret_cast<uint4 *>(dr + p.H + c8) =
+                                make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                        }
+                    }
+                }
+            } else {
+                const int m = c.m0 + (int)rank * B_BM + l;
+                const bool empty_expert = c.nk == 0;
+                if (m < p.M) {
+                    float *o = m < p.m_split
+                                   ? p.out + ((size_t)c.expert * p.m_split + m) * p.N
+                                   : p.out_hi + ((size_t)c.expert * (p.M - p.m_split) + (m - p.m_split)) * p.N;
+#pragma unroll 1
+                    for (int ch = 0; ch < B_BN / 32; ++ch) {
+                        uint32_t d[32];
+                        tmem_ld_32x32b_x32(tbase + ch * 32, d);
+                        tc_wait_ld();
+                        const int col0 = c.n0 + ch * 32;
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            if (col0 + v * 4 < p.N)
+                                *reinterpret_cast<uint4 *>(o + col0 + v * 4) =
+                                    empty_expert ? make_uint4(0, 0, 0, 0)
+                                                 : make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2],
+                                                              d[v * 4 + 3]);
+                    }
+                } else {
+                    // keep the warp's TMEM loads uniform
+#pragma unroll 1
+                    for (int ch = 0; ch < B_BN / 32; ++ch) {
+                        uint32_t d[32];
+                        tmem_ld_32x32b_x32(tbase + ch * 32, d);
+                        tc_wait_ld();
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * sizeof(uint64_t)));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs (which read both CTAs' smem) are done
+    if (threadIdx.x == 0 && *abort_flag) {
+        raise_flag(p.status, FLAG_TIMEOUT);
+        atomicCAS(p.status + 1, 0, 1 + blockIdx.x);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, B_TMEM_COLS);
+    }
+}
+
+int max_bwd_clusters(size_t smem) {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev] = {0};
+    static size_t cached_smem[kMaxDev] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    if (cached[dev] > 0 && cached_smem[dev] == smem) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(B_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void *)bwd_pair_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cached[dev] = n;
+    cached_smem[dev] = smem;
+    return n;
+}
+
+cudaError_t launch_bwd(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                       const BwdParams &p, long long tiles, size_t smem, cudaStream_t stream) {
+    const int clusters_max = max_bwd_clusters(smem);
+    if (clusters_max <= 0) return cudaErrorLaunchOutOfResources;
+    const int clusters = (int)std::max<long long>(1, std::min<long long>(clusters_max, tiles));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(B_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = MOE_PDL ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_pair_kernel, a, b0, b1, p);
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
+
+// Rows of the permuted buffers that hold no token (token_of_row == -1) are
+// set to zero in each listed bf16 buffer, so that whole 64-row K blocks of a
+// segment can be reduced over.
+__global__ void __launch_bounds__(256)
+zero_pad_rows_kernel(const int *__restrict__ token_of_row, int64_t rows, __nv_bfloat16 *b0, int c0,
+                     __nv_bfloat16 *b1, int c1, __nv_bfloat16 *b2, int c2) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= rows || token_of_row[r] >= 0) return;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    __nv_bfloat16 *bufs[3] = {b0, b1, b2};
+    const int cols[3] = {c0, c1, c2};
+    for (int b = 0; b < 3; ++b) {
+        if (!bufs[b]) continue;
+        uint4 *row = reinterpret_cast<uint4 *>(bufs[b] + (size_t)r * cols[b]);
+        for (int v = lane; v < cols[b] / 8; v += 32) row[v] = z;
+    }
+}
+
+}  // namespace
+
+int64_t grouped_bwd_smem(int E_local) { return (int64_t)bwd_smem_bytes(E_local); }
+
+cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const void *gu,
+                                      const void *gy, const int *seg_offsets,
+                                      const int *tokens_per_expert, const int *token_of_row,
+                                      const void *w1, const void *w3, const void *w2,
+                                      void *dgu, float *dxp, float *dw1, float *dw3, float *dw2,
+                                      int D, int H_local, int e_first, int E_local,
+                                      int64_t rows_alloc, int *status, cudaStream_t stream) {
+    if (E_local == 0 || rows_alloc == 0) return cudaSuccess;
+    const size_t smem = bwd_smem_bytes(E_local);
+    if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+    cudaError_t err = ensure_smem((const void *)bwd_pair_kernel, smem);
+    if (err != cudaSuccess) return err;
+
+    // padding rows of the saved x_perm and h and of gy read as zeros
+    {
+        const int64_t blocks = (rows_alloc * 32 + 255) / 256;
+        if ((err = launch_pdl(zero_pad_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                              token_of_row, rows_alloc, (__nv_bfloat16 *)x_perm, D,
+                              (__nv_bfloat16 *)h, H_local, (__nv_bfloat16 *)gy, D)) != cudaSuccess)
+            return err;
+        count_launch();
+    }
+    const long long blk_bound = (rows_alloc + B_PAIR_M - 1) / B_PAIR_M + E_local;
+
+    BwdParams base{};
+    base.E_local = E_local;
+    base.e_first = e_first;
+    base.rows_alloc = (int)rows_alloc;
+    base.seg_off = seg_offsets;
+    base.tpe = tokens_per_expert;
+    base.status = status;
+    base.H = H_local;
+
+    CUtensorMap tA, tB0, tB1;
+    // 1. dh = gy . w2_e, fused SwiGLU backward -> dgu  (m-grouped, K = D)
+    {
+        BwdParams p = base;
+        p.sched = BS_MGROUPED;
+        p.epi = BE_SWIGLU_BWD;
+        p.a_mn = 0;
+        p.b_mn = 1;
+        p.N = H_local;
+        p.nk = D / B_BK;
+        p.nt = (H_local + B_BN - 1) / B_BN;
+        p.k_split = p.nk;
+        p.gu = (const __nv_bfloat16 *)gu;
+        p.dgu = (__nv_bfloat16 *)dgu;
+        if (!make_tmap_2d(&tA, gy, D, rows_alloc, B_BM) ||
+            !make_tmap_3d(&tB0, w2, H_local, D, E_local, B_BK))
+            return cudaErrorInvalidValue;
+        if ((err = launch_bwd(tA, tB0, tB0, p, blk_bound * p.nt, smem, stream)) != cudaSuccess)
+            return err;
+    }
+    // 2. dxp = [dg | du] . [w1_e ; w3_e]  (m-grouped, K = 2H, fp32 out)
+    {
+        BwdParams p = base;
+        p.sched = BS_MGROUPED;
+        p.epi = BE_STORE;
+        p.a_mn = 0;
+        p.b_mn = 1;
+        p.N = D;
+        p.nk = 2 * H_local / B_BK;
+        p.nt = (D + B_BN - 1) / B_BN;
+        p.k_split = H_local / B_BK;
+        p.out = dxp;
+        if (!make_tmap_2d(&tA, dgu, 2 * (uint64_t)H_local, rows_alloc, B_BM) ||
+            !make_tmap_3d(&tB0, w1, D, H_local, E_local, B_BK) ||
+            !make_tmap_3d(&tB1, w3, D, H_local, E_local, B_BK))
+            return cudaErrorInvalidValue;
+        if ((err = launch_bwd(tA, tB0, tB1, p, blk_bound * p.nt, smem, stream)) != cudaSuccess)
+            return err;
+    }
+    // 3. dw2_e = gy_e^T . h_e  (k-grouped: M = D, N = H)
+    {
+        BwdParams p = base;
+        p.sched = BS_KGROUPED;
+        p.epi = BE_STORE;
+        p.a_mn = 1;
+        p.b_mn = 1;
+        p.M = D;
+        p.N = H_local;
+        p.mt = (D + B_PAIR_M - 1) / B_PAIR_M;
+        p.nt = (H_local + B_BN - 1) / B_BN;
+        p.out = dw2;
+        p.out_hi = dw2;
+        p.m_split = D;
+        if (!make_tmap_2d(&tA, gy, D, rows_alloc, B_BK) ||
+            !make_tmap_2d(&tB0, h, H_local, rows_alloc, B_BK))
+            return cudaErrorInvalidValue;
+        if ((err = launch_bwd(tA, tB0, tB0, p, (long long)E_local * p.mt * p.nt, smem, stream)) !=
+            cudaSuccess)
+            return err;
+    }
+    // 4. [dw1_e ; dw3_e] = [dg | du]_e^T . x_e  (k-grouped: M = 2H, N = D)
+    {
+        BwdParams p = base;
+        p.sched = BS_KGROUPED;
+        p.epi = BE_STORE;
+        p.a_mn = 1;
+        p.b_mn = 1;
+        p.M = 2 * H_local;
+        p.N = D;
+        p.mt = (2 * H_local + B_PAIR_M - 1) / B_PAIR_M;
+        p.nt = (D + B_BN - 1) / B_BN;
+        p.out = dw1;
+        p.out_hi = dw3;
+        p.m_split = H_local;
+        if (!make_tmap_2d(&tA, dgu, 2 * (uint64_t)H_local, rows_alloc, B_BK) ||
+            !make_tmap_2d(&tB0, x_perm, D, rows_alloc, B_BK))
+            return cudaErrorInvalidValue;
+        if ((err = launch_bwd(tA, tB0, tB0, p, (long long)E_local * p.mt * p.nt, smem, stream)) !=
+            cudaSuccess)
+            return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

@@ -106,6 +106,7 @@ struct PairParams {
     const int *seg_off;
     const int *tpe;
     void *out0;           // bf16 h [rows, H_local]
+    __nv_bfloat16 *gu_out;  // training forward: g | u pre-activations [rows, 2 H_local] (or null)
     void *out1;           // fp32 y [rows, D]
     int *done;            // SCHED_BOTH: [max_blocks] GEMM1 epilogue warps finished, per block
     int max_blocks;       // SCHED_BOTH: entries of done[]
@@ -412,6 +413,12 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                                         const float uv = xb[j * 32 + lane];
                                         hcol[(size_t)(ch * 32 + j) * p.n_out0] =
                                             __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
+                                        if (p.gu_out) {
+                                            __nv_bfloat16 *gr = p.gu_out +
+                                                (size_t)(c.row0 + ch * 32 + j) * 2 * p.n_out0 + u;
+                                            gr[0] = __float2bfloat16_rn(gv);
+                                            gr[p.n_out0] = __float2bfloat16_rn(uv);
+                                        }
                                     }
                                 }
                             }
@@ -470,6 +477,22 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                                 }
                                 *reinterpret_cast<uint4 *>(hrow + col0 + v * 8) =
                                     make_uint4(w[0], w[1], w[2], w[3]);
+                                if (p.gu_out) {
+                                    // training forward: keep g and u for the backward
+                                    __nv_bfloat16 *gr = p.gu_out +
+                                        (size_t)(crow0 + r) * 2 * p.n_out0 + col0 + v * 8;
+                                    uint32_t pg[4], pu[4];
+#pragma unroll
+                                    for (int e2 = 0; e2 < 4; ++e2) {
+                                        pg[e2] = pack_bf16x2_p(__uint_as_float(g[v * 8 + e2 * 2]),
+                                                               __uint_as_float(g[v * 8 + e2 * 2 + 1]));
+                                        pu[e2] = pack_bf16x2_p(__uint_as_float(u[v * 8 + e2 * 2]),
+                                                               __uint_as_float(u[v * 8 + e2 * 2 + 1]));
+                                    }
+                                    *reinterpret_cast<uint4 *>(gr) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+                                    *reinterpret_cast<uint4 *>(gr + p.n_out0) =
+                                        make_uint4(pu[0], pu[1], pu[2], pu[3]);
+                                }
                             }
                         }
                     }
@@ -614,7 +637,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
                                             const void *w3, const void *w2, void *h, void *y_perm,
                                             int D, int H_local, int e_first, int E_local,
                                             int64_t rows_alloc, int *scratch, int *status,
-                                            cudaStream_t stream, bool *launched) {
+                                            cudaStream_t stream, bool *launched, void *gu) {
     *launched = false;
     if (E_local == 0 || rows_alloc == 0) {
         *launched = true;
@@ -654,6 +677,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     p.tpe = tokens_per_expert;
     p.out0 = h;
     p.out1 = y_perm;
+    p.gu_out = (__nv_bfloat16 *)gu;
     p.status = status;
 
     int dev = 0;

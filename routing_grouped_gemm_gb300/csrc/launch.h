@@ -105,7 +105,40 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
                                             const void *w3, const void *w2, void *h, void *y_perm,
                                             int D, int H_local, int e_first, int E_local,
                                             int64_t rows_alloc, int *scratch, int *status,
-                                            cudaStream_t stream, bool *launched);
+                                            cudaStream_t stream, bool *launched,
+                                            void *gu = nullptr);
+
+// Backward of the bf16 grouped SwiGLU on CTA pairs: dgu = SwiGLU'(gy . w2_e)
+// with the saved gate/up gu, dxp = dgu . [w1_e; w3_e] (fp32), and the weight
+// gradients dw1, dw3 [E_local, H, D], dw2 [E_local, D, H] (fp32).  Padding
+// rows of x_perm, h and gy are set to zero first.  Needs D and H_local
+// multiples of 64 and segments starting on multiples of 64 rows.
+cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const void *gu,
+                                      const void *gy, const int *seg_offsets,
+                                      const int *tokens_per_expert, const int *token_of_row,
+                                      const void *w1, const void *w3, const void *w2,
+                                      void *dgu, float *dxp, float *dw1, float *dw3, float *dw2,
+                                      int D, int H_local, int e_first, int E_local,
+                                      int64_t rows_alloc, int *status, cudaStream_t stream);
+int64_t grouped_bwd_smem(int E_local);
+
+// Backward of the combine: gy[row] = bf16(w * dout[t]) (rows without a token
+// untouched) and dw[t, j] = <dout[t], y_perm[row]>.
+cudaError_t launch_combine_bwd(const void *dout, const float *y_perm, const int *row_of,
+                               const float *topk_w, void *gy, float *dw, int T, int D, int k,
+                               int64_t rows_alloc, int is_bf16, int *status, cudaStream_t stream);
+
+// Backward of the dispatch: dx[t] = sum_j dxp[row_of[t, j]] (+ add[t] when add).
+cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float *add, void *dx,
+                                int T, int D, int k, int64_t rows_alloc, int is_bf16,
+                                cudaStream_t stream);
+
+// Backward of the router from dw: dl [T, E], dbias [E] (or null), dwg [E, D]
+// and the router's part of dx, dx_router [T, D] (fp32).
+cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits,
+                              const int *topk_idx, const float *topk_w, const float *dw, float *dl,
+                              float *dx_router, float *dwg, float *dbias, int T, int D, int E,
+                              int k, int score, int renorm, int is_bf16, cudaStream_t stream);
 
 // bf16 tcgen05 grouped SwiGLU (both GEMMs), one CTA per tile.
 cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offsets,

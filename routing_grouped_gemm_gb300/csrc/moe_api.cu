@@ -1,5 +1,6 @@
 // C ABI of the MoE layer local data path: argument validation, workspace
 // carving and the launch sequence.  Declarations and contracts: moe.h.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <atomic>
 #include <stdint.h>
@@ -15,7 +16,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 10200;  // 1.2.0
+constexpr int32_t kAbiVersion = 10300;  // 1.3.0
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int64_t kAlign = 256;
@@ -160,6 +161,64 @@ int64_t layer_ws_layout(const moe_config *c, char *base, LayerWs *L) {
         L->y_perm = p_yp;
     }
     return off;
+}
+
+// Training workspace: the layer workspace, then what the backward needs
+// besides it: the gate/up pre-activations gu [rows, 2H] (bf16), the router
+// logits [T, E], and the backward's own buffers gy [rows, D] (bf16), dgu
+// [rows, 2H] (bf16), dxp [rows, D], dw [T, k], dl [T, E], dx_router [T, D]
+// (fp32).
+struct TrainWs {
+    __nv_bfloat16 *gu, *gy, *dgu;
+    float *logits, *dxp, *dw, *dl, *dxr;
+};
+
+int64_t train_ws_layout(const moe_config *c, char *base, TrainWs *W) {
+    int64_t off = layer_ws_layout(c, nullptr, nullptr);
+    const int64_t rows = rows_alloc_of(c);
+    auto take = [&](int64_t bytes) -> char * {
+        char *p = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return p;
+    };
+    char *p_gu = take(rows * 2 * c->H_local * 2);
+    char *p_lg = take((int64_t)c->T * c->E * 4);
+    char *p_gy = take(rows * c->D * 2);
+    char *p_dgu = take(rows * 2 * c->H_local * 2);
+    char *p_dxp = take(rows * c->D * 4);
+    char *p_dw = take((int64_t)c->T * c->k * 4);
+    char *p_dl = take((int64_t)c->T * c->E * 4);
+    char *p_dxr = take((int64_t)c->T * c->D * 4);
+    if (W) {
+        W->gu = reinterpret_cast<__nv_bfloat16 *>(p_gu);
+        W->logits = reinterpret_cast<float *>(p_lg);
+        W->gy = reinterpret_cast<__nv_bfloat16 *>(p_gy);
+        W->dgu = reinterpret_cast<__nv_bfloat16 *>(p_dgu);
+        W->dxp = reinterpret_cast<float *>(p_dxp);
+        W->dw = reinterpret_cast<float *>(p_dw);
+        W->dl = reinterpret_cast<float *>(p_dl);
+        W->dxr = reinterpret_cast<float *>(p_dxr);
+    }
+    return off;
+}
+
+// What the training forward and the backward support: bf16, every expert
+// and the whole H on this call, dimensions in whole 64-element blocks and
+// segments on 64-row boundaries (the k-grouped weight gradients reduce over
+// whole 64-row blocks of each segment).
+moe_status train_supported(const moe_config *c) {
+    if (c->dtype != MOE_BF16) return arg_fail("training path: bf16 only", MOE_ERR_UNSUPPORTED);
+    if (c->e_first != 0 || c->E_local != c->E)
+        return arg_fail("training path: every expert on this call (no expert range)",
+                        MOE_ERR_UNSUPPORTED);
+    if (c->D % 64 || c->H_local % 64)
+        return arg_fail("training path: D and H_local must be multiples of 64", MOE_ERR_UNSUPPORTED);
+    if (c->layout == MOE_LAYOUT_CONTIGUOUS ? c->align_m % 64 != 0 : c->capacity % 64 != 0)
+        return arg_fail("training path: align_m (capacity) must be a multiple of 64",
+                        MOE_ERR_UNSUPPORTED);
+    if (moe::grouped_bwd_smem(c->E_local) > 227 * 1024)
+        return arg_fail("training path: too many experts for one CTA's tile table", MOE_ERR_UNSUPPORTED);
+    return MOE_OK;
 }
 
 bool need16(const void *p) { return p && aligned(p, 16); }
@@ -415,6 +474,93 @@ MOE_EXPORT moe_status moe_layer_forward_host(const moe_config *cfg, const void *
         return st;
     e = cudaMemcpyAsync(out_host, out_dev, (size_t)act_bytes(cfg), cudaMemcpyDeviceToHost, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_host: copy out");
+}
+
+MOE_EXPORT int64_t moe_layer_train_workspace_size(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK || train_supported(cfg) != MOE_OK) return -1;
+    return train_ws_layout(cfg, nullptr, nullptr);
+}
+
+MOE_EXPORT moe_status moe_layer_forward_train(const moe_config *cfg, const void *x, const void *wg,
+                                              const float *bias, const void *w1, const void *w3,
+                                              const void *w2, void *out, void *ws, size_t ws_bytes,
+                                              moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = train_supported(cfg)) != MOE_OK) return st;
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < train_ws_layout(cfg, nullptr, nullptr))
+        return arg_fail("workspace too small for moe_layer_forward_train", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!need16(x) || !need16(wg) || !need16(out) || (bias && !aligned(bias, 4)) || !need16(w1) ||
+        !need16(w3) || !need16(w2))
+        return arg_fail("moe_layer_forward_train: NULL or misaligned tensor");
+    LayerWs L;
+    TrainWs W;
+    carve_step(cfg, ws, ws_bytes, &L.step);
+    layer_ws_layout(cfg, static_cast<char *>(ws), &L);
+    train_ws_layout(cfg, static_cast<char *>(ws), &W);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = do_route(cfg, x, wg, bias, W.logits, L.topk_idx, L.topk_w, L.step, s)) != MOE_OK)
+        return st;
+    if ((st = do_permute(cfg, x, L.topk_idx, L.tpe, L.seg_off, L.row_of, L.token_of_row, L.x_perm,
+                         L.step, s)) != MOE_OK)
+        return st;
+    if (rows_alloc_of(cfg) > 0) {
+        bool launched = false;
+        cudaError_t e = moe::launch_grouped_swiglu_bf16_pair(
+            L.x_perm, L.seg_off, L.tpe, w1, w3, w2, L.h, L.y_perm, cfg->D, cfg->H_local,
+            cfg->e_first, cfg->E_local, rows_alloc_of(cfg), L.step.grouped, &L.step.status->flags, s,
+            &launched, W.gu);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_layer_forward_train: grouped SwiGLU");
+        if (!launched)
+            return arg_fail("moe_layer_forward_train: the CTA-pair kernel cannot run here",
+                            MOE_ERR_UNSUPPORTED);
+    }
+    return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
+}
+
+MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *wg,
+                                         const void *w1, const void *w3, const void *w2,
+                                         const void *dout, void *dx, float *dwg, float *dbias,
+                                         float *dw1, float *dw3, float *dw2, void *ws,
+                                         size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = train_supported(cfg)) != MOE_OK) return st;
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < train_ws_layout(cfg, nullptr, nullptr))
+        return arg_fail("workspace too small for moe_layer_backward", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!need16(x) || !need16(wg) || !need16(w1) || !need16(w3) || !need16(w2) || !need16(dout) ||
+        !need16(dx) || !need16(dwg) || !need16(dw1) || !need16(dw3) || !need16(dw2) ||
+        (dbias && !aligned(dbias, 4)))
+        return arg_fail("moe_layer_backward: NULL or misaligned tensor");
+    LayerWs L;
+    TrainWs W;
+    carve_step(cfg, ws, ws_bytes, &L.step);
+    layer_ws_layout(cfg, static_cast<char *>(ws), &L);
+    train_ws_layout(cfg, static_cast<char *>(ws), &W);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t rows = rows_alloc_of(cfg);
+    int *flags = &L.step.status->flags;
+    cudaError_t e = moe::launch_combine_bwd(dout, (const float *)L.y_perm, L.row_of, L.topk_w, W.gy,
+                                            W.dw, cfg->T, cfg->D, cfg->k, rows, 1, flags, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: combine backward");
+    if (rows > 0) {
+        e = moe::launch_grouped_swiglu_bwd(L.x_perm, L.h, W.gu, W.gy, L.seg_off, L.tpe,
+                                           L.token_of_row, w1, w3, w2, W.dgu, W.dxp, dw1, dw3, dw2,
+                                           cfg->D, cfg->H_local, cfg->e_first, cfg->E_local, rows,
+                                           flags, s);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: grouped SwiGLU backward");
+    }
+    e = moe::launch_router_bwd(x, wg, W.logits, L.topk_idx, L.topk_w, W.dw, W.dl, W.dxr, dwg, dbias,
+                               cfg->T, cfg->D, cfg->E, cfg->k, cfg->score, cfg->renorm, 1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: router backward");
+    e = moe::launch_dispatch_bwd(W.dxp, L.row_of, W.dxr, dx, cfg->T, cfg->D, cfg->k, rows, 1, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_backward: dispatch backward");
 }
 
 MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream) {

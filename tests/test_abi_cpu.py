@@ -122,6 +122,21 @@ def test_layer_host_workspace_size(moe):
     assert moe.layer_host_workspace_size(cfg) == moe.layer_workspace_size(cfg) + extra
 
 
+@pytest.mark.parametrize("over", [dict(dtype=1), dict(e_first=2, E_local=6), dict(D=96),
+                                  dict(H_local=80), dict(align_m=32)])
+def test_training_path_rejects_unsupported_configs(moe, over):
+    kw = dict(T=64, D=128, H_local=128, E=8, k=2)
+    kw.update(over)
+    if "dtype" in over:
+        kw["dtype"] = moe.MOE_F32
+    cfg = moe.Config(**kw)
+    assert moe.validate_config(cfg) == moe.MOE_OK
+    assert moe.layer_train_workspace_size(cfg) == -1
+    c = cfg.c()
+    assert moe._lib.moe_layer_forward_train(ctypes.byref(c), 0, 0, None, 0, 0, 0, 0, 0, 0, None) == \
+        moe.MOE_ERR_UNSUPPORTED
+
+
 def test_host_rejections_launch_nothing(moe):
     lib = moe._lib
     before = moe.kernel_launches()

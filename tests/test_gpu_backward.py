@@ -1,0 +1,139 @@
+"""GPU parity of the layer backward (moe_layer_forward_train + moe_layer_backward).
+
+Every gradient is compared with the oracle's fp64 backward of the fp64
+layer ("Expert Parallelism (EP)" page, section 5), evaluated on the very
+bf16 values the GPU holds.  The GPU keeps bf16 intermediates where the
+forward does (h, and the saved gate/up pre-activations) and where the
+backward feeds the tensor cores (gy = w * dout, and dg | du), each rounded
+once to nearest-even (relative error <= 2^-9 each); every contraction
+accumulates in fp32.
+
+Measures, per gradient: RMS(gpu - oracle) / RMS(oracle) and
+max |gpu - oracle| / max |oracle|, both bounded by GRAD_TOL.  Up to four
+bf16 roundings (h or g|u in the forward, gy, dg|du, and dx itself) reach an
+element, each <= 2^-9 of its magnitude, and the weight gradients sum them
+over an expert's rows with random signs: measured on GB300 the first ratio
+is 0.15-0.35% and the second 0.1-0.5% on every case here.  (max / RMS is not
+used: weight gradients are heavy-tailed, their largest entries about ten
+RMS out, so a rounding-level error on them reads as several percent.)
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+GRAD_TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import routing_grouped_gemm_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _bf(t):
+    return t.to(torch.bfloat16)
+
+
+def _f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _errs(got, ref):
+    err = got - ref
+    rms = float(np.sqrt(np.mean(err ** 2)) / (np.sqrt(np.mean(ref ** 2)) + 1e-30))
+    mx = float(np.max(np.abs(err)) / (np.max(np.abs(ref)) + 1e-30))
+    return rms, mx
+
+
+def _run(moe, T, D, H, E, k, score, renorm, seed, n_group=0, topk_group=0, empty_expert=None):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    x = _bf(torch.randn((T, D), generator=g, device="cuda"))
+    # router weights scaled so that logits are O(1..3): selections do not
+    # hinge on rounding-level ties
+    wg = _bf(torch.randn((E, D), generator=g, device="cuda") * (2.0 / D ** 0.5))
+    bias = torch.randn((E,), generator=g, device="cuda") * 0.1
+    if empty_expert is not None:
+        bias[empty_expert] = -30.0
+    w1 = _bf(torch.randn((E, H, D), generator=g, device="cuda") * 0.05)
+    w3 = _bf(torch.randn((E, H, D), generator=g, device="cuda") * 0.05)
+    w2 = _bf(torch.randn((E, D, H), generator=g, device="cuda") * 0.05)
+    dout = _bf(torch.randn((T, D), generator=g, device="cuda"))
+    cfg = moe.Config(T=T, D=D, H_local=H, E=E, k=k, dtype=moe.MOE_BF16,
+                     score=moe.MOE_SCORE_SOFTMAX if score == "softmax" else moe.MOE_SCORE_SIGMOID,
+                     renorm=int(renorm), n_group=n_group, topk_group=topk_group)
+    ws = moe.alloc_workspace(cfg, train=True)
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    moe.moe_layer_forward_train(cfg, x, wg, bias, w1, w3, w2, out, ws)
+    grads = dict(dx=torch.empty((T, D), dtype=torch.bfloat16, device="cuda"),
+                 dwg=torch.empty((E, D), device="cuda"), dbias=torch.empty((E,), device="cuda"),
+                 dw1=torch.empty((E, H, D), device="cuda"), dw3=torch.empty((E, H, D), device="cuda"),
+                 dw2=torch.empty((E, D, H), device="cuda"))
+    moe.moe_layer_backward(cfg, x, wg, w1, w3, w2, dout, grads["dx"], grads["dwg"], grads["dbias"],
+                           grads["dw1"], grads["dw3"], grads["dw2"], ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    inputs = dict(x=x, wg=wg, bias=bias, w1=w1, w3=w3, w2=w2, dout=dout)
+    return cfg, ws, out, grads, inputs
+
+
+def _oracle(inputs, k, score, renorm, n_group=0, topk_group=0):
+    f = {n: _f64(t) for n, t in inputs.items()}
+    sc = oracle.SOFTMAX if score == "softmax" else oracle.SIGMOID
+    return oracle.moe_backward(f["x"], f["wg"], f["bias"], f["w1"], f["w3"], f["w2"], f["dout"], k,
+                               sc, renorm, n_group, topk_group)
+
+
+CASES = [
+    # T, D, H, E, k, score, renorm, groups
+    (300, 256, 128, 8, 2, "softmax", True, (0, 0)),
+    (512, 512, 256, 16, 4, "softmax", True, (0, 0)),   # several 256-row blocks per expert
+    (256, 128, 192, 16, 4, "sigmoid", True, (4, 2)),
+    (200, 192, 64, 8, 2, "softmax", False, (0, 0)),
+    (150, 128, 128, 6, 3, "sigmoid", False, (0, 0)),
+]
+
+
+@pytest.mark.parametrize("T,D,H,E,k,score,renorm,groups", CASES)
+def test_backward_matches_oracle(moe, T, D, H, E, k, score, renorm, groups):
+    cfg, ws, out, grads, inputs = _run(moe, T, D, H, E, k, score, renorm, seed=T + E,
+                                       n_group=groups[0], topk_group=groups[1])
+    ref = _oracle(inputs, k, score, renorm, *groups)
+    views = moe.layer_views(cfg, ws)
+    # the same selection on both sides (fp32 keys vs fp64 logits, no near ties here)
+    assert np.array_equal(views["topk_idx"].cpu().numpy(), ref["topk_idx"])
+    for name in ("dx", "dwg", "dbias", "dw1", "dw3", "dw2"):
+        rms, mx = _errs(_f64(grads[name]), ref[name])
+        assert rms < GRAD_TOL and mx < GRAD_TOL, f"{name}: rms ratio {rms:.2e}, max ratio {mx:.2e}"
+
+
+def test_backward_empty_expert_and_determinism(moe):
+    T, D, H, E, k = 256, 128, 128, 8, 2
+    cfg, ws, out, grads, inputs = _run(moe, T, D, H, E, k, "softmax", True, seed=5, empty_expert=3)
+    ref = _oracle(inputs, k, "softmax", True)
+    assert 3 not in set(ref["topk_idx"].reshape(-1).tolist())
+    for name in ("dw1", "dw3", "dw2"):
+        assert (grads[name][3] == 0).all()
+    first = {n: t.clone() for n, t in grads.items()}
+    # the same forward and backward again: bit for bit
+    x, wg, bias, w1, w3, w2, dout = (inputs[n] for n in ("x", "wg", "bias", "w1", "w3", "w2", "dout"))
+    moe.moe_layer_forward_train(cfg, x, wg, bias, w1, w3, w2, out, ws)
+    moe.moe_layer_backward(cfg, x, wg, w1, w3, w2, dout, grads["dx"], grads["dwg"], grads["dbias"],
+                           grads["dw1"], grads["dw3"], grads["dw2"], ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    for n in first:
+        assert torch.equal(first[n], grads[n]), n
+
+
+def test_training_forward_equals_forward(moe):
+    T, D, H, E, k = 500, 256, 192, 16, 4
+    cfg, ws, out, grads, inputs = _run(moe, T, D, H, E, k, "softmax", True, seed=9)
+    lws = moe.alloc_workspace(cfg, layer=True)
+    ref = torch.empty_like(out)
+    moe.moe_layer_forward(cfg, inputs["x"], inputs["wg"], inputs["bias"], inputs["w1"], inputs["w3"],
+                          inputs["w2"], ref, lws)
+    assert moe.moe_get_device_status(lws) == moe.MOE_OK
+    assert torch.equal(out, ref)
