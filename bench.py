@@ -260,6 +260,66 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
 
 
 
+def run_backward(moe, cfg, inp, stream, dev, args, peaks):
+    """The training step's backward on the same batch: moe_layer_forward_train,
+    then moe_layer_backward (all gradients), timed with CUDA events on the
+    launching stream.  The expert GEMMs of the backward do 12 R D H FLOPs
+    (dgrad 6 R D H, wgrad 6 R D H)."""
+    import torch
+    w = inp.w
+    tws = moe.alloc_workspace(cfg, train=True, device=dev)
+    out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    g = torch.Generator(device=dev).manual_seed(1)
+    dout = torch.randn((w.T, w.D), generator=g, device=dev).to(torch.bfloat16)
+    dx = torch.empty_like(out)
+    dwg = torch.empty((w.E, w.D), device=dev)
+    dbias = torch.empty((w.E,), device=dev)
+    dw1 = torch.empty((w.E, w.H, w.D), device=dev)
+    dw3 = torch.empty((w.E, w.H, w.D), device=dev)
+    dw2 = torch.empty((w.E, w.D, w.H), device=dev)
+
+    def fwd():
+        moe.moe_layer_forward_train(cfg, inp.x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, tws,
+                                    stream)
+
+    def bwd():
+        moe.moe_layer_backward(cfg, inp.x, inp.wg, inp.w1, inp.w3, inp.w2, dout, dx, dwg, dbias,
+                               dw1, dw3, dw2, tws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    st = moe.moe_get_device_status(tws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after backward warm-up: {moe.status_string(st)}")
+    n = max(10, args.steps // 8)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    n0 = moe.kernel_launches()
+    for i in range(n):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    launches = (moe.kernel_launches() - n0) / n
+    torch.cuda.synchronize(dev)
+    st = moe.moe_get_device_status(tws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after backward: {moe.status_string(st)}")
+    f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n
+    flops = 12.0 * w.T * w.k * w.D * w.H
+    tf = flops / (b_ms * 1e-3) / 1e12
+    del tws, dw1, dw3, dw2
+    return {"api": "moe_layer_forward_train + moe_layer_backward (dx, dwg, dbias, dw1, dw3, dw2)",
+            "forward_train_ms": f_ms, "backward_ms": b_ms,
+            "training_step_tokens_per_s": w.T / ((f_ms + b_ms) * 1e-3),
+            "backward_expert_flops": flops, "backward_tflops": tf,
+            "backward_frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "launches_per_forward_and_backward": launches}
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -354,6 +414,9 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(moe, cfg, inp, out, stream, dev, world, args)
+    backward = None
+    if not args.no_backward:
+        backward = run_backward(moe, cfg, inp, stream, dev, args, load_peaks())
     alg = algorithmic(w)
     peaks = load_peaks()
     gemm_ms = float(mean_parts[2])
@@ -387,6 +450,7 @@ def run_gpu(args):
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
                               "zeros": int((tpe_h == 0).sum())},
         "e2e": e2e,
+        "backward": backward,
         "gpu_launches": n_launches,
         "clocks": clk.summary(),
     }
@@ -415,6 +479,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--no-backward", action="store_true", help="skip the training backward leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

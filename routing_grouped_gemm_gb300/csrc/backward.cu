@@ -74,29 +74,65 @@ combine_bwd_kernel(const void *__restrict__ dout, const float *__restrict__ y_pe
     }
 }
 
-// One warp per token: dx[t] = sum_j dxp[row_of[t, j]] (+ add[t]), fp32 in
-// slot order, rounded once to the output type.
+// One warp per token: dx[t] = sum_j dxp[row_of[t, j]] + r[t], fp32 in slot
+// order, rounded once to the output type; r[t] = add[t] when add, else (wg
+// given) sum_j dl[t, e_j] wg[e_j] in slot order.
 template <bool BF16>
 __global__ void __launch_bounds__(256)
 dispatch_bwd_kernel(const float *__restrict__ dxp, const int *__restrict__ row_of,
-                    const float *__restrict__ add, void *__restrict__ dx, int T, int k, int D,
-                    long long rows_alloc) {
+                    const float *__restrict__ add, const int *__restrict__ topk_idx,
+                    const float *__restrict__ dl, const void *__restrict__ wg, int E,
+                    void *__restrict__ dx, int T, int k, int D, long long rows_alloc) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     const int t = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
+    // lane j < k holds slot j: its row, its expert and dl at that expert
+    int my_r = -1, my_e = -1;
+    float my_g = 0.f;
+    if (lane < k) {
+        my_r = row_of[(size_t)t * k + lane];
+        if (my_r < 0 || (long long)my_r >= rows_alloc) my_r = -1;
+        if (!add && wg) {
+            my_e = topk_idx[(size_t)t * k + lane];
+            if (my_e < 0 || my_e >= E) my_e = -1;
+            else my_g = dl[(size_t)t * E + my_e];
+        }
+    }
     for (int d0 = lane * 4; d0 < D; d0 += 128) {
         float a[4] = {0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
-            const int r = row_of[(size_t)t * k + j];
-            if (r < 0 || (long long)r >= rows_alloc) continue;
+            const int r = __shfl_sync(0xffffffffu, my_r, j);
+            if (r < 0) continue;
             const float4 v = __ldcs(reinterpret_cast<const float4 *>(dxp + (size_t)r * D + d0));
             a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
         }
         if (add) {
             const float4 v = *reinterpret_cast<const float4 *>(add + (size_t)t * D + d0);
             a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
+        } else if (wg) {
+            for (int j = 0; j < k; ++j) {
+                const int e = __shfl_sync(0xffffffffu, my_e, j);
+                const float g = __shfl_sync(0xffffffffu, my_g, j);
+                if (e < 0) continue;
+                float w[4];
+                if (BF16) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(
+                        static_cast<const __nv_bfloat16 *>(wg) + (size_t)e * D + d0);
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+                    w[0] = __low2float(h2[0]);
+                    w[1] = __high2float(h2[0]);
+                    w[2] = __low2float(h2[1]);
+                    w[3] = __high2float(h2[1]);
+                } else {
+                    const float4 v = *reinterpret_cast<const float4 *>(
+                        static_cast<const float *>(wg) + (size_t)e * D + d0);
+                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = fmaf(g, w[i], a[i]);
+            }
         }
         if (BF16) {
             __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]);
@@ -167,79 +203,138 @@ router_dl_kernel(const float *__restrict__ logits, const int *__restrict__ topk_
     }
 }
 
-// C[m, n] = sum_k A(m, k) B(k, n) (+ C when accumulate), fp32, k ascending:
-// A(m, k) = a[m * a_m + k * a_k], B(k, n) = b[k * b_k + n * b_n]; a, b fp32
-// (ABF16 / BBF16: bf16).  64 x 64 tiles, 4 x 4 per thread.
-constexpr int SG_T = 64, SG_K = 16;
-template <bool ABF16, bool BBF16>
+// Split-K SIMT GEMM for the router's two products (fp32 FMAs; the router's
+// gradients stay in fp32):  split z computes
+//   C_z(m, n) = sum_{k in [z kc, (z+1) kc)} A(m, k) B(k, n),  k ascending,
+// A(m, k) = a[m * a_m + k * a_k] fp32 (a_m == 1 or a_k == 1), B(k, n) =
+// b[k * ldb + n] (bf16 or fp32), into c + z * M * N (row stride N).  When
+// colsum is given, the blocks of the first N tile also write
+// colsum[z * M + m] = sum_k A(m, k) over the split, in the same k order.
+// 64 x 128 tiles, 4 x 8 outputs per thread, N a multiple of 4.
+constexpr int RG_BM = 64, RG_BN = 128, RG_BK = 32, RG_PAD = 4;
+template <bool BBF16>
 __global__ void __launch_bounds__(256)
-simt_gemm_kernel(const void *__restrict__ a, long long a_m, long long a_k,
-                 const void *__restrict__ b, long long b_k, long long b_n, float *__restrict__ c,
-                 int M, int N, int K, int accumulate) {
+router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
+                   const void *__restrict__ b, long long ldb, float *__restrict__ c,
+                   float *__restrict__ colsum, int M, int N, int K, int kc) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
-    __shared__ float sa[SG_K][SG_T + 1], sb[SG_K][SG_T + 1];
-    const int m0 = blockIdx.y * SG_T, n0 = blockIdx.x * SG_T;
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    float acc[4][4] = {};
-    auto ld = [](const void *p, long long i, bool bf) -> float {
-        return bf ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i])
-                  : static_cast<const float *>(p)[i];
-    };
-    for (int k0 = 0; k0 < K; k0 += SG_K) {
-        for (int i = threadIdx.x; i < SG_K * SG_T; i += blockDim.x) {
-            const int kk = i / SG_T, mm = i % SG_T;
-            const int m = m0 + mm, n = n0 + mm, k = k0 + kk;
-            sa[kk][mm] = (m < M && k < K) ? ld(a, (long long)m * a_m + (long long)k * a_k, ABF16) : 0.f;
-            sb[kk][mm] = (n < N && k < K) ? ld(b, (long long)k * b_k + (long long)n * b_n, BBF16) : 0.f;
+    __shared__ __align__(16) float As[RG_BK][RG_BM + RG_PAD];
+    __shared__ __align__(16) float Bs[RG_BK][RG_BN];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int m0 = blockIdx.y * RG_BM, n0 = blockIdx.x * RG_BN, z = blockIdx.z;
+    const int kb = z * kc, ke = min(K, kb + kc);
+    const bool do_sum = colsum != nullptr && blockIdx.x == 0 && tid < RG_BM;
+    float acc[4][8] = {};
+    float cs = 0.f;
+    for (int k0 = kb; k0 < ke; k0 += RG_BK) {
+        if (a_m == 1) {  // m contiguous in memory: consecutive threads take consecutive m
+            for (int i = tid; i < RG_BK * RG_BM; i += 256) {
+                const int kk = i / RG_BM, mm = i % RG_BM, m = m0 + mm, k = k0 + kk;
+                As[kk][mm] = (m < M && k < ke) ? a[(long long)m + (long long)k * a_k] : 0.f;
+            }
+        } else {  // k contiguous
+            for (int i = tid; i < RG_BK * RG_BM; i += 256) {
+                const int kk = i % RG_BK, mm = i / RG_BK, m = m0 + mm, k = k0 + kk;
+                As[kk][mm] = (m < M && k < ke) ? a[(long long)m * a_m + (long long)k] : 0.f;
+            }
+        }
+        for (int i = tid; i < RG_BK * RG_BN / 4; i += 256) {
+            const int kk = i / (RG_BN / 4), nn = (i % (RG_BN / 4)) * 4, n = n0 + nn, k = k0 + kk;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (n < N && k < ke) {
+                if (BBF16) {
+                    const uint2 q = *reinterpret_cast<const uint2 *>(
+                        static_cast<const __nv_bfloat16 *>(b) + (long long)k * ldb + n);
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&q);
+                    v = make_float4(__low2float(h2[0]), __high2float(h2[0]), __low2float(h2[1]),
+                                    __high2float(h2[1]));
+                } else {
+                    v = *reinterpret_cast<const float4 *>(static_cast<const float *>(b) +
+                                                          (long long)k * ldb + n);
+                }
+            }
+            *reinterpret_cast<float4 *>(&Bs[kk][nn]) = v;
         }
         __syncthreads();
-#pragma unroll
-        for (int kk = 0; kk < SG_K; ++kk) {
-            float av[4], bv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                av[i] = sa[kk][ty * 4 + i];
-                bv[i] = sb[kk][tx * 4 + i];
-            }
+        if (do_sum)
+            for (int kk = 0; kk < RG_BK; ++kk) cs += As[kk][tid];
+#pragma unroll 8
+        for (int kk = 0; kk < RG_BK; ++kk) {
+            const float4 av = *reinterpret_cast<const float4 *>(&As[kk][ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[kk][RG_BN / 2 + tx * 4]);
+            const float ar[4] = {av.x, av.y, av.z, av.w};
+            const float br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
         }
         __syncthreads();
     }
+    float *cz = c + (size_t)z * M * N;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= M) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
-            if (m < M && n < N) {
-                float *p = c + (size_t)m * N + n;
-                *p = accumulate ? *p + acc[i][j] : acc[i][j];
-            }
+        for (int h = 0; h < 2; ++h) {
+            const int n = n0 + h * (RG_BN / 2) + tx * 4;
+            if (n < N)
+                *reinterpret_cast<float4 *>(cz + (size_t)m * N + n) =
+                    make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
+        }
+    }
+    if (do_sum && m0 + tid < M) colsum[(size_t)z * M + m0 + tid] = cs;
+}
+
+// out[i] = sum_z part[z * n + i], z ascending (n a multiple of 4); the same
+// for the column sums: bias_out[m] = sum_z bias_part[z * M + m].
+__global__ void __launch_bounds__(256)
+split_sum_kernel(const float *__restrict__ part, int S, long long n, float *__restrict__ out,
+                 const float *__restrict__ bias_part, int M, float *__restrict__ bias_out) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n / 4; i += stride) {
+        float4 s = reinterpret_cast<const float4 *>(part)[i];
+        for (int z = 1; z < S; ++z) {
+            const float4 v = reinterpret_cast<const float4 *>(part + (size_t)z * n)[i];
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
+        reinterpret_cast<float4 *>(out)[i] = s;
+    }
+    if (bias_out)
+        for (long long m = (long long)blockIdx.x * blockDim.x + threadIdx.x; m < M; m += stride) {
+            float s = bias_part[m];
+            for (int z = 1; z < S; ++z) s += bias_part[(size_t)z * M + m];
+            bias_out[m] = s;
         }
 }
 
-// dbias[e] = sum_t dl[t, e], tokens in order.
-__global__ void __launch_bounds__(256)
-column_sum_kernel(const float *__restrict__ dl, float *__restrict__ out, int T, int E) {
-    griddep_launch_dependents();  // the next kernel may be scheduled now
-    griddep_wait();               // every input of this kernel is complete
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    float s = 0.f;
-    for (int t = 0; t < T; ++t) s += dl[(size_t)t * E + e];
-    out[e] = s;
+// Splits of dwg's K (= T): enough (tile, split) blocks for two waves of the
+// 152 SMs, at least 256 tokens per split, at most 16 splits.
+struct RouterSplit {
+    int S, kc;
+};
+RouterSplit router_split(int T, int D, int E) {
+    const long long tiles = (long long)((E + RG_BM - 1) / RG_BM) * ((D + RG_BN - 1) / RG_BN);
+    long long S = std::max(1LL, (304 + tiles - 1) / tiles);
+    S = std::min<long long>({S, 16, std::max(1, T / 256)});
+    int kc = (int)(((T + S - 1) / S + RG_BK - 1) / RG_BK * RG_BK);
+    if (kc == 0) kc = RG_BK;
+    return {(int)((T + kc - 1) / kc), kc};
 }
 
-template <bool ABF16, bool BBF16>
-cudaError_t simt_gemm(const void *a, long long a_m, long long a_k, const void *b, long long b_k,
-                      long long b_n, float *c, int M, int N, int K, cudaStream_t stream) {
+template <bool BBF16>
+cudaError_t router_gemm(const float *a, long long a_m, long long a_k, const void *b, long long ldb,
+                        float *c, float *colsum, int M, int N, int K, int S, int kc,
+                        cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
-    const dim3 grid((N + SG_T - 1) / SG_T, (M + SG_T - 1) / SG_T);
-    const cudaError_t e = launch_pdl(simt_gemm_kernel<ABF16, BBF16>, grid, dim3(256), 0, stream, a,
-                                     a_m, a_k, b, b_k, b_n, c, M, N, K, 0);
+    const dim3 grid((N + RG_BN - 1) / RG_BN, (M + RG_BM - 1) / RG_BM, S);
+    const cudaError_t e = launch_pdl(router_gemm_kernel<BBF16>, grid, dim3(256), 0, stream, a, a_m,
+                                     a_k, b, ldb, c, colsum, M, N, K, kc);
     if (e == cudaSuccess) count_launch();
     return e;
 }
@@ -262,42 +357,57 @@ cudaError_t launch_combine_bwd(const void *dout, const float *y_perm, const int 
     return e;
 }
 
-cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float *add, void *dx,
-                                int T, int D, int k, int64_t rows_alloc, int is_bf16,
+cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float *add,
+                                const int *topk_idx, const float *dl, const void *wg, int E,
+                                void *dx, int T, int D, int k, int64_t rows_alloc, int is_bf16,
                                 cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
+    if (k > 32) return cudaErrorInvalidValue;  // one lane per slot
     const dim3 grid((unsigned)((T + 7) / 8));
     const cudaError_t e =
         is_bf16 ? launch_pdl(dispatch_bwd_kernel<true>, grid, dim3(256), 0, stream, dxp, row_of, add,
-                             dx, T, k, D, (long long)rows_alloc)
+                             topk_idx, dl, wg, E, dx, T, k, D, (long long)rows_alloc)
                 : launch_pdl(dispatch_bwd_kernel<false>, grid, dim3(256), 0, stream, dxp, row_of,
-                             add, dx, T, k, D, (long long)rows_alloc);
+                             add, topk_idx, dl, wg, E, dx, T, k, D, (long long)rows_alloc);
     if (e == cudaSuccess) count_launch();
     return e;
 }
 
+int64_t router_bwd_scratch_floats(int T, int D, int E) {
+    const RouterSplit sp = router_split(T, D, E);
+    return sp.S > 1 ? (int64_t)sp.S * E * D + (int64_t)sp.S * E : 0;
+}
+
 cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits,
                               const int *topk_idx, const float *topk_w, const float *dw, float *dl,
-                              float *dx_router, float *dwg, float *dbias, int T, int D, int E,
-                              int k, int score, int renorm, int is_bf16, cudaStream_t stream) {
+                              float *dx_router, float *dwg, float *dbias, float *scratch, int T,
+                              int D, int E, int k, int score, int renorm, int is_bf16,
+                              cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
+    if (D % 4) return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl(router_dl_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, stream,
                                logits, topk_idx, topk_w, dw, dl, T, E, k, score, renorm);
     if (e != cudaSuccess) return e;
     count_launch();
-    if (dbias) {
-        if ((e = launch_pdl(column_sum_kernel, dim3((unsigned)((E + 255) / 256)), dim3(256), 0,
-                            stream, (const float *)dl, dbias, T, E)) != cudaSuccess)
+    // dwg [E, D] = dl^T x  (K = T, split), dbias = the column sums of dl
+    const RouterSplit sp = router_split(T, D, E);
+    float *c = sp.S > 1 ? scratch : dwg;
+    float *cs = !dbias ? nullptr : (sp.S > 1 ? scratch + (size_t)sp.S * E * D : dbias);
+    e = is_bf16 ? router_gemm<true>(dl, 1, E, x, D, c, cs, E, D, T, sp.S, sp.kc, stream)
+                : router_gemm<false>(dl, 1, E, x, D, c, cs, E, D, T, sp.S, sp.kc, stream);
+    if (e != cudaSuccess) return e;
+    if (sp.S > 1) {
+        const long long n = (long long)E * D;
+        const unsigned blocks = (unsigned)std::min<long long>((n / 4 + 255) / 256, 4 * 152);
+        if ((e = launch_pdl(split_sum_kernel, dim3(blocks), dim3(256), 0, stream, (const float *)c,
+                            sp.S, n, dwg, (const float *)cs, E, dbias)) != cudaSuccess)
             return e;
         count_launch();
     }
-    // dwg [E, D] = dl^T x  (K = T);  dx_router [T, D] = dl wg  (K = E)
-    if (is_bf16) {
-        if ((e = simt_gemm<false, true>(dl, 1, E, x, D, 1, dwg, E, D, T, stream)) != cudaSuccess) return e;
-        return simt_gemm<false, true>(dl, E, 1, wg, D, 1, dx_router, T, D, E, stream);
-    }
-    if ((e = simt_gemm<false, false>(dl, 1, E, x, D, 1, dwg, E, D, T, stream)) != cudaSuccess) return e;
-    return simt_gemm<false, false>(dl, E, 1, wg, D, 1, dx_router, T, D, E, stream);
+    // dx_router [T, D] = dl wg  (K = E), only where dl is dense
+    if (!router_dl_dense(score, renorm)) return cudaSuccess;
+    return is_bf16 ? router_gemm<true>(dl, E, 1, wg, D, dx_router, nullptr, T, D, E, 1, E, stream)
+                   : router_gemm<false>(dl, E, 1, wg, D, dx_router, nullptr, T, D, E, 1, E, stream);
 }
 
 }  // namespace moe

@@ -33,7 +33,7 @@ constexpr int B_BM = 128;                         // M rows per CTA
 constexpr int B_PAIR_M = 2 * B_BM;
 constexpr int B_BN = 256;                         // N of the pair MMA
 constexpr int B_BK = 64;
-constexpr int B_STAGES = 6;
+constexpr int B_MAX_STAGES = 6;
 constexpr int B_A_BYTES = B_BM * B_BK * 2;        // 16 KB
 constexpr int B_B_BYTES = (B_BN / 2) * B_BK * 2;  // 16 KB: this CTA's half of B
 constexpr int B_STAGE_BYTES = B_A_BYTES + B_B_BYTES;
@@ -42,8 +42,14 @@ constexpr int B_EPI_WARPS = 4;
 constexpr int B_THREADS = 64 + 32 * B_EPI_WARPS;
 constexpr int B_ACC_COLS = 256;
 constexpr int B_TMEM_COLS = 512;
-constexpr int B_NBARS = 24;
+constexpr int B_NBARS = 32;
 constexpr int B_SIGNALS = 2 * B_EPI_WARPS;
+// Epilogue staging, per epilogue warp: two 4 KB output boxes (32 rows x 32
+// fp32, or the dg and du halves of 32 rows x 32 bf16 each) and, for the
+// SwiGLU backward, two 4 KB input boxes (the saved g and u of the chunk).
+constexpr int B_BOX_BYTES = 4096;
+constexpr int B_EPI_BYTES_STORE = 2 * B_BOX_BYTES;
+constexpr int B_EPI_BYTES_SWIGLU = 4 * B_BOX_BYTES;
 
 enum : int {
     BS_MGROUPED = 0,  // tiles over each expert's rows; K fixed
@@ -61,19 +67,26 @@ struct BwdParams {
     int M, N, nk;          // k-grouped: per-expert M x N; m-grouped: N and K / 64
     int mt, nt;            // tiles along M (k-grouped) and N
     int k_split;           // m-grouped: k-blocks >= k_split read B from tmB1 (at k - k_split)
+    int m_split;           // k-grouped: output rows m >= m_split go through the second output map
+    int stages;            // smem ring depth
+    int epi_bytes;         // staging bytes per epilogue warp
     const int *seg_off, *tpe;
-    float *out;            // BE_STORE: m-grouped [rows, N] (ld N); k-grouped [E_local, M, N]
-    float *out_hi;         // k-grouped: output rows m >= m_split go here ([E_local, M - m_split, N])
-    int m_split;           //   (M when unused)
-    const __nv_bfloat16 *gu;  // BE_SWIGLU_BWD: [rows, 2H] saved g | u
-    __nv_bfloat16 *dgu;       //                [rows, 2H] dg | du out
     int H;
     int *status;
 };
 
-size_t bwd_smem_bytes(int E_local) {
-    return 1024 + (size_t)B_STAGES * B_STAGE_BYTES + B_NBARS * sizeof(uint64_t) + 16 +
-           sizeof(int) * (4 * (size_t)E_local + 1);
+// Shared memory: 1 KB alignment slack, the ring, the epilogue staging, the
+// barriers, the TMEM slot / abort flag and the tile table.
+size_t bwd_smem_bytes(int E_local, int stages, int epi_bytes) {
+    return 1024 + (size_t)stages * B_STAGE_BYTES + (size_t)B_EPI_WARPS * epi_bytes +
+           B_NBARS * sizeof(uint64_t) + 16 + sizeof(int) * (4 * (size_t)E_local + 1);
+}
+
+// The deepest ring (at most B_MAX_STAGES, at least 2) that fits 227 KB.
+int bwd_stages(int E_local, int epi_bytes) {
+    for (int st = B_MAX_STAGES; st >= 2; --st)
+        if (bwd_smem_bytes(E_local, st, epi_bytes) <= 227 * 1024) return st;
+    return 0;
 }
 
 struct BwdTile {
@@ -117,18 +130,22 @@ __device__ __forceinline__ BwdTile decode_bwd(int v, const BwdParams &p, const i
 
 __global__ void __launch_bounds__(B_THREADS, 1)
 bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, const BwdParams p) {
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                const __grid_constant__ CUtensorMap tmO1, const BwdParams p) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + B_STAGES * B_STAGE_BYTES);
-    uint64_t *full = bars;                   // [B_STAGES]  leader: both CTAs' TMA -> MMA
-    uint64_t *empty = bars + B_STAGES;       // [B_STAGES]  MMA -> each CTA's TMA
-    uint64_t *tfull = bars + 2 * B_STAGES;   // [2]         MMA -> each CTA's epilogue
-    uint64_t *tempty = tfull + 2;            // [2]         leader: both epilogues -> MMA
-    uint64_t *drain = tempty + 2;            // [1]         leader: MMA completion at exit
+    const int n_st = p.stages;
+    uint8_t *epi = ring + n_st * B_STAGE_BYTES;  // 1 KB aligned
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + B_EPI_WARPS * p.epi_bytes);
+    uint64_t *full = bars;                       // [stages] leader: both CTAs' TMA -> MMA
+    uint64_t *empty = bars + B_MAX_STAGES;       // [stages] MMA -> each CTA's TMA
+    uint64_t *tfull = bars + 2 * B_MAX_STAGES;   // [2]      MMA -> each CTA's epilogue
+    uint64_t *tempty = tfull + 2;                // [2]      leader: both epilogues -> MMA
+    uint64_t *drain = tempty + 2;                // [1]      leader: MMA completion at exit
+    uint64_t *ldbar = drain + 1;                 // [2 per epilogue warp] g/u box loads
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B_NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *s_base = reinterpret_cast<int *>(tmem_slot + 4);
@@ -145,7 +162,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         build_tile_table(lane, p.E_local, p.e_first, p.rows_alloc, B_PAIR_M, p.seg_off, p.tpe,
                          s_base, s_valid, s_mtoff, blockIdx.x == 0 ? p.status : nullptr, s_end);
         if (lane == 0) {
-            for (int s = 0; s < B_STAGES; ++s) {
+            for (int s = 0; s < n_st; ++s) {
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], 1);
             }
@@ -154,11 +171,14 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 mbar_init(&tempty[a], B_SIGNALS);
             }
             mbar_init(drain, 1);
+            for (int i = 0; i < 2 * B_EPI_WARPS; ++i) mbar_init(&ldbar[i], 1);
             *abort_flag = 0;
             fence_mbarrier_init();
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB0);
             prefetch_tmap(&tmB1);
+            prefetch_tmap(&tmO0);
+            prefetch_tmap(&tmO1);
         }
     } else if (warp == 1) {
         tmem_alloc_pair(tmem_slot, B_TMEM_COLS);
@@ -209,7 +229,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         tma_load_2d_pair(sb, &tmB0, fb, n, k0);
                         tma_load_2d_pair(sb + B_CHUNK, &tmB0, fb, n + 64, k0);
                     }
-                    if (++s == B_STAGES) { s = 0; ph ^= 1u; }
+                    if (++s == n_st) { s = 0; ph ^= 1u; }
                 }
             }
         }
@@ -241,7 +261,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         tc_mma_f16_pair(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair(&empty[s], 0x3);
-                    if (++s == B_STAGES) { s = 0; ph ^= 1u; }
+                    if (++s == n_st) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 // an expert without rows issues no MMA: its epilogue writes zeros
@@ -253,114 +273,154 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     } else {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        // Each warp owns 32 accumulator rows (its TMEM lane quarter) and
+        // moves them out in 32-column chunks: TMEM -> registers -> a
+        // swizzled smem box -> one TMA store, double-buffered so a store
+        // drains while the next chunk is formed.  The SwiGLU backward also
+        // brings the chunk's saved g and u in by TMA, one chunk ahead.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int wi = warp - 2;
+        uint8_t *stg = epi + wi * p.epi_bytes;   // out boxes [0, 8 KB), in boxes [8, 16 KB)
+        uint64_t *lb = ldbar + 2 * wi;
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
-        const int l = q * 32 + lane;  // this lane's accumulator row within the CTA
+        const bool swiglu = p.epi == BE_SWIGLU_BWD;
+        uint32_t n_store = 0, n_load = 0, n_used = 0;  // warp-uniform counters
+        bool ok = true;
         int it = 0;
-        for (int tile = pair_id; tile < total_tiles; tile += n_pairs, ++it) {
+        for (int tile = pair_id; ok && tile < total_tiles; tile += n_pairs, ++it) {
             const BwdTile c = decode_bwd(tile, p, s_mtoff, s_base, s_valid, s_end);
             const int acc = it & 1;
             const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
-            const bool got = mbar_wait_bounded(&tfull[acc], acc_ph, abort_flag);
-            if (!__all_sync(0xffffffffu, got)) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * B_ACC_COLS);
+            const int wrow = (int)rank * B_BM + q * 32;  // this warp's first row in the pair tile
+            bool active;
+            int y0 = 0;  // the box's row coordinate
+            const CUtensorMap *to = &tmO0;
             if (p.sched == BS_MGROUPED) {
-                const int rl = (int)rank * B_BM + l;  // row within the pair tile
-                const int r = c.row0 + rl;
-                const bool valid = rl < c.nvalid;
-                const bool pad = !valid && rl < c.seg_rows;  // padding row of this segment
-#pragma unroll 1
-                for (int ch = 0; ch < B_BN / 32; ++ch) {
-                    uint32_t d[32];
-                    tmem_ld_32x32b_x32(tbase + ch * 32, d);
-                    tc_wait_ld();
-                    const int col0 = c.n0 + ch * 32;
-                    if (p.epi == BE_STORE) {
-                        if (valid) {
-                            float *o = p.out + (size_t)r * p.N;
-#pragma unroll
-                            for (int v = 0; v < 8; ++v)
-                                if (col0 + v * 4 < p.N)
-                                    *reinterpret_cast<uint4 *>(o + col0 + v * 4) =
-                                        make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2], d[v * 4 + 3]);
-                        }
-                    } else if (valid || pad) {
-                        // dh -> dg, du; padding rows of the segment get zeros (the
-                        // k-grouped wgrad reads whole 64-row blocks)
-                        const size_t ld2 = 2 * (size_t)p.H;
-                        const __nv_bfloat16 *gr = p.gu + (size_t)r * ld2;
-                        __nv_bfloat16 *dr = p.dgu + (size_t)r * ld2;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int c8 = col0 + v * 8;
-                            if (c8 >= p.H) break;
-                            uint4 gq = make_uint4(0, 0, 0, 0), uq = make_uint4(0, 0, 0, 0);
-                            if (valid) {
-                                gq = *reinterpret_cast<const uint4 *>(gr + c8);
-                                uq = *reinterpret_cast<const uint4 *>(gr + p.H + c8);
-                            }
-                            const __nv_bfloat16 *gv = reinterpret_cast<const __nv_bfloat16 *>(&gq);
-                            const __nv_bfloat16 *uv = reinterpret_cast<const __nv_bfloat16 *>(&uq);
-                            uint32_t og[4], ou[4];
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                float dg[2], du[2];
-#pragma unroll
-                                for (int z = 0; z < 2; ++z) {
-                                    const int i = v * 8 + e2 * 2 + z;
-                                    const float dh = valid ? __uint_as_float(d[i]) : 0.f;
-                                    const float g = __bfloat162float(gv[e2 * 2 + z]);
-                                    const float u = __bfloat162float(uv[e2 * 2 + z]);
-                                    const float sg = 1.f / (1.f + __expf(-g));
-                                    dg[z] = dh * u * sg * (1.f + g * (1.f - sg));
-                                    du[z] = dh * g * sg;
-                                }
-                                __nv_bfloat162 pg = __floats2bfloat162_rn(dg[0], dg[1]);
-                                __nv_bfloat162 pu = __floats2bfloat162_rn(du[0], du[1]);
-                                og[e2] = *reinterpret_cast<uint32_t *>(&pg);
-                                ou[e2] = *reinterpret_cast<uint32_t *>(&pu);
-                            }
-                            *reinterpret_cast<uint4 *>(dr + c8) = make_uint4(og[0], og[1], og[2], og[3]);
-                            *reinterpret_cast<uint4 *>(dr + p.H + c8) =
-                                make_uint4(ou[0], ou[1], ou[2], ou[3]);
-                        }
-                    }
-                }
+                active = wrow < c.seg_rows;  // segments end on 32-row boundaries
+                y0 = c.row0 + wrow;
             } else {
-                const int m = c.m0 + (int)rank * B_BM + l;
-                const bool empty_expert = c.nk == 0;
-                if (m < p.M) {
-                    float *o = m < p.m_split
-                                   ? p.out + ((size_t)c.expert * p.m_split + m) * p.N
-                                   : p.out_hi + ((size_t)c.expert * (p.M - p.m_split) + (m - p.m_split)) * p.N;
-#pragma unroll 1
-                    for (int ch = 0; ch < B_BN / 32; ++ch) {
-                        uint32_t d[32];
-                        tmem_ld_32x32b_x32(tbase + ch * 32, d);
-                        tc_wait_ld();
-                        const int col0 = c.n0 + ch * 32;
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            if (col0 + v * 4 < p.N)
-                                *reinterpret_cast<uint4 *>(o + col0 + v * 4) =
-                                    empty_expert ? make_uint4(0, 0, 0, 0)
-                                                 : make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2],
-                                                              d[v * 4 + 3]);
-                    }
+                const int m = c.m0 + wrow;
+                active = m < p.M;
+                if (m < p.m_split) {
+                    y0 = m;
                 } else {
-                    // keep the warp's TMEM loads uniform
-#pragma unroll 1
-                    for (int ch = 0; ch < B_BN / 32; ++ch) {
-                        uint32_t d[32];
-                        tmem_ld_32x32b_x32(tbase + ch * 32, d);
-                        tc_wait_ld();
-                    }
+                    y0 = m - p.m_split;
+                    to = &tmO1;
                 }
             }
+            const int n_ch = active ? min(B_BN / 32, (p.N - c.n0) / 32) : 0;
+            auto issue_load = [&](int ch) {  // g and u of chunk ch -> in box (n_load & 1)
+                if (lane == 0) {
+                    uint8_t *ib = stg + 2 * B_BOX_BYTES + (n_load & 1) * B_BOX_BYTES;
+                    uint64_t *bar = &lb[n_load & 1];
+                    const int col = c.n0 + ch * 32;
+                    mbar_arrive_expect_tx(bar, B_BOX_BYTES);
+                    tma_load_2d(ib, &tmO0, bar, col, y0);
+                    tma_load_2d(ib + B_BOX_BYTES / 2, &tmO0, bar, p.H + col, y0);
+                }
+                ++n_load;
+            };
+            if (swiglu && n_ch > 0) {
+                // the tile's g and u head for L2 while its MMAs run; chunk 0 for smem
+                if (lane < 2 * n_ch)
+                    tma_prefetch_l2_2d(&tmO0, (lane & 1 ? p.H : 0) + c.n0 + (lane >> 1) * 32, y0);
+                issue_load(0);
+            }
+            const bool got = mbar_wait_bounded(&tfull[acc], acc_ph, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * B_ACC_COLS);
+            const int rl = wrow + lane;  // this lane's row within the pair tile
+            const bool valid = rl < c.nvalid;
+            const bool empty_expert = p.sched == BS_KGROUPED && c.nk == 0;
+#pragma unroll 1
+            for (int ch = 0; ch < n_ch; ++ch) {
+                uint32_t d[32];
+                tmem_ld_32x32b_x32(tbase + ch * 32, d);
+                const uint8_t *ib = nullptr;
+                if (swiglu) {
+                    if (ch + 1 < n_ch) issue_load(ch + 1);
+                    const bool in_ok =
+                        mbar_wait_bounded(&lb[n_used & 1], (n_used >> 1) & 1u, abort_flag);
+                    ib = stg + 2 * B_BOX_BYTES + (n_used & 1) * B_BOX_BYTES;
+                    ++n_used;
+                    if (!__all_sync(0xffffffffu, in_ok)) { ok = false; break; }
+                }
+                tc_wait_ld();
+                if (lane == 0) bulk_wait_group_read<1>();  // this out box's previous store has read it
+                __syncwarp();
+                uint8_t *ob = stg + (n_store & 1) * B_BOX_BYTES;
+                const int col0 = c.n0 + ch * 32;
+                if (!swiglu) {
+                    // 32 x 32 fp32 box, 128-byte swizzle: 16-byte unit j of row r at (j ^ (r & 7))
+                    uint8_t *row = ob + lane * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 v = empty_expert ? make_uint4(0, 0, 0, 0)
+                                                     : make_uint4(d[j * 4], d[j * 4 + 1],
+                                                                  d[j * 4 + 2], d[j * 4 + 3]);
+                        *reinterpret_cast<uint4 *>(row + ((j ^ (lane & 7)) << 4)) = v;
+                    }
+                } else {
+                    // g, u in and dg, du out: 32 x 32 bf16 boxes, 64-byte swizzle: 16-byte unit
+                    // j of row r at (j ^ ((r >> 1) & 3)); dh -> dg = dh u s (1 + g (1 - s)),
+                    // du = dh g s (s the sigmoid of g); rows past the valid ones get zeros
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+                        const uint4 gq = *reinterpret_cast<const uint4 *>(ib + off);
+                        const uint4 uq = *reinterpret_cast<const uint4 *>(ib + B_BOX_BYTES / 2 + off);
+                        const __nv_bfloat16 *gv = reinterpret_cast<const __nv_bfloat16 *>(&gq);
+                        const __nv_bfloat16 *uv = reinterpret_cast<const __nv_bfloat16 *>(&uq);
+                        uint32_t og[4], ou[4];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            float dg[2], du[2];
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                const float dh = __uint_as_float(d[j * 8 + e2 * 2 + z]);
+                                const float g = __bfloat162float(gv[e2 * 2 + z]);
+                                const float u = __bfloat162float(uv[e2 * 2 + z]);
+                                const float sg = __fdividef(1.f, 1.f + __expf(-g));
+                                dg[z] = valid ? dh * u * sg * (1.f + g * (1.f - sg)) : 0.f;
+                                du[z] = valid ? dh * g * sg : 0.f;
+                            }
+                            __nv_bfloat162 pg = __floats2bfloat162_rn(dg[0], dg[1]);
+                            __nv_bfloat162 pu = __floats2bfloat162_rn(du[0], du[1]);
+                            og[e2] = *reinterpret_cast<uint32_t *>(&pg);
+                            ou[e2] = *reinterpret_cast<uint32_t *>(&pu);
+                        }
+                        *reinterpret_cast<uint4 *>(ob + off) = make_uint4(og[0], og[1], og[2], og[3]);
+                        *reinterpret_cast<uint4 *>(ob + B_BOX_BYTES / 2 + off) =
+                            make_uint4(ou[0], ou[1], ou[2], ou[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (swiglu) {
+                        tma_store_2d(&tmO1, ob, col0, y0);
+                        tma_store_2d(&tmO1, ob + B_BOX_BYTES / 2, p.H + col0, y0);
+                    } else if (p.sched == BS_MGROUPED) {
+                        tma_store_2d(to, ob, col0, y0);
+                    } else {
+                        tma_store_3d(to, ob, col0, y0, c.expert);
+                    }
+                    bulk_commit_group();
+                }
+                ++n_store;
+            }
+            if (!ok) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * sizeof(uint64_t)));
+        }
+        if (lane == 0) bulk_wait_group_all();  // every store has landed before the CTA exits
+        // a g/u load still in flight after an abort lands before the smem goes away
+        while (n_used < n_load) {
+            volatile int local_abort = 0;
+            mbar_wait_bounded(&lb[n_used & 1], (n_used >> 1) & 1u, &local_abort);
+            ++n_used;
         }
     }
 
@@ -406,7 +466,13 @@ int max_bwd_clusters(size_t smem) {
 }
 
 cudaError_t launch_bwd(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
-                       const BwdParams &p, long long tiles, size_t smem, cudaStream_t stream) {
+                       const CUtensorMap &o0, const CUtensorMap &o1, BwdParams p, long long tiles,
+                       cudaStream_t stream) {
+    p.stages = bwd_stages(p.E_local, p.epi_bytes);
+    if (p.stages == 0) return cudaErrorInvalidConfiguration;
+    const size_t smem = bwd_smem_bytes(p.E_local, p.stages, p.epi_bytes);
+    cudaError_t err = ensure_smem((const void *)bwd_pair_kernel, smem);
+    if (err != cudaSuccess) return err;
     const int clusters_max = max_bwd_clusters(smem);
     if (clusters_max <= 0) return cudaErrorLaunchOutOfResources;
     const int clusters = (int)std::max<long long>(1, std::min<long long>(clusters_max, tiles));
@@ -424,35 +490,48 @@ cudaError_t launch_bwd(const CUtensorMap &a, const CUtensorMap &b0, const CUtens
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = MOE_PDL ? 2 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_pair_kernel, a, b0, b1, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_pair_kernel, a, b0, b1, o0, o1, p);
     if (e == cudaSuccess) count_launch();
     return e;
 }
 
-// Rows of the permuted buffers that hold no token (token_of_row == -1) are
-// set to zero in each listed bf16 buffer, so that whole 64-row K blocks of a
-// segment can be reduced over.
+// The rows that the k-grouped weight gradients read past a segment's valid
+// rows -- [b + v, b + ceil64(v)) for local expert i with b = seg_off[i] and v
+// its valid rows -- are set to zero in each listed bf16 buffer, so whole
+// 64-row K blocks of a segment can be reduced over.  Block (i, y) takes
+// every gridDim.y-th such row of expert i.
 __global__ void __launch_bounds__(256)
-zero_pad_rows_kernel(const int *__restrict__ token_of_row, int64_t rows, __nv_bfloat16 *b0, int c0,
-                     __nv_bfloat16 *b1, int c1, __nv_bfloat16 *b2, int c2) {
+zero_pad_rows_kernel(const int *__restrict__ seg_off, const int *__restrict__ tpe, int e_first,
+                     int64_t rows, __nv_bfloat16 *b0, int c0, __nv_bfloat16 *b1, int c1,
+                     __nv_bfloat16 *b2, int c2) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
-    const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (r >= rows || token_of_row[r] >= 0) return;
+    const int i = blockIdx.x;
+    const int sb = seg_off[i], se = seg_off[i + 1];
+    const int c = tpe[e_first + i];
+    if (sb < 0 || se < sb || se > rows || c < 0) return;  // flagged by the GEMM kernels
+    const int v = min(c, se - sb);
+    const int pad_end = min(se, sb + (v + 63) / 64 * 64);
     const uint4 z = make_uint4(0, 0, 0, 0);
     __nv_bfloat16 *bufs[3] = {b0, b1, b2};
     const int cols[3] = {c0, c1, c2};
-    for (int b = 0; b < 3; ++b) {
-        if (!bufs[b]) continue;
-        uint4 *row = reinterpret_cast<uint4 *>(bufs[b] + (size_t)r * cols[b]);
-        for (int v = lane; v < cols[b] / 8; v += 32) row[v] = z;
-    }
+    for (int r = sb + v + (int)blockIdx.y; r < pad_end; r += (int)gridDim.y)
+        for (int q = 0; q < 3; ++q) {
+            if (!bufs[q]) continue;
+            uint4 *row = reinterpret_cast<uint4 *>(bufs[q] + (size_t)r * cols[q]);
+            for (int u = threadIdx.x; u < cols[q] / 8; u += blockDim.x) row[u] = z;
+        }
 }
 
 }  // namespace
 
-int64_t grouped_bwd_smem(int E_local) { return (int64_t)bwd_smem_bytes(E_local); }
+int64_t grouped_bwd_smem(int E_local) {
+    // the SwiGLU backward's staging is the larger; both need a ring of >= 2 stages
+    return bwd_stages(E_local, B_EPI_BYTES_SWIGLU) == 0
+               ? (int64_t)bwd_smem_bytes(E_local, 2, B_EPI_BYTES_SWIGLU)
+               : (int64_t)bwd_smem_bytes(E_local, bwd_stages(E_local, B_EPI_BYTES_SWIGLU),
+                                         B_EPI_BYTES_SWIGLU);
+}
 
 cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const void *gu,
                                       const void *gy, const int *seg_offsets,
@@ -461,22 +540,19 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
                                       void *dgu, float *dxp, float *dw1, float *dw3, float *dw2,
                                       int D, int H_local, int e_first, int E_local,
                                       int64_t rows_alloc, int *status, cudaStream_t stream) {
+    (void)token_of_row;
     if (E_local == 0 || rows_alloc == 0) return cudaSuccess;
-    const size_t smem = bwd_smem_bytes(E_local);
-    if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-    cudaError_t err = ensure_smem((const void *)bwd_pair_kernel, smem);
-    if (err != cudaSuccess) return err;
-
+    if (D % 32 || H_local % 32) return cudaErrorInvalidValue;  // whole 32-column boxes
+    cudaError_t err;
     // padding rows of the saved x_perm and h and of gy read as zeros
-    {
-        const int64_t blocks = (rows_alloc * 32 + 255) / 256;
-        if ((err = launch_pdl(zero_pad_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
-                              token_of_row, rows_alloc, (__nv_bfloat16 *)x_perm, D,
-                              (__nv_bfloat16 *)h, H_local, (__nv_bfloat16 *)gy, D)) != cudaSuccess)
-            return err;
-        count_launch();
-    }
+    if ((err = launch_pdl(zero_pad_rows_kernel, dim3((unsigned)E_local, 8), dim3(256), 0, stream,
+                          seg_offsets, tokens_per_expert, e_first, rows_alloc,
+                          (__nv_bfloat16 *)x_perm, D, (__nv_bfloat16 *)h, H_local,
+                          (__nv_bfloat16 *)gy, D)) != cudaSuccess)
+        return err;
+    count_launch();
     const long long blk_bound = (rows_alloc + B_PAIR_M - 1) / B_PAIR_M + E_local;
+    const uint64_t rows = (uint64_t)rows_alloc, H2 = 2 * (uint64_t)H_local;
 
     BwdParams base{};
     base.E_local = E_local;
@@ -486,25 +562,27 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
     base.tpe = tokens_per_expert;
     base.status = status;
     base.H = H_local;
+    base.epi_bytes = B_EPI_BYTES_STORE;
 
-    CUtensorMap tA, tB0, tB1;
+    CUtensorMap tA, tB0, tB1, tO0, tO1;
     // 1. dh = gy . w2_e, fused SwiGLU backward -> dgu  (m-grouped, K = D)
     {
         BwdParams p = base;
         p.sched = BS_MGROUPED;
         p.epi = BE_SWIGLU_BWD;
+        p.epi_bytes = B_EPI_BYTES_SWIGLU;
         p.a_mn = 0;
         p.b_mn = 1;
         p.N = H_local;
         p.nk = D / B_BK;
         p.nt = (H_local + B_BN - 1) / B_BN;
         p.k_split = p.nk;
-        p.gu = (const __nv_bfloat16 *)gu;
-        p.dgu = (__nv_bfloat16 *)dgu;
         if (!make_tmap_2d(&tA, gy, D, rows_alloc, B_BM) ||
-            !make_tmap_3d(&tB0, w2, H_local, D, E_local, B_BK))
+            !make_tmap_3d(&tB0, w2, H_local, D, E_local, B_BK) ||
+            !make_tmap_tile(&tO0, gu, 2, H2, rows, 0, 32, 32, 64) ||
+            !make_tmap_tile(&tO1, dgu, 2, H2, rows, 0, 32, 32, 64))
             return cudaErrorInvalidValue;
-        if ((err = launch_bwd(tA, tB0, tB0, p, blk_bound * p.nt, smem, stream)) != cudaSuccess)
+        if ((err = launch_bwd(tA, tB0, tB0, tO0, tO1, p, blk_bound * p.nt, stream)) != cudaSuccess)
             return err;
     }
     // 2. dxp = [dg | du] . [w1_e ; w3_e]  (m-grouped, K = 2H, fp32 out)
@@ -518,12 +596,12 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.nk = 2 * H_local / B_BK;
         p.nt = (D + B_BN - 1) / B_BN;
         p.k_split = H_local / B_BK;
-        p.out = dxp;
-        if (!make_tmap_2d(&tA, dgu, 2 * (uint64_t)H_local, rows_alloc, B_BM) ||
+        if (!make_tmap_2d(&tA, dgu, H2, rows_alloc, B_BM) ||
             !make_tmap_3d(&tB0, w1, D, H_local, E_local, B_BK) ||
-            !make_tmap_3d(&tB1, w3, D, H_local, E_local, B_BK))
+            !make_tmap_3d(&tB1, w3, D, H_local, E_local, B_BK) ||
+            !make_tmap_tile(&tO0, dxp, 4, D, rows, 0, 32, 32, 128))
             return cudaErrorInvalidValue;
-        if ((err = launch_bwd(tA, tB0, tB1, p, blk_bound * p.nt, smem, stream)) != cudaSuccess)
+        if ((err = launch_bwd(tA, tB0, tB1, tO0, tO0, p, blk_bound * p.nt, stream)) != cudaSuccess)
             return err;
     }
     // 3. dw2_e = gy_e^T . h_e  (k-grouped: M = D, N = H)
@@ -537,14 +615,13 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.N = H_local;
         p.mt = (D + B_PAIR_M - 1) / B_PAIR_M;
         p.nt = (H_local + B_BN - 1) / B_BN;
-        p.out = dw2;
-        p.out_hi = dw2;
         p.m_split = D;
         if (!make_tmap_2d(&tA, gy, D, rows_alloc, B_BK) ||
-            !make_tmap_2d(&tB0, h, H_local, rows_alloc, B_BK))
+            !make_tmap_2d(&tB0, h, H_local, rows_alloc, B_BK) ||
+            !make_tmap_tile(&tO0, dw2, 4, H_local, D, E_local, 32, 32, 128))
             return cudaErrorInvalidValue;
-        if ((err = launch_bwd(tA, tB0, tB0, p, (long long)E_local * p.mt * p.nt, smem, stream)) !=
-            cudaSuccess)
+        if ((err = launch_bwd(tA, tB0, tB0, tO0, tO0, p, (long long)E_local * p.mt * p.nt,
+                              stream)) != cudaSuccess)
             return err;
     }
     // 4. [dw1_e ; dw3_e] = [dg | du]_e^T . x_e  (k-grouped: M = 2H, N = D)
@@ -558,14 +635,14 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.N = D;
         p.mt = (2 * H_local + B_PAIR_M - 1) / B_PAIR_M;
         p.nt = (D + B_BN - 1) / B_BN;
-        p.out = dw1;
-        p.out_hi = dw3;
         p.m_split = H_local;
-        if (!make_tmap_2d(&tA, dgu, 2 * (uint64_t)H_local, rows_alloc, B_BK) ||
-            !make_tmap_2d(&tB0, x_perm, D, rows_alloc, B_BK))
+        if (!make_tmap_2d(&tA, dgu, H2, rows_alloc, B_BK) ||
+            !make_tmap_2d(&tB0, x_perm, D, rows_alloc, B_BK) ||
+            !make_tmap_tile(&tO0, dw1, 4, D, H_local, E_local, 32, 32, 128) ||
+            !make_tmap_tile(&tO1, dw3, 4, D, H_local, E_local, 32, 32, 128))
             return cudaErrorInvalidValue;
-        if ((err = launch_bwd(tA, tB0, tB0, p, (long long)E_local * p.mt * p.nt, smem, stream)) !=
-            cudaSuccess)
+        if ((err = launch_bwd(tA, tB0, tB0, tO0, tO1, p, (long long)E_local * p.mt * p.nt,
+                              stream)) != cudaSuccess)
             return err;
     }
     return cudaSuccess;

@@ -48,6 +48,11 @@ bool make_tmap_3d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows
 // fp32 row-major [rows, cols], box = box_cols x box_rows, 128-byte swizzle.
 bool make_tmap_2d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
                       uint32_t box_cols, uint32_t box_rows);
+// Row-major [experts, rows, cols] (experts = 0: a 2-D [rows, cols]) of 2- or 4-byte
+// elements (bf16 / fp32), box = box_cols x box_rows (x 1), swizzle of
+// 32, 64 or 128 bytes (box_cols x element bytes must equal it).
+bool make_tmap_tile(CUtensorMap *m, const void *base, int elem_bytes, uint64_t cols, uint64_t rows,
+                    uint64_t experts, uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
 int sm_count();  // SMs of the current device (0 on error)
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
@@ -128,17 +133,31 @@ cudaError_t launch_combine_bwd(const void *dout, const float *y_perm, const int 
                                const float *topk_w, void *gy, float *dw, int T, int D, int k,
                                int64_t rows_alloc, int is_bf16, int *status, cudaStream_t stream);
 
-// Backward of the dispatch: dx[t] = sum_j dxp[row_of[t, j]] (+ add[t] when add).
-cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float *add, void *dx,
-                                int T, int D, int k, int64_t rows_alloc, int is_bf16,
+// Backward of the dispatch: dx[t] = sum_j dxp[row_of[t, j]] + r[t], where
+// r[t] = add[t] when add, else sum_j dl[t, e_j] wg[e_j] (e_j = topk_idx[t, j];
+// the router's part of dx when dl is zero off the selected experts), else 0.
+cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float *add,
+                                const int *topk_idx, const float *dl, const void *wg, int E,
+                                void *dx, int T, int D, int k, int64_t rows_alloc, int is_bf16,
                                 cudaStream_t stream);
 
+// dl is dense (every expert's logit gets a gradient) only for a softmax
+// over all E without renormalisation; otherwise it is zero off the k
+// selected experts of each token.
+inline bool router_dl_dense(int score, int renorm) { return score == 0 && !renorm; }
+
+// Floats of scratch launch_router_bwd needs for the split-K partials of
+// dwg and dbias (0 when one split suffices).
+int64_t router_bwd_scratch_floats(int T, int D, int E);
+
 // Backward of the router from dw: dl [T, E], dbias [E] (or null), dwg [E, D]
-// and the router's part of dx, dx_router [T, D] (fp32).
+// and, when router_dl_dense, the router's part of dx, dx_router [T, D]
+// (fp32); otherwise dx_router is left to launch_dispatch_bwd.
 cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits,
                               const int *topk_idx, const float *topk_w, const float *dw, float *dl,
-                              float *dx_router, float *dwg, float *dbias, int T, int D, int E,
-                              int k, int score, int renorm, int is_bf16, cudaStream_t stream);
+                              float *dx_router, float *dwg, float *dbias, float *scratch, int T,
+                              int D, int E, int k, int score, int renorm, int is_bf16,
+                              cudaStream_t stream);
 
 // bf16 tcgen05 grouped SwiGLU (both GEMMs), one CTA per tile.
 cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offsets,

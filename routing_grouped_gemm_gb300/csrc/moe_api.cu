@@ -167,10 +167,10 @@ int64_t layer_ws_layout(const moe_config *c, char *base, LayerWs *L) {
 // besides it: the gate/up pre-activations gu [rows, 2H] (bf16), the router
 // logits [T, E], and the backward's own buffers gy [rows, D] (bf16), dgu
 // [rows, 2H] (bf16), dxp [rows, D], dw [T, k], dl [T, E], dx_router [T, D]
-// (fp32).
+// and the router backward's split-K partials (fp32).
 struct TrainWs {
     __nv_bfloat16 *gu, *gy, *dgu;
-    float *logits, *dxp, *dw, *dl, *dxr;
+    float *logits, *dxp, *dw, *dl, *dxr, *rsplit;
 };
 
 int64_t train_ws_layout(const moe_config *c, char *base, TrainWs *W) {
@@ -189,6 +189,7 @@ int64_t train_ws_layout(const moe_config *c, char *base, TrainWs *W) {
     char *p_dw = take((int64_t)c->T * c->k * 4);
     char *p_dl = take((int64_t)c->T * c->E * 4);
     char *p_dxr = take((int64_t)c->T * c->D * 4);
+    char *p_rs = take(moe::router_bwd_scratch_floats(c->T, c->D, c->E) * 4);
     if (W) {
         W->gu = reinterpret_cast<__nv_bfloat16 *>(p_gu);
         W->logits = reinterpret_cast<float *>(p_lg);
@@ -198,6 +199,7 @@ int64_t train_ws_layout(const moe_config *c, char *base, TrainWs *W) {
         W->dw = reinterpret_cast<float *>(p_dw);
         W->dl = reinterpret_cast<float *>(p_dl);
         W->dxr = reinterpret_cast<float *>(p_dxr);
+        W->rsplit = reinterpret_cast<float *>(p_rs);
     }
     return off;
 }
@@ -509,10 +511,12 @@ MOE_EXPORT moe_status moe_layer_forward_train(const moe_config *cfg, const void 
         return st;
     if (rows_alloc_of(cfg) > 0) {
         bool launched = false;
+        const char *sel = getenv("MOE_GROUPED_KERNEL");  // "pair2": two launches, as in do_grouped
+        const bool two_launches = sel && strcmp(sel, "pair2") == 0;
         cudaError_t e = moe::launch_grouped_swiglu_bf16_pair(
             L.x_perm, L.seg_off, L.tpe, w1, w3, w2, L.h, L.y_perm, cfg->D, cfg->H_local,
-            cfg->e_first, cfg->E_local, rows_alloc_of(cfg), L.step.grouped, &L.step.status->flags, s,
-            &launched, W.gu);
+            cfg->e_first, cfg->E_local, rows_alloc_of(cfg), two_launches ? nullptr : L.step.grouped,
+            &L.step.status->flags, s, &launched, W.gu);
         if (e != cudaSuccess) return cuda_fail(e, "moe_layer_forward_train: grouped SwiGLU");
         if (!launched)
             return arg_fail("moe_layer_forward_train: the CTA-pair kernel cannot run here",
@@ -557,9 +561,13 @@ MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, c
         if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: grouped SwiGLU backward");
     }
     e = moe::launch_router_bwd(x, wg, W.logits, L.topk_idx, L.topk_w, W.dw, W.dl, W.dxr, dwg, dbias,
-                               cfg->T, cfg->D, cfg->E, cfg->k, cfg->score, cfg->renorm, 1, s);
+                               W.rsplit, cfg->T, cfg->D, cfg->E, cfg->k, cfg->score, cfg->renorm, 1,
+                               s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: router backward");
-    e = moe::launch_dispatch_bwd(W.dxp, L.row_of, W.dxr, dx, cfg->T, cfg->D, cfg->k, rows, 1, s);
+    // the router's part of dx: a GEMM where dl is dense, else folded in here
+    const bool dense = moe::router_dl_dense(cfg->score, cfg->renorm);
+    e = moe::launch_dispatch_bwd(W.dxp, L.row_of, dense ? W.dxr : nullptr, L.topk_idx, W.dl, wg,
+                                 cfg->E, dx, cfg->T, cfg->D, cfg->k, rows, 1, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_backward: dispatch backward");
 }
 
