@@ -17,11 +17,31 @@
 namespace moe {
 namespace {
 
+// Slots handled together: their loads are issued before any of them is
+// used, so a warp keeps BW_SLOTS row reads in flight.
+constexpr int BW_SLOTS = 8;
+constexpr int DB_SLOTS = 4;  // the dispatch backward also holds wg rows: fewer registers
+
+__device__ __forceinline__ void load4(const void *p, size_t i, bool bf16, float (&g)[4]) {
+    if (bf16) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p) + i);
+        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+        g[0] = __low2float(h2[0]);
+        g[1] = __high2float(h2[0]);
+        g[2] = __low2float(h2[1]);
+        g[3] = __high2float(h2[1]);
+    } else {
+        const float4 v = *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+        g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+    }
+}
+
 // One warp per token.  gy[row] = bf16(w_j * dout[t]) for each slot j whose
-// row is in the buffer; dw[t, j] = <dout[t], y_perm[row]> (fp32, lanes'
-// partial sums added in a fixed butterfly order), 0 for a slot without row.
+// row is in the buffer; dw[t, j] = <dout[t], y_perm[row]> (fp32: each lane
+// sums its columns in order, then the lanes' sums are added in a fixed
+// butterfly order), 0 for a slot without row.
 template <bool BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 combine_bwd_kernel(const void *__restrict__ dout, const float *__restrict__ y_perm,
                    const int *__restrict__ row_of, const float *__restrict__ topk_w,
                    __nv_bfloat16 *__restrict__ gy, float *__restrict__ dw, int T, int k, int D,
@@ -31,46 +51,57 @@ combine_bwd_kernel(const void *__restrict__ dout, const float *__restrict__ y_pe
     const int t = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
-    for (int j = 0; j < k; ++j) {
-        int r = row_of[(size_t)t * k + j];
-        if (r < -1 || (long long)r >= rows_alloc) {
-            if (lane == 0) raise_flag(status, FLAG_BAD_ROUTING);
-            r = -1;
+    int my_r = -1;
+    float my_w = 0.f;
+    if (lane < k) {
+        my_r = row_of[(size_t)t * k + lane];
+        my_w = topk_w[(size_t)t * k + lane];
+        if (my_r < -1 || (long long)my_r >= rows_alloc) {
+            raise_flag(status, FLAG_BAD_ROUTING);
+            my_r = -1;
         }
-        const float w = topk_w[(size_t)t * k + j];
-        float dot = 0.f;
-        if (r >= 0) {
-            for (int d0 = lane * 4; d0 < D; d0 += 128) {
-                float g[4];
-                if (BF16) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(
-                        static_cast<const __nv_bfloat16 *>(dout) + (size_t)t * D + d0);
-                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
-                    g[0] = __low2float(h2[0]);
-                    g[1] = __high2float(h2[0]);
-                    g[2] = __low2float(h2[1]);
-                    g[3] = __high2float(h2[1]);
-                } else {
-                    const float4 v = *reinterpret_cast<const float4 *>(
-                        static_cast<const float *>(dout) + (size_t)t * D + d0);
-                    g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
-                }
-                const float4 y = *reinterpret_cast<const float4 *>(y_perm + (size_t)r * D + d0);
-                dot = fmaf(g[0], y.x, dot);
-                dot = fmaf(g[1], y.y, dot);
-                dot = fmaf(g[2], y.z, dot);
-                dot = fmaf(g[3], y.w, dot);
-                __nv_bfloat162 lo = __floats2bfloat162_rn(w * g[0], w * g[1]);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(w * g[2], w * g[3]);
+    }
+    for (int j0 = 0; j0 < k; j0 += BW_SLOTS) {
+        int r[BW_SLOTS];
+        float w[BW_SLOTS], dot[BW_SLOTS];
+#pragma unroll
+        for (int u = 0; u < BW_SLOTS; ++u) {
+            const int j = j0 + u;
+            r[u] = __shfl_sync(0xffffffffu, my_r, j & 31);
+            w[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
+            if (j >= k) r[u] = -1;
+            dot[u] = 0.f;
+        }
+        for (int d0 = lane * 4; d0 < D; d0 += 128) {
+            float g[4];
+            load4(dout, (size_t)t * D + d0, BF16, g);
+            float4 y[BW_SLOTS];
+#pragma unroll
+            for (int u = 0; u < BW_SLOTS; ++u)
+                if (r[u] >= 0)
+                    y[u] = __ldcs(reinterpret_cast<const float4 *>(y_perm + (size_t)r[u] * D + d0));
+#pragma unroll
+            for (int u = 0; u < BW_SLOTS; ++u) {
+                if (r[u] < 0) continue;
+                dot[u] = fmaf(g[0], y[u].x, dot[u]);
+                dot[u] = fmaf(g[1], y[u].y, dot[u]);
+                dot[u] = fmaf(g[2], y[u].z, dot[u]);
+                dot[u] = fmaf(g[3], y[u].w, dot[u]);
+                __nv_bfloat162 lo = __floats2bfloat162_rn(w[u] * g[0], w[u] * g[1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(w[u] * g[2], w[u] * g[3]);
                 uint2 o;
                 o.x = *reinterpret_cast<uint32_t *>(&lo);
                 o.y = *reinterpret_cast<uint32_t *>(&hi);
-                *reinterpret_cast<uint2 *>(gy + (size_t)r * D + d0) = o;
+                *reinterpret_cast<uint2 *>(gy + (size_t)r[u] * D + d0) = o;
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (lane == 0) dw[(size_t)t * k + j] = dot;
+        for (int u = 0; u < BW_SLOTS; ++u) {
+            float v = dot[u];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0 && j0 + u < k) dw[(size_t)t * k + j0 + u] = v;
+        }
     }
 }
 
@@ -78,7 +109,7 @@ combine_bwd_kernel(const void *__restrict__ dout, const float *__restrict__ y_pe
 // order, rounded once to the output type; r[t] = add[t] when add, else (wg
 // given) sum_j dl[t, e_j] wg[e_j] in slot order.
 template <bool BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 dispatch_bwd_kernel(const float *__restrict__ dxp, const int *__restrict__ row_of,
                     const float *__restrict__ add, const int *__restrict__ topk_idx,
                     const float *__restrict__ dl, const void *__restrict__ wg, int E,
@@ -102,36 +133,42 @@ dispatch_bwd_kernel(const float *__restrict__ dxp, const int *__restrict__ row_o
     }
     for (int d0 = lane * 4; d0 < D; d0 += 128) {
         float a[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int r = __shfl_sync(0xffffffffu, my_r, j);
-            if (r < 0) continue;
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(dxp + (size_t)r * D + d0));
-            a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
+        for (int j0 = 0; j0 < k; j0 += DB_SLOTS) {
+            int r[DB_SLOTS];
+            float4 v[DB_SLOTS];
+#pragma unroll
+            for (int u = 0; u < DB_SLOTS; ++u) {
+                r[u] = __shfl_sync(0xffffffffu, my_r, (j0 + u) & 31);
+                if (j0 + u >= k) r[u] = -1;
+                if (r[u] >= 0)
+                    v[u] = __ldcs(reinterpret_cast<const float4 *>(dxp + (size_t)r[u] * D + d0));
+            }
+#pragma unroll
+            for (int u = 0; u < DB_SLOTS; ++u) {
+                if (r[u] < 0) continue;
+                a[0] += v[u].x; a[1] += v[u].y; a[2] += v[u].z; a[3] += v[u].w;
+            }
         }
         if (add) {
             const float4 v = *reinterpret_cast<const float4 *>(add + (size_t)t * D + d0);
             a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
         } else if (wg) {
-            for (int j = 0; j < k; ++j) {
-                const int e = __shfl_sync(0xffffffffu, my_e, j);
-                const float g = __shfl_sync(0xffffffffu, my_g, j);
-                if (e < 0) continue;
-                float w[4];
-                if (BF16) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(
-                        static_cast<const __nv_bfloat16 *>(wg) + (size_t)e * D + d0);
-                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
-                    w[0] = __low2float(h2[0]);
-                    w[1] = __high2float(h2[0]);
-                    w[2] = __low2float(h2[1]);
-                    w[3] = __high2float(h2[1]);
-                } else {
-                    const float4 v = *reinterpret_cast<const float4 *>(
-                        static_cast<const float *>(wg) + (size_t)e * D + d0);
-                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            for (int j0 = 0; j0 < k; j0 += DB_SLOTS) {
+                int e[DB_SLOTS];
+                float g[DB_SLOTS], w[DB_SLOTS][4];
+#pragma unroll
+                for (int u = 0; u < DB_SLOTS; ++u) {
+                    e[u] = __shfl_sync(0xffffffffu, my_e, (j0 + u) & 31);
+                    g[u] = __shfl_sync(0xffffffffu, my_g, (j0 + u) & 31);
+                    if (j0 + u >= k) e[u] = -1;
+                    if (e[u] >= 0) load4(wg, (size_t)e[u] * D + d0, BF16, w[u]);
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) a[i] = fmaf(g, w[i], a[i]);
+                for (int u = 0; u < DB_SLOTS; ++u) {
+                    if (e[u] < 0) continue;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) a[i] = fmaf(g[u], w[u][i], a[i]);
+                }
             }
         }
         if (BF16) {
@@ -345,12 +382,12 @@ cudaError_t launch_combine_bwd(const void *dout, const float *y_perm, const int 
                                const float *topk_w, void *gy, float *dw, int T, int D, int k,
                                int64_t rows_alloc, int is_bf16, int *status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const dim3 grid((unsigned)((T + 7) / 8));
+    const dim3 grid((unsigned)((T + 3) / 4));  // 4 warps (tokens) per block
     const cudaError_t e =
-        is_bf16 ? launch_pdl(combine_bwd_kernel<true>, grid, dim3(256), 0, stream, dout, y_perm,
+        is_bf16 ? launch_pdl(combine_bwd_kernel<true>, grid, dim3(128), 0, stream, dout, y_perm,
                              row_of, topk_w, (__nv_bfloat16 *)gy, dw, T, k, D, (long long)rows_alloc,
                              status)
-                : launch_pdl(combine_bwd_kernel<false>, grid, dim3(256), 0, stream, dout, y_perm,
+                : launch_pdl(combine_bwd_kernel<false>, grid, dim3(128), 0, stream, dout, y_perm,
                              row_of, topk_w, (__nv_bfloat16 *)gy, dw, T, k, D, (long long)rows_alloc,
                              status);
     if (e == cudaSuccess) count_launch();
@@ -363,11 +400,11 @@ cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float
                                 cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     if (k > 32) return cudaErrorInvalidValue;  // one lane per slot
-    const dim3 grid((unsigned)((T + 7) / 8));
+    const dim3 grid((unsigned)((T + 3) / 4));  // 4 warps (tokens) per block
     const cudaError_t e =
-        is_bf16 ? launch_pdl(dispatch_bwd_kernel<true>, grid, dim3(256), 0, stream, dxp, row_of, add,
+        is_bf16 ? launch_pdl(dispatch_bwd_kernel<true>, grid, dim3(128), 0, stream, dxp, row_of, add,
                              topk_idx, dl, wg, E, dx, T, k, D, (long long)rows_alloc)
-                : launch_pdl(dispatch_bwd_kernel<false>, grid, dim3(256), 0, stream, dxp, row_of,
+                : launch_pdl(dispatch_bwd_kernel<false>, grid, dim3(128), 0, stream, dxp, row_of,
                              add, topk_idx, dl, wg, E, dx, T, k, D, (long long)rows_alloc);
     if (e == cudaSuccess) count_launch();
     return e;

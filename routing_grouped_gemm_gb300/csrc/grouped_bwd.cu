@@ -38,12 +38,20 @@ constexpr int B_A_BYTES = B_BM * B_BK * 2;        // 16 KB
 constexpr int B_B_BYTES = (B_BN / 2) * B_BK * 2;  // 16 KB: this CTA's half of B
 constexpr int B_STAGE_BYTES = B_A_BYTES + B_B_BYTES;
 constexpr int B_CHUNK = 64 * B_BK * 2;            // one MN-major box: 64 M/N elements x 64 K rows
-constexpr int B_EPI_WARPS = 4;
-constexpr int B_THREADS = 64 + 32 * B_EPI_WARPS;
+constexpr int B_MAX_EPI_WARPS = 8;  // 4 or 8: each TMEM lane quarter drained by 1 or 2 warps
+constexpr int B_MAX_THREADS = 64 + 32 * B_MAX_EPI_WARPS;
 constexpr int B_ACC_COLS = 256;
 constexpr int B_TMEM_COLS = 512;
-constexpr int B_NBARS = 32;
-constexpr int B_SIGNALS = 2 * B_EPI_WARPS;
+constexpr int B_NBARS = 40;
+#ifndef MOE_BWD_EPI_WARPS_STORE
+#define MOE_BWD_EPI_WARPS_STORE 8
+#endif
+#ifndef MOE_BWD_EPI_WARPS_SWIGLU
+#define MOE_BWD_EPI_WARPS_SWIGLU 4
+#endif
+#ifndef MOE_BWD_EPI_WARPS_DGRAD
+#define MOE_BWD_EPI_WARPS_DGRAD 4
+#endif
 // Epilogue staging, per epilogue warp: two 4 KB output boxes (32 rows x 32
 // fp32, or the dg and du halves of 32 rows x 32 bf16 each) and, for the
 // SwiGLU backward, two 4 KB input boxes (the saved g and u of the chunk).
@@ -70,6 +78,7 @@ struct BwdParams {
     int m_split;           // k-grouped: output rows m >= m_split go through the second output map
     int stages;            // smem ring depth
     int epi_bytes;         // staging bytes per epilogue warp
+    int epi_warps;         // 4 or 8 epilogue warps
     const int *seg_off, *tpe;
     int H;
     int *status;
@@ -77,15 +86,15 @@ struct BwdParams {
 
 // Shared memory: 1 KB alignment slack, the ring, the epilogue staging, the
 // barriers, the TMEM slot / abort flag and the tile table.
-size_t bwd_smem_bytes(int E_local, int stages, int epi_bytes) {
-    return 1024 + (size_t)stages * B_STAGE_BYTES + (size_t)B_EPI_WARPS * epi_bytes +
+size_t bwd_smem_bytes(int E_local, int stages, int epi_bytes, int epi_warps) {
+    return 1024 + (size_t)stages * B_STAGE_BYTES + (size_t)epi_warps * epi_bytes +
            B_NBARS * sizeof(uint64_t) + 16 + sizeof(int) * (4 * (size_t)E_local + 1);
 }
 
 // The deepest ring (at most B_MAX_STAGES, at least 2) that fits 227 KB.
-int bwd_stages(int E_local, int epi_bytes) {
+int bwd_stages(int E_local, int epi_bytes, int epi_warps) {
     for (int st = B_MAX_STAGES; st >= 2; --st)
-        if (bwd_smem_bytes(E_local, st, epi_bytes) <= 227 * 1024) return st;
+        if (bwd_smem_bytes(E_local, st, epi_bytes, epi_warps) <= 227 * 1024) return st;
     return 0;
 }
 
@@ -128,7 +137,7 @@ __device__ __forceinline__ BwdTile decode_bwd(int v, const BwdParams &p, const i
     return c;
 }
 
-__global__ void __launch_bounds__(B_THREADS, 1)
+__global__ void __launch_bounds__(B_MAX_THREADS, 1)
 bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const BwdParams p) {
@@ -139,7 +148,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const int n_st = p.stages;
     uint8_t *epi = ring + n_st * B_STAGE_BYTES;  // 1 KB aligned
-    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + B_EPI_WARPS * p.epi_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi + p.epi_warps * p.epi_bytes);
     uint64_t *full = bars;                       // [stages] leader: both CTAs' TMA -> MMA
     uint64_t *empty = bars + B_MAX_STAGES;       // [stages] MMA -> each CTA's TMA
     uint64_t *tfull = bars + 2 * B_MAX_STAGES;   // [2]      MMA -> each CTA's epilogue
@@ -168,10 +177,10 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(&tfull[a], 1);
-                mbar_init(&tempty[a], B_SIGNALS);
+                mbar_init(&tempty[a], 2 * p.epi_warps);  // every epilogue warp of both CTAs
             }
             mbar_init(drain, 1);
-            for (int i = 0; i < 2 * B_EPI_WARPS; ++i) mbar_init(&ldbar[i], 1);
+            for (int i = 0; i < 2 * p.epi_warps; ++i) mbar_init(&ldbar[i], 1);
             *abort_flag = 0;
             fence_mbarrier_init();
             prefetch_tmap(&tmA);
@@ -280,6 +289,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // brings the chunk's saved g and u in by TMA, one chunk ahead.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int wi = warp - 2;
+        // with 8 warps, two share a lane quarter and split the tile's columns
+        const int n_grp = p.epi_warps / 4, grp = wi / 4, ch_per = (B_BN / 32) / n_grp;
         uint8_t *stg = epi + wi * p.epi_bytes;   // out boxes [0, 8 KB), in boxes [8, 16 KB)
         uint64_t *lb = ldbar + 2 * wi;
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
@@ -308,7 +319,10 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     to = &tmO1;
                 }
             }
-            const int n_ch = active ? min(B_BN / 32, (p.N - c.n0) / 32) : 0;
+            // this warp's chunks: [ch_lo, ch_hi) of the tile's 32-column chunks
+            const int ch_lo = grp * ch_per;
+            const int ch_hi = active ? min(ch_lo + ch_per, (p.N - c.n0) / 32) : 0;
+            const int n_ch = max(0, ch_hi - ch_lo);
             auto issue_load = [&](int ch) {  // g and u of chunk ch -> in box (n_load & 1)
                 if (lane == 0) {
                     uint8_t *ib = stg + 2 * B_BOX_BYTES + (n_load & 1) * B_BOX_BYTES;
@@ -323,8 +337,9 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (swiglu && n_ch > 0) {
                 // the tile's g and u head for L2 while its MMAs run; chunk 0 for smem
                 if (lane < 2 * n_ch)
-                    tma_prefetch_l2_2d(&tmO0, (lane & 1 ? p.H : 0) + c.n0 + (lane >> 1) * 32, y0);
-                issue_load(0);
+                    tma_prefetch_l2_2d(&tmO0, (lane & 1 ? p.H : 0) + c.n0 + (ch_lo + (lane >> 1)) * 32,
+                                       y0);
+                issue_load(ch_lo);
             }
             const bool got = mbar_wait_bounded(&tfull[acc], acc_ph, abort_flag);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -334,12 +349,12 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const bool valid = rl < c.nvalid;
             const bool empty_expert = p.sched == BS_KGROUPED && c.nk == 0;
 #pragma unroll 1
-            for (int ch = 0; ch < n_ch; ++ch) {
+            for (int ch = ch_lo; ch < ch_hi; ++ch) {
                 uint32_t d[32];
                 tmem_ld_32x32b_x32(tbase + ch * 32, d);
                 const uint8_t *ib = nullptr;
                 if (swiglu) {
-                    if (ch + 1 < n_ch) issue_load(ch + 1);
+                    if (ch + 1 < ch_hi) issue_load(ch + 1);
                     const bool in_ok =
                         mbar_wait_bounded(&lb[n_used & 1], (n_used >> 1) & 1u, abort_flag);
                     ib = stg + 2 * B_BOX_BYTES + (n_used & 1) * B_BOX_BYTES;
@@ -437,16 +452,18 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 }
 
-int max_bwd_clusters(size_t smem) {
+int max_bwd_clusters(size_t smem, int threads) {
     constexpr int kMaxDev = 64;
     static int cached[kMaxDev] = {0};
     static size_t cached_smem[kMaxDev] = {0};
+    static int cached_threads[kMaxDev] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    if (cached[dev] > 0 && cached_smem[dev] == smem) return cached[dev];
+    if (cached[dev] > 0 && cached_smem[dev] == smem && cached_threads[dev] == threads)
+        return cached[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256);
-    cfg.blockDim = dim3(B_THREADS);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -462,23 +479,25 @@ int max_bwd_clusters(size_t smem) {
     }
     cached[dev] = n;
     cached_smem[dev] = smem;
+    cached_threads[dev] = threads;
     return n;
 }
 
 cudaError_t launch_bwd(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                        const CUtensorMap &o0, const CUtensorMap &o1, BwdParams p, long long tiles,
                        cudaStream_t stream) {
-    p.stages = bwd_stages(p.E_local, p.epi_bytes);
+    p.stages = bwd_stages(p.E_local, p.epi_bytes, p.epi_warps);
     if (p.stages == 0) return cudaErrorInvalidConfiguration;
-    const size_t smem = bwd_smem_bytes(p.E_local, p.stages, p.epi_bytes);
+    const size_t smem = bwd_smem_bytes(p.E_local, p.stages, p.epi_bytes, p.epi_warps);
+    const int threads = 64 + 32 * p.epi_warps;
     cudaError_t err = ensure_smem((const void *)bwd_pair_kernel, smem);
     if (err != cudaSuccess) return err;
-    const int clusters_max = max_bwd_clusters(smem);
+    const int clusters_max = max_bwd_clusters(smem, threads);
     if (clusters_max <= 0) return cudaErrorLaunchOutOfResources;
     const int clusters = (int)std::max<long long>(1, std::min<long long>(clusters_max, tiles));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(B_THREADS);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -526,11 +545,11 @@ zero_pad_rows_kernel(const int *__restrict__ seg_off, const int *__restrict__ tp
 }  // namespace
 
 int64_t grouped_bwd_smem(int E_local) {
-    // the SwiGLU backward's staging is the larger; both need a ring of >= 2 stages
-    return bwd_stages(E_local, B_EPI_BYTES_SWIGLU) == 0
-               ? (int64_t)bwd_smem_bytes(E_local, 2, B_EPI_BYTES_SWIGLU)
-               : (int64_t)bwd_smem_bytes(E_local, bwd_stages(E_local, B_EPI_BYTES_SWIGLU),
-                                         B_EPI_BYTES_SWIGLU);
+    // the largest of the four launches' needs, each with a ring of >= 2 stages
+    const int64_t a = (int64_t)bwd_smem_bytes(E_local, 2, B_EPI_BYTES_SWIGLU, MOE_BWD_EPI_WARPS_SWIGLU);
+    const int64_t b = (int64_t)bwd_smem_bytes(E_local, 2, B_EPI_BYTES_STORE, MOE_BWD_EPI_WARPS_STORE);
+    const int64_t c = (int64_t)bwd_smem_bytes(E_local, 2, B_EPI_BYTES_STORE, MOE_BWD_EPI_WARPS_DGRAD);
+    return std::max({a, b, c});
 }
 
 cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const void *gu,
@@ -563,6 +582,7 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
     base.status = status;
     base.H = H_local;
     base.epi_bytes = B_EPI_BYTES_STORE;
+    base.epi_warps = MOE_BWD_EPI_WARPS_STORE;
 
     CUtensorMap tA, tB0, tB1, tO0, tO1;
     // 1. dh = gy . w2_e, fused SwiGLU backward -> dgu  (m-grouped, K = D)
@@ -571,6 +591,7 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.sched = BS_MGROUPED;
         p.epi = BE_SWIGLU_BWD;
         p.epi_bytes = B_EPI_BYTES_SWIGLU;
+        p.epi_warps = MOE_BWD_EPI_WARPS_SWIGLU;
         p.a_mn = 0;
         p.b_mn = 1;
         p.N = H_local;
@@ -596,6 +617,7 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.nk = 2 * H_local / B_BK;
         p.nt = (D + B_BN - 1) / B_BN;
         p.k_split = H_local / B_BK;
+        p.epi_warps = MOE_BWD_EPI_WARPS_DGRAD;
         if (!make_tmap_2d(&tA, dgu, H2, rows_alloc, B_BM) ||
             !make_tmap_3d(&tB0, w1, D, H_local, E_local, B_BK) ||
             !make_tmap_3d(&tB1, w3, D, H_local, E_local, B_BK) ||
