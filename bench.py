@@ -335,9 +335,23 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
 
     w = moe_inputs.WORKLOADS[WORKLOAD]
+    if args.scale:
+        # a reduced case of the same workload (profiling captures only)
+        over = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.scale.split(",")}
+        w = w.scaled(**over)
     inp = moe_inputs.make_inputs(w, device=dev, seed=rank)
     cfg = moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k, dtype=moe.MOE_BF16,
                      score=moe.MOE_SCORE_SOFTMAX, renorm=1, align_m=128)
+    if args.backward_only:
+        backward = run_backward(moe, cfg, inp, torch.cuda.current_stream(dev), dev, args,
+                                load_peaks())
+        if rank == 0:
+            print(json.dumps({"workload": WORKLOAD, "scale": args.scale or None,
+                              "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
+                              "backward": backward}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     ra = moe.rows_alloc(cfg)
     ws = moe.alloc_workspace(cfg, device=dev)
     logits = None
@@ -480,7 +494,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--no-backward", action="store_true", help="skip the training backward leg")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the training step (forward_train + backward), print its JSON")
+    ap.add_argument("--scale", default="",
+                    help="with --backward-only: override workload sizes, e.g. E=16,k=2 (profiling)")
     args = ap.parse_args()
+    if args.scale and not args.backward_only:
+        ap.error("--scale is for --backward-only profiling runs")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

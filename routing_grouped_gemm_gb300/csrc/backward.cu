@@ -195,9 +195,13 @@ dispatch_bwd_kernel(const float *__restrict__ dxp, const int *__restrict__ row_o
 __global__ void __launch_bounds__(256)
 router_dl_kernel(const float *__restrict__ logits, const int *__restrict__ topk_idx,
                  const float *__restrict__ topk_w, const float *__restrict__ dw,
-                 float *__restrict__ dl, int T, int E, int k, int score, int renorm) {
+                 float *__restrict__ dl, int T, int E, int k, int score, int renorm,
+                 int *__restrict__ ctr, int n_ctr) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
+    // the split-K counters of the router GEMM that follows start at zero
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ctr[i] = 0;
     const int t = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -241,43 +245,50 @@ router_dl_kernel(const float *__restrict__ logits, const int *__restrict__ topk_
 }
 
 // Split-K SIMT GEMM for the router's two products (fp32 FMAs; the router's
-// gradients stay in fp32):  split z computes
-//   C_z(m, n) = sum_{k in [z kc, (z+1) kc)} A(m, k) B(k, n),  k ascending,
+// gradients stay in fp32):
+//   C(m, n) = sum_k A(m, k) B(k, n),
 // A(m, k) = a[m * a_m + k * a_k] fp32 (a_m == 1 or a_k == 1), B(k, n) =
-// b[k * ldb + n] (bf16 or fp32), into c + z * M * N (row stride N).  When
-// colsum is given, the blocks of the first N tile also write
-// colsum[z * M + m] = sum_k A(m, k) over the split, in the same k order.
-// 64 x 128 tiles, 4 x 8 outputs per thread, N a multiple of 4.
+// b[k * ldb + n] (bf16 or fp32), C row-major [M, N].  With colsum, the
+// blocks of the first N tile also form colsum[m] = sum_k A(m, k).  Split z
+// of S sums k in [z kc, (z+1) kc) in ascending order; with S > 1 each split
+// writes its partial tile to part (cpart for the column sums) and the last
+// split of a tile to finish (a per-tile counter in ctr, zero on entry and
+// left zero) adds the S partials in split order, so the result does not
+// depend on which split finishes last.  64 x 128 tiles, 4 x 8 outputs per
+// thread, the next K slice loaded into registers while the current one is
+// multiplied; N a multiple of 4.
 constexpr int RG_BM = 64, RG_BN = 128, RG_BK = 32, RG_PAD = 4;
 template <bool BBF16>
 __global__ void __launch_bounds__(256)
 router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
                    const void *__restrict__ b, long long ldb, float *__restrict__ c,
-                   float *__restrict__ colsum, int M, int N, int K, int kc) {
+                   float *__restrict__ colsum, float *__restrict__ part, float *__restrict__ cpart,
+                   int *__restrict__ ctr, int M, int N, int K, int kc, int S) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     __shared__ __align__(16) float As[RG_BK][RG_BM + RG_PAD];
     __shared__ __align__(16) float Bs[RG_BK][RG_BN];
+    __shared__ int s_last;
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int m0 = blockIdx.y * RG_BM, n0 = blockIdx.x * RG_BN, z = blockIdx.z;
     const int kb = z * kc, ke = min(K, kb + kc);
     const bool do_sum = colsum != nullptr && blockIdx.x == 0 && tid < RG_BM;
-    float acc[4][8] = {};
-    float cs = 0.f;
-    for (int k0 = kb; k0 < ke; k0 += RG_BK) {
-        if (a_m == 1) {  // m contiguous in memory: consecutive threads take consecutive m
-            for (int i = tid; i < RG_BK * RG_BM; i += 256) {
-                const int kk = i / RG_BM, mm = i % RG_BM, m = m0 + mm, k = k0 + kk;
-                As[kk][mm] = (m < M && k < ke) ? a[(long long)m + (long long)k * a_k] : 0.f;
-            }
-        } else {  // k contiguous
-            for (int i = tid; i < RG_BK * RG_BM; i += 256) {
-                const int kk = i % RG_BK, mm = i / RG_BK, m = m0 + mm, k = k0 + kk;
-                As[kk][mm] = (m < M && k < ke) ? a[(long long)m * a_m + (long long)k] : 0.f;
-            }
+    const bool a_mcont = a_m == 1;
+    float ra[8];
+    float4 rb[4];
+    auto gload = [&](int k0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = tid + 256 * u;
+            const int kk = a_mcont ? i / RG_BM : i % RG_BK;
+            const int mm = a_mcont ? i % RG_BM : i / RG_BK;
+            const int m = m0 + mm, k = k0 + kk;
+            ra[u] = (m < M && k < ke) ? a[(long long)m * a_m + (long long)k * a_k] : 0.f;
         }
-        for (int i = tid; i < RG_BK * RG_BN / 4; i += 256) {
-            const int kk = i / (RG_BN / 4), nn = (i % (RG_BN / 4)) * 4, n = n0 + nn, k = k0 + kk;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = tid + 256 * u;
+            const int kk = i / (RG_BN / 4), n = n0 + (i % (RG_BN / 4)) * 4, k = k0 + kk;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (n < N && k < ke) {
                 if (BBF16) {
@@ -291,9 +302,26 @@ router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
                                                           (long long)k * ldb + n);
                 }
             }
-            *reinterpret_cast<float4 *>(&Bs[kk][nn]) = v;
+            rb[u] = v;
+        }
+    };
+    float acc[4][8] = {};
+    float cs = 0.f;
+    if (kb < ke) gload(kb);
+    for (int k0 = kb; k0 < ke; k0 += RG_BK) {
+        __syncthreads();  // the previous slice's products are done with smem
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = tid + 256 * u;
+            As[a_mcont ? i / RG_BM : i % RG_BK][a_mcont ? i % RG_BM : i / RG_BK] = ra[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = tid + 256 * u;
+            *reinterpret_cast<float4 *>(&Bs[i / (RG_BN / 4)][(i % (RG_BN / 4)) * 4]) = rb[u];
         }
         __syncthreads();
+        if (k0 + RG_BK < ke) gload(k0 + RG_BK);  // in flight during the products below
         if (do_sum)
             for (int kk = 0; kk < RG_BK; ++kk) cs += As[kk][tid];
 #pragma unroll 8
@@ -308,9 +336,8 @@ router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
         }
-        __syncthreads();
     }
-    float *cz = c + (size_t)z * M * N;
+    float *dst = S > 1 ? part + (size_t)z * M * N : c;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int m = m0 + ty * 4 + i;
@@ -319,35 +346,43 @@ router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
         for (int h = 0; h < 2; ++h) {
             const int n = n0 + h * (RG_BN / 2) + tx * 4;
             if (n < N)
-                *reinterpret_cast<float4 *>(cz + (size_t)m * N + n) =
+                *reinterpret_cast<float4 *>(dst + (size_t)m * N + n) =
                     make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
         }
     }
-    if (do_sum && m0 + tid < M) colsum[(size_t)z * M + m0 + tid] = cs;
-}
-
-// out[i] = sum_z part[z * n + i], z ascending (n a multiple of 4); the same
-// for the column sums: bias_out[m] = sum_z bias_part[z * M + m].
-__global__ void __launch_bounds__(256)
-split_sum_kernel(const float *__restrict__ part, int S, long long n, float *__restrict__ out,
-                 const float *__restrict__ bias_part, int M, float *__restrict__ bias_out) {
-    griddep_launch_dependents();  // the next kernel may be scheduled now
-    griddep_wait();               // every input of this kernel is complete
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n / 4; i += stride) {
-        float4 s = reinterpret_cast<const float4 *>(part)[i];
-        for (int z = 1; z < S; ++z) {
-            const float4 v = reinterpret_cast<const float4 *>(part + (size_t)z * n)[i];
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    if (do_sum && m0 + tid < M) (S > 1 ? cpart + (size_t)z * M : colsum)[m0 + tid] = cs;
+    if (S == 1) return;
+    // the last split of this tile adds the partials in split order
+    __threadfence();
+    __syncthreads();
+    const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+    if (tid == 0) s_last = atomicAdd(&ctr[tile], 1) == S - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = n0 + h * (RG_BN / 2) + tx * 4;
+            if (n >= N) continue;
+            float4 sum = __ldcg(reinterpret_cast<const float4 *>(part + (size_t)m * N + n));
+            for (int zz = 1; zz < S; ++zz) {
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4 *>(part + ((size_t)zz * M + m) * N + n));
+                sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+            *reinterpret_cast<float4 *>(c + (size_t)m * N + n) = sum;
         }
-        reinterpret_cast<float4 *>(out)[i] = s;
     }
-    if (bias_out)
-        for (long long m = (long long)blockIdx.x * blockDim.x + threadIdx.x; m < M; m += stride) {
-            float s = bias_part[m];
-            for (int z = 1; z < S; ++z) s += bias_part[(size_t)z * M + m];
-            bias_out[m] = s;
-        }
+    if (do_sum && m0 + tid < M) {
+        float sum = __ldcg(cpart + m0 + tid);
+        for (int zz = 1; zz < S; ++zz) sum += __ldcg(cpart + (size_t)zz * M + m0 + tid);
+        colsum[m0 + tid] = sum;
+    }
+    if (tid == 0) ctr[tile] = 0;  // ready for the next call
 }
 
 // Splits of dwg's K (= T): enough (tile, split) blocks for two waves of the
@@ -366,12 +401,12 @@ RouterSplit router_split(int T, int D, int E) {
 
 template <bool BBF16>
 cudaError_t router_gemm(const float *a, long long a_m, long long a_k, const void *b, long long ldb,
-                        float *c, float *colsum, int M, int N, int K, int S, int kc,
-                        cudaStream_t stream) {
+                        float *c, float *colsum, float *part, float *cpart, int *ctr, int M, int N,
+                        int K, int S, int kc, cudaStream_t stream) {
     if (M == 0 || N == 0) return cudaSuccess;
     const dim3 grid((N + RG_BN - 1) / RG_BN, (M + RG_BM - 1) / RG_BM, S);
     const cudaError_t e = launch_pdl(router_gemm_kernel<BBF16>, grid, dim3(256), 0, stream, a, a_m,
-                                     a_k, b, ldb, c, colsum, M, N, K, kc);
+                                     a_k, b, ldb, c, colsum, part, cpart, ctr, M, N, K, kc, S);
     if (e == cudaSuccess) count_launch();
     return e;
 }
@@ -410,9 +445,12 @@ cudaError_t launch_dispatch_bwd(const float *dxp, const int *row_of, const float
     return e;
 }
 
+// Router backward scratch (S > 1): partial tiles [S, E, D], partial column
+// sums [S, E], then one counter per output tile (ints).
 int64_t router_bwd_scratch_floats(int T, int D, int E) {
     const RouterSplit sp = router_split(T, D, E);
-    return sp.S > 1 ? (int64_t)sp.S * E * D + (int64_t)sp.S * E : 0;
+    const int64_t tiles = (int64_t)((E + RG_BM - 1) / RG_BM) * ((D + RG_BN - 1) / RG_BN);
+    return sp.S > 1 ? (int64_t)sp.S * E * D + (int64_t)sp.S * E + tiles : 0;
 }
 
 cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits,
@@ -422,29 +460,28 @@ cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits
                               cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     if (D % 4) return cudaErrorInvalidValue;
+    const RouterSplit sp = router_split(T, D, E);
+    const int tiles = ((E + RG_BM - 1) / RG_BM) * ((D + RG_BN - 1) / RG_BN);
+    float *part = sp.S > 1 ? scratch : nullptr;
+    float *cpart = sp.S > 1 ? scratch + (size_t)sp.S * E * D : nullptr;
+    int *ctr = sp.S > 1 ? reinterpret_cast<int *>(cpart + (size_t)sp.S * E) : nullptr;
     cudaError_t e = launch_pdl(router_dl_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, stream,
-                               logits, topk_idx, topk_w, dw, dl, T, E, k, score, renorm);
+                               logits, topk_idx, topk_w, dw, dl, T, E, k, score, renorm, ctr,
+                               ctr ? tiles : 0);
     if (e != cudaSuccess) return e;
     count_launch();
     // dwg [E, D] = dl^T x  (K = T, split), dbias = the column sums of dl
-    const RouterSplit sp = router_split(T, D, E);
-    float *c = sp.S > 1 ? scratch : dwg;
-    float *cs = !dbias ? nullptr : (sp.S > 1 ? scratch + (size_t)sp.S * E * D : dbias);
-    e = is_bf16 ? router_gemm<true>(dl, 1, E, x, D, c, cs, E, D, T, sp.S, sp.kc, stream)
-                : router_gemm<false>(dl, 1, E, x, D, c, cs, E, D, T, sp.S, sp.kc, stream);
+    e = is_bf16 ? router_gemm<true>(dl, 1, E, x, D, dwg, dbias, part, cpart, ctr, E, D, T, sp.S,
+                                    sp.kc, stream)
+                : router_gemm<false>(dl, 1, E, x, D, dwg, dbias, part, cpart, ctr, E, D, T, sp.S,
+                                     sp.kc, stream);
     if (e != cudaSuccess) return e;
-    if (sp.S > 1) {
-        const long long n = (long long)E * D;
-        const unsigned blocks = (unsigned)std::min<long long>((n / 4 + 255) / 256, 4 * 152);
-        if ((e = launch_pdl(split_sum_kernel, dim3(blocks), dim3(256), 0, stream, (const float *)c,
-                            sp.S, n, dwg, (const float *)cs, E, dbias)) != cudaSuccess)
-            return e;
-        count_launch();
-    }
     // dx_router [T, D] = dl wg  (K = E), only where dl is dense
     if (!router_dl_dense(score, renorm)) return cudaSuccess;
-    return is_bf16 ? router_gemm<true>(dl, E, 1, wg, D, dx_router, nullptr, T, D, E, 1, E, stream)
-                   : router_gemm<false>(dl, E, 1, wg, D, dx_router, nullptr, T, D, E, 1, E, stream);
+    return is_bf16 ? router_gemm<true>(dl, E, 1, wg, D, dx_router, nullptr, nullptr, nullptr,
+                                       nullptr, T, D, E, 1, E, stream)
+                   : router_gemm<false>(dl, E, 1, wg, D, dx_router, nullptr, nullptr, nullptr,
+                                        nullptr, T, D, E, 1, E, stream);
 }
 
 }  // namespace moe

@@ -94,6 +94,8 @@ CASES = [
     (256, 128, 192, 16, 4, "sigmoid", True, (4, 2)),
     (200, 192, 64, 8, 2, "softmax", False, (0, 0)),
     (150, 128, 128, 6, 3, "sigmoid", False, (0, 0)),
+    (4096, 128, 64, 8, 2, "softmax", True, (0, 0)),    # router weight gradient split 16 ways
+    (2048, 128, 64, 8, 3, "softmax", False, (0, 0)),   # split 8 ways, dense router dx
 ]
 
 
