@@ -24,6 +24,10 @@ What each function follows (page title, section):
                           "Expert Tensor Parallel design" page, section 4.3
 * ``unpermute_combine``   "Expert Parallelism (EP)" section 1, combine
                           post-process (top-k weighted reduce back to order)
+* ``e4m3_*``/``quantize_rows_e4m3`` the FP8 step of the same page's next
+                          steps (e4m3 dispatched activations with scales);
+                          the scale granularity is a reading (one binary32
+                          scale per row: amax / 448)
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, invariants, brute force and the worked example of the
@@ -103,6 +107,11 @@ def _load():
             lib.oracle_grouped_gemm1_swiglu.argtypes = [I, I, I, P, P, P, I, P, P, I, I, P, I]
             lib.oracle_grouped_gemm2.argtypes = [I, I, I, P, P, P, I, P, I, I, P, I]
             lib.oracle_unpermute_combine.argtypes = [I, I, I, P, I, P, P, P]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_value.argtypes = [I]
+            lib.oracle_e4m3_encode.restype = I
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_quantize_rows_e4m3.argtypes = [L, I, P, P, P]
             _lib = lib
     return _lib
 
@@ -401,3 +410,42 @@ def moe_backward(x, wg, bias, w1, w3, w2, dout, k: int, score: int, renorm: bool
     if st != OK:
         raise ValueError("oracle.moe_backward: bad arguments")
     return r
+
+
+# --------------------------------------------------------------------------
+# FP8 e4m3
+# --------------------------------------------------------------------------
+
+def e4m3_value(code: int) -> float:
+    """Value of an e4m3 ("fn": no infinities, max 448) code."""
+    return float(_load().oracle_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest e4m3 code of the binary32 value v (ties to even, saturating)."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(v))))
+
+
+def e4m3_table() -> np.ndarray:
+    """float64 [256]: the value of every code (NaN for the two NaN codes)."""
+    return np.array([e4m3_value(c) for c in range(256)], np.float64)
+
+
+def quantize_rows_e4m3(src) -> tuple:
+    """Row-wise e4m3 quantisation of a [rows, cols] array of binary32 values
+    (bf16 bit patterns are widened exactly): (codes uint8, scales float32)."""
+    a = np.asarray(src)
+    if a.dtype == np.uint16:
+        a = (a.astype(np.uint32) << 16).view(np.float32)
+    a = _c(a, np.float32)
+    rows, cols = a.shape
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty(rows, np.float32)
+    _load().oracle_quantize_rows_e4m3(rows, cols, _p(a), _p(q), _p(sc))
+    return q, sc
+
+
+def dequantize_rows_e4m3(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """float64 scale[r] * value(codes[r, c]) (exact in fp64)."""
+    tab = e4m3_table()
+    return tab[np.asarray(codes, np.uint8)] * np.asarray(scales, np.float64)[:, None]

@@ -874,3 +874,76 @@ int oracle_moe_backward(int T, int D, int H, int E, int k, const double *x, cons
     free(y); free(dy);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* FP8 e4m3 dispatch (the FP8 next step of the pages: e4m3 dispatched      */
+/* activations with scales feeding an FP8 grouped GEMM)                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The e4m3 format ("fn" variant): 1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities; exponent field 15 with mantissa 7 is NaN,
+ * so the largest finite value is 1.75 * 2^8 = 448.  Exponent field 0 holds
+ * the subnormals m/8 * 2^-6.
+ */
+double oracle_e4m3_value(int code)
+{
+    int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/*
+ * Nearest e4m3 code of a binary32 value, ties to the even mantissa, values
+ * beyond the largest finite magnitude saturated to +-448, NaN to 0x7f.
+ * Every step is exact in double: the input has 24 significant bits.
+ */
+int oracle_e4m3_encode(float vf)
+{
+    double v = (double)vf;
+    if (v != v) return 0x7f;
+    int sign = v < 0.0 || (v == 0.0 && signbit(v)) ? 0x80 : 0;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7e;
+    if (a < ldexp(1.0, -6)) {                 /* subnormal range, step 2^-9 */
+        double m = rint(a / ldexp(1.0, -9)); /* rint: nearest, ties to even */
+        return sign | (int)m;                 /* m = 8 is the code of 2^-6 */
+    }
+    int e2;
+    frexp(a, &e2);                            /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;                           /* a in [2^e, 2^(e+1)) */
+    double mf = rint((a / ldexp(1.0, e) - 1.0) * 8.0);
+    if (mf == 8.0) { mf = 0.0; e += 1; }
+    int field = e + 7;
+    if (field > 15 || (field == 15 && mf == 7.0)) return sign | 0x7e;
+    return sign | (field << 3) | (int)mf;
+}
+
+/*
+ * Row-wise quantisation (the reading taken for the scale granularity): for
+ * each row r of src [rows, cols] (binary32 values, e.g. bf16 activations or
+ * weights widened exactly), amax = max_c |src[r,c]|, scale[r] = amax / 448
+ * computed in binary32 (1 when amax is 0), and dst[r,c] = e4m3 code of the
+ * binary32 quotient src[r,c] / scale[r].  The dequantised value is
+ * scale[r] * e4m3_value(dst[r,c]).
+ */
+void oracle_quantize_rows_e4m3(long rows, int cols, const float *src, uint8_t *dst, float *scale)
+{
+    for (long r = 0; r < rows; ++r) {
+        const float *x = src + (size_t)r * cols;
+        float amax = 0.0f;
+        for (int c = 0; c < cols; ++c) {
+            float a = fabsf(x[c]);
+            if (a > amax) amax = a;
+        }
+        volatile float s = amax > 0.0f ? amax / 448.0f : 1.0f;  /* one binary32 division */
+        scale[r] = s;
+        for (int c = 0; c < cols; ++c) {
+            volatile float q = x[c] / s;                         /* binary32 quotient */
+            dst[(size_t)r * cols + c] = (uint8_t)oracle_e4m3_encode(q);
+        }
+    }
+}
