@@ -296,6 +296,71 @@ moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *
                               float *dw2, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * FP8 e4m3 dispatch (page "Expert Parallelism (EP)", llm-infra-atlas: the FP8
+ * dispatch of its next steps -- dispatched activations as e4m3 values with
+ * scales feeding an FP8 grouped GEMM).  The page does not fix the scale
+ * granularity; these calls use one binary32 scale per row:
+ *   s[r] = max_c |v[r, c]| / 448  (1 for an all-zero row),
+ *   q[r, c] = e4m3(v[r, c] / s[r])  (nearest, ties to even, saturating to
+ *   +-448; NaN to 0x7f), both divisions correctly rounded binary32;
+ *   value(q) * s[r] reconstructs v[r, c] within half an e4m3 step.
+ * e4m3 is the "fn" format: bias 7, 3 mantissa bits, no infinities.
+ * Per-row scales factor out of a GEMM's K sum, so GEMM1 runs on the codes
+ * (tcgen05 kind::f8f6f4, fp32 accumulate) and multiplies its accumulator by
+ * s_x[row] * s_w[unit] before SwiGLU; h stays bf16 and GEMM2 stays bf16.
+ */
+
+/*
+ * Row-wise quantisation of bf16 src [rows, cols] (cols % 16 == 0) into
+ * codes dst [rows, cols] (uint8) and scale [rows] (fp32): the form the FP8
+ * calls take w1 and w3 in (rows = E_local * H_local, cols = D).  Device
+ * pointers; 16-byte aligned src and dst.
+ */
+moe_status moe_quantize_rows_fp8(const void *src, int64_t rows, int32_t cols, uint8_t *dst,
+                                 float *scale, moe_stream_t stream);
+
+/*
+ * moe_permute with the dispatched rows quantised: x [T, D] bf16 in;
+ * x_perm_q [rows_alloc, D] e4m3 codes and x_scale [rows_alloc] fp32 out
+ * (each token's row quantised once, copied to its k rows with its scale).
+ * Counts, offsets, row_of and token_of_row exactly as moe_permute.
+ * Requires dtype MOE_BF16, D % 16 == 0 and k <= 32 (else MOE_ERR_UNSUPPORTED).
+ */
+moe_status moe_permute_fp8(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                           int32_t *tokens_per_expert, int32_t *seg_offsets, int32_t *row_of,
+                           int32_t *token_of_row, uint8_t *x_perm_q, float *x_scale, void *ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu with GEMM1 on e4m3 operands:
+ *   g = s_x[r] s_w1[e, n] sum_d q_x[r, d] q_w1[e, n, d],  u likewise with w3,
+ *   h[r, n] = bf16(SiLU(g) u),  y_perm = h w2_e^T (bf16 x bf16, fp32).
+ * x_perm_q / x_scale as moe_permute_fp8 writes them; w1_q, w3_q
+ * [E_local, H_local, D] codes with w1_scale, w3_scale [E_local, H_local]
+ * (moe_quantize_rows_fp8 of the bf16 weights); w2 bf16 [E_local, D, H_local];
+ * h bf16 [rows_alloc, H_local], y_perm fp32 [rows_alloc, D].
+ * MOE_ERR_UNSUPPORTED for more local experts than the CTA-pair kernel's
+ * shared-memory tile table holds.
+ */
+moe_status moe_grouped_swiglu_fp8(const moe_config *cfg, const uint8_t *x_perm_q,
+                                  const float *x_scale, const int32_t *seg_offsets,
+                                  const int32_t *tokens_per_expert, const uint8_t *w1_q,
+                                  const float *w1_scale, const uint8_t *w3_q,
+                                  const float *w3_scale, const void *w2, void *h, void *y_perm,
+                                  void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_forward with the FP8 dispatch and GEMM1: route (bf16 x, fp32
+ * keys, as moe_route_topk), moe_permute_fp8, moe_grouped_swiglu_fp8 and the
+ * combine, on one stream.  Workspace: moe_layer_workspace_size (it holds the
+ * codes in the x_perm buffer and one scale per row).
+ */
+moe_status moe_layer_forward_fp8(const moe_config *cfg, const void *x, const void *wg,
+                                 const float *bias, const uint8_t *w1_q, const float *w1_scale,
+                                 const uint8_t *w3_q, const float *w3_scale, const void *w2,
+                                 void *out, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_permute without a workspace (this entry point has no counterpart in
  * the pages; it exists for callers that cannot allocate device memory).
  *

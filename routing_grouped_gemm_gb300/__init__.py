@@ -33,6 +33,7 @@ ABI_SYMBOLS = (
     "moe_get_device_status", "moe_permute_noalloc", "moe_kernel_launches",
     "moe_layer_host_workspace_size", "moe_layer_forward_host",
     "moe_layer_train_workspace_size", "moe_layer_forward_train", "moe_layer_backward",
+    "moe_quantize_rows_fp8", "moe_permute_fp8", "moe_grouped_swiglu_fp8", "moe_layer_forward_fp8",
 )
 
 
@@ -77,6 +78,10 @@ def _load() -> ctypes.CDLL:
         "moe_layer_train_workspace_size": (I64, [C]),
         "moe_layer_forward_train": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_layer_backward": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_quantize_rows_fp8": (I32, [P, I64, I32, P, P, P]),
+        "moe_permute_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_grouped_swiglu_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_layer_forward_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -388,6 +393,91 @@ def moe_layer_backward(cfg: Config, x, wg, w1, w3, w2, dout, dx, dwg, dbias, dw1
            "moe_layer_backward")
 
 
+# --------------------------------------------------------------------------
+# FP8 e4m3 dispatch and GEMM1 (codes are torch.uint8 tensors)
+# --------------------------------------------------------------------------
+
+def moe_quantize_rows_fp8(src, dst, scale, stream=None):
+    """Row-wise e4m3 codes and fp32 scales of a bf16 tensor viewed as [rows, cols]."""
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src: a contiguous bf16 CUDA tensor")
+    cols = src.shape[-1]
+    rows = src.numel() // cols if cols else 0
+    _expect(dst, tuple(src.shape), torch.uint8, "dst")
+    _expect(scale, tuple(src.shape[:-1]), torch.float32, "scale")
+    _check(_lib.moe_quantize_rows_fp8(_ptr(src), rows, cols, _ptr(dst), _ptr(scale),
+                                      _stream(stream)), "moe_quantize_rows_fp8")
+
+
+def quantize_weights_fp8(w, stream=None):
+    """(codes uint8, scales fp32 [..., rows]) of a bf16 weight [E, H, D] (one scale per row)."""
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    moe_quantize_rows_fp8(w, q, sc, stream)
+    return q, sc
+
+
+def moe_permute_fp8(cfg: Config, x, topk_idx, tokens_per_expert, seg_offsets, row_of, token_of_row,
+                    x_perm_q, x_scale, ws, stream=None):
+    ra = rows_alloc(cfg)
+    _expect(x, (cfg.T, cfg.D), torch.bfloat16, "x")
+    _expect(topk_idx, (cfg.T, cfg.k), torch.int32, "topk_idx")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(seg_offsets, (cfg.e_local + 1,), torch.int32, "seg_offsets")
+    _expect(row_of, (cfg.T, cfg.k), torch.int32, "row_of")
+    _expect(token_of_row, (ra,), torch.int32, "token_of_row")
+    _expect(x_perm_q, (ra, cfg.D), torch.uint8, "x_perm_q")
+    _expect(x_scale, (ra,), torch.float32, "x_scale")
+    c = cfg.c()
+    _check(_lib.moe_permute_fp8(ctypes.byref(c), _ptr(x), _ptr(topk_idx), _ptr(tokens_per_expert),
+                                _ptr(seg_offsets), _ptr(row_of), _ptr(token_of_row),
+                                _ptr(x_perm_q), _ptr(x_scale), _ptr(ws), ws.numel(),
+                                _stream(stream)), "moe_permute_fp8")
+
+
+def moe_grouped_swiglu_fp8(cfg: Config, x_perm_q, x_scale, seg_offsets, tokens_per_expert, w1_q,
+                           w1_scale, w3_q, w3_scale, w2, h, y_perm, ws, stream=None):
+    ra = rows_alloc(cfg)
+    el = cfg.e_local
+    _expect(x_perm_q, (ra, cfg.D), torch.uint8, "x_perm_q")
+    _expect(x_scale, (ra,), torch.float32, "x_scale")
+    _expect(seg_offsets, (el + 1,), torch.int32, "seg_offsets")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(w1_q, (el, cfg.H_local, cfg.D), torch.uint8, "w1_q")
+    _expect(w3_q, (el, cfg.H_local, cfg.D), torch.uint8, "w3_q")
+    _expect(w1_scale, (el, cfg.H_local), torch.float32, "w1_scale")
+    _expect(w3_scale, (el, cfg.H_local), torch.float32, "w3_scale")
+    _expect(w2, (el, cfg.D, cfg.H_local), torch.bfloat16, "w2")
+    _expect(h, (ra, cfg.H_local), torch.bfloat16, "h")
+    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    c = cfg.c()
+    _check(_lib.moe_grouped_swiglu_fp8(ctypes.byref(c), _ptr(x_perm_q), _ptr(x_scale),
+                                       _ptr(seg_offsets), _ptr(tokens_per_expert), _ptr(w1_q),
+                                       _ptr(w1_scale), _ptr(w3_q), _ptr(w3_scale), _ptr(w2),
+                                       _ptr(h), _ptr(y_perm), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "moe_grouped_swiglu_fp8")
+
+
+def moe_layer_forward_fp8(cfg: Config, x, wg, bias, w1_q, w1_scale, w3_q, w3_scale, w2, out, ws,
+                          stream=None):
+    el = cfg.e_local
+    _expect(x, (cfg.T, cfg.D), torch.bfloat16, "x")
+    _expect(wg, (cfg.E, cfg.D), torch.bfloat16, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    _expect(w1_q, (el, cfg.H_local, cfg.D), torch.uint8, "w1_q")
+    _expect(w3_q, (el, cfg.H_local, cfg.D), torch.uint8, "w3_q")
+    _expect(w1_scale, (el, cfg.H_local), torch.float32, "w1_scale")
+    _expect(w3_scale, (el, cfg.H_local), torch.float32, "w3_scale")
+    _expect(w2, (el, cfg.D, cfg.H_local), torch.bfloat16, "w2")
+    _expect(out, (cfg.T, cfg.D), torch.bfloat16, "out")
+    c = cfg.c()
+    _check(_lib.moe_layer_forward_fp8(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w1_q),
+                                      _ptr(w1_scale), _ptr(w3_q), _ptr(w3_scale), _ptr(w2),
+                                      _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_layer_forward_fp8")
+
+
 def moe_get_device_status(ws, stream=None) -> int:
     """Synchronise, read and clear the workspace status word (returns a code)."""
     return int(_lib.moe_get_device_status(_ptr(ws), ws.numel(), _stream(stream)))
@@ -398,7 +488,8 @@ def layer_views(cfg: Config, ws: torch.Tensor) -> dict:
 
     Mirrors the carving order of the library (256-byte aligned regions after
     the step workspace): topk_idx, topk_w, tokens_per_expert, seg_offsets,
-    row_of, token_of_row, x_perm, h, y_perm.
+    row_of, token_of_row, x_perm (x_perm_q: the FP8 layer's codes in the same
+    bytes), h, y_perm, x_scale (the FP8 layer's row scales).
     """
     def up(n):
         return (n + 255) // 256 * 256
@@ -418,8 +509,12 @@ def layer_views(cfg: Config, ws: torch.Tensor) -> dict:
             ("token_of_row", ra, torch.int32, (ra,)),
             ("x_perm", ra * cfg.D, dt, (ra, cfg.D)),
             ("h", ra * cfg.H_local, dt, (ra, cfg.H_local)),
-            ("y_perm", ra * cfg.D, torch.float32, (ra, cfg.D))):
+            ("y_perm", ra * cfg.D, torch.float32, (ra, cfg.D)),
+            ("x_scale", ra, torch.float32, (ra,))):
         nbytes = n * (4 if tdt in (torch.int32, torch.float32) else eb)
         out[name] = ws[off:off + nbytes].view(tdt).view(shape)
+        if name == "x_perm":
+            # moe_layer_forward_fp8 keeps the e4m3 codes at the start of this buffer
+            out["x_perm_q"] = ws[off:off + ra * cfg.D].view(ra, cfg.D)
         off += up(nbytes)
     return out

@@ -354,6 +354,18 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// The same for e4m3 operands (kind::f8f6f4): K = 32 per instruction, i.e.
+// the same 32 bytes of each K-major row as a K = 16 bf16 MMA.
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` (same offset) in every CTA of `mask` when the pair's
 // tcgen05 ops issued so far by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t mask) {
@@ -427,6 +439,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4)                       // D format: f32
            | (1u << 7)                     // A format: bf16
            | (1u << 10)                    // B format: bf16
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// kind::f8f6f4 with both operands e4m3 (format code 0 in bits 7-9 and
+// 10-12), fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                       // D format: f32
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }

@@ -69,8 +69,6 @@ constexpr int P_EPI_WARPS = 4;
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
 constexpr int P_ACC_COLS = 256;
 constexpr int P_TMEM_COLS = 512;
-constexpr uint32_t P_IDESC = idesc_bf16_f32(P_PAIR_M, P_BN);
-constexpr uint32_t P_IDESC_HALF = idesc_bf16_f32(P_PAIR_M / 2, P_BN);
 constexpr int P_NBARS = 24;
 // An expert's last tile with at most P_SWAP_MAX valid rows runs transposed:
 // the weights are the M=256 operand and the tile's tokens the N operand
@@ -107,6 +105,10 @@ struct PairParams {
     const int *tpe;
     void *out0;           // bf16 h [rows, H_local]
     __nv_bfloat16 *gu_out;  // training forward: g | u pre-activations [rows, 2 H_local] (or null)
+    // FP8 GEMM1: x_perm, w1 and w3 are e4m3 codes (K blocks of 128 per stage)
+    // with one scale per row of x_perm and per row of w1 / w3 ([E_local, H_local])
+    int g1_fp8;
+    const float *x_scale, *w1_scale, *w3_scale;
     void *out1;           // fp32 y [rows, D]
     int *done;            // SCHED_BOTH: [max_blocks] GEMM1 epilogue warps finished, per block
     int max_blocks;       // SCHED_BOTH: entries of done[]
@@ -256,6 +258,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const CUtensorMap *ta = c.mode ? (half ? &tmH64 : &tmH) : (half ? &tmX64 : &tmX);
                 const CUtensorMap *t16 = c.mode ? &tmH16 : &tmX16;
                 const int nk = c.mode ? p.nk1 : p.nk0;
+                // K elements per stage: 64 bf16 or 128 e4m3 (128 bytes either way)
+                const int kel = (c.mode == 0 && p.g1_fp8) ? 2 * P_BK : P_BK;
                 bool ok = true;
                 if (c.mode == 1 && p.sched == SCHED_BOTH) {
                     // h rows of this block: every GEMM1 tile of the block has stored them
@@ -274,22 +278,22 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         // token rows into the B slot (this CTA's half of N), 16 rows a load
                         if (c.mode == 0) {
                             const int hrow = c.nt * 128 + (int)rank * 64;
-                            tma_load_3d_pair(sa, &tmW1, fb, kb * P_BK, hrow, c.expert);
-                            tma_load_3d_pair(sa + P_A_BYTES / 2, &tmW3, fb, kb * P_BK, hrow, c.expert);
+                            tma_load_3d_pair(sa, &tmW1, fb, kb * kel, hrow, c.expert);
+                            tma_load_3d_pair(sa + P_A_BYTES / 2, &tmW3, fb, kb * kel, hrow, c.expert);
                         } else {
                             tma_load_3d_pair(sa, &tmW2, fb, kb * P_BK, c.nt * P_BN + (int)rank * 128,
                                              c.expert);
                         }
                         for (int i = 0; i < srows / 16; ++i)
-                            tma_load_2d_pair(sb + i * 16 * P_BK * 2, t16, fb, kb * P_BK, arow + 16 * i);
+                            tma_load_2d_pair(sb + i * 16 * P_BK * 2, t16, fb, kb * kel, arow + 16 * i);
                         if (++s == P_STAGES) { s = 0; ph ^= 1u; }
                         continue;
                     }
-                    tma_load_2d_pair(sa, ta, fb, kb * P_BK, arow);
+                    tma_load_2d_pair(sa, ta, fb, kb * kel, arow);
                     if (c.mode == 0) {
                         const int hrow = c.nt * 128 + (int)rank * 64;
-                        tma_load_3d_pair(sb, &tmW1, fb, kb * P_BK, hrow, c.expert);
-                        tma_load_3d_pair(sb + P_B_BYTES / 2, &tmW3, fb, kb * P_BK, hrow, c.expert);
+                        tma_load_3d_pair(sb, &tmW1, fb, kb * kel, hrow, c.expert);
+                        tma_load_3d_pair(sb + P_B_BYTES / 2, &tmW3, fb, kb * kel, hrow, c.expert);
                     } else {
                         tma_load_3d_pair(sb, &tmW2, fb, kb * P_BK, c.nt * P_BN + (int)rank * 128,
                                          c.expert);
@@ -310,10 +314,10 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const int acc = it & 1;
                 const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
                 const PairTile c = decode_pair(tile, p, n_blocks, s_mtoff, s_base, s_valid);
-                const uint32_t idesc =
-                    c.nvalid <= P_SWAP_MAX ? idesc_bf16_f32(P_PAIR_M, (c.nvalid + 31) & ~31)
-                    : c.nvalid <= P_BM     ? P_IDESC_HALF
-                                           : P_IDESC;
+                const bool f8 = c.mode == 0 && p.g1_fp8;
+                const int mm = c.nvalid <= P_BM && c.nvalid > P_SWAP_MAX ? P_PAIR_M / 2 : P_PAIR_M;
+                const int nn = c.nvalid <= P_SWAP_MAX ? (c.nvalid + 31) & ~31 : P_BN;
+                const uint32_t idesc = f8 ? idesc_e4m3_f32(mm, nn) : idesc_bf16_f32(mm, nn);
                 const int nk = c.mode ? p.nk1 : p.nk0;
                 if (!mbar_wait_bounded(&tempty[acc], acc_ph ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -323,11 +327,19 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(ring + s * P_STAGE_BYTES);
                     const uint32_t b_addr = a_addr + P_A_BYTES;
+                    // four MMAs of 32 bytes of K each: K = 16 bf16 or 32 e4m3
+                    if (f8) {
 #pragma unroll
-                    for (int kk = 0; kk < P_BK / 16; ++kk) {
-                        tc_mma_f16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
-                                        sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                                        (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < P_BK / 16; ++kk)
+                            tc_mma_f8_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
+                                           sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                           (kb | kk) != 0 ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < P_BK / 16; ++kk)
+                            tc_mma_f16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + kk * 32),
+                                            sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                            (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair(&empty[s], 0x3);
                     if (++s == P_STAGES) { s = 0; ph ^= 1u; }
@@ -389,6 +401,10 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     float *xb = xbuf + slot * 1024;  // [32 tokens][32 lanes]
                     const int u = c.nt * 128 + (int)rank * 64 + (l & 63);
                     __nv_bfloat16 *hcol = static_cast<__nv_bfloat16 *>(p.out0) + (size_t)c.row0 * p.n_out0 + u;
+                    // FP8 GEMM1: this lane's hidden unit's w1 / w3 scales
+                    const bool scaled = p.g1_fp8 && q < 2 && u < p.n_out0;
+                    const float sw1u = scaled ? p.w1_scale[(size_t)c.expert * p.n_out0 + u] : 1.f;
+                    const float sw3u = scaled ? p.w3_scale[(size_t)c.expert * p.n_out0 + u] : 1.f;
 #pragma unroll 1
                     for (int ch = 0; ch < nsw / 32; ++ch, ++xi) {
                         uint32_t d[32];
@@ -409,8 +425,13 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) {
                                     if (ch * 32 + j < c.nvalid) {
-                                        const float gv = __uint_as_float(d[j]);
-                                        const float uv = xb[j * 32 + lane];
+                                        float gv = __uint_as_float(d[j]);
+                                        float uv = xb[j * 32 + lane];
+                                        if (scaled) {
+                                            const float sx = p.x_scale[c.row0 + ch * 32 + j];
+                                            gv *= sx * sw1u;
+                                            uv *= sx * sw3u;
+                                        }
                                         hcol[(size_t)(ch * 32 + j) * p.n_out0] =
                                             __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
                                         if (p.gu_out) {
@@ -449,6 +470,10 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     // h chunks of 32 hidden units: gate at TMEM column gc, up at gc + 64
                     __nv_bfloat16 *hrow = static_cast<__nv_bfloat16 *>(p.out0) + orow;
                     const int nch = half ? 2 : 4;
+                    // FP8 GEMM1: the row's x scale; column scales of w1 / w3 below
+                    const float sxr = p.g1_fp8 && row_ok ? p.x_scale[crow0 + r] : 1.f;
+                    const float *sw1 = p.g1_fp8 ? p.w1_scale + (size_t)c.expert * p.n_out0 : nullptr;
+                    const float *sw3 = p.g1_fp8 ? p.w3_scale + (size_t)c.expert * p.n_out0 : nullptr;
 #pragma unroll 1
                     for (int ch = 0; ch < nch; ++ch) {
                         const int gc = half ? ch * 32 : (ch >> 1) * 128 + (ch & 1) * 32;
@@ -469,8 +494,12 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 #pragma unroll
                                     for (int z = 0; z < 2; ++z) {
                                         const int idx = v * 8 + e2 * 2 + z;
-                                        const float gv = __uint_as_float(g[idx]);
-                                        const float uv = __uint_as_float(u[idx]);
+                                        float gv = __uint_as_float(g[idx]);
+                                        float uv = __uint_as_float(u[idx]);
+                                        if (p.g1_fp8) {
+                                            gv *= sxr * sw1[col0 + v * 8 + e2 * 2 + z];
+                                            uv *= sxr * sw3[col0 + v * 8 + e2 * 2 + z];
+                                        }
                                         hv[z] = gv / (1.f + __expf(-gv)) * uv;
                                     }
                                     w[e2] = pack_bf16x2_p(hv[0], hv[1]);
@@ -632,56 +661,17 @@ int64_t grouped_pair_scratch_ints(int64_t rows_alloc, int E_local) {
     return 32 + (rows_alloc + P_PAIR_M - 1) / P_PAIR_M + E_local;
 }
 
-cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_offsets,
-                                            const int *tokens_per_expert, const void *w1,
-                                            const void *w3, const void *w2, void *h, void *y_perm,
-                                            int D, int H_local, int e_first, int E_local,
-                                            int64_t rows_alloc, int *scratch, int *status,
-                                            cudaStream_t stream, bool *launched, void *gu) {
-    *launched = false;
-    if (E_local == 0 || rows_alloc == 0) {
-        *launched = true;
-        return cudaSuccess;
-    }
-    const size_t smem = pair_smem_bytes(E_local);
-    if (smem > 227 * 1024) return cudaSuccess;  // not launched: caller falls back
-    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel, smem);
-    if (err != cudaSuccess) return err;
-    const int clusters_max = max_pair_clusters(smem);
-    if (clusters_max <= 0) return cudaSuccess;  // not launched: caller falls back
+namespace {
 
-    PairMaps m;
-    if (!make_tmap_2d(&m.x, x_perm, D, rows_alloc, P_BM) ||
-        !make_tmap_2d(&m.x64, x_perm, D, rows_alloc, P_BM / 2) ||
-        !make_tmap_2d(&m.x16, x_perm, D, rows_alloc, 16) ||
-        !make_tmap_3d(&m.w1, w1, D, H_local, E_local, 64) ||
-        !make_tmap_3d(&m.w3, w3, D, H_local, E_local, 64) ||
-        !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
-        !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
-        !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
-        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128))
-        return cudaErrorInvalidValue;
+// Runs GEMM1 + GEMM2 of the tile table: one cooperative launch for short
+// calls where the device accepts it, else two launches.
+cudaError_t run_pair(const PairMaps &m, const PairParams &p, int64_t rows_alloc, int E_local,
+                     int clusters_max, size_t smem, int *scratch, cudaStream_t stream,
+                     bool *launched) {
     const long long pt_bound = (rows_alloc + P_PAIR_M - 1) / P_PAIR_M + E_local;
-
-    PairParams p{};
-    p.E_local = E_local;
-    p.e_first = e_first;
-    p.rows_alloc = (int)rows_alloc;
-    p.nk0 = (D + P_BK - 1) / P_BK;
-    p.nk1 = (H_local + P_BK - 1) / P_BK;
-    p.nt0 = (H_local + 127) / 128;
-    p.nt1 = (D + P_BN - 1) / P_BN;
-    p.n_out0 = H_local;
-    p.n_out1 = D;
-    p.seg_off = seg_offsets;
-    p.tpe = tokens_per_expert;
-    p.out0 = h;
-    p.out1 = y_perm;
-    p.gu_out = (__nv_bfloat16 *)gu;
-    p.status = status;
-
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+    cudaError_t err;
 #ifndef MOE_PAIR_FUSED
 #define MOE_PAIR_FUSED 1
 #endif
@@ -722,6 +712,107 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     if ((err = launch_pair(m, p2, c2, smem, false, stream)) != cudaSuccess) return err;
     *launched = true;
     return cudaSuccess;
+}
+
+PairParams pair_params(const int *seg_offsets, const int *tokens_per_expert, void *h,
+                       void *y_perm, int D, int H_local, int e_first, int E_local,
+                       int64_t rows_alloc, int *status) {
+    PairParams p{};
+    p.E_local = E_local;
+    p.e_first = e_first;
+    p.rows_alloc = (int)rows_alloc;
+    p.nk0 = (D + P_BK - 1) / P_BK;
+    p.nk1 = (H_local + P_BK - 1) / P_BK;
+    p.nt0 = (H_local + 127) / 128;
+    p.nt1 = (D + P_BN - 1) / P_BN;
+    p.n_out0 = H_local;
+    p.n_out1 = D;
+    p.seg_off = seg_offsets;
+    p.tpe = tokens_per_expert;
+    p.out0 = h;
+    p.out1 = y_perm;
+    p.status = status;
+    return p;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_offsets,
+                                            const int *tokens_per_expert, const void *w1,
+                                            const void *w3, const void *w2, void *h, void *y_perm,
+                                            int D, int H_local, int e_first, int E_local,
+                                            int64_t rows_alloc, int *scratch, int *status,
+                                            cudaStream_t stream, bool *launched, void *gu) {
+    *launched = false;
+    if (E_local == 0 || rows_alloc == 0) {
+        *launched = true;
+        return cudaSuccess;
+    }
+    const size_t smem = pair_smem_bytes(E_local);
+    if (smem > 227 * 1024) return cudaSuccess;  // not launched: caller falls back
+    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel, smem);
+    if (err != cudaSuccess) return err;
+    const int clusters_max = max_pair_clusters(smem);
+    if (clusters_max <= 0) return cudaSuccess;  // not launched: caller falls back
+
+    PairMaps m;
+    if (!make_tmap_2d(&m.x, x_perm, D, rows_alloc, P_BM) ||
+        !make_tmap_2d(&m.x64, x_perm, D, rows_alloc, P_BM / 2) ||
+        !make_tmap_2d(&m.x16, x_perm, D, rows_alloc, 16) ||
+        !make_tmap_3d(&m.w1, w1, D, H_local, E_local, 64) ||
+        !make_tmap_3d(&m.w3, w3, D, H_local, E_local, 64) ||
+        !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
+        !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
+        !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
+        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128))
+        return cudaErrorInvalidValue;
+    PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
+                               E_local, rows_alloc, status);
+    p.gu_out = (__nv_bfloat16 *)gu;
+    return run_pair(m, p, rows_alloc, E_local, clusters_max, smem, scratch, stream, launched);
+}
+
+cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float *x_scale,
+                                           const int *seg_offsets, const int *tokens_per_expert,
+                                           const uint8_t *w1_q, const float *w1_scale,
+                                           const uint8_t *w3_q, const float *w3_scale,
+                                           const void *w2, void *h, void *y_perm, int D,
+                                           int H_local, int e_first, int E_local,
+                                           int64_t rows_alloc, int *scratch, int *status,
+                                           cudaStream_t stream, bool *launched) {
+    *launched = false;
+    if (E_local == 0 || rows_alloc == 0) {
+        *launched = true;
+        return cudaSuccess;
+    }
+    const size_t smem = pair_smem_bytes(E_local);
+    if (smem > 227 * 1024) return cudaSuccess;  // not launched
+    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel, smem);
+    if (err != cudaSuccess) return err;
+    const int clusters_max = max_pair_clusters(smem);
+    if (clusters_max <= 0) return cudaSuccess;  // not launched
+
+    // e4m3 operands of GEMM1: boxes of 128 K elements (128 bytes, the same
+    // 128-byte swizzled rows as the bf16 boxes of 64)
+    PairMaps m;
+    if (!make_tmap_tile(&m.x, x_perm_q, 1, D, rows_alloc, 0, 128, P_BM, 128) ||
+        !make_tmap_tile(&m.x64, x_perm_q, 1, D, rows_alloc, 0, 128, P_BM / 2, 128) ||
+        !make_tmap_tile(&m.x16, x_perm_q, 1, D, rows_alloc, 0, 128, 16, 128) ||
+        !make_tmap_tile(&m.w1, w1_q, 1, D, H_local, E_local, 128, 64, 128) ||
+        !make_tmap_tile(&m.w3, w3_q, 1, D, H_local, E_local, 128, 64, 128) ||
+        !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
+        !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
+        !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
+        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128))
+        return cudaErrorInvalidValue;
+    PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
+                               E_local, rows_alloc, status);
+    p.g1_fp8 = 1;
+    p.nk0 = (D + 2 * P_BK - 1) / (2 * P_BK);
+    p.x_scale = x_scale;
+    p.w1_scale = w1_scale;
+    p.w3_scale = w3_scale;
+    return run_pair(m, p, rows_alloc, E_local, clusters_max, smem, scratch, stream, launched);
 }
 
 }  // namespace moe

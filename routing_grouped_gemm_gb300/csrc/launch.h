@@ -48,8 +48,8 @@ bool make_tmap_3d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows
 // fp32 row-major [rows, cols], box = box_cols x box_rows, 128-byte swizzle.
 bool make_tmap_2d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
                       uint32_t box_cols, uint32_t box_rows);
-// Row-major [experts, rows, cols] (experts = 0: a 2-D [rows, cols]) of 2- or 4-byte
-// elements (bf16 / fp32), box = box_cols x box_rows (x 1), swizzle of
+// Row-major [experts, rows, cols] (experts = 0: a 2-D [rows, cols]) of 1-, 2- or
+// 4-byte elements (e4m3 codes / bf16 / fp32), box = box_cols x box_rows (x 1), swizzle of
 // 32, 64 or 128 bytes (box_cols x element bytes must equal it).
 bool make_tmap_tile(CUtensorMap *m, const void *base, int elem_bytes, uint64_t cols, uint64_t rows,
                     uint64_t experts, uint32_t box_cols, uint32_t box_rows, int swizzle_bytes);
@@ -83,7 +83,15 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                            int *seg_offsets, int *row_of, int *token_of_row, void *x_perm,
                            int T, int D, int E, int k, int e_first, int E_local, int layout,
                            int align_m, int capacity, int64_t rows_alloc, int elem_bytes,
-                           int *scratch, int *status, cudaStream_t stream);
+                           int *scratch, int *status, cudaStream_t stream,
+                           float *x_scale = nullptr);  // set: bf16 x -> e4m3 x_perm + row scales
+
+// Row-wise e4m3 quantisation of bf16 rows [rows, cols] (cols % 8 == 0):
+// scale[r] = amax / 448 (1 for a zero row), codes = e4m3(x / scale).  With
+// row_of [rows, k], row t's codes and scale go to rows row_of[t, j] (the
+// dispatch), else to row t.
+cudaError_t launch_quantize_rows_e4m3(const void *src, int64_t rows, int cols, const int *row_of,
+                                      int k, uint8_t *dst, float *scale, cudaStream_t stream);
 
 cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *topk_w, void *out,
                            int T, int D, int k, int64_t rows_alloc, int is_bf16, int *status,
@@ -98,6 +106,19 @@ cudaError_t launch_grouped_swiglu_f32(const float *x_perm, const int *seg_offset
 
 // Scratch ints of the pair kernel's one-launch schedule (block counters);
 // they must be zero before the first call and are left zero by each call.
+// The same with GEMM1 on e4m3 operands (kind::f8f6f4): x_perm_q [rows, D]
+// and w1_q / w3_q [E_local, H_local, D] codes with one scale per row
+// (x_scale [rows], w1_scale / w3_scale [E_local, H_local]); GEMM1's fp32
+// accumulator is multiplied by x_scale[row] * w_scale[unit] before SwiGLU.
+// GEMM2 stays bf16.  D % 16 == 0.
+cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float *x_scale,
+                                           const int *seg_offsets, const int *tokens_per_expert,
+                                           const uint8_t *w1_q, const float *w1_scale,
+                                           const uint8_t *w3_q, const float *w3_scale,
+                                           const void *w2, void *h, void *y_perm, int D,
+                                           int H_local, int e_first, int E_local,
+                                           int64_t rows_alloc, int *scratch, int *status,
+                                           cudaStream_t stream, bool *launched);
 int64_t grouped_pair_scratch_ints(int64_t rows_alloc, int E_local);
 
 // bf16 tcgen05 grouped SwiGLU on CTA pairs (cta_group::2).  With `scratch`

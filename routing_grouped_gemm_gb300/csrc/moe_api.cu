@@ -16,7 +16,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 10300;  // 1.3.0
+constexpr int32_t kAbiVersion = 10400;  // 1.4.0
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int64_t kAlign = 256;
@@ -128,6 +128,7 @@ struct LayerWs {
     int *topk_idx, *tpe, *seg_off, *row_of, *token_of_row;
     float *topk_w;
     void *x_perm, *h, *y_perm;
+    float *x_scale;  // FP8 layer: one scale per row of x_perm
 };
 
 int64_t layer_ws_layout(const moe_config *c, char *base, LayerWs *L) {
@@ -149,7 +150,9 @@ int64_t layer_ws_layout(const moe_config *c, char *base, LayerWs *L) {
     char *p_xp = take(rows * c->D * eb);
     char *p_h = take(rows * c->H_local * eb);
     char *p_yp = take(rows * c->D * 4);  // y_perm is fp32 for every dtype
+    char *p_xs = take(rows * 4);
     if (L) {
+        L->x_scale = reinterpret_cast<float *>(p_xs);
         L->topk_idx = reinterpret_cast<int *>(p_idx);
         L->topk_w = reinterpret_cast<float *>(p_w);
         L->tpe = reinterpret_cast<int *>(p_tpe);
@@ -241,11 +244,11 @@ moe_status do_route(const moe_config *c, const void *x, const void *wg, const fl
 
 moe_status do_permute(const moe_config *c, const void *x, const int32_t *topk_idx, int32_t *tpe,
                       int32_t *seg, int32_t *row_of, int32_t *tor, void *x_perm, const StepWs &w,
-                      cudaStream_t s) {
+                      cudaStream_t s, float *x_scale = nullptr) {
     cudaError_t e = moe::launch_permute(x, topk_idx, tpe, seg, row_of, tor, x_perm, c->T, c->D, c->E,
                                         c->k, c->e_first, c->E_local, c->layout, c->align_m,
                                         c->capacity, rows_alloc_of(c), elem_bytes(c), w.scratch,
-                                        &w.status->flags, s);
+                                        &w.status->flags, s, x_scale);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_permute");
 }
 
@@ -289,6 +292,33 @@ moe_status do_grouped(const moe_config *c, const void *x_perm, const int32_t *se
                                            (float *)y_perm, c->D, c->H_local, c->e_first,
                                            c->E_local, rows_alloc_of(c), &w.status->flags, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_grouped_swiglu");
+}
+
+// What the FP8 path supports: bf16 activations, D in whole 16-byte rows of
+// e4m3 codes and k <= 32 (one lane per slot in the quantising dispatch).
+moe_status fp8_supported(const moe_config *c) {
+    if (c->dtype != MOE_BF16) return arg_fail("FP8 path: bf16 activations only", MOE_ERR_UNSUPPORTED);
+    if (c->D % 16) return arg_fail("FP8 path: D must be a multiple of 16", MOE_ERR_UNSUPPORTED);
+    if (c->k > 32) return arg_fail("FP8 path: k <= 32", MOE_ERR_UNSUPPORTED);
+    return MOE_OK;
+}
+
+moe_status do_grouped_fp8(const moe_config *c, const void *x_perm_q, const float *x_scale,
+                          const int32_t *seg, const int32_t *tpe, const void *w1_q,
+                          const float *w1_scale, const void *w3_q, const float *w3_scale,
+                          const void *w2, void *h, void *y_perm, const StepWs &w, cudaStream_t s) {
+    const char *sel = getenv("MOE_GROUPED_KERNEL");
+    const bool two_launches = sel && strcmp(sel, "pair2") == 0;
+    bool launched = false;
+    const cudaError_t e = moe::launch_grouped_swiglu_fp8_pair(
+        (const uint8_t *)x_perm_q, x_scale, seg, tpe, (const uint8_t *)w1_q, w1_scale,
+        (const uint8_t *)w3_q, w3_scale, w2, h, y_perm, c->D, c->H_local, c->e_first, c->E_local,
+        rows_alloc_of(c), two_launches ? nullptr : w.grouped, &w.status->flags, s, &launched);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_grouped_swiglu_fp8");
+    if (!launched)
+        return arg_fail("moe_grouped_swiglu_fp8: too many local experts for the pair kernel",
+                        MOE_ERR_UNSUPPORTED);
+    return MOE_OK;
 }
 
 moe_status do_combine(const moe_config *c, const void *y_perm, const int32_t *row_of,
@@ -569,6 +599,94 @@ MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, c
     e = moe::launch_dispatch_bwd(W.dxp, L.row_of, dense ? W.dxr : nullptr, L.topk_idx, W.dl, wg,
                                  cfg->E, dx, cfg->T, cfg->D, cfg->k, rows, 1, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_backward: dispatch backward");
+}
+
+MOE_EXPORT moe_status moe_quantize_rows_fp8(const void *src, int64_t rows, int32_t cols,
+                                           uint8_t *dst, float *scale, moe_stream_t stream) {
+    if (rows < 0 || cols <= 0 || cols % 16) return arg_fail("moe_quantize_rows_fp8: bad shape");
+    if (rows == 0) return MOE_OK;
+    if (!need16(src) || !need16(dst) || !scale || !aligned(scale, 4))
+        return arg_fail("moe_quantize_rows_fp8: NULL or misaligned tensor");
+    const cudaError_t e = moe::launch_quantize_rows_e4m3(src, rows, cols, nullptr, 1, dst, scale,
+                                                         (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_quantize_rows_fp8");
+}
+
+MOE_EXPORT moe_status moe_permute_fp8(const moe_config *cfg, const void *x,
+                                      const int32_t *topk_idx, int32_t *tokens_per_expert,
+                                      int32_t *seg_offsets, int32_t *row_of,
+                                      int32_t *token_of_row, uint8_t *x_perm_q, float *x_scale,
+                                      void *ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = fp8_supported(cfg)) != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (!tokens_per_expert || !seg_offsets) return arg_fail("moe_permute_fp8: NULL tensor");
+    if (cfg->T > 0 && (!topk_idx || !row_of || !need16(x)))
+        return arg_fail("moe_permute_fp8: NULL or misaligned tensor");
+    if (rows_alloc_of(cfg) > 0 &&
+        (!token_of_row || !need16(x_perm_q) || !x_scale || !aligned(x_scale, 4)))
+        return arg_fail("moe_permute_fp8: NULL or misaligned tensor");
+    return do_permute(cfg, x, topk_idx, tokens_per_expert, seg_offsets, row_of, token_of_row,
+                      x_perm_q, w, (cudaStream_t)stream, x_scale);
+}
+
+MOE_EXPORT moe_status moe_grouped_swiglu_fp8(const moe_config *cfg, const uint8_t *x_perm_q,
+                                             const float *x_scale, const int32_t *seg_offsets,
+                                             const int32_t *tokens_per_expert,
+                                             const uint8_t *w1_q, const float *w1_scale,
+                                             const uint8_t *w3_q, const float *w3_scale,
+                                             const void *w2, void *h, void *y_perm, void *ws,
+                                             size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = fp8_supported(cfg)) != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (cfg->E_local == 0 || rows_alloc_of(cfg) == 0) return MOE_OK;
+    if (!seg_offsets || !tokens_per_expert) return arg_fail("moe_grouped_swiglu_fp8: NULL offsets");
+    if (!need16(x_perm_q) || !need16(w1_q) || !need16(w3_q) || !need16(w2) || !need16(h) ||
+        !need16(y_perm) || !x_scale || !w1_scale || !w3_scale || !aligned(x_scale, 4) ||
+        !aligned(w1_scale, 4) || !aligned(w3_scale, 4))
+        return arg_fail("moe_grouped_swiglu_fp8: NULL or misaligned tensor");
+    return do_grouped_fp8(cfg, x_perm_q, x_scale, seg_offsets, tokens_per_expert, w1_q, w1_scale,
+                          w3_q, w3_scale, w2, h, y_perm, w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_layer_forward_fp8(const moe_config *cfg, const void *x, const void *wg,
+                                            const float *bias, const uint8_t *w1_q,
+                                            const float *w1_scale, const uint8_t *w3_q,
+                                            const float *w3_scale, const void *w2, void *out,
+                                            void *ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = fp8_supported(cfg)) != MOE_OK) return st;
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < layer_ws_layout(cfg, nullptr, nullptr))
+        return arg_fail("workspace too small for moe_layer_forward_fp8", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!need16(x) || !need16(wg) || !need16(out) || (bias && !aligned(bias, 4)))
+        return arg_fail("moe_layer_forward_fp8: NULL or misaligned tensor");
+    if (cfg->E_local > 0 &&
+        (!need16(w1_q) || !need16(w3_q) || !need16(w2) || !w1_scale || !w3_scale ||
+         !aligned(w1_scale, 4) || !aligned(w3_scale, 4)))
+        return arg_fail("moe_layer_forward_fp8: NULL or misaligned expert weights");
+    LayerWs L;
+    carve_step(cfg, ws, ws_bytes, &L.step);
+    layer_ws_layout(cfg, static_cast<char *>(ws), &L);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = do_route(cfg, x, wg, bias, nullptr, L.topk_idx, L.topk_w, L.step, s)) != MOE_OK)
+        return st;
+    if ((st = do_permute(cfg, x, L.topk_idx, L.tpe, L.seg_off, L.row_of, L.token_of_row, L.x_perm,
+                         L.step, s, L.x_scale)) != MOE_OK)
+        return st;
+    if (cfg->E_local > 0 && rows_alloc_of(cfg) > 0 &&
+        (st = do_grouped_fp8(cfg, L.x_perm, L.x_scale, L.seg_off, L.tpe, w1_q, w1_scale, w3_q,
+                             w3_scale, w2, L.h, L.y_perm, L.step, s)) != MOE_OK)
+        return st;
+    return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
 }
 
 MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream) {

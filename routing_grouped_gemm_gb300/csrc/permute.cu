@@ -457,7 +457,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                            int *seg_offsets, int *row_of, int *token_of_row, void *x_perm,
                            int T, int D, int E, int k, int e_first, int E_local, int layout,
                            int align_m, int capacity, int64_t rows_alloc, int elem_bytes,
-                           int *scratch, int *status, cudaStream_t stream) {
+                           int *scratch, int *status, cudaStream_t stream, float *x_scale) {
     const int nblk = (T + PB_TOKENS - 1) / PB_TOKENS;
     int *blk_cnt = scratch;
     int *blk_base = scratch + (size_t)nblk * E;
@@ -502,6 +502,8 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
+    if (x_scale)  // FP8 dispatch: the copy quantises each token row once
+        return launch_quantize_rows_e4m3(x, T, D, row_of, k, (uint8_t *)x_perm, x_scale, stream);
     const int vpr = D * elem_bytes / 16;
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;

@@ -74,7 +74,7 @@ bool make_tmap_2d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t 
 bool make_tmap_tile(CUtensorMap *m, const void *base, int elem_bytes, uint64_t cols, uint64_t rows,
                     uint64_t experts, uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
     EncodeTiledFn f = encode_fn();
-    if (!f || (elem_bytes != 2 && elem_bytes != 4)) return false;
+    if (!f || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4)) return false;
     if (box_cols * (uint32_t)elem_bytes != (uint32_t)swizzle_bytes) return false;
     const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -86,7 +86,10 @@ bool make_tmap_tile(CUtensorMap *m, const void *base, int elem_bytes, uint64_t c
     const cuuint64_t strides[2] = {cols * elem_bytes, cols * rows * elem_bytes};
     const cuuint32_t box[3] = {box_cols, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return f(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+    const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return f(m, dt,
              rank, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
