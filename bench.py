@@ -260,6 +260,59 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
 
 
 
+def run_fp8(moe, cfg, inp, stream, dev, args, peaks):
+    """The FP8 variant of the same step: moe_layer_forward_fp8 (e4m3 dispatch,
+    GEMM1 on e4m3 codes with per-row scales, GEMM2 in bf16), the weights
+    quantised once before timing, as in inference.  Also times the grouped
+    call alone.  Its FLOPs are 4 R D H in e4m3 and 2 R D H in bf16; the
+    peak fraction compares the time both would take at the measured bf16
+    peak and twice it for e4m3 (the nominal dense fp8 : bf16 ratio)."""
+    import torch
+    w = inp.w
+    w1q, w1s = moe.quantize_weights_fp8(inp.w1)
+    w3q, w3s = moe.quantize_weights_fp8(inp.w3)
+    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
+    out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    views = moe.layer_views(cfg, lws)
+
+    def step():
+        moe.moe_layer_forward_fp8(cfg, inp.x, inp.wg, inp.bias, w1q, w1s, w3q, w3s, inp.w2, out,
+                                  lws, stream)
+
+    def grouped():
+        moe.moe_grouped_swiglu_fp8(cfg, views["x_perm_q"], views["x_scale"], views["seg_offsets"],
+                                   views["tokens_per_expert"], w1q, w1s, w3q, w3s, inp.w2,
+                                   views["h"], views["y_perm"], lws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    res = {}
+    for name, fn in (("step", step), ("grouped", grouped)):
+        n = max(20, args.steps // 4)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = e0.elapsed_time(e1) / n
+    st = moe.moe_get_device_status(lws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after the fp8 leg: {moe.status_string(st)}")
+    R = w.T * w.k
+    f8_flops, bf_flops = 4.0 * R * w.D * w.H, 2.0 * R * w.D * w.H
+    ideal_ms = (f8_flops / (2 * peaks["bf16_tflops"] * 1e12) + bf_flops / (peaks["bf16_tflops"] * 1e12)) * 1e3
+    return {"api": "moe_layer_forward_fp8 (C ABI), weights quantised once",
+            "dtype": "e4m3 GEMM1 operands (one fp32 scale per row), bf16 GEMM2",
+            "ms_per_step": res["step"], "value": w.T / (res["step"] * 1e-3), "unit": UNIT,
+            "grouped_ms": res["grouped"],
+            "grouped_tflops": (f8_flops + bf_flops) / (res["grouped"] * 1e-3) / 1e12,
+            "grouped_frac_of_peak": ideal_ms / res["grouped"],
+            "peak_note": "e4m3 at 2x the measured bf16 burst peak, bf16 at the measured peak"}
+
+
 def run_backward(moe, cfg, inp, stream, dev, args, peaks):
     """The training step's backward on the same batch: moe_layer_forward_train,
     then moe_layer_backward (all gradients), timed with CUDA events on the
@@ -428,6 +481,9 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(moe, cfg, inp, out, stream, dev, world, args)
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = run_fp8(moe, cfg, inp, stream, dev, args, load_peaks())
     backward = None
     if not args.no_backward:
         backward = run_backward(moe, cfg, inp, stream, dev, args, load_peaks())
@@ -464,6 +520,7 @@ def run_gpu(args):
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
                               "zeros": int((tpe_h == 0).sum())},
         "e2e": e2e,
+        "fp8": fp8,
         "backward": backward,
         "gpu_launches": n_launches,
         "clocks": clk.summary(),
@@ -494,6 +551,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--no-backward", action="store_true", help="skip the training backward leg")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (e4m3 GEMM1) leg")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the training step (forward_train + backward), print its JSON")
     ap.add_argument("--scale", default="",

@@ -148,6 +148,13 @@ __device__ __forceinline__ PairTile decode_pair(int v, const PairParams &p, int 
     return c;
 }
 
+// SiLU(g) = g / (1 + e^-g) with the fast approximate division (2 ulp in
+// fp32, far below h's bf16 rounding).  The correctly rounded division cost
+// the e4m3 GEMM1 a third of its time on GB300 (fine-grained GEMM1 alone:
+// 221 against 149 us); the bf16 GEMM1, bound by its operands, is unchanged.
+// For g < -87 the divisor overflows and the quotient is 0, as SiLU is there.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -421,19 +428,24 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         } else {
                             const bool ok = mbar_wait_bounded(&xfull[slot], xph, abort_flag);
                             if (!__all_sync(0xffffffffu, ok)) { xok = false; break; }
-                            if (u < p.n_out0) {
+                            // FP8: lane j fetches the x scale of token ch * 32 + j and
+                            // the whole warp takes it by shuffle (uniform control flow)
+                            const bool f8s = p.g1_fp8 != 0;
+                            const float sxl = f8s && ch * 32 + lane < c.nvalid
+                                                  ? p.x_scale[c.row0 + ch * 32 + lane] : 1.f;
+                            {
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) {
-                                    if (ch * 32 + j < c.nvalid) {
+                                    const float sx = f8s ? __shfl_sync(0xffffffffu, sxl, j) : 1.f;
+                                    if (u < p.n_out0 && ch * 32 + j < c.nvalid) {
                                         float gv = __uint_as_float(d[j]);
                                         float uv = xb[j * 32 + lane];
                                         if (scaled) {
-                                            const float sx = p.x_scale[c.row0 + ch * 32 + j];
                                             gv *= sx * sw1u;
                                             uv *= sx * sw3u;
                                         }
                                         hcol[(size_t)(ch * 32 + j) * p.n_out0] =
-                                            __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
+                                            __float2bfloat16_rn(silu_f(gv) * uv);
                                         if (p.gu_out) {
                                             __nv_bfloat16 *gr = p.gu_out +
                                                 (size_t)(c.row0 + ch * 32 + j) * 2 * p.n_out0 + u;
@@ -478,50 +490,64 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     for (int ch = 0; ch < nch; ++ch) {
                         const int gc = half ? ch * 32 : (ch >> 1) * 128 + (ch & 1) * 32;
                         const int hcol = half ? nhalf * 64 + ch * 32 : ch * 32;
+                        const int col0 = c.nt * 128 + hcol;
+                        // FP8: lane i fetches the scales of unit col0 + i (in flight
+                        // with the TMEM loads); the elements take them by shuffle
+                        float s1 = 1.f, s3 = 1.f;
+                        if (p.g1_fp8 && col0 + lane < n_out) {
+                            s1 = sw1[col0 + lane];
+                            s3 = sw3[col0 + lane];
+                        }
                         uint32_t g[32], u[32];
                         tmem_ld_32x32b_x32(tbase + gc, g);
                         tmem_ld_32x32b_x32(tbase + gc + 64, u);
                         tc_wait_ld();
-                        const int col0 = c.nt * 128 + hcol;
-                        if (row_ok) {
 #pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                if (col0 + v * 8 >= n_out) break;
-                                uint32_t w[4];
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 >= n_out) break;  // uniform across the warp
+                            // FP8: row scale times the units' scales, shuffled from
+                            // the lanes that fetched them (every lane takes part)
+                            float a1[8], a3[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                a1[i] = p.g1_fp8 ? sxr * __shfl_sync(0xffffffffu, s1, v * 8 + i) : 1.f;
+                                a3[i] = p.g1_fp8 ? sxr * __shfl_sync(0xffffffffu, s3, v * 8 + i) : 1.f;
+                            }
+                            if (!row_ok) continue;
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                float hv[2];
+#pragma unroll
+                                for (int z = 0; z < 2; ++z) {
+                                    const int idx = v * 8 + e2 * 2 + z;
+                                    float gv = __uint_as_float(g[idx]);
+                                    float uv = __uint_as_float(u[idx]);
+                                    if (p.g1_fp8) {
+                                        gv *= a1[e2 * 2 + z];
+                                        uv *= a3[e2 * 2 + z];
+                                    }
+                                    hv[z] = silu_f(gv) * uv;
+                                }
+                                w[e2] = pack_bf16x2_p(hv[0], hv[1]);
+                            }
+                            *reinterpret_cast<uint4 *>(hrow + col0 + v * 8) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                            if (p.gu_out) {
+                                // training forward: keep g and u for the backward
+                                __nv_bfloat16 *gr = p.gu_out +
+                                    (size_t)(crow0 + r) * 2 * p.n_out0 + col0 + v * 8;
+                                uint32_t pg[4], pu[4];
 #pragma unroll
                                 for (int e2 = 0; e2 < 4; ++e2) {
-                                    float hv[2];
-#pragma unroll
-                                    for (int z = 0; z < 2; ++z) {
-                                        const int idx = v * 8 + e2 * 2 + z;
-                                        float gv = __uint_as_float(g[idx]);
-                                        float uv = __uint_as_float(u[idx]);
-                                        if (p.g1_fp8) {
-                                            gv *= sxr * sw1[col0 + v * 8 + e2 * 2 + z];
-                                            uv *= sxr * sw3[col0 + v * 8 + e2 * 2 + z];
-                                        }
-                                        hv[z] = gv / (1.f + __expf(-gv)) * uv;
-                                    }
-                                    w[e2] = pack_bf16x2_p(hv[0], hv[1]);
+                                    pg[e2] = pack_bf16x2_p(__uint_as_float(g[v * 8 + e2 * 2]),
+                                                           __uint_as_float(g[v * 8 + e2 * 2 + 1]));
+                                    pu[e2] = pack_bf16x2_p(__uint_as_float(u[v * 8 + e2 * 2]),
+                                                           __uint_as_float(u[v * 8 + e2 * 2 + 1]));
                                 }
-                                *reinterpret_cast<uint4 *>(hrow + col0 + v * 8) =
-                                    make_uint4(w[0], w[1], w[2], w[3]);
-                                if (p.gu_out) {
-                                    // training forward: keep g and u for the backward
-                                    __nv_bfloat16 *gr = p.gu_out +
-                                        (size_t)(crow0 + r) * 2 * p.n_out0 + col0 + v * 8;
-                                    uint32_t pg[4], pu[4];
-#pragma unroll
-                                    for (int e2 = 0; e2 < 4; ++e2) {
-                                        pg[e2] = pack_bf16x2_p(__uint_as_float(g[v * 8 + e2 * 2]),
-                                                               __uint_as_float(g[v * 8 + e2 * 2 + 1]));
-                                        pu[e2] = pack_bf16x2_p(__uint_as_float(u[v * 8 + e2 * 2]),
-                                                               __uint_as_float(u[v * 8 + e2 * 2 + 1]));
-                                    }
-                                    *reinterpret_cast<uint4 *>(gr) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
-                                    *reinterpret_cast<uint4 *>(gr + p.n_out0) =
-                                        make_uint4(pu[0], pu[1], pu[2], pu[3]);
-                                }
+                                *reinterpret_cast<uint4 *>(gr) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+                                *reinterpret_cast<uint4 *>(gr + p.n_out0) =
+                                    make_uint4(pu[0], pu[1], pu[2], pu[3]);
                             }
                         }
                     }
