@@ -395,6 +395,13 @@ def run_gpu(args):
     inp = moe_inputs.make_inputs(w, device=dev, seed=rank)
     cfg = moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k, dtype=moe.MOE_BF16,
                      score=moe.MOE_SCORE_SOFTMAX, renorm=1, align_m=128)
+    if args.fp8_only:
+        fp8 = run_fp8(moe, cfg, inp, torch.cuda.current_stream(dev), dev, args, load_peaks())
+        if rank == 0:
+            print(json.dumps({"workload": WORKLOAD, "fp8": fp8}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     if args.backward_only:
         backward = run_backward(moe, cfg, inp, torch.cuda.current_stream(dev), dev, args,
                                 load_peaks())
@@ -552,6 +559,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--no-backward", action="store_true", help="skip the training backward leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (e4m3 GEMM1) leg")
+    ap.add_argument("--fp8-only", action="store_true", help="time only the FP8 leg, print its JSON")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the training step (forward_train + backward), print its JSON")
     ap.add_argument("--scale", default="",
