@@ -260,6 +260,41 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
 
 
 
+def run_fused(moe, cfg, inp, stream, dev, args):
+    """The same step through moe_layer_forward_fused: the combine fused into
+    GEMM2's epilogue (fp32 atomic adds into a [T, D] accumulator, then one
+    rounding kernel), so y_perm is never written or read back."""
+    import torch
+    w = inp.w
+    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
+    out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        moe.moe_layer_forward_fused(cfg, inp.x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out,
+                                    lws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(20, args.steps // 4)
+    n0 = moe.kernel_launches()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = (moe.kernel_launches() - n0) / n
+    st = moe.moe_get_device_status(lws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after the fused leg: {moe.status_string(st)}")
+    ms = e0.elapsed_time(e1) / n
+    return {"api": "moe_layer_forward_fused (C ABI): combine in GEMM2's epilogue, fp32 atomics",
+            "ms_per_step": ms, "value": w.T / (ms * 1e-3), "unit": UNIT,
+            "launches_per_step": launches, "deterministic": False}
+
+
 def run_fp8(moe, cfg, inp, stream, dev, args, peaks):
     """The FP8 variant of the same step: moe_layer_forward_fp8 (e4m3 dispatch,
     GEMM1 on e4m3 codes with per-row scales, GEMM2 in bf16), the weights
@@ -488,6 +523,9 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(moe, cfg, inp, out, stream, dev, world, args)
+    fused = None
+    if not args.no_fused:
+        fused = run_fused(moe, cfg, inp, stream, dev, args)
     fp8 = None
     if not args.no_fp8:
         fp8 = run_fp8(moe, cfg, inp, stream, dev, args, load_peaks())
@@ -527,6 +565,7 @@ def run_gpu(args):
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
                               "zeros": int((tpe_h == 0).sum())},
         "e2e": e2e,
+        "fused_combine": fused,
         "fp8": fp8,
         "backward": backward,
         "gpu_launches": n_launches,
@@ -559,6 +598,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--no-backward", action="store_true", help="skip the training backward leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (e4m3 GEMM1) leg")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused-combine leg")
     ap.add_argument("--fp8-only", action="store_true", help="time only the FP8 leg, print its JSON")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the training step (forward_train + backward), print its JSON")

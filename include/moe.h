@@ -361,6 +361,22 @@ moe_status moe_layer_forward_fp8(const moe_config *cfg, const void *x, const voi
                                  void *out, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_layer_forward with the combine fused into the grouped GEMM's second
+ * GEMM ([EP] section 2: the permute / combine fusion that removes a round
+ * trip of the routed rows): GEMM2's epilogue multiplies each row's fp32
+ * result by its slot weight and adds it into an fp32 [T, D] accumulator
+ * (the y_perm buffer of ws) with atomic adds; a last kernel rounds it to
+ * the bf16 out.  y_perm is never written.  The sum over a token's slots
+ * runs in whatever order the tiles finish, so -- unlike moe_layer_forward --
+ * results may differ in the last bits from run to run.  bf16, D % 4 == 0,
+ * workspace moe_layer_workspace_size.
+ */
+moe_status moe_layer_forward_fused(const moe_config *cfg, const void *x, const void *wg,
+                                   const float *bias, const void *w1, const void *w3,
+                                   const void *w2, void *out, void *ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
+/*
  * moe_permute without a workspace (this entry point has no counterpart in
  * the pages; it exists for callers that cannot allocate device memory).
  *

@@ -34,6 +34,7 @@ ABI_SYMBOLS = (
     "moe_layer_host_workspace_size", "moe_layer_forward_host",
     "moe_layer_train_workspace_size", "moe_layer_forward_train", "moe_layer_backward",
     "moe_quantize_rows_fp8", "moe_permute_fp8", "moe_grouped_swiglu_fp8", "moe_layer_forward_fp8",
+    "moe_layer_forward_fused",
 )
 
 
@@ -82,6 +83,7 @@ def _load() -> ctypes.CDLL:
         "moe_permute_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_grouped_swiglu_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_layer_forward_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_layer_forward_fused": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -476,6 +478,25 @@ def moe_layer_forward_fp8(cfg: Config, x, wg, bias, w1_q, w1_scale, w3_q, w3_sca
                                       _ptr(w1_scale), _ptr(w3_q), _ptr(w3_scale), _ptr(w2),
                                       _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_layer_forward_fp8")
+
+
+def moe_layer_forward_fused(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None):
+    """moe_layer_forward with the combine fused into GEMM2's epilogue (fp32
+    atomics; not bitwise reproducible run to run)."""
+    el = cfg.e_local
+    dt = cfg.torch_dtype
+    _expect(x, (cfg.T, cfg.D), dt, "x")
+    _expect(wg, (cfg.E, cfg.D), dt, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    _expect(out, (cfg.T, cfg.D), dt, "out")
+    c = cfg.c()
+    _check(_lib.moe_layer_forward_fused(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w1),
+                                        _ptr(w3), _ptr(w2), _ptr(out), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "moe_layer_forward_fused")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

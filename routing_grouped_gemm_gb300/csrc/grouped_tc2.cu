@@ -109,6 +109,13 @@ struct PairParams {
     // with one scale per row of x_perm and per row of w1 / w3 ([E_local, H_local])
     int g1_fp8;
     const float *x_scale, *w1_scale, *w3_scale;
+    // Combine fused into GEMM2: its epilogue adds w * y for each row into
+    // comb [T, n_out1] (fp32 atomics; the token and slot weight of row r from
+    // token_of_row, row_of [T, k] and topk_w) instead of storing y_perm
+    float *comb;
+    const int *token_of_row, *row_of;
+    const float *topk_w;
+    int k;
     void *out1;           // fp32 y [rows, D]
     int *done;            // SCHED_BOTH: [max_blocks] GEMM1 epilogue warps finished, per block
     int max_blocks;       // SCHED_BOTH: entries of done[]
@@ -154,6 +161,15 @@ __device__ __forceinline__ PairTile decode_pair(int v, const PairParams &p, int 
 // 221 against 149 us); the bf16 GEMM1, bound by its operands, is unchanged.
 // For g < -87 the divisor overflows and the quotient is 0, as SiLU is there.
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
+// Slot weight of row r of token t (0 when the row is not one of t's slots).
+__device__ __forceinline__ float slot_weight(const PairParams &p, int r, int t) {
+    if (t < 0) return 0.f;
+    const int *ro = p.row_of + (size_t)t * p.k;
+    for (int j = 0; j < p.k; ++j)
+        if (ro[j] == r) return p.topk_w[(size_t)t * p.k + j];
+    return 0.f;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -391,12 +407,27 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     for (int ch = 0; ch < nsw / 32; ++ch) {
                         uint32_t d[32];
                         tmem_ld_32x32b_x32(tb + ch * 32, d);
+                        // fused combine: lane j looks up token ch * 32 + j and its
+                        // slot weight; the warp takes them by shuffle
+                        int tl = -1;
+                        float wl = 0.f;
+                        if (p.comb && ch * 32 + lane < c.nvalid) {
+                            const int rr = c.row0 + ch * 32 + lane;
+                            tl = p.token_of_row[rr];
+                            wl = slot_weight(p, rr, tl);
+                        }
                         tc_wait_ld();
-                        if (dcol < p.n_out1) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (ch * 32 + j < c.nvalid)
+                        for (int j = 0; j < 32; ++j) {
+                            const int tj = p.comb ? __shfl_sync(0xffffffffu, tl, j) : -1;
+                            const float wj = p.comb ? __shfl_sync(0xffffffffu, wl, j) : 0.f;
+                            if (dcol < p.n_out1 && ch * 32 + j < c.nvalid) {
+                                if (!p.comb)
                                     ycol[(size_t)(ch * 32 + j) * p.n_out1] = __uint_as_float(d[j]);
+                                else if (tj >= 0)
+                                    atomicAdd(p.comb + (size_t)tj * p.n_out1 + dcol,
+                                              wj * __uint_as_float(d[j]));
+                            }
                         }
                     }
                 } else {
@@ -554,6 +585,14 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 } else {
                     float *yrow = static_cast<float *>(p.out1) + orow;
                     const int nch = half ? 4 : P_BN / 32;
+                    // fused combine: this lane's token and slot weight
+                    int tok = -1;
+                    float wr = 0.f;
+                    if (p.comb && row_ok) {
+                        tok = p.token_of_row[crow0 + r];
+                        wr = slot_weight(p, crow0 + r, tok);
+                    }
+                    float *crow = p.comb && tok >= 0 ? p.comb + (size_t)tok * n_out : nullptr;
 #pragma unroll 1
                     for (int ch = 0; ch < nch; ++ch) {
                         uint32_t d[32];
@@ -564,8 +603,16 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
                                 if (col0 + v * 4 >= n_out) break;
-                                *reinterpret_cast<uint4 *>(yrow + col0 + v * 4) =
-                                    make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2], d[v * 4 + 3]);
+                                if (!p.comb) {
+                                    *reinterpret_cast<uint4 *>(yrow + col0 + v * 4) =
+                                        make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2], d[v * 4 + 3]);
+                                } else if (crow) {
+                                    atomicAdd(reinterpret_cast<float4 *>(crow + col0 + v * 4),
+                                              make_float4(wr * __uint_as_float(d[v * 4]),
+                                                          wr * __uint_as_float(d[v * 4 + 1]),
+                                                          wr * __uint_as_float(d[v * 4 + 2]),
+                                                          wr * __uint_as_float(d[v * 4 + 3])));
+                                }
                             }
                         }
                     }
@@ -768,7 +815,8 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
                                             const void *w3, const void *w2, void *h, void *y_perm,
                                             int D, int H_local, int e_first, int E_local,
                                             int64_t rows_alloc, int *scratch, int *status,
-                                            cudaStream_t stream, bool *launched, void *gu) {
+                                            cudaStream_t stream, bool *launched, void *gu,
+                                            const FusedCombine *fc) {
     *launched = false;
     if (E_local == 0 || rows_alloc == 0) {
         *launched = true;
@@ -795,6 +843,13 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
                                E_local, rows_alloc, status);
     p.gu_out = (__nv_bfloat16 *)gu;
+    if (fc) {
+        p.comb = fc->comb;
+        p.token_of_row = fc->token_of_row;
+        p.row_of = fc->row_of;
+        p.topk_w = fc->topk_w;
+        p.k = fc->k;
+    }
     return run_pair(m, p, rows_alloc, E_local, clusters_max, smem, scratch, stream, launched);
 }
 

@@ -84,7 +84,11 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                            int T, int D, int E, int k, int e_first, int E_local, int layout,
                            int align_m, int capacity, int64_t rows_alloc, int elem_bytes,
                            int *scratch, int *status, cudaStream_t stream,
-                           float *x_scale = nullptr);  // set: bf16 x -> e4m3 x_perm + row scales
+                           float *x_scale = nullptr,   // set: bf16 x -> e4m3 x_perm + row scales
+                           float *zero_out = nullptr);  // set: zero rows [T, D] fp32 (fused combine)
+
+// out[i] = bf16(comb[i]) for the fused combine's fp32 accumulator (n % 4 == 0).
+cudaError_t launch_comb_to_bf16(const float *comb, void *out, int64_t n, cudaStream_t stream);
 
 // Row-wise e4m3 quantisation of bf16 rows [rows, cols] (cols % 8 == 0):
 // scale[r] = amax / 448 (1 for a zero row), codes = e4m3(x / scale).  With
@@ -121,6 +125,17 @@ cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float 
                                            cudaStream_t stream, bool *launched);
 int64_t grouped_pair_scratch_ints(int64_t rows_alloc, int E_local);
 
+// Combine fused into the grouped GEMM's second GEMM: its epilogue adds
+// topk_w[t, j] * y for each row r = row_of[t, j] into comb [T, D] (fp32,
+// zeroed beforehand) with atomic adds, instead of storing y_perm.  The sum
+// over a token's slots then runs in no fixed order.
+struct FusedCombine {
+    float *comb;
+    const int *token_of_row, *row_of;
+    const float *topk_w;
+    int k;
+};
+
 // bf16 tcgen05 grouped SwiGLU on CTA pairs (cta_group::2).  With `scratch`
 // both GEMMs run in one cooperative launch; without it, or where the device
 // refuses a cooperative cluster launch, in two.  Sets *launched to false (and
@@ -132,7 +147,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
                                             int D, int H_local, int e_first, int E_local,
                                             int64_t rows_alloc, int *scratch, int *status,
                                             cudaStream_t stream, bool *launched,
-                                            void *gu = nullptr);
+                                            void *gu = nullptr, const FusedCombine *fc = nullptr);
 
 // Backward of the bf16 grouped SwiGLU on CTA pairs: dgu = SwiGLU'(gy . w2_e)
 // with the saved gate/up gu, dxp = dgu . [w1_e; w3_e] (fp32), and the weight

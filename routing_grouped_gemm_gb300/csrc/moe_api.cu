@@ -244,11 +244,11 @@ moe_status do_route(const moe_config *c, const void *x, const void *wg, const fl
 
 moe_status do_permute(const moe_config *c, const void *x, const int32_t *topk_idx, int32_t *tpe,
                       int32_t *seg, int32_t *row_of, int32_t *tor, void *x_perm, const StepWs &w,
-                      cudaStream_t s, float *x_scale = nullptr) {
+                      cudaStream_t s, float *x_scale = nullptr, float *zero_out = nullptr) {
     cudaError_t e = moe::launch_permute(x, topk_idx, tpe, seg, row_of, tor, x_perm, c->T, c->D, c->E,
                                         c->k, c->e_first, c->E_local, c->layout, c->align_m,
                                         c->capacity, rows_alloc_of(c), elem_bytes(c), w.scratch,
-                                        &w.status->flags, s, x_scale);
+                                        &w.status->flags, s, x_scale, zero_out);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_permute");
 }
 
@@ -687,6 +687,53 @@ MOE_EXPORT moe_status moe_layer_forward_fp8(const moe_config *cfg, const void *x
                              w3_scale, w2, L.h, L.y_perm, L.step, s)) != MOE_OK)
         return st;
     return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
+}
+
+MOE_EXPORT moe_status moe_layer_forward_fused(const moe_config *cfg, const void *x, const void *wg,
+                                              const float *bias, const void *w1, const void *w3,
+                                              const void *w2, void *out, void *ws,
+                                              size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->dtype != MOE_BF16)
+        return arg_fail("moe_layer_forward_fused: bf16 only", MOE_ERR_UNSUPPORTED);
+    if (cfg->D % 4) return arg_fail("moe_layer_forward_fused: D % 4 != 0", MOE_ERR_UNSUPPORTED);
+    // the fp32 accumulator [T, D] lives in the y_perm buffer, which it must fit
+    if (rows_alloc_of(cfg) < cfg->T || cfg->E_local == 0)
+        return moe_layer_forward(cfg, x, wg, bias, w1, w3, w2, out, ws, ws_bytes, stream);
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < layer_ws_layout(cfg, nullptr, nullptr))
+        return arg_fail("workspace too small for moe_layer_forward_fused", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!need16(x) || !need16(wg) || !need16(out) || (bias && !aligned(bias, 4)))
+        return arg_fail("moe_layer_forward_fused: NULL or misaligned tensor");
+    if (!need16(w1) || !need16(w3) || !need16(w2))
+        return arg_fail("moe_layer_forward_fused: NULL or misaligned expert weights");
+    LayerWs L;
+    carve_step(cfg, ws, ws_bytes, &L.step);
+    layer_ws_layout(cfg, static_cast<char *>(ws), &L);
+    cudaStream_t s = (cudaStream_t)stream;
+    float *comb = static_cast<float *>(L.y_perm);
+    if ((st = do_route(cfg, x, wg, bias, nullptr, L.topk_idx, L.topk_w, L.step, s)) != MOE_OK)
+        return st;
+    if ((st = do_permute(cfg, x, L.topk_idx, L.tpe, L.seg_off, L.row_of, L.token_of_row, L.x_perm,
+                         L.step, s, nullptr, comb)) != MOE_OK)
+        return st;
+    const moe::FusedCombine fc{comb, L.token_of_row, L.row_of, L.topk_w, cfg->k};
+    const char *sel = getenv("MOE_GROUPED_KERNEL");
+    const bool two_launches = sel && strcmp(sel, "pair2") == 0;
+    bool launched = false;
+    cudaError_t e = moe::launch_grouped_swiglu_bf16_pair(
+        L.x_perm, L.seg_off, L.tpe, w1, w3, w2, L.h, L.y_perm, cfg->D, cfg->H_local, cfg->e_first,
+        cfg->E_local, rows_alloc_of(cfg), two_launches ? nullptr : L.step.grouped,
+        &L.step.status->flags, s, &launched, nullptr, &fc);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_layer_forward_fused: grouped SwiGLU");
+    if (!launched)
+        return arg_fail("moe_layer_forward_fused: too many local experts for the pair kernel",
+                        MOE_ERR_UNSUPPORTED);
+    e = moe::launch_comb_to_bf16(comb, out, (int64_t)cfg->T * cfg->D, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_fused: output");
 }
 
 MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream) {

@@ -323,12 +323,17 @@ constexpr int CP_UNROLL = 4;
 
 __global__ void __launch_bounds__(256)
 permute_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ row_of,
-                    uint4 *__restrict__ x_perm, int T, int k, int vpr) {
+                    uint4 *__restrict__ x_perm, int T, int k, int vpr,
+                    float4 *__restrict__ zero_out, int zvpr) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
+    if (zero_out) {  // the fused combine's accumulator row of this token starts at zero
+        float4 *z = zero_out + (size_t)t * zvpr;
+        for (int v = lane; v < zvpr; v += 32) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const int my_row = lane < k ? row_of[(size_t)t * k + lane] : -1;
     const uint4 *src = x + (size_t)t * vpr;
     for (int v0 = 0; v0 < vpr; v0 += 32 * CP_UNROLL) {
@@ -457,7 +462,8 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                            int *seg_offsets, int *row_of, int *token_of_row, void *x_perm,
                            int T, int D, int E, int k, int e_first, int E_local, int layout,
                            int align_m, int capacity, int64_t rows_alloc, int elem_bytes,
-                           int *scratch, int *status, cudaStream_t stream, float *x_scale) {
+                           int *scratch, int *status, cudaStream_t stream, float *x_scale,
+                           float *zero_out) {
     const int nblk = (T + PB_TOKENS - 1) / PB_TOKENS;
     int *blk_cnt = scratch;
     int *blk_base = scratch + (size_t)nblk * E;
@@ -508,10 +514,41 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;
     if ((err = launch_pdl(permute_copy_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
-                          (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr)) != cudaSuccess)
+                          (const uint4 *)x, row_of, (uint4 *)x_perm, T, k, vpr,
+                          (float4 *)zero_out, D / 4)) != cudaSuccess)
         return err;
     count_launch();
     return cudaGetLastError();
+}
+
+namespace {
+// out[i] = bf16(comb[i]), four elements per thread step.
+__global__ void __launch_bounds__(256)
+comb_to_bf16_kernel(const float4 *__restrict__ comb, uint2 *__restrict__ out, long long n4) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 v = __ldcs(comb + i);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t *>(&lo);
+        o.y = *reinterpret_cast<uint32_t *>(&hi);
+        out[i] = o;
+    }
+}
+}  // namespace
+
+cudaError_t launch_comb_to_bf16(const float *comb, void *out, int64_t n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    if (n % 4) return cudaErrorInvalidValue;
+    const long long n4 = n / 4;
+    const unsigned blocks = (unsigned)std::min<long long>((n4 + 255) / 256, 8 * 152);
+    const cudaError_t e = launch_pdl(comb_to_bf16_kernel, dim3(blocks), dim3(256), 0, stream,
+                                     (const float4 *)comb, (uint2 *)out, n4);
+    if (e == cudaSuccess) count_launch();
+    return e;
 }
 
 cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *topk_w, void *out,
