@@ -58,8 +58,13 @@ constexpr int P_BM = 128;                        // rows per CTA
 constexpr int P_PAIR_M = 2 * P_BM;               // rows per pair tile
 constexpr int P_BN = 256;                        // N of the pair MMA
 constexpr int P_BK = 64;
+// GEMM2's fp32 y through shared memory and TMA stores (1) or straight
+// from registers (0); the staging takes one ring stage's worth of smem.
+#ifndef MOE_PAIR_TMA_Y
+#define MOE_PAIR_TMA_Y 1
+#endif
 #ifndef MOE_PAIR_STAGES
-#define MOE_PAIR_STAGES 6
+#define MOE_PAIR_STAGES (MOE_PAIR_TMA_Y ? 5 : 6)
 #endif
 constexpr int P_STAGES = MOE_PAIR_STAGES;
 constexpr int P_A_BYTES = P_BM * P_BK * 2;       // 16 KB
@@ -85,6 +90,9 @@ constexpr int P_NBARS = 24;
 constexpr int P_SWAP_MAX = MOE_PAIR_SWAP_MAX;
 static_assert(P_SWAP_MAX <= P_PAIR_M, "a transposed tile holds at most 256 tokens");
 constexpr int P_XBUF_BYTES = 2 * 32 * 32 * 4;  // GEMM1 transposed tiles: up -> gate handoff
+// GEMM2 y staging: per epilogue warp two 32 x 32 fp32 boxes (128-byte swizzle)
+constexpr int P_YBOX_BYTES = 32 * 32 * 4;
+constexpr int P_YSTAGE_BYTES = MOE_PAIR_TMA_Y ? P_EPI_WARPS * 2 * P_YBOX_BYTES : 0;
 
 
 // Tile schedules.
@@ -124,7 +132,8 @@ struct PairParams {
 };
 
 size_t pair_smem_bytes(int E_local) {
-    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES + P_NBARS * sizeof(uint64_t) + 16 +
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES + P_YSTAGE_BYTES +
+           P_NBARS * sizeof(uint64_t) + 16 +
            sizeof(int) * (4 * (size_t)E_local + 1);
 }
 
@@ -182,7 +191,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
                     const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmH64,
                     const __grid_constant__ CUtensorMap tmH16,
-                    const __grid_constant__ CUtensorMap tmW2, const PairParams p) {
+                    const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmY,
+                    const PairParams p) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint8_t smem_raw[];
@@ -190,7 +200,9 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     // transposed GEMM1 tiles hand the up values over through xbuf [2][32 tokens][32 lanes]
     float *xbuf = reinterpret_cast<float *>(ring + P_STAGES * P_STAGE_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES);
+    uint8_t *ystage = ring + P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES;  // 1 KB aligned
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(ring + P_STAGES * P_STAGE_BYTES + P_XBUF_BYTES + P_YSTAGE_BYTES);
     uint64_t *full = bars;                   // [P_STAGES]  leader: both CTAs' TMA -> MMA
     uint64_t *empty = bars + P_STAGES;       // [P_STAGES]  MMA -> each CTA's TMA
     uint64_t *tfull = bars + 2 * P_STAGES;   // [2]         MMA -> each CTA's epilogue
@@ -238,6 +250,7 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 prefetch_tmap(&tmW3);
             }
             if (p.sched != SCHED_GEMM1) {
+                prefetch_tmap(&tmY);
                 prefetch_tmap(&tmH);
                 prefetch_tmap(&tmH64);
                 prefetch_tmap(&tmH16);
@@ -377,11 +390,15 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
     } else {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
-        // Each warp owns 32 accumulator rows (its TMEM lane quarter) and
-        // stores them straight from registers, valid rows only.  (Staging
-        // through shared memory for TMA stores was measured slower: the
-        // stores then compete with the operand loads for the TMA unit.)
+        // Each warp owns 32 accumulator rows (its TMEM lane quarter).  h
+        // (GEMM1) goes out straight from registers, valid rows only.  GEMM2's
+        // fp32 y goes out through a swizzled smem box and a TMA store per
+        // 32-column chunk (double-buffered) when all 32 of the warp's rows are
+        // valid, else straight from registers as well, so rows without a
+        // token are never written.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint8_t *ybuf = ystage + (warp - 2) * 2 * P_YBOX_BYTES;
+        uint32_t n_ystore = 0;  // TMA stores issued by this warp (selects the box)
         const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
         int it = 0;
         uint32_t xi = 0;  // handoffs done through xbuf (transposed GEMM1 tiles)
@@ -585,6 +602,9 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 } else {
                     float *yrow = static_cast<float *>(p.out1) + orow;
                     const int nch = half ? 4 : P_BN / 32;
+                    // this warp's 32 rows start at wrow within the CTA's rows
+                    const int wrow = half ? (q & 1) * 32 : q * 32;
+                    const bool tma_y = MOE_PAIR_TMA_Y && !p.comb && wrow + 32 <= cvalid;
                     // fused combine: this lane's token and slot weight
                     int tok = -1;
                     float wr = 0.f;
@@ -599,6 +619,26 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         tmem_ld_32x32b_x32(tbase + ch * 32, d);
                         tc_wait_ld();
                         const int col0 = c.nt * P_BN + nhalf * 128 + ch * 32;
+                        if (tma_y) {
+                            if (col0 >= n_out) continue;  // uniform across the warp
+                            if (lane == 0) bulk_wait_group_read<1>();  // this box's last store has read it
+                            __syncwarp();
+                            // row `lane` of the box; 16-byte unit j at (j ^ (lane & 7))
+                            uint8_t *brow = ybuf + (n_ystore & 1) * P_YBOX_BYTES + lane * 128;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<uint4 *>(brow + ((j ^ (lane & 7)) << 4)) =
+                                    make_uint4(d[j * 4], d[j * 4 + 1], d[j * 4 + 2], d[j * 4 + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmY, ybuf + (n_ystore & 1) * P_YBOX_BYTES, col0,
+                                             crow0 + wrow);
+                                bulk_commit_group();
+                            }
+                            ++n_ystore;
+                            continue;
+                        }
                         if (row_ok) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
@@ -636,6 +676,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         }
     }
 
+    if (warp >= 2 && (threadIdx.x & 31) == 0)
+        bulk_wait_group_all();  // every y store has landed before the CTA exits
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the leader's MMAs (which read both CTAs' smem) are done
@@ -693,7 +735,7 @@ int max_pair_clusters(size_t smem) {
 }
 
 struct PairMaps {
-    CUtensorMap x, x64, x16, w1, w3, h, h64, h16, w2;
+    CUtensorMap x, x64, x16, w1, w3, h, h64, h16, w2, y;
 };
 
 cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, size_t smem,
@@ -720,7 +762,7 @@ cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, si
     cfg.attrs = attr;
     cfg.numAttrs = (cooperative || MOE_PDL) ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_pair_kernel, m.x, m.x64, m.x16, m.w1,
-                                             m.w3, m.h, m.h64, m.h16, m.w2, p);
+                                             m.w3, m.h, m.h64, m.h16, m.w2, m.y, p);
     if (e == cudaSuccess) count_launch();
     return e;
 }
@@ -838,7 +880,8 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
         !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
         !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
         !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
-        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128))
+        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128) ||
+        !make_tmap_tile(&m.y, y_perm, 4, D, rows_alloc, 0, 32, 32, 128))
         return cudaErrorInvalidValue;
     PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
                                E_local, rows_alloc, status);
@@ -884,7 +927,8 @@ cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float 
         !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
         !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
         !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
-        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128))
+        !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128) ||
+        !make_tmap_tile(&m.y, y_perm, 4, D, rows_alloc, 0, 32, 32, 128))
         return cudaErrorInvalidValue;
     PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
                                E_local, rows_alloc, status);
