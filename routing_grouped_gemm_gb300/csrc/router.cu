@@ -237,6 +237,7 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
 // tensor-core logits: part[s][e][t] = sum over D-slice s of x[t,:] wg[e,:]
 // ---------------------------------------------------------------------
 constexpr int RC_BM = 128, RC_BK = 64, RC_STAGES = 4, RC_THREADS = 192;
+constexpr int RC_NBARS = 2 * RC_STAGES + 2;  // full, empty, done (+1 spare)
 // The cluster form runs extra warps that only join the reduction and top-k.
 #ifndef MOE_ROUTER_CL_WARPS
 #define MOE_ROUTER_CL_WARPS 16
@@ -261,7 +262,7 @@ struct RouterTcParams {
 __host__ __device__ inline int rc_stage_bytes(int n_pad) { return RC_A_BYTES + n_pad * RC_BK * 2; }
 
 inline size_t rc_smem_bytes(int n_pad) {
-    return 1024 + (size_t)RC_STAGES * rc_stage_bytes(n_pad) + 16 * sizeof(uint64_t) + 16;
+    return 1024 + (size_t)RC_STAGES * rc_stage_bytes(n_pad) + RC_NBARS * sizeof(uint64_t) + 16;
 }
 
 __host__ __device__ inline uint32_t rc_tmem_cols(int n_pad) {
@@ -290,7 +291,7 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     uint64_t *full = bars;                 // [RC_STAGES]
     uint64_t *empty = bars + RC_STAGES;    // [RC_STAGES]
     uint64_t *done = bars + 2 * RC_STAGES; // accumulator complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + RC_NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
