@@ -139,3 +139,37 @@ def test_training_forward_equals_forward(moe):
                           inputs["w2"], ref, lws)
     assert moe.moe_get_device_status(lws) == moe.MOE_OK
     assert torch.equal(out, ref)
+
+
+def test_backward_masked_layout_equals_contiguous(moe):
+    """The masked layout (capacity = T, nothing dropped) holds the same rows
+    per expert in the same order as the contiguous one, so every gradient
+    is bit-identical."""
+    T, D, H, E, k = 256, 128, 128, 8, 2
+    res = {}
+    for layout in (moe.MOE_LAYOUT_CONTIGUOUS, moe.MOE_LAYOUT_MASKED):
+        g = torch.Generator(device="cuda").manual_seed(21)
+        x = _bf(torch.randn((T, D), generator=g, device="cuda"))
+        wg = _bf(torch.randn((E, D), generator=g, device="cuda") * (2.0 / D ** 0.5))
+        w1 = _bf(torch.randn((E, H, D), generator=g, device="cuda") * 0.05)
+        w3 = _bf(torch.randn((E, H, D), generator=g, device="cuda") * 0.05)
+        w2 = _bf(torch.randn((E, D, H), generator=g, device="cuda") * 0.05)
+        dout = _bf(torch.randn((T, D), generator=g, device="cuda"))
+        cfg = moe.Config(T=T, D=D, H_local=H, E=E, k=k, dtype=moe.MOE_BF16,
+                         score=moe.MOE_SCORE_SOFTMAX, renorm=1, layout=layout,
+                         capacity=T if layout == moe.MOE_LAYOUT_MASKED else 0)
+        ws = moe.alloc_workspace(cfg, train=True)
+        out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+        moe.moe_layer_forward_train(cfg, x, wg, None, w1, w3, w2, out, ws)
+        gr = dict(dx=torch.empty((T, D), dtype=torch.bfloat16, device="cuda"),
+                  dwg=torch.empty((E, D), device="cuda"), dbias=torch.empty((E,), device="cuda"),
+                  dw1=torch.empty((E, H, D), device="cuda"), dw3=torch.empty((E, H, D), device="cuda"),
+                  dw2=torch.empty((E, D, H), device="cuda"))
+        moe.moe_layer_backward(cfg, x, wg, w1, w3, w2, dout, gr["dx"], gr["dwg"], gr["dbias"],
+                               gr["dw1"], gr["dw3"], gr["dw2"], ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        res[layout] = (out, gr)
+    (o0, g0), (o1, g1) = res[moe.MOE_LAYOUT_CONTIGUOUS], res[moe.MOE_LAYOUT_MASKED]
+    assert torch.equal(o0, o1)
+    for name in g0:
+        assert torch.equal(g0[name], g1[name]), name

@@ -162,6 +162,7 @@ def test_grouped_fp8_tile_shapes(moe, kernel, monkeypatch):
 @pytest.mark.parametrize("name,over,n_sample", [
     ("fine-grained-bf16", dict(T=640), 96),
     ("deepseek-v3-shaped", dict(T=300), 12),
+    ("decode-masked", dict(), 16),           # masked layout, capacity = T
 ])
 def test_layer_fp8_matches_oracle(moe, name, over, n_sample):
     w = moe_inputs.WORKLOADS[name].scaled(**over)
@@ -222,3 +223,24 @@ def test_fp8_rejects_unsupported(moe):
     out = torch.empty_like(x)
     with pytest.raises(moe.MoeError):
         moe.moe_layer_forward_fp8(cfg, x, wg, None, q, s, q, s, w2, out, ws)
+
+
+def test_layer_fp8_expert_ranges_sum_to_layer(moe):
+    """Expert-range shards of the FP8 layer add up to the whole FP8 layer."""
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=512, D=512, H=256, E=16)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=6)
+    w1q, w1s = _weights_fp8(moe, inp.w1)
+    w3q, w3s = _weights_fp8(moe, inp.w3)
+
+    def run(cfg, e0, el):
+        ws = moe.alloc_workspace(cfg, layer=True)
+        out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device="cuda")
+        moe.moe_layer_forward_fp8(cfg, inp.x, inp.wg, inp.bias, w1q[e0:e0 + el], w1s[e0:e0 + el],
+                                  w3q[e0:e0 + el], w3s[e0:e0 + el], inp.w2[e0:e0 + el], out, ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        return out.double()
+
+    full = run(cfg_for(moe, w), 0, w.E)
+    total = sum(run(cfg_for(moe, w, e_first=e0, E_local=8), e0, 8) for e0 in (0, 8))
+    rms = full.pow(2).mean().sqrt().item()
+    assert (total - full).abs().max().item() <= 2e-2 * rms
