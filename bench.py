@@ -395,16 +395,35 @@ def run_backward(moe, cfg, inp, stream, dev, args, peaks):
     st = moe.moe_get_device_status(tws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after backward: {moe.status_string(st)}")
+    # the same backward with bf16 expert weight gradients
+    b1, b3, b2 = (torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for t in (dw1, dw3, dw2))
+
+    def bwd16():
+        moe.moe_layer_backward(cfg, inp.x, inp.wg, inp.w1, inp.w3, inp.w2, dout, dx, dwg, dbias,
+                               b1, b3, b2, tws, stream)
+
+    for _ in range(3):
+        bwd16()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        bwd16()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    b16_ms = e0.elapsed_time(e1) / n
     f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
     b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n
     flops = 12.0 * w.T * w.k * w.D * w.H
     tf = flops / (b_ms * 1e-3) / 1e12
-    del tws, dw1, dw3, dw2
+    del tws, dw1, dw3, dw2, b1, b3, b2
     return {"api": "moe_layer_forward_train + moe_layer_backward (dx, dwg, dbias, dw1, dw3, dw2)",
             "forward_train_ms": f_ms, "backward_ms": b_ms,
             "training_step_tokens_per_s": w.T / ((f_ms + b_ms) * 1e-3),
             "backward_expert_flops": flops, "backward_tflops": tf,
             "backward_frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "backward_bf16_weight_grads_ms": b16_ms,
+            "backward_bf16_weight_grads_tflops": flops / (b16_ms * 1e-3) / 1e12,
             "launches_per_forward_and_backward": launches}
 
 

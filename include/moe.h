@@ -296,6 +296,18 @@ moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *
                               float *dw2, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_layer_backward with the expert weight gradients dw1, dw3, dw2 in
+ * wgrad_dtype: MOE_F32 (the same as moe_layer_backward) or MOE_BF16 (each
+ * fp32 sum rounded once to nearest-even bf16: half the bytes of the
+ * weight-gradient writes, which bound those GEMMs).  dwg and dbias stay fp32.
+ */
+moe_status moe_layer_backward_ex(const moe_config *cfg, const void *x, const void *wg,
+                                 const void *w1, const void *w3, const void *w2, const void *dout,
+                                 void *dx, float *dwg, float *dbias, void *dw1, void *dw3,
+                                 void *dw2, int32_t wgrad_dtype, void *ws, size_t ws_bytes,
+                                 moe_stream_t stream);
+
+/*
  * FP8 e4m3 dispatch (page "Expert Parallelism (EP)", llm-infra-atlas: the FP8
  * dispatch of its next steps -- dispatched activations as e4m3 values with
  * scales feeding an FP8 grouped GEMM).  The page does not fix the scale

@@ -34,7 +34,7 @@ ABI_SYMBOLS = (
     "moe_layer_host_workspace_size", "moe_layer_forward_host",
     "moe_layer_train_workspace_size", "moe_layer_forward_train", "moe_layer_backward",
     "moe_quantize_rows_fp8", "moe_permute_fp8", "moe_grouped_swiglu_fp8", "moe_layer_forward_fp8",
-    "moe_layer_forward_fused",
+    "moe_layer_forward_fused", "moe_layer_backward_ex",
 )
 
 
@@ -84,6 +84,7 @@ def _load() -> ctypes.CDLL:
         "moe_grouped_swiglu_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_layer_forward_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_layer_forward_fused": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_layer_backward_ex": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -376,23 +377,31 @@ def moe_layer_forward_train(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, strea
 
 def moe_layer_backward(cfg: Config, x, wg, w1, w3, w2, dout, dx, dwg, dbias, dw1, dw3, dw2, ws,
                        stream=None):
-    """Gradients for the forward last run by moe_layer_forward_train on ws."""
+    """Gradients for the forward last run by moe_layer_forward_train on ws.
+
+    dw1, dw3 and dw2 may be fp32 or bf16 (all three the same); dwg and dbias
+    are fp32.
+    """
     dt = cfg.torch_dtype
     el = cfg.e_local
     f32 = torch.float32
+    wdt = dw1.dtype if dw1 is not None else f32
+    if wdt not in (torch.float32, torch.bfloat16):
+        raise ValueError("dw1, dw3, dw2: float32 or bfloat16")
     _expect(dout, (cfg.T, cfg.D), dt, "dout")
     _expect(dx, (cfg.T, cfg.D), dt, "dx")
     _expect(dwg, (cfg.E, cfg.D), f32, "dwg")
     if dbias is not None:
         _expect(dbias, (cfg.E,), f32, "dbias")
-    _expect(dw1, (el, cfg.H_local, cfg.D), f32, "dw1")
-    _expect(dw3, (el, cfg.H_local, cfg.D), f32, "dw3")
-    _expect(dw2, (el, cfg.D, cfg.H_local), f32, "dw2")
+    _expect(dw1, (el, cfg.H_local, cfg.D), wdt, "dw1")
+    _expect(dw3, (el, cfg.H_local, cfg.D), wdt, "dw3")
+    _expect(dw2, (el, cfg.D, cfg.H_local), wdt, "dw2")
     c = cfg.c()
-    _check(_lib.moe_layer_backward(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(w1), _ptr(w3), _ptr(w2),
-                                   _ptr(dout), _ptr(dx), _ptr(dwg), _ptr(dbias), _ptr(dw1),
-                                   _ptr(dw3), _ptr(dw2), _ptr(ws), ws.numel(), _stream(stream)),
-           "moe_layer_backward")
+    _check(_lib.moe_layer_backward_ex(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(w1), _ptr(w3),
+                                      _ptr(w2), _ptr(dout), _ptr(dx), _ptr(dwg), _ptr(dbias),
+                                      _ptr(dw1), _ptr(dw3), _ptr(dw2),
+                                      MOE_BF16 if wdt == torch.bfloat16 else MOE_F32, _ptr(ws),
+                                      ws.numel(), _stream(stream)), "moe_layer_backward")
 
 
 # --------------------------------------------------------------------------

@@ -79,6 +79,7 @@ struct BwdParams {
     int stages;            // smem ring depth
     int epi_bytes;         // staging bytes per epilogue warp
     int epi_warps;         // 4 or 8 epilogue warps
+    int out_bf16;          // BE_STORE: the output boxes hold bf16 (32 x 32, 64-byte swizzle)
     const int *seg_off, *tpe;
     int H;
     int *status;
@@ -366,7 +367,22 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 __syncwarp();
                 uint8_t *ob = stg + (n_store & 1) * B_BOX_BYTES;
                 const int col0 = c.n0 + ch * 32;
-                if (!swiglu) {
+                if (!swiglu && p.out_bf16) {
+                    // 32 x 32 bf16 box, 64-byte swizzle: 16-byte unit j of row r at (j ^ ((r >> 1) & 3))
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                empty_expert ? 0.f : __uint_as_float(d[j * 8 + e2 * 2]),
+                                empty_expert ? 0.f : __uint_as_float(d[j * 8 + e2 * 2 + 1]));
+                            w[e2] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(ob + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else if (!swiglu) {
                     // 32 x 32 fp32 box, 128-byte swizzle: 16-byte unit j of row r at (j ^ (r & 7))
                     uint8_t *row = ob + lane * 128;
 #pragma unroll
@@ -556,9 +572,10 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
                                       const void *gy, const int *seg_offsets,
                                       const int *tokens_per_expert, const int *token_of_row,
                                       const void *w1, const void *w3, const void *w2,
-                                      void *dgu, float *dxp, float *dw1, float *dw3, float *dw2,
+                                      void *dgu, float *dxp, void *dw1, void *dw3, void *dw2,
                                       int D, int H_local, int e_first, int E_local,
-                                      int64_t rows_alloc, int *status, cudaStream_t stream) {
+                                      int64_t rows_alloc, int *status, cudaStream_t stream,
+                                      int grad_bf16) {
     (void)token_of_row;
     if (E_local == 0 || rows_alloc == 0) return cudaSuccess;
     if (D % 32 || H_local % 32) return cudaErrorInvalidValue;  // whole 32-column boxes
@@ -638,9 +655,11 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.mt = (D + B_PAIR_M - 1) / B_PAIR_M;
         p.nt = (H_local + B_BN - 1) / B_BN;
         p.m_split = D;
+        p.out_bf16 = grad_bf16;
+        const int eb = grad_bf16 ? 2 : 4;  // 32-column boxes: 64 or 128 bytes wide
         if (!make_tmap_2d(&tA, gy, D, rows_alloc, B_BK) ||
             !make_tmap_2d(&tB0, h, H_local, rows_alloc, B_BK) ||
-            !make_tmap_tile(&tO0, dw2, 4, H_local, D, E_local, 32, 32, 128))
+            !make_tmap_tile(&tO0, dw2, eb, H_local, D, E_local, 32, 32, 32 * eb))
             return cudaErrorInvalidValue;
         if ((err = launch_bwd(tA, tB0, tB0, tO0, tO0, p, (long long)E_local * p.mt * p.nt,
                               stream)) != cudaSuccess)
@@ -658,10 +677,12 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
         p.mt = (2 * H_local + B_PAIR_M - 1) / B_PAIR_M;
         p.nt = (D + B_BN - 1) / B_BN;
         p.m_split = H_local;
+        p.out_bf16 = grad_bf16;
+        const int eb = grad_bf16 ? 2 : 4;
         if (!make_tmap_2d(&tA, dgu, H2, rows_alloc, B_BK) ||
             !make_tmap_2d(&tB0, x_perm, D, rows_alloc, B_BK) ||
-            !make_tmap_tile(&tO0, dw1, 4, D, H_local, E_local, 32, 32, 128) ||
-            !make_tmap_tile(&tO1, dw3, 4, D, H_local, E_local, 32, 32, 128))
+            !make_tmap_tile(&tO0, dw1, eb, D, H_local, E_local, 32, 32, 32 * eb) ||
+            !make_tmap_tile(&tO1, dw3, eb, D, H_local, E_local, 32, 32, 32 * eb))
             return cudaErrorInvalidValue;
         if ((err = launch_bwd(tA, tB0, tB0, tO0, tO1, p, (long long)E_local * p.mt * p.nt,
                               stream)) != cudaSuccess)

@@ -151,16 +151,18 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
 
 // Backward of the bf16 grouped SwiGLU on CTA pairs: dgu = SwiGLU'(gy . w2_e)
 // with the saved gate/up gu, dxp = dgu . [w1_e; w3_e] (fp32), and the weight
-// gradients dw1, dw3 [E_local, H, D], dw2 [E_local, D, H] (fp32).  Padding
+// gradients dw1, dw3 [E_local, H, D], dw2 [E_local, D, H] (fp32, or bf16 with
+// grad_bf16: the fp32 sums rounded once).  Padding
 // rows of x_perm, h and gy are set to zero first.  Needs D and H_local
 // multiples of 64 and segments starting on multiples of 64 rows.
 cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const void *gu,
                                       const void *gy, const int *seg_offsets,
                                       const int *tokens_per_expert, const int *token_of_row,
                                       const void *w1, const void *w3, const void *w2,
-                                      void *dgu, float *dxp, float *dw1, float *dw3, float *dw2,
+                                      void *dgu, float *dxp, void *dw1, void *dw3, void *dw2,
                                       int D, int H_local, int e_first, int E_local,
-                                      int64_t rows_alloc, int *status, cudaStream_t stream);
+                                      int64_t rows_alloc, int *status, cudaStream_t stream,
+                                      int grad_bf16 = 0);  // dw1, dw3, dw2 in bf16 (else fp32)
 int64_t grouped_bwd_smem(int E_local);
 
 // Backward of the combine: gy[row] = bf16(w * dout[t]) (rows without a token

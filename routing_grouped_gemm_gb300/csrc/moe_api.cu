@@ -555,11 +555,13 @@ MOE_EXPORT moe_status moe_layer_forward_train(const moe_config *cfg, const void 
     return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
 }
 
-MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *wg,
-                                         const void *w1, const void *w3, const void *w2,
-                                         const void *dout, void *dx, float *dwg, float *dbias,
-                                         float *dw1, float *dw3, float *dw2, void *ws,
-                                         size_t ws_bytes, moe_stream_t stream) {
+MOE_EXPORT moe_status moe_layer_backward_ex(const moe_config *cfg, const void *x, const void *wg,
+                                            const void *w1, const void *w3, const void *w2,
+                                            const void *dout, void *dx, float *dwg, float *dbias,
+                                            void *dw1, void *dw3, void *dw2, int32_t wgrad_dtype,
+                                            void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (wgrad_dtype != MOE_F32 && wgrad_dtype != MOE_BF16)
+        return arg_fail("moe_layer_backward_ex: wgrad_dtype must be MOE_F32 or MOE_BF16");
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     if ((st = train_supported(cfg)) != MOE_OK) return st;
@@ -587,7 +589,7 @@ MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, c
         e = moe::launch_grouped_swiglu_bwd(L.x_perm, L.h, W.gu, W.gy, L.seg_off, L.tpe,
                                            L.token_of_row, w1, w3, w2, W.dgu, W.dxp, dw1, dw3, dw2,
                                            cfg->D, cfg->H_local, cfg->e_first, cfg->E_local, rows,
-                                           flags, s);
+                                           flags, s, wgrad_dtype == MOE_BF16);
         if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: grouped SwiGLU backward");
     }
     e = moe::launch_router_bwd(x, wg, W.logits, L.topk_idx, L.topk_w, W.dw, W.dl, W.dxr, dwg, dbias,
@@ -734,6 +736,15 @@ MOE_EXPORT moe_status moe_layer_forward_fused(const moe_config *cfg, const void 
                         MOE_ERR_UNSUPPORTED);
     e = moe::launch_comb_to_bf16(comb, out, (int64_t)cfg->T * cfg->D, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_fused: output");
+}
+
+MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *wg,
+                                         const void *w1, const void *w3, const void *w2,
+                                         const void *dout, void *dx, float *dwg, float *dbias,
+                                         float *dw1, float *dw3, float *dw2, void *ws,
+                                         size_t ws_bytes, moe_stream_t stream) {
+    return moe_layer_backward_ex(cfg, x, wg, w1, w3, w2, dout, dx, dwg, dbias, dw1, dw3, dw2,
+                                 MOE_F32, ws, ws_bytes, stream);
 }
 
 MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream) {

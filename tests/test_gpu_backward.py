@@ -173,3 +173,22 @@ def test_backward_masked_layout_equals_contiguous(moe):
     assert torch.equal(o0, o1)
     for name in g0:
         assert torch.equal(g0[name], g1[name]), name
+
+
+def test_backward_bf16_weight_gradients_are_rounded_fp32(moe):
+    """With bf16 weight gradients, each is the fp32 result rounded once to
+    nearest-even; dx, dwg and dbias do not change."""
+    T, D, H, E, k = 512, 256, 192, 8, 2
+    cfg, ws, out, g32, inputs = _run(moe, T, D, H, E, k, "softmax", True, seed=31)
+    g16 = {n: torch.empty_like(t, dtype=torch.bfloat16) for n, t in g32.items()
+           if n in ("dw1", "dw3", "dw2")}
+    rest = dict(dx=torch.empty_like(g32["dx"]), dwg=torch.empty_like(g32["dwg"]),
+                dbias=torch.empty_like(g32["dbias"]))
+    moe.moe_layer_backward(cfg, inputs["x"], inputs["wg"], inputs["w1"], inputs["w3"], inputs["w2"],
+                           inputs["dout"], rest["dx"], rest["dwg"], rest["dbias"], g16["dw1"],
+                           g16["dw3"], g16["dw2"], ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    for n in ("dw1", "dw3", "dw2"):
+        assert torch.equal(g16[n], g32[n].to(torch.bfloat16)), n
+    for n in ("dx", "dwg", "dbias"):
+        assert torch.equal(rest[n], g32[n]), n
