@@ -385,6 +385,90 @@ router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
     if (tid == 0) ctr[tile] = 0;  // ready for the next call
 }
 
+// dwg and dbias from the expert-contiguous layout, where dl is zero off each
+// token's selected experts and every selected (token, expert) has a row:
+//   dwg[e, :] = sum_{rows r of e} dl[t_r, e] x[t_r, :],  dbias[e] = sum_r dl[t_r, e]
+// Block (c, e) walks the segment in chunks of RS_CHUNK rows: the block first
+// stages each row's token and dl value in shared memory, then 8 warps take
+// the chunk's rows round-robin, each lane 8 columns of the 256-column chunk c
+// (one 16-byte load of x's row, which the L2 holds).  The warps' partial
+// sums are added in warp order, so the result is deterministic.
+constexpr int RS_COLS = 256, RS_WARPS = 8, RS_CHUNK = 512;
+template <bool BF16>
+__global__ void __launch_bounds__(32 * RS_WARPS)
+router_wgrad_seg_kernel(const void *__restrict__ x, const float *__restrict__ dl,
+                        const int *__restrict__ seg_off, const int *__restrict__ tpe,
+                        const int *__restrict__ token_of_row, int T, int D, int E,
+                        float *__restrict__ dwg, float *__restrict__ dbias) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    __shared__ float part[RS_WARPS][RS_COLS + 1];
+    __shared__ float bpart[RS_WARPS];
+    __shared__ int s_tok[RS_CHUNK];
+    __shared__ float s_g[RS_CHUNK];
+    const int e = blockIdx.y, c0 = blockIdx.x * RS_COLS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = seg_off[e], n = min(tpe[e], seg_off[e + 1] - seg_off[e]);
+    const int col = c0 + lane * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float bsum = 0.f;
+    for (int base = 0; base < n; base += RS_CHUNK) {
+        const int m = min(RS_CHUNK, n - base);
+        __syncthreads();  // the previous chunk's entries are consumed
+        for (int i = threadIdx.x; i < m; i += blockDim.x) {
+            const int t = token_of_row[b + base + i];
+            const bool ok = t >= 0 && t < T;
+            s_tok[i] = ok ? t : -1;
+            s_g[i] = ok ? dl[(size_t)t * E + e] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int i = warp; i < m; i += RS_WARPS) {
+            const int t = s_tok[i];
+            if (t < 0) continue;
+            const float g = s_g[i];
+            bsum += g;
+            if (col < D) {
+                float v[8];
+                if (BF16) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(x) + (size_t)t * D + col);
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v[2 * u] = __low2float(h2[u]);
+                        v[2 * u + 1] = __high2float(h2[u]);
+                    }
+                } else {
+                    const float4 a = *reinterpret_cast<const float4 *>(
+                        static_cast<const float *>(x) + (size_t)t * D + col);
+                    const float4 a2 = *reinterpret_cast<const float4 *>(
+                        static_cast<const float *>(x) + (size_t)t * D + col + 4);
+                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                    v[4] = a2.x; v[5] = a2.y; v[6] = a2.z; v[7] = a2.w;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc[u] = fmaf(g, v[u], acc[u]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) part[warp][lane * 8 + u] = acc[u];
+    if (lane == 0) bpart[warp] = bsum;
+    __syncthreads();
+    for (int cc = threadIdx.x; cc < RS_COLS; cc += blockDim.x) {
+        if (c0 + cc >= D) continue;
+        float sum = part[0][cc];
+        for (int w = 1; w < RS_WARPS; ++w) sum += part[w][cc];
+        dwg[(size_t)e * D + c0 + cc] = sum;
+    }
+    if (dbias && blockIdx.x == 0 && threadIdx.x == 0) {
+        float sum = bpart[0];
+        for (int w = 1; w < RS_WARPS; ++w) sum += bpart[w];
+        dbias[e] = sum;
+    }
+}
+
 // Splits of dwg's K (= T): enough (tile, split) blocks for two waves of the
 // 152 SMs, at least 256 tokens per split, at most 16 splits.
 struct RouterSplit {
@@ -457,7 +541,7 @@ cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits
                               const int *topk_idx, const float *topk_w, const float *dw, float *dl,
                               float *dx_router, float *dwg, float *dbias, float *scratch, int T,
                               int D, int E, int k, int score, int renorm, int is_bf16,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const RouterSegments *segs) {
     if (T == 0) return cudaSuccess;
     if (D % 4) return cudaErrorInvalidValue;
     const RouterSplit sp = router_split(T, D, E);
@@ -470,6 +554,18 @@ cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits
                                ctr ? tiles : 0);
     if (e != cudaSuccess) return e;
     count_launch();
+    if (segs && !router_dl_dense(score, renorm) && D % 8 == 0) {
+        // dl is zero off the selected experts: sum x rows over each expert's segment
+        const dim3 grid((unsigned)((D + RS_COLS - 1) / RS_COLS), (unsigned)E);
+        e = is_bf16 ? launch_pdl(router_wgrad_seg_kernel<true>, grid, dim3(32 * RS_WARPS), 0,
+                                 stream, x, (const float *)dl, segs->seg_off, segs->tpe,
+                                 segs->token_of_row, T, D, E, dwg, dbias)
+                    : launch_pdl(router_wgrad_seg_kernel<false>, grid, dim3(32 * RS_WARPS), 0,
+                                 stream, x, (const float *)dl, segs->seg_off, segs->tpe,
+                                 segs->token_of_row, T, D, E, dwg, dbias);
+        if (e == cudaSuccess) count_launch();
+        return e;
+    }
     // dwg [E, D] = dl^T x  (K = T, split), dbias = the column sums of dl
     e = is_bf16 ? router_gemm<true>(dl, 1, E, x, D, dwg, dbias, part, cpart, ctr, E, D, T, sp.S,
                                     sp.kc, stream)

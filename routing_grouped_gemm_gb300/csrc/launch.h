@@ -188,14 +188,22 @@ inline bool router_dl_dense(int score, int renorm) { return score == 0 && !renor
 // dwg and dbias (0 when one split suffices).
 int64_t router_bwd_scratch_floats(int T, int D, int E);
 
+// The expert-contiguous layout of every expert (seg_off [E + 1], tpe [E],
+// token_of_row), with no slot dropped: each (token, selected expert) has a row.
+struct RouterSegments {
+    const int *seg_off, *tpe, *token_of_row;
+};
+
 // Backward of the router from dw: dl [T, E], dbias [E] (or null), dwg [E, D]
 // and, when router_dl_dense, the router's part of dx, dx_router [T, D]
-// (fp32); otherwise dx_router is left to launch_dispatch_bwd.
+// (fp32); otherwise dx_router is left to launch_dispatch_bwd.  With segs and
+// dl zero off the selected experts, dwg and dbias are sums over each
+// expert's segment instead of a dense GEMM over all T.
 cudaError_t launch_router_bwd(const void *x, const void *wg, const float *logits,
                               const int *topk_idx, const float *topk_w, const float *dw, float *dl,
                               float *dx_router, float *dwg, float *dbias, float *scratch, int T,
                               int D, int E, int k, int score, int renorm, int is_bf16,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const RouterSegments *segs = nullptr);
 
 // bf16 tcgen05 grouped SwiGLU (both GEMMs), one CTA per tile.
 cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offsets,

@@ -592,9 +592,12 @@ MOE_EXPORT moe_status moe_layer_backward_ex(const moe_config *cfg, const void *x
                                            flags, s, wgrad_dtype == MOE_BF16);
         if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: grouped SwiGLU backward");
     }
+    // the contiguous layout drops no slot: the router's weight gradient can
+    // follow the expert segments
+    const moe::RouterSegments segs{L.seg_off, L.tpe, L.token_of_row};
     e = moe::launch_router_bwd(x, wg, W.logits, L.topk_idx, L.topk_w, W.dw, W.dl, W.dxr, dwg, dbias,
                                W.rsplit, cfg->T, cfg->D, cfg->E, cfg->k, cfg->score, cfg->renorm, 1,
-                               s);
+                               s, cfg->layout == MOE_LAYOUT_CONTIGUOUS ? &segs : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: router backward");
     // the router's part of dx: a GEMM where dl is dense, else folded in here
     const bool dense = moe::router_dl_dense(cfg->score, cfg->renorm);
