@@ -20,7 +20,10 @@ namespace {
 // Slots handled together: their loads are issued before any of them is
 // used, so a warp keeps BW_SLOTS row reads in flight.
 constexpr int BW_SLOTS = 8;
-constexpr int DB_SLOTS = 4;  // the dispatch backward also holds wg rows: fewer registers
+#ifndef MOE_DB_SLOTS
+#define MOE_DB_SLOTS 4
+#endif
+constexpr int DB_SLOTS = MOE_DB_SLOTS;  // the dispatch backward also holds wg rows: fewer registers
 
 __device__ __forceinline__ void load4(const void *p, size_t i, bool bf16, float (&g)[4]) {
     if (bf16) {
