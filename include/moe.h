@@ -236,10 +236,12 @@ int64_t moe_layer_host_workspace_size(const moe_config *cfg);
  * moe_layer_forward with the activations in HOST memory: x_host [T, D] and
  * out_host [T, D] (dtype, row-major) are host pointers; the router and
  * expert weights stay device pointers.  On `stream`, the call copies x_host
- * into device staging carved from ws, runs steps 1-5, and copies the
- * output back to out_host (one cudaMemcpyAsync each way).  out_host holds
- * the result once `stream` has completed.  Page-locked host buffers let the
- * copies run asynchronously; pageable ones work but the copies then
+ * into device staging carved from ws (one cudaMemcpyAsync) and runs steps
+ * 1-5.  When out_host is page-locked memory mapped into the device's
+ * address space, the combine writes the output there directly; otherwise it
+ * writes device staging that one cudaMemcpyAsync copies back.  out_host
+ * holds the result once `stream` has completed.  Page-locked host buffers
+ * let the copies run asynchronously; pageable ones work but the copies then
  * synchronise with the host.  ws_bytes >= moe_layer_host_workspace_size(cfg).
  */
 moe_status moe_layer_forward_host(const moe_config *cfg, const void *x_host, const void *wg,

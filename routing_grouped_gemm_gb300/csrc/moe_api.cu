@@ -501,9 +501,27 @@ MOE_EXPORT moe_status moe_layer_forward_host(const moe_config *cfg, const void *
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemcpyAsync(x_dev, x_host, (size_t)act_bytes(cfg), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_layer_forward_host: copy in");
-    if ((st = moe_layer_forward(cfg, x_dev, wg, bias, w1, w3, w2, out_dev, ws, (size_t)lws, stream)) !=
-        MOE_OK)
+    // A page-locked out_host mapped into the device's address space takes the
+    // combine's stores directly: the write-back over the host link then runs
+    // under the combine's reads of y_perm instead of after them.  Otherwise
+    // the output is staged on the device and copied back.
+    void *out_target = out_dev;
+    bool direct = false;
+    const char *dsel = getenv("MOE_HOST_DIRECT");
+    cudaPointerAttributes pa{};
+    if (!(dsel && strcmp(dsel, "0") == 0)) {
+        if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer && aligned(pa.devicePointer, 16)) {
+            out_target = pa.devicePointer;
+            direct = true;
+        } else {
+            cudaGetLastError();
+        }
+    }
+    if ((st = moe_layer_forward(cfg, x_dev, wg, bias, w1, w3, w2, out_target, ws, (size_t)lws,
+                                stream)) != MOE_OK)
         return st;
+    if (direct) return MOE_OK;
     e = cudaMemcpyAsync(out_host, out_dev, (size_t)act_bytes(cfg), cudaMemcpyDeviceToHost, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_host: copy out");
 }

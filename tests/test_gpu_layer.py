@@ -165,10 +165,12 @@ def test_layer_group_limited_routing(moe):
     assert max(len(set(row // (w.E // w.n_group))) for row in idx) <= w.topk_group
 
 
-def test_layer_forward_host_buffers(moe):
-    """The host-buffer entry point copies x in and out around the same layer:
-    bit-identical to moe_layer_forward, also on a second call that reuses
-    the workspace with another input."""
+@pytest.mark.parametrize("pinned_out", [True, False])
+def test_layer_forward_host_buffers(moe, pinned_out):
+    """The host-buffer entry point around the same layer: bit-identical to
+    moe_layer_forward, also on a second call that reuses the workspace with
+    another input -- with a page-locked out_host (the combine writes it
+    directly) and a pageable one (staged and copied back)."""
     w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=700, D=512, H=384)
     cfg = cfg_for(moe, w)
     hws = moe.alloc_workspace(cfg, host=True)
@@ -176,7 +178,9 @@ def test_layer_forward_host_buffers(moe):
         inp = moe_inputs.make_inputs(w, device="cuda", seed=seed)
         ref, _, _ = run_layer(moe, cfg, inp)
         x_host = inp.x.cpu().pin_memory()
-        out_host = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16).pin_memory()
+        out_host = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16)
+        if pinned_out:
+            out_host = out_host.pin_memory()
         moe.moe_layer_forward_host(cfg, x_host, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out_host,
                                    hws)
         torch.cuda.synchronize()
