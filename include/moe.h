@@ -399,7 +399,7 @@ moe_status moe_layer_forward_fused(const moe_config *cfg, const void *x, const v
  * tensors, or latency-critical loops where an allocation's implicit device
  * synchronisation is not acceptable.  This call does the same work as
  * moe_permute (same arguments and outputs, same bit-exact results) but keeps
- * its scratch in a fixed 1 MiB device array inside the library, which every
+ * its scratch in a fixed device array of about 1 MiB inside the library, which every
  * GPU that loads the library holds until the process exits.  It allocates
  * nothing.
  *   Limit: 2 * ceil(T / 256) * E <= 262144 (e.g. T = 16384 with E <= 2048);
@@ -410,8 +410,10 @@ moe_status moe_layer_forward_fused(const moe_config *cfg, const void *x, const v
  *   The first call on each device looks up the array's device address
  *     (with that device current); make that first call before any stream
  *     capture.
- *   Every call shares the one array and leaves its contents behind; nothing
- *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *   Every call shares the one array and leaves its contents behind; the
+ *     one word that must be zero between calls (a completion ticket) starts
+ *     at zero when the library loads and every call returns it to zero.
+ *     Calls whose kernels overlap on the GPU
  *     (other streams, other host threads) race on it: order them on one
  *     stream.
  */

@@ -11,10 +11,12 @@
 // every GPU that loads the library.
 //
 // The scratch holds the per-block expert counts and per-block row bases of
-// the counting sort (2 * ceil(T / 256) * E int32).  Nothing in it has to
-// start at zero: the count kernel writes every count and the scan kernel
-// writes every base before they are read.  The array keeps whatever the
-// last call left in it.  All calls share it, so two calls whose kernels
+// the counting sort (2 * ceil(T / 256) * E int32, plus per-warp masks for
+// small count matrices) after a 64-int head whose first word is the count
+// kernel's completion ticket.  The ticket must start at zero, which a
+// __device__ array does at module load, and every call leaves it at zero;
+// everything else is written before it is read.  The array keeps whatever
+// the last call left in it.  All calls share it, so two calls whose kernels
 // overlap on the GPU (different streams, or different host threads without
 // ordering) race on it and produce wrong permutations; issue them in order
 // on one stream, or use moe_permute with separate workspaces instead.
@@ -31,10 +33,10 @@
 
 namespace {
 
-// Fixed scratch: 1 MiB of int32.  Holds 2 * ceil(T / 256) * E entries, so
-// for example T = 16384 tokens with E <= 2048 experts, or T = 131072 tokens
-// with E <= 256 experts.
-constexpr size_t kNoAllocScratchInts = (1u << 20) / sizeof(int);
+// Fixed scratch: the 64-int head and 1 MiB of int32.  Holds 2 * ceil(T / 256)
+// * E entries, so for example T = 16384 tokens with E <= 2048 experts, or
+// T = 131072 tokens with E <= 256 experts.
+constexpr size_t kNoAllocScratchInts = 64 + (1u << 20) / sizeof(int);
 static __device__ __align__(256) int g_noalloc_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
@@ -77,8 +79,8 @@ MOE_EXPORT moe_status moe_permute_noalloc(const moe_config *cfg, const void *x,
     if (need > (int64_t)kNoAllocScratchInts) {
         char msg[200];
         snprintf(msg, sizeof msg,
-                 "moe_permute_noalloc: 2*ceil(T/256)*E = %lld ints exceeds the fixed scratch of "
-                 "%lld ints; use moe_permute with a workspace",
+                 "moe_permute_noalloc: the counting sort needs %lld ints, more than the fixed "
+                 "scratch of %lld ints; use moe_permute with a workspace",
                  (long long)need, (long long)kNoAllocScratchInts);
         fail(msg);
         return MOE_ERR_UNSUPPORTED;

@@ -21,6 +21,15 @@
 //   scan  : one CTA computes tokens_per_expert, the padded segment offsets,
 //           each block's first row per local expert and the padding rows
 //   copy  : one warp per token reads x[t] once and writes its k copies
+//
+// For count matrices up to CS_MAX_CELLS the same counting sort runs in two
+// launches instead of three:
+//   count+scan : each block stores its per-warp masks with the rows of
+//                earlier warps of the block; the last block to finish
+//                (a self-resetting ticket, no waiting) derives the totals,
+//                the padded offsets and each block's first row per expert
+//   index+copy : one warp per token ranks its k slots from those tables and
+//                copies x[t] to the rows it found
 #include <algorithm>
 
 #include "common.cuh"
@@ -318,6 +327,187 @@ permute_index_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
     }
 }
 
+// ---------------------------------------------------------------------
+// two-launch form: count+scan, then index+copy
+// ---------------------------------------------------------------------
+constexpr int CS_MAX_CELLS = 8192;  // nblk * E staged in the last block's shared memory
+
+// Each block: masks of its 8 warps per expert -> wmeta[(8b + w) E + e] =
+// (mask, rows of e in warps 0..w-1 of the block) and blk_cnt[b E + e].  The
+// last block to finish stages blk_cnt in shared memory and writes
+// tokens_per_expert, seg_offsets, blk_base[b E_local + i] (the absolute
+// first row of block b in local expert i), the padding entries of
+// token_of_row and the masked-capacity flag.
+__global__ void __launch_bounds__(PB_TOKENS)
+permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int e_first,
+                          int E_local, int layout, int align_m, int capacity, long long rows_alloc,
+                          int *__restrict__ blk_cnt, int2 *__restrict__ wmeta,
+                          int *__restrict__ blk_base, unsigned *__restrict__ ticket,
+                          int *__restrict__ tokens_per_expert, int *__restrict__ seg_offsets,
+                          int *__restrict__ token_of_row, int *status) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t *s_mask = s_dyn;  // [PB_WARPS][E]
+    __shared__ int s_last;
+    __shared__ int s_warp_sum[PB_WARPS];
+    const int tid = threadIdx.x, b = blockIdx.x, nblk = gridDim.x;
+
+    build_masks(topk_idx, T, k, E, s_mask, status);
+    __syncthreads();
+    for (int e = tid; e < E; e += PB_TOKENS) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < PB_WARPS; ++w) {
+            const uint32_t m = s_mask[w * E + e];
+            wmeta[((size_t)b * PB_WARPS + w) * E + e] = make_int2((int)m, run);
+            run += __popc(m);
+        }
+        blk_cnt[(size_t)b * E + e] = run;
+    }
+    __threadfence();  // this block's counts are visible before its ticket
+    __syncthreads();
+    if (tid == 0) s_last = atomicInc(ticket, (unsigned)(nblk - 1)) == (unsigned)(nblk - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    int *s_cnt = reinterpret_cast<int *>(s_mask + PB_WARPS * E);  // [nblk][E]
+    int *s_tot = s_cnt + (size_t)nblk * E;                           // [E]
+    int *s_off = s_tot + E;                                          // [E_local + 1]
+    for (int c = tid; c < nblk * E; c += PB_TOKENS) s_cnt[c] = __ldcg(blk_cnt + c);
+    __syncthreads();
+    for (int e = tid; e < E; e += PB_TOKENS) {
+        int tot = 0;
+        for (int bb = 0; bb < nblk; ++bb) tot += s_cnt[bb * E + e];
+        s_tot[e] = tot;
+        tokens_per_expert[e] = tot;
+    }
+    __syncthreads();
+    // padded sizes of the local segments -> exclusive scan (thread chunks)
+    const int per = (E_local + PB_TOKENS - 1) / PB_TOKENS;
+    const int lo = tid * per, hi = min(E_local, lo + per);
+    int run = 0;
+    for (int i = lo; i < hi; ++i) {
+        const int c = s_tot[e_first + i];
+        int size;
+        if (layout == 1) {
+            size = capacity;
+            if (c > capacity) raise_flag(status, FLAG_CAPACITY);
+        } else {
+            size = (c + align_m - 1) / align_m * align_m;
+        }
+        s_off[i] = size;  // temporarily the size
+        run += size;
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp_sum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_warp_sum[w];
+    int acc = base + incl - run;
+    for (int i = lo; i < hi; ++i) {
+        const int size = s_off[i];
+        s_off[i] = acc;
+        acc += size;
+    }
+    if (tid == PB_TOKENS - 1) s_off[E_local] = acc;
+    __syncthreads();
+    for (int i = tid; i <= E_local; i += PB_TOKENS) seg_offsets[i] = s_off[i];
+    for (int i = tid; i < E_local; i += PB_TOKENS) {
+        const int e = e_first + i;
+        int row = s_off[i];
+        for (int bb = 0; bb < nblk; ++bb) {
+            blk_base[(size_t)bb * E_local + i] = row;
+            row += s_cnt[bb * E + e];
+        }
+    }
+    // padding rows of each local segment (a warp per segment), then the rows
+    // after the last segment
+    for (int i = warp; i < E_local; i += PB_WARPS) {
+        const int used = min(s_tot[e_first + i], s_off[i + 1] - s_off[i]);
+        for (int r = s_off[i] + used + lane; r < s_off[i + 1]; r += 32) token_of_row[r] = -1;
+    }
+    for (long long r = (long long)s_off[E_local] + tid; r < rows_alloc; r += PB_TOKENS)
+        token_of_row[r] = -1;
+}
+
+// One warp per token.  Lane j < k ranks slot j: the slot is active when its
+// expert id is in [0, E) and no earlier slot of the token names it; a local
+// expert i gets row blk_base[b][i] + (rows of the expert in earlier warps of
+// the block) + popc(mask & lanes below), or -1 past the segment's end (the
+// masked layout's capacity, flagged by the count kernel).  Then x[t] is read
+// once in 16-byte vectors and written to every row found.
+constexpr int IC_UNROLL = 8;
+
+__global__ void __launch_bounds__(256)
+permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ topk_idx,
+                          const int2 *__restrict__ wmeta, const int *__restrict__ blk_base,
+                          const int *__restrict__ seg_offsets, int *__restrict__ row_of,
+                          int *__restrict__ token_of_row, uint4 *__restrict__ x_perm, int T, int k,
+                          int E, int e_first, int E_local, int vpr, float4 *__restrict__ zero_out,
+                          int zvpr) {
+    griddep_launch_dependents();  // the next kernel may be scheduled now
+    griddep_wait();               // every input of this kernel is complete
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int e = lane < k ? topk_idx[(size_t)t * k + lane] : -1;
+    const uint4 *src = x + (size_t)t * vpr;
+    uint4 buf[IC_UNROLL];
+#pragma unroll
+    for (int u = 0; u < IC_UNROLL; ++u) {  // the first chunk of x[t] is in flight meanwhile
+        const int v = u * 32 + lane;
+        if (v < vpr) buf[u] = __ldcs(src + v);
+    }
+    bool act = lane < k && e >= 0 && e < E;
+    for (int q = 0; q < k; ++q) {
+        const int o = __shfl_sync(0xffffffffu, e, q);
+        if (q < lane && o == e) act = false;
+    }
+    const int i = e - e_first;
+    int my_row = -1;
+    if (act && i >= 0 && i < E_local) {
+        const int2 m = wmeta[(size_t)(t >> 5) * E + e];
+        const int cand = blk_base[(size_t)(t / PB_TOKENS) * E_local + i] + m.y +
+                         __popc((uint32_t)m.x & ((1u << (t & 31)) - 1u));
+        if (cand < seg_offsets[i + 1]) {
+            my_row = cand;
+            token_of_row[cand] = t;
+        }
+    }
+    if (lane < k) row_of[(size_t)t * k + lane] = my_row;
+    if (zero_out) {  // the fused combine's accumulator row of this token starts at zero
+        float4 *z = zero_out + (size_t)t * zvpr;
+        for (int v = lane; v < zvpr; v += 32) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int v0 = 0;;) {
+        for (int j = 0; j < k; ++j) {
+            const int r = __shfl_sync(0xffffffffu, my_row, j);
+            if (r < 0) continue;
+            uint4 *dst = x_perm + (size_t)r * vpr;
+#pragma unroll
+            for (int u = 0; u < IC_UNROLL; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < vpr) dst[v] = buf[u];
+            }
+        }
+        v0 += 32 * IC_UNROLL;
+        if (v0 >= vpr) break;
+#pragma unroll
+        for (int u = 0; u < IC_UNROLL; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < vpr) buf[u] = __ldcs(src + v);
+        }
+    }
+}
+
 // One warp per token: read x[t] once in 16-byte vectors, write k copies.
 constexpr int CP_UNROLL = 4;
 
@@ -453,9 +643,14 @@ combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
 
 }  // namespace
 
+// Scratch: [0, 64) the count+scan kernel's ticket (zero between calls),
+// then blk_cnt [nblk][E], blk_base [nblk][E], and for the two-launch form
+// (nblk E <= CS_MAX_CELLS) wmeta [8 nblk][E] of int2.
+constexpr int64_t SCR_HEAD = 64;
+
 int64_t permute_scratch_ints(int T, int E) {
-    const int64_t nblk = (T + PB_TOKENS - 1) / PB_TOKENS;
-    return 2 * nblk * (int64_t)E;
+    const int64_t cells = (T + PB_TOKENS - 1) / PB_TOKENS * (int64_t)E;
+    return SCR_HEAD + 2 * cells + (cells <= CS_MAX_CELLS ? 2 * PB_WARPS * cells : 0);
 }
 
 cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_expert,
@@ -465,10 +660,34 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                            int *scratch, int *status, cudaStream_t stream, float *x_scale,
                            float *zero_out) {
     const int nblk = (T + PB_TOKENS - 1) / PB_TOKENS;
-    int *blk_cnt = scratch;
-    int *blk_base = scratch + (size_t)nblk * E;
+    unsigned *ticket = reinterpret_cast<unsigned *>(scratch);
+    int *blk_cnt = scratch + SCR_HEAD;
+    int *blk_base = blk_cnt + (size_t)nblk * E;
+    int2 *wmeta = reinterpret_cast<int2 *>(blk_base + (size_t)nblk * E);
     const size_t mask_smem = sizeof(uint32_t) * PB_WARPS * (size_t)E;
     cudaError_t err;
+    if (nblk > 0 && (int64_t)nblk * E <= CS_MAX_CELLS && !x_scale) {
+        const size_t smem =
+            mask_smem + sizeof(int) * ((size_t)nblk * E + E + E_local + 1);
+        err = ensure_smem((const void *)permute_count_scan_kernel, smem);
+        if (err != cudaSuccess) return err;
+        if ((err = launch_pdl(permute_count_scan_kernel, dim3(nblk), dim3(PB_TOKENS), smem, stream,
+                              topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity,
+                              (long long)rows_alloc, blk_cnt, wmeta, blk_base, ticket,
+                              tokens_per_expert, seg_offsets, token_of_row, status)) != cudaSuccess)
+            return err;
+        count_launch();
+        const int warps_per_block = 8;
+        const int blocks = (T + warps_per_block - 1) / warps_per_block;
+        if ((err = launch_pdl(permute_index_copy_kernel, dim3(blocks), dim3(32 * warps_per_block), 0,
+                              stream, (const uint4 *)x, topk_idx, (const int2 *)wmeta,
+                              (const int *)blk_base, (const int *)seg_offsets, row_of, token_of_row,
+                              (uint4 *)x_perm, T, k, E, e_first, E_local, D * elem_bytes / 16,
+                              (float4 *)zero_out, D / 4)) != cudaSuccess)
+            return err;
+        count_launch();
+        return cudaGetLastError();
+    }
     if (nblk > 0) {
         err = ensure_smem((const void *)permute_count_kernel, mask_smem);
         if (err != cudaSuccess) return err;

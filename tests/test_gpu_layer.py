@@ -198,16 +198,16 @@ def test_layer_k32_many_experts(moe):
 
 def test_layer_launch_count(moe):
     # bf16, E <= 256: router logits on the tensor cores with the top-k in the
-    # same cluster launch (1), count + fused scan/index (2; 4 blocks x 64
-    # experts fit the fused scan), row copy (1), GEMM1 and GEMM2 in one
-    # pair-kernel launch (1), combine (1)
+    # same cluster launch (1), count with the scan in its last block (1;
+    # 4 blocks x 64 experts fit it), ranks with the row copy (1), GEMM1 and
+    # GEMM2 in one pair-kernel launch (1), combine (1)
     w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=1024, D=512, H=256)
     inp = moe_inputs.make_inputs(w, device="cuda", seed=9)
     cfg = cfg_for(moe, w)
     run_layer(moe, cfg, inp)
     before = moe.kernel_launches()
     run_layer(moe, cfg, inp)
-    assert moe.kernel_launches() - before == 6
+    assert moe.kernel_launches() - before == 5
 
 
 # ------------------------------------------------------------------ full sizes

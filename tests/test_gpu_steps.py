@@ -198,10 +198,10 @@ def test_route_nan_logit_sets_status(moe):
 
 # ------------------------------------------------------------------ permute
 
-def _run_permute(moe, cfg, x, idx):
+def _run_permute(moe, cfg, x, idx, ws=None):
     ra = moe.rows_alloc(cfg)
     el = cfg.e_local
-    ws = moe.alloc_workspace(cfg)
+    ws = moe.alloc_workspace(cfg) if ws is None else ws
     tpe = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
     seg = torch.empty(el + 1, dtype=torch.int32, device="cuda")
     row_of = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
@@ -219,6 +219,7 @@ def _run_permute(moe, cfg, x, idx):
     (2000, 32, 8, 8, 8, 12, 0.8),        # expert range, small alignment
     (513, 256, 8, 128, 0, 256, 0.3),
     (700, 5, 1, 16, 2, 2, 0.0),          # k = 1
+    (32768, 64, 8, 128, 0, 64, 0.5),     # 128 x 64 counts: the largest two-launch case
     (20000, 256, 8, 128, 0, 256, 0.3),   # count matrix above the fused-scan limit
     (3000, 1024, 32, 128, 0, 1024, 0.5),  # the largest E and k the ABI accepts
     (70000, 64, 8, 128, 0, 64, 1.0),     # T above 2^16, R = 560000 rows
@@ -242,6 +243,23 @@ def test_permute_bitexact(moe, T, E, k, align, e_first, E_local, skew, dt):
     xh = moe_inputs.host_array(x)
     ref = oracle.permute_rows(xh, lay["token_of_row"])
     assert np.array_equal(moe_inputs.host_array(xp)[filled], ref[filled])   # bit for bit
+
+
+def test_permute_workspace_reuse(moe):
+    """Back-to-back permutes on one workspace: the count kernel's completion
+    ticket returns to zero after every call, so each call's layout is exact."""
+    T, E, k, D = 3000, 64, 6, 64
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16)
+    ws = moe.alloc_workspace(cfg)
+    x = torch.randn(T, D, device="cuda").to(torch.bfloat16)
+    for seed, skew in ((1, 0.0), (2, 1.2), (3, 0.4)):
+        idx = moe_inputs.random_topk_idx(T, E, k, seed=seed, skew=skew)
+        st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx, ws)
+        assert st == moe.MOE_OK
+        lay = oracle.layout(idx, E, 0, E, oracle.CONTIGUOUS, 128)
+        assert np.array_equal(seg, lay["seg_offsets"])
+        assert np.array_equal(row_of, lay["row_of"])
+        assert np.array_equal(tor, lay["token_of_row"])
 
 
 def test_permute_masked_and_capacity(moe):
