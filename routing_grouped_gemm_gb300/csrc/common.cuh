@@ -56,16 +56,6 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// Order of the router's selection key: larger value first, equal values by
-// lower expert index, NaN after every number (two NaNs by index).
-__device__ __forceinline__ bool key_before(float a, int ia, float b, int ib) {
-    const bool na = a != a, nb = b != b;
-    if (na || nb) return (na && nb) ? (ia < ib) : nb;
-    if (a > b) return true;
-    if (a < b) return false;
-    return ia < ib;
-}
-
 // ---------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------
@@ -134,6 +124,14 @@ __device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
 
 // Orders this thread's generic-proxy global accesses with its async-proxy
 // (TMA) accesses, in both directions.
+// fence.acq_rel at GPU scope.  After a bar.sync it also orders the block's
+// earlier writes (release); after a relaxed atomic it gives that read
+// acquire semantics for the thread's later reads and, through a following
+// bar.sync, for the block's.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }

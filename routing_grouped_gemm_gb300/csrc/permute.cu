@@ -28,11 +28,13 @@
 //                earlier warps of the block; the last block to finish
 //                (a self-resetting ticket, no waiting) derives the totals,
 //                the padded offsets and each block's first row per expert
-//   index+copy : one warp per token ranks its k slots from those tables and
-//                copies x[t] to the rows it found
+//   index+copy : one warp per token ranks its k slots from those tables,
+//                copies x[t] to the rows it found and writes a share of the
+//                padding entries of token_of_row
 #include <algorithm>
 
 #include "common.cuh"
+#include "e4m3_row.cuh"
 #include "launch.h"
 
 namespace moe {
@@ -365,12 +367,17 @@ permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
         }
         blk_cnt[(size_t)b * E + e] = run;
     }
-    __threadfence();  // this block's counts are visible before its ticket
+    // the block's counts (ordered before thread 0 by the barrier) are
+    // released with its ticket; the last block acquires all of them
     __syncthreads();
-    if (tid == 0) s_last = atomicInc(ticket, (unsigned)(nblk - 1)) == (unsigned)(nblk - 1);
+    if (tid == 0) {
+        fence_acq_rel_gpu();
+        const bool last = atomicInc(ticket, (unsigned)(nblk - 1)) == (unsigned)(nblk - 1);
+        if (last) fence_acq_rel_gpu();
+        s_last = last;
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
 
     int *s_cnt = reinterpret_cast<int *>(s_mask + PB_WARPS * E);  // [nblk][E]
     int *s_tot = s_cnt + (size_t)nblk * E;                           // [E]
@@ -428,14 +435,8 @@ permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
             row += s_cnt[bb * E + e];
         }
     }
-    // padding rows of each local segment (a warp per segment), then the rows
-    // after the last segment
-    for (int i = warp; i < E_local; i += PB_WARPS) {
-        const int used = min(s_tot[e_first + i], s_off[i + 1] - s_off[i]);
-        for (int r = s_off[i] + used + lane; r < s_off[i + 1]; r += 32) token_of_row[r] = -1;
-    }
-    for (long long r = (long long)s_off[E_local] + tid; r < rows_alloc; r += PB_TOKENS)
-        token_of_row[r] = -1;
+    // the padding entries of token_of_row are written by the index+copy
+    // kernel, spread over its warps
 }
 
 // One warp per token.  Lane j < k ranks slot j: the slot is active when its
@@ -443,16 +444,22 @@ permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
 // expert i gets row blk_base[b][i] + (rows of the expert in earlier warps of
 // the block) + popc(mask & lanes below), or -1 past the segment's end (the
 // masked layout's capacity, flagged by the count kernel).  Then x[t] is read
-// once in 16-byte vectors and written to every row found.
+// once in 16-byte vectors and written to every row found -- or, for the FP8
+// dispatch (kFp8), quantised to e4m3 once with one scale per row and the
+// codes and scale written to every row found.  Warp t also writes -1 into
+// token_of_row for the padding rows of local segments i = t, t + T, ... and
+// for its 32-row share of the rows after the last segment.
 constexpr int IC_UNROLL = 8;
 
+template <bool kFp8>
 __global__ void __launch_bounds__(256)
 permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ topk_idx,
                           const int2 *__restrict__ wmeta, const int *__restrict__ blk_base,
                           const int *__restrict__ seg_offsets, int *__restrict__ row_of,
                           int *__restrict__ token_of_row, uint4 *__restrict__ x_perm, int T, int k,
                           int E, int e_first, int E_local, int vpr, float4 *__restrict__ zero_out,
-                          int zvpr) {
+                          int zvpr, const int *__restrict__ tokens_per_expert,
+                          long long rows_alloc, int cols, float *__restrict__ x_scale) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -461,10 +468,12 @@ permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ t
     const int e = lane < k ? topk_idx[(size_t)t * k + lane] : -1;
     const uint4 *src = x + (size_t)t * vpr;
     uint4 buf[IC_UNROLL];
+    if (!kFp8) {
 #pragma unroll
-    for (int u = 0; u < IC_UNROLL; ++u) {  // the first chunk of x[t] is in flight meanwhile
-        const int v = u * 32 + lane;
-        if (v < vpr) buf[u] = __ldcs(src + v);
+        for (int u = 0; u < IC_UNROLL; ++u) {  // the first chunk of x[t] is in flight meanwhile
+            const int v = u * 32 + lane;
+            if (v < vpr) buf[u] = __ldcs(src + v);
+        }
     }
     bool act = lane < k && e >= 0 && e < E;
     for (int q = 0; q < k; ++q) {
@@ -483,6 +492,19 @@ permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ t
         }
     }
     if (lane < k) row_of[(size_t)t * k + lane] = my_row;
+    for (int s = t; s < E_local; s += T) {
+        const int lo = seg_offsets[s], hi = seg_offsets[s + 1];
+        const int used = min(tokens_per_expert[e_first + s], hi - lo);
+        for (int r = lo + used + lane; r < hi; r += 32) token_of_row[r] = -1;
+    }
+    for (long long r = (long long)seg_offsets[E_local] + (long long)t * 32 + lane; r < rows_alloc;
+         r += (long long)T * 32)
+        token_of_row[r] = -1;
+    if (kFp8) {
+        quantize_row_e4m3_warp(src, cols, my_row, k, reinterpret_cast<uint8_t *>(x_perm), x_scale,
+                               lane);
+        return;
+    }
     if (zero_out) {  // the fused combine's accumulator row of this token starts at zero
         float4 *z = zero_out + (size_t)t * zvpr;
         for (int v = lane; v < zvpr; v += 32) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -666,7 +688,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     int2 *wmeta = reinterpret_cast<int2 *>(blk_base + (size_t)nblk * E);
     const size_t mask_smem = sizeof(uint32_t) * PB_WARPS * (size_t)E;
     cudaError_t err;
-    if (nblk > 0 && (int64_t)nblk * E <= CS_MAX_CELLS && !x_scale) {
+    if (nblk > 0 && (int64_t)nblk * E <= CS_MAX_CELLS) {
         const size_t smem =
             mask_smem + sizeof(int) * ((size_t)nblk * E + E + E_local + 1);
         err = ensure_smem((const void *)permute_count_scan_kernel, smem);
@@ -679,11 +701,15 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         count_launch();
         const int warps_per_block = 8;
         const int blocks = (T + warps_per_block - 1) / warps_per_block;
-        if ((err = launch_pdl(permute_index_copy_kernel, dim3(blocks), dim3(32 * warps_per_block), 0,
-                              stream, (const uint4 *)x, topk_idx, (const int2 *)wmeta,
+        if (x_scale && (D % 8 || k > 32)) return cudaErrorInvalidValue;
+        if ((err = launch_pdl(x_scale ? permute_index_copy_kernel<true>
+                                      : permute_index_copy_kernel<false>,
+                              dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+                              (const uint4 *)x, topk_idx, (const int2 *)wmeta,
                               (const int *)blk_base, (const int *)seg_offsets, row_of, token_of_row,
                               (uint4 *)x_perm, T, k, E, e_first, E_local, D * elem_bytes / 16,
-                              (float4 *)zero_out, D / 4)) != cudaSuccess)
+                              (float4 *)zero_out, D / 4, (const int *)tokens_per_expert,
+                              (long long)rows_alloc, D, x_scale)) != cudaSuccess)
             return err;
         count_launch();
         return cudaGetLastError();

@@ -41,11 +41,12 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 }
 
 // Top-k of one token's E keys (in shared memory) by one warp: k rounds of a
-// warp-wide arg-max in the selection order of key_before (larger key first,
-// equal keys by lower expert index, NaN last), then the routing weights:
-// softmax over all E (or sigmoid) of the chosen keys, divided by their sum
-// when renormalising.  Lane i owns experts i, i+32, ... (E <= 1024); the
-// winner of round j is kept by lane j, which computes and writes slot j.
+// warp-wide arg-max in selection order (larger key first, equal keys by
+// lower expert index, NaN after every number, -0 equal to +0), then the
+// routing weights: softmax over all E (or sigmoid) of the chosen keys,
+// divided by their sum when renormalising.  Lane i owns experts i, i+32, ...
+// (E <= 1024); the winner of round j is kept by lane j, which computes and
+// writes slot j.
 //
 // Group-limited routing (n_group > 1; page "Expert Parallelism (EP)",
 // section 3): first each of the n_group groups of E/n_group consecutive
@@ -53,82 +54,118 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 // (added in selection order), the topk_group best groups are kept (ties to
 // the lower group, NaN last), and the k rounds only consider their experts.
 
-// Warp-wide arg-max in selection order; every lane ends with the winner.
-__device__ __forceinline__ void warp_argmax(float &bv, int &be) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe >= 0 && (be < 0 || key_before(ov, oe, bv, be))) { bv = ov; be = oe; }
-    }
+// The selection order as one unsigned 64-bit number, larger = chosen first.
+// High word: the key's binary32 bits mapped order-preservingly onto unsigned
+// integers (negative values bit-inverted, the sign bit set on the others),
+// with -0 folded onto +0 and NaN mapped to 0, below every number.  Low word:
+// ~e, so that of two equal keys the lower expert index is larger.  0 means
+// "no candidate": a real candidate's low word ~e is nonzero.
+__device__ __forceinline__ uint64_t sel_key(float v, int e) {
+    uint32_t b = __float_as_uint(v);
+    b = b == 0x80000000u ? 0u : b;
+    uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    u = v != v ? 0u : u;
+    return ((uint64_t)u << 32) | (uint64_t)(~(uint32_t)e);
 }
 
-__device__ void warp_topk_weights(const float *l, int E, int k, int score, int renorm,
-                                  int n_group, int topk_group, int t,
-                                  int *__restrict__ topk_idx, float *__restrict__ topk_w,
-                                  int *status, int lane) {
+// Warp-wide maximum of the lanes' selection keys (two redux.sync steps: the
+// high words, then the low words of the lanes that hold the largest high
+// word); every lane gets the result.
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t x) {
+    const uint32_t hi = (uint32_t)(x >> 32);
+    const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? (uint32_t)x : 0u);
+    return ((uint64_t)mhi << 32) | mlo;
+}
+
+__device__ __forceinline__ int key_expert(uint64_t x) { return x ? (int)~(uint32_t)x : -1; }
+
+// KC: selection keys cached in registers per lane (E <= 32 KC); the keys are
+// formed once, and each round is a masked maximum over the cache plus the
+// warp-wide maximum.
+template <int KC>
+__device__ __forceinline__ void warp_topk_cached(const float *l, int E, int k, int score,
+                                                 int renorm, int n_group, int topk_group, int t,
+                                                 int *__restrict__ topk_idx,
+                                                 float *__restrict__ topk_w, int *status,
+                                                 int lane) {
+    uint64_t key[KC];  // key[q]: expert lane + 32 q, 0 when absent
     bool any_nan = false;
-    for (int e = lane; e < E; e += 32) any_nan |= (l[e] != l[e]);
+#pragma unroll
+    for (int q = 0; q < KC; ++q) {
+        const int e = lane + 32 * q;
+        const float v = e < E ? l[e] : 0.f;
+        any_nan |= v != v;
+        key[q] = e < E ? sel_key(v, e) : 0ull;
+    }
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) raise_flag(status, FLAG_BAD_ROUTING);
 
     const bool grouped = n_group > 1;
-    const int gsz = grouped ? E / n_group : E;
-    uint32_t allowed = 0xffffffffu;  // bit g: group g may be chosen
+    uint32_t avail = 0xffffffffu;  // bit q: expert lane + 32 q may still be chosen
     if (grouped) {
+        const int gsz = E / n_group;
         const int m = k / topk_group;
         float my_score = 0.f;  // lane g: score of group g
         for (int g = 0; g < n_group; ++g) {
             const int e0 = g * gsz;
-            uint32_t gt = 0;  // bit q: expert e0 + lane + 32 q already counted
+            uint32_t in = 0;  // bit q: expert lane + 32 q is in group g
+#pragma unroll
+            for (int q = 0; q < KC; ++q) {
+                const int e = lane + 32 * q;
+                if (e >= e0 && e < e0 + gsz) in |= 1u << q;
+            }
             float sum = 0.f;
             for (int i = 0; i < m; ++i) {
-                float bv = 0.f;
-                int be = -1;
-                for (int q = 0, e = e0 + lane; e < e0 + gsz; ++q, e += 32) {
-                    if (gt & (1u << q)) continue;
-                    if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
+                uint64_t best = 0;
+#pragma unroll
+                for (int q = 0; q < KC; ++q) {
+                    const uint64_t c = ((in >> q) & 1u) ? key[q] : 0ull;
+                    best = c > best ? c : best;
                 }
-                warp_argmax(bv, be);
-                if (be >= 0 && ((be - e0) & 31) == lane) gt |= 1u << ((be - e0) >> 5);
-                sum += bv;
+                const int be = key_expert(warp_max_key(best));
+                if (be >= 0 && (be & 31) == lane) in &= ~(1u << (be >> 5));
+                sum += be >= 0 ? l[be] : 0.f;
             }
             if (lane == g) my_score = sum;
         }
-        allowed = 0;
+        uint32_t allowed = 0;  // bit g: group g may be chosen
         for (int r = 0; r < topk_group; ++r) {
-            float bv = 0.f;
-            int be = -1;
-            if (lane < n_group && !(allowed & (1u << lane))) { bv = my_score; be = lane; }
-            warp_argmax(bv, be);
-            if (be >= 0) allowed |= 1u << be;
+            const uint64_t c =
+                (lane < n_group && !(allowed & (1u << lane))) ? sel_key(my_score, lane) : 0ull;
+            const int bg = key_expert(warp_max_key(c));
+            if (bg >= 0) allowed |= 1u << bg;
+        }
+        avail = 0;
+#pragma unroll
+        for (int q = 0; q < KC; ++q) {
+            const int e = lane + 32 * q;
+            if (e < E && ((allowed >> (e / gsz)) & 1u)) avail |= 1u << q;
         }
     }
 
-    uint32_t taken = 0;  // bit q: expert lane + 32 q already chosen
-    int my_e = -1;       // slot `lane`'s expert and key (lanes < k)
+    int my_e = -1;  // slot `lane`'s expert and key (lanes < k)
     float my_v = 0.f, top = 0.f;
     for (int j = 0; j < k; ++j) {
-        float bv = 0.f;
-        int be = -1;
-        for (int q = 0, e = lane; e < E; ++q, e += 32) {
-            if (taken & (1u << q)) continue;
-            if (grouped && !((allowed >> (e / gsz)) & 1u)) continue;
-            if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
+        uint64_t best = 0;
+#pragma unroll
+        for (int q = 0; q < KC; ++q) {
+            const uint64_t c = ((avail >> q) & 1u) ? key[q] : 0ull;
+            best = c > best ? c : best;
         }
-        warp_argmax(bv, be);
-        if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
+        const int be = key_expert(warp_max_key(best));
+        const float bv = be >= 0 ? l[be] : 0.f;
+        if (be >= 0 && (be & 31) == lane) avail &= ~(1u << (be >> 5));
         if (lane == j) { my_e = be; my_v = bv; }
         if (j == 0) top = bv;  // the largest chosen key (unless NaN)
     }
     if (grouped && score == 0 && !renorm) {
         // softmax over all E: shift by the largest key of all, which may lie
         // in a group that was not chosen
-        float bv = 0.f;
-        int be = -1;
-        for (int e = lane; e < E; e += 32)
-            if (be < 0 || key_before(l[e], e, bv, be)) { bv = l[e]; be = e; }
-        warp_argmax(bv, be);
-        top = bv;
+        uint64_t best = 0;
+#pragma unroll
+        for (int q = 0; q < KC; ++q) best = key[q] > best ? key[q] : best;
+        const int be = key_expert(warp_max_key(best));
+        top = be >= 0 ? l[be] : 0.f;
     }
 
     float p = 0.f;
@@ -150,6 +187,23 @@ __device__ void warp_topk_weights(const float *l, int E, int k, int score, int r
         topk_idx[(size_t)t * k + lane] = my_e;
         topk_w[(size_t)t * k + lane] = p / div;
     }
+}
+
+// EMAX: the largest E the calling kernel handles (256 or 1024).
+template <int EMAX>
+__device__ void warp_topk_weights(const float *l, int E, int k, int score, int renorm,
+                                  int n_group, int topk_group, int t,
+                                  int *__restrict__ topk_idx, float *__restrict__ topk_w,
+                                  int *status, int lane) {
+    if (E <= 64)
+        warp_topk_cached<2>(l, E, k, score, renorm, n_group, topk_group, t, topk_idx, topk_w,
+                            status, lane);
+    else if (EMAX <= 256 || E <= 256)
+        warp_topk_cached<8>(l, E, k, score, renorm, n_group, topk_group, t, topk_idx, topk_w,
+                            status, lane);
+    else
+        warp_topk_cached<32>(l, E, k, score, renorm, n_group, topk_group, t, topk_idx, topk_w,
+                             status, lane);
 }
 
 template <typename T>
@@ -227,8 +281,8 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
     for (int tt = warp; tt < RT_TOKENS; tt += RT_THREADS / 32) {
         const int t = t0 + tt;
         if (t >= Tn) break;
-        warp_topk_weights(s_logit + tt * E, E, k, score, renorm, n_group, topk_group, t, topk_idx,
-                          topk_w, status, lane);
+        warp_topk_weights<1024>(s_logit + tt * E, E, k, score, renorm, n_group, topk_group, t,
+                                topk_idx, topk_w, status, lane);
     }
 }
 
@@ -430,24 +484,36 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         for (int tl = tl0 + warp; tl < tl1; tl += nwarps) {
             const int t = m0 + tl;
             if (t >= p.T) break;
-            for (int e = lane; e < p.E; e += 32) {
-                const uint32_t off = (uint32_t)((tl * ld + e) * sizeof(float));
-                // all splits' loads in flight together, then the sum in split order
-                float part[kRouterMaxSplits];
+            for (int e0 = lane; e0 < p.E; e0 += 64) {
+                // the loads of two expert columns and all splits in flight
+                // together, then each sum in split order
+                float part[2][kRouterMaxSplits];
 #pragma unroll
-                for (int sidx = 0; sidx < kRouterMaxSplits; ++sidx)
-                    if (sidx < S) part[sidx] = ld_shared_cluster_f32(mapa_shared(sp_local + off, (uint32_t)sidx));
-                float v = 0.f;
+                for (int u = 0; u < 2; ++u) {
+                    const int e = e0 + 32 * u;
+                    const uint32_t off = (uint32_t)((tl * ld + e) * sizeof(float));
 #pragma unroll
-                for (int sidx = 0; sidx < kRouterMaxSplits; ++sidx)
-                    if (sidx < S) v += part[sidx];
-                if (p.bias) v += p.bias[e];
-                key[e] = v;
-                if (p.logits_out) p.logits_out[(size_t)t * p.E + e] = v;
+                    for (int sidx = 0; sidx < kRouterMaxSplits; ++sidx)
+                        if (sidx < S && e < p.E)
+                            part[u][sidx] = ld_shared_cluster_f32(mapa_shared(sp_local + off, (uint32_t)sidx));
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int e = e0 + 32 * u;
+                    if (e >= p.E) break;
+                    float v = 0.f;
+#pragma unroll
+                    for (int sidx = 0; sidx < kRouterMaxSplits; ++sidx)
+                        if (sidx < S) v += part[u][sidx];
+                    if (p.bias) v += p.bias[e];
+                    key[e] = v;
+                    if (p.logits_out) p.logits_out[(size_t)t * p.E + e] = v;
+                }
             }
             __syncwarp();
-            warp_topk_weights(key, p.E, p.k, p.score, p.renorm, p.n_group, p.topk_group, t,
-                              p.topk_idx, p.topk_w, p.status, lane);
+            warp_topk_weights<kRouterTcMaxE>(key, p.E, p.k, p.score, p.renorm, p.n_group,
+                                             p.topk_group, t, p.topk_idx, p.topk_w, p.status,
+                                             lane);
             __syncwarp();
         }
         cluster_sync();  // the peers are done reading this CTA's partial
@@ -488,8 +554,8 @@ router_reduce_topk_kernel(const float *__restrict__ part, int splits, const floa
         const float *l = s_key + tt * ld;
         if (logits_out)
             for (int e = lane; e < E; e += 32) logits_out[(size_t)tok * E + e] = l[e];
-        warp_topk_weights(l, E, k, score, renorm, n_group, topk_group, tok, topk_idx, topk_w, status,
-                          lane);
+        warp_topk_weights<kRouterTcMaxE>(l, E, k, score, renorm, n_group, topk_group, tok,
+                                         topk_idx, topk_w, status, lane);
     }
 }
 

@@ -179,6 +179,39 @@ def test_route_largest_E_and_k_bitexact(moe, dt):
         np.testing.assert_allclose(gw.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("n_group,topk_group", [(0, 0), (4, 2)])
+def test_route_special_keys_order(moe, dt, n_group, topk_group):
+    """+inf, -inf and NaN keys in one token: the selection takes +inf first,
+    -inf after every finite key and NaN last, equal keys by lower index --
+    the same as the oracle's top-k on the GPU's own logits."""
+    T, D, E, k = 96, 64, 32, 10
+    rng = np.random.default_rng(5)
+    x = rng.integers(-3, 4, size=(T, D)).astype(np.float32)
+    wg = rng.integers(-2, 3, size=(E, D)).astype(np.float32)
+    # where x[t, 0] = inf: per 8 experts one +inf, one -inf and six NaN keys,
+    # so the 10 slots take 4 x +inf, 4 x -inf and the 2 lowest NaN experts
+    wg[:, 0] = np.tile([1.0, 0.0, -1.0, 0.0, 0.0, 0.0, 0.0, 0.0], E // 8)
+    x[::3, 0] = np.inf                                    # a third of the tokens
+    x[1::6, 0] = -np.inf                                  # and a sixth with -inf
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k,
+                     dtype=moe.MOE_F32 if dt == "f32" else moe.MOE_BF16,
+                     score=moe.MOE_SCORE_SIGMOID, renorm=1, n_group=n_group,
+                     topk_group=topk_group)
+    ws = moe.alloc_workspace(cfg)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    gidx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(cfg, _dev(x, tdt), _dev(wg, tdt), None, logits, gidx, gw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
+    keys = logits.cpu().numpy()
+    assert np.isnan(keys).any() and np.isposinf(keys).any() and np.isneginf(keys).any()
+    oidx, st = oracle.topk(keys, k, n_group, topk_group)
+    assert st == oracle.BAD_ROUTING
+    assert np.array_equal(gidx.cpu().numpy(), oidx)
+
+
 def test_route_nan_logit_sets_status(moe):
     T, D, E, k = 64, 64, 16, 4
     x = torch.randn(T, D, device="cuda")
