@@ -613,6 +613,70 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_dispatch_bandwidth(args):
+    """--dispatch-bandwidth: the permute and combine calls alone on the contiguous bf16
+    workloads, each call timed between CUDA events after an L2 flush (a 256 MB write);
+    one JSON line per workload, rates against the measured copy bandwidth."""
+    import torch
+
+    import moe_inputs
+    import routing_grouped_gemm_gb300 as moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    for name in ("fine-grained-bf16", "zipf-skewed", "deepseek-v3-shaped"):
+        w = moe_inputs.WORKLOADS[name]
+        inp = moe_inputs.make_inputs(w, device=dev, seed=0, weights=False)
+        cfg = moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k, dtype=moe.MOE_BF16,
+                         score=moe.MOE_SCORE_SOFTMAX if w.score == "softmax"
+                         else moe.MOE_SCORE_SIGMOID,
+                         renorm=int(w.renorm), align_m=128, n_group=w.n_group,
+                         topk_group=w.topk_group)
+        ws = moe.alloc_workspace(cfg, device=dev)
+        idx = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+        wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+        moe.moe_route_topk(cfg, inp.x, inp.wg, inp.bias, None, idx, wts, ws)
+        ra = moe.rows_alloc(cfg)
+        tpe = torch.empty(w.E, dtype=torch.int32, device=dev)
+        seg = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+        row_of = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+        tor = torch.empty(ra, dtype=torch.int32, device=dev)
+        xp = torch.empty((ra, w.D), dtype=torch.bfloat16, device=dev)
+        y = torch.randn((ra, w.D), dtype=torch.float32, device=dev)
+        out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+        calls = {
+            "permute": lambda: moe.moe_permute(cfg, inp.x, idx, tpe, seg, row_of, tor, xp, ws),
+            "combine": lambda: moe.moe_unpermute_combine(cfg, y, row_of, wts, out, ws),
+        }
+        calls["permute"]()
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        R = int((row_of >= 0).sum().item())
+        nbytes = {"permute": w.T * w.D * 2 + R * w.D * 2,
+                  "combine": R * w.D * 4 + w.T * w.D * 2 + w.T * w.k * 8}
+        line = {"workload": name, "T": w.T, "D": w.D, "E": w.E, "k": w.k, "routed_rows": R,
+                "l2": "flushed before every call", "steps": args.steps, "warmup": args.warmup}
+        for key, fn in calls.items():
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                if i >= args.warmup:
+                    ev[i - args.warmup][0].record()
+                fn()
+                if i >= args.warmup:
+                    ev[i - args.warmup][1].record()
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+            gbs = nbytes[key] / (ms * 1e-3) / 1e9
+            line[key] = {"us": ms * 1e3, "bytes": nbytes[key], "gbs": gbs,
+                         "frac_of_copy_peak": gbs / peaks["hbm_gbs"]}
+        print(json.dumps(line), flush=True)
+        del inp, xp, y, out, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -628,6 +692,8 @@ def main():
     ap.add_argument("--fp8-only", action="store_true", help="time only the FP8 leg, print its JSON")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the training step (forward_train + backward), print its JSON")
+    ap.add_argument("--dispatch-bandwidth", action="store_true",
+                    help="time only the permute and combine calls on three workloads")
     ap.add_argument("--scale", default="",
                     help="with --backward-only: override workload sizes, e.g. E=16,k=2 (profiling)")
     args = ap.parse_args()
@@ -637,6 +703,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.dispatch_bandwidth:
+        run_dispatch_bandwidth(args)
     else:
         run_gpu(args)
 
