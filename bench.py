@@ -57,6 +57,24 @@ def algorithmic(w):
     )
 
 
+def max_over_ranks(value_ms, dev):
+    """The slowest rank's time: every rank gets the maximum over the process
+    group (the value itself when there is no group or only one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value_ms
+    t = torch.tensor([float(value_ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_tokens_per_s(world, tokens_per_rank, ms_per_step):
+    """Whole-job throughput of `world` replicas that each route tokens_per_rank
+    tokens per step, over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -223,7 +241,6 @@ def run_reference(args):
 def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
     """moe_layer_forward through host buffers: pinned x in, out back, every step."""
     import torch
-    import torch.distributed as dist
     w = inp.w
     lws = moe.alloc_workspace(cfg, host=True, device=dev)
     x_host = inp.x.cpu().pin_memory()
@@ -244,15 +261,11 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
     st = moe.moe_get_device_status(lws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after e2e: {moe.status_string(st)}")
-    return {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
+    return {"value": replica_tokens_per_s(world, w.T, e2e_ms), "unit": UNIT,
             "h2d_bytes_per_step": int(x_host.numel() * 2),
             "d2h_bytes_per_step": int(out_host.numel() * 2),
             "api": "moe_layer_forward_host (C ABI): pinned host x copied in, out copied back, every step"}
@@ -526,11 +539,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     st = moe.moe_get_device_status(ws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
@@ -543,7 +552,7 @@ def run_gpu(args):
     parts = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
     mean_parts = parts.mean(0)
     ms_per_step = elapsed_ms / args.steps
-    value = world * w.T / (ms_per_step * 1e-3)
+    value = replica_tokens_per_s(world, w.T, ms_per_step)
 
     # end to end: moe_layer_forward with pinned host input / output each step
     e2e = None
