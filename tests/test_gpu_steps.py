@@ -249,6 +249,7 @@ def _run_permute(moe, cfg, x, idx, ws=None):
     (1000, 16, 4, 128, 0, 16, 1.3),      # ragged tail block, empty experts
     (257, 64, 6, 128, 0, 64, 0.0),
     (31, 8, 2, 1, 0, 8, 0.0),            # fewer tokens than a warp, no padding
+    (40, 256, 8, 128, 0, 256, 0.5),      # fewer tokens than experts: a warp pads several segments
     (2000, 32, 8, 8, 8, 12, 0.8),        # expert range, small alignment
     (513, 256, 8, 128, 0, 256, 0.3),
     (700, 5, 1, 16, 2, 2, 0.0),          # k = 1
@@ -324,6 +325,22 @@ def test_permute_masked_and_capacity(moe):
         for t in toks[cap2:]:
             j = int(np.nonzero(idx[t] == e)[0][0])
             assert row2[t, j] == -1
+
+
+def test_permute_masked_few_tokens(moe):
+    """Masked layout with fewer tokens than local experts: every segment's unused
+    capacity rows are -1 in token_of_row, written by the copy kernel's warps."""
+    T, E, k, D, cap = 20, 48, 4, 64, 5
+    idx = moe_inputs.random_topk_idx(T, E, k, seed=12, skew=0.7)
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
+                     layout=moe.MOE_LAYOUT_MASKED, capacity=cap, e_first=4, E_local=40)
+    x = torch.randn(T, D, device="cuda").to(torch.bfloat16)
+    st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
+    lay = oracle.layout(idx, E, 4, 40, oracle.MASKED, 1, cap)
+    assert st == (moe.MOE_OK if lay["status"] == oracle.OK else moe.MOE_ERR_CAPACITY)
+    for a, b in ((tpe, "tokens_per_expert"), (seg, "seg_offsets"), (row_of, "row_of"),
+                 (tor, "token_of_row")):
+        assert np.array_equal(a, lay[b])
 
 
 def test_permute_bad_ids_flagged_and_skipped(moe):
