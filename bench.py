@@ -15,7 +15,7 @@ Multi-GPU: the path does not exchange data; each rank runs an independent
 replica on its own GPU ("scaling": "weak") and value = all ranks' tokens / the
 slowest rank's time.
 
---impl reference times the CPU oracle (the reference arm of this build) on
+--impl reference times the CPU oracle (the reference arm) on
 the same workload and prints the same kind of line with "impl": "reference".
 """
 from __future__ import annotations
