@@ -688,6 +688,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     int2 *wmeta = reinterpret_cast<int2 *>(blk_base + (size_t)nblk * E);
     const size_t mask_smem = sizeof(uint32_t) * PB_WARPS * (size_t)E;
     cudaError_t err;
+    if (x_scale && (D % 8 || k > 32)) return cudaErrorInvalidValue;  // before any launch
     if (nblk > 0 && (int64_t)nblk * E <= CS_MAX_CELLS) {
         const size_t smem =
             mask_smem + sizeof(int) * ((size_t)nblk * E + E + E_local + 1);
@@ -701,7 +702,6 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         count_launch();
         const int warps_per_block = 8;
         const int blocks = (T + warps_per_block - 1) / warps_per_block;
-        if (x_scale && (D % 8 || k > 32)) return cudaErrorInvalidValue;
         if ((err = launch_pdl(x_scale ? permute_index_copy_kernel<true>
                                       : permute_index_copy_kernel<false>,
                               dim3(blocks), dim3(32 * warps_per_block), 0, stream,
