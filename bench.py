@@ -8,8 +8,10 @@ One step = router top-k -> permute -> grouped SwiGLU (GEMM1 + gate, GEMM2)
 -> weighted combine, issued as the four step calls of the C ABI on one
 stream.  The line reports routed tokens/s (value), the grouped GEMM's
 TFLOP/s against the measured bf16 peak (roofline), permute and combine GB/s
-(breakdown), an end-to-end figure through moe_layer_forward with host
-buffers (e2e), and the CPU oracle timed on a bounded sample (cpu_baseline).
+(breakdown), an end-to-end figure with host buffers through the host
+pipeline, every step copying its input in and its output out (e2e; the
+one-call-at-a-time figure beside it), and the CPU oracle timed on a bounded
+sample (cpu_baseline).
 
 Multi-GPU: the path does not exchange data; each rank runs an independent
 replica on its own GPU ("scaling": "weak") and value = all ranks' tokens / the
@@ -239,38 +241,71 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
-    """moe_layer_forward through host buffers: pinned x in, out back, every step."""
+    """End to end through host buffers: every step copies its pinned x in and
+    its output out.  The headline figure runs the steps through the host
+    pipeline (moe_host_pipeline: each step's copies overlap the neighbouring
+    steps' compute, as a serving loop would run them); the single-call figure
+    through moe_layer_forward_host, one step at a time on one stream."""
     import torch
     w = inp.w
-    lws = moe.alloc_workspace(cfg, host=True, device=dev)
+    e_steps = max(10, args.steps // 4)
     x_host = inp.x.cpu().pin_memory()
     out_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step():
+    # single call: copy in, layer, copy out, all on `stream`
+    lws = moe.alloc_workspace(cfg, host=True, device=dev)
+
+    def single_step():
         moe.moe_layer_forward_host(cfg, x_host, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out_host,
                                    lws, stream)
 
     for _ in range(max(3, args.warmup)):
-        e2e_step()
+        single_step()
     torch.cuda.synchronize(dev)
-    e_steps = max(10, args.steps // 4)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e_steps):
-        e2e_step()
+        single_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
+    single_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
     st = moe.moe_get_device_status(lws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after e2e: {moe.status_string(st)}")
-    return {"value": replica_tokens_per_s(world, w.T, e2e_ms), "unit": UNIT,
+    del lws
+
+    # pipelined: the timed region opens on an idle device and closes after
+    # the pipeline's sync (every output copy done)
+    pipe = moe.HostPipeline(cfg, device=dev)
+    try:
+        def piped_step():
+            pipe.submit(x_host, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out_host, stream)
+
+        for _ in range(max(3, args.warmup)):
+            piped_step()
+        pipe.sync()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(e_steps):
+            piped_step()
+        pipe.sync()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        piped_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
+    finally:
+        pipe.close()
+    return {"value": replica_tokens_per_s(world, w.T, piped_ms), "unit": UNIT,
             "h2d_bytes_per_step": int(x_host.numel() * 2),
             "d2h_bytes_per_step": int(out_host.numel() * 2),
-            "api": "moe_layer_forward_host (C ABI): pinned host x copied in, out copied back, every step"}
-
-
+            "ms_per_step": piped_ms, "steps": e_steps,
+            "api": "moe_host_pipeline (C ABI, depth 2): every step copies its pinned x in and its "
+                   "output out on the pipeline's copy streams, overlapping the neighbouring steps' "
+                   "compute",
+            "single_call": {"value": replica_tokens_per_s(world, w.T, single_ms), "unit": UNIT,
+                            "ms_per_step": single_ms,
+                            "api": "moe_layer_forward_host (C ABI): copy in, layer, copy out on one "
+                                   "stream, one step at a time"}}
 
 
 def run_fused(moe, cfg, inp, stream, dev, args):

@@ -250,6 +250,49 @@ moe_status moe_layer_forward_host(const moe_config *cfg, const void *x_host, con
                                   moe_stream_t stream);
 
 /*
+ * A depth-2 pipeline of moe_layer_forward calls with HOST activations (this
+ * entry point has no counterpart in the pages; it is how a serving loop
+ * keeps the host link and the GPU busy together).  Each submitted call
+ * copies its x_host in and its result out, like moe_layer_forward_host, but
+ * on two streams of the pipeline: the input copy of a call runs while the
+ * previous call computes, and its output copy while the next call computes.
+ * Device staging alternates between two slots of x and of out.
+ *
+ *   moe_host_pipeline_workspace_size: bytes of the caller's workspace (the
+ *     layer workspace plus two x slots and two out slots), or -1 for a bad
+ *     config.
+ *   moe_host_pipeline_create: checks the config and the workspace (device
+ *     memory, zero-filled once, 256-byte aligned, ws_bytes >= the size
+ *     above) and creates the pipeline's two streams and its events on the
+ *     current device.  Allocates no device memory.  *out receives the
+ *     handle (NULL on failure).
+ *   moe_host_pipeline_submit: queues one call: x_host [T, D] and out_host
+ *     [T, D] (dtype, row-major) are host pointers, the weights device
+ *     pointers, `stream` the compute stream, the same for every call of a
+ *     pipeline (the calls share the layer workspace's intermediates and
+ *     rely on that stream's order).  Returns after queueing.  The
+ *     host buffers of every submitted call must stay valid, and x_host
+ *     unchanged, until moe_host_pipeline_sync returns; out_host holds the
+ *     call's output from then on.  Page-locked buffers let the copies
+ *     overlap the compute.
+ *   moe_host_pipeline_sync: waits for every submitted call, output copies
+ *     included, then returns the workspace status word like
+ *     moe_get_device_status (and clears it).
+ *   moe_host_pipeline_destroy: waits for the pipeline's streams and frees
+ *     its streams, events and handle (NULL is a no-op).
+ * Host-side argument errors are returned before anything is queued.
+ */
+typedef struct moe_host_pipeline moe_host_pipeline;
+int64_t moe_host_pipeline_workspace_size(const moe_config *cfg);
+moe_status moe_host_pipeline_create(const moe_config *cfg, void *ws, size_t ws_bytes,
+                                    moe_host_pipeline **out);
+moe_status moe_host_pipeline_submit(moe_host_pipeline *pipe, const void *x_host, const void *wg,
+                                    const float *bias, const void *w1, const void *w3,
+                                    const void *w2, void *out_host, moe_stream_t stream);
+moe_status moe_host_pipeline_sync(moe_host_pipeline *pipe);
+void moe_host_pipeline_destroy(moe_host_pipeline *pipe);
+
+/*
  * Training: the forward that keeps what the backward needs, and the backward
  * of the whole layer ("Expert Parallelism (EP)", section 5: the backward runs
  * the forward in mirror -- the combine's backward is a dispatch of the output

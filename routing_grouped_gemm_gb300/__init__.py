@@ -35,6 +35,8 @@ ABI_SYMBOLS = (
     "moe_layer_train_workspace_size", "moe_layer_forward_train", "moe_layer_backward",
     "moe_quantize_rows_fp8", "moe_permute_fp8", "moe_grouped_swiglu_fp8", "moe_layer_forward_fp8",
     "moe_layer_forward_fused", "moe_layer_backward_ex",
+    "moe_host_pipeline_workspace_size", "moe_host_pipeline_create", "moe_host_pipeline_submit",
+    "moe_host_pipeline_sync", "moe_host_pipeline_destroy",
 )
 
 
@@ -85,6 +87,11 @@ def _load() -> ctypes.CDLL:
         "moe_layer_forward_fp8": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_layer_forward_fused": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_layer_backward_ex": (I32, [C, P, P, P, P, P, P, P, P, P, P, P, P, I32, P, SZ, P]),
+        "moe_host_pipeline_workspace_size": (I64, [C]),
+        "moe_host_pipeline_create": (I32, [C, P, SZ, ctypes.POINTER(P)]),
+        "moe_host_pipeline_submit": (I32, [P, P, P, P, P, P, P, P, P]),
+        "moe_host_pipeline_sync": (I32, [P]),
+        "moe_host_pipeline_destroy": (None, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -356,6 +363,72 @@ def moe_layer_forward_host(cfg: Config, x_host, wg, bias, w1, w3, w2, out_host, 
     _check(_lib.moe_layer_forward_host(ctypes.byref(c), x_host.data_ptr(), _ptr(wg), _ptr(bias),
                                        _ptr(w1), _ptr(w3), _ptr(w2), out_host.data_ptr(), _ptr(ws),
                                        ws.numel(), _stream(stream)), "moe_layer_forward_host")
+
+
+def host_pipeline_workspace_size(cfg: Config) -> int:
+    c = cfg.c()
+    return int(_lib.moe_host_pipeline_workspace_size(ctypes.byref(c)))
+
+
+class HostPipeline:
+    """moe_host_pipeline: moe_layer_forward calls on host activations whose
+    input and output copies overlap the neighbouring calls' compute.
+
+    submit() queues one call (x_host, out_host: contiguous host tensors,
+    page-locked for overlap; every call on the same compute stream); sync()
+    waits for all of them, output copies included, and raises on a flagged
+    device status.  Host buffers must stay valid, and x_host unchanged,
+    until sync() returns."""
+
+    def __init__(self, cfg: Config, device="cuda"):
+        n = host_pipeline_workspace_size(cfg)
+        if n < 0:
+            raise MoeError(MOE_ERR_INVALID_ARG, "host pipeline workspace size")
+        self.cfg = cfg
+        self.ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+        self._c = cfg.c()
+        h = ctypes.c_void_p()
+        _check(_lib.moe_host_pipeline_create(ctypes.byref(self._c), _ptr(self.ws), self.ws.numel(),
+                                             ctypes.byref(h)), "moe_host_pipeline_create")
+        self._h = h
+        self._keep = []
+
+    def submit(self, x_host, wg, bias, w1, w3, w2, out_host, stream=None):
+        cfg = self.cfg
+        dt = cfg.torch_dtype
+        el = cfg.e_local
+        for t, shape, name in ((x_host, (cfg.T, cfg.D), "x_host"),
+                               (out_host, (cfg.T, cfg.D), "out_host")):
+            if tuple(t.shape) != shape or t.dtype != dt or t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name}: expected a contiguous host tensor {shape} {dt}")
+        _expect(wg, (cfg.E, cfg.D), dt, "wg")
+        if bias is not None:
+            _expect(bias, (cfg.E,), torch.float32, "bias")
+        _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+        _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+        _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+        self._keep.append((x_host, out_host))  # alive until sync()
+        _check(_lib.moe_host_pipeline_submit(self._h, x_host.data_ptr(), _ptr(wg), _ptr(bias),
+                                             _ptr(w1), _ptr(w3), _ptr(w2), out_host.data_ptr(),
+                                             _stream(stream)), "moe_host_pipeline_submit")
+
+    def sync(self):
+        st = int(_lib.moe_host_pipeline_sync(self._h))
+        self._keep.clear()
+        if st != MOE_OK:
+            raise MoeError(st, "moe_host_pipeline_sync")
+
+    def close(self):
+        if self._h:
+            _lib.moe_host_pipeline_destroy(self._h)
+            self._h = None
+            self._keep.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def moe_layer_forward_train(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None):

@@ -16,7 +16,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 10400;  // 1.4.0
+constexpr int32_t kAbiVersion = 10500;  // 1.5.0
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int64_t kAlign = 256;
@@ -525,6 +525,141 @@ MOE_EXPORT moe_status moe_layer_forward_host(const moe_config *cfg, const void *
     e = cudaMemcpyAsync(out_host, out_dev, (size_t)act_bytes(cfg), cudaMemcpyDeviceToHost, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_host: copy out");
 }
+
+// ---------------------------------------------------------------------
+// Host-buffer pipeline: workspace = layer workspace | x slot 0 | x slot 1 |
+// out slot 0 | out slot 1.  Per call (slot = call number mod 2):
+//   h2d stream:     wait x_free[slot]; copy x_host -> x slot; record x_ready
+//   compute stream: wait x_ready; route, permute; record x_free; grouped;
+//                   wait out_free[slot]; combine -> out slot; record out_ready
+//   d2h stream:     wait out_ready; copy out slot -> out_host; record out_free
+// A fresh event counts as complete, so the first use of a slot waits on
+// nothing.
+// ---------------------------------------------------------------------
+struct moe_host_pipeline {
+    moe_config cfg;
+    char *ws;
+    size_t ws_bytes;
+    int64_t lws, slot_bytes;
+    cudaStream_t h2d, d2h, last_compute;
+    cudaEvent_t x_ready[2], x_free[2], out_ready[2], out_free[2];
+    unsigned long long calls;
+};
+
+static int64_t pipeline_ws_bytes(const moe_config *cfg) {
+    return layer_ws_layout(cfg, nullptr, nullptr) + 4 * align_up(act_bytes(cfg));
+}
+
+MOE_EXPORT int64_t moe_host_pipeline_workspace_size(const moe_config *cfg) {
+    return validate(cfg) == MOE_OK ? pipeline_ws_bytes(cfg) : -1;
+}
+
+static void pipeline_free(moe_host_pipeline *p) {
+    if (!p) return;
+    if (p->h2d) cudaStreamSynchronize(p->h2d);
+    if (p->d2h) cudaStreamSynchronize(p->d2h);
+    for (int i = 0; i < 2; ++i) {
+        cudaEvent_t *evs[4] = {&p->x_ready[i], &p->x_free[i], &p->out_ready[i], &p->out_free[i]};
+        for (cudaEvent_t *ev : evs)
+            if (*ev) cudaEventDestroy(*ev);
+    }
+    if (p->h2d) cudaStreamDestroy(p->h2d);
+    if (p->d2h) cudaStreamDestroy(p->d2h);
+    delete p;
+}
+
+MOE_EXPORT moe_status moe_host_pipeline_create(const moe_config *cfg, void *ws, size_t ws_bytes,
+                                               moe_host_pipeline **out) {
+    if (!out) return arg_fail("moe_host_pipeline_create: out is NULL");
+    *out = nullptr;
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < pipeline_ws_bytes(cfg))
+        return arg_fail("workspace too small for moe_host_pipeline", MOE_ERR_WORKSPACE);
+    moe_host_pipeline *p = new moe_host_pipeline{};
+    p->cfg = *cfg;
+    p->ws = static_cast<char *>(ws);
+    p->ws_bytes = ws_bytes;
+    p->lws = layer_ws_layout(cfg, nullptr, nullptr);
+    p->slot_bytes = align_up(act_bytes(cfg));
+    cudaError_t e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        cudaEvent_t *evs[4] = {&p->x_ready[i], &p->x_free[i], &p->out_ready[i], &p->out_free[i]};
+        for (cudaEvent_t *ev : evs)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        pipeline_free(p);
+        return cuda_fail(e, "moe_host_pipeline_create");
+    }
+    *out = p;
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_host_pipeline_submit(moe_host_pipeline *p, const void *x_host,
+                                               const void *wg, const float *bias, const void *w1,
+                                               const void *w3, const void *w2, void *out_host,
+                                               moe_stream_t stream) {
+    if (!p) return arg_fail("moe_host_pipeline_submit: pipeline is NULL");
+    const moe_config *cfg = &p->cfg;
+    if (cfg->T == 0) return MOE_OK;
+    if (!x_host || !out_host) return arg_fail("moe_host_pipeline_submit: NULL host buffer");
+    if (!need16(wg) || (bias && !aligned(bias, 4)))
+        return arg_fail("moe_host_pipeline_submit: NULL or misaligned router weights");
+    if (cfg->E_local > 0 && (!need16(w1) || !need16(w3) || !need16(w2)))
+        return arg_fail("moe_host_pipeline_submit: NULL or misaligned expert weights");
+    const int slot = (int)(p->calls & 1);
+    void *x_dev = p->ws + p->lws + slot * p->slot_bytes;
+    void *out_dev = p->ws + p->lws + (2 + slot) * p->slot_bytes;
+    const size_t n = (size_t)act_bytes(cfg);
+    cudaStream_t s = (cudaStream_t)stream;
+    LayerWs L;
+    carve_step(cfg, p->ws, (size_t)p->lws, &L.step);
+    layer_ws_layout(cfg, p->ws, &L);
+    cudaError_t e;
+    if ((e = cudaStreamWaitEvent(p->h2d, p->x_free[slot], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(x_dev, x_host, n, cudaMemcpyHostToDevice, p->h2d)) != cudaSuccess ||
+        (e = cudaEventRecord(p->x_ready[slot], p->h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, p->x_ready[slot], 0)) != cudaSuccess)
+        return cuda_fail(e, "moe_host_pipeline_submit: copy in");
+    moe_status st;
+    if ((st = do_route(cfg, x_dev, wg, bias, nullptr, L.topk_idx, L.topk_w, L.step, s)) != MOE_OK)
+        return st;
+    if ((st = do_permute(cfg, x_dev, L.topk_idx, L.tpe, L.seg_off, L.row_of, L.token_of_row,
+                         L.x_perm, L.step, s)) != MOE_OK)
+        return st;
+    if ((e = cudaEventRecord(p->x_free[slot], s)) != cudaSuccess)
+        return cuda_fail(e, "moe_host_pipeline_submit: event");
+    if (cfg->E_local > 0 && rows_alloc_of(cfg) > 0 &&
+        (st = do_grouped(cfg, L.x_perm, L.seg_off, L.tpe, w1, w3, w2, L.h, L.y_perm, L.step, s)) !=
+            MOE_OK)
+        return st;
+    if ((e = cudaStreamWaitEvent(s, p->out_free[slot], 0)) != cudaSuccess)
+        return cuda_fail(e, "moe_host_pipeline_submit: event");
+    if ((st = do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out_dev, L.step, s)) != MOE_OK)
+        return st;
+    if ((e = cudaEventRecord(p->out_ready[slot], s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(p->d2h, p->out_ready[slot], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(out_host, out_dev, n, cudaMemcpyDeviceToHost, p->d2h)) != cudaSuccess ||
+        (e = cudaEventRecord(p->out_free[slot], p->d2h)) != cudaSuccess)
+        return cuda_fail(e, "moe_host_pipeline_submit: copy out");
+    p->last_compute = s;
+    ++p->calls;
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_host_pipeline_sync(moe_host_pipeline *p) {
+    if (!p) return arg_fail("moe_host_pipeline_sync: pipeline is NULL");
+    cudaError_t e = cudaStreamSynchronize(p->h2d);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->d2h);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_host_pipeline_sync");
+    return moe_get_device_status(p->ws, p->ws_bytes, (moe_stream_t)p->last_compute);
+}
+
+MOE_EXPORT void moe_host_pipeline_destroy(moe_host_pipeline *p) { pipeline_free(p); }
 
 MOE_EXPORT int64_t moe_layer_train_workspace_size(const moe_config *cfg) {
     if (validate(cfg) != MOE_OK || train_supported(cfg) != MOE_OK) return -1;

@@ -148,6 +148,31 @@ def test_host_rejections_launch_nothing(moe):
     assert moe.kernel_launches() == before
 
 
+def test_host_pipeline_host_checks(moe):
+    """The host pipeline checks its config, workspace and handle on the host,
+    before it creates a stream or queues anything."""
+    lib = moe._lib
+    cfg = _cfg(moe)
+    n = moe.host_pipeline_workspace_size(cfg)
+    assert n >= moe.layer_host_workspace_size(cfg) > 0
+    assert moe.host_pipeline_workspace_size(_cfg(moe, D=12)) == -1
+    h = ctypes.c_void_p(123)
+    c = cfg.c()
+    assert lib.moe_host_pipeline_create(ctypes.byref(c), None, n, ctypes.byref(h)) == \
+        moe.MOE_ERR_WORKSPACE
+    assert not h.value                                   # NULL on failure
+    bad = _cfg(moe, k=0).c()
+    assert lib.moe_host_pipeline_create(ctypes.byref(bad), 256, n, ctypes.byref(h)) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_host_pipeline_create(ctypes.byref(c), 256, n, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_host_pipeline_create(ctypes.byref(c), 256, n - 1, ctypes.byref(h)) == \
+        moe.MOE_ERR_WORKSPACE
+    assert lib.moe_host_pipeline_submit(None, 0, 0, None, 0, 0, 0, 0, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_host_pipeline_sync(None) == moe.MOE_ERR_INVALID_ARG
+    lib.moe_host_pipeline_destroy(None)                  # a no-op
+
+
 def test_status_strings(moe):
     assert moe.status_string(moe.MOE_OK) == "MOE_OK"
     assert moe.status_string(moe.MOE_ERR_CAPACITY) == "MOE_ERR_CAPACITY"

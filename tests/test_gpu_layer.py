@@ -188,6 +188,43 @@ def test_layer_forward_host_buffers(moe, pinned_out):
         assert torch.equal(out_host, ref.cpu())
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_pipeline_matches_layer_forward(moe, pinned):
+    """Five calls queued back to back on the host pipeline, each with its own
+    input and output buffer (the two device slots are each reused twice or
+    more), then a sixth after a sync: every output is bit-identical to
+    moe_layer_forward on the same input, with page-locked and with pageable
+    host buffers."""
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=700, D=512, H=384)
+    cfg = cfg_for(moe, w)
+    base = moe_inputs.make_inputs(w, device="cuda", seed=21)
+    xs = [moe_inputs.make_inputs(w, device="cuda", seed=30 + i, weights=False).x for i in range(6)]
+    refs = []
+    lws = moe.alloc_workspace(cfg, layer=True)
+    for x in xs:
+        out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device="cuda")
+        moe.moe_layer_forward(cfg, x, base.wg, base.bias, base.w1, base.w3, base.w2, out, lws)
+        refs.append(out.cpu())
+    assert moe.moe_get_device_status(lws) == moe.MOE_OK
+
+    def host(t):
+        return t.pin_memory() if pinned else t
+
+    pipe = moe.HostPipeline(cfg)
+    try:
+        x_hosts = [host(x.cpu()) for x in xs]
+        outs = [host(torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16)) for _ in xs]
+        for i in range(5):
+            pipe.submit(x_hosts[i], base.wg, base.bias, base.w1, base.w3, base.w2, outs[i])
+        pipe.sync()
+        pipe.submit(x_hosts[5], base.wg, base.bias, base.w1, base.w3, base.w2, outs[5])
+        pipe.sync()
+    finally:
+        pipe.close()
+    for i in range(6):
+        assert torch.equal(outs[i], refs[i]), i
+
+
 def test_layer_k32_many_experts(moe):
     """k = 32 of E = 256 (the largest k the ABI accepts), bf16."""
     w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=96, E=256, k=32, D=256, H=128)
