@@ -268,9 +268,10 @@ moe_status moe_layer_forward_host(const moe_config *cfg, const void *x_host, con
  *     handle (NULL on failure).
  *   moe_host_pipeline_submit: queues one call: x_host [T, D] and out_host
  *     [T, D] (dtype, row-major) are host pointers, the weights device
- *     pointers, `stream` the compute stream, the same for every call of a
- *     pipeline (the calls share the layer workspace's intermediates and
- *     rely on that stream's order).  Returns after queueing.  The
+ *     pointers, `stream` the compute stream, the same for every call
+ *     between two syncs (the calls share the layer workspace's
+ *     intermediates and rely on that stream's order; another stream there
+ *     is MOE_ERR_INVALID_ARG).  Returns after queueing.  The
  *     host buffers of every submitted call must stay valid, and x_host
  *     unchanged, until moe_host_pipeline_sync returns; out_host holds the
  *     call's output from then on.  Page-locked buffers let the copies

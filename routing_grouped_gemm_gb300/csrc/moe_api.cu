@@ -544,6 +544,7 @@ struct moe_host_pipeline {
     cudaStream_t h2d, d2h, last_compute;
     cudaEvent_t x_ready[2], x_free[2], out_ready[2], out_free[2];
     unsigned long long calls;
+    unsigned long long pending;  // calls submitted since the last sync
 };
 
 static int64_t pipeline_ws_bytes(const moe_config *cfg) {
@@ -611,6 +612,8 @@ MOE_EXPORT moe_status moe_host_pipeline_submit(moe_host_pipeline *p, const void 
         return arg_fail("moe_host_pipeline_submit: NULL or misaligned router weights");
     if (cfg->E_local > 0 && (!need16(w1) || !need16(w3) || !need16(w2)))
         return arg_fail("moe_host_pipeline_submit: NULL or misaligned expert weights");
+    if (p->pending > 0 && (cudaStream_t)stream != p->last_compute)
+        return arg_fail("moe_host_pipeline_submit: calls between two syncs must share one stream");
     const int slot = (int)(p->calls & 1);
     void *x_dev = p->ws + p->lws + slot * p->slot_bytes;
     void *out_dev = p->ws + p->lws + (2 + slot) * p->slot_bytes;
@@ -648,6 +651,7 @@ MOE_EXPORT moe_status moe_host_pipeline_submit(moe_host_pipeline *p, const void 
         return cuda_fail(e, "moe_host_pipeline_submit: copy out");
     p->last_compute = s;
     ++p->calls;
+    ++p->pending;
     return MOE_OK;
 }
 
@@ -656,6 +660,7 @@ MOE_EXPORT moe_status moe_host_pipeline_sync(moe_host_pipeline *p) {
     cudaError_t e = cudaStreamSynchronize(p->h2d);
     if (e == cudaSuccess) e = cudaStreamSynchronize(p->d2h);
     if (e != cudaSuccess) return cuda_fail(e, "moe_host_pipeline_sync");
+    p->pending = 0;
     return moe_get_device_status(p->ws, p->ws_bytes, (moe_stream_t)p->last_compute);
 }
 

@@ -218,6 +218,10 @@ def test_host_pipeline_matches_layer_forward(moe, pinned):
             pipe.submit(x_hosts[i], base.wg, base.bias, base.w1, base.w3, base.w2, outs[i])
         pipe.sync()
         pipe.submit(x_hosts[5], base.wg, base.bias, base.w1, base.w3, base.w2, outs[5])
+        other = torch.cuda.Stream()
+        with pytest.raises(moe.MoeError):     # another stream while a call is pending
+            pipe.submit(x_hosts[0], base.wg, base.bias, base.w1, base.w3, base.w2, outs[0],
+                        stream=other)
         pipe.sync()
     finally:
         pipe.close()
