@@ -17,7 +17,8 @@
 namespace moe {
 namespace {
 
-constexpr int F_BM = 64, F_BN = 64, F_BK = 16, F_THREADS = 256;
+constexpr int F_BM = 64, F_BN = 64, F_BK = 32, F_THREADS = 256;
+constexpr int F_PER = F_BM * F_BK / F_THREADS;  // tile elements each thread stages per k-step
 constexpr int F_LD = F_BM + 4;
 constexpr int F_MAX_EXPERTS = 1024;
 
@@ -57,16 +58,33 @@ grouped_f32_kernel(const float *__restrict__ A, int K, const float *__restrict__
 #pragma unroll
         for (int b = 0; b < 4; ++b) accg[a][b] = accu[a][b] = 0.f;
 
-    for (int k0 = 0; k0 < K; k0 += F_BK) {
-        for (int e = tid; e < F_BM * F_BK; e += F_THREADS) {
+    // the next k-step's tiles are loaded into registers while this one is
+    // multiplied out of shared memory
+    float ra[F_PER], rg[F_PER], ru[F_PER];
+    auto load_tiles = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < F_PER; ++q) {
+            const int e = tid + q * F_THREADS;
             const int r = e / F_BK, kk = e % F_BK;
-            As[kk][r] = (r < nvalid && k0 + kk < K) ? A[(size_t)(row0 + r) * K + k0 + kk] : 0.f;
+            ra[q] = (r < nvalid && k0 + kk < K) ? A[(size_t)(row0 + r) * K + k0 + kk] : 0.f;
             const int n = n0 + r;
             const bool okb = n < N && k0 + kk < K;
-            Bgs[kk][r] = okb ? Bg_e[(size_t)n * K + k0 + kk] : 0.f;
-            if (MODE == 1) Bus[kk][r] = okb ? Bu_e[(size_t)n * K + k0 + kk] : 0.f;
+            rg[q] = okb ? Bg_e[(size_t)n * K + k0 + kk] : 0.f;
+            if (MODE == 1) ru[q] = okb ? Bu_e[(size_t)n * K + k0 + kk] : 0.f;
+        }
+    };
+    load_tiles(0);
+    for (int k0 = 0; k0 < K; k0 += F_BK) {
+#pragma unroll
+        for (int q = 0; q < F_PER; ++q) {
+            const int e = tid + q * F_THREADS;
+            const int r = e / F_BK, kk = e % F_BK;
+            As[kk][r] = ra[q];
+            Bgs[kk][r] = rg[q];
+            if (MODE == 1) Bus[kk][r] = ru[q];
         }
         __syncthreads();
+        if (k0 + F_BK < K) load_tiles(k0 + F_BK);
 #pragma unroll
         for (int kk = 0; kk < F_BK; ++kk) {
             float av[4], gv[4], uv[4];

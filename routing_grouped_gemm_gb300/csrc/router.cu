@@ -33,6 +33,8 @@ constexpr int RT_BK = 32;       // reduction slice
 constexpr int RT_THREADS = 256;
 constexpr int SX_LD = RT_TOKENS + 1;  // padded strides keep the transposing
 constexpr int SW_LD = RT_ECHUNK + 1;  // shared-memory stores conflict-free
+static_assert(RT_TOKENS * RT_BK % RT_THREADS == 0 && RT_ECHUNK * RT_BK % RT_THREADS == 0,
+              "each thread stages whole shares of the x and W_g slices");
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
@@ -231,20 +233,41 @@ router_topk_kernel(const T *__restrict__ x, const T *__restrict__ wg, const floa
 #pragma unroll
             for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 
-        for (int d0 = 0; d0 < D; d0 += RT_BK) {
-            // x slice: 32 tokens x 32 d, stored transposed [d][token]
-            for (int i = tid; i < RT_TOKENS * RT_BK; i += RT_THREADS) {
+        // the next D slice is loaded into registers while this one is
+        // multiplied out of shared memory
+        constexpr int XPER = RT_TOKENS * RT_BK / RT_THREADS, WPER = RT_ECHUNK * RT_BK / RT_THREADS;
+        float rx[XPER], rw[WPER];
+        auto load_slices = [&](int d0) {
+#pragma unroll
+            for (int q = 0; q < XPER; ++q) {  // x slice: 32 tokens x 32 d
+                const int i = tid + q * RT_THREADS;
                 const int tt = i / RT_BK, dd = i % RT_BK;
                 const int t = t0 + tt, d = d0 + dd;
-                s_x[dd * SX_LD + tt] = (t < Tn && d < D) ? to_f32(x[(size_t)t * D + d]) : 0.f;
+                rx[q] = (t < Tn && d < D) ? to_f32(x[(size_t)t * D + d]) : 0.f;
             }
-            // W_g slice: 128 experts x 32 d, stored transposed [d][expert]
-            for (int i = tid; i < RT_ECHUNK * RT_BK; i += RT_THREADS) {
+#pragma unroll
+            for (int q = 0; q < WPER; ++q) {  // W_g slice: 128 experts x 32 d
+                const int i = tid + q * RT_THREADS;
                 const int ee = i / RT_BK, dd = i % RT_BK;
                 const int e = e0 + ee, d = d0 + dd;
-                s_w[dd * SW_LD + ee] = (e < E && d < D) ? to_f32(wg[(size_t)e * D + d]) : 0.f;
+                rw[q] = (e < E && d < D) ? to_f32(wg[(size_t)e * D + d]) : 0.f;
+            }
+        };
+        load_slices(0);
+        for (int d0 = 0; d0 < D; d0 += RT_BK) {
+            // both slices stored transposed: [d][token] and [d][expert]
+#pragma unroll
+            for (int q = 0; q < XPER; ++q) {
+                const int i = tid + q * RT_THREADS;
+                s_x[(i % RT_BK) * SX_LD + i / RT_BK] = rx[q];
+            }
+#pragma unroll
+            for (int q = 0; q < WPER; ++q) {
+                const int i = tid + q * RT_THREADS;
+                s_w[(i % RT_BK) * SW_LD + i / RT_BK] = rw[q];
             }
             __syncthreads();
+            if (d0 + RT_BK < D) load_slices(d0 + RT_BK);
 #pragma unroll 8
             for (int dd = 0; dd < RT_BK; ++dd) {
                 float xv[4], wv[4];

@@ -229,6 +229,42 @@ def test_host_pipeline_matches_layer_forward(moe, pinned):
         assert torch.equal(outs[i], refs[i]), i
 
 
+@pytest.mark.parametrize("name,over", [
+    ("fine-grained-bf16", dict(T=700, D=512, H=384)),
+    ("tiny-fp32", dict()),
+])
+def test_layer_forward_in_cuda_graph(moe, name, over):
+    """moe_layer_forward captured once into a CUDA graph (after a warm-up call
+    outside the capture) and replayed on new inputs written into the same
+    buffers: every replay is bit-identical to a direct call."""
+    w = moe_inputs.WORKLOADS[name].scaled(**over)
+    cfg = cfg_for(moe, w)
+    base = moe_inputs.make_inputs(w, device="cuda", seed=41)
+    x = base.x.clone()
+    out = torch.empty_like(x)
+    ws = moe.alloc_workspace(cfg, layer=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        moe.moe_layer_forward(cfg, x, base.wg, base.bias, base.w1, base.w3, base.w2, out, ws, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_layer_forward(cfg, x, base.wg, base.bias, base.w1, base.w3, base.w2, out, ws, s)
+    ref_ws = moe.alloc_workspace(cfg, layer=True)
+    for seed in (42, 43, 44):
+        xi = moe_inputs.make_inputs(w, device="cuda", seed=seed, weights=False).x
+        x.copy_(xi)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = torch.empty_like(x)
+        moe.moe_layer_forward(cfg, xi, base.wg, base.bias, base.w1, base.w3, base.w2, ref, ref_ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), seed
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+
+
 def test_layer_k32_many_experts(moe):
     """k = 32 of E = 256 (the largest k the ABI accepts), bf16."""
     w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=96, E=256, k=32, D=256, H=128)
