@@ -229,6 +229,78 @@ def test_host_pipeline_matches_layer_forward(moe, pinned):
         assert torch.equal(outs[i], refs[i]), i
 
 
+def test_host_pipeline_shard_and_masked_layout(moe):
+    """The host pipeline on an expert-range x H shard of the masked (decode)
+    layout: three queued calls, each bit-identical to moe_layer_forward on
+    the same shard."""
+    w = moe_inputs.WORKLOADS["decode-masked"].scaled(D=1024, H=512)
+    El, Hl = w.E // w.ep, w.H // w.tp
+    es, hs = slice(2 * El, 3 * El), slice(Hl, 2 * Hl)
+    cfg = cfg_for(moe, w, e_first=2 * El, E_local=El, H_local=Hl)
+    base = moe_inputs.make_inputs(w, device="cuda", seed=51)
+    w1, w3 = base.w1[es, hs].contiguous(), base.w3[es, hs].contiguous()
+    w2 = base.w2[es, :, hs].contiguous()
+    xs = [moe_inputs.make_inputs(w, device="cuda", seed=52 + i, weights=False).x for i in range(3)]
+    lws = moe.alloc_workspace(cfg, layer=True)
+    refs = []
+    for x in xs:
+        out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device="cuda")
+        moe.moe_layer_forward(cfg, x, base.wg, base.bias, w1, w3, w2, out, lws)
+        refs.append(out.cpu())
+    assert moe.moe_get_device_status(lws) == moe.MOE_OK
+    pipe = moe.HostPipeline(cfg)
+    try:
+        x_hosts = [x.cpu().pin_memory() for x in xs]
+        outs = [torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16).pin_memory()
+                for _ in xs]
+        for xh, oh in zip(x_hosts, outs):
+            pipe.submit(xh, base.wg, base.bias, w1, w3, w2, oh)
+        pipe.sync()
+    finally:
+        pipe.close()
+    for i in range(3):
+        assert torch.equal(outs[i], refs[i]), i
+
+
+def test_fp8_layer_in_cuda_graph(moe):
+    """moe_layer_forward_fp8 (quantising dispatch, e4m3 GEMM1) captured into a
+    CUDA graph after a warm-up call and replayed on new inputs: bit-identical
+    to direct calls."""
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=600, D=512, H=384)
+    cfg = cfg_for(moe, w)
+    base = moe_inputs.make_inputs(w, device="cuda", seed=61)
+    w1q, w1s = moe.quantize_weights_fp8(base.w1)
+    w3q, w3s = moe.quantize_weights_fp8(base.w3)
+    x = base.x.clone()
+    out = torch.empty_like(x)
+    ws = moe.alloc_workspace(cfg, layer=True)
+
+    def call(xx, oo, wws, stream=None):
+        moe.moe_layer_forward_fp8(cfg, xx, base.wg, base.bias, w1q, w1s, w3q, w3s, base.w2, oo,
+                                  wws, stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(x, out, ws, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(x, out, ws, s)
+    ref_ws = moe.alloc_workspace(cfg, layer=True)
+    for seed in (62, 63):
+        xi = moe_inputs.make_inputs(w, device="cuda", seed=seed, weights=False).x
+        x.copy_(xi)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = torch.empty_like(x)
+        call(xi, ref, ref_ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), seed
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+
+
 @pytest.mark.parametrize("name,over", [
     ("fine-grained-bf16", dict(T=700, D=512, H=384)),
     ("tiny-fp32", dict()),
