@@ -224,16 +224,25 @@ def rows_alloc(T, k, E_local, layout=CONTIGUOUS, align_m=128, capacity=0) -> int
 
 def layout(idx: np.ndarray, E: int, e_first: int = 0, E_local=None,
            layout_kind: int = CONTIGUOUS, align_m: int = 128, capacity: int = 0):
-    """tokens_per_expert, segment offsets and the permutation (dict)."""
+    """tokens_per_expert, segment offsets and the permutation (dict).
+
+    The layout is complete for every status but BAD_ARG: a masked expert over
+    ``capacity`` keeps its first ``capacity`` tokens (status CAPACITY), and a
+    slot with an id outside [0, E) or an id repeated within its token is left
+    out (status BAD_ROUTING; CAPACITY is reported first when both happen).
+    """
     idx = _c(idx, np.int32)
     T, k = idx.shape
     if E_local is None:
         E_local = E - e_first
     ra = rows_alloc(T, k, E_local, layout_kind, align_m, capacity)
-    cnt = np.zeros(E, np.int32)
-    seg = np.zeros(E_local + 1, np.int32)
-    row_of = np.empty((T, k), np.int32)
-    tor = np.empty(max(ra, 1), np.int32)
+    # outputs start as a sentinel no layout contains, so an array the C code
+    # did not write (a rejected argument) cannot pass for a result
+    unset = np.iinfo(np.int32).min
+    cnt = np.full(E, unset, np.int32)
+    seg = np.full(E_local + 1, unset, np.int32)
+    row_of = np.full((T, k), unset, np.int32)
+    tor = np.full(max(ra, 1), unset, np.int32)
     st = _load().oracle_layout(T, k, E, e_first, E_local, layout_kind, align_m, capacity,
                                _p(idx), _p(cnt), _p(seg), _p(row_of), _p(tor), ra)
     return dict(status=st, tokens_per_expert=cnt, seg_offsets=seg, row_of=row_of,

@@ -358,33 +358,64 @@ long oracle_rows_alloc(int T, int k, int E_local, int layout, int align_m,
 }
 
 /*
- * tokens_per_expert over all E experts ([EP] section 1, "preprocess").
+ * Slot (t, j) of a caller-supplied routing table takes part in the layout
+ * when its expert id lies in [0, E) and no earlier slot of the same token
+ * names the same expert.  A token reaches each expert at most once ([EP]
+ * section 1: top-k picks k distinct experts); an id outside [0, E) or a
+ * repeated id is a contract violation, and that slot is left out.
+ */
+static int slot_valid(const int32_t *row, int j, int E)
+{
+    int e = row[j];
+    if (e < 0 || e >= E) return 0;
+    for (int q = 0; q < j; ++q)
+        if (row[q] == e) return 0;
+    return 1;
+}
+
+/*
+ * tokens_per_expert over all E experts ([EP] section 1, "preprocess"),
+ * counting the valid slots only.
  * Segment offsets over the local range [e_first, e_first + E_local):
  *   contiguous: each segment padded up to a multiple of align_m
  *               ([EP] section 2: segments aligned to the GEMM M tile);
- *   masked:     segment i starts at i * capacity; cnt > capacity is an error.
+ *   masked:     segment i starts at i * capacity ([EP] sections 2 and 6,
+ *               "masked" per-expert buffers of fixed capacity).
  * Inside a segment, rows hold the routed tokens in ascending token order.
- * row_of[t, j] is that row (or -1 when expert idx[t,j] is not local);
- * token_of_row[r] is the token in row r, or -1 for padding rows.
+ * row_of[t, j] is that row (or -1 when expert idx[t,j] is not local, the
+ * slot is not valid, or the token was dropped); token_of_row[r] is the token
+ * in row r, or -1 for padding rows.
+ *
+ * Contract violations still produce the whole layout:
+ *   - a masked expert with more than `capacity` tokens keeps its first
+ *     `capacity` tokens in token order and drops the rest (row_of = -1);
+ *     tokens_per_expert still counts every routed token; the return value
+ *     is ORC_CAPACITY;
+ *   - an invalid slot (see slot_valid) is neither counted nor placed; the
+ *     return value is ORC_BAD_ROUTING unless a capacity overflow also
+ *     happened (ORC_CAPACITY is reported first).
  */
 int oracle_layout(int T, int k, int E, int e_first, int E_local, int layout,
                   int align_m, int capacity, const int32_t *topk_idx,
                   int32_t *cnt, int32_t *seg_off, int32_t *row_of,
                   int32_t *token_of_row, long rows_alloc)
 {
-    if (E_local < 0 || e_first < 0 || e_first + E_local > E || align_m < 1)
+    if (E_local < 0 || e_first < 0 || e_first + E_local > E || align_m < 1 ||
+        (layout == ORC_MASKED && capacity < 0))
         return ORC_BAD_ARG;
+    int bad = 0, over = 0;
     for (int e = 0; e < E; ++e) cnt[e] = 0;
-    for (long i = 0; i < (long)T * k; ++i) {
-        int e = topk_idx[i];
-        if (e < 0 || e >= E) return ORC_BAD_ROUTING;
-        cnt[e] += 1;
-    }
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int32_t *row = topk_idx + (size_t)t * k;
+            if (slot_valid(row, j, E)) cnt[row[j]] += 1;
+            else bad = 1;
+        }
     seg_off[0] = 0;
     for (int i = 0; i < E_local; ++i) {
         int c = cnt[e_first + i];
         if (layout == ORC_MASKED) {
-            if (c > capacity) return ORC_CAPACITY;
+            if (c > capacity) over = 1;
             seg_off[i + 1] = (i + 1) * capacity;
         } else {
             int padded = (c + align_m - 1) / align_m * align_m;
@@ -397,14 +428,18 @@ int oracle_layout(int T, int k, int E, int e_first, int E_local, int layout,
     for (int i = 0; i < E_local; ++i) {
         int e = e_first + i, n = 0;
         for (int t = 0; t < T; ++t)
-            for (int j = 0; j < k; ++j)
-                if (topk_idx[(size_t)t * k + j] == e) {
-                    int r = seg_off[i] + n;
-                    row_of[(size_t)t * k + j] = r;
-                    token_of_row[r] = t;
-                    n += 1;
-                }
+            for (int j = 0; j < k; ++j) {
+                const int32_t *row = topk_idx + (size_t)t * k;
+                if (row[j] != e || !slot_valid(row, j, E)) continue;
+                if (layout == ORC_MASKED && n >= capacity) continue;  /* dropped */
+                int r = seg_off[i] + n;
+                row_of[(size_t)t * k + j] = r;
+                token_of_row[r] = t;
+                n += 1;
+            }
     }
+    if (over) return ORC_CAPACITY;
+    if (bad) return ORC_BAD_ROUTING;
     return ORC_OK;
 }
 

@@ -306,6 +306,64 @@ def test_layout_expert_range_and_masked():
     assert over["status"] == oracle.CAPACITY
 
 
+# A routing table with one out-of-range id (t3 slot 0), one negative id (t4
+# slot 1) and one id repeated within a token (t2 slot 1).  Every expected
+# array below was worked out by hand from the layout's definition: valid
+# slots counted per expert, segments in expert order, tokens ascending inside
+# a segment.
+_BAD_IDX = np.array([[0, 1], [1, 0], [2, 2], [5, 1], [0, -1], [3, 0]], np.int32)
+
+
+def test_layout_bad_ids_hand_example():
+    """Reading R15: an invalid slot is neither counted nor placed."""
+    lay = oracle.layout(_BAD_IDX, 4, align_m=1)
+    assert lay["status"] == oracle.BAD_ROUTING
+    assert list(lay["tokens_per_expert"]) == [4, 3, 1, 1]          # 9 = 12 - 3 slots
+    assert list(lay["seg_offsets"]) == [0, 4, 7, 8, 9]
+    assert lay["row_of"].tolist() == [[0, 4], [5, 1], [7, -1], [-1, 6], [2, -1], [8, 3]]
+    assert list(lay["token_of_row"][:9]) == [0, 1, 4, 5, 0, 1, 3, 2, 5]
+    assert (lay["token_of_row"][9:] == -1).all()
+    # an expert range [1, 3) padded to 2 rows
+    lr = oracle.layout(_BAD_IDX, 4, e_first=1, E_local=2, align_m=2)
+    assert lr["status"] == oracle.BAD_ROUTING
+    assert list(lr["tokens_per_expert"]) == [4, 3, 1, 1]
+    assert list(lr["seg_offsets"]) == [0, 4, 6]
+    assert lr["row_of"].tolist() == [[-1, 0], [1, -1], [4, -1], [-1, 2], [-1, -1], [-1, -1]]
+    assert list(lr["token_of_row"][:6]) == [0, 1, 3, -1, 2, -1]
+    assert (lr["token_of_row"][6:] == -1).all()
+
+
+def test_layout_capacity_overflow_hand_example():
+    """Reading R7: a masked expert over capacity keeps its first `capacity`
+    tokens in token order; the count still covers every routed token."""
+    idx = np.array([[0, 1], [1, 0], [2, 0], [0, 3]], np.int32)
+    lay = oracle.layout(idx, 4, layout_kind=oracle.MASKED, capacity=2)
+    assert lay["status"] == oracle.CAPACITY
+    assert lay["rows_alloc"] == 8
+    assert list(lay["tokens_per_expert"]) == [4, 2, 1, 1]
+    assert list(lay["seg_offsets"]) == [0, 2, 4, 6, 8]
+    assert lay["row_of"].tolist() == [[0, 2], [3, 1], [4, -1], [-1, 6]]
+    assert list(lay["token_of_row"]) == [0, 1, 0, 1, 2, -1, 3, -1]
+    # with invalid slots as well: both rules apply, capacity is reported first
+    lb = oracle.layout(_BAD_IDX, 4, layout_kind=oracle.MASKED, capacity=2)
+    assert lb["status"] == oracle.CAPACITY
+    assert list(lb["tokens_per_expert"]) == [4, 3, 1, 1]
+    assert lb["row_of"].tolist() == [[0, 2], [3, 1], [4, -1], [-1, -1], [-1, -1], [6, -1]]
+    assert list(lb["token_of_row"]) == [0, 1, 0, 1, 2, -1, 5, -1]
+    # capacity 0: nothing is placed
+    l0 = oracle.layout(idx, 4, layout_kind=oracle.MASKED, capacity=0)
+    assert l0["status"] == oracle.CAPACITY and l0["rows_alloc"] == 0
+    assert (l0["row_of"] == -1).all()
+
+
+def test_layout_rejected_arguments_leave_sentinels():
+    """A rejected argument writes nothing; the wrapper's arrays then hold a
+    sentinel that no layout contains, so they cannot match a result."""
+    lay = oracle.layout(_BAD_IDX, 4, e_first=3, E_local=2)        # range beyond E
+    assert lay["status"] == oracle.BAD_ARG
+    assert (lay["row_of"] < -1).all()
+
+
 def test_permute_then_unpermute_is_identity():
     from moe_inputs import random_topk_idx
     rng = np.random.default_rng(8)
