@@ -1,17 +1,20 @@
 """Benchmark of the MoE layer local data path on one GB300 (or N replicas).
 
-Workload: fine-grained-bf16 (T=4096 tokens, D=2048, H=1408, E=64 experts,
-top-6, softmax renormalised; bf16 activations and weights, fp32
+Default workload: fine-grained-bf16 (T=4096 tokens, D=2048, H=1408, E=64
+experts, top-6, softmax renormalised; bf16 activations and weights, fp32
 accumulation), seeded synthetic inputs from moe_inputs.py, resident in HBM.
+``--workload NAME`` times another workload of moe_inputs.WORKLOADS instead
+(``--workload all``: one line per workload, in the specification's order).
 
 One step = router top-k -> permute -> grouped SwiGLU (GEMM1 + gate, GEMM2)
 -> weighted combine, issued as the four step calls of the C ABI on one
-stream.  The line reports routed tokens/s (value), the grouped GEMM's
-TFLOP/s against the measured bf16 peak (roofline), permute and combine GB/s
-(breakdown), an end-to-end figure with host buffers through the host
-pipeline, every step copying its input in and its output out (e2e; the
-one-call-at-a-time figure beside it), and the CPU oracle timed on a bounded
-sample (cpu_baseline).
+stream.  The line reports tokens/s (value: T tokens per step, each routed to
+k experts), the dominant kernel against its roof (roofline: the grouped
+SwiGLU on the tensor cores, on HBM for the masked decode layout, on the FP32
+ALUs for the fp32 workload), permute and combine GB/s (breakdown), an
+end-to-end figure with host buffers through the host pipeline, every step
+copying its input in and its output out (e2e; the one-call-at-a-time figure
+beside it), and the CPU oracle timed on a bounded sample (cpu_baseline).
 
 Multi-GPU: the path does not exchange data; each rank runs an independent
 replica on its own GPU ("scaling": "weak") and value = all ranks' tokens / the
@@ -35,10 +38,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "fine-grained-bf16"
+WORKLOAD = "fine-grained-bf16"   # the default line
 METRIC = "MoE layer routed tokens/s"
 UNIT = "tokens/s"
-L2_NOTE = "inputs larger than L2: 1.1 GB of expert weights per step, no flush"
+L2_BYTES = 129 * 1000 * 1000        # GB300 L2 (126 MiB)
+VALUE_COUNTS = ("tokens: T per step (every token routed to k experts; the expert rows per "
+                "step are T*k)")
 
 
 def dist_env():
@@ -48,15 +53,68 @@ def dist_env():
     return rank, world, local
 
 
-def algorithmic(w):
-    R = w.T * w.k
+def algorithmic(w, R=None, touched=None):
+    """Algorithmic work of one step: R routed expert rows (T*k unless given),
+    `touched` experts with at least one row (all E unless given)."""
+    R = w.T * w.k if R is None else R
+    touched = w.E if touched is None else touched
     b = 2 if w.dtype == "bf16" else 4
     return dict(
         ffn_flops=6.0 * R * w.D * w.H,
         permute_bytes=float(w.T * w.D * b + R * w.D * b),
-        # y_perm is the fp32 accumulator of the second GEMM
-        combine_bytes=float(R * w.D * 4 + w.T * w.D * b + R * 8),
+        # the method's combine bytes: y rows read once, out written once, the
+        # row index and weight of every slot
+        combine_bytes=float(R * w.D * b + w.T * w.D * b + R * 8),
+        # what the combine moves here: y_perm is the second GEMM's fp32 accumulator
+        combine_bytes_moved=float(R * w.D * 4 + w.T * w.D * b + R * 8),
+        # the grouped call when it streams weights (masked decode): the touched
+        # experts' w1, w3, w2 once, x_perm rows read, h written and read, y written
+        grouped_bytes=float(touched * 3 * w.D * w.H * b + R * w.D * b + 2 * R * w.H * b
+                            + R * w.D * 4),
+        weight_bytes=float(w.E * 3 * w.D * w.H * b),
     )
+
+
+def workload_config(moe, w):
+    """The C ABI configuration of a workload (its layout, router and dtype)."""
+    return moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k,
+                      dtype=moe.MOE_F32 if w.dtype == "f32" else moe.MOE_BF16,
+                      score=moe.MOE_SCORE_SOFTMAX if w.score == "softmax" else moe.MOE_SCORE_SIGMOID,
+                      renorm=int(w.renorm),
+                      layout=moe.MOE_LAYOUT_MASKED if w.layout == "masked"
+                      else moe.MOE_LAYOUT_CONTIGUOUS,
+                      align_m=128, capacity=w.T if w.layout == "masked" else 0,
+                      n_group=w.n_group, topk_group=w.topk_group)
+
+
+def needs_l2_flush(w):
+    """Whether one step's inputs fit in L2 (then every timed step is preceded
+    by an L2 flush and timed on its own)."""
+    return algorithmic(w)["weight_bytes"] < 2 * L2_BYTES
+
+
+def l2_note(w):
+    if needs_l2_flush(w):
+        return ("L2 flushed (256 MB write) before every timed step; each step timed between "
+                "its own CUDA events")
+    gb = algorithmic(w)["weight_bytes"] / 1e9
+    return f"inputs larger than L2: {gb:.1f} GB of expert weights per step, no flush"
+
+
+def workload_data_note(w):
+    return (f"synthetic (seeded N(0,1) activations, N(0,{w.wstd}) weights"
+            + (", Zipf(1.2)-shaped router bias" if w.zipf_s else "") + ")")
+
+
+def router_note(w):
+    r = f"{w.score}, renormalised over top-k" if w.renorm else f"{w.score}, not renormalised"
+    if w.n_group:
+        r += f", {w.topk_group} of {w.n_group} groups"
+    return r
+
+
+def layout_note(w):
+    return ("masked, capacity = T" if w.layout == "masked" else "contiguous, align_m=128")
 
 
 def max_over_ranks(value_ms, dev):
@@ -83,27 +141,47 @@ def load_peaks():
         d = json.load(open(p))
         return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
                     bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                    source="measured")
-    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+                    sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                sm_max_mhz=2070.0, source="fallback")
 
 
-def kernel_source_hash():
+# grouped SwiGLU kernel that dominates each workload's step, and its sources
+GROUPED_KERNEL = {
+    "tiny-fp32": ("grouped_f32_kernel (fp32 SIMT FFMA, GEMM1 + SwiGLU and GEMM2)",
+                  ("grouped_f32.cu", "common.cuh")),
+    "decode-masked": ("grouped_tc_kernel (tcgen05, one CTA per 128x256 tile, masked tile table)",
+                      ("grouped_tc.cu", "common.cuh")),
+}
+PAIR_KERNEL = ("grouped_pair_kernel (tcgen05 cta_group::2, GEMM1 + SwiGLU, GEMM2)",
+               ("grouped_tc2.cu", "common.cuh"))
+
+
+def grouped_kernel(workload):
+    return GROUPED_KERNEL.get(workload, PAIR_KERNEL)
+
+
+def kernel_source_hash(workload=WORKLOAD):
     h = hashlib.sha256()
-    for f in ("grouped_tc2.cu", "common.cuh"):
+    for f in grouped_kernel(workload)[1]:
         h.update(open(os.path.join(ROOT, "routing_grouped_gemm_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the grouped GEMM from a committed ncu summary,
-    only if it was taken on the current kernel source."""
+def recorded_traffic(workload=WORKLOAD):
+    """DRAM bytes per call of the grouped SwiGLU from a committed ncu summary
+    (profiles/grouped_swiglu_traffic.json, one entry per workload), only if it
+    was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "grouped_swiglu_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("kernel_source_hash") != kernel_source_hash() or d.get("workload") != WORKLOAD:
+    entry = d.get(workload) if isinstance(d, dict) else None
+    if not isinstance(entry, dict):
         return None
-    return d.get("dram_bytes_per_call")
+    if entry.get("kernel_source_hash") != kernel_source_hash(workload):
+        return None
+    return entry.get("dram_bytes_per_call")
 
 
 class ClockSampler:
@@ -163,29 +241,60 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_tokens_per_s(inp_host, w, n_tokens, seed=0, nthreads=None):
-    """Time the oracle's whole layer (router + per-token experts) on a sample."""
+def oracle_tokens_per_s(x, wg, bias, expert, w, n_tokens, seed=0, nthreads=None):
+    """Time the oracle's whole layer (router + per-token experts) on a sample
+    of n_tokens tokens.  x, wg: host arrays; bias: host fp64 or None;
+    expert(e) -> host (w1[e], w3[e], w2[e]).  Only the experts the sample
+    reaches are fetched, before the timed part."""
     import numpy as np
     import oracle
-    x, wg, w1, w3, w2 = inp_host
     rng = np.random.default_rng(seed)
     toks = np.sort(rng.choice(w.T, size=n_tokens, replace=False)).astype(np.int32)
     nth = nthreads or oracle.default_threads()
-    t0 = time.perf_counter()
+    score = oracle.SOFTMAX if w.score == "softmax" else oracle.SIGMOID
     xs = x[toks]
-    _, _, idx, wts, _ = oracle.route(xs, wg, None, w.k,
-                                     oracle.SOFTMAX if w.score == "softmax" else oracle.SIGMOID,
-                                     w.renorm, nthreads=nth)
-    oracle.moe_tokens(np.arange(n_tokens), xs, list(w1), list(w3), list(w2), idx, wts,
+    _, _, idx, _, _ = oracle.route(xs, wg, bias, w.k, score, w.renorm, nthreads=nth,
+                                   n_group=w.n_group, topk_group=w.topk_group)
+    used = sorted(set(int(e) for e in np.unique(idx)))
+    w1s, w3s, w2s = [None] * w.E, [None] * w.E, [None] * w.E
+    for e in used:
+        w1s[e], w3s[e], w2s[e] = expert(e)
+    t0 = time.perf_counter()
+    _, _, idx, wts, _ = oracle.route(xs, wg, bias, w.k, score, w.renorm, nthreads=nth,
+                                     n_group=w.n_group, topk_group=w.topk_group)
+    oracle.moe_tokens(np.arange(n_tokens), xs, w1s, w3s, w2s, idx, wts,
                       round_h=(w.dtype == "bf16"), nthreads=nth)
     dt = time.perf_counter() - t0
     return n_tokens / dt, dt, nth
 
 
-def host_inputs(inp):
+def host_router_inputs(inp):
+    """Host copies of x, W_g and the bias (fp64) in the oracle's conventions."""
+    import numpy as np
     import moe_inputs
     H = moe_inputs.host_array
-    return H(inp.x), H(inp.wg), H(inp.w1), H(inp.w3), H(inp.w2)
+    bias = None if inp.bias is None else inp.bias.detach().cpu().numpy().astype(np.float64)
+    return H(inp.x), H(inp.wg), bias
+
+
+def host_expert(inp):
+    """expert(e) -> host copies of the GPU's w1[e], w3[e], w2[e]."""
+    import moe_inputs
+    H = moe_inputs.host_array
+    return lambda e: (H(inp.w1[e]), H(inp.w3[e]), H(inp.w2[e]))
+
+
+def cpu_baseline(inp, w, seconds, seed=7):
+    """The oracle as it stands on a token sample sized to about `seconds`."""
+    x, wg, bias = host_router_inputs(inp)
+    expert = host_expert(inp)
+    tps, _, nth = oracle_tokens_per_s(x, wg, bias, expert, w, min(w.T, 16), seed=99)
+    n = int(max(16, min(w.T, tps * seconds)))
+    tps, dt, nth = oracle_tokens_per_s(x, wg, bias, expert, w, n, seed=seed)
+    return {"value": tps, "unit": UNIT, "cores": nth, "kind": "oracle",
+            "sample": f"{n} sampled tokens of the {w.name} batch, router + per-token experts in "
+                      f"fp64 ({dt:.1f} s)",
+            "cpu": cpu_model()}
 
 
 def cpu_model():
@@ -199,35 +308,51 @@ def cpu_model():
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle as it stands, on the host cores."""
+    """Reference arm: the CPU oracle as it stands, on the host cores, on a
+    bounded token sample of the workload per step."""
     import torch
     import moe_inputs
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = moe_inputs.WORKLOADS[WORKLOAD]
-    inp = moe_inputs.make_inputs(w, device="cpu", seed=0)
-    hin = host_inputs(inp)
+    name = getattr(args, "workload", None) or WORKLOAD
+    if name == "all":
+        name = WORKLOAD
+    w = moe_inputs.WORKLOADS[name]
+    inp = moe_inputs.make_inputs(w, device="cpu", seed=0, weights=False)
+    x, wg, bias = host_router_inputs(inp)
+    cache = {}
+
+    def expert(e):
+        # the weights of the experts the samples reach, drawn on the host
+        # with the workload's distribution
+        if e not in cache:
+            cache[e] = tuple(moe_inputs.host_array(t) for t in moe_inputs.expert_weights(w, e))
+        return cache[e]
+
     # calibrate so the whole run stays within about two minutes
-    tps, _, nth = oracle_tokens_per_s(hin, w, 16, seed=99)
+    tps, _, nth = oracle_tokens_per_s(x, wg, bias, expert, w, min(w.T, 16), seed=99)
     budget_s = 120.0
     per_step = max(1, min(w.T, int(tps * budget_s / max(1, args.steps + args.warmup))))
     for i in range(args.warmup):
-        oracle_tokens_per_s(hin, w, per_step, seed=i)
+        oracle_tokens_per_s(x, wg, bias, expert, w, per_step, seed=i)
     times = []
     for i in range(args.steps):
-        _, dt, _ = oracle_tokens_per_s(hin, w, per_step, seed=1000 + i)
+        _, dt, _ = oracle_tokens_per_s(x, wg, bias, expert, w, per_step, seed=1000 + i)
         times.append(dt)
     total = sum(times)
     value = per_step * args.steps / total
-    sample = f"{per_step} sampled tokens per step of the {WORKLOAD} batch (router + per-token experts)"
+    sample = (f"{per_step} sampled tokens per step of the {name} batch of {w.T} "
+              f"(router + per-token experts in fp64)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * total / args.steps * (w.T / per_step),
+        # measured: the mean time of one timed step, i.e. of `per_step` tokens
+        "ms_per_step": 1e3 * total / args.steps,
+        "tokens_per_step": per_step, "value_counts": VALUE_COUNTS,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
+        "config": {"workload": name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
                    "parallelism": "replicas" if world > 1 else "single", "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle",
                          "sample": sample, "cpu": cpu_model()},
@@ -248,9 +373,10 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
     through moe_layer_forward_host, one step at a time on one stream."""
     import torch
     w = inp.w
-    e_steps = max(10, args.steps // 4)
+    e_steps = args.steps  # the same number of timed steps as the device-resident loop
     x_host = inp.x.cpu().pin_memory()
-    out_host = torch.empty((w.T, w.D), dtype=torch.bfloat16).pin_memory()
+    out_host = torch.empty((w.T, w.D), dtype=inp.x.dtype).pin_memory()
+    eb = inp.x.element_size()
 
     # single call: copy in, layer, copy out, all on `stream`
     lws = moe.alloc_workspace(cfg, host=True, device=dev)
@@ -296,8 +422,8 @@ def run_e2e(moe, cfg, inp, out, stream, dev, world, args):
     finally:
         pipe.close()
     return {"value": replica_tokens_per_s(world, w.T, piped_ms), "unit": UNIT,
-            "h2d_bytes_per_step": int(x_host.numel() * 2),
-            "d2h_bytes_per_step": int(out_host.numel() * 2),
+            "h2d_bytes_per_step": int(x_host.numel() * eb),
+            "d2h_bytes_per_step": int(out_host.numel() * eb),
             "ms_per_step": piped_ms, "steps": e_steps,
             "api": "moe_host_pipeline (C ABI, depth 2): every step copies its pinned x in and its "
                    "output out on the pipeline's copy streams, overlapping the neighbouring steps' "
@@ -475,7 +601,44 @@ def run_backward(moe, cfg, inp, stream, dev, args, peaks):
             "launches_per_forward_and_backward": launches}
 
 
-def run_gpu(args):
+def roofline(w, moe, cfg, gemm_ms, R, touched, peaks, gemm_launches, dev):
+    """The dominant kernel of the step (the grouped SwiGLU call) against its
+    roof: the bf16 tensor peak, HBM for the masked decode layout (it streams
+    the touched experts' weights once), the FP32 FFMA rate for fp32."""
+    import torch
+    alg = algorithmic(w, R, touched)
+    name = grouped_kernel(w.name)[0]
+    kernel = f"{name}: {gemm_launches} launch{'es' if gemm_launches != 1 else ''} per call"
+    if w.layout == "masked":
+        achieved = alg["grouped_bytes"] / (gemm_ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": f"{peaks['source']} copy bandwidth",
+                "traffic": recorded_traffic(w.name),
+                "algorithmic_bytes_per_call": alg["grouped_bytes"],
+                "algorithmic_bytes_note": "touched experts' w1, w3, w2 once + x_perm rows read + "
+                                          "h written and read + fp32 y written",
+                "touched_experts": touched, "tflops": alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12}
+    achieved = alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12
+    if w.dtype == "f32":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12   # FFMA lanes x 2 FLOP x clock
+        return {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {peaks['sm_max_mhz']:.0f} MHz",
+                "traffic": recorded_traffic(w.name),
+                "algorithmic_flops_per_call": alg["ffn_flops"],
+                "note": "0.1 GFLOP per call: bound by launch and pipeline latency, not by the ALUs"}
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"],
+            "peak_source": f"{peaks['source']} bf16 burst",
+            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+            "traffic": recorded_traffic(w.name),
+            "algorithmic_flops_per_call": alg["ffn_flops"]}
+
+
+def run_gpu(args, name):
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -484,35 +647,29 @@ def run_gpu(args):
     import routing_grouped_gemm_gb300 as moe
 
     rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    w = moe_inputs.WORKLOADS[WORKLOAD]
+    w = moe_inputs.WORKLOADS[name]
     if args.scale:
         # a reduced case of the same workload (profiling captures only)
         over = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.scale.split(",")}
         w = w.scaled(**over)
+    default = name == WORKLOAD
     inp = moe_inputs.make_inputs(w, device=dev, seed=rank)
-    cfg = moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k, dtype=moe.MOE_BF16,
-                     score=moe.MOE_SCORE_SOFTMAX, renorm=1, align_m=128)
+    cfg = workload_config(moe, w)
+    dt = moe_inputs.torch_dtype(w)
     if args.fp8_only:
         fp8 = run_fp8(moe, cfg, inp, torch.cuda.current_stream(dev), dev, args, load_peaks())
         if rank == 0:
-            print(json.dumps({"workload": WORKLOAD, "fp8": fp8}), flush=True)
-        if world > 1:
-            dist.destroy_process_group()
+            print(json.dumps({"workload": name, "fp8": fp8}), flush=True)
         return
     if args.backward_only:
         backward = run_backward(moe, cfg, inp, torch.cuda.current_stream(dev), dev, args,
                                 load_peaks())
         if rank == 0:
-            print(json.dumps({"workload": WORKLOAD, "scale": args.scale or None,
+            print(json.dumps({"workload": name, "scale": args.scale or None,
                               "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
                               "backward": backward}), flush=True)
-        if world > 1:
-            dist.destroy_process_group()
         return
     ra = moe.rows_alloc(cfg)
     ws = moe.alloc_workspace(cfg, device=dev)
@@ -520,14 +677,15 @@ def run_gpu(args):
     topk_idx = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
     topk_w = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
     tpe = torch.empty(w.E, dtype=torch.int32, device=dev)
-    seg = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    seg = torch.empty(cfg.e_local + 1, dtype=torch.int32, device=dev)
     row_of = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
     tor = torch.empty(ra, dtype=torch.int32, device=dev)
-    x_perm = torch.empty((ra, w.D), dtype=torch.bfloat16, device=dev)
-    h = torch.empty((ra, w.H), dtype=torch.bfloat16, device=dev)
+    x_perm = torch.empty((ra, w.D), dtype=dt, device=dev)
+    h = torch.empty((ra, w.H), dtype=dt, device=dev)
     y_perm = torch.empty((ra, w.D), dtype=torch.float32, device=dev)
-    out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((w.T, w.D), dtype=dt, device=dev)
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev) if needs_l2_flush(w) else None
 
     def step(ev=None):
         if ev is not None:
@@ -558,23 +716,37 @@ def run_gpu(args):
 
     # the timed loop has events only at its two ends: events between the
     # calls would cut the programmatic launch overlap of consecutive kernels;
-    # the per-call breakdown comes from a second, separately timed loop
+    # the per-call breakdown comes from a second, separately timed loop.
+    # Where the inputs fit in L2, every step is timed on its own after a flush.
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
         n_launch0 = moe.kernel_launches()
-        for i in range(args.steps):
-            step()
-        n_launches = moe.kernel_launches() - n_launch0
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
+        if flush is None:
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for i in range(args.steps):
+                step()
+            t_end.record(stream)
+            n_launches = moe.kernel_launches() - n_launch0
+            torch.cuda.synchronize(dev)
+            local_ms = t_start.elapsed_time(t_end)
+        else:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush.zero_()
+                evs[i][0].record(stream)
+                step()
+                evs[i][1].record(stream)
+            n_launches = moe.kernel_launches() - n_launch0
+            torch.cuda.synchronize(dev)
+            local_ms = sum(a.elapsed_time(b) for a, b in evs)
     if world > 1:
         dist.barrier()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    elapsed_ms = max_over_ranks(local_ms, dev)
     st = moe.moe_get_device_status(ws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
@@ -582,6 +754,8 @@ def run_gpu(args):
     n_parts = max(20, args.steps // 4)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_parts)]
     for i in range(n_parts):
+        if flush is not None:
+            flush.zero_()
         step(evs[i])
     torch.cuda.synchronize(dev)
     parts = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
@@ -589,72 +763,78 @@ def run_gpu(args):
     ms_per_step = elapsed_ms / args.steps
     value = replica_tokens_per_s(world, w.T, ms_per_step)
 
-    # end to end: moe_layer_forward with pinned host input / output each step
+    # end to end: host x in and host out every step, through the C ABI
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(moe, cfg, inp, out, stream, dev, world, args)
-    fused = None
-    if not args.no_fused:
+    fused = fp8 = backward = None
+    if default and not args.no_fused:
         fused = run_fused(moe, cfg, inp, stream, dev, args)
-    fp8 = None
-    if not args.no_fp8:
+    if default and not args.no_fp8:
         fp8 = run_fp8(moe, cfg, inp, stream, dev, args, load_peaks())
-    backward = None
-    if not args.no_backward:
+    if default and not args.no_backward:
         backward = run_backward(moe, cfg, inp, stream, dev, args, load_peaks())
-    alg = algorithmic(w)
+    tpe_h = tpe.cpu().numpy()
+    local_cnt = tpe_h[cfg.e_first:cfg.e_first + cfg.e_local]
+    R = int(np.minimum(local_cnt, cfg.capacity).sum() if w.layout == "masked" else local_cnt.sum())
+    touched = int((local_cnt > 0).sum())
+    alg = algorithmic(w, R, touched)
     peaks = load_peaks()
     gemm_ms = float(mean_parts[2])
-    achieved = alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12
-    tpe_h = tpe.cpu().numpy()
+    roof = roofline(w, moe, cfg, gemm_ms, R, touched, peaks, gemm_launches, dev)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
-        "config": {"workload": WORKLOAD, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
-                   "router": "softmax, renormalised over top-k", "layout": "contiguous, align_m=128",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single", "l2": L2_NOTE},
-        "roofline": {"kernel": "grouped SwiGLU on CTA pairs (GEMM1 + SwiGLU, GEMM2): "
-                               f"{gemm_launches} launch{'es' if gemm_launches != 1 else ''} per call",
-                     "bound": "tensor", "achieved": achieved,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"],
-                     "peak_source": f"{peaks['source']} bf16 burst",
-                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "traffic": recorded_traffic(),
-                     "algorithmic_flops_per_call": alg["ffn_flops"]},
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": workload_data_note(w),
+        "value_counts": VALUE_COUNTS, "tokens_per_step": w.T, "routed_rows_per_step": R,
+        "config": {"workload": name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
+                   "router": router_note(w), "layout": layout_note(w),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single", "l2": l2_note(w)},
+        "roofline": roof,
         "breakdown_ms": {"route": float(mean_parts[0]), "permute": float(mean_parts[1]),
                          "grouped_swiglu": gemm_ms, "combine": float(mean_parts[3])},
         "bandwidth": {
             "permute_gbs": alg["permute_bytes"] / (mean_parts[1] * 1e-3) / 1e9,
             "combine_gbs": alg["combine_bytes"] / (mean_parts[3] * 1e-3) / 1e9,
+            "combine_gbs_moved": alg["combine_bytes_moved"] / (mean_parts[3] * 1e-3) / 1e9,
+            "combine_note": "combine_gbs counts the method's bytes (y rows at the activation "
+                            "width); combine_gbs_moved counts the fp32 y_perm actually read",
             "hbm_peak_gbs": peaks["hbm_gbs"]},
-        "gemm_tflops": achieved,
+        "gemm_tflops": alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12,
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
                               "zeros": int((tpe_h == 0).sum())},
         "e2e": e2e,
-        "fused_combine": fused,
-        "fp8": fp8,
-        "backward": backward,
         "gpu_launches": n_launches,
         "clocks": clk.summary(),
     }
+    if default:
+        line.update({"fused_combine": fused, "fp8": fp8, "backward": backward})
 
     if rank == 0 and not args.no_cpu_baseline:
-        hin = host_inputs(inp)
-        tps, _, nth = oracle_tokens_per_s(hin, w, 16, seed=99)
-        n = int(max(16, min(w.T, tps * args.cpu_seconds)))
-        tps, dt, nth = oracle_tokens_per_s(hin, w, n, seed=7)
-        line["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": nth, "kind": "oracle",
-                                "sample": f"{n} sampled tokens of the {WORKLOAD} batch, router + "
-                                          f"per-token experts in fp64 ({dt:.1f} s)",
-                                "cpu": cpu_model()}
+        line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+    del inp, ws, x_perm, h, y_perm, out, flush
+    torch.cuda.empty_cache()
+
+
+def run_gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+    import moe_inputs
+    rank, world, local = dist_env()
     if world > 1:
-        dist.destroy_process_group()
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    try:
+        names = moe_inputs.WORKLOAD_ORDER if args.workload == "all" else [args.workload]
+        for name in names:
+            run_gpu(args, name)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
 
 
 def run_dispatch_bandwidth(args):
@@ -727,6 +907,8 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="a workload of moe_inputs.WORKLOADS, or 'all' (one line each)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
@@ -743,6 +925,11 @@ def main():
     args = ap.parse_args()
     if args.scale and not args.backward_only:
         ap.error("--scale is for --backward-only profiling runs")
+    import moe_inputs
+    if args.workload != "all" and args.workload not in moe_inputs.WORKLOADS:
+        ap.error(f"unknown workload {args.workload!r}")
+    if (args.fp8_only or args.backward_only) and args.workload != WORKLOAD:
+        ap.error("--fp8-only and --backward-only time the default workload")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
@@ -750,7 +937,7 @@ def main():
     elif args.dispatch_bandwidth:
         run_dispatch_bandwidth(args)
     else:
-        run_gpu(args)
+        run_gpu_arm(args)
 
 
 if __name__ == "__main__":

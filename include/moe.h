@@ -453,7 +453,10 @@ moe_status moe_layer_forward_fused(const moe_config *cfg, const void *x, const v
  *     The caller zeroes it; moe_get_device_status does not see these flags.
  *   The first call on each device looks up the array's device address
  *     (with that device current); make that first call before any stream
- *     capture.
+ *     capture.  The address is looked up again when the device's current
+ *     context is not the one it was taken in (after cudaDeviceReset the
+ *     library's module, and the array with it, load anew); a call made
+ *     under stream capture after such a reset is not supported.
  *   Every call shares the one array and leaves its contents behind; the
  *     one word that must be zero between calls (a completion ticket) starts
  *     at zero when the library loads and every call returns it to zero.
@@ -469,7 +472,9 @@ moe_status moe_permute_noalloc(const moe_config *cfg, const void *x, const int32
 /*
  * Synchronises `stream`, reads the workspace status word, clears it and
  * returns the most serious flagged condition (MOE_OK if none).  Order:
- * TIMEOUT, CAPACITY, BAD_ROUTING.
+ * TIMEOUT, then MOE_ERR_CUDA for a kernel that found itself launched
+ * without the thread-block cluster it needs (it did no work), then
+ * CAPACITY, BAD_ROUTING.
  */
 moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream);
 

@@ -130,6 +130,22 @@ def zipf_bias(w: Workload, device, seed: int) -> torch.Tensor:
     return b.to(torch.float32).to(device)
 
 
+def expert_weights(w: Workload, e: int, device="cpu", seed: int = 0):
+    """w1[e], w3[e], w2[e] drawn alone, with the workload's distribution.
+
+    Each expert here has its own generator streams, so any subset of experts
+    can be drawn without the others (used where only the experts a token
+    sample reaches are needed).  The values are not those make_inputs()
+    gives expert e; only the distribution is the same.
+    """
+    dt = torch_dtype(w)
+    out = []
+    for sid, shape in ((STREAM_W1, (w.H, w.D)), (STREAM_W3, (w.H, w.D)), (STREAM_W2, (w.D, w.H))):
+        g = _gen(device, seed * 4099 + e + 1, 100 + sid)
+        out.append(_normal(shape, w.wstd, g, device, dt))
+    return tuple(out)
+
+
 def make_inputs(w: Workload, device="cpu", seed: int = 0, weights: bool = True) -> Inputs:
     dt = torch_dtype(w)
     x = _normal((w.T, w.D), 1.0, _gen(device, seed, STREAM_X), device, dt)

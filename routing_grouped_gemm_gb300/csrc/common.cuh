@@ -12,6 +12,7 @@ enum : int {
     FLAG_BAD_ROUTING = 1,
     FLAG_CAPACITY = 2,
     FLAG_TIMEOUT = 4,
+    FLAG_LAUNCH = 8,  // a kernel found itself launched in a shape it cannot run (no work done)
 };
 
 // Status block at the start of every workspace.
@@ -33,6 +34,17 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// After an abort, bulk copies a CTA issued for pipeline stages that no
+// consumer will wait for may still be landing in its shared memory.  They
+// take microseconds; the CTA waits this long (%globaltimer) before it meets
+// its peer and exits, so none lands in shared memory the CTA no longer owns.
+constexpr unsigned long long kSettleNs = 100ull * 1000ull;  // 100 us
+
+__device__ __forceinline__ void settle_inflight_copies() {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kSettleNs) __nanosleep(1000);
 }
 
 // Programmatic dependent launch.  A kernel launched with programmatic stream
@@ -273,6 +285,12 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
 // ---------------------------------------------------------------------
 // CTA pairs (cluster of 2) for cta_group::2
 // ---------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -457,6 +457,9 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     tc_fence_before();
     __syncthreads();
+    // after an abort this CTA's producer may have loads in flight for stages
+    // the MMA warp never consumed; the peer waits at the cluster barrier too
+    if (threadIdx.x == 0 && *abort_flag) settle_inflight_copies();
     cluster_sync();  // the leader's MMAs (which read both CTAs' smem) are done
     if (threadIdx.x == 0 && *abort_flag) {
         raise_flag(p.status, FLAG_TIMEOUT);

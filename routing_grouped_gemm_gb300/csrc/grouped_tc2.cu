@@ -195,6 +195,13 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     const PairParams p) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
+    // Every role below assumes a cluster of two CTAs (pair MMAs, the peer's
+    // barriers, paired TMEM allocation).  A launch in any other shape does no
+    // work and reports it instead of reaching an instruction it cannot run.
+    if (cluster_nctarank() != 2) {
+        if (threadIdx.x == 0) raise_flag(p.status, FLAG_LAUNCH);
+        return;
+    }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -680,6 +687,9 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         bulk_wait_group_all();  // every y store has landed before the CTA exits
     tc_fence_before();
     __syncthreads();
+    // after an abort this CTA's producer may have loads in flight for stages
+    // the MMA warp never consumed; the peer waits at the cluster barrier too
+    if (threadIdx.x == 0 && *abort_flag) settle_inflight_copies();
     cluster_sync();  // the leader's MMAs (which read both CTAs' smem) are done
     if (threadIdx.x == 0 && *abort_flag) {
         raise_flag(p.status, FLAG_TIMEOUT);

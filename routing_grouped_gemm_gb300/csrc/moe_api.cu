@@ -925,6 +925,11 @@ MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe
         snprintf(g_last_error, sizeof g_last_error, "bounded device wait ran out (CTA %d)", host[1] - 1);
         return MOE_ERR_TIMEOUT;
     }
+    if (host[0] & moe::FLAG_LAUNCH) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "a kernel was launched without the thread-block cluster it needs; no work done");
+        return MOE_ERR_CUDA;
+    }
     if (host[0] & moe::FLAG_CAPACITY) return MOE_ERR_CAPACITY;
     if (host[0] & moe::FLAG_BAD_ROUTING) return MOE_ERR_BAD_ROUTING;
     return MOE_OK;

@@ -20,6 +20,7 @@
 // overlap on the GPU (different streams, or different host threads without
 // ordering) race on it and produce wrong permutations; issue them in order
 // on one stream, or use moe_permute with separate workspaces instead.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -42,23 +43,49 @@ static __device__ __align__(256) int g_noalloc_scratch[kNoAllocScratchInts];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 int *g_scratch_addr[kMaxDevices] = {nullptr};
+CUcontext g_scratch_ctx[kMaxDevices] = {nullptr};
 
 void fail(const char *msg) { moe::set_last_error(msg); }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// The context current on the calling thread (null if the driver entry point
+// is unavailable).  Taken through the runtime's driver entry-point query, so
+// the library does not link the driver library itself.
+CUcontext current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    }
+    CUcontext c = nullptr;
+    if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+    return c;
+}
+
 // Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current).  In host code the name
-// g_noalloc_scratch is only a host-side stand-in, never a device address.
+// per device (with that device current) and again whenever the device's
+// current context is not the one the address was taken in (the module, and
+// with it the array, is loaded anew into a context created after
+// cudaDeviceReset).  In host code the name g_noalloc_scratch is only a
+// host-side stand-in, never a device address.
 cudaError_t scratch_address(int **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    const CUcontext ctx = current_context();
+    if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = static_cast<int *>(p);
+        g_scratch_ctx[dev] = current_context();
     }
     *out = g_scratch_addr[dev];
     return cudaSuccess;

@@ -489,6 +489,8 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     if (threadIdx.x == 0 && *abort_flag) {
         raise_flag(p.status, FLAG_TIMEOUT);
         atomicCAS(p.status + 1, 0, 1 + blockIdx.x);
+        // loads issued for stages the MMA warp never consumed land first
+        settle_inflight_copies();
     }
     if (warp == 1) {
         tc_fence_after();

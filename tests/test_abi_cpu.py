@@ -207,3 +207,20 @@ def test_permute_noalloc_rejects_problems_beyond_its_scratch_on_the_host(moe):
     bad = _cfg(moe, k=0).c()
     assert lib.moe_permute_noalloc(ctypes.byref(bad), 0, 0, 0, 0, 0, 0, 0, None, None) == \
         moe.MOE_ERR_INVALID_ARG
+
+
+def test_noalloc_permute_limit_checked_on_the_host(moe):
+    """moe_permute_noalloc refuses, before any launch or pointer check, a
+    problem one 256-token count block past its fixed array; the largest
+    problem that fits gets past the limit (and then fails on the NULL
+    tensors, still on the host)."""
+    lib = moe._lib
+    over = _cfg(moe, T=131072 + 256, D=64, E=256, k=1).c()
+    st = lib.moe_permute_noalloc(ctypes.byref(over), None, None, None, None, None, None, None,
+                                 None, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+    assert "fixed scratch" in moe.last_error_string()
+    fits = _cfg(moe, T=131072, D=64, E=256, k=1).c()
+    st = lib.moe_permute_noalloc(ctypes.byref(fits), None, None, None, None, None, None, None,
+                                 None, None)
+    assert st == moe.MOE_ERR_INVALID_ARG

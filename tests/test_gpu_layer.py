@@ -12,8 +12,8 @@ import torch
 
 import moe_inputs
 import oracle
-from helpers import (cfg_for, check_layout_properties, oracle_out_tokens, oracle_route, rel_err,
-                     routing_agreement, to_f64, tol)
+from helpers import (cfg_for, check_layout_properties, oracle_out_tokens, oracle_route, oscore,
+                     rel_err, routing_agreement, to_f64, tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -377,6 +377,23 @@ def test_layer_full_size_sampled(moe, name, n_sample):
     out, views, ws = run_layer(moe, cfg, inp)
     check_against_oracle(moe, w, inp, out, views, n_sample, seed=1)
     idx = views["topk_idx"].cpu().numpy()
+    # whole-batch routing: the router call on the same inputs returns the
+    # layer's top-k and its fp32 logits; the oracle's selection on those
+    # logits is the same for every token, and so are the weights
+    logits = torch.empty((w.T, w.E), dtype=torch.float32, device="cuda")
+    gidx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gw = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    rws = moe.alloc_workspace(cfg)
+    moe.moe_route_topk(cfg, inp.x, inp.wg, inp.bias, logits, gidx, gw, rws)
+    assert moe.moe_get_device_status(rws) == moe.MOE_OK
+    assert np.array_equal(gidx.cpu().numpy(), idx)
+    assert torch.equal(gw, views["topk_w"])
+    keys = logits.cpu().numpy()
+    oidx, st = oracle.topk(keys, w.k, w.n_group, w.topk_group)
+    assert st == oracle.OK
+    assert np.array_equal(idx, oidx)
+    ow = oracle.topk_weights(keys, oidx, oscore(w), w.renorm)
+    np.testing.assert_allclose(gw.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
     cnt = views["tokens_per_expert"].cpu().numpy()
     assert int(cnt.sum()) == w.T * w.k
     lay = (cnt, views["seg_offsets"].cpu().numpy(), views["row_of"].cpu().numpy(),

@@ -67,6 +67,47 @@ def test_route_exact_logits_bitexact(moe, dt, score, renorm, n_group, topk_group
     np.testing.assert_allclose(gw.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("T,D,E,k,score", [
+    (4096, 2048, 64, 6, "softmax"),    # 32 m-tiles: the D reduction split 4 ways per cluster
+    (4096, 1024, 256, 8, "sigmoid"),
+    (8192, 1024, 64, 6, "softmax"),    # 64 m-tiles: 2 splits
+    (8192, 1024, 256, 8, "sigmoid"),
+    (16384, 512, 64, 8, "softmax"),    # 128 m-tiles: 1 split
+    (16384, 512, 256, 8, "sigmoid"),
+])
+@pytest.mark.parametrize("mode", ["cluster", "split"])
+def test_route_exact_logits_full_batch_sizes(moe, T, D, E, k, score, mode, monkeypatch):
+    """The batch sizes of the bf16 workloads, where the router splits the D
+    reduction 4, 2 or 1 ways: on exact-integer inputs the fp32 logits, the
+    whole batch's top-k and the weights equal the oracle's (one cluster launch
+    and the two-kernel form)."""
+    if mode == "split":
+        monkeypatch.setenv("MOE_ROUTER_KERNEL", "split")
+    x, wg = moe_inputs.exact_router_inputs(T, D, E, seed=T + E)
+    bias = ((np.arange(E) * 7) % 9 - 4).astype(np.float32) / 4.0
+    renorm = True
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
+                     score=moe.MOE_SCORE_SOFTMAX if score == "softmax" else moe.MOE_SCORE_SIGMOID,
+                     renorm=int(renorm))
+    ws = moe.alloc_workspace(cfg)
+    logits = torch.full((T, E), float("nan"), device="cuda")
+    gidx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    gw = torch.full((T, k), float("nan"), device="cuda")
+    moe.moe_route_topk(cfg, _dev(x, torch.bfloat16), _dev(wg, torch.bfloat16), _dev(bias),
+                       logits, gidx, gw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    ref = oracle.router_logits(x, wg, bias.astype(np.float64))
+    keys = ref.astype(np.float32)
+    assert np.array_equal(logits.cpu().numpy(), keys)                    # exact
+    oidx, st = oracle.topk(keys, k)
+    assert st == oracle.OK
+    assert sum(len(set(keys[t])) < E for t in range(0, T, 16)) > T // 64   # ties occur
+    assert np.array_equal(gidx.cpu().numpy(), oidx)                       # whole batch
+    ow = oracle.topk_weights(keys, oidx, oracle.SOFTMAX if score == "softmax" else oracle.SIGMOID,
+                             renorm)
+    np.testing.assert_allclose(gw.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+
+
 @pytest.mark.parametrize("name", moe_inputs.WORKLOAD_ORDER)
 def test_route_workload_shapes(moe, name):
     """Config-shaped random inputs: logits within tolerance, selection valid."""
@@ -311,53 +352,72 @@ def test_permute_masked_and_capacity(moe):
                  (tor, "token_of_row")):
         assert np.array_equal(a, lay[b])
     check_layout_properties(idx, (tpe, seg, row_of, tor), E, 0, E, masked_cap=cap)
-    # capacity exceeded: first `cap2` tokens kept per expert, the rest dropped and flagged
+    # capacity exceeded (reading R7): the first `cap2` tokens of each expert
+    # kept, the rest dropped and flagged -- the oracle's layout bit for bit
     cap2 = int(np.median(cnt))
     cfg2 = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
                       layout=moe.MOE_LAYOUT_MASKED, capacity=cap2)
-    st2, tpe2, seg2, row2, tor2, _ = _run_permute(moe, cfg2, x, idx)
+    st2, tpe2, seg2, row2, tor2, xp2 = _run_permute(moe, cfg2, x, idx)
+    lay2 = oracle.layout(idx, E, 0, E, oracle.MASKED, 1, cap2)
+    assert lay2["status"] == oracle.CAPACITY
     assert st2 == moe.MOE_ERR_CAPACITY
-    assert np.array_equal(tpe2, cnt)
-    for e in range(E):
-        toks = np.nonzero((idx == e).any(1))[0]
-        kept = toks[:cap2]
-        assert np.array_equal(tor2[e * cap2:e * cap2 + len(kept)], kept)
-        for t in toks[cap2:]:
-            j = int(np.nonzero(idx[t] == e)[0][0])
-            assert row2[t, j] == -1
+    for a, b in ((tpe2, "tokens_per_expert"), (seg2, "seg_offsets"), (row2, "row_of"),
+                 (tor2, "token_of_row")):
+        assert np.array_equal(a, lay2[b])
+    filled = lay2["token_of_row"] >= 0
+    ref = oracle.permute_rows(moe_inputs.host_array(x), lay2["token_of_row"])
+    assert np.array_equal(moe_inputs.host_array(xp2)[filled], ref[filled])
 
 
-def test_permute_masked_few_tokens(moe):
-    """Masked layout with fewer tokens than local experts: every segment's unused
-    capacity rows are -1 in token_of_row, written by the copy kernel's warps."""
-    T, E, k, D, cap = 20, 48, 4, 64, 5
+@pytest.mark.parametrize("cap", [5, 1, 0])
+def test_permute_masked_few_tokens(moe, cap):
+    """Masked layout with fewer tokens than local experts, an expert range,
+    and capacities that do (1, 0) and may not (5) overflow: every array equals
+    the oracle's layout, whatever the status; unused capacity rows are -1."""
+    T, E, k, D = 20, 48, 4, 64
     idx = moe_inputs.random_topk_idx(T, E, k, seed=12, skew=0.7)
     cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_BF16,
                      layout=moe.MOE_LAYOUT_MASKED, capacity=cap, e_first=4, E_local=40)
     x = torch.randn(T, D, device="cuda").to(torch.bfloat16)
     st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
     lay = oracle.layout(idx, E, 4, 40, oracle.MASKED, 1, cap)
+    assert lay["status"] in (oracle.OK, oracle.CAPACITY)
+    if cap < 2:
+        assert lay["status"] == oracle.CAPACITY               # the case overflows
     assert st == (moe.MOE_OK if lay["status"] == oracle.OK else moe.MOE_ERR_CAPACITY)
     for a, b in ((tpe, "tokens_per_expert"), (seg, "seg_offsets"), (row_of, "row_of"),
                  (tor, "token_of_row")):
         assert np.array_equal(a, lay[b])
 
 
-def test_permute_bad_ids_flagged_and_skipped(moe):
+@pytest.mark.parametrize("layout", ["contiguous", "masked"])
+def test_permute_bad_ids_flagged_and_skipped(moe, layout):
+    """Reading R15: out-of-range, negative and repeated ids are skipped and
+    flagged; the rest of the layout equals the oracle's bit for bit."""
     T, E, k, D = 100, 8, 2, 32
     idx = moe_inputs.random_topk_idx(T, E, k, seed=9)
     idx[5, 1] = E          # out of range
     idx[9, 0] = -3         # negative
     idx[11, 1] = idx[11, 0]  # duplicate expert within a token
-    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_F32, align_m=4)
+    masked = layout == "masked"
+    cap = T if masked else 0
+    cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, dtype=moe.MOE_F32, align_m=4,
+                     layout=moe.MOE_LAYOUT_MASKED if masked else moe.MOE_LAYOUT_CONTIGUOUS,
+                     capacity=cap)
     x = torch.randn(T, D, device="cuda")
     st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
     assert st == moe.MOE_ERR_BAD_ROUTING
+    lay = oracle.layout(idx, E, 0, E, oracle.MASKED if masked else oracle.CONTIGUOUS,
+                        1 if masked else 4, cap)
+    assert lay["status"] == oracle.BAD_ROUTING
     assert row_of[5, 1] == -1 and row_of[9, 0] == -1 and row_of[11, 1] == -1
     assert tpe.sum() == T * k - 3
-    good = row_of >= 0
-    tt = np.broadcast_to(np.arange(T)[:, None], idx.shape)
-    assert np.array_equal(tor[row_of[good]], tt[good])
+    for a, b in ((tpe, "tokens_per_expert"), (seg, "seg_offsets"), (row_of, "row_of"),
+                 (tor, "token_of_row")):
+        assert np.array_equal(a, lay[b])
+    filled = lay["token_of_row"] >= 0
+    ref = oracle.permute_rows(moe_inputs.host_array(x), lay["token_of_row"])
+    assert np.array_equal(moe_inputs.host_array(xp)[filled], ref[filled])
 
 
 def test_permute_empty_batch(moe):

@@ -7,14 +7,17 @@ entry point keeps that scratch in a fixed array inside the library.  These
 checks call it through the C ABI twice in a row -- the second call on a
 different problem, so it starts from the first call's leftovers -- and
 compare every output with moe_permute on the same inputs, bit for bit (the
-tolerance of all integer and byte work in these tests).  This file is
-collected last on purpose.
+tolerance of all integer and byte work in these tests), and the layout with
+the CPU oracle's.  The cases take each form of the counting sort: up to 8192
+count cells (ceil(T / 256) * E), 8192 to 16384, and above that up to the
+fixed array's limit.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
 import moe_inputs
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +53,7 @@ def _compare(moe, cfg, idx, x):
     ws = moe.alloc_workspace(cfg)
     moe.moe_permute(cfg, x, idx, ref["tpe"], ref["seg"], ref["row_of"], ref["tor"], ref["xp"], ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    del ws
     got = _outputs(moe, cfg)
     flags = torch.zeros(1, dtype=torch.int32, device="cuda")
     moe.moe_permute_noalloc(cfg, x, idx, got["tpe"], got["seg"], got["row_of"], got["tor"],
@@ -61,10 +65,17 @@ def _compare(moe, cfg, idx, x):
     filled = ref["tor"] >= 0
     assert torch.equal(got["xp"][filled], ref["xp"][filled])
     assert int(got["tpe"].sum()) == cfg.T * cfg.k
+    lay = oracle.layout(idx.cpu().numpy(), cfg.E, cfg.e_first, cfg.e_local, oracle.CONTIGUOUS,
+                        cfg.align_m)
+    assert lay["status"] == oracle.OK
+    for name, key in (("tpe", "tokens_per_expert"), ("seg", "seg_offsets"),
+                      ("row_of", "row_of"), ("tor", "token_of_row")):
+        assert np.array_equal(got[name].cpu().numpy(), lay[key]), name
+    return got
 
 
 def test_noalloc_matches_permute_on_two_calls_in_a_row(moe):
-    # first call: a large skewed batch (fills much of the fixed scratch)
+    # first call: a large skewed batch (4096 count cells: the two-launch form)
     cfg1, idx1, x1 = _case(moe, T=16384, E=64, k=8, D=512, align=128, skew=1.2, seed=21)
     _compare(moe, cfg1, idx1, x1)
     # second call: a different, smaller problem over an expert range; the
@@ -72,3 +83,19 @@ def test_noalloc_matches_permute_on_two_calls_in_a_row(moe):
     cfg2, idx2, x2 = _case(moe, T=777, E=48, k=6, D=264, align=8, skew=0.4, seed=22,
                            e_first=8, E_local=30)
     _compare(moe, cfg2, idx2, x2)
+
+
+@pytest.mark.parametrize("T,E,k", [
+    (16384, 256, 8),    # 16384 count cells: the index kernel re-derives the scan
+    (131072, 256, 8),   # 131072 cells: count, scan, index, copy; exactly the array's limit
+])
+def test_noalloc_large_count_matrices(moe, T, E, k):
+    cfg, idx, x = _case(moe, T=T, E=E, k=k, D=64, align=128, skew=0.6, seed=T + E)
+    cells = -(-T // 256) * E
+    assert cells > 8192
+    got = _compare(moe, cfg, idx, x)
+    del got
+    # and a small call right after it, on what the large one left in the array
+    cfg2, idx2, x2 = _case(moe, T=300, E=16, k=4, D=128, align=16, skew=0.9, seed=5)
+    _compare(moe, cfg2, idx2, x2)
+
