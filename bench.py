@@ -26,6 +26,7 @@ the same workload and prints the same kind of line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -654,9 +655,20 @@ def run_gpu(args, name):
         # a reduced case of the same workload (profiling captures only)
         over = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.scale.split(",")}
         w = w.scaled(**over)
-    default = name == WORKLOAD
+    default = name == WORKLOAD and not args.shard
     inp = moe_inputs.make_inputs(w, device=dev, seed=rank)
     cfg = workload_config(moe, w)
+    if args.shard:
+        # the first expert range and H shard of an EP x TP split (profiling
+        # captures only): experts [0, E/EP), hidden units [0, H/TP)
+        ep, tp = (int(v) for v in args.shard.split(","))
+        el, hl = w.E // ep, w.H // tp
+        inp.w1 = inp.w1[:el, :hl].contiguous()
+        inp.w3 = inp.w3[:el, :hl].contiguous()
+        inp.w2 = inp.w2[:el, :, :hl].contiguous()
+        torch.cuda.empty_cache()
+        w = w.scaled(H=hl)
+        cfg = dataclasses.replace(cfg, H_local=hl, E_local=el)
     dt = moe_inputs.torch_dtype(w)
     if args.fp8_only:
         fp8 = run_fp8(moe, cfg, inp, torch.cuda.current_stream(dev), dev, args, load_peaks())
@@ -790,6 +802,7 @@ def run_gpu(args, name):
         "data": workload_data_note(w),
         "value_counts": VALUE_COUNTS, "tokens_per_step": w.T, "routed_rows_per_step": R,
         "config": {"workload": name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k,
+                   "shard": args.shard or None,
                    "router": router_note(w), "layout": layout_note(w),
                    "parallelism": f"replicas x{world}" if world > 1 else "single", "l2": l2_note(w)},
         "roofline": roof,
@@ -812,7 +825,7 @@ def run_gpu(args, name):
     if default:
         line.update({"fused_combine": fused, "fp8": fp8, "backward": backward})
 
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.shard:
         line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -850,8 +863,17 @@ def run_dispatch_bandwidth(args):
     torch.cuda.set_device(dev)
     peaks = load_peaks()
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
-    for name in ("fine-grained-bf16", "zipf-skewed", "deepseek-v3-shaped"):
-        w = moe_inputs.WORKLOADS[name]
+    cases = [moe_inputs.WORKLOADS[n] for n in ("fine-grained-bf16", "zipf-skewed",
+                                               "deepseek-v3-shaped")]
+    # a long prefill batch: 128 count blocks x 256 experts = 32768 count cells,
+    # above both single-pass limits, so the permute runs its four-launch chain
+    # (D = 1024 keeps the case near 2 GB on the device)
+    cases.append(moe_inputs.WORKLOADS["zipf-skewed"].scaled(
+        name="prefill-32k-e256-d1024", T=32768, D=1024, E=256, zipf_s=None))
+    if args.workload not in ("all", WORKLOAD):
+        cases = [c for c in cases if c.name == args.workload]
+    for w in cases:
+        name = w.name
         inp = moe_inputs.make_inputs(w, device=dev, seed=0, weights=False)
         cfg = moe.Config(T=w.T, D=w.D, H_local=w.H, E=w.E, k=w.k, dtype=moe.MOE_BF16,
                          score=moe.MOE_SCORE_SOFTMAX if w.score == "softmax"
@@ -922,11 +944,14 @@ def main():
                     help="time only the permute and combine calls on three workloads")
     ap.add_argument("--scale", default="",
                     help="with --backward-only: override workload sizes, e.g. E=16,k=2 (profiling)")
+    ap.add_argument("--shard", default="",
+                    help="EP,TP: time the first expert range and H shard only, e.g. 8,4 (profiling)")
     args = ap.parse_args()
     if args.scale and not args.backward_only:
         ap.error("--scale is for --backward-only profiling runs")
     import moe_inputs
-    if args.workload != "all" and args.workload not in moe_inputs.WORKLOADS:
+    if (args.workload != "all" and args.workload not in moe_inputs.WORKLOADS
+            and not args.dispatch_bandwidth):
         ap.error(f"unknown workload {args.workload!r}")
     if (args.fp8_only or args.backward_only) and args.workload != WORKLOAD:
         ap.error("--fp8-only and --backward-only time the default workload")
