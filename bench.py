@@ -470,6 +470,72 @@ def run_fused(moe, cfg, inp, stream, dev, args):
             "launches_per_step": launches, "deterministic": False}
 
 
+def run_gather(moe, cfg, inp, stream, dev, args):
+    """The dispatch fused into GEMM1's operand load: moe_layer_forward_gather
+    against moe_layer_forward in the same loop shape, and the step through
+    the step calls (route, permute_index, grouped_swiglu_gather, combine)
+    with CUDA events between them.  Bitwise the same output."""
+    import torch
+    w = inp.w
+    lws = moe.alloc_workspace(cfg, layer=True, device=dev)
+    out = torch.empty((w.T, w.D), dtype=inp.x.dtype, device=dev)
+    views = moe.layer_views(cfg, lws)
+
+    def layer_gather():
+        moe.moe_layer_forward_gather(cfg, inp.x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out,
+                                     lws, stream)
+
+    def layer_copy():
+        moe.moe_layer_forward(cfg, inp.x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, lws,
+                              stream)
+
+    n = max(20, args.steps // 2)
+    res = {}
+    for _ in range(2):  # two rounds, alternating, so drift hits both alike
+        for name, fn in (("layer_forward_ms", layer_copy), ("layer_forward_gather_ms", layer_gather)):
+            for _ in range(3):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            res.setdefault(name, []).append(e0.elapsed_time(e1) / n)
+    st = moe.moe_get_device_status(lws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after the gather leg: {moe.status_string(st)}")
+    # per-call breakdown of the gather step
+    v = views
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        moe.moe_route_topk(cfg, inp.x, inp.wg, inp.bias, None, v["topk_idx"], v["topk_w"], lws, stream)
+        ev[i][1].record(stream)
+        moe.moe_permute_index(cfg, v["topk_idx"], v["tokens_per_expert"], v["seg_offsets"],
+                              v["row_of"], v["token_of_row"], lws, stream)
+        ev[i][2].record(stream)
+        moe.moe_grouped_swiglu_gather(cfg, inp.x, v["token_of_row"], v["seg_offsets"],
+                                      v["tokens_per_expert"], inp.w1, inp.w3, inp.w2, v["h"],
+                                      v["y_perm"], lws, stream)
+        ev[i][3].record(stream)
+        moe.moe_unpermute_combine(cfg, v["y_perm"], v["row_of"], v["topk_w"], out, lws, stream)
+        ev[i][4].record(stream)
+    torch.cuda.synchronize(dev)
+    parts = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / n for j in range(4)]
+    st = moe.moe_get_device_status(lws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after the gather breakdown: {moe.status_string(st)}")
+    lf, lg = min(res["layer_forward_ms"]), min(res["layer_forward_gather_ms"])
+    return {"api": "moe_layer_forward_gather (C ABI): GEMM1 reads x[token_of_row[r]], no x_perm",
+            "layer_forward_ms": lf, "layer_forward_gather_ms": lg,
+            "value": w.T / (lg * 1e-3), "unit": UNIT, "speedup": lf / lg,
+            "breakdown_ms": {"route": parts[0], "permute_index": parts[1],
+                             "grouped_swiglu_gather": parts[2], "combine": parts[3]},
+            "rounds_ms": res}
+
+
 def run_fp8(moe, cfg, inp, stream, dev, args, peaks):
     """The FP8 variant of the same step: moe_layer_forward_fp8 (e4m3 dispatch,
     GEMM1 on e4m3 codes with per-row scales, GEMM2 in bf16), the weights
@@ -779,7 +845,9 @@ def run_gpu(args, name):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(moe, cfg, inp, out, stream, dev, world, args)
-    fused = fp8 = backward = None
+    fused = fp8 = backward = gather = None
+    if w.dtype == "bf16" and not args.no_gather:
+        gather = run_gather(moe, cfg, inp, stream, dev, args)
     if default and not args.no_fused:
         fused = run_fused(moe, cfg, inp, stream, dev, args)
     if default and not args.no_fp8:
@@ -819,6 +887,7 @@ def run_gpu(args, name):
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
                               "zeros": int((tpe_h == 0).sum())},
         "e2e": e2e,
+        "gather": gather,
         "gpu_launches": n_launches,
         "clocks": clk.summary(),
     }
@@ -937,6 +1006,8 @@ def main():
     ap.add_argument("--no-backward", action="store_true", help="skip the training backward leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (e4m3 GEMM1) leg")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused-combine leg")
+    ap.add_argument("--no-gather", action="store_true",
+                    help="skip the leg with the dispatch fused into GEMM1's operand load")
     ap.add_argument("--fp8-only", action="store_true", help="time only the FP8 leg, print its JSON")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the training step (forward_train + backward), print its JSON")

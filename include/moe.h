@@ -435,6 +435,47 @@ moe_status moe_layer_forward_fused(const moe_config *cfg, const void *x, const v
                                    moe_stream_t stream);
 
 /*
+ * The dispatch fused into the first GEMM's operand load ("Expert Parallelism
+ * (EP)", section 4: the dispatch folded into the neighbouring kernel so the
+ * routed rows skip one HBM round trip; section 2: the expert-contiguous,
+ * M-tile-aligned layout the grouped GEMM reads).  The permuted copy x_perm
+ * is never made: GEMM1 reads row r of the layout as x[token_of_row[r]].
+ *
+ * moe_permute_index: moe_permute without the row copy -- the same
+ * tokens_per_expert, seg_offsets, row_of and token_of_row, bit for bit, and
+ * the same status flags; x and x_perm are not taken.
+ */
+moe_status moe_permute_index(const moe_config *cfg, const int32_t *topk_idx,
+                             int32_t *tokens_per_expert, int32_t *seg_offsets, int32_t *row_of,
+                             int32_t *token_of_row, void *ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu with GEMM1's rows gathered from x [T, D] (bf16) by
+ * token_of_row [rows_alloc] (as moe_permute / moe_permute_index write it;
+ * -1 rows are read as zeros).  h and y_perm are bit for bit those of
+ * moe_grouped_swiglu on the x_perm that moe_permute would have written.
+ * bf16 only (MOE_ERR_UNSUPPORTED otherwise); it always runs the CTA-pair
+ * kernel, whatever the rows per expert.
+ */
+moe_status moe_grouped_swiglu_gather(const moe_config *cfg, const void *x,
+                                     const int32_t *token_of_row, const int32_t *seg_offsets,
+                                     const int32_t *tokens_per_expert, const void *w1,
+                                     const void *w3, const void *w2, void *h, void *y_perm,
+                                     void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_forward with the two calls above in place of moe_permute and
+ * moe_grouped_swiglu: route, permute_index, grouped_swiglu_gather, combine,
+ * on one stream.  The output equals moe_layer_forward's bit for bit.  bf16
+ * only; workspace moe_layer_workspace_size (its x_perm region is unused).
+ */
+moe_status moe_layer_forward_gather(const moe_config *cfg, const void *x, const void *wg,
+                                    const float *bias, const void *w1, const void *w3,
+                                    const void *w2, void *out, void *ws, size_t ws_bytes,
+                                    moe_stream_t stream);
+
+/*
  * moe_permute without a workspace (this entry point has no counterpart in
  * the pages; it exists for callers that cannot allocate device memory).
  *

@@ -37,6 +37,7 @@ ABI_SYMBOLS = (
     "moe_layer_forward_fused", "moe_layer_backward_ex",
     "moe_host_pipeline_workspace_size", "moe_host_pipeline_create", "moe_host_pipeline_submit",
     "moe_host_pipeline_sync", "moe_host_pipeline_destroy",
+    "moe_permute_index", "moe_grouped_swiglu_gather", "moe_layer_forward_gather",
 )
 
 
@@ -92,6 +93,9 @@ def _load() -> ctypes.CDLL:
         "moe_host_pipeline_submit": (I32, [P, P, P, P, P, P, P, P, P]),
         "moe_host_pipeline_sync": (I32, [P]),
         "moe_host_pipeline_destroy": (None, [P]),
+        "moe_permute_index": (I32, [C, P, P, P, P, P, P, SZ, P]),
+        "moe_grouped_swiglu_gather": (I32, [C, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_layer_forward_gather": (I32, [C, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -267,6 +271,21 @@ def moe_permute(cfg: Config, x, topk_idx, tokens_per_expert, seg_offsets, row_of
     _check(_lib.moe_permute(ctypes.byref(c), _ptr(x), _ptr(topk_idx), _ptr(tokens_per_expert),
                             _ptr(seg_offsets), _ptr(row_of), _ptr(token_of_row), _ptr(x_perm),
                             _ptr(ws), ws.numel(), _stream(stream)), "moe_permute")
+
+
+def moe_permute_index(cfg: Config, topk_idx, tokens_per_expert, seg_offsets, row_of, token_of_row,
+                      ws, stream=None):
+    """moe_permute without the row copy: the layout arrays only."""
+    ra = rows_alloc(cfg)
+    _expect(topk_idx, (cfg.T, cfg.k), torch.int32, "topk_idx")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(seg_offsets, (cfg.e_local + 1,), torch.int32, "seg_offsets")
+    _expect(row_of, (cfg.T, cfg.k), torch.int32, "row_of")
+    _expect(token_of_row, (ra,), torch.int32, "token_of_row")
+    c = cfg.c()
+    _check(_lib.moe_permute_index(ctypes.byref(c), _ptr(topk_idx), _ptr(tokens_per_expert),
+                                  _ptr(seg_offsets), _ptr(row_of), _ptr(token_of_row), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "moe_permute_index")
 
 
 def moe_permute_noalloc(cfg: Config, x, topk_idx, tokens_per_expert, seg_offsets, row_of,
@@ -560,6 +579,47 @@ def moe_layer_forward_fp8(cfg: Config, x, wg, bias, w1_q, w1_scale, w3_q, w3_sca
                                       _ptr(w1_scale), _ptr(w3_q), _ptr(w3_scale), _ptr(w2),
                                       _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_layer_forward_fp8")
+
+
+def moe_grouped_swiglu_gather(cfg: Config, x, token_of_row, seg_offsets, tokens_per_expert, w1,
+                              w3, w2, h, y_perm, ws, stream=None):
+    """moe_grouped_swiglu with GEMM1's rows read from x by token_of_row."""
+    ra = rows_alloc(cfg)
+    dt = cfg.torch_dtype
+    el = cfg.e_local
+    _expect(x, (cfg.T, cfg.D), dt, "x")
+    _expect(token_of_row, (ra,), torch.int32, "token_of_row")
+    _expect(seg_offsets, (el + 1,), torch.int32, "seg_offsets")
+    _expect(tokens_per_expert, (cfg.E,), torch.int32, "tokens_per_expert")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    _expect(h, (ra, cfg.H_local), dt, "h")
+    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    c = cfg.c()
+    _check(_lib.moe_grouped_swiglu_gather(ctypes.byref(c), _ptr(x), _ptr(token_of_row),
+                                          _ptr(seg_offsets), _ptr(tokens_per_expert), _ptr(w1),
+                                          _ptr(w3), _ptr(w2), _ptr(h), _ptr(y_perm), _ptr(ws),
+                                          ws.numel(), _stream(stream)), "moe_grouped_swiglu_gather")
+
+
+def moe_layer_forward_gather(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None):
+    """moe_layer_forward with the dispatch fused into GEMM1's operand load
+    (no x_perm); bitwise the same output."""
+    el = cfg.e_local
+    dt = cfg.torch_dtype
+    _expect(x, (cfg.T, cfg.D), dt, "x")
+    _expect(wg, (cfg.E, cfg.D), dt, "wg")
+    if bias is not None:
+        _expect(bias, (cfg.E,), torch.float32, "bias")
+    _expect(w1, (el, cfg.H_local, cfg.D), dt, "w1")
+    _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
+    _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
+    _expect(out, (cfg.T, cfg.D), dt, "out")
+    c = cfg.c()
+    _check(_lib.moe_layer_forward_gather(ctypes.byref(c), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w1),
+                                         _ptr(w3), _ptr(w2), _ptr(out), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "moe_layer_forward_gather")
 
 
 def moe_layer_forward_fused(cfg: Config, x, wg, bias, w1, w3, w2, out, ws, stream=None):

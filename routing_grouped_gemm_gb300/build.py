@@ -20,6 +20,10 @@ LIB = os.path.join(LIBDIR, "libmoe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
+# Extra -D definitions for the kernels' compile-time switches (MOE_PDL,
+# MOE_PAIR_STAGES, MOE_GATHER_ACQ_CLUSTER, ...), space separated, e.g.
+# MOE_NVCC_DEFINES="-DMOE_PAIR_FUSED=0"; empty for the default build.
+EXTRA_DEFINES = os.environ.get("MOE_NVCC_DEFINES", "").split()
 
 
 def nvcc() -> str:
@@ -47,7 +51,7 @@ def stale() -> bool:
 
 def _compile(src: str, ptxas_verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *EXTRA_DEFINES, "-c", src, "-o", obj]
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)

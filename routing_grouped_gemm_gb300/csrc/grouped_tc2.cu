@@ -71,7 +71,18 @@ constexpr int P_A_BYTES = P_BM * P_BK * 2;       // 16 KB
 constexpr int P_B_BYTES = (P_BN / 2) * P_BK * 2; // 16 KB: this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_EPI_WARPS = 4;
-constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
+// Gather mode (a separate instantiation): GEMM1's A rows come straight
+// from x by token_of_row, copied by extra warps instead of TMA-loaded from
+// x_perm.
+constexpr int P_GATHER_WARPS = 4;  // one per stage in flight (stage n: warp n % 4)
+// The MMA warp's wait on a stage with gathered rows acquires at cluster
+// scope (1) or CTA scope (0).
+#ifndef MOE_GATHER_ACQ_CLUSTER
+#define MOE_GATHER_ACQ_CLUSTER 1
+#endif
+constexpr int pair_threads(bool gather) {
+    return 64 + 32 * P_EPI_WARPS + (gather ? 32 * P_GATHER_WARPS : 0);
+}
 constexpr int P_ACC_COLS = 256;
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_NBARS = 24;
@@ -121,6 +132,11 @@ struct PairParams {
     // comb [T, n_out1] (fp32 atomics; the token and slot weight of row r from
     // token_of_row, row_of [T, k] and topk_w) instead of storing y_perm
     float *comb;
+    // Gather mode (the kGather instantiation, bf16 GEMM1): A rows of GEMM1
+    // tiles are x[token_of_row[row]] ([T, D] bf16, D = n_out1), copied by the
+    // gather warps; the full barriers then also count their arrivals
+    const __nv_bfloat16 *xg;
+    int x_rows;           // gather: T (a token id outside [0, T) reads as a zero row)
     const int *token_of_row, *row_of;
     const float *topk_w;
     int k;
@@ -185,7 +201,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2_p(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(P_THREADS, 1)
+template <bool kGather>
+__global__ void __launch_bounds__(pair_threads(kGather), 1)
 grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmX64,
                     const __grid_constant__ CUtensorMap tmX16,
                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
@@ -235,7 +252,9 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                          s_base, s_valid, s_mtoff, blockIdx.x == 0 ? p.status : nullptr, s_end);
         if (lane == 0) {
             for (int s = 0; s < P_STAGES; ++s) {
-                mbar_init(&full[s], 1);    // the leader's producer posts both CTAs' bytes
+                // the leader's producer posts both CTAs' bytes (and, gathering, the
+                // stage's gather warp in each CTA arrives once its rows are stored)
+                mbar_init(&full[s], kGather ? 1 + 2 : 1);
                 mbar_init(&empty[s], 1);   // one multicast commit per use
             }
             for (int a = 0; a < 2; ++a) {
@@ -295,9 +314,11 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const bool half = !swap && c.nvalid <= P_BM;      // M=128: 64 rows per CTA
                 const int srows = ((c.nvalid + 31) & ~31) / 2;    // transposed: token rows per CTA
                 const int arow = c.row0 + (int)rank * (swap ? srows : half ? P_BM / 2 : P_BM);
+                // gathering: the token rows of GEMM1 tiles come from the gather warps
+                const bool gath = kGather && c.mode == 0;
                 const uint32_t tx =
-                    2u * (swap ? P_A_BYTES + srows * P_BK * 2
-                               : half ? P_A_BYTES / 2 + P_B_BYTES : P_STAGE_BYTES);
+                    2u * (swap ? P_A_BYTES + (gath ? 0 : srows * P_BK * 2)
+                               : (gath ? 0 : half ? P_A_BYTES / 2 : P_A_BYTES) + P_B_BYTES);
                 const CUtensorMap *ta = c.mode ? (half ? &tmH64 : &tmH) : (half ? &tmX64 : &tmX);
                 const CUtensorMap *t16 = c.mode ? &tmH16 : &tmX16;
                 const int nk = c.mode ? p.nk1 : p.nk0;
@@ -312,7 +333,11 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 }
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    if (leader) mbar_arrive_expect_tx(&full[s], tx);
+                    if (leader) {
+                        mbar_arrive_expect_tx(&full[s], tx);
+                        // a GEMM2 stage has no gathered rows: their arrivals are posted here
+                        if (kGather && c.mode != 0) mbar_arrive_cnt(&full[s], 2);
+                    }
                     uint8_t *sa = ring + s * P_STAGE_BYTES;
                     uint8_t *sb = sa + P_A_BYTES;
                     const uint32_t fb = full_leader + (uint32_t)(s * sizeof(uint64_t));
@@ -327,12 +352,14 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                             tma_load_3d_pair(sa, &tmW2, fb, kb * P_BK, c.nt * P_BN + (int)rank * 128,
                                              c.expert);
                         }
-                        for (int i = 0; i < srows / 16; ++i)
-                            tma_load_2d_pair(sb + i * 16 * P_BK * 2, t16, fb, kb * kel, arow + 16 * i);
+                        if (!gath)
+                            for (int i = 0; i < srows / 16; ++i)
+                                tma_load_2d_pair(sb + i * 16 * P_BK * 2, t16, fb, kb * kel,
+                                                 arow + 16 * i);
                         if (++s == P_STAGES) { s = 0; ph ^= 1u; }
                         continue;
                     }
-                    tma_load_2d_pair(sa, ta, fb, kb * kel, arow);
+                    if (!gath) tma_load_2d_pair(sa, ta, fb, kb * kel, arow);
                     if (c.mode == 0) {
                         const int hrow = c.nt * 128 + (int)rank * 64;
                         tma_load_3d_pair(sb, &tmW1, fb, kb * kel, hrow, c.expert);
@@ -366,7 +393,11 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * P_ACC_COLS);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait_bounded(&full[s], ph, abort_flag)) { ok = false; break; }
+                    // gathered rows of the peer were written by its threads: cluster acquire
+                    if (!mbar_wait_bounded(&full[s], ph, abort_flag, kGather && MOE_GATHER_ACQ_CLUSTER)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(ring + s * P_STAGE_BYTES);
                     const uint32_t b_addr = a_addr + P_A_BYTES;
@@ -395,7 +426,7 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             volatile int local_abort = 0;
             mbar_wait_bounded(drain, 0u, &local_abort);
         }
-    } else {
+    } else if (warp < 2 + P_EPI_WARPS) {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
         // Each warp owns 32 accumulator rows (its TMEM lane quarter).  h
         // (GEMM1) goes out straight from registers, valid rows only.  GEMM2's
@@ -681,9 +712,83 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + (uint32_t)(acc * sizeof(uint64_t)));
         }
+    } else if constexpr (kGather) {
+        // ---------------- GEMM1 A-row gather (warps 6..9) ----------------
+        // Gather warp g fills the pipeline stages n with n % 4 == g, so four
+        // stages are in flight across the warps.  For its stage the warp loads
+        // every A row of this CTA (the token rows of a transposed tile, which
+        // go to the B slot): the row's 128-byte K slice of x[token_of_row[row]],
+        // four whole rows per instruction (lanes 8 i .. 8 i + 7: row 4 it + i,
+        // 16-byte piece lane & 7), into registers; pad rows and the K tail past
+        // D are zeros.  The loads are in flight while the warp waits for the
+        // stage to be free.  It then stores the pieces where the 128-byte
+        // swizzle of a TMA load puts them (piece j of row r at j ^ (r & 7)),
+        // orders the stores for the async proxy (the MMA reads the stage
+        // through it) and lane 0 arrives on the leader's full barrier.  The
+        // warp has no load outstanding when it fences and arrives, so neither
+        // waits for another stage's loads.
+        const int gw = warp - 2 - P_EPI_WARPS;
+        const int sub = lane >> 3, ch = lane & 7;
+        const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0);
+        const int upr = p.n_out1 / 8;  // 16-byte units in a row of x (D / 8)
+        const uint4 *xv = reinterpret_cast<const uint4 *>(p.xg);
+        int s = 0;
+        uint32_t ph = 0, n = 0;  // ring position, its phase, stages passed
+        bool ok = true;
+        for (int tile = pair_id; ok && tile < total_tiles; tile += n_pairs) {
+            const PairTile c = decode_pair(tile, p, n_blocks, s_mtoff, s_base, s_valid);
+            const int nk = c.mode ? p.nk1 : p.nk0;
+            if (c.mode != 0) {  // A is h, loaded by TMA; the producer arrives for us
+                for (int kb = 0; kb < nk; ++kb, ++n)
+                    if (++s == P_STAGES) { s = 0; ph ^= 1u; }
+                continue;
+            }
+            const bool swap = c.nvalid <= P_SWAP_MAX;
+            const bool half = !swap && c.nvalid <= P_BM;
+            const int nrows = swap ? ((c.nvalid + 31) & ~31) / 2 : half ? P_BM / 2 : P_BM;
+            const int rel0 = (int)rank * nrows;  // this CTA's first row within the pair tile
+            // lane l holds the tokens of rows l, l + 32, l + 64, l + 96
+            int tk[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = q * 32 + lane;
+                tk[q] = r < nrows && rel0 + r < c.nvalid ? p.token_of_row[c.row0 + rel0 + r] : -1;
+                if (tk[q] >= p.x_rows) tk[q] = -1;
+            }
+            const int slot = swap ? P_A_BYTES : 0;
+            for (int kb = 0; kb < nk; ++kb, ++n) {
+                if ((int)(n % P_GATHER_WARPS) == gw) {
+                    const int u = kb * (P_BK / 8) + ch;
+                    uint4 b[32];
+#pragma unroll
+                    for (int it = 0; it < 32; ++it) {
+                        const int r = it * 4 + sub;
+                        const int t = __shfl_sync(0xffffffffu, tk[it >> 3], r & 31);
+                        b[it] = make_uint4(0u, 0u, 0u, 0u);
+                        if (r < nrows && t >= 0 && u < upr) b[it] = __ldcg(xv + (size_t)t * upr + u);
+                    }
+                    // lane 0 waits for the free stage and the warp follows it; the
+                    // warp stops as a whole if the wait gave up
+                    bool got = true;
+                    if (lane == 0) got = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                    uint8_t *st = ring + s * P_STAGE_BYTES + slot;
+#pragma unroll
+                    for (int it = 0; it < 32; ++it) {
+                        const int r = it * 4 + sub;
+                        if (r < nrows)
+                            *reinterpret_cast<uint4 *>(st + r * 128 + ((ch ^ (r & 7)) << 4)) = b[it];
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(full_leader + (uint32_t)(s * sizeof(uint64_t)));
+                }
+                if (++s == P_STAGES) { s = 0; ph ^= 1u; }
+            }
+        }
     }
 
-    if (warp >= 2 && (threadIdx.x & 31) == 0)
+    if (warp >= 2 && warp < 2 + P_EPI_WARPS && (threadIdx.x & 31) == 0)
         bulk_wait_group_all();  // every y store has landed before the CTA exits
     tc_fence_before();
     __syncthreads();
@@ -716,7 +821,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 }
 
 // clusters of two that fit at once on the current device (0 if none)
-int max_pair_clusters(size_t smem) {
+template <bool G>
+int max_pair_clusters_t(size_t smem) {
     constexpr int kMaxDev = 64;
     static int cached[kMaxDev] = {0};
     static size_t cached_smem[kMaxDev] = {0};
@@ -725,7 +831,7 @@ int max_pair_clusters(size_t smem) {
     if (cached[dev] > 0 && cached_smem[dev] == smem) return cached[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256);
-    cfg.blockDim = dim3(P_THREADS);
+    cfg.blockDim = dim3(pair_threads(G));
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -735,7 +841,7 @@ int max_pair_clusters(size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (void *)grouped_pair_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, (void *)grouped_pair_kernel<G>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -744,15 +850,20 @@ int max_pair_clusters(size_t smem) {
     return n;
 }
 
+int max_pair_clusters(size_t smem, bool gather) {
+    const int n = max_pair_clusters_t<false>(smem);
+    return gather ? std::min(n, max_pair_clusters_t<true>(smem)) : n;
+}
+
 struct PairMaps {
     CUtensorMap x, x64, x16, w1, w3, h, h64, h16, w2, y;
 };
 
 cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, size_t smem,
-                        bool cooperative, cudaStream_t stream) {
+                        bool cooperative, bool gather, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(P_THREADS);
+    cfg.blockDim = dim3(pair_threads(gather));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     // the cooperative one-launch form keeps plain stream order; the
@@ -771,8 +882,11 @@ cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, si
     }
     cfg.attrs = attr;
     cfg.numAttrs = (cooperative || MOE_PDL) ? 2 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_pair_kernel, m.x, m.x64, m.x16, m.w1,
-                                             m.w3, m.h, m.h64, m.h16, m.w2, m.y, p);
+    const cudaError_t e =
+        gather ? cudaLaunchKernelEx(&cfg, grouped_pair_kernel<true>, m.x, m.x64, m.x16, m.w1, m.w3,
+                                    m.h, m.h64, m.h16, m.w2, m.y, p)
+               : cudaLaunchKernelEx(&cfg, grouped_pair_kernel<false>, m.x, m.x64, m.x16, m.w1, m.w3,
+                                    m.h, m.h64, m.h16, m.w2, m.y, p);
     if (e == cudaSuccess) count_launch();
     return e;
 }
@@ -792,7 +906,7 @@ namespace {
 // calls where the device accepts it, else two launches.
 cudaError_t run_pair(const PairMaps &m, const PairParams &p, int64_t rows_alloc, int E_local,
                      int clusters_max, size_t smem, int *scratch, cudaStream_t stream,
-                     bool *launched) {
+                     bool *launched, bool gather = false) {
     const long long pt_bound = (rows_alloc + P_PAIR_M - 1) / P_PAIR_M + E_local;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
@@ -816,7 +930,7 @@ cudaError_t run_pair(const PairMaps &m, const PairParams &p, int64_t rows_alloc,
         pb.finish = scratch;
         pb.done = scratch + 32;
         pb.max_blocks = (int)pt_bound;
-        err = launch_pair(m, pb, c, smem, true, stream);
+        err = launch_pair(m, pb, c, smem, true, gather, stream);
         if (err == cudaSuccess) {
             g_coop_ok[dev] = 1;
             *launched = true;
@@ -830,11 +944,11 @@ cudaError_t run_pair(const PairMaps &m, const PairParams &p, int64_t rows_alloc,
     PairParams p1 = p;
     p1.sched = SCHED_GEMM1;
     const int c1 = (int)std::min<long long>(clusters_max, pt_bound * p.nt0);
-    if ((err = launch_pair(m, p1, c1, smem, false, stream)) != cudaSuccess) return err;
+    if ((err = launch_pair(m, p1, c1, smem, false, gather, stream)) != cudaSuccess) return err;
     PairParams p2 = p;
-    p2.sched = SCHED_GEMM2;
+    p2.sched = SCHED_GEMM2;  // A is h: the plain instantiation
     const int c2 = (int)std::min<long long>(clusters_max, pt_bound * p.nt1);
-    if ((err = launch_pair(m, p2, c2, smem, false, stream)) != cudaSuccess) return err;
+    if ((err = launch_pair(m, p2, c2, smem, false, false, stream)) != cudaSuccess) return err;
     *launched = true;
     return cudaSuccess;
 }
@@ -868,7 +982,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
                                             int D, int H_local, int e_first, int E_local,
                                             int64_t rows_alloc, int *scratch, int *status,
                                             cudaStream_t stream, bool *launched, void *gu,
-                                            const FusedCombine *fc) {
+                                            const FusedCombine *fc, const GatherA *ga) {
     *launched = false;
     if (E_local == 0 || rows_alloc == 0) {
         *launched = true;
@@ -876,15 +990,20 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     }
     const size_t smem = pair_smem_bytes(E_local);
     if (smem > 227 * 1024) return cudaSuccess;  // not launched: caller falls back
-    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel, smem);
+    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel<false>, smem);
     if (err != cudaSuccess) return err;
-    const int clusters_max = max_pair_clusters(smem);
+    if (ga && (err = ensure_smem((const void *)grouped_pair_kernel<true>, smem)) != cudaSuccess)
+        return err;
+    const int clusters_max = max_pair_clusters(smem, ga != nullptr);
     if (clusters_max <= 0) return cudaSuccess;  // not launched: caller falls back
 
     PairMaps m;
-    if (!make_tmap_2d(&m.x, x_perm, D, rows_alloc, P_BM) ||
-        !make_tmap_2d(&m.x64, x_perm, D, rows_alloc, P_BM / 2) ||
-        !make_tmap_2d(&m.x16, x_perm, D, rows_alloc, 16) ||
+    // gathering, the x maps are not read; they are built over x so they are valid
+    const void *xa = ga ? ga->x : x_perm;
+    const int64_t xrows = ga ? ga->T : rows_alloc;
+    if (!make_tmap_2d(&m.x, xa, D, xrows, P_BM) ||
+        !make_tmap_2d(&m.x64, xa, D, xrows, P_BM / 2) ||
+        !make_tmap_2d(&m.x16, xa, D, xrows, 16) ||
         !make_tmap_3d(&m.w1, w1, D, H_local, E_local, 64) ||
         !make_tmap_3d(&m.w3, w3, D, H_local, E_local, 64) ||
         !make_tmap_2d(&m.h, h, H_local, rows_alloc, P_BM) ||
@@ -896,6 +1015,11 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
     PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
                                E_local, rows_alloc, status);
     p.gu_out = (__nv_bfloat16 *)gu;
+    if (ga) {
+        p.xg = (const __nv_bfloat16 *)ga->x;
+        p.x_rows = (int)ga->T;
+        p.token_of_row = ga->token_of_row;
+    }
     if (fc) {
         p.comb = fc->comb;
         p.token_of_row = fc->token_of_row;
@@ -903,7 +1027,8 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
         p.topk_w = fc->topk_w;
         p.k = fc->k;
     }
-    return run_pair(m, p, rows_alloc, E_local, clusters_max, smem, scratch, stream, launched);
+    return run_pair(m, p, rows_alloc, E_local, clusters_max, smem, scratch, stream, launched,
+                    ga != nullptr);
 }
 
 cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float *x_scale,
@@ -921,9 +1046,9 @@ cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float 
     }
     const size_t smem = pair_smem_bytes(E_local);
     if (smem > 227 * 1024) return cudaSuccess;  // not launched
-    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel, smem);
+    cudaError_t err = ensure_smem((const void *)grouped_pair_kernel<false>, smem);
     if (err != cudaSuccess) return err;
-    const int clusters_max = max_pair_clusters(smem);
+    const int clusters_max = max_pair_clusters(smem, false);
     if (clusters_max <= 0) return cudaSuccess;  // not launched
 
     // e4m3 operands of GEMM1: boxes of 128 K elements (128 bytes, the same

@@ -136,6 +136,14 @@ struct FusedCombine {
     int k;
 };
 
+// GEMM1's A rows gathered from the token rows: row r of the grouped layout
+// is x[token_of_row[r]] (x: [T, D] bf16), so x_perm need not exist.
+struct GatherA {
+    const void *x;
+    const int *token_of_row;
+    int64_t T;
+};
+
 // bf16 tcgen05 grouped SwiGLU on CTA pairs (cta_group::2).  With `scratch`
 // both GEMMs run in one cooperative launch; without it, or where the device
 // refuses a cooperative cluster launch, in two.  Sets *launched to false (and
@@ -147,7 +155,8 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
                                             int D, int H_local, int e_first, int E_local,
                                             int64_t rows_alloc, int *scratch, int *status,
                                             cudaStream_t stream, bool *launched,
-                                            void *gu = nullptr, const FusedCombine *fc = nullptr);
+                                            void *gu = nullptr, const FusedCombine *fc = nullptr,
+                                            const GatherA *ga = nullptr);
 
 // Backward of the bf16 grouped SwiGLU on CTA pairs: dgu = SwiGLU'(gy . w2_e)
 // with the saved gate/up gu, dxp = dgu . [w1_e; w3_e] (fp32), and the weight

@@ -899,6 +899,96 @@ MOE_EXPORT moe_status moe_layer_forward_fused(const moe_config *cfg, const void 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_forward_fused: output");
 }
 
+moe_status do_grouped_gather(const moe_config *c, const void *x, const int32_t *tor,
+                              const int32_t *seg, const int32_t *tpe, const void *w1,
+                              const void *w3, const void *w2, void *h, void *y_perm,
+                              const StepWs &w, cudaStream_t s) {
+    const char *sel = getenv("MOE_GROUPED_KERNEL");
+    const bool two_launches = sel && strcmp(sel, "pair2") == 0;
+    bool launched = false;
+    const moe::GatherA ga{x, tor, c->T};
+    const cudaError_t e = moe::launch_grouped_swiglu_bf16_pair(
+        nullptr, seg, tpe, w1, w3, w2, h, y_perm, c->D, c->H_local, c->e_first, c->E_local,
+        rows_alloc_of(c), two_launches ? nullptr : w.grouped, &w.status->flags, s, &launched,
+        nullptr, nullptr, &ga);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_grouped_swiglu_gather");
+    if (!launched)
+        return arg_fail("moe_grouped_swiglu_gather: too many local experts for the pair kernel",
+                        MOE_ERR_UNSUPPORTED);
+    return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_permute_index(const moe_config *cfg, const int32_t *topk_idx,
+                                        int32_t *tokens_per_expert, int32_t *seg_offsets,
+                                        int32_t *row_of, int32_t *token_of_row, void *ws,
+                                        size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (!tokens_per_expert || !seg_offsets) return arg_fail("moe_permute_index: NULL tensor");
+    if (cfg->T > 0 && (!topk_idx || !row_of)) return arg_fail("moe_permute_index: NULL tensor");
+    if (rows_alloc_of(cfg) > 0 && !token_of_row)
+        return arg_fail("moe_permute_index: NULL token_of_row");
+    return do_permute(cfg, nullptr, topk_idx, tokens_per_expert, seg_offsets, row_of,
+                      token_of_row, nullptr, w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_grouped_swiglu_gather(const moe_config *cfg, const void *x,
+                                                const int32_t *token_of_row,
+                                                const int32_t *seg_offsets,
+                                                const int32_t *tokens_per_expert, const void *w1,
+                                                const void *w3, const void *w2, void *h,
+                                                void *y_perm, void *ws, size_t ws_bytes,
+                                                moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->dtype != MOE_BF16)
+        return arg_fail("moe_grouped_swiglu_gather: bf16 only", MOE_ERR_UNSUPPORTED);
+    StepWs w;
+    if ((st = carve_step(cfg, ws, ws_bytes, &w)) != MOE_OK) return st;
+    if (cfg->E_local == 0 || rows_alloc_of(cfg) == 0) return MOE_OK;
+    if (!seg_offsets || !tokens_per_expert || !token_of_row)
+        return arg_fail("moe_grouped_swiglu_gather: NULL offsets or token_of_row");
+    if (!need16(x) || !need16(w1) || !need16(w3) || !need16(w2) || !need16(h) || !need16(y_perm))
+        return arg_fail("moe_grouped_swiglu_gather: NULL or misaligned tensor");
+    return do_grouped_gather(cfg, x, token_of_row, seg_offsets, tokens_per_expert, w1, w3, w2, h,
+                             y_perm, w, (cudaStream_t)stream);
+}
+
+MOE_EXPORT moe_status moe_layer_forward_gather(const moe_config *cfg, const void *x,
+                                               const void *wg, const float *bias, const void *w1,
+                                               const void *w3, const void *w2, void *out,
+                                               void *ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (cfg->dtype != MOE_BF16)
+        return arg_fail("moe_layer_forward_gather: bf16 only", MOE_ERR_UNSUPPORTED);
+    if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
+    if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
+    if ((int64_t)ws_bytes < layer_ws_layout(cfg, nullptr, nullptr))
+        return arg_fail("workspace too small for moe_layer_forward_gather", MOE_ERR_WORKSPACE);
+    if (cfg->T == 0) return MOE_OK;
+    if (!need16(x) || !need16(wg) || !need16(out) || (bias && !aligned(bias, 4)))
+        return arg_fail("moe_layer_forward_gather: NULL or misaligned tensor");
+    if (cfg->E_local > 0 && (!need16(w1) || !need16(w3) || !need16(w2)))
+        return arg_fail("moe_layer_forward_gather: NULL or misaligned expert weights");
+    LayerWs L;
+    carve_step(cfg, ws, ws_bytes, &L.step);
+    layer_ws_layout(cfg, static_cast<char *>(ws), &L);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = do_route(cfg, x, wg, bias, nullptr, L.topk_idx, L.topk_w, L.step, s)) != MOE_OK)
+        return st;
+    if ((st = do_permute(cfg, nullptr, L.topk_idx, L.tpe, L.seg_off, L.row_of, L.token_of_row,
+                         nullptr, L.step, s)) != MOE_OK)
+        return st;
+    if (cfg->E_local > 0 && rows_alloc_of(cfg) > 0 &&
+        (st = do_grouped_gather(cfg, x, L.token_of_row, L.seg_off, L.tpe, w1, w3, w2, L.h,
+                                L.y_perm, L.step, s)) != MOE_OK)
+        return st;
+    return do_combine(cfg, L.y_perm, L.row_of, L.topk_w, out, L.step, s);
+}
+
 MOE_EXPORT moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *wg,
                                          const void *w1, const void *w3, const void *w2,
                                          const void *dout, void *dx, float *dwg, float *dbias,

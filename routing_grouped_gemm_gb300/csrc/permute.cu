@@ -439,7 +439,8 @@ permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
     // kernel, spread over its warps
 }
 
-// One warp per token.  Lane j < k ranks slot j: the slot is active when its
+// One warp per token (x_perm NULL: the layout arrays only, no row copy).
+// Lane j < k ranks slot j: the slot is active when its
 // expert id is in [0, E) and no earlier slot of the token names it; a local
 // expert i gets row blk_base[b][i] + (rows of the expert in earlier warps of
 // the block) + popc(mask & lanes below), or -1 past the segment's end (the
@@ -468,7 +469,7 @@ permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ t
     const int e = lane < k ? topk_idx[(size_t)t * k + lane] : -1;
     const uint4 *src = x + (size_t)t * vpr;
     uint4 buf[IC_UNROLL];
-    if (!kFp8) {
+    if (!kFp8 && x_perm) {
 #pragma unroll
         for (int u = 0; u < IC_UNROLL; ++u) {  // the first chunk of x[t] is in flight meanwhile
             const int v = u * 32 + lane;
@@ -509,6 +510,7 @@ permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ t
         float4 *z = zero_out + (size_t)t * zvpr;
         for (int v = lane; v < zvpr; v += 32) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    if (!x_perm) return;  // the layout only (GEMM1 gathers the rows from x itself)
     for (int v0 = 0;;) {
         for (int j = 0; j < k; ++j) {
             const int r = __shfl_sync(0xffffffffu, my_row, j);
@@ -755,6 +757,7 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     }
     if (x_scale)  // FP8 dispatch: the copy quantises each token row once
         return launch_quantize_rows_e4m3(x, T, D, row_of, k, (uint8_t *)x_perm, x_scale, stream);
+    if (!x_perm) return cudaSuccess;  // the layout only
     const int vpr = D * elem_bytes / 16;
     const int warps_per_block = 8;
     const int blocks = (T + warps_per_block - 1) / warps_per_block;

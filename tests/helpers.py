@@ -125,3 +125,42 @@ def check_layout_properties(idx, lay, E, e_first, E_local, align_m=None, masked_
     assert (row_of[~local] == -1).all()
     tt = np.broadcast_to(np.arange(T)[:, None], idx.shape)
     assert np.array_equal(tor[row_of[local]], tt[local])
+
+
+def assert_grouped_parity(lay, xp, w1, w3, w2, h, y, rb):
+    """Grouped SwiGLU outputs h and y (CUDA tensors) against the oracle's
+    grouped form over the layout `lay`, on the A rows xp (CUDA tensor
+    [rows, D]); rb: bf16 (element-wise bounds) or fp32 (1e-4)."""
+    H_ = moe_inputs.host_array
+    seg, cnt = lay["seg_offsets"], lay["tokens_per_expert"]
+    E_local = len(cnt)
+    oh = oracle.grouped_gemm1_swiglu(H_(xp), seg, cnt, list(H_(w1)), list(H_(w3)), round_h=rb)
+    filled = lay["token_of_row"] >= 0
+    gh = to_f64(h)
+    # second GEMM from the oracle's own h (no GPU value feeds the oracle)
+    ohb = oh.astype(np.float32)
+    oy = oracle.grouped_gemm2(ohb, seg, cnt, list(H_(w2)))
+    gy = to_f64(y)
+    if rb:
+        # h is a bf16 intermediate rounded once on each side: compared per element
+        assert within_bf16_rounding(gh[filled], oh[filled]) <= 1.0
+        # y (fp32) differs by what those h differences carry through w2, plus
+        # fp32 accumulation error: |dy| <= |dh| |w2|^T + 2^-20 |h| |w2|^T
+        w2h = to_f64(w2)
+        dh = np.abs(np.nan_to_num(gh) - np.nan_to_num(oh))
+        for i in range(E_local):
+            rows = np.arange(seg[i], seg[i] + cnt[i])
+            if len(rows) == 0:
+                continue
+            aw2 = np.abs(w2h[i])
+            bound = dh[rows] @ aw2.T + 2.0 ** -20 * (np.abs(oh[rows]) @ aw2.T) + 1e-30
+            assert (np.abs(gy[rows] - oy[rows]) <= bound).all(), f"expert {i}"
+        assert rel_err(gy[filled], oy[filled]) < 1e-2
+    else:
+        assert rel_err(gh[filled], oh[filled]) < 1e-4
+        assert rel_err(gy[filled], oy[filled]) < 1e-4
+    # rows that hold no token (padding and past the last segment) are never written
+    tail = ~filled
+    if tail.any():
+        tt = torch.from_numpy(tail).cuda()
+        assert torch.isnan(h.float()[tt]).all() and torch.isnan(y[tt]).all()

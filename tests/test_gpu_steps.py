@@ -10,7 +10,8 @@ import torch
 
 import moe_inputs
 import oracle
-from helpers import check_layout_properties, rel_err, to_f64, within_bf16_rounding
+from helpers import (assert_grouped_parity as _assert_grouped_parity, check_layout_properties,
+                     rel_err, to_f64, within_bf16_rounding)
 
 pytestmark = pytest.mark.gpu
 
@@ -470,42 +471,6 @@ def test_grouped_swiglu_parity(moe, dt, T, E_local, k, D, H, align, kernel, monk
     monkeypatch.setenv("MOE_GROUPED_KERNEL", kernel)
     lay, xp, w1, w3, w2, h, y = _grouped_case(moe, dt, T, E_local, k, D, H, align, seed=T + H)
     _assert_grouped_parity(lay, xp, w1, w3, w2, h, y, dt == "bf16")
-
-
-def _assert_grouped_parity(lay, xp, w1, w3, w2, h, y, rb):
-    H_ = moe_inputs.host_array
-    seg, cnt = lay["seg_offsets"], lay["tokens_per_expert"]
-    E_local = len(cnt)
-    oh = oracle.grouped_gemm1_swiglu(H_(xp), seg, cnt, list(H_(w1)), list(H_(w3)), round_h=rb)
-    filled = lay["token_of_row"] >= 0
-    gh = to_f64(h)
-    # second GEMM from the oracle's own h (no GPU value feeds the oracle)
-    ohb = oh.astype(np.float32)
-    oy = oracle.grouped_gemm2(ohb, seg, cnt, list(H_(w2)))
-    gy = to_f64(y)
-    if rb:
-        # h is a bf16 intermediate rounded once on each side: compared per element
-        assert within_bf16_rounding(gh[filled], oh[filled]) <= 1.0
-        # y (fp32) differs by what those h differences carry through w2, plus
-        # fp32 accumulation error: |dy| <= |dh| |w2|^T + 2^-20 |h| |w2|^T
-        w2h = to_f64(w2)
-        dh = np.abs(np.nan_to_num(gh) - np.nan_to_num(oh))
-        for i in range(E_local):
-            rows = np.arange(seg[i], seg[i] + cnt[i])
-            if len(rows) == 0:
-                continue
-            aw2 = np.abs(w2h[i])
-            bound = dh[rows] @ aw2.T + 2.0 ** -20 * (np.abs(oh[rows]) @ aw2.T) + 1e-30
-            assert (np.abs(gy[rows] - oy[rows]) <= bound).all(), f"expert {i}"
-        assert rel_err(gy[filled], oy[filled]) < 1e-2
-    else:
-        assert rel_err(gh[filled], oh[filled]) < 1e-4
-        assert rel_err(gy[filled], oy[filled]) < 1e-4
-    # rows that hold no token (padding and past the last segment) are never written
-    tail = ~filled
-    if tail.any():
-        tt = torch.from_numpy(tail).cuda()
-        assert torch.isnan(h.float()[tt]).all() and torch.isnan(y[tt]).all()
 
 
 @pytest.mark.parametrize("kernel", ["pair", "pair2", "single"])
