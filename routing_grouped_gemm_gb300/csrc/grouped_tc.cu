@@ -87,9 +87,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// A tile with at most TC_A16_MAX valid rows loads only those rows, in boxes
+// of 16 (tmA16), instead of the whole 128-row A box; the rows past them hold
+// whatever the stage held before and give output rows that are not stored.
+// (Masked decode: about four rows per expert, so the full box read 32x the
+// needed bytes of x_perm and h.)
+constexpr int TC_A16_MAX = 64;
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
-grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                  const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
+grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA16,
+                  const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                  const TcParams p) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     extern __shared__ uint8_t smem_raw[];
@@ -125,6 +133,7 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             *abort_flag = 0;
             fence_mbarrier_init();
             prefetch_tmap(&tmA);
+            prefetch_tmap(&tmA16);
             prefetch_tmap(&tmB0);
             if (p.mode == 0) prefetch_tmap(&tmB1);
         }
@@ -150,12 +159,20 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileCoord c = decode_tile(tile, p.n_tiles, s_mtoff, s_base, s_valid, p.E_local);
+                const int na16 = c.nvalid <= TC_A16_MAX ? (c.nvalid + 15) / 16 : 0;
+                const uint32_t tx = (na16 ? na16 * 16 * TC_BK * 2 : TC_A_BYTES) + TC_B_BYTES;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], TC_STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[s], tx);
                     uint8_t *sa = ring + s * TC_STAGE_BYTES;
                     uint8_t *sb = sa + TC_A_BYTES;
-                    tma_load_2d(sa, &tmA, &full[s], kb * TC_BK, c.row0);
+                    if (na16) {
+                        for (int i = 0; i < na16; ++i)
+                            tma_load_2d(sa + i * 16 * TC_BK * 2, &tmA16, &full[s], kb * TC_BK,
+                                        c.row0 + 16 * i);
+                    } else {
+                        tma_load_2d(sa, &tmA, &full[s], kb * TC_BK, c.row0);
+                    }
                     if (p.mode == 0) {
                         tma_load_3d(sb, &tmB0, &full[s], kb * TC_BK, c.nt * 128, c.expert);
                         tma_load_3d(sb + TC_B_BYTES / 2, &tmB1, &full[s], kb * TC_BK, c.nt * 128,
@@ -304,11 +321,13 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
                                        int D, int H_local, int e_first, int E_local,
                                        int64_t rows_alloc, int *status, cudaStream_t stream) {
     if (E_local == 0 || rows_alloc == 0) return cudaSuccess;
-    CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
+    CUtensorMap tm_x, tm_x16, tm_w1, tm_w3, tm_h, tm_h16, tm_w2;
     if (!make_tmap_2d(&tm_x, x_perm, D, rows_alloc, TC_BM) ||
+        !make_tmap_2d(&tm_x16, x_perm, D, rows_alloc, 16) ||
         !make_tmap_3d(&tm_w1, w1, D, H_local, E_local, 128) ||
         !make_tmap_3d(&tm_w3, w3, D, H_local, E_local, 128) ||
         !make_tmap_2d(&tm_h, h, H_local, rows_alloc, TC_BM) ||
+        !make_tmap_2d(&tm_h16, h, H_local, rows_alloc, 16) ||
         !make_tmap_3d(&tm_w2, w2, H_local, D, E_local, TC_BN))
         return cudaErrorInvalidValue;
     const int nsm = sm_count();
@@ -332,7 +351,7 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p1.status = status;
     const long long g1 = std::min<long long>(nsm, mt_bound * p1.n_tiles);
     if ((err = launch_pdl(grouped_tc_kernel, dim3((unsigned)g1), dim3(TC_THREADS), smem, stream,
-                          tm_x, tm_w1, tm_w3, p1)) != cudaSuccess)
+                          tm_x, tm_x16, tm_w1, tm_w3, p1)) != cudaSuccess)
         return err;
     count_launch();
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -345,7 +364,7 @@ cudaError_t launch_grouped_swiglu_bf16(const void *x_perm, const int *seg_offset
     p2.out = y_perm;
     const long long g2 = std::min<long long>(nsm, mt_bound * p2.n_tiles);
     if ((err = launch_pdl(grouped_tc_kernel, dim3((unsigned)g2), dim3(TC_THREADS), smem, stream,
-                          tm_h, tm_w2, tm_w2, p2)) != cudaSuccess)
+                          tm_h, tm_h16, tm_w2, tm_w2, p2)) != cudaSuccess)
         return err;
     count_launch();
     return cudaGetLastError();
