@@ -335,11 +335,14 @@ permute_index_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
 constexpr int CS_MAX_CELLS = 8192;  // nblk * E staged in the last block's shared memory
 
 // Each block: masks of its 8 warps per expert -> wmeta[(8b + w) E + e] =
-// (mask, rows of e in warps 0..w-1 of the block) and blk_cnt[b E + e].  The
+// (mask, rows of e in warps 0..w-1 of the block) and blk_cnt[b E + e].  With
+// kScan = false that is all (small count matrices: every index+copy block
+// derives the offsets from blk_cnt).  Otherwise the
 // last block to finish stages blk_cnt in shared memory and writes
 // tokens_per_expert, seg_offsets, blk_base[b E_local + i] (the absolute
 // first row of block b in local expert i), the padding entries of
 // token_of_row and the masked-capacity flag.
+template <bool kScan>
 __global__ void __launch_bounds__(PB_TOKENS)
 permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E, int e_first,
                           int E_local, int layout, int align_m, int capacity, long long rows_alloc,
@@ -367,6 +370,7 @@ permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
         }
         blk_cnt[(size_t)b * E + e] = run;
     }
+    if (!kScan) return;  // the index+copy blocks derive the offsets themselves
     // the block's counts (ordered before thread 0 by the barrier) are
     // released with its ticket; the last block acquires all of them
     __syncthreads();
@@ -452,19 +456,102 @@ permute_count_scan_kernel(const int *__restrict__ topk_idx, int T, int k, int E,
 // for its 32-row share of the rows after the last segment.
 constexpr int IC_UNROLL = 8;
 
-template <bool kFp8>
+// Offsets of the small count matrices (kDerive): every block stages the
+// per-expert totals and its count block's prefix from blk_cnt [nblk][E],
+// scans the padded local segment sizes into seg_offsets in shared memory
+// (block 0 also writes tokens_per_expert, seg_offsets and the capacity
+// flag), so no block of the count kernel has to wait for the others.
+constexpr int DERIVE_MAX_CELLS = 2048;  // nblk * E read by every block
+
+__device__ __forceinline__ void derive_offsets(const int *__restrict__ blk_cnt, int nblk, int b,
+                                               int E, int e_first, int E_local, int layout,
+                                               int align_m, int capacity, int *s_tot, int *s_pre,
+                                               int *s_off, int *s_wsum,
+                                               int *__restrict__ tokens_per_expert,
+                                               int *__restrict__ seg_offsets, int *status) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+        int tot = 0, pre = 0;
+        for (int bb = 0; bb < nblk; ++bb) {
+            const int c = __ldcg(blk_cnt + (size_t)bb * E + e);
+            tot += c;
+            pre += bb < b ? c : 0;
+        }
+        s_tot[e] = tot;
+        s_pre[e] = pre;
+    }
+    __syncthreads();
+    const int nt = blockDim.x;
+    const int per = (E_local + nt - 1) / nt;
+    const int lo = tid * per, hi = min(E_local, lo + per);
+    int run = 0;
+    for (int i = lo; i < hi; ++i) {
+        const int c = s_tot[e_first + i];
+        const int size = layout == 1 ? capacity : (c + align_m - 1) / align_m * align_m;
+        s_off[i] = size;  // temporarily the size
+        run += size;
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_wsum[w];
+    int acc = base + incl - run;
+    for (int i = lo; i < hi; ++i) {
+        const int size = s_off[i];
+        s_off[i] = acc;
+        acc += size;
+    }
+    if (tid == nt - 1) s_off[E_local] = acc;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = tid; e < E; e += nt) tokens_per_expert[e] = s_tot[e];
+        for (int i = tid; i <= E_local; i += nt) seg_offsets[i] = s_off[i];
+        if (layout == 1)
+            for (int i = tid; i < E_local; i += nt)
+                if (s_tot[e_first + i] > capacity) raise_flag(status, FLAG_CAPACITY);
+    }
+}
+
+template <bool kFp8, bool kDerive>
 __global__ void __launch_bounds__(256)
 permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ topk_idx,
                           const int2 *__restrict__ wmeta, const int *__restrict__ blk_base,
-                          const int *__restrict__ seg_offsets, int *__restrict__ row_of,
+                          const int *__restrict__ seg_offsets_in, int *__restrict__ row_of,
                           int *__restrict__ token_of_row, uint4 *__restrict__ x_perm, int T, int k,
                           int E, int e_first, int E_local, int vpr, float4 *__restrict__ zero_out,
-                          int zvpr, const int *__restrict__ tokens_per_expert,
-                          long long rows_alloc, int cols, float *__restrict__ x_scale) {
+                          int zvpr, const int *__restrict__ tokens_per_expert_in,
+                          long long rows_alloc, int cols, float *__restrict__ x_scale,
+                          const int *__restrict__ blk_cnt, int nblk, int layout, int align_m,
+                          int capacity, int *__restrict__ tpe_out, int *__restrict__ seg_out,
+                          int *status) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    // offsets: derived here (kDerive; the whole block takes part before any
+    // warp leaves), or written by the count kernel's last block
+    extern __shared__ int s_dv[];
+    const int *seg_offsets = seg_offsets_in;
+    const int *tokens_per_expert = tokens_per_expert_in;
+    int *s_pre = nullptr;
+    if (kDerive) {
+        int *s_tot = s_dv;
+        s_pre = s_tot + E;
+        int *s_off = s_pre + E;
+        int *s_wsum = s_off + E_local + 1;
+        derive_offsets(blk_cnt, nblk, (blockIdx.x * (blockDim.x >> 5)) / PB_TOKENS, E, e_first,
+                       E_local, layout, align_m, capacity, s_tot, s_pre, s_off, s_wsum, tpe_out,
+                       seg_out, status);
+        seg_offsets = s_off;
+        tokens_per_expert = s_tot;
+    }
     if (t >= T) return;
     const int e = lane < k ? topk_idx[(size_t)t * k + lane] : -1;
     const uint4 *src = x + (size_t)t * vpr;
@@ -485,8 +572,9 @@ permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ t
     int my_row = -1;
     if (act && i >= 0 && i < E_local) {
         const int2 m = wmeta[(size_t)(t >> 5) * E + e];
-        const int cand = blk_base[(size_t)(t / PB_TOKENS) * E_local + i] + m.y +
-                         __popc((uint32_t)m.x & ((1u << (t & 31)) - 1u));
+        const int first = kDerive ? seg_offsets[i] + s_pre[e]
+                                  : blk_base[(size_t)(t / PB_TOKENS) * E_local + i];
+        const int cand = first + m.y + __popc((uint32_t)m.x & ((1u << (t & 31)) - 1u));
         if (cand < seg_offsets[i + 1]) {
             my_row = cand;
             token_of_row[cand] = t;
@@ -692,11 +780,17 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
     cudaError_t err;
     if (x_scale && (D % 8 || k > 32)) return cudaErrorInvalidValue;  // before any launch
     if (nblk > 0 && (int64_t)nblk * E <= CS_MAX_CELLS) {
+        // small count matrices: the copy blocks derive the offsets themselves
+        const bool derive = (int64_t)nblk * E <= DERIVE_MAX_CELLS;
         const size_t smem =
-            mask_smem + sizeof(int) * ((size_t)nblk * E + E + E_local + 1);
-        err = ensure_smem((const void *)permute_count_scan_kernel, smem);
+            mask_smem + (derive ? 0 : sizeof(int) * ((size_t)nblk * E + E + E_local + 1));
+        const void *ck = derive ? (const void *)permute_count_scan_kernel<false>
+                                : (const void *)permute_count_scan_kernel<true>;
+        err = ensure_smem(ck, smem);
         if (err != cudaSuccess) return err;
-        if ((err = launch_pdl(permute_count_scan_kernel, dim3(nblk), dim3(PB_TOKENS), smem, stream,
+        if ((err = launch_pdl(derive ? permute_count_scan_kernel<false>
+                                     : permute_count_scan_kernel<true>,
+                              dim3(nblk), dim3(PB_TOKENS), smem, stream,
                               topk_idx, T, k, E, e_first, E_local, layout, align_m, capacity,
                               (long long)rows_alloc, blk_cnt, wmeta, blk_base, ticket,
                               tokens_per_expert, seg_offsets, token_of_row, status)) != cudaSuccess)
@@ -704,14 +798,21 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
         count_launch();
         const int warps_per_block = 8;
         const int blocks = (T + warps_per_block - 1) / warps_per_block;
-        if ((err = launch_pdl(x_scale ? permute_index_copy_kernel<true>
-                                      : permute_index_copy_kernel<false>,
-                              dim3(blocks), dim3(32 * warps_per_block), 0, stream,
+        const size_t csmem = derive ? sizeof(int) * (2 * (size_t)E + E_local + 1 + 8) : 0;
+        auto copy_kernel = x_scale ? (derive ? permute_index_copy_kernel<true, true>
+                                             : permute_index_copy_kernel<true, false>)
+                                   : (derive ? permute_index_copy_kernel<false, true>
+                                             : permute_index_copy_kernel<false, false>);
+        if (csmem > 0 && (err = ensure_smem((const void *)copy_kernel, csmem)) != cudaSuccess)
+            return err;
+        if ((err = launch_pdl(copy_kernel, dim3(blocks), dim3(32 * warps_per_block), csmem, stream,
                               (const uint4 *)x, topk_idx, (const int2 *)wmeta,
                               (const int *)blk_base, (const int *)seg_offsets, row_of, token_of_row,
                               (uint4 *)x_perm, T, k, E, e_first, E_local, D * elem_bytes / 16,
                               (float4 *)zero_out, D / 4, (const int *)tokens_per_expert,
-                              (long long)rows_alloc, D, x_scale)) != cudaSuccess)
+                              (long long)rows_alloc, D, x_scale, (const int *)blk_cnt, nblk,
+                              layout, align_m, capacity, tokens_per_expert, seg_offsets,
+                              status)) != cudaSuccess)
             return err;
         count_launch();
         return cudaGetLastError();
