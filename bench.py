@@ -66,12 +66,12 @@ def algorithmic(w, R=None, touched=None):
         # the method's combine bytes: y rows read once, out written once, the
         # row index and weight of every slot
         combine_bytes=float(R * w.D * b + w.T * w.D * b + R * 8),
-        # what the combine moves here: y_perm is the second GEMM's fp32 accumulator
-        combine_bytes_moved=float(R * w.D * 4 + w.T * w.D * b + R * 8),
+        # what the combine moves here: y_perm is fp16 (bf16 layers) or fp32
+        combine_bytes_moved=float(R * w.D * b + w.T * w.D * b + R * 8),
         # the grouped call when it streams weights (masked decode): the touched
         # experts' w1, w3, w2 once, x_perm rows read, h written and read, y written
         grouped_bytes=float(touched * 3 * w.D * w.H * b + R * w.D * b + 2 * R * w.H * b
-                            + R * w.D * 4),
+                            + R * w.D * b),
         weight_bytes=float(w.E * 3 * w.D * w.H * b),
     )
 
@@ -684,7 +684,7 @@ def roofline(w, moe, cfg, gemm_ms, R, touched, peaks, gemm_launches, dev):
                 "traffic": recorded_traffic(w.name),
                 "algorithmic_bytes_per_call": alg["grouped_bytes"],
                 "algorithmic_bytes_note": "touched experts' w1, w3, w2 once + x_perm rows read + "
-                                          "h written and read + fp32 y written",
+                                          "h written and read + y written (fp16)",
                 "touched_experts": touched, "tflops": alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12}
     achieved = alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12
     if w.dtype == "f32":
@@ -760,7 +760,7 @@ def run_gpu(args, name):
     tor = torch.empty(ra, dtype=torch.int32, device=dev)
     x_perm = torch.empty((ra, w.D), dtype=dt, device=dev)
     h = torch.empty((ra, w.H), dtype=dt, device=dev)
-    y_perm = torch.empty((ra, w.D), dtype=torch.float32, device=dev)
+    y_perm = torch.empty((ra, w.D), dtype=cfg.y_dtype, device=dev)
     out = torch.empty((w.T, w.D), dtype=dt, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev) if needs_l2_flush(w) else None
@@ -881,7 +881,8 @@ def run_gpu(args, name):
             "combine_gbs": alg["combine_bytes"] / (mean_parts[3] * 1e-3) / 1e9,
             "combine_gbs_moved": alg["combine_bytes_moved"] / (mean_parts[3] * 1e-3) / 1e9,
             "combine_note": "combine_gbs counts the method's bytes (y rows at the activation "
-                            "width); combine_gbs_moved counts the fp32 y_perm actually read",
+                            "width); combine_gbs_moved counts the y_perm actually read (fp16 for "
+                            "bf16 layers, so the two agree there)",
             "hbm_peak_gbs": peaks["hbm_gbs"]},
         "gemm_tflops": alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12,
         "tokens_per_expert": {"min": int(tpe_h.min()), "max": int(tpe_h.max()),
@@ -959,7 +960,7 @@ def run_dispatch_bandwidth(args):
         row_of = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
         tor = torch.empty(ra, dtype=torch.int32, device=dev)
         xp = torch.empty((ra, w.D), dtype=torch.bfloat16, device=dev)
-        y = torch.randn((ra, w.D), dtype=torch.float32, device=dev)
+        y = torch.randn((ra, w.D), dtype=torch.float32, device=dev).to(cfg.y_dtype)
         out = torch.empty((w.T, w.D), dtype=torch.bfloat16, device=dev)
         calls = {
             "permute": lambda: moe.moe_permute(cfg, inp.x, idx, tpe, seg, row_of, tor, xp, ws),
@@ -969,7 +970,7 @@ def run_dispatch_bandwidth(args):
         assert moe.moe_get_device_status(ws) == moe.MOE_OK
         R = int((row_of >= 0).sum().item())
         nbytes = {"permute": w.T * w.D * 2 + R * w.D * 2,
-                  "combine": R * w.D * 4 + w.T * w.D * 2 + w.T * w.k * 8}
+                  "combine": R * w.D * 2 + w.T * w.D * 2 + w.T * w.k * 8}
         line = {"workload": name, "T": w.T, "D": w.D, "E": w.E, "k": w.k, "routed_rows": R,
                 "l2": "flushed before every call", "steps": args.steps, "warmup": args.warmup}
         for key, fn in calls.items():

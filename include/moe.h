@@ -27,8 +27,11 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller, dense,
  *     row-major, and 16-byte aligned.  The library allocates nothing.
  *   - Element type of x, W_g, weights, x_perm, h and out is cfg->dtype
- *     (MOE_F32 or MOE_BF16).  y_perm (the second GEMM's accumulator), router
- *     bias, logits and topk_w are always fp32; indices are int32.
+ *     (MOE_F32 or MOE_BF16).  y_perm (the second GEMM's result per routed
+ *     row) is fp32 for MOE_F32 and fp16 for MOE_BF16: the fp32 accumulator
+ *     rounded once to nearest-even fp16, which keeps 3 more significant bits
+ *     than bf16 at half the bytes of fp32.  Router bias, logits and topk_w
+ *     are always fp32; indices are int32.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
  *     legacy default stream) and performs no host synchronisation.
  *   - Host-side argument errors are returned before anything is launched.
@@ -190,9 +193,12 @@ moe_status moe_permute(const moe_config *cfg, const void *x, const int32_t *topk
  *   w1, w3 [E_local, H_local, D]; w2 [E_local, D, H_local] (dtype).
  *   h [rows_alloc, H_local] (dtype, written for valid rows):
  *     h = SiLU(x_perm w1^T) * (x_perm w3^T), fp32 accumulation, one rounding.
- *   y_perm [rows_alloc, D] fp32 (written for valid rows): y = h w2^T, the
- *     fp32 accumulator itself -- it is rounded to dtype only after the
- *     weighted combine.
+ *   y_perm [rows_alloc, D] (written for valid rows): y = h w2^T accumulated
+ *     in fp32; stored as that fp32 value for MOE_F32, rounded once to fp16
+ *     for MOE_BF16.  A bf16 result that fp16 cannot hold (|y| >= 65520,
+ *     which rounds to infinity) is flagged in the status word:
+ *     moe_get_device_status then returns MOE_ERR_UNSUPPORTED (the stored
+ *     value is +-inf).  The weighted combine widens the fp16 value to fp32.
  *   Rows that hold no token (padding) and rows of other segments are never
  *   written.
  * Segments may have any length; offsets outside [0, rows_alloc] flag
@@ -208,8 +214,9 @@ moe_status moe_grouped_swiglu(const moe_config *cfg, const void *x_perm,
  * (EP)", section 1 combine post-process; section 5: the transpose of the
  * dispatch permute).
  *   out[t, :] = sum_{j < k, row_of[t,j] >= 0} topk_w[t, j] * y_perm[row_of[t, j], :]
- * y_perm [rows_alloc, D] fp32; summed in fp32 in slot order j, rounded once
- * to dtype into out [T, D].  Tokens with no
+ * y_perm [rows_alloc, D] (fp32 for MOE_F32, fp16 for MOE_BF16, as
+ * moe_grouped_swiglu writes it); summed in fp32 in slot order j, rounded
+ * once to dtype into out [T, D].  Tokens with no
  * local expert get zeros.  Rows >= rows_alloc flag MOE_ERR_BAD_ROUTING and
  * are skipped.
  */
@@ -392,11 +399,12 @@ moe_status moe_permute_fp8(const moe_config *cfg, const void *x, const int32_t *
 /*
  * moe_grouped_swiglu with GEMM1 on e4m3 operands:
  *   g = s_x[r] s_w1[e, n] sum_d q_x[r, d] q_w1[e, n, d],  u likewise with w3,
- *   h[r, n] = bf16(SiLU(g) u),  y_perm = h w2_e^T (bf16 x bf16, fp32).
+ *   h[r, n] = bf16(SiLU(g) u),  y_perm = fp16(h w2_e^T) (bf16 x bf16, fp32
+ *   accumulation, one rounding).
  * x_perm_q / x_scale as moe_permute_fp8 writes them; w1_q, w3_q
  * [E_local, H_local, D] codes with w1_scale, w3_scale [E_local, H_local]
  * (moe_quantize_rows_fp8 of the bf16 weights); w2 bf16 [E_local, D, H_local];
- * h bf16 [rows_alloc, H_local], y_perm fp32 [rows_alloc, D].
+ * h bf16 [rows_alloc, H_local], y_perm fp16 [rows_alloc, D].
  * MOE_ERR_UNSUPPORTED for more local experts than the CTA-pair kernel's
  * shared-memory tile table holds.
  */
@@ -515,7 +523,8 @@ moe_status moe_permute_noalloc(const moe_config *cfg, const void *x, const int32
  * returns the most serious flagged condition (MOE_OK if none).  Order:
  * TIMEOUT, then MOE_ERR_CUDA for a kernel that found itself launched
  * without the thread-block cluster it needs (it did no work), then
- * CAPACITY, BAD_ROUTING.
+ * MOE_ERR_UNSUPPORTED for a bf16 expert output beyond fp16's range in
+ * y_perm, then CAPACITY, BAD_ROUTING.
  */
 moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe_stream_t stream);
 

@@ -143,6 +143,11 @@ class Config:
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == MOE_BF16 else torch.float32
 
+    @property
+    def y_dtype(self) -> torch.dtype:
+        """Element type of y_perm: fp16 for bf16 layers, fp32 for fp32 ones."""
+        return torch.float16 if self.dtype == MOE_BF16 else torch.float32
+
 
 def status_string(st: int) -> str:
     return _lib.moe_status_string(int(st)).decode()
@@ -326,7 +331,7 @@ def moe_grouped_swiglu(cfg: Config, x_perm, seg_offsets, tokens_per_expert, w1, 
     _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
     _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
     _expect(h, (ra, cfg.H_local), dt, "h")
-    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    _expect(y_perm, (ra, cfg.D), cfg.y_dtype, "y_perm")
     c = cfg.c()
     _check(_lib.moe_grouped_swiglu(ctypes.byref(c), _ptr(x_perm), _ptr(seg_offsets),
                                    _ptr(tokens_per_expert), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(h),
@@ -337,7 +342,7 @@ def moe_grouped_swiglu(cfg: Config, x_perm, seg_offsets, tokens_per_expert, w1, 
 def moe_unpermute_combine(cfg: Config, y_perm, row_of, topk_w, out, ws, stream=None):
     ra = rows_alloc(cfg)
     dt = cfg.torch_dtype
-    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    _expect(y_perm, (ra, cfg.D), cfg.y_dtype, "y_perm")
     _expect(row_of, (cfg.T, cfg.k), torch.int32, "row_of")
     _expect(topk_w, (cfg.T, cfg.k), torch.float32, "topk_w")
     _expect(out, (cfg.T, cfg.D), dt, "out")
@@ -552,7 +557,7 @@ def moe_grouped_swiglu_fp8(cfg: Config, x_perm_q, x_scale, seg_offsets, tokens_p
     _expect(w3_scale, (el, cfg.H_local), torch.float32, "w3_scale")
     _expect(w2, (el, cfg.D, cfg.H_local), torch.bfloat16, "w2")
     _expect(h, (ra, cfg.H_local), torch.bfloat16, "h")
-    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    _expect(y_perm, (ra, cfg.D), cfg.y_dtype, "y_perm")
     c = cfg.c()
     _check(_lib.moe_grouped_swiglu_fp8(ctypes.byref(c), _ptr(x_perm_q), _ptr(x_scale),
                                        _ptr(seg_offsets), _ptr(tokens_per_expert), _ptr(w1_q),
@@ -595,7 +600,7 @@ def moe_grouped_swiglu_gather(cfg: Config, x, token_of_row, seg_offsets, tokens_
     _expect(w3, (el, cfg.H_local, cfg.D), dt, "w3")
     _expect(w2, (el, cfg.D, cfg.H_local), dt, "w2")
     _expect(h, (ra, cfg.H_local), dt, "h")
-    _expect(y_perm, (ra, cfg.D), torch.float32, "y_perm")
+    _expect(y_perm, (ra, cfg.D), cfg.y_dtype, "y_perm")
     c = cfg.c()
     _check(_lib.moe_grouped_swiglu_gather(ctypes.byref(c), _ptr(x), _ptr(token_of_row),
                                           _ptr(seg_offsets), _ptr(tokens_per_expert), _ptr(w1),
@@ -661,7 +666,6 @@ def layer_views(cfg: Config, ws: torch.Tensor) -> dict:
     ra = rows_alloc(cfg)
     el = cfg.e_local
     dt = cfg.torch_dtype
-    eb = 2 if cfg.dtype == MOE_BF16 else 4
     out = {}
     for name, n, tdt, shape in (
             ("topk_idx", R, torch.int32, (cfg.T, cfg.k)),
@@ -672,12 +676,15 @@ def layer_views(cfg: Config, ws: torch.Tensor) -> dict:
             ("token_of_row", ra, torch.int32, (ra,)),
             ("x_perm", ra * cfg.D, dt, (ra, cfg.D)),
             ("h", ra * cfg.H_local, dt, (ra, cfg.H_local)),
-            ("y_perm", ra * cfg.D, torch.float32, (ra, cfg.D)),
+            ("y_perm", ra * cfg.D, cfg.y_dtype, (ra, cfg.D)),
             ("x_scale", ra, torch.float32, (ra,))):
-        nbytes = n * (4 if tdt in (torch.int32, torch.float32) else eb)
+        nbytes = n * (4 if tdt in (torch.int32, torch.float32) else 2)
+        region = nbytes
+        if name == "y_perm" and cfg.dtype == MOE_BF16:
+            region = max(nbytes, cfg.T * cfg.D * 4)   # also holds the fused combine's fp32 sums
         out[name] = ws[off:off + nbytes].view(tdt).view(shape)
         if name == "x_perm":
             # moe_layer_forward_fp8 keeps the e4m3 codes at the start of this buffer
             out["x_perm_q"] = ws[off:off + ra * cfg.D].view(ra, cfg.D)
-        off += up(nbytes)
+        off += up(region)
     return out

@@ -40,12 +40,12 @@ __device__ __forceinline__ void load4(const void *p, size_t i, bool bf16, float 
 }
 
 // One warp per token.  gy[row] = bf16(w_j * dout[t]) for each slot j whose
-// row is in the buffer; dw[t, j] = <dout[t], y_perm[row]> (fp32: each lane
-// sums its columns in order, then the lanes' sums are added in a fixed
-// butterfly order), 0 for a slot without row.
+// row is in the buffer; dw[t, j] = <dout[t], y_perm[row]> (y_perm fp16, the
+// products and sums fp32: each lane sums its columns in order, then the
+// lanes' sums are added in a fixed butterfly order), 0 for a slot without row.
 template <bool BF16>
 __global__ void __launch_bounds__(128)
-combine_bwd_kernel(const void *__restrict__ dout, const float *__restrict__ y_perm,
+combine_bwd_kernel(const void *__restrict__ dout, const __half *__restrict__ y_perm,
                    const int *__restrict__ row_of, const float *__restrict__ topk_w,
                    __nv_bfloat16 *__restrict__ gy, float *__restrict__ dw, int T, int k, int D,
                    long long rows_alloc, int *status) {
@@ -78,18 +78,20 @@ combine_bwd_kernel(const void *__restrict__ dout, const float *__restrict__ y_pe
         for (int d0 = lane * 4; d0 < D; d0 += 128) {
             float g[4];
             load4(dout, (size_t)t * D + d0, BF16, g);
-            float4 y[BW_SLOTS];
+            uint2 y[BW_SLOTS];
 #pragma unroll
             for (int u = 0; u < BW_SLOTS; ++u)
                 if (r[u] >= 0)
-                    y[u] = __ldcs(reinterpret_cast<const float4 *>(y_perm + (size_t)r[u] * D + d0));
+                    y[u] = __ldcs(reinterpret_cast<const uint2 *>(y_perm + (size_t)r[u] * D + d0));
 #pragma unroll
             for (int u = 0; u < BW_SLOTS; ++u) {
                 if (r[u] < 0) continue;
-                dot[u] = fmaf(g[0], y[u].x, dot[u]);
-                dot[u] = fmaf(g[1], y[u].y, dot[u]);
-                dot[u] = fmaf(g[2], y[u].z, dot[u]);
-                dot[u] = fmaf(g[3], y[u].w, dot[u]);
+                const float2 ya = __half22float2(*reinterpret_cast<const __half2 *>(&y[u].x));
+                const float2 yb = __half22float2(*reinterpret_cast<const __half2 *>(&y[u].y));
+                dot[u] = fmaf(g[0], ya.x, dot[u]);
+                dot[u] = fmaf(g[1], ya.y, dot[u]);
+                dot[u] = fmaf(g[2], yb.x, dot[u]);
+                dot[u] = fmaf(g[3], yb.y, dot[u]);
                 __nv_bfloat162 lo = __floats2bfloat162_rn(w[u] * g[0], w[u] * g[1]);
                 __nv_bfloat162 hi = __floats2bfloat162_rn(w[u] * g[2], w[u] * g[3]);
                 uint2 o;
@@ -500,17 +502,17 @@ cudaError_t router_gemm(const float *a, long long a_m, long long a_k, const void
 
 }  // namespace
 
-cudaError_t launch_combine_bwd(const void *dout, const float *y_perm, const int *row_of,
+cudaError_t launch_combine_bwd(const void *dout, const void *y_perm, const int *row_of,
                                const float *topk_w, void *gy, float *dw, int T, int D, int k,
                                int64_t rows_alloc, int is_bf16, int *status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const dim3 grid((unsigned)((T + 3) / 4));  // 4 warps (tokens) per block
     const cudaError_t e =
-        is_bf16 ? launch_pdl(combine_bwd_kernel<true>, grid, dim3(128), 0, stream, dout, y_perm,
-                             row_of, topk_w, (__nv_bfloat16 *)gy, dw, T, k, D, (long long)rows_alloc,
+        is_bf16 ? launch_pdl(combine_bwd_kernel<true>, grid, dim3(128), 0, stream, dout,
+                             (const __half *)y_perm, row_of, topk_w, (__nv_bfloat16 *)gy, dw, T, k, D, (long long)rows_alloc,
                              status)
-                : launch_pdl(combine_bwd_kernel<false>, grid, dim3(128), 0, stream, dout, y_perm,
-                             row_of, topk_w, (__nv_bfloat16 *)gy, dw, T, k, D, (long long)rows_alloc,
+                : launch_pdl(combine_bwd_kernel<false>, grid, dim3(128), 0, stream, dout,
+                             (const __half *)y_perm, row_of, topk_w, (__nv_bfloat16 *)gy, dw, T, k, D, (long long)rows_alloc,
                              status);
     if (e == cudaSuccess) count_launch();
     return e;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,7 +14,12 @@ enum : int {
     FLAG_CAPACITY = 2,
     FLAG_TIMEOUT = 4,
     FLAG_LAUNCH = 8,  // a kernel found itself launched in a shape it cannot run (no work done)
+    FLAG_RANGE = 16,  // an expert output beyond the fp16 range of y_perm (bf16 layers)
 };
+
+// The smallest magnitude that rounds to infinity in IEEE binary16 (round to
+// nearest even): 65504 + half an ulp (16).
+constexpr float kHalfOverflow = 65520.f;
 
 // Status block at the start of every workspace.
 struct StatusBlock {
@@ -22,6 +28,11 @@ struct StatusBlock {
     int pad[62];
 };
 static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 
 __device__ __forceinline__ void raise_flag(int *status, int f) {
     if (status) atomicOr(status, f);

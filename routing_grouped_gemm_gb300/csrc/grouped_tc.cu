@@ -21,8 +21,8 @@
 //     one N=256 B tile, so each accumulator holds gate and up for the same
 //     hidden units and the epilogue writes h = SiLU(gate) * up directly;
 //   * GEMM2 (mode 1) is a plain N=256 tile of w2; its fp32 accumulator is
-//     stored as is (y_perm stays fp32 until the weighted combine rounds the
-//     token's output once).
+//     stored as fp16 (11 significant bits; the weighted combine sums in fp32
+//     and rounds the token's output to bf16 once).
 //   * every mbarrier wait is bounded; a wait that runs out raises
 //     FLAG_TIMEOUT, the CTA drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -53,7 +53,7 @@ struct TcParams {
     int rows_alloc;
     const int *seg_off;
     const int *tpe;
-    void *out;      // mode 0: bf16 h [rows, H_local]; mode 1: fp32 y [rows, D]
+    void *out;      // mode 0: bf16 h [rows, H_local]; mode 1: fp16 y [rows, D]
     int *status;
 };
 
@@ -275,7 +275,8 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
             } else {
-                float *yrow = static_cast<float *>(p.out) + orow;
+                __half *yrow = static_cast<__half *>(p.out) + orow;
+                bool over = false;  // a stored value beyond the fp16 range
 #pragma unroll 1
                 for (int ch = 0; ch < TC_BN / 32; ++ch) {
                     uint32_t d[32];
@@ -284,13 +285,22 @@ grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const int col0 = c.nt * TC_BN + ch * 32;
                     if (row_ok) {
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            if (col0 + v * 4 >= p.N_out) break;
-                            *reinterpret_cast<uint4 *>(yrow + col0 + v * 4) =
-                                make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2], d[v * 4 + 3]);
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 >= p.N_out) break;
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const float a = __uint_as_float(d[v * 8 + e2 * 2]);
+                                const float b = __uint_as_float(d[v * 8 + e2 * 2 + 1]);
+                                over |= fabsf(a) >= kHalfOverflow || fabsf(b) >= kHalfOverflow;
+                                w[e2] = pack_half2(a, b);
+                            }
+                            *reinterpret_cast<uint4 *>(yrow + col0 + v * 8) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
+                if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(p.status, FLAG_RANGE);
             }
             tc_fence_before();
             __syncwarp();

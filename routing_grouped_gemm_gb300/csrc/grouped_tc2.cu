@@ -17,7 +17,9 @@
 //     rows of w3, so the pair's N=256 columns are [gate, up] of hidden units
 //     n0..n0+63 and then of n0+64..n0+127; the epilogue pairs column c with
 //     c+64 and writes h = SiLU(gate) * up directly.  GEMM2: the two CTAs hold
-//     consecutive 128-row halves of a 256-row w2 tile and store y in fp32;
+//     consecutive 128-row halves of a 256-row w2 tile and store y in fp16
+//     (the fp32 accumulator rounded once; a value beyond the fp16 range
+//     raises FLAG_RANGE);
 //   * an expert's last tile with at most 128 valid rows runs as an M=128
 //     pair MMA (64 rows per CTA) instead of M=256, so segments are padded to
 //     128 rows as with single-SM tiles.  With M=128 each CTA's 64 rows sit in
@@ -58,8 +60,8 @@ constexpr int P_BM = 128;                        // rows per CTA
 constexpr int P_PAIR_M = 2 * P_BM;               // rows per pair tile
 constexpr int P_BN = 256;                        // N of the pair MMA
 constexpr int P_BK = 64;
-// GEMM2's fp32 y through shared memory and TMA stores (1) or straight
-// from registers (0); the staging takes one ring stage's worth of smem.
+// GEMM2's y through shared memory and TMA stores (1) or straight from
+// registers (0); the staging takes one ring stage's worth of smem.
 #ifndef MOE_PAIR_TMA_Y
 #define MOE_PAIR_TMA_Y 1
 #endif
@@ -101,8 +103,8 @@ constexpr int P_NBARS = 24;
 constexpr int P_SWAP_MAX = MOE_PAIR_SWAP_MAX;
 static_assert(P_SWAP_MAX <= P_PAIR_M, "a transposed tile holds at most 256 tokens");
 constexpr int P_XBUF_BYTES = 2 * 32 * 32 * 4;  // GEMM1 transposed tiles: up -> gate handoff
-// GEMM2 y staging: per epilogue warp two 32 x 32 fp32 boxes (128-byte swizzle)
-constexpr int P_YBOX_BYTES = 32 * 32 * 4;
+// GEMM2 y staging: per epilogue warp two boxes of 32 rows x 64 fp16 (128-byte swizzle)
+constexpr int P_YBOX_BYTES = 32 * 64 * 2;
 constexpr int P_YSTAGE_BYTES = MOE_PAIR_TMA_Y ? P_EPI_WARPS * 2 * P_YBOX_BYTES : 0;
 
 
@@ -140,7 +142,7 @@ struct PairParams {
     const int *token_of_row, *row_of;
     const float *topk_w;
     int k;
-    void *out1;           // fp32 y [rows, D]
+    void *out1;           // fp16 y [rows, D]
     int *done;            // SCHED_BOTH: [max_blocks] GEMM1 epilogue warps finished, per block
     int max_blocks;       // SCHED_BOTH: entries of done[]
     int *finish;          // SCHED_BOTH: CTAs finished; the last one zeroes done[] and itself
@@ -430,9 +432,9 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
         // Each warp owns 32 accumulator rows (its TMEM lane quarter).  h
         // (GEMM1) goes out straight from registers, valid rows only.  GEMM2's
-        // fp32 y goes out through a swizzled smem box and a TMA store per
-        // 32-column chunk (double-buffered) when all 32 of the warp's rows are
-        // valid, else straight from registers as well, so rows without a
+        // y, rounded to fp16, goes out through a swizzled smem box and a TMA
+        // store per 64 columns (double-buffered) when all 32 of the warp's rows
+        // are valid, else straight from registers as well, so rows without a
         // token are never written.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint8_t *ybuf = ystage + (warp - 2) * 2 * P_YBOX_BYTES;
@@ -455,9 +457,10 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const int l = q * 32 + lane;
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_ACC_COLS);
                 if (c.mode == 1) {
-                    // y column of this lane; each store is 32 consecutive fp32 of one row
+                    // y column of this lane; each store is 32 consecutive fp16 of one row
                     const int dcol = c.nt * P_BN + (int)rank * 128 + l;
-                    float *ycol = static_cast<float *>(p.out1) + (size_t)c.row0 * p.n_out1 + dcol;
+                    __half *ycol = static_cast<__half *>(p.out1) + (size_t)c.row0 * p.n_out1 + dcol;
+                    bool over = false;  // a stored value beyond the fp16 range
 #pragma unroll 1
                     for (int ch = 0; ch < nsw / 32; ++ch) {
                         uint32_t d[32];
@@ -477,14 +480,17 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                             const int tj = p.comb ? __shfl_sync(0xffffffffu, tl, j) : -1;
                             const float wj = p.comb ? __shfl_sync(0xffffffffu, wl, j) : 0.f;
                             if (dcol < p.n_out1 && ch * 32 + j < c.nvalid) {
-                                if (!p.comb)
-                                    ycol[(size_t)(ch * 32 + j) * p.n_out1] = __uint_as_float(d[j]);
-                                else if (tj >= 0)
+                                if (!p.comb) {
+                                    const float v = __uint_as_float(d[j]);
+                                    over |= fabsf(v) >= kHalfOverflow;
+                                    ycol[(size_t)(ch * 32 + j) * p.n_out1] = __float2half_rn(v);
+                                } else if (tj >= 0)
                                     atomicAdd(p.comb + (size_t)tj * p.n_out1 + dcol,
                                               wj * __uint_as_float(d[j]));
                             }
                         }
                     }
+                    if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(p.status, FLAG_RANGE);
                 } else {
                     // lanes 0-63: gate of hidden unit u, lanes 64-127: up of the same
                     // units.  The up warps (quarters 2, 3) hand their values to the
@@ -638,7 +644,8 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         }
                     }
                 } else {
-                    float *yrow = static_cast<float *>(p.out1) + orow;
+                    // y in fp16: two 32-column TMEM chunks make one 128-byte row of 64 values
+                    __half *yrow = static_cast<__half *>(p.out1) + orow;
                     const int nch = half ? 4 : P_BN / 32;
                     // this warp's 32 rows start at wrow within the CTA's rows
                     const int wrow = half ? (q & 1) * 32 : q * 32;
@@ -651,12 +658,36 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         wr = slot_weight(p, crow0 + r, tok);
                     }
                     float *crow = p.comb && tok >= 0 ? p.comb + (size_t)tok * n_out : nullptr;
+                    bool over = false;  // a stored value beyond the fp16 range
 #pragma unroll 1
-                    for (int ch = 0; ch < nch; ++ch) {
-                        uint32_t d[32];
-                        tmem_ld_32x32b_x32(tbase + ch * 32, d);
+                    for (int ch = 0; ch < nch; ch += 2) {
+                        uint32_t d[64];
+                        tmem_ld_32x32b_x32(tbase + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(d));
+                        tmem_ld_32x32b_x32(tbase + (ch + 1) * 32,
+                                           *reinterpret_cast<uint32_t(*)[32]>(d + 32));
                         tc_wait_ld();
                         const int col0 = c.nt * P_BN + nhalf * 128 + ch * 32;
+                        if (p.comb) {
+                            if (row_ok && crow) {
+#pragma unroll
+                                for (int v = 0; v < 16; ++v) {
+                                    if (col0 + v * 4 >= n_out) break;
+                                    atomicAdd(reinterpret_cast<float4 *>(crow + col0 + v * 4),
+                                              make_float4(wr * __uint_as_float(d[v * 4]),
+                                                          wr * __uint_as_float(d[v * 4 + 1]),
+                                                          wr * __uint_as_float(d[v * 4 + 2]),
+                                                          wr * __uint_as_float(d[v * 4 + 3])));
+                                }
+                            }
+                            continue;
+                        }
+                        uint32_t hv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float a = __uint_as_float(d[2 * i]), b = __uint_as_float(d[2 * i + 1]);
+                            over |= fabsf(a) >= kHalfOverflow || fabsf(b) >= kHalfOverflow;
+                            hv[i] = pack_half2(a, b);
+                        }
                         if (tma_y) {
                             if (col0 >= n_out) continue;  // uniform across the warp
                             if (lane == 0) bulk_wait_group_read<1>();  // this box's last store has read it
@@ -666,7 +697,7 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
                                 *reinterpret_cast<uint4 *>(brow + ((j ^ (lane & 7)) << 4)) =
-                                    make_uint4(d[j * 4], d[j * 4 + 1], d[j * 4 + 2], d[j * 4 + 3]);
+                                    make_uint4(hv[j * 4], hv[j * 4 + 1], hv[j * 4 + 2], hv[j * 4 + 3]);
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
@@ -680,20 +711,13 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         if (row_ok) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
-                                if (col0 + v * 4 >= n_out) break;
-                                if (!p.comb) {
-                                    *reinterpret_cast<uint4 *>(yrow + col0 + v * 4) =
-                                        make_uint4(d[v * 4], d[v * 4 + 1], d[v * 4 + 2], d[v * 4 + 3]);
-                                } else if (crow) {
-                                    atomicAdd(reinterpret_cast<float4 *>(crow + col0 + v * 4),
-                                              make_float4(wr * __uint_as_float(d[v * 4]),
-                                                          wr * __uint_as_float(d[v * 4 + 1]),
-                                                          wr * __uint_as_float(d[v * 4 + 2]),
-                                                          wr * __uint_as_float(d[v * 4 + 3])));
-                                }
+                                if (col0 + v * 8 >= n_out) break;
+                                *reinterpret_cast<uint4 *>(yrow + col0 + v * 8) =
+                                    make_uint4(hv[v * 4], hv[v * 4 + 1], hv[v * 4 + 2], hv[v * 4 + 3]);
                             }
                         }
                     }
+                    if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(p.status, FLAG_RANGE);
                 }
             }
             }
@@ -1010,7 +1034,7 @@ cudaError_t launch_grouped_swiglu_bf16_pair(const void *x_perm, const int *seg_o
         !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
         !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
         !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128) ||
-        !make_tmap_tile(&m.y, y_perm, 4, D, rows_alloc, 0, 32, 32, 128))
+        !make_tmap_tile(&m.y, y_perm, 2, D, rows_alloc, 0, 64, 32, 128))
         return cudaErrorInvalidValue;
     PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
                                E_local, rows_alloc, status);
@@ -1063,7 +1087,7 @@ cudaError_t launch_grouped_swiglu_fp8_pair(const uint8_t *x_perm_q, const float 
         !make_tmap_2d(&m.h64, h, H_local, rows_alloc, P_BM / 2) ||
         !make_tmap_2d(&m.h16, h, H_local, rows_alloc, 16) ||
         !make_tmap_3d(&m.w2, w2, H_local, D, E_local, 128) ||
-        !make_tmap_tile(&m.y, y_perm, 4, D, rows_alloc, 0, 32, 32, 128))
+        !make_tmap_tile(&m.y, y_perm, 2, D, rows_alloc, 0, 64, 32, 128))
         return cudaErrorInvalidValue;
     PairParams p = pair_params(seg_offsets, tokens_per_expert, h, y_perm, D, H_local, e_first,
                                E_local, rows_alloc, status);

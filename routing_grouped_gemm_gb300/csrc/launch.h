@@ -176,7 +176,7 @@ int64_t grouped_bwd_smem(int E_local);
 
 // Backward of the combine: gy[row] = bf16(w * dout[t]) (rows without a token
 // untouched) and dw[t, j] = <dout[t], y_perm[row]>.
-cudaError_t launch_combine_bwd(const void *dout, const float *y_perm, const int *row_of,
+cudaError_t launch_combine_bwd(const void *dout, const void *y_perm, const int *row_of,
                                const float *topk_w, void *gy, float *dw, int T, int D, int k,
                                int64_t rows_alloc, int is_bf16, int *status, cudaStream_t stream);
 

@@ -2,6 +2,8 @@
 // carving and the launch sequence.  Declarations and contracts: moe.h.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <atomic>
 #include <stdint.h>
 #include <stdio.h>
@@ -149,7 +151,10 @@ int64_t layer_ws_layout(const moe_config *c, char *base, LayerWs *L) {
     char *p_tor = take(4 * rows);
     char *p_xp = take(rows * c->D * eb);
     char *p_h = take(rows * c->H_local * eb);
-    char *p_yp = take(rows * c->D * 4);  // y_perm is fp32 for every dtype
+    // y_perm: fp16 for bf16 layers, fp32 for fp32 ones; for bf16 the region
+    // also holds moe_layer_forward_fused's fp32 [T, D] accumulator
+    char *p_yp = take(c->dtype == MOE_BF16 ? std::max(rows * c->D * 2, (int64_t)c->T * c->D * 4)
+                                           : rows * c->D * 4);
     char *p_xs = take(rows * 4);
     if (L) {
         L->x_scale = reinterpret_cast<float *>(p_xs);
@@ -740,7 +745,7 @@ MOE_EXPORT moe_status moe_layer_backward_ex(const moe_config *cfg, const void *x
     cudaStream_t s = (cudaStream_t)stream;
     const int64_t rows = rows_alloc_of(cfg);
     int *flags = &L.step.status->flags;
-    cudaError_t e = moe::launch_combine_bwd(dout, (const float *)L.y_perm, L.row_of, L.topk_w, W.gy,
+    cudaError_t e = moe::launch_combine_bwd(dout, L.y_perm, L.row_of, L.topk_w, W.gy,
                                             W.dw, cfg->T, cfg->D, cfg->k, rows, 1, flags, s);
     if (e != cudaSuccess) return cuda_fail(e, "moe_layer_backward: combine backward");
     if (rows > 0) {
@@ -861,8 +866,8 @@ MOE_EXPORT moe_status moe_layer_forward_fused(const moe_config *cfg, const void 
     if (cfg->dtype != MOE_BF16)
         return arg_fail("moe_layer_forward_fused: bf16 only", MOE_ERR_UNSUPPORTED);
     if (cfg->D % 4) return arg_fail("moe_layer_forward_fused: D % 4 != 0", MOE_ERR_UNSUPPORTED);
-    // the fp32 accumulator [T, D] lives in the y_perm buffer, which it must fit
-    if (rows_alloc_of(cfg) < cfg->T || cfg->E_local == 0)
+    // the fp32 accumulator [T, D] lives in the y_perm region (sized to hold it)
+    if (cfg->E_local == 0)
         return moe_layer_forward(cfg, x, wg, bias, w1, w3, w2, out, ws, ws_bytes, stream);
     if (!ws) return arg_fail("workspace is NULL", MOE_ERR_WORKSPACE);
     if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
@@ -1019,6 +1024,11 @@ MOE_EXPORT moe_status moe_get_device_status(const void *ws, size_t ws_bytes, moe
         snprintf(g_last_error, sizeof g_last_error,
                  "a kernel was launched without the thread-block cluster it needs; no work done");
         return MOE_ERR_CUDA;
+    }
+    if (host[0] & moe::FLAG_RANGE) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "an expert output is beyond the fp16 range of y_perm (|y| >= 65520)");
+        return MOE_ERR_UNSUPPORTED;
     }
     if (host[0] & moe::FLAG_CAPACITY) return MOE_ERR_CAPACITY;
     if (host[0] & moe::FLAG_BAD_ROUTING) return MOE_ERR_BAD_ROUTING;

@@ -670,29 +670,36 @@ constexpr int CB_SLOTS = 8;  // slots whose loads are issued together
 #endif
 constexpr int CB_PARTS = MOE_COMBINE_PARTS;  // warps per token (1: 45 us, 2: 52 us, 4: 51 us
                                               // on the fine-grained step)
+// 32-vector chunks of the row whose loads one warp issues together
+#ifndef MOE_COMBINE_CHUNKS
+#define MOE_COMBINE_CHUNKS 1
+#endif
+constexpr int CB_CHUNKS = MOE_COMBINE_CHUNKS;
 
-// y_perm is fp32 for every dtype; out is bf16 or fp32.  The loop over
-// 16-byte output vectors is uniform across the warp (the shuffles inside
-// need every lane), with per-lane predicates for the row tail.
+// y_perm is fp16 for bf16 layers (out bf16) and fp32 for fp32 layers.  The
+// loop over 16-byte output vectors is uniform across the warp (the shuffles
+// inside need every lane), with per-lane predicates for the row tail.
+#ifndef MOE_COMBINE_MINB
+#define MOE_COMBINE_MINB 1
+#endif
 template <bool BF16>
-__global__ void __launch_bounds__(256)
-combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
+__global__ void __launch_bounds__(256, MOE_COMBINE_MINB)
+combine_kernel(const void *__restrict__ y, const int *__restrict__ row_of,
                const float *__restrict__ topk_w, void *__restrict__ out, int T, int k, int D,
                long long rows_alloc, int *status) {
     griddep_launch_dependents();  // the next kernel may be scheduled now
     griddep_wait();               // every input of this kernel is complete
     // One warp per (token, part): a token's row is split into CB_PARTS parts
     // of whole 32-vector chunks, so the grid has CB_PARTS x T warps.
-    constexpr int EPV = BF16 ? 8 : 4;      // output elements per 16-byte vector
-    const int vpr_out = D / EPV;           // output vectors per row
-    const int f4_per_out = EPV / 4;        // fp32 float4 loads per output vector
-    const int yvpr = D / 4;                // float4 per y row
-    const int nchunk = (vpr_out + 31) / 32;
+    constexpr int EPV = BF16 ? 8 : 4;      // output (and y) elements per 16-byte vector
+    const int vpr = D / EPV;               // 16-byte vectors per output row and per y row
+    const int nchunk = (vpr + 31) / 32;
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int t = (int)(wid / CB_PARTS);
     const int part = (int)(wid - (long long)t * CB_PARTS);
     if (t >= T) return;
+    const uint4 *yv = static_cast<const uint4 *>(y);
     int my_row = -1;
     float my_w = 0.f;
     if (lane < k) {
@@ -704,51 +711,71 @@ combine_kernel(const float4 *__restrict__ y, const int *__restrict__ row_of,
         }
     }
     const int c_lo = part * nchunk / CB_PARTS, c_hi = (part + 1) * nchunk / CB_PARTS;
-    for (int c = c_lo; c < c_hi; ++c) {
-        const int v = c * 32 + lane;
-        const bool act = v < vpr_out;
-        float acc[EPV];
+    for (int c = c_lo; c < c_hi; c += CB_CHUNKS) {
+        int v[CB_CHUNKS];
+        bool act[CB_CHUNKS];
+        float acc[CB_CHUNKS][EPV];
 #pragma unroll
-        for (int i = 0; i < EPV; ++i) acc[i] = 0.f;
+        for (int q = 0; q < CB_CHUNKS; ++q) {
+            v[q] = (c + q) * 32 + lane;
+            act[q] = c + q < c_hi && v[q] < vpr;
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) acc[q][i] = 0.f;
+        }
         for (int j0 = 0; j0 < k; j0 += CB_SLOTS) {
-            float4 val[CB_SLOTS][EPV / 4];
+            uint4 val[CB_SLOTS][CB_CHUNKS];
             float wj[CB_SLOTS];
-            bool ok[CB_SLOTS];
+            int rj[CB_SLOTS];
 #pragma unroll
             for (int u = 0; u < CB_SLOTS; ++u) {
                 const int j = j0 + u;
-                const int r = __shfl_sync(0xffffffffu, my_row, j & 31);
+                rj[u] = __shfl_sync(0xffffffffu, my_row, j & 31);
                 wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
-                ok[u] = act && (j < k) && (r >= 0);
-                if (ok[u]) {
+                if (j >= k) rj[u] = -1;
 #pragma unroll
-                    for (int q = 0; q < EPV / 4; ++q)
-                        val[u][q] = __ldcs(y + (size_t)r * yvpr + (size_t)v * f4_per_out + q);
-                }
+                for (int q = 0; q < CB_CHUNKS; ++q)
+                    if (act[q] && rj[u] >= 0) val[u][q] = __ldcs(yv + (size_t)rj[u] * vpr + v[q]);
             }
 #pragma unroll
             for (int u = 0; u < CB_SLOTS; ++u) {
-                if (!ok[u]) continue;
 #pragma unroll
-                for (int q = 0; q < EPV / 4; ++q) {
-                    acc[4 * q + 0] = fmaf(wj[u], val[u][q].x, acc[4 * q + 0]);
-                    acc[4 * q + 1] = fmaf(wj[u], val[u][q].y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(wj[u], val[u][q].z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(wj[u], val[u][q].w, acc[4 * q + 3]);
+                for (int q = 0; q < CB_CHUNKS; ++q) {
+                    if (!act[q] || rj[u] < 0) continue;
+                    float f[EPV];
+                    if constexpr (BF16) {
+                        const __half2 *h2 = reinterpret_cast<const __half2 *>(&val[u][q]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 p2 = __half22float2(h2[i]);
+                            f[2 * i] = p2.x;
+                            f[2 * i + 1] = p2.y;
+                        }
+                    } else {
+                        f[0] = __uint_as_float(val[u][q].x);
+                        f[1] = __uint_as_float(val[u][q].y);
+                        f[2] = __uint_as_float(val[u][q].z);
+                        f[3] = __uint_as_float(val[u][q].w);
+                    }
+#pragma unroll
+                    for (int i = 0; i < EPV; ++i) acc[q][i] = fmaf(wj[u], f[i], acc[q][i]);
                 }
             }
         }
-        if (!act) continue;
-        uint4 o;
-        if (BF16) {
-            __nv_bfloat162 *hh = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) hh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        } else {
-            o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                           __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+        for (int q = 0; q < CB_CHUNKS; ++q) {
+            if (!act[q]) continue;
+            uint4 o;
+            if (BF16) {
+                __nv_bfloat162 *hh = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    hh[i] = __floats2bfloat162_rn(acc[q][2 * i], acc[q][2 * i + 1]);
+            } else {
+                o = make_uint4(__float_as_uint(acc[q][0]), __float_as_uint(acc[q][1]),
+                               __float_as_uint(acc[q][2]), __float_as_uint(acc[q][3]));
+            }
+            reinterpret_cast<uint4 *>(out)[(size_t)t * vpr + v[q]] = o;
         }
-        reinterpret_cast<uint4 *>(out)[(size_t)t * vpr_out + v] = o;
     }
 }
 
@@ -909,11 +936,9 @@ cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *t
     const int blocks = (int)((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t err =
         is_bf16 ? launch_pdl(combine_kernel<true>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
-                             (const float4 *)y_perm, row_of, topk_w, out, T, k, D,
-                             (long long)rows_alloc, status)
+                             y_perm, row_of, topk_w, out, T, k, D, (long long)rows_alloc, status)
                 : launch_pdl(combine_kernel<false>, dim3(blocks), dim3(32 * warps_per_block), 0, stream,
-                             (const float4 *)y_perm, row_of, topk_w, out, T, k, D,
-                             (long long)rows_alloc, status);
+                             y_perm, row_of, topk_w, out, T, k, D, (long long)rows_alloc, status);
     if (err != cudaSuccess) return err;
     count_launch();
     return cudaSuccess;

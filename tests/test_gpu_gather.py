@@ -55,7 +55,7 @@ def _grouped_both(moe, cfg, x, lay_copy, lay_idx, w1, w3, w2, ws):
     for gather in (False, True):
         tpe, seg, row_of, tor, xp = lay_idx if gather else lay_copy
         h = torch.full((ra, cfg.H_local), float("nan"), device="cuda").to(torch.bfloat16)
-        y = torch.full((ra, cfg.D), float("nan"), device="cuda")
+        y = torch.full((ra, cfg.D), float("nan"), device="cuda").to(cfg.y_dtype)
         if gather:
             moe.moe_grouped_swiglu_gather(cfg, x, tor, seg, tpe, w1, w3, w2, h, y, ws)
         else:

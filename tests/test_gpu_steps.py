@@ -447,7 +447,7 @@ def _grouped_case(moe, dt, T, E_local, k, D, H, align, seed, skew=1.0):
     assert moe.rows_alloc(cfg) == ra
     ws = moe.alloc_workspace(cfg)
     h = torch.full((ra, H), float("nan"), device="cuda").to(tdt)
-    y = torch.full((ra, D), float("nan"), device="cuda")          # fp32 accumulator
+    y = torch.full((ra, D), float("nan"), device="cuda").to(cfg.y_dtype)
     moe.moe_grouped_swiglu(cfg, xp, _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"]),
                            w1, w3, w2, h, y, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
@@ -497,7 +497,7 @@ def test_grouped_tile_shapes(moe, kernel, monkeypatch):
     assert moe.rows_alloc(cfg) == ra
     ws = moe.alloc_workspace(cfg)
     h = torch.full((ra, H), float("nan"), device="cuda").to(torch.bfloat16)
-    y = torch.full((ra, D), float("nan"), device="cuda")
+    y = torch.full((ra, D), float("nan"), device="cuda").to(cfg.y_dtype)
     moe.moe_grouped_swiglu(cfg, xp, _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"]),
                            w1, w3, w2, h, y, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
@@ -507,7 +507,7 @@ def test_grouped_tile_shapes(moe, kernel, monkeypatch):
 def _grouped_run(moe, cfg, lay, xp, w1, w3, w2, ws):
     ra, H, D = lay["rows_alloc"], cfg.H_local, cfg.D
     h = torch.full((ra, H), float("nan"), device="cuda").to(torch.bfloat16)
-    y = torch.full((ra, D), float("nan"), device="cuda")
+    y = torch.full((ra, D), float("nan"), device="cuda").to(cfg.y_dtype)
     before = moe.kernel_launches()
     moe.moe_grouped_swiglu(cfg, xp, _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"]),
                            w1, w3, w2, h, y, ws)
@@ -562,7 +562,7 @@ def test_grouped_overlapping_segments_flagged(moe):
     w = torch.zeros((E_local, H, D), dtype=torch.bfloat16, device="cuda")
     w2 = torch.zeros((E_local, D, H), dtype=torch.bfloat16, device="cuda")
     h = torch.zeros((ra, H), dtype=torch.bfloat16, device="cuda")
-    y = torch.zeros((ra, D), dtype=torch.float32, device="cuda")
+    y = torch.zeros((ra, D), dtype=cfg.y_dtype, device="cuda")
     moe.moe_grouped_swiglu(cfg, xp, seg, cnt, w, w, w2, h, y, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
 
@@ -578,7 +578,7 @@ def test_grouped_swiglu_bad_offsets_flagged(moe):
     w = torch.zeros((E_local, H, D), dtype=torch.bfloat16, device="cuda")
     w2 = torch.zeros((E_local, D, H), dtype=torch.bfloat16, device="cuda")
     h = torch.zeros((ra, H), dtype=torch.bfloat16, device="cuda")
-    y = torch.zeros((ra, D), dtype=torch.float32, device="cuda")
+    y = torch.zeros((ra, D), dtype=cfg.y_dtype, device="cuda")
     moe.moe_grouped_swiglu(cfg, xp, seg, cnt, w, w, w2, h, y, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
 
@@ -594,15 +594,15 @@ def test_combine_parity(moe, dt, T, E, k, D, e_first, E_local):
     lay = oracle.layout(idx, E, e_first, E_local, oracle.CONTIGUOUS, 128)
     ra = lay["rows_alloc"]
     tdt = torch.bfloat16 if dt == "bf16" else torch.float32
-    y = torch.randn((ra, D), device="cuda")                       # fp32 accumulator
     w = moe_inputs.random_weights(T, k, seed=T)
     cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=k, e_first=e_first, E_local=E_local,
                      dtype=moe.MOE_BF16 if dt == "bf16" else moe.MOE_F32)
+    y = torch.randn((ra, D), device="cuda").to(cfg.y_dtype)     # fp16 (bf16 layers) or fp32
     ws = moe.alloc_workspace(cfg)
     out = torch.empty((T, D), dtype=tdt, device="cuda")
     moe.moe_unpermute_combine(cfg, y, _dev(lay["row_of"]), _dev(w), out, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
-    yh = moe_inputs.host_array(y)
+    yh = y.double().cpu().numpy()                                # exact
     ref = oracle.unpermute_combine(yh, lay["row_of"], w.astype(np.float64))
     # bound: fp32 accumulation error (k terms) plus one final rounding (one ulp)
     yabs = np.abs(to_f64(y))
@@ -618,11 +618,12 @@ def test_permute_then_combine_is_identity(moe):
     T, E, D = 999, 24, 520
     idx = moe_inputs.random_topk_idx(T, E, 1, seed=1)
     cfg = moe.Config(T=T, D=D, H_local=8, E=E, k=1, dtype=moe.MOE_BF16)
-    x = torch.randn(T, D, device="cuda").to(torch.bfloat16)
+    # multiples of 1/8 up to 16: exact in bf16, in the fp16 of y_perm and in fp32
+    x = (torch.randint(-128, 129, (T, D), device="cuda").float() / 8).to(torch.bfloat16)
     st, tpe, seg, row_of, tor, xp = _run_permute(moe, cfg, x, idx)
     assert st == moe.MOE_OK
     out = torch.empty_like(x)
     ws = moe.alloc_workspace(cfg)
-    moe.moe_unpermute_combine(cfg, xp.float(), _dev(row_of), torch.ones((T, 1), device="cuda"), out,
-                              ws)
+    moe.moe_unpermute_combine(cfg, xp.to(cfg.y_dtype), _dev(row_of), torch.ones((T, 1), device="cuda"),
+                              out, ws)
     assert torch.equal(out, x)

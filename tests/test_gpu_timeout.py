@@ -61,7 +61,7 @@ def test_grouped_wait_runs_out_and_the_next_call_recovers(moe, monkeypatch):
 
     def call():
         h = torch.zeros((ra, H), dtype=torch.bfloat16, device="cuda")
-        y = torch.zeros((ra, D), dtype=torch.float32, device="cuda")
+        y = torch.zeros((ra, D), dtype=cfg.y_dtype, device="cuda")
         n0 = moe.kernel_launches()
         moe.moe_grouped_swiglu(cfg, xp, seg, tpe, w1, w3, w2, h, y, ws)
         n = moe.kernel_launches() - n0
