@@ -11,6 +11,8 @@
 // order), so every result is bit-identical run to run.
 #include <algorithm>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -43,8 +45,24 @@ __device__ __forceinline__ void load4(const void *p, size_t i, bool bf16, float 
 // row is in the buffer; dw[t, j] = <dout[t], y_perm[row]> (y_perm fp16, the
 // products and sums fp32: each lane sums its columns in order, then the
 // lanes' sums are added in a fixed butterfly order), 0 for a slot without row.
+// Blocks per SM the register budget is capped for: 8 (64 registers, no
+// spills) puts one block per 4 tokens of the fine-grained batch (1024 blocks)
+// in a single wave of 152 SMs; uncapped (134 registers) 3 blocks per SM fit.
+// Fine-grained: 35.4 against 49.4 us under ncu, backward 1.102-1.105 against
+// 1.118-1.119 ms.  16-byte row vectors per lane (MOE_COMBINE_BWD_VEC=8) were
+// no faster (37.3 us; 34.7 us capped at 6 blocks, backward 1.106 ms).
+#ifndef MOE_COMBINE_BWD_MINB
+#define MOE_COMBINE_BWD_MINB 8
+#endif
+// elements of a row per lane per step (4: 8-byte fp16 loads, 8: 16-byte)
+#ifndef MOE_COMBINE_BWD_VEC
+#define MOE_COMBINE_BWD_VEC 4
+#endif
+constexpr int CBW_VEC = MOE_COMBINE_BWD_VEC;
+static_assert(CBW_VEC == 4 || CBW_VEC == 8, "4 or 8 elements per lane");
+using CbwVec = std::conditional_t<CBW_VEC == 8, uint4, uint2>;
 template <bool BF16>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, MOE_COMBINE_BWD_MINB)
 combine_bwd_kernel(const void *__restrict__ dout, const __half *__restrict__ y_perm,
                    const int *__restrict__ row_of, const float *__restrict__ topk_w,
                    __nv_bfloat16 *__restrict__ gy, float *__restrict__ dw, int T, int k, int D,
@@ -75,29 +93,39 @@ combine_bwd_kernel(const void *__restrict__ dout, const __half *__restrict__ y_p
             if (j >= k) r[u] = -1;
             dot[u] = 0.f;
         }
-        for (int d0 = lane * 4; d0 < D; d0 += 128) {
-            float g[4];
-            load4(dout, (size_t)t * D + d0, BF16, g);
-            uint2 y[BW_SLOTS];
+        for (int d0 = lane * CBW_VEC; d0 < D; d0 += 32 * CBW_VEC) {
+            float g[CBW_VEC];
+            {
+                float g4[4];
+#pragma unroll
+                for (int q = 0; q < CBW_VEC / 4; ++q) {
+                    load4(dout, (size_t)t * D + d0 + 4 * q, BF16, g4);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) g[4 * q + i] = g4[i];
+                }
+            }
+            CbwVec y[BW_SLOTS];
 #pragma unroll
             for (int u = 0; u < BW_SLOTS; ++u)
                 if (r[u] >= 0)
-                    y[u] = __ldcs(reinterpret_cast<const uint2 *>(y_perm + (size_t)r[u] * D + d0));
+                    y[u] = __ldcs(reinterpret_cast<const CbwVec *>(y_perm + (size_t)r[u] * D + d0));
 #pragma unroll
             for (int u = 0; u < BW_SLOTS; ++u) {
                 if (r[u] < 0) continue;
-                const float2 ya = __half22float2(*reinterpret_cast<const __half2 *>(&y[u].x));
-                const float2 yb = __half22float2(*reinterpret_cast<const __half2 *>(&y[u].y));
-                dot[u] = fmaf(g[0], ya.x, dot[u]);
-                dot[u] = fmaf(g[1], ya.y, dot[u]);
-                dot[u] = fmaf(g[2], yb.x, dot[u]);
-                dot[u] = fmaf(g[3], yb.y, dot[u]);
-                __nv_bfloat162 lo = __floats2bfloat162_rn(w[u] * g[0], w[u] * g[1]);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(w[u] * g[2], w[u] * g[3]);
-                uint2 o;
-                o.x = *reinterpret_cast<uint32_t *>(&lo);
-                o.y = *reinterpret_cast<uint32_t *>(&hi);
-                *reinterpret_cast<uint2 *>(gy + (size_t)r[u] * D + d0) = o;
+                const __half2 *yh = reinterpret_cast<const __half2 *>(&y[u]);
+                uint32_t ow[CBW_VEC / 2];
+#pragma unroll
+                for (int i = 0; i < CBW_VEC / 2; ++i) {
+                    const float2 f = __half22float2(yh[i]);
+                    dot[u] = fmaf(g[2 * i], f.x, dot[u]);
+                    dot[u] = fmaf(g[2 * i + 1], f.y, dot[u]);
+                    __nv_bfloat162 b = __floats2bfloat162_rn(w[u] * g[2 * i], w[u] * g[2 * i + 1]);
+                    ow[i] = *reinterpret_cast<uint32_t *>(&b);
+                }
+                if constexpr (CBW_VEC == 8)
+                    *reinterpret_cast<uint4 *>(gy + (size_t)r[u] * D + d0) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                else
+                    *reinterpret_cast<uint2 *>(gy + (size_t)r[u] * D + d0) = make_uint2(ow[0], ow[1]);
             }
         }
 #pragma unroll

@@ -669,21 +669,33 @@ constexpr int CB_SLOTS = 8;  // slots whose loads are issued together
 #define MOE_COMBINE_PARTS 1
 #endif
 constexpr int CB_PARTS = MOE_COMBINE_PARTS;  // warps per token (1: 45 us, 2: 52 us, 4: 51 us
-                                              // on the fine-grained step)
+                                              // on the fine-grained step, fp32 y_perm)
 // 32-vector chunks of the row whose loads one warp issues together
 #ifndef MOE_COMBINE_CHUNKS
 #define MOE_COMBINE_CHUNKS 1
 #endif
 constexpr int CB_CHUNKS = MOE_COMBINE_CHUNKS;
 
+// Blocks per SM the register budget is capped for.  4 (64 registers, no
+// spills): 512 blocks of 8 warps fit in one wave of 152 SMs, where the
+// uncapped kernel (84 registers, 3 blocks per SM) ran a second, nearly empty
+// wave.  Fine-grained combine 23.1 against 28.2 us in the step (three
+// repeats), 27.0 against 30.5 us alone with a cold L2; DeepSeek-V3-shaped
+// 175.8 against 190.6 us.  2 blocks per SM, two 32-vector chunks per load
+// batch, and two or four warps per token were slower or equal.
+#ifndef MOE_COMBINE_MINB
+#define MOE_COMBINE_MINB 4
+#endif
+#ifndef MOE_COMBINE_WPB
+#define MOE_COMBINE_WPB 8
+#endif
+constexpr int CB_WPB = MOE_COMBINE_WPB;  // warps per block
+
 // y_perm is fp16 for bf16 layers (out bf16) and fp32 for fp32 layers.  The
 // loop over 16-byte output vectors is uniform across the warp (the shuffles
 // inside need every lane), with per-lane predicates for the row tail.
-#ifndef MOE_COMBINE_MINB
-#define MOE_COMBINE_MINB 1
-#endif
 template <bool BF16>
-__global__ void __launch_bounds__(256, MOE_COMBINE_MINB)
+__global__ void __launch_bounds__(32 * CB_WPB, MOE_COMBINE_MINB)
 combine_kernel(const void *__restrict__ y, const int *__restrict__ row_of,
                const float *__restrict__ topk_w, void *__restrict__ out, int T, int k, int D,
                long long rows_alloc, int *status) {
@@ -931,7 +943,7 @@ cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *t
                            int T, int D, int k, int64_t rows_alloc, int is_bf16, int *status,
                            cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const int warps_per_block = 8;
+    const int warps_per_block = CB_WPB;
     const long long warps = (long long)T * CB_PARTS;
     const int blocks = (int)((warps + warps_per_block - 1) / warps_per_block);
     const cudaError_t err =
