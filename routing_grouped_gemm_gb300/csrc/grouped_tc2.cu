@@ -685,7 +685,10 @@ grouped_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const float a = __uint_as_float(d[2 * i]), b = __uint_as_float(d[2 * i + 1]);
-                            over |= fabsf(a) >= kHalfOverflow || fabsf(b) >= kHalfOverflow;
+                            // only values that are stored count: rows without a token
+                            // and columns past n_out (n_out is even) hold garbage
+                            if (row_ok && col0 + 2 * i < n_out)
+                                over |= fabsf(a) >= kHalfOverflow || fabsf(b) >= kHalfOverflow;
                             hv[i] = pack_half2(a, b);
                         }
                         if (tma_y) {

@@ -583,6 +583,47 @@ def test_grouped_swiglu_bad_offsets_flagged(moe):
     assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BAD_ROUTING
 
 
+@pytest.mark.parametrize("kernel", ["pair", "pair2", "single"])
+def test_grouped_fp16_range_flagged(moe, kernel, monkeypatch):
+    """A bf16 layer stores y_perm in fp16.  An expert whose outputs exceed
+    fp16's range (|y| >= 65520 rounds to infinity) must be reported
+    (MOE_ERR_UNSUPPORTED), whether its tile is a transposed tail (20 rows),
+    a full tile or an M=128 tail (300 rows); the flag is cleared by the read
+    and the next in-range call reports MOE_OK."""
+    counts = [20, 64, 300, 130]
+    E_local, D, H = len(counts), 320, 192
+    idx = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])[:, None]
+    idx = idx[np.random.default_rng(5).permutation(len(idx))]
+    T = len(idx)
+    lay = oracle.layout(idx, E_local, 0, E_local, oracle.CONTIGUOUS, 128)
+    monkeypatch.setenv("MOE_GROUPED_KERNEL", kernel)
+    ra = lay["rows_alloc"]
+    g = torch.Generator(device="cuda").manual_seed(12)
+    xp = torch.randn((ra, D), generator=g, device="cuda").to(torch.bfloat16)
+    w1 = (torch.randn((E_local, H, D), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    w3 = (torch.randn((E_local, H, D), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn((E_local, D, H), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    cfg = moe.Config(T=T, D=D, H_local=H, E=E_local, k=1, align_m=128, dtype=moe.MOE_BF16)
+    ws = moe.alloc_workspace(cfg)
+    seg, cnt = _dev(lay["seg_offsets"]), _dev(lay["tokens_per_expert"])
+    h = torch.empty((ra, H), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((ra, D), dtype=cfg.y_dtype, device="cuda")
+    assert y.dtype == torch.float16
+    for big in ([0], [2], [0, 2]):
+        w2b = w2.clone()
+        for e in big:
+            w2b[e] = (w2b[e].float() * 4.0e5).to(torch.bfloat16)
+        moe.moe_grouped_swiglu(cfg, xp, seg, cnt, w1, w3, w2b, h, y, ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_ERR_UNSUPPORTED, big
+        for e in big:
+            rows = slice(int(lay["seg_offsets"][e]), int(lay["seg_offsets"][e]) + counts[e])
+            assert torch.isinf(y[rows]).any()
+        # the status word was cleared by the read; an in-range call is clean
+        moe.moe_grouped_swiglu(cfg, xp, seg, cnt, w1, w3, w2, h, y, ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        assert torch.isfinite(y[torch.from_numpy(lay["token_of_row"] >= 0).cuda()]).all()
+
+
 # ------------------------------------------------------------------ combine
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
