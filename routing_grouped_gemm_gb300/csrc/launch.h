@@ -97,6 +97,8 @@ cudaError_t launch_comb_to_bf16(const float *comb, void *out, int64_t n, cudaStr
 cudaError_t launch_quantize_rows_e4m3(const void *src, int64_t rows, int cols, const int *row_of,
                                       int k, uint8_t *dst, float *scale, cudaStream_t stream);
 
+// out[t] = sum_j w[t, j] y_perm[row_of[t, j]], fp32 in slot order, rounded
+// once; y_perm fp16 with a bf16 out (is_bf16), fp32 with an fp32 out.
 cudaError_t launch_combine(const void *y_perm, const int *row_of, const float *topk_w, void *out,
                            int T, int D, int k, int64_t rows_alloc, int is_bf16, int *status,
                            cudaStream_t stream);
@@ -175,7 +177,8 @@ cudaError_t launch_grouped_swiglu_bwd(const void *x_perm, const void *h, const v
 int64_t grouped_bwd_smem(int E_local);
 
 // Backward of the combine: gy[row] = bf16(w * dout[t]) (rows without a token
-// untouched) and dw[t, j] = <dout[t], y_perm[row]>.
+// untouched) and dw[t, j] = <dout[t], y_perm[row]> (y_perm fp16, as the bf16
+// forward stores it).
 cudaError_t launch_combine_bwd(const void *dout, const void *y_perm, const int *row_of,
                                const float *topk_w, void *gy, float *dw, int T, int D, int k,
                                int64_t rows_alloc, int is_bf16, int *status, cudaStream_t stream);
