@@ -7,8 +7,10 @@ accumulation), seeded synthetic inputs from moe_inputs.py, resident in HBM.
 (``--workload all``: one line per workload, in the specification's order).
 
 One step = router top-k -> permute -> grouped SwiGLU (GEMM1 + gate, GEMM2)
--> weighted combine, issued as the four step calls of the C ABI on one
-stream.  The line reports tokens/s (value: T tokens per step, each routed to
+-> weighted combine, issued as one moe_layer_forward call of the C ABI (the
+layer call a user makes; every intermediate in its workspace).  A second loop
+times the four step calls one by one for the per-call breakdown.  The line
+reports tokens/s (value: T tokens per step, each routed to
 k experts), the dominant kernel against its roof (roofline: the grouped
 SwiGLU on the tensor cores, on HBM for the masked decode layout, on the FP32
 ALUs for the fp32 workload), permute and combine GB/s (breakdown), an
@@ -781,16 +783,28 @@ def run_gpu(args, name):
         if ev is not None:
             ev[4].record(stream)
 
+    # the timed step is the layer call a user makes (one C-ABI call: route,
+    # permute, grouped SwiGLU, combine on one stream, every intermediate in
+    # its workspace); the per-call breakdown below times the four step calls
+    # one by one
+    lws = moe.alloc_workspace(cfg, device=dev, layer=True)
+
+    def layer_step():
+        moe.moe_layer_forward(cfg, inp.x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, lws,
+                              stream)
+
     for _ in range(max(3, args.warmup)):
         step()
+        layer_step()
     # launches of one grouped SwiGLU call (one cooperative launch or two)
     n0 = moe.kernel_launches()
     moe.moe_grouped_swiglu(cfg, x_perm, seg, tpe, inp.w1, inp.w3, inp.w2, h, y_perm, ws, stream)
     gemm_launches = moe.kernel_launches() - n0
     torch.cuda.synchronize(dev)
-    st = moe.moe_get_device_status(ws, stream)
-    if st != moe.MOE_OK:
-        raise RuntimeError(f"device status after warm-up: {moe.status_string(st)}")
+    for wsx in (ws, lws):
+        st = moe.moe_get_device_status(wsx, stream)
+        if st != moe.MOE_OK:
+            raise RuntimeError(f"device status after warm-up: {moe.status_string(st)}")
 
     # the timed loop has events only at its two ends: events between the
     # calls would cut the programmatic launch overlap of consecutive kernels;
@@ -806,7 +820,7 @@ def run_gpu(args, name):
             t_end = torch.cuda.Event(enable_timing=True)
             t_start.record(stream)
             for i in range(args.steps):
-                step()
+                layer_step()
             t_end.record(stream)
             n_launches = moe.kernel_launches() - n_launch0
             torch.cuda.synchronize(dev)
@@ -817,7 +831,7 @@ def run_gpu(args, name):
             for i in range(args.steps):
                 flush.zero_()
                 evs[i][0].record(stream)
-                step()
+                layer_step()
                 evs[i][1].record(stream)
             n_launches = moe.kernel_launches() - n_launch0
             torch.cuda.synchronize(dev)
@@ -825,7 +839,7 @@ def run_gpu(args, name):
     if world > 1:
         dist.barrier()
     elapsed_ms = max_over_ranks(local_ms, dev)
-    st = moe.moe_get_device_status(ws, stream)
+    st = moe.moe_get_device_status(lws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
 
@@ -836,6 +850,9 @@ def run_gpu(args, name):
             flush.zero_()
         step(evs[i])
     torch.cuda.synchronize(dev)
+    st = moe.moe_get_device_status(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after the breakdown: {moe.status_string(st)}")
     parts = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])  # ms
     mean_parts = parts.mean(0)
     ms_per_step = elapsed_ms / args.steps
@@ -874,8 +891,13 @@ def run_gpu(args, name):
                    "router": router_note(w), "layout": layout_note(w),
                    "parallelism": f"replicas x{world}" if world > 1 else "single", "l2": l2_note(w)},
         "roofline": roof,
+        "api": "moe_layer_forward (C ABI): one call per step; intermediates in its workspace",
         "breakdown_ms": {"route": float(mean_parts[0]), "permute": float(mean_parts[1]),
                          "grouped_swiglu": gemm_ms, "combine": float(mean_parts[3])},
+        "breakdown_note": "the four step calls (moe_route_topk, moe_permute, moe_grouped_swiglu, "
+                          "moe_unpermute_combine) one by one, CUDA events between them; the "
+                          "layer call also lets the router write the dispatch's count input "
+                          "where the count matrix is small, one launch fewer",
         "bandwidth": {
             "permute_gbs": alg["permute_bytes"] / (mean_parts[1] * 1e-3) / 1e9,
             "combine_gbs": alg["combine_bytes"] / (mean_parts[3] * 1e-3) / 1e9,
