@@ -519,8 +519,18 @@ __device__ __forceinline__ void derive_offsets(const int *__restrict__ blk_cnt, 
     }
 }
 
+// Tokens (warps) per block of the index+copy kernel.  16: half as many
+// blocks derive the offsets from the count matrix as with 8, two blocks per
+// SM in one wave.  Fine-grained permute call 25.8-26.5 against 26.5-26.9 us in
+// the step (three repeats), 28.0 against 29.4 us alone with a cold L2;
+// 32 tokens per block: 26.8-27.6 us.
+#ifndef MOE_IC_WARPS
+#define MOE_IC_WARPS 16
+#endif
+constexpr int IC_WARPS = MOE_IC_WARPS;
+static_assert(PB_TOKENS % IC_WARPS == 0, "a block's tokens lie in one count block");
 template <bool kFp8, bool kDerive>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(32 * IC_WARPS)
 permute_index_copy_kernel(const uint4 *__restrict__ x, const int *__restrict__ topk_idx,
                           const int2 *__restrict__ wmeta, const int *__restrict__ blk_base,
                           const int *__restrict__ seg_offsets_in, int *__restrict__ row_of,
@@ -835,9 +845,10 @@ cudaError_t launch_permute(const void *x, const int *topk_idx, int *tokens_per_e
                               tokens_per_expert, seg_offsets, token_of_row, status)) != cudaSuccess)
             return err;
         count_launch();
-        const int warps_per_block = 8;
+        const int warps_per_block = IC_WARPS;
         const int blocks = (T + warps_per_block - 1) / warps_per_block;
-        const size_t csmem = derive ? sizeof(int) * (2 * (size_t)E + E_local + 1 + 8) : 0;
+        const size_t csmem =
+            derive ? sizeof(int) * (2 * (size_t)E + E_local + 1 + warps_per_block) : 0;
         auto copy_kernel = x_scale ? (derive ? permute_index_copy_kernel<true, true>
                                              : permute_index_copy_kernel<true, false>)
                                    : (derive ? permute_index_copy_kernel<false, true>
