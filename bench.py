@@ -294,9 +294,14 @@ def cpu_baseline(inp, w, seconds, seed=7):
     tps, _, nth = oracle_tokens_per_s(x, wg, bias, expert, w, min(w.T, 16), seed=99)
     n = int(max(16, min(w.T, tps * seconds)))
     tps, dt, nth = oracle_tokens_per_s(x, wg, bias, expert, w, n, seed=seed)
+    # the same on one thread, on a sample of about a second
+    n1 = int(max(4, min(w.T, tps / nth)))
+    tps1, dt1, _ = oracle_tokens_per_s(x, wg, bias, expert, w, n1, seed=seed + 1, nthreads=1)
     return {"value": tps, "unit": UNIT, "cores": nth, "kind": "oracle",
             "sample": f"{n} sampled tokens of the {w.name} batch, router + per-token experts in "
                       f"fp64 ({dt:.1f} s)",
+            "single_thread": {"value": tps1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} sampled tokens ({dt1:.1f} s)"},
             "cpu": cpu_model()}
 
 
