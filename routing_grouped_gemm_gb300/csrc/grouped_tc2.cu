@@ -49,6 +49,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "launch.h"
@@ -921,6 +922,25 @@ cudaError_t launch_pair(const PairMaps &m, const PairParams &p, int clusters, si
 // 0: not known yet, 1: this device runs cooperative cluster launches, -1: it refused one
 int g_coop_ok[64] = {0};
 
+// A CUDA profiler attached to the process: Nsight Compute starts its target
+// with NV_NSIGHT_INJECTION_TRANSPORT_TYPE and NV_COMPUTE_PROFILER_PERFWORKS_DIR
+// in the environment, CUPTI-based tools name their injection library in
+// CUDA_INJECTION64_PATH.  Under Nsight Compute the cooperative cluster launch
+// of both GEMMs has ended in LaunchFailed while the same program ran clean
+// without it, so with a profiler attached the GEMMs always run as two
+// launches of the same kernel (the form the profiles describe).
+bool profiler_attached() {
+    static const bool attached = [] {
+        for (const char *name : {"NV_NSIGHT_INJECTION_TRANSPORT_TYPE",
+                                 "NV_COMPUTE_PROFILER_PERFWORKS_DIR", "CUDA_INJECTION64_PATH"}) {
+            const char *v = getenv(name);
+            if (v != nullptr && v[0] != '\0') return true;
+        }
+        return false;
+    }();
+    return attached;
+}
+
 }  // namespace
 
 int64_t grouped_pair_scratch_ints(int64_t rows_alloc, int E_local) {
@@ -948,7 +968,8 @@ cudaError_t run_pair(const PairMaps &m, const PairParams &p, int64_t rows_alloc,
     // even), so long calls keep two launches.
     const long long tiles_est = pt_bound * (p.nt0 + p.nt1);
     const bool short_call = tiles_est <= 64LL * clusters_max;
-    if (MOE_PAIR_FUSED && short_call && scratch && dev >= 0 && g_coop_ok[dev] >= 0) {
+    if (MOE_PAIR_FUSED && short_call && scratch && dev >= 0 && g_coop_ok[dev] >= 0 &&
+        !profiler_attached()) {
         // one cooperative launch over both GEMMs; scratch[0] = finish count,
         // scratch[32..] = per-block GEMM1 counts (zero between launches)
         PairParams pb = p;
