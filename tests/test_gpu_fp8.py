@@ -163,6 +163,7 @@ def test_grouped_fp8_tile_shapes(moe, kernel, monkeypatch):
 
 @pytest.mark.parametrize("name,over,n_sample", [
     ("fine-grained-bf16", dict(T=640), 96),
+    ("fine-grained-bf16", dict(), 24),      # the benchmark's FP8 step at full size, sampled
     ("deepseek-v3-shaped", dict(T=300), 12),
     ("decode-masked", dict(), 16),           # masked layout, capacity = T
 ])
