@@ -112,7 +112,8 @@ const char *moe_status_string(int32_t status);
 /* Text of the last host-side error of the calling thread ("" if none). */
 const char *moe_last_error_string(void);
 
-/* ABI version: major * 10000 + minor * 100 + patch. */
+/* ABI version: major * 10000 + minor * 100 + patch.  2.0.0 made y_perm of
+ * bf16 layers fp16 (it was fp32 in 1.x). */
 int32_t moe_abi_version(void);
 
 /*

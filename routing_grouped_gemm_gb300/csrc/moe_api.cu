@@ -18,7 +18,8 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 10500;  // 1.5.0
+// 2.0.0: y_perm of bf16 layers is fp16 (fp32 up to 1.5.0)
+constexpr int32_t kAbiVersion = 20000;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int64_t kAlign = 256;
