@@ -345,6 +345,25 @@ def test_layer_k32_many_experts(moe):
     check_against_oracle(moe, w, inp, out, views, 24)
 
 
+@pytest.mark.parametrize("kernel", ["auto", "pair"])
+def test_layer_max_experts(moe, kernel, monkeypatch):
+    """E = 1024, the most experts the ABI accepts: the SIMT router above 256
+    experts, a count matrix of 6 x 1024 cells, about 12 rows per expert (the
+    one-CTA grouped kernel is chosen; "pair" forces the CTA-pair kernel and
+    its 1024-expert tile table)."""
+    if kernel == "pair":
+        monkeypatch.setenv("MOE_GROUPED_KERNEL", "pair")
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=1500, D=256, H=128, E=1024, k=8)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=17)
+    cfg = cfg_for(moe, w)
+    out, views, _ = run_layer(moe, cfg, inp)
+    check_against_oracle(moe, w, inp, out, views, 48)
+    idx = views["topk_idx"].cpu().numpy()
+    lay = (views["tokens_per_expert"].cpu().numpy(), views["seg_offsets"].cpu().numpy(),
+           views["row_of"].cpu().numpy(), views["token_of_row"].cpu().numpy())
+    check_layout_properties(idx, lay, w.E, 0, w.E, align_m=cfg.align_m)
+
+
 def test_layer_launch_count(moe):
     # bf16, E <= 256: router logits on the tensor cores with the top-k in the
     # same cluster launch (1), count with the scan in its last block (1;
