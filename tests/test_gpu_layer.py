@@ -147,6 +147,27 @@ def test_layer_single_token_and_k1(moe):
     check_against_oracle(moe, w, inp, out, views, 1)
 
 
+@pytest.mark.parametrize("T,E,k,D,H,renorm", [
+    (300, 1, 1, 256, 128, True),    # one expert: every token in one segment, weight 1
+    (200, 4, 4, 128, 64, False),    # k = E: every token to every expert (softmax weights)
+    (100, 8, 2, 8, 8, True),        # the smallest widths: D = H = 8 (one 16-byte row)
+])
+def test_layer_degenerate_shapes(moe, T, E, k, D, H, renorm):
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=T, E=E, k=k, D=D, H=H, renorm=renorm)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=T + E)
+    cfg = cfg_for(moe, w)
+    out, views, _ = run_layer(moe, cfg, inp)
+    check_against_oracle(moe, w, inp, out, views, min(T, 32))
+    idx = views["topk_idx"].cpu().numpy()
+    lay = (views["tokens_per_expert"].cpu().numpy(), views["seg_offsets"].cpu().numpy(),
+           views["row_of"].cpu().numpy(), views["token_of_row"].cpu().numpy())
+    check_layout_properties(idx, lay, w.E, 0, w.E, align_m=cfg.align_m)
+    if k == E:
+        assert (np.sort(idx, axis=1) == np.arange(E)).all()
+    if E == 1:
+        assert np.allclose(views["topk_w"].cpu().numpy(), 1.0)
+
+
 def test_layer_is_deterministic(moe):
     w = moe_inputs.WORKLOADS["zipf-skewed"].scaled(T=3000)
     inp = moe_inputs.make_inputs(w, device="cuda", seed=8)
