@@ -675,15 +675,42 @@ def run_backward(moe, cfg, inp, stream, dev, args, peaks):
             "launches_per_forward_and_backward": launches}
 
 
+def floors(w, R, touched, peaks):
+    """The grouped call's two lower bounds in ms: its FLOPs at the bf16 tensor
+    peak and its algorithmic bytes at the copy rate.  The larger one is the
+    roof that binds (the classic roofline: attainable = min(peak, intensity x
+    bandwidth))."""
+    alg = algorithmic(w, R, touched)
+    return (alg["ffn_flops"] / (peaks["bf16_tflops"] * 1e12) * 1e3,
+            alg["grouped_bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e3)
+
+
+def grouped_bound(w, R, touched, peaks):
+    """"alu" for fp32, else "hbm" when the call's byte floor is above its FLOP
+    floor (the masked decode layout, and the 256-expert layer whose ~256 rows
+    per expert give each weight byte fewer FLOPs than the ridge point), else
+    "tensor"."""
+    if w.dtype == "f32":
+        return "alu"
+    compute_ms, hbm_ms = floors(w, R, touched, peaks)
+    return "hbm" if w.layout == "masked" or hbm_ms > compute_ms else "tensor"
+
+
 def roofline(w, moe, cfg, gemm_ms, R, touched, peaks, gemm_launches, dev):
-    """The dominant kernel of the step (the grouped SwiGLU call) against its
-    roof: the bf16 tensor peak, HBM for the masked decode layout (it streams
-    the touched experts' weights once), the FP32 FFMA rate for fp32."""
+    """The dominant kernel of the step (the grouped SwiGLU call) against the
+    roof that binds it: the bf16 tensor peak, or HBM where the call's
+    algorithmic bytes take longer at the copy rate than its FLOPs at the tensor
+    peak (it streams the touched experts' weights once); the FP32 FFMA rate
+    for fp32.  Both floors are reported beside the fraction."""
     import torch
     alg = algorithmic(w, R, touched)
     name = grouped_kernel(w.name)[0]
     kernel = f"{name}: {gemm_launches} launch{'es' if gemm_launches != 1 else ''} per call"
-    if w.layout == "masked":
+    compute_ms, hbm_ms = floors(w, R, touched, peaks)
+    both = {"compute_floor_ms": compute_ms, "hbm_floor_ms": hbm_ms,
+            "frac_of_tensor": compute_ms / gemm_ms, "frac_of_hbm": hbm_ms / gemm_ms}
+    bound = grouped_bound(w, R, touched, peaks)
+    if bound == "hbm":
         achieved = alg["grouped_bytes"] / (gemm_ms * 1e-3) / 1e9
         return {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -692,7 +719,8 @@ def roofline(w, moe, cfg, gemm_ms, R, touched, peaks, gemm_launches, dev):
                 "algorithmic_bytes_per_call": alg["grouped_bytes"],
                 "algorithmic_bytes_note": "touched experts' w1, w3, w2 once + x_perm rows read + "
                                           "h written and read + y written (fp16)",
-                "touched_experts": touched, "tflops": alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12}
+                "touched_experts": touched, "tflops": alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12,
+                **both}
     achieved = alg["ffn_flops"] / (gemm_ms * 1e-3) / 1e12
     if w.dtype == "f32":
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -709,7 +737,7 @@ def roofline(w, moe, cfg, gemm_ms, R, touched, peaks, gemm_launches, dev):
             "peak_source": f"{peaks['source']} bf16 burst",
             "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
             "traffic": recorded_traffic(w.name),
-            "algorithmic_flops_per_call": alg["ffn_flops"]}
+            "algorithmic_flops_per_call": alg["ffn_flops"], **both}
 
 
 def run_gpu(args, name):

@@ -86,3 +86,25 @@ def test_recorded_traffic_is_near_the_algorithmic_bytes():
     d = moe_inputs.WORKLOADS["decode-masked"]
     dec = bench.algorithmic(d, d.T * d.k, 250)["grouped_bytes"]
     assert 0.98 < rec["decode-masked"]["dram_bytes_per_call"] / dec < 1.05
+
+
+def test_binding_roof_per_workload():
+    """The roof the grouped call is reported against is the larger of its two
+    floors: FLOPs at the tensor peak, algorithmic bytes at the copy rate.  The
+    fine-grained call sits at the ridge (221 against 216 us at the measured
+    peaks); the 256-expert layer (about 256 rows per expert) is byte-bound."""
+    bench = _bench()
+    peaks = {"hbm_gbs": 6687.5, "bf16_tflops": 1927.1}
+    W = moe_inputs.WORKLOADS
+    want = {"fine-grained-bf16": "tensor", "zipf-skewed": "tensor", "deepseek-v3-shaped": "hbm",
+            "decode-masked": "hbm", "tiny-fp32": "alu"}
+    for name, bound in want.items():
+        w = W[name]
+        assert bench.grouped_bound(w, w.T * w.k, w.E, peaks) == bound, name
+    w = W["fine-grained-bf16"]
+    compute_ms, hbm_ms = bench.floors(w, w.T * w.k, w.E, peaks)
+    assert abs(compute_ms - 425_201_762_304 / 1927.1e12 * 1e3) < 1e-9
+    assert 0.215 < hbm_ms < 0.218 and 0.220 < compute_ms < 0.221
+    d = W["deepseek-v3-shaped"]
+    compute_ms, hbm_ms = bench.floors(d, d.T * d.k, d.E, peaks)
+    assert hbm_ms > 1.2 * compute_ms
