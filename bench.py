@@ -664,15 +664,68 @@ def run_backward(moe, cfg, inp, stream, dev, args, peaks):
     b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n
     flops = 12.0 * w.T * w.k * w.D * w.H
     tf = flops / (b_ms * 1e-3) / 1e12
+    fl32 = backward_floors(w, peaks, 4)
+    fl16 = backward_floors(w, peaks, 2)
     del tws, dw1, dw3, dw2, b1, b3, b2
     return {"api": "moe_layer_forward_train + moe_layer_backward (dx, dwg, dbias, dw1, dw3, dw2)",
             "forward_train_ms": f_ms, "backward_ms": b_ms,
             "training_step_tokens_per_s": w.T / ((f_ms + b_ms) * 1e-3),
             "backward_expert_flops": flops, "backward_tflops": tf,
             "backward_frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "backward_floor_ms": fl32["total_floor_ms"],
+            "backward_frac_of_floor": fl32["total_floor_ms"] / b_ms,
             "backward_bf16_weight_grads_ms": b16_ms,
             "backward_bf16_weight_grads_tflops": flops / (b16_ms * 1e-3) / 1e12,
+            "backward_bf16_weight_grads_floor_ms": fl16["total_floor_ms"],
+            "backward_bf16_weight_grads_frac_of_floor": fl16["total_floor_ms"] / b16_ms,
+            "floor_note": "per kernel the larger of its FLOPs at the bf16 burst peak and its "
+                          "algorithmic bytes at the copy rate, summed; with fp32 weight "
+                          "gradients all four expert GEMMs are byte-bound",
+            "floors_by_kernel": {k: {"bound": v["bound"],
+                                     "floor_ms": max(v["compute_floor_ms"], v["hbm_floor_ms"])}
+                                 for k, v in fl32.items() if k != "total_floor_ms"},
             "launches_per_forward_and_backward": launches}
+
+
+def backward_floors(w, peaks, wgrad_bytes=4):
+    """Lower bounds of the layer backward, kernel by kernel: each kernel's
+    FLOPs at the bf16 tensor peak or its algorithmic bytes at the copy rate,
+    whichever is larger, summed over the kernels.  Bytes count the valid rows
+    (R = T k) once per read or write of each operand; dx_perm and the router's
+    dense dx part are fp32, the expert weight gradients `wgrad_bytes` wide."""
+    R, T, D, H, E = w.T * w.k, w.T, w.D, w.H, w.E
+    b = 2
+    dense = w.score == "softmax" and not w.renorm   # dl nonzero on every expert
+    parts = {
+        # dout read, y_perm (fp16) read, gy written, slot index and weight, dw
+        "combine_bwd": (0.0, T * D * b + 2 * R * D * b + R * 12),
+        # gy, w2, the saved gate/up read; dg/du written
+        "dgrad2_swiglu_bwd": (2.0 * R * D * H, R * D * b + E * D * H * b + 2 * R * 2 * H * b),
+        # dg/du, w1 and w3 read; dx_perm written (fp32)
+        "dgrad1": (4.0 * R * D * H, R * 2 * H * b + 2 * E * H * D * b + R * D * 4),
+        # gy and h read; dw2 written
+        "wgrad2": (2.0 * R * D * H, R * D * b + R * H * b + E * D * H * wgrad_bytes),
+        # dg/du and x_perm read; dw1 and dw3 written
+        "wgrad13": (4.0 * R * D * H, R * 2 * H * b + R * D * b + 2 * E * H * D * wgrad_bytes),
+        # logits, dw read, dl written; dW_g = dl^T x (x read once); where dl is
+        # dense (softmax without renorm) the dx part dl wg is a GEMM (fp32 out)
+        "router_bwd": (4.0 * T * E * D, T * E * 4 * 2 + R * 4 + T * D * b + E * D * 4 + E * D * b
+                       + T * D * 4) if dense else
+                      (2.0 * R * D, T * E * 4 * 2 + R * 4 + T * D * b + E * D * 4),
+        # dx_perm (fp32) and the router's dx part read (dense: the fp32 GEMM
+        # output; else wg and each slot's dl), dx written
+        "dispatch_bwd": (0.0, R * D * 4 + R * 4 + T * D * 4 + T * D * b) if dense else
+                        (2.0 * R * D, R * D * 4 + R * 4 + E * D * b + R * 4 + T * D * b),
+    }
+    out = {}
+    for name, (flops, nbytes) in parts.items():
+        c = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+        m = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+        out[name] = {"flops": flops, "bytes": float(nbytes), "compute_floor_ms": c,
+                     "hbm_floor_ms": m, "bound": "hbm" if m > c else "tensor"}
+    out["total_floor_ms"] = sum(max(v["compute_floor_ms"], v["hbm_floor_ms"])
+                                for v in out.values())
+    return out
 
 
 def floors(w, R, touched, peaks):

@@ -108,3 +108,25 @@ def test_binding_roof_per_workload():
     d = W["deepseek-v3-shaped"]
     compute_ms, hbm_ms = bench.floors(d, d.T * d.k, d.E, peaks)
     assert hbm_ms > 1.2 * compute_ms
+
+
+def test_backward_floors():
+    """The backward's floor is the sum over its kernels of the larger of FLOPs
+    at the tensor peak and algorithmic bytes at the copy rate.  With fp32
+    weight gradients every expert GEMM is byte-bound (dgrad2 reads the saved
+    gate/up and writes dg/du, dgrad1 writes fp32 dx_perm, the wgrads write 0.74
+    and 1.48 GB); with bf16 ones wgrad13 becomes tensor-bound."""
+    bench = _bench()
+    peaks = {"hbm_gbs": 6687.5, "bf16_tflops": 1927.1}
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"]
+    R, D, H, E = w.T * w.k, w.D, w.H, w.E
+    f32 = bench.backward_floors(w, peaks, 4)
+    f16 = bench.backward_floors(w, peaks, 2)
+    gemms = ("dgrad2_swiglu_bwd", "dgrad1", "wgrad2", "wgrad13")
+    assert sum(f32[g]["flops"] for g in gemms) == 12.0 * R * D * H
+    assert all(f32[g]["bound"] == "hbm" for g in gemms)
+    assert f16["wgrad13"]["bound"] == "tensor"
+    assert f32["wgrad13"]["bytes"] - f16["wgrad13"]["bytes"] == 2 * E * H * D * 2
+    assert f32["wgrad2"]["bytes"] == R * D * 2 + R * H * 2 + E * D * H * 4
+    assert 0.73 < f32["total_floor_ms"] < 0.74
+    assert 0.56 < f16["total_floor_ms"] < 0.58
