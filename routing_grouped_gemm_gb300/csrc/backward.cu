@@ -422,11 +422,17 @@ router_gemm_kernel(const float *__restrict__ a, long long a_m, long long a_k,
 // token's selected experts and every selected (token, expert) has a row:
 //   dwg[e, :] = sum_{rows r of e} dl[t_r, e] x[t_r, :],  dbias[e] = sum_r dl[t_r, e]
 // Block (c, e) walks the segment in chunks of RS_CHUNK rows: the block first
-// stages each row's token and dl value in shared memory, then 8 warps take
+// stages each row's token and dl value in shared memory, then its warps take
 // the chunk's rows round-robin, each lane 8 columns of the 256-column chunk c
 // (one 16-byte load of x's row, which the L2 holds).  The warps' partial
 // sums are added in warp order, so the result is deterministic.
-constexpr int RS_COLS = 256, RS_WARPS = 8, RS_CHUNK = 512;
+// 16 warps (24 rows of a 384-row segment each, four loads in flight per
+// warp): fine-grained backward 1.085-1.088 ms against 1.095-1.096 ms with 8
+// and 1.090 ms with 32.
+#ifndef MOE_RS_WARPS
+#define MOE_RS_WARPS 16
+#endif
+constexpr int RS_COLS = 256, RS_WARPS = MOE_RS_WARPS, RS_CHUNK = 512;
 template <bool BF16>
 __global__ void __launch_bounds__(32 * RS_WARPS)
 router_wgrad_seg_kernel(const void *__restrict__ x, const float *__restrict__ dl,
