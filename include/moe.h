@@ -343,6 +343,8 @@ moe_status moe_layer_forward_train(const moe_config *cfg, const void *x, const v
  *   with renorm), dbias = sum_t dl,  dwg = dl^T x.
  * The backward overwrites the padding rows of the saved x_perm and h with
  * zeros.  Reduction orders are fixed: results are bit-identical run to run.
+ * With T = 0 there is nothing to differentiate: dx has no rows, and dwg,
+ * dbias, dw1, dw3 and dw2 are set to zero (only their pointers are checked).
  */
 moe_status moe_layer_backward(const moe_config *cfg, const void *x, const void *wg,
                               const void *w1, const void *w3, const void *w2, const void *dout,

@@ -733,7 +733,21 @@ MOE_EXPORT moe_status moe_layer_backward_ex(const moe_config *cfg, const void *x
     if (!aligned(ws, kAlign)) return arg_fail("workspace must be 256-byte aligned", MOE_ERR_WORKSPACE);
     if ((int64_t)ws_bytes < train_ws_layout(cfg, nullptr, nullptr))
         return arg_fail("workspace too small for moe_layer_backward", MOE_ERR_WORKSPACE);
-    if (cfg->T == 0) return MOE_OK;
+    if (cfg->T == 0) {
+        // no token: dx has no rows, and every parameter gradient is zero
+        if (!need16(dwg) || !need16(dw1) || !need16(dw3) || !need16(dw2) ||
+            (dbias && !aligned(dbias, 4)))
+            return arg_fail("moe_layer_backward: NULL or misaligned tensor");
+        cudaStream_t s = (cudaStream_t)stream;
+        const size_t wb = wgrad_dtype == MOE_BF16 ? 2 : 4;
+        const size_t ehd = (size_t)cfg->E * cfg->H_local * cfg->D;
+        cudaError_t e = cudaMemsetAsync(dwg, 0, (size_t)cfg->E * cfg->D * sizeof(float), s);
+        if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, cfg->E * sizeof(float), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dw1, 0, ehd * wb, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dw3, 0, ehd * wb, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, ehd * wb, s);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_layer_backward: zero gradients");
+    }
     if (!need16(x) || !need16(wg) || !need16(w1) || !need16(w3) || !need16(w2) || !need16(dout) ||
         !need16(dx) || !need16(dwg) || !need16(dw1) || !need16(dw3) || !need16(dw2) ||
         (dbias && !aligned(dbias, 4)))

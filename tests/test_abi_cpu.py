@@ -224,3 +224,20 @@ def test_noalloc_permute_limit_checked_on_the_host(moe):
     st = lib.moe_permute_noalloc(ctypes.byref(fits), None, None, None, None, None, None, None,
                                  None, None)
     assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_backward_checks_gradients_on_the_host(moe):
+    """With T = 0 the backward zeroes the parameter gradients; a NULL or
+    misaligned gradient pointer is rejected on the host before that."""
+    cfg = moe.Config(T=0, D=128, H_local=128, E=8, k=2, dtype=moe.MOE_BF16)
+    n = moe.layer_train_workspace_size(cfg)
+    assert n > 0
+    c = cfg.c()
+    lib = moe._lib
+    n0 = moe.kernel_launches()
+    # dwg NULL, then dw1 misaligned; the workspace pointer is only checked for alignment
+    assert lib.moe_layer_backward_ex(ctypes.byref(c), 0, 0, 0, 0, 0, 0, 0, None, None, 256, 256,
+                                     256, moe.MOE_F32, 256, n, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_backward_ex(ctypes.byref(c), 0, 0, 0, 0, 0, 0, 0, 256, None, 264, 256,
+                                     256, moe.MOE_F32, 256, n, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.kernel_launches() == n0

@@ -151,6 +151,7 @@ def test_layer_single_token_and_k1(moe):
     (300, 1, 1, 256, 128, True),    # one expert: every token in one segment, weight 1
     (200, 4, 4, 128, 64, False),    # k = E: every token to every expert (softmax weights)
     (100, 8, 2, 8, 8, True),        # the smallest widths: D = H = 8 (one 16-byte row)
+    (1, 64, 6, 2048, 1408, True),   # one token at full widths: six one-row expert segments
 ])
 def test_layer_degenerate_shapes(moe, T, E, k, D, H, renorm):
     w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=T, E=E, k=k, D=D, H=H, renorm=renorm)
@@ -450,3 +451,31 @@ def test_layer_full_size_sampled(moe, name, n_sample):
         assert (cnt == 0).sum() >= w.zipf_empty
     del inp, out, views, ws
     torch.cuda.empty_cache()
+
+
+def test_layer_empty_batch(moe):
+    """T = 0: the layer call launches nothing and returns MOE_OK; the training
+    backward has no dx rows to write and sets every parameter gradient to
+    zero (in fp32 and in bf16)."""
+    w = moe_inputs.WORKLOADS["fine-grained-bf16"].scaled(T=64, E=8, D=256, H=128)
+    inp = moe_inputs.make_inputs(w, device="cuda", seed=2)
+    cfg = cfg_for(moe, w, T=0)
+    x = torch.empty((0, w.D), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((0, w.D), dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(cfg, layer=True)
+    n0 = moe.kernel_launches()
+    moe.moe_layer_forward(cfg, x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, ws)
+    assert moe.kernel_launches() == n0
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    tws = moe.alloc_workspace(cfg, train=True)
+    moe.moe_layer_forward_train(cfg, x, inp.wg, inp.bias, inp.w1, inp.w3, inp.w2, out, tws)
+    for wdt in (torch.float32, torch.bfloat16):
+        dwg = torch.full((w.E, w.D), float("nan"), device="cuda")
+        dbias = torch.full((w.E,), float("nan"), device="cuda")
+        dws = [torch.full(s, float("nan"), dtype=wdt, device="cuda")
+               for s in ((w.E, w.H, w.D), (w.E, w.H, w.D), (w.E, w.D, w.H))]
+        moe.moe_layer_backward(cfg, x, inp.wg, inp.w1, inp.w3, inp.w2, out, out, dwg, dbias,
+                               *dws, tws)
+        assert moe.moe_get_device_status(tws) == moe.MOE_OK
+        for t in (dwg, dbias, *dws):
+            assert (t.float() == 0).all()
